@@ -1,0 +1,202 @@
+/*
+ * paged_kv.h -- C ABI of the GB300 (sm_103a) paged-KV RoPE + attention library
+ * (libpaged_kv.so).
+ *
+ * One inflight batch per call: requests are packed with no padding, context (prefill or
+ * chunked-context) requests first, generation (decode) requests after.  For every new token
+ * the library rotates Q and K (GPT-NeoX RoPE), appends K and V into a paged KV pool through
+ * each request's block table, and then runs causal GQA self-attention over the pool.
+ *
+ * Sources (web pages on one LLM serving engine, cited by title and section):
+ *   [ARCH]   "TensorRT-LLM 源码完全拆解(一):整体架构与模块全景" (pinghaoyang.com.cn)
+ *   [NOTES]  "TensorRT-LLM 1.0 源码学习笔记" (openharmonycrossplatform.csdn.net)
+ *   [REPORT] TensorRT-LLM source report at adg.csdn.net/69730cc6
+ *
+ * Conventions shared by every entry point
+ *   - All pointers named d_* and all tensor pointers (q, k, v, q_out, out, pool, rope table,
+ *     workspace, error word) are DEVICE pointers; h_* pointers are HOST pointers.
+ *   - The caller owns every buffer.  The library allocates no device memory, keeps no state
+ *     between calls other than cached device attributes, and never synchronises the stream:
+ *     each call only enqueues kernels on `stream` and returns (same-stream FIFO ordering as in
+ *     [NOTES] 五 "完整的推理流程", 5.2 CPU/GPU Overlap).
+ *   - Return value: PKV_OK (0) or a negative PKV_ERR_* detected on the host before anything
+ *     was enqueued.  Errors only the device can see (a page id outside [0, num_blocks), a
+ *     bounded wait that ran out) are OR-ed as PKV_DEVERR_* bits into the caller's device int
+ *     `d_error`; the offending access is skipped, no kernel traps.  The caller zeroes d_error
+ *     and reads it back when it wants to know.
+ *   - Tensors are bf16 unless stated otherwise; rows are 16-byte aligned (row strides are in
+ *     elements and must be multiples of 8; base pointers 16-byte aligned).
+ */
+#ifndef PAGED_KV_H_
+#define PAGED_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t; /* == cudaStream_t; NULL = legacy default stream */
+
+/* ---- status codes ----------------------------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARGUMENT (-1) /* NULL pointer, negative or inconsistent count          */
+#define PKV_ERR_UNSUPPORTED (-2)      /* head_dim not 64/128, tokens_per_block not 16..128,
+                                         Hq not a multiple of Hkv, group > 16, bad dtype       */
+#define PKV_ERR_BATCH_ORDER (-3)      /* a context request after a generation request, or a
+                                         generation request with context_length != 1          */
+#define PKV_ERR_CAPACITY (-4)         /* past + new exceeds max_blocks_per_seq * tokens_per_block
+                                         or the RoPE table's max_pos                           */
+#define PKV_ERR_ALIGNMENT (-5)        /* pointer or row stride not 16-byte aligned            */
+#define PKV_ERR_WORKSPACE (-6)        /* workspace NULL or smaller than the size query said     */
+#define PKV_ERR_CUDA (-7)             /* a CUDA runtime/driver call failed (launch, tensor map) */
+
+/* ---- device error bits (OR-ed into *d_error) ---------------------------------------------- */
+#define PKV_DEVERR_BAD_PAGE 1u        /* block-table entry outside [0, num_blocks): skipped     */
+#define PKV_DEVERR_TIMEOUT 2u         /* a bounded mbarrier / TMA wait gave up                   */
+#define PKV_DEVERR_PLAN_MISMATCH 4u   /* device metadata disagrees with the host copies         */
+
+/* ---- KV-pool element type ([ARCH] "KVCacheManager 的三个对外接口": kv_cache_dtype) --------- */
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
+
+/* ---- request phase ([REPORT] 1.1 host_request_types) --------------------------------------- */
+typedef enum { PKV_REQ_CONTEXT = 0, PKV_REQ_GENERATION = 1 } pkv_req_type;
+
+/*
+ * One layer's KV pool.  Layout [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim],
+ * row-major, K at index 0 and V at index 1 of dim 1 ([ARCH] "KVCacheManager 的三个对外接口",
+ * get_buffers).  Element type bf16, or one byte per element (OCP FP8 E4M3) with one scale for
+ * the whole pool ([NOTES] 6.4 "量化": quantise on write with kv_scale_orig_quant, dequantise on
+ * read with kv_scale_quant_orig).
+ */
+typedef struct pkv_pool {
+  void* pool;                /* device, 16-byte aligned                                        */
+  int32_t dtype;             /* pkv_dtype                                                      */
+  int32_t num_blocks;        /* pages in the pool                                              */
+  int32_t tokens_per_block;  /* 16, 32, 64 or 128                                               */
+  int32_t num_kv_heads;      /* Hkv                                                            */
+  int32_t head_dim;          /* D: 64 or 128                                                   */
+  float kv_scale_quant_orig; /* FP8: dequantisation multiplier (value = code * this); ignored for bf16 */
+  float kv_scale_orig_quant; /* FP8: quantisation multiplier (code = e4m3(x * this)), normally
+                                (float)(1 / kv_scale_quant_orig); ignored for bf16            */
+} pkv_pool;
+
+/*
+ * One inflight batch ([ARCH] "AttentionMetadata 的字段与它的含义": seq_lens on host plus
+ * seq_lens_cuda on device, context_lens, num_contexts; [REPORT] 1.2 KeyValueCacheParams:
+ * host_past_key_value_lengths, kv_cache_block_offsets; [REPORT] 1.3: context requests first).
+ * Request r owns packed rows cu_r .. cu_r + context_lengths[r] - 1, cu_r being the sum of
+ * context_lengths over earlier requests.  Its KV sequence after this step's append has
+ * L_r = past_kv_lengths[r] + context_lengths[r] tokens; token t of it lives in page
+ * block_offsets[r * max_blocks_per_seq + t / tokens_per_block], slot t % tokens_per_block.
+ * The host and device copies must hold the same values; the host copies plan the launch, the
+ * device copies are what the kernels read (a disagreement is flagged PKV_DEVERR_PLAN_MISMATCH
+ * where it is detectable).  Two requests may share a page read-only (prefix reuse).
+ */
+typedef struct pkv_batch {
+  int32_t num_requests;       /* R = num_contexts + number of generation requests             */
+  int32_t num_contexts;       /* C: requests 0 .. C-1 are context requests                    */
+  int32_t num_tokens;         /* T = sum of context_lengths                                   */
+  int32_t max_blocks_per_seq; /* row length of the block table                                */
+  const int32_t* h_request_types;   /* host [R], pkv_req_type                                 */
+  const int32_t* h_context_lengths; /* host [R], new tokens this step (1 for generation)      */
+  const int32_t* h_past_kv_lengths; /* host [R], tokens already in the pool                   */
+  const int32_t* d_context_lengths; /* device copy of h_context_lengths                       */
+  const int32_t* d_past_kv_lengths; /* device copy of h_past_kv_lengths                       */
+  const int32_t* d_block_offsets;   /* device [R, max_blocks_per_seq] page ids                */
+} pkv_batch;
+
+/*
+ * Bytes of the fp32 (cos, sin) RoPE table for positions 0 .. max_pos-1: max_pos * head_dim * 4.
+ */
+size_t paged_rope_table_bytes(int32_t head_dim, int32_t max_pos);
+
+/*
+ * Fill a HOST buffer with the GPT-NeoX RoPE table ([REPORT] 1.1: rotary_embedding, "GPT-NeoX"
+ * variant): entry [p][j] = (cos(p * theta_j), sin(p * theta_j)) with theta_j = base^(-2j/D),
+ * j < D/2, each computed in fp64 and rounded once to fp32.  The caller uploads it once per
+ * (base, D, max_pos); paged_kv_append_rope reads it.  Returns PKV_OK or
+ * PKV_ERR_INVALID_ARGUMENT.  Host-only set-up, not part of the per-step path.
+ */
+int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float* h_table);
+
+/*
+ * RoPE + append ([NOTES] 二.2 "KVCacheManager 详解": the attention op writes each new token's
+ * K/V into the pages named by the block table; [ARCH] "AttentionMetadata 的字段与它的含义":
+ * the backend may apply RoPE itself when position_ids is None; [NOTES] 6.4 "量化": quantise
+ * on write).  For every packed row (request r, index i, position p = past_r + i):
+ *   q_out[row, h*D:(h+1)*D] = bf16(rope(q[row, h*D:(h+1)*D], p))          for h < Hq
+ *   pool[page, 0, slot, h, :] = bf16(rope(k[row, h*D:...], p))            for h < Hkv
+ *   pool[page, 1, slot, h, :] = v[row, h*D:...]
+ * (FP8 pool: e4m3(x * kv_scale_orig_quant) with round-to-nearest-even, saturating to +-448.)
+ * rope(x, p): y_j = x_j c - x_{j+D/2} s, y_{j+D/2} = x_{j+D/2} c + x_j s, (c, s) = table[p][j],
+ * evaluated in fp32 as fma(x_j, c, -(x_{j+D/2} * s)) and fma(x_{j+D/2}, c, x_j * s).
+ *   q, k, v      device bf16 rows [T, Hq*D], [T, Hkv*D], [T, Hkv*D] with row strides in
+ *                elements (a fused QKV tensor can be passed as three views)
+ *   q_out        device bf16 [T, q_out_row_stride]; may equal q (in-place, same stride)
+ *   rope_table   device fp32 table from paged_rope_table_build, max_pos rows
+ *   d_error      device int32, PKV_DEVERR_* bits OR-ed in (bad page: that token's pool write
+ *                is skipped, q_out is still written)
+ * Every pool byte not addressed by a new token is left untouched.  T == 0 is a no-op.
+ */
+int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
+                         const void* q, int64_t q_row_stride, const void* k,
+                         int64_t k_row_stride, const void* v, int64_t v_row_stride, void* q_out,
+                         int64_t q_out_row_stride, const float* rope_table, int32_t max_pos,
+                         int32_t* d_error, pkv_stream_t stream);
+
+/*
+ * Workspace bytes paged_attention_forward needs for this pool geometry, batch and head count
+ * (device plan + fp32 split-KV partials; [NOTES] 五 5.1: the runtime checks that the scratch
+ * workspace is large enough).  0 on invalid arguments.
+ */
+size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* batch,
+                                      int32_t num_q_heads);
+
+/*
+ * Causal GQA attention over the paged pool, after paged_kv_append_rope on the same stream
+ * ([NOTES] 6.1 "两者分工": input length > 1 runs the context (flash-attention) path, length 1
+ * the generation (paged attention) path; 6.2 "Flash Attention算法核心"; 6.3 "Paged Attention
+ * Kernel 内部"; [ARCH] "AttentionMetadata 的字段与它的含义": flattened (num_tokens, heads*D)
+ * tensors).  For packed row (r, i), query head h, KV head h / (Hq/Hkv), position p = past_r + i:
+ *   out[row, h*D:(h+1)*D] = sum_{t <= p} softmax_t(softmax_scale * <q_rot[row,h], K_t>) V_t
+ * with K_t, V_t read through the block table (FP8 pool: value = code * kv_scale_quant_orig),
+ * fp32 accumulation, bf16 output.
+ *   q_rot        device bf16 [T, q_row_stride] rotated queries (q_out of the append)
+ *   out          device bf16 [T, Hq*D] (row stride Hq*D)
+ *   workspace    device, at least paged_attention_workspace_size bytes, 256-byte aligned;
+ *                its contents need not be initialised and are scratch after the call
+ *   d_error      device int32 error bits as above
+ * Context rows use a tcgen05/TMEM tensor-core kernel, generation rows a split-KV decode kernel
+ * plus a log-sum-exp combine; all launches go to `stream`.  T == 0 is a no-op.
+ */
+int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
+                            const void* q_rot, int64_t q_row_stride, void* out,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            int32_t* d_error, pkv_stream_t stream);
+
+/* Number of kernels the last successful call of either entry point on this thread enqueued. */
+int32_t paged_kv_last_launch_count(void);
+
+/* Name of the i-th kernel the last call on this thread enqueued ("append_rope", "plan",
+ * "context_attn", "decode_splitkv", "combine"), or NULL when i is out of range. */
+const char* paged_kv_last_launch_name(int32_t i);
+
+/*
+ * Optional per-kernel timing for profiling harnesses.  `events` points to 2 * max_kernels
+ * cudaEvent_t handles (created by the caller, host array owned by the caller and kept alive
+ * while set).  Every later call on this thread records events[2i] on the stream just before
+ * its i-th kernel and events[2i + 1] just after it, for i < max_kernels.  NULL turns it off.
+ * Returns PKV_OK or PKV_ERR_INVALID_ARGUMENT.
+ */
+int paged_kv_set_kernel_events(void* const* events, int32_t max_kernels);
+
+/* Static string for a PKV_OK / PKV_ERR_* code. */
+const char* paged_kv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H_ */

@@ -1,0 +1,282 @@
+"""Python binding of libpaged_kv.so, the GB300 (sm_103a) paged-KV RoPE + attention library.
+
+Argument marshalling only: every step of the hot path runs in the library's CUDA kernels.
+PyTorch provides device memory and streams.  The entry points keep the C names:
+
+    paged_rope_table_build(base, head_dim, max_pos, device)        -> fp32 table on the device
+    paged_kv_append_rope(pool, batch, num_q_heads, q, k, v, q_out, rope_table, d_error)
+    paged_attention_workspace_size(pool, batch, num_q_heads)       -> bytes
+    paged_attention_forward(pool, batch, num_q_heads, q_rot, out, softmax_scale, workspace, d_error)
+
+``pool`` is a :class:`KVPool` (the [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim]
+tensor plus its dtype and FP8 scales) and ``batch`` a :class:`BatchMeta` (host and device
+copies of the per-request metadata).  A missing or unloadable library raises immediately; there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
+
+PKV_OK = 0
+PKV_BF16 = 0
+PKV_FP8_E4M3 = 1
+PKV_REQ_CONTEXT = 0
+PKV_REQ_GENERATION = 1
+PKV_DEVERR_BAD_PAGE = 1
+PKV_DEVERR_TIMEOUT = 2
+PKV_DEVERR_PLAN_MISMATCH = 4
+
+# the C ABI's exported symbols (include/paged_kv.h)
+EXPORTS = (
+    "paged_rope_table_bytes",
+    "paged_rope_table_build",
+    "paged_kv_append_rope",
+    "paged_attention_workspace_size",
+    "paged_attention_forward",
+    "paged_kv_last_launch_count",
+    "paged_kv_last_launch_name",
+    "paged_kv_set_kernel_events",
+    "paged_kv_status_string",
+)
+
+
+class PkvPool(C.Structure):
+    _fields_ = [("pool", C.c_void_p), ("dtype", C.c_int32), ("num_blocks", C.c_int32),
+                ("tokens_per_block", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("kv_scale_quant_orig", C.c_float),
+                ("kv_scale_orig_quant", C.c_float)]
+
+
+class PkvBatch(C.Structure):
+    _fields_ = [("num_requests", C.c_int32), ("num_contexts", C.c_int32),
+                ("num_tokens", C.c_int32), ("max_blocks_per_seq", C.c_int32),
+                ("h_request_types", C.c_void_p), ("h_context_lengths", C.c_void_p),
+                ("h_past_kv_lengths", C.c_void_p), ("d_context_lengths", C.c_void_p),
+                ("d_past_kv_lengths", C.c_void_p), ("d_block_offsets", C.c_void_p)]
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libpaged_kv.so (built in-tree by ``paged_kv_cache_rope_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise PagedKVError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_cache_rope_gb300.build` (CUDA 13, sm_103a)")
+        L = C.CDLL(LIB_PATH)
+        P, i32, i64, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+        L.paged_rope_table_bytes.argtypes = [i32, i32]
+        L.paged_rope_table_bytes.restype = sz
+        L.paged_rope_table_build.argtypes = [C.c_double, i32, i32, P]
+        L.paged_rope_table_build.restype = C.c_int
+        L.paged_kv_append_rope.argtypes = [P, P, i32, P, i64, P, i64, P, i64, P, i64, P, i32, P, P]
+        L.paged_kv_append_rope.restype = C.c_int
+        L.paged_attention_workspace_size.argtypes = [P, P, i32]
+        L.paged_attention_workspace_size.restype = sz
+        L.paged_attention_forward.argtypes = [P, P, i32, P, i64, P, C.c_float, P, sz, P, P]
+        L.paged_attention_forward.restype = C.c_int
+        L.paged_kv_last_launch_count.argtypes = []
+        L.paged_kv_last_launch_count.restype = i32
+        L.paged_kv_last_launch_name.argtypes = [i32]
+        L.paged_kv_last_launch_name.restype = C.c_char_p
+        L.paged_kv_set_kernel_events.argtypes = [P, i32]
+        L.paged_kv_set_kernel_events.restype = C.c_int
+        L.paged_kv_status_string.argtypes = [C.c_int]
+        L.paged_kv_status_string.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().paged_kv_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != PKV_OK:
+        raise PagedKVError(f"{what}: {status_string(code)} ({code})")
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+@dataclasses.dataclass
+class KVPool:
+    """One layer's paged KV pool [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim]
+    (bf16, or uint8 holding E4M3 codes with one per-pool scale)."""
+    data: torch.Tensor
+    kv_scale_quant_orig: float = 1.0
+    kv_scale_orig_quant: float = 1.0
+
+    def __post_init__(self):
+        assert self.data.dim() == 5 and self.data.shape[1] == 2, "pool must be [NB, 2, B, Hkv, D]"
+        assert self.data.is_contiguous()
+        assert self.data.dtype in (torch.bfloat16, torch.uint8, torch.float8_e4m3fn)
+
+    @property
+    def fp8(self) -> bool:
+        return self.data.dtype != torch.bfloat16
+
+    def c(self) -> PkvPool:
+        NB, _, B, Hkv, D = self.data.shape
+        return PkvPool(self.data.data_ptr(), PKV_FP8_E4M3 if self.fp8 else PKV_BF16, NB, B, Hkv, D,
+                       float(self.kv_scale_quant_orig), float(self.kv_scale_orig_quant))
+
+
+class BatchMeta:
+    """Host and device copies of one inflight batch's metadata (context requests first)."""
+
+    def __init__(self, request_types, context_lengths, past_kv_lengths, block_offsets, device):
+        self.h_request_types = np.ascontiguousarray(request_types, dtype=np.int32)
+        self.h_context_lengths = np.ascontiguousarray(context_lengths, dtype=np.int32)
+        self.h_past_kv_lengths = np.ascontiguousarray(past_kv_lengths, dtype=np.int32)
+        tbl = np.ascontiguousarray(block_offsets, dtype=np.int32)
+        if tbl.ndim == 1:
+            tbl = tbl.reshape(len(self.h_context_lengths), -1)
+        self.h_block_offsets = tbl
+        self.d_context_lengths = torch.from_numpy(self.h_context_lengths.copy()).to(device)
+        self.d_past_kv_lengths = torch.from_numpy(self.h_past_kv_lengths.copy()).to(device)
+        self.d_block_offsets = torch.from_numpy(tbl.copy()).to(device)
+
+    @property
+    def num_requests(self) -> int:
+        return int(self.h_context_lengths.shape[0])
+
+    @property
+    def num_contexts(self) -> int:
+        return int((self.h_request_types == PKV_REQ_CONTEXT).sum())
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.h_context_lengths.sum())
+
+    def c(self) -> PkvBatch:
+        R = self.num_requests
+        return PkvBatch(R, self.num_contexts, self.num_tokens, int(self.h_block_offsets.shape[1]),
+                        self.h_request_types.ctypes.data, self.h_context_lengths.ctypes.data,
+                        self.h_past_kv_lengths.ctypes.data, self.d_context_lengths.data_ptr(),
+                        self.d_past_kv_lengths.data_ptr(), self.d_block_offsets.data_ptr())
+
+
+# --- entry points --------------------------------------------------------------------------
+
+def paged_rope_table_build(base: float, head_dim: int, max_pos: int, device="cuda") -> torch.Tensor:
+    """GPT-NeoX (cos, sin) table [max_pos, head_dim // 2, 2] fp32, built on the host by the
+    library and uploaded once."""
+    host = np.empty((max_pos, head_dim // 2, 2), dtype=np.float32)
+    _check(lib().paged_rope_table_build(float(base), int(head_dim), int(max_pos), host.ctypes.data),
+           "paged_rope_table_build")
+    return torch.from_numpy(host).to(device)
+
+
+def paged_kv_append_rope(pool: KVPool, batch: BatchMeta, num_q_heads: int, q: torch.Tensor,
+                         k: torch.Tensor, v: torch.Tensor, q_out: torch.Tensor,
+                         rope_table: torch.Tensor, d_error: torch.Tensor, stream=None) -> None:
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_out", q_out)):
+        assert t.dtype == torch.bfloat16 and t.dim() == 2 and t.stride(1) == 1, name
+    assert rope_table.dtype == torch.float32 and rope_table.is_contiguous()
+    pc, bc = pool.c(), batch.c()
+    code = lib().paged_kv_append_rope(
+        C.byref(pc), C.byref(bc), int(num_q_heads), _ptr(q), q.stride(0), _ptr(k), k.stride(0),
+        _ptr(v), v.stride(0), _ptr(q_out), q_out.stride(0), _ptr(rope_table),
+        int(rope_table.shape[0]), _ptr(d_error), _stream_ptr(stream))
+    _check(code, "paged_kv_append_rope")
+
+
+def paged_attention_workspace_size(pool: KVPool, batch: BatchMeta, num_q_heads: int) -> int:
+    pc, bc = pool.c(), batch.c()
+    return int(lib().paged_attention_workspace_size(C.byref(pc), C.byref(bc), int(num_q_heads)))
+
+
+def paged_attention_forward(pool: KVPool, batch: BatchMeta, num_q_heads: int, q_rot: torch.Tensor,
+                            out: torch.Tensor, softmax_scale: float, workspace: torch.Tensor,
+                            d_error: torch.Tensor, stream=None) -> None:
+    assert q_rot.dtype == torch.bfloat16 and q_rot.stride(1) == 1
+    assert out.dtype == torch.bfloat16 and out.is_contiguous()
+    pc, bc = pool.c(), batch.c()
+    code = lib().paged_attention_forward(
+        C.byref(pc), C.byref(bc), int(num_q_heads), _ptr(q_rot), q_rot.stride(0), _ptr(out),
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(d_error), _stream_ptr(stream))
+    _check(code, "paged_attention_forward")
+
+
+def last_launch_count() -> int:
+    return int(lib().paged_kv_last_launch_count())
+
+
+def last_launch_names() -> list[str]:
+    out = []
+    for i in range(last_launch_count()):
+        n = lib().paged_kv_last_launch_name(i)
+        out.append(n.decode() if n else "?")
+    return out
+
+
+class KernelEvents:
+    """Caller-owned cudaEvent_t handles the library records around each of its kernels
+    (``paged_kv_set_kernel_events``); used by the benchmark to time kernels on their stream."""
+
+    def __init__(self, max_kernels: int):
+        self.max_kernels = max_kernels
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_kernels)]
+        for e in self.events:  # force creation of the underlying CUDA events
+            e.record()
+        self._arr = (C.c_void_p * (2 * max_kernels))(*[int(e.cuda_event) for e in self.events])
+
+    def __enter__(self):
+        _check(lib().paged_kv_set_kernel_events(self._arr, self.max_kernels), "paged_kv_set_kernel_events")
+        return self
+
+    def __exit__(self, *exc):
+        lib().paged_kv_set_kernel_events(None, 0)
+
+    def elapsed_ms(self, i: int) -> float:
+        return self.events[2 * i].elapsed_time(self.events[2 * i + 1])
+
+
+class PagedAttentionStep:
+    """One layer step (append + attention) over a resident pool, with every buffer allocated
+    once up front so repeated calls allocate nothing."""
+
+    def __init__(self, pool: KVPool, batch: BatchMeta, num_q_heads: int, head_dim: int,
+                 rope_table: torch.Tensor, softmax_scale: float | None = None):
+        dev = pool.data.device
+        self.pool, self.batch, self.Hq, self.D = pool, batch, int(num_q_heads), int(head_dim)
+        self.rope_table = rope_table
+        self.softmax_scale = softmax_scale if softmax_scale is not None else head_dim ** -0.5
+        T = batch.num_tokens
+        self.q_out = torch.empty(T, self.Hq * self.D, dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty(T, self.Hq * self.D, dtype=torch.bfloat16, device=dev)
+        ws = paged_attention_workspace_size(pool, batch, num_q_heads)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.d_error = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.launches = 0
+
+    def __call__(self, q, k, v, stream=None) -> torch.Tensor:
+        paged_kv_append_rope(self.pool, self.batch, self.Hq, q, k, v, self.q_out,
+                             self.rope_table, self.d_error, stream)
+        n = last_launch_count()
+        paged_attention_forward(self.pool, self.batch, self.Hq, self.q_out, self.out,
+                                self.softmax_scale, self.workspace, self.d_error, stream)
+        self.launches = n + last_launch_count()
+        return self.out

@@ -1,0 +1,435 @@
+// api.cpp -- C-ABI front end of libpaged_kv.so: argument validation, launch planning and
+// dispatch.  Everything here runs on the host and only enqueues work on the caller's stream;
+// no device memory is allocated and the stream is never synchronised.
+//
+// Dispatch follows "TensorRT-LLM 1.0 源码学习笔记" 6.1 "两者分工": context requests (input length
+// > 1, and chunked-context requests) go to the flash-attention style tensor-core kernel,
+// generation requests (length 1) to the paged split-KV decode kernel.  Batch ordering (context
+// requests first) follows adg.csdn.net/69730cc6 section 1.3; the workspace-size query mirrors
+// the scratch-workspace check of section 5.1 of the same notes page.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "paged_kv.h"
+
+namespace {
+
+thread_local int32_t g_last_launches = 0;
+thread_local const char* g_last_names[8] = {nullptr};
+thread_local void* const* g_events = nullptr;
+thread_local int32_t g_events_n = 0;
+
+// Brackets one kernel launch of the current call with the caller's timing events (if set) and
+// records its name.
+struct LaunchScope {
+  int idx;
+  cudaStream_t s;
+  LaunchScope(int i, const char* name, cudaStream_t st) : idx(i), s(st) {
+    if (idx < 8) g_last_names[idx] = name;
+    if (g_events && idx < g_events_n) cudaEventRecord(static_cast<cudaEvent_t>(g_events[2 * idx]), s);
+  }
+  ~LaunchScope() {
+    if (g_events && idx < g_events_n) cudaEventRecord(static_cast<cudaEvent_t>(g_events[2 * idx + 1]), s);
+  }
+};
+
+void reset_names() {
+  for (auto& n : g_last_names) n = nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (sms[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 152;
+  }
+  return sms[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 map (64-wide head-dim half, head-dim halves, heads, rows) with a 128-byte swizzle;
+// box = one 64-wide half of `box_rows` rows of one head.
+bool encode_rows_map(CUtensorMap* map, const void* base, int D, int heads, int64_t rows, int64_t row_bytes,
+                     int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[4] = {64, 1, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct HostPlan {
+  int R = 0, C = 0, G = 0, T = 0, ctx_tokens = 0;
+  int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
+  pkv::PlanLayout lay{};
+};
+
+int validate_pool(const pkv_pool* pool) {
+  if (!pool || !pool->pool) return PKV_ERR_INVALID_ARGUMENT;
+  if (pool->dtype != PKV_BF16 && pool->dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0) return PKV_ERR_INVALID_ARGUMENT;
+  const int B = pool->tokens_per_block;
+  if (B != 16 && B != 32 && B != 64 && B != 128) return PKV_ERR_UNSUPPORTED;
+  if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(pool->pool)) return PKV_ERR_ALIGNMENT;
+  if (pool->dtype == PKV_FP8_E4M3 &&
+      !(std::isfinite(pool->kv_scale_quant_orig) && std::isfinite(pool->kv_scale_orig_quant) &&
+        pool->kv_scale_quant_orig > 0.f && pool->kv_scale_orig_quant > 0.f))
+    return PKV_ERR_INVALID_ARGUMENT;
+  return PKV_OK;
+}
+
+// Checks the batch against the host copies and fills the counts shared by both entry points.
+int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
+  if (!b) return PKV_ERR_INVALID_ARGUMENT;
+  if (Hq <= 0 || Hq % pool->num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
+  if (Hq / pool->num_kv_heads > 16) return PKV_ERR_UNSUPPORTED;
+  const int R = b->num_requests, C = b->num_contexts;
+  if (R < 0 || C < 0 || C > R || b->num_tokens < 0) return PKV_ERR_INVALID_ARGUMENT;
+  hp->R = R;
+  hp->C = C;
+  hp->G = R - C;
+  hp->T = b->num_tokens;
+  if (R == 0) return b->num_tokens == 0 ? PKV_OK : PKV_ERR_INVALID_ARGUMENT;
+  if (b->max_blocks_per_seq <= 0) return PKV_ERR_INVALID_ARGUMENT;
+  if (!b->h_request_types || !b->h_context_lengths || !b->h_past_kv_lengths || !b->d_context_lengths ||
+      !b->d_past_kv_lengths || !b->d_block_offsets)
+    return PKV_ERR_INVALID_ARGUMENT;
+  const int64_t cap = static_cast<int64_t>(b->max_blocks_per_seq) * pool->tokens_per_block;
+  int64_t T = 0, ctx_tokens = 0;
+  for (int r = 0; r < R; ++r) {
+    const int type = b->h_request_types[r];
+    const int n = b->h_context_lengths[r], past = b->h_past_kv_lengths[r];
+    if (n < 1 || past < 0) return PKV_ERR_INVALID_ARGUMENT;
+    if (r < C) {
+      if (type != PKV_REQ_CONTEXT) return PKV_ERR_BATCH_ORDER;
+      ctx_tokens += n;
+    } else {
+      if (type != PKV_REQ_GENERATION || n != 1) return PKV_ERR_BATCH_ORDER;
+    }
+    if (static_cast<int64_t>(past) + n > cap) return PKV_ERR_CAPACITY;
+    if (static_cast<int64_t>(past) + n > INT32_MAX / 2) return PKV_ERR_CAPACITY;
+    T += n;
+  }
+  if (T != b->num_tokens) return PKV_ERR_INVALID_ARGUMENT;
+  hp->ctx_tokens = static_cast<int>(ctx_tokens);
+  return PKV_OK;
+}
+
+// Decode split length (tokens, multiple of 16): about 4 CTAs per SM over the whole batch, each
+// CTA streaming 64..512 tokens of one KV head.
+int choose_kv_chunk(const pkv_batch* b, int C, int Hkv) {
+  int64_t total = 0;
+  for (int r = C; r < b->num_requests; ++r) total += b->h_past_kv_lengths[r] + 1;
+  const int64_t target = static_cast<int64_t>(device_sm_count()) * 4;
+  int64_t chunk = (total * Hkv + target - 1) / std::max<int64_t>(target, 1);
+  chunk = (chunk + 15) / 16 * 16;
+  return static_cast<int>(std::min<int64_t>(512, std::max<int64_t>(64, chunk)));
+}
+
+void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
+  hp->num_tiles = 0;
+  for (int r = 0; r < hp->C; ++r) hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxTileM - 1) / pkv::kCtxTileM;
+  hp->kv_chunk = choose_kv_chunk(b, hp->C, pool->num_kv_heads);
+  hp->num_splits = 0;
+  hp->max_splits = 0;
+  for (int r = hp->C; r < hp->R; ++r) {
+    const int s = (b->h_past_kv_lengths[r] + 1 + hp->kv_chunk - 1) / hp->kv_chunk;
+    hp->num_splits += s;
+    hp->max_splits = std::max(hp->max_splits, s);
+  }
+  pkv::PlanLayout& L = hp->lay;
+  L.cu_q = 0;
+  L.tile_prefix = L.cu_q + hp->R + 1;
+  L.split_prefix = L.tile_prefix + hp->C + 1;
+  L.int_words = L.split_prefix + hp->G + 1;
+  const int64_t int_bytes = (L.int_words * 4 + 255) / 256 * 256;
+  const int64_t D = pool->head_dim;
+  L.part_o = int_bytes;
+  L.part_ml = L.part_o + (static_cast<int64_t>(hp->num_splits) * Hq * D * 4 + 255) / 256 * 256;
+  L.total_bytes = L.part_ml + (static_cast<int64_t>(hp->num_splits) * Hq * 2 * 4 + 255) / 256 * 256;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* paged_kv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported geometry or dtype";
+    case PKV_ERR_BATCH_ORDER: return "batch order: context requests must come first, generation requests have one token";
+    case PKV_ERR_CAPACITY: return "sequence exceeds block table or RoPE table capacity";
+    case PKV_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t paged_kv_last_launch_count(void) { return g_last_launches; }
+
+const char* paged_kv_last_launch_name(int32_t i) {
+  return (i >= 0 && i < g_last_launches && i < 8) ? g_last_names[i] : nullptr;
+}
+
+int paged_kv_set_kernel_events(void* const* events, int32_t max_kernels) {
+  if (events && max_kernels <= 0) return PKV_ERR_INVALID_ARGUMENT;
+  g_events = events;
+  g_events_n = events ? max_kernels : 0;
+  return PKV_OK;
+}
+
+size_t paged_rope_table_bytes(int32_t head_dim, int32_t max_pos) {
+  if (head_dim <= 0 || max_pos <= 0) return 0;
+  return static_cast<size_t>(max_pos) * static_cast<size_t>(head_dim) * sizeof(float);
+}
+
+int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float* h_table) {
+  if (!h_table || head_dim <= 0 || (head_dim & 1) || max_pos <= 0 || !(base > 0.0)) return PKV_ERR_INVALID_ARGUMENT;
+  const int half = head_dim / 2;
+  std::vector<double> theta(half);
+  for (int j = 0; j < half; ++j) theta[j] = std::pow(base, -(2.0 * static_cast<double>(j)) / static_cast<double>(head_dim));
+  for (int64_t p = 0; p < max_pos; ++p) {
+    float* row = h_table + p * head_dim;
+    for (int j = 0; j < half; ++j) {
+      const double a = static_cast<double>(p) * theta[j];
+      row[2 * j] = static_cast<float>(std::cos(a));
+      row[2 * j + 1] = static_cast<float>(std::sin(a));
+    }
+  }
+  return PKV_OK;
+}
+
+int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q,
+                         int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                         int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
+                         int32_t max_pos, int32_t* d_error, pkv_stream_t stream) {
+  g_last_launches = 0;
+  int st = validate_pool(pool);
+  if (st) return st;
+  HostPlan hp;
+  st = validate_batch(pool, batch, num_q_heads, &hp);
+  if (st) return st;
+  if (hp.T == 0) return PKV_OK;
+  const int D = pool->head_dim, Hkv = pool->num_kv_heads;
+  if (!q || !k || !v || !q_out || !rope_table || max_pos <= 0) return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(rope_table))
+    return PKV_ERR_ALIGNMENT;
+  if ((q_row_stride & 7) || (k_row_stride & 7) || (v_row_stride & 7) || (q_out_row_stride & 7)) return PKV_ERR_ALIGNMENT;
+  if (q_row_stride < static_cast<int64_t>(num_q_heads) * D || q_out_row_stride < static_cast<int64_t>(num_q_heads) * D ||
+      k_row_stride < static_cast<int64_t>(Hkv) * D || v_row_stride < static_cast<int64_t>(Hkv) * D)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (q_out == q && q_out_row_stride != q_row_stride) return PKV_ERR_INVALID_ARGUMENT;
+  for (int r = 0; r < hp.R; ++r)
+    if (static_cast<int64_t>(batch->h_past_kv_lengths[r]) + batch->h_context_lengths[r] > max_pos) return PKV_ERR_CAPACITY;
+  if (hp.R > 12000) return PKV_ERR_UNSUPPORTED;  // in-CTA prefix scan keeps R + 1 ints in shared memory
+
+  pkv::AppendParams p{};
+  p.R = hp.R;
+  p.T = hp.T;
+  p.Hq = num_q_heads;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.B = pool->tokens_per_block;
+  p.NB = pool->num_blocks;
+  p.max_blocks = batch->max_blocks_per_seq;
+  p.q = static_cast<const uint16_t*>(q);
+  p.q_stride = q_row_stride;
+  p.k = static_cast<const uint16_t*>(k);
+  p.k_stride = k_row_stride;
+  p.v = static_cast<const uint16_t*>(v);
+  p.v_stride = v_row_stride;
+  p.q_out = static_cast<uint16_t*>(q_out);
+  p.q_out_stride = q_out_row_stride;
+  p.rope = reinterpret_cast<const float2*>(rope_table);
+  p.max_pos = max_pos;
+  p.pool = pool->pool;
+  p.inv_scale = pool->kv_scale_orig_quant;
+  p.ctx_len = batch->d_context_lengths;
+  p.past = batch->d_past_kv_lengths;
+  p.tbl = batch->d_block_offsets;
+  p.d_error = d_error;
+  reset_names();
+  cudaError_t e;
+  {
+    LaunchScope ls(0, "append_rope", reinterpret_cast<cudaStream_t>(stream));
+    e = pkv::launch_append(p, pool->dtype == PKV_FP8_E4M3, reinterpret_cast<cudaStream_t>(stream));
+  }
+  if (e == cudaSuccess) g_last_launches = 1;
+  return cuda_status(e);
+}
+
+size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads) {
+  if (validate_pool(pool)) return 0;
+  HostPlan hp;
+  if (validate_batch(pool, batch, num_q_heads, &hp)) return 0;
+  plan_attention(pool, batch, num_q_heads, &hp);
+  return static_cast<size_t>(hp.lay.total_bytes);
+}
+
+int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q_rot,
+                            int64_t q_row_stride, void* out, float softmax_scale, void* workspace,
+                            size_t workspace_bytes, int32_t* d_error, pkv_stream_t stream) {
+  g_last_launches = 0;
+  int st = validate_pool(pool);
+  if (st) return st;
+  HostPlan hp;
+  st = validate_batch(pool, batch, num_q_heads, &hp);
+  if (st) return st;
+  if (hp.T == 0) return PKV_OK;
+  const int D = pool->head_dim, Hkv = pool->num_kv_heads;
+  if (!q_rot || !out) return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q_rot) || !aligned16(out) || (q_row_stride & 7)) return PKV_ERR_ALIGNMENT;
+  if (q_row_stride < static_cast<int64_t>(num_q_heads) * D) return PKV_ERR_INVALID_ARGUMENT;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARGUMENT;
+  const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+  if (fp8 && hp.C > 0) return PKV_ERR_UNSUPPORTED;  // context kernel reads bf16 pools only
+  plan_attention(pool, batch, num_q_heads, &hp);
+  if (!workspace || workspace_bytes < static_cast<size_t>(hp.lay.total_bytes)) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* ws = static_cast<int32_t*>(workspace);
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  pkv::PlanParams pp{};
+  pp.R = hp.R;
+  pp.C = hp.C;
+  pp.G = hp.G;
+  pp.T = hp.T;
+  pp.expect_tiles = hp.num_tiles;
+  pp.expect_splits = hp.num_splits;
+  pp.kv_chunk = hp.kv_chunk;
+  pp.ctx_len = batch->d_context_lengths;
+  pp.past = batch->d_past_kv_lengths;
+  pp.ws = ws;
+  pp.lay = hp.lay;
+  pp.d_error = d_error;
+  int launches = 0;
+  reset_names();
+  cudaError_t e;
+  {
+    LaunchScope ls(launches, "plan", s);
+    e = pkv::launch_plan(pp, s);
+  }
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  ++launches;
+
+  if (hp.C > 0) {
+    CUtensorMap qmap, kvmap;
+    if (!encode_rows_map(&qmap, q_rot, D, num_q_heads, hp.T, q_row_stride * 2, pkv::kCtxTileM)) return PKV_ERR_CUDA;
+    const int64_t pool_rows = static_cast<int64_t>(pool->num_blocks) * 2 * pool->tokens_per_block;
+    if (!encode_rows_map(&kvmap, pool->pool, D, Hkv, pool_rows, static_cast<int64_t>(Hkv) * D * 2,
+                         std::min(pool->tokens_per_block, pkv::kCtxTileN)))
+      return PKV_ERR_CUDA;
+    pkv::ContextParams cp{};
+    cp.C = hp.C;
+    cp.T = hp.T;
+    cp.Hq = num_q_heads;
+    cp.Hkv = Hkv;
+    cp.group = num_q_heads / Hkv;
+    cp.D = D;
+    cp.B = pool->tokens_per_block;
+    cp.NB = pool->num_blocks;
+    cp.max_blocks = batch->max_blocks_per_seq;
+    cp.num_tiles = hp.num_tiles;
+    cp.cu_q = ws + hp.lay.cu_q;
+    cp.tile_prefix = ws + hp.lay.tile_prefix;
+    cp.ctx_len = batch->d_context_lengths;
+    cp.past = batch->d_past_kv_lengths;
+    cp.tbl = batch->d_block_offsets;
+    cp.pool = static_cast<const uint8_t*>(pool->pool);
+    cp.out = static_cast<uint16_t*>(out);
+    cp.out_stride = static_cast<int64_t>(num_q_heads) * D;
+    cp.scale_log2 = scale_log2;
+    cp.d_error = d_error;
+    {
+      LaunchScope ls(launches, "context_attn", s);
+      e = pkv::launch_context(cp, &qmap, &kvmap, fp8, s);
+    }
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    ++launches;
+  }
+
+  if (hp.G > 0) {
+    pkv::DecodeParams dp{};
+    dp.C = hp.C;
+    dp.G = hp.G;
+    dp.Hq = num_q_heads;
+    dp.Hkv = Hkv;
+    dp.group = num_q_heads / Hkv;
+    dp.D = D;
+    dp.B = pool->tokens_per_block;
+    dp.NB = pool->num_blocks;
+    dp.max_blocks = batch->max_blocks_per_seq;
+    dp.kv_chunk = hp.kv_chunk;
+    dp.gen_row0 = hp.ctx_tokens;
+    dp.total_splits = hp.num_splits;
+    dp.pool = static_cast<const uint8_t*>(pool->pool);
+    dp.kv_scale = fp8 ? pool->kv_scale_quant_orig : 1.0f;
+    dp.scale_log2 = scale_log2;
+    dp.q = static_cast<const uint16_t*>(q_rot);
+    dp.q_stride = q_row_stride;
+    dp.out = static_cast<uint16_t*>(out);
+    dp.past = batch->d_past_kv_lengths;
+    dp.tbl = batch->d_block_offsets;
+    dp.split_prefix = ws + hp.lay.split_prefix;
+    dp.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_o);
+    dp.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_ml);
+    dp.d_error = d_error;
+    {
+      LaunchScope ls(launches, "decode_splitkv", s);
+      e = pkv::launch_decode(dp, fp8, s, nullptr);
+    }
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    ++launches;
+    if (hp.max_splits > 1) {
+      {
+        LaunchScope ls(launches, "combine", s);
+        e = pkv::launch_combine(dp, s);
+      }
+      if (e != cudaSuccess) return PKV_ERR_CUDA;
+      ++launches;
+    }
+  }
+  g_last_launches = launches;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,551 @@
+// decode_attn.cu -- launch plan, split-KV ("flash-decoding") paged attention for generation
+// requests, and the log-sum-exp combine of the splits.
+//
+// Pages: "TensorRT-LLM 1.0 源码学习笔记", 6.3 "Paged Attention Kernel 内部" (one query token per
+// generation request; loop over the request's KV blocks through the block pointers; QK^T,
+// softmax, weighted sum of V) and 6.1 "两者分工" (generation = input length 1);
+// "TensorRT-LLM 源码完全拆解(一)", "AttentionMetadata 的字段与它的含义" (packed rows, host and
+// device copies of the lengths); "TensorRT-LLM框架概述" (intelliparadigm.com) section 1: decode
+// is bound by memory bandwidth.
+//
+// Redesign for GB300 (the pages' kernel gives one CTA per (request, head); here):
+//   * the work unit is (generation request, KV head, split of kv_chunk tokens), so short and
+//     long requests both fill 152 SMs;
+//   * a CTA's warps each stream their own run of 16-token tiles with a cp.async ring through
+//     shared memory (zero-fill past the sequence end), one block-table lookup per tile;
+//   * each KV head is read once for its whole GQA query group: S^T = K Q^T and
+//     O^T += V^T P^T run on mma.sync m16n8k16 with the group (up to 8 heads per n-tile) on N;
+//   * online softmax in base 2 with warp-shuffle column maxima; warps merge in shared memory;
+//   * splits of one request are merged by combine_kernel with a log-sum-exp rescale.
+// FP8 pools: codes convert exactly to f16 (cvt e4m3x2 -> f16x2); Q is scaled by a power of two
+// into f16 range, and the per-pool scale is applied to scores and outputs in fp32.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+// --------------------------------------------------------------------------------------------
+// plan: prefix sums the other kernels index with (one CTA)
+// --------------------------------------------------------------------------------------------
+constexpr int kPlanThreads = 256;
+
+// One pass over the requests: exclusive prefix sums of (new tokens, context query tiles,
+// generation splits) at once, so the whole plan costs a single sweep of block-wide scans.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+  __shared__ int3 s_warp[kPlanThreads / 32];
+  __shared__ int3 s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int32_t* cu = p.ws + p.lay.cu_q;
+  int32_t* tiles = p.ws + p.lay.tile_prefix;
+  int32_t* splits = p.ws + p.lay.split_prefix;
+  const int C = p.C, chunk = p.kv_chunk;
+  bool bad = false;
+  if (tid == 0) s_carry = make_int3(0, 0, 0);
+  __syncthreads();
+  for (int base = 0; base < p.R; base += kPlanThreads) {
+    const int r = base + tid;
+    int3 x = make_int3(0, 0, 0);
+    if (r < p.R) {
+      const int n = __ldg(p.ctx_len + r);
+      x.x = n;
+      if (r < C) {
+        x.y = (n + kCtxTileM - 1) / kCtxTileM;
+      } else {
+        x.z = (__ldg(p.past + r) + 1 + chunk - 1) / chunk;
+        bad |= n != 1;
+      }
+    }
+    int3 incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, incl.x, o);
+      const int b = __shfl_up_sync(0xffffffffu, incl.y, o);
+      const int c = __shfl_up_sync(0xffffffffu, incl.z, o);
+      if (lane >= o) {
+        incl.x += a;
+        incl.y += b;
+        incl.z += c;
+      }
+    }
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int3 w = lane < kPlanThreads / 32 ? s_warp[lane] : make_int3(0, 0, 0);
+      int3 wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, wi.x, o);
+        const int b = __shfl_up_sync(0xffffffffu, wi.y, o);
+        const int c = __shfl_up_sync(0xffffffffu, wi.z, o);
+        if (lane >= o) {
+          wi.x += a;
+          wi.y += b;
+          wi.z += c;
+        }
+      }
+      if (lane < kPlanThreads / 32) s_warp[lane] = make_int3(wi.x - w.x, wi.y - w.y, wi.z - w.z);
+    }
+    __syncthreads();
+    const int3 cy = s_carry, wo = s_warp[wid];
+    const int ex = cy.x + wo.x + incl.x - x.x, ey = cy.y + wo.y + incl.y - x.y, ez = cy.z + wo.z + incl.z - x.z;
+    if (r < p.R) {
+      cu[r] = ex;
+      if (r < C) tiles[r] = ey;
+      else splits[r - C] = ez;
+    }
+    __syncthreads();
+    if (tid == kPlanThreads - 1) s_carry = make_int3(ex + x.x, ey + x.y, ez + x.z);
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int3 t = s_carry;
+    cu[p.R] = t.x;
+    tiles[C] = t.y;
+    splits[p.G] = t.z;
+    bad |= (t.x != p.T) || (t.y != p.expect_tiles) || (t.z != p.expect_splits);
+  }
+  if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+}
+
+// --------------------------------------------------------------------------------------------
+// split-KV decode
+// --------------------------------------------------------------------------------------------
+template <int D, bool FP8>
+struct DecodeCfg {
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+  static constexpr int kChunksPerRow = kRowBytes / 16;
+  static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one of K or V
+  static constexpr int kStages = FP8 ? 6 : 3;
+  static constexpr int kWarpBytes = kStages * 2 * kTileBytes;
+  static constexpr int kSmemBytes = kWarps * kWarpBytes;
+};
+
+// Physical 16-byte chunk of logical chunk c in tile row `row` (bank-conflict-free layouts for
+// the fragment loads below; each is a bijection inside a row).
+template <int D, bool FP8>
+__device__ __forceinline__ int swz_k(int row, int c) {
+  if constexpr (FP8 && D == 64) return c ^ (row & 3);
+  else return c ^ (row & 7);
+}
+template <int D, bool FP8>
+__device__ __forceinline__ int swz_v(int row, int c) {
+  if constexpr (!FP8) return c ^ (row & 7);
+  else if constexpr (D == 128) return c ^ (((row >> 1) & 3) << 1);
+  else return c ^ (((row >> 1) & 1) << 1);
+}
+
+template <int D, bool FP8, int NT>
+__global__ void __launch_bounds__(DecodeCfg<D, FP8>::kThreads)
+decode_splitkv_kernel(DecodeParams p) {
+  using Cfg = DecodeCfg<D, FP8>;
+  constexpr int KS = D / 16;  // k-steps over the head dim / m-tiles of O^T
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g8 = lane >> 2, q4 = lane & 3;  // fragment row group / column pair
+  const int item = blockIdx.x, h = blockIdx.y;
+
+  // ---- which generation request and split this CTA owns ----
+  if (item >= p.total_splits) return;
+  int lo = 0, hi = p.G - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.split_prefix + mid) <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  const int gr = lo, r = p.C + gr;
+  const int s_idx = item - __ldg(p.split_prefix + gr);
+  const int num_splits = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
+  const int L = __ldg(p.past + r) + 1;
+  const int t_begin = s_idx * p.kv_chunk;
+  const int t_end = min(L, t_begin + p.kv_chunk);
+  if (s_idx >= num_splits || t_begin >= t_end) {
+    if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+    return;
+  }
+  const int n_tiles = (t_end - t_begin + kDecodeTile - 1) / kDecodeTile;
+  const int my_first = (warp * n_tiles) / Cfg::kWarps;
+  const int my_n = ((warp + 1) * n_tiles) / Cfg::kWarps - my_first;
+  const int qrow = p.gen_row0 + gr;
+  const uint16_t* qbase = p.q + static_cast<int64_t>(qrow) * p.q_stride;
+
+  // ---- Q fragments (B operand of S^T = K Q^T): column n = query head h*group + nt*8 + g8 ----
+  uint32_t qb[NT][KS][2];
+  float colscale[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hl = nt * 8 + g8;
+    const bool valid = hl < p.group;
+    const uint16_t* qh = qbase + static_cast<int64_t>(h * p.group + (valid ? hl : 0)) * D;
+    if constexpr (!FP8) {
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qb[nt][kk][0] = valid ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * q4) : 0u;
+        qb[nt][kk][1] = valid ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * q4 + 8) : 0u;
+      }
+      colscale[nt][0] = colscale[nt][1] = p.scale_log2;
+    } else {
+      // this lane holds head-dim slice [q4*D/4, (q4+1)*D/4); k-step kk uses 4 consecutive dims
+      float x[D / 4];
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < D / 4; e += 2) {
+        uint32_t w = valid ? *reinterpret_cast<const uint32_t*>(qh + q4 * (D / 4) + e) : 0u;
+        x[e] = __uint_as_float(w << 16);
+        x[e + 1] = __uint_as_float(w & 0xFFFF0000u);
+        amax = fmaxf(amax, fmaxf(fabsf(x[e]), fabsf(x[e + 1])));
+      }
+      amax = warp_max_xor(amax, 1);
+      amax = warp_max_xor(amax, 2);
+      int ex = 0;
+      if (amax > 0.f) frexpf(amax, &ex);
+      const float up = ldexpf(1.f, 8 - ex);  // amax * up lies in [128, 256)
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qb[nt][kk][0] = pack_f16x2(x[4 * kk] * up, x[4 * kk + 1] * up);
+        qb[nt][kk][1] = pack_f16x2(x[4 * kk + 2] * up, x[4 * kk + 3] * up);
+      }
+      // score columns 2*q4, 2*q4+1 belong to heads held by lanes (2*q4)*4 and (2*q4+1)*4
+      const float down = 1.f / up;
+      const float d0 = __shfl_sync(0xffffffffu, down, (2 * q4) * 4);
+      const float d1 = __shfl_sync(0xffffffffu, down, (2 * q4 + 1) * 4);
+      colscale[nt][0] = d0 * p.kv_scale * p.scale_log2;
+      colscale[nt][1] = d1 * p.kv_scale * p.scale_log2;
+    }
+  }
+
+  float o[NT][KS][4];
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+  }
+
+  uint8_t* wbuf = smem + warp * Cfg::kWarpBytes;
+  const uint32_t wbuf_s = smem_u32(wbuf);
+  const int32_t* tbl_r = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
+  const int64_t row_pitch = static_cast<int64_t>(p.Hkv) * Cfg::kRowBytes;  // bytes between slots
+  const int64_t kv_pitch = static_cast<int64_t>(p.B) * row_pitch;           // K -> V in a page
+
+  auto load_tile = [&](int tile, int stage) {
+    const int t0 = t_begin + (my_first + tile) * kDecodeTile;
+    const int lb = t0 / p.B, slot0 = t0 - lb * p.B;
+    int page = lb < p.max_blocks ? __ldg(tbl_r + lb) : -1;
+    bool page_ok = page >= 0 && page < p.NB;
+    if (!page_ok) {
+      if (lane == 0) flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+      page = 0;
+    }
+    const uint8_t* kbase = p.pool + (static_cast<int64_t>(page) * 2 * kv_pitch) +
+                           static_cast<int64_t>(slot0) * row_pitch + static_cast<int64_t>(h) * Cfg::kRowBytes;
+    const uint32_t sK = wbuf_s + stage * 2 * Cfg::kTileBytes;
+    const uint32_t sV = sK + Cfg::kTileBytes;
+#pragma unroll
+    for (int i = 0; i < Cfg::kChunksPerRow / 2; ++i) {
+      const int c_lin = lane + 32 * i;
+      const int row = c_lin / Cfg::kChunksPerRow, c = c_lin % Cfg::kChunksPerRow;
+      const bool ok = page_ok && (t0 + row < t_end);
+      const uint8_t* src = kbase + row * row_pitch + c * 16;
+      cp_async_16(sK + row * Cfg::kRowBytes + (swz_k<D, FP8>(row, c) << 4), ok ? src : p.pool, ok ? 16u : 0u);
+      cp_async_16(sV + row * Cfg::kRowBytes + (swz_v<D, FP8>(row, c) << 4), ok ? src + kv_pitch : p.pool,
+                  ok ? 16u : 0u);
+    }
+  };
+
+  constexpr int S = Cfg::kStages;
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < my_n) load_tile(s, s);
+    cp_async_commit();
+  }
+
+  for (int it = 0; it < my_n; ++it) {
+    cp_async_wait<S - 2>();
+    __syncwarp();
+    {
+      const int nxt = it + S - 1;
+      if (nxt < my_n) load_tile(nxt, nxt % S);
+      cp_async_commit();
+    }
+    const int stage = it % S;
+    const uint32_t sK = wbuf_s + stage * 2 * Cfg::kTileBytes;
+    const uint32_t sV = sK + Cfg::kTileBytes;
+    const int t0 = t_begin + (my_first + it) * kDecodeTile;
+
+    // ---- S^T[16 tokens x 8 heads] = K Q^T ----
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    if constexpr (!FP8) {
+      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t a[4];
+        ldmatrix_x4(a, sK + row * Cfg::kRowBytes + (swz_k<D, FP8>(row, 2 * kk + (lane >> 4)) << 4));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+      }
+    } else {
+      constexpr int CPL = D / 64;  // 16-byte chunks per lane per row
+      uint4 kw[2][CPL];
+      const uint8_t* sKp = wbuf + stage * 2 * Cfg::kTileBytes;
+#pragma unroll
+      for (int rs = 0; rs < 2; ++rs) {
+        const int row = g8 + 8 * rs;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i)
+          kw[rs][i] = *reinterpret_cast<const uint4*>(sKp + row * Cfg::kRowBytes +
+                                                      (swz_k<D, FP8>(row, q4 * CPL + i) << 4));
+      }
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2]);
+        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2]);
+        const uint32_t lo_w = w0[kk & 3], hi_w = w1[kk & 3];
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo_w & 0xFFFF));
+        a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo_w >> 16));
+        a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi_w & 0xFFFF));
+        a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi_w >> 16));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+      }
+    }
+
+    // ---- online softmax over this tile (columns 2*q4, 2*q4+1; rows g8, g8+8) ----
+    uint32_t pb[NT][2];
+    const bool r0_ok = t0 + g8 < t_end, r1_ok = t0 + g8 + 8 < t_end;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float s0 = r0_ok ? sacc[nt][0] * colscale[nt][0] : -INFINITY;
+      float s1 = r0_ok ? sacc[nt][1] * colscale[nt][1] : -INFINITY;
+      float s2 = r1_ok ? sacc[nt][2] * colscale[nt][0] : -INFINITY;
+      float s3 = r1_ok ? sacc[nt][3] * colscale[nt][1] : -INFINITY;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) {
+        mx0 = warp_max_xor(mx0, msk);
+        mx1 = warp_max_xor(mx1, msk);
+      }
+      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+      const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+      const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+      const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+      l_run[nt][0] = l_run[nt][0] * al0 + p0 + p2;
+      l_run[nt][1] = l_run[nt][1] * al1 + p1 + p3;
+      m_run[nt][0] = mn0;
+      m_run[nt][1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[nt][mt][0] *= al0;
+        o[nt][mt][1] *= al1;
+        o[nt][mt][2] *= al0;
+        o[nt][mt][3] *= al1;
+      }
+      if constexpr (!FP8) {
+        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+      } else {
+        pb[nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
+        pb[nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+      }
+    }
+
+    // ---- O^T[D x 8 heads] += V^T P^T ----
+    if constexpr (!FP8) {
+      const int row = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, sV + row * Cfg::kRowBytes + (swz_v<D, FP8>(row, 2 * mt + ((lane >> 3) & 1)) << 4));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
+      }
+    } else {
+      const uint8_t* sVp = wbuf + stage * 2 * Cfg::kTileBytes + Cfg::kTileBytes;
+      const int rows[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+#pragma unroll
+      for (int pp = 0; pp < D / 32; ++pp) {
+        const int c = 2 * pp + (g8 >> 2), in_chunk = (4 * g8) & 15;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w[i] = *reinterpret_cast<const uint32_t*>(sVp + rows[i] * Cfg::kRowBytes +
+                                                    (swz_v<D, FP8>(rows[i], c) << 4) + in_chunk);
+        // 4x4 byte transpose: dj = (w0.bj, w1.bj, w2.bj, w3.bj) = dim j at tokens 2q,2q+1,2q+8,2q+9
+        const uint32_t x0 = __byte_perm(w[0], w[1], 0x5140), x1 = __byte_perm(w[0], w[1], 0x7362);
+        const uint32_t y0 = __byte_perm(w[2], w[3], 0x5140), y1 = __byte_perm(w[2], w[3], 0x7362);
+        const uint32_t dj[4] = {__byte_perm(x0, y0, 0x5410), __byte_perm(x0, y0, 0x7632),
+                                __byte_perm(x1, y1, 0x5410), __byte_perm(x1, y1, 0x7632)};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half] & 0xFFFF));
+          a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half + 1] & 0xFFFF));
+          a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half] >> 16));
+          a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half + 1] >> 16));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[nt][0], pb[nt][1]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // ---- finish per-warp row sums, then merge the warps of this CTA in shared memory ----
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = l_run[nt][j];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l_run[nt][j] = v;
+    }
+  __syncthreads();  // every warp is done with its ring; reuse shared memory for the merge
+  constexpr int HN = NT * 8;
+  float* sm_o = reinterpret_cast<float*>(smem);             // [warps][HN][D]
+  float* sm_m = sm_o + Cfg::kWarps * HN * D;                 // [warps][HN]
+  float* sm_l = sm_m + Cfg::kWarps * HN;                     // [warps][HN]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    if (g8 == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        sm_m[warp * HN + nt * 8 + 2 * q4 + j] = m_run[nt][j];
+        sm_l[warp * HN + nt * 8 + 2 * q4 + j] = l_run[nt][j];
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int rho = g8 + 8 * (j >> 1);
+        int d;
+        if constexpr (!FP8) d = 16 * mt + rho;
+        else d = 32 * (mt >> 1) + 4 * (rho & 7) + 2 * (mt & 1) + (rho >> 3);
+        sm_o[(warp * HN + nt * 8 + 2 * q4 + (j & 1)) * D + d] = o[nt][mt][j];
+      }
+  }
+  __syncthreads();
+  const int64_t hq0 = static_cast<int64_t>(h) * p.group;
+  for (int idx = threadIdx.x; idx < p.group * D; idx += Cfg::kThreads) {
+    const int hl = idx / D, d = idx - hl * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < Cfg::kWarps; ++w) M = fmaxf(M, sm_m[w * HN + hl]);
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < Cfg::kWarps; ++w) {
+      const float f = exp2f(sm_m[w * HN + hl] - M);
+      acc += f * sm_o[(w * HN + hl) * D + d];
+      lsum += f * sm_l[w * HN + hl];
+    }
+    acc *= p.kv_scale;
+    if (num_splits == 1) {
+      __nv_bfloat16 b = __float2bfloat16_rn(acc / lsum);
+      p.out[static_cast<int64_t>(qrow) * p.Hq * D + (hq0 + hl) * D + d] = *reinterpret_cast<uint16_t*>(&b);
+    } else {
+      const int64_t pi = static_cast<int64_t>(item) * p.Hq + hq0 + hl;
+      p.part_o[pi * D + d] = acc;
+      if (d == 0) {
+        p.part_ml[pi * 2] = M;
+        p.part_ml[pi * 2 + 1] = lsum;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------------------------
+// log-sum-exp combine of the splits of each generation request
+// --------------------------------------------------------------------------------------------
+constexpr int kCombineWarps = 4;
+
+// One warp per (generation request, query head); lane i owns 4 consecutive head dims.
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int gr = w / p.Hq, hq = w - gr * p.Hq;
+  if (gr >= p.G) return;
+  const int first = __ldg(p.split_prefix + gr);
+  const int S = __ldg(p.split_prefix + gr + 1) - first;
+  if (S <= 1) return;  // written directly by the decode kernel
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + static_cast<int64_t>(first) * p.Hq + hq;
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[static_cast<int64_t>(s) * p.Hq].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const int D = p.D;
+  const bool active = lane < D / 4;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(first) * p.Hq + hq) * D) + lane;
+  const int64_t stride4 = static_cast<int64_t>(p.Hq) * D / 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < S; ++s) {
+    const float2 m_l = ml[static_cast<int64_t>(s) * p.Hq];
+    const float f = exp2f(m_l.x - M);
+    lsum += f * m_l.y;
+    if (active) {
+      const float4 v = po[s * stride4];
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+  }
+  if (active) {
+    const float inv = 1.f / lsum;
+    const int64_t qrow = p.gen_row0 + gr;
+    uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    *reinterpret_cast<uint2*>(p.out + qrow * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
+  }
+}
+
+template <int D, bool FP8, int NT>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
+  using Cfg = DecodeCfg<D, FP8>;
+  auto kern = decode_splitkv_kernel<D, FP8, NT>;
+  static_assert(Cfg::kSmemBytes >= Cfg::kWarps * NT * 8 * (D + 2) * 4, "merge buffer must fit");
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.total_splits, p.Hkv);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches) {
+  cudaError_t e;
+  const int nt = p.group > 8 ? 2 : 1;
+  if (p.D == 128) {
+    if (fp8) e = nt == 1 ? launch_decode_t<128, true, 1>(p, s) : launch_decode_t<128, true, 2>(p, s);
+    else e = nt == 1 ? launch_decode_t<128, false, 1>(p, s) : launch_decode_t<128, false, 2>(p, s);
+  } else {
+    if (fp8) e = nt == 1 ? launch_decode_t<64, true, 1>(p, s) : launch_decode_t<64, true, 2>(p, s);
+    else e = nt == 1 ? launch_decode_t<64, false, 1>(p, s) : launch_decode_t<64, false, 2>(p, s);
+  }
+  if (e == cudaSuccess && launches) ++*launches;
+  return e;
+}
+
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s) {
+  const int64_t warps = static_cast<int64_t>(p.G) * p.Hq;
+  combine_kernel<<<static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,95 @@
+// internal.h -- parameter blocks and launchers shared between the C-ABI front end (api.cpp)
+// and the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "paged_kv.h"
+
+namespace pkv {
+
+constexpr int kCtxTileM = 128;   // query rows per context-attention tile (tcgen05 M)
+constexpr int kCtxTileN = 128;   // keys per context-attention KV tile
+constexpr int kDecodeTile = 16;  // tokens per decode warp tile (mma.sync M)
+
+// Device-side plan written by plan_kernel into the front of the workspace (int32 words).
+struct PlanLayout {
+  int64_t cu_q;          // [R + 1]  exclusive prefix of context_lengths
+  int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxTileM) over context requests
+  int64_t split_prefix;  // [G + 1]  prefix of ceil(L_r / kv_chunk) over generation requests
+  int64_t int_words;     // total int32 words of the plan
+  int64_t part_o;        // byte offset of fp32 partial outputs [num_splits, Hq, D]
+  int64_t part_ml;       // byte offset of fp32 (m, l) pairs   [num_splits, Hq, 2]
+  int64_t total_bytes;
+};
+
+struct AppendParams {
+  int32_t R, T, Hq, Hkv, D, B, NB, max_blocks;
+  const uint16_t* q;
+  int64_t q_stride;
+  const uint16_t* k;
+  int64_t k_stride;
+  const uint16_t* v;
+  int64_t v_stride;
+  uint16_t* q_out;
+  int64_t q_out_stride;
+  const float2* rope;  // [max_pos, D/2]
+  int32_t max_pos;
+  void* pool;
+  float inv_scale;
+  const int32_t* ctx_len;
+  const int32_t* past;
+  const int32_t* tbl;
+  int32_t* d_error;
+};
+
+struct PlanParams {
+  int32_t R, C, G, T, expect_tiles, expect_splits, kv_chunk;
+  const int32_t* ctx_len;
+  const int32_t* past;
+  int32_t* ws;  // plan words
+  PlanLayout lay;
+  int32_t* d_error;
+};
+
+struct DecodeParams {
+  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, gen_row0, total_splits;
+  const uint8_t* pool;
+  float kv_scale;           // dequantisation multiplier (1 for bf16)
+  float scale_log2;         // softmax_scale * log2(e)
+  const uint16_t* q;        // rotated q rows (bf16)
+  int64_t q_stride;
+  uint16_t* out;            // [T, Hq*D] bf16
+  const int32_t* past;
+  const int32_t* tbl;
+  const int32_t* split_prefix;
+  float* part_o;
+  float* part_ml;
+  int32_t* d_error;
+};
+
+struct ContextParams {
+  int32_t C, T, Hq, Hkv, group, D, B, NB, max_blocks, num_tiles;
+  const int32_t* cu_q;
+  const int32_t* tile_prefix;
+  const int32_t* ctx_len;
+  const int32_t* past;
+  const int32_t* tbl;
+  const uint8_t* pool;      // for the device-side page checks
+  uint16_t* out;
+  int64_t out_stride;
+  float scale_log2;
+  int32_t* d_error;
+};
+
+cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches);
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s);
+// q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
+cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map,
+                           bool fp8, cudaStream_t s);
+
+}  // namespace pkv

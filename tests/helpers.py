@@ -1,0 +1,91 @@
+"""Shared test plumbing: run one batch through the CUDA library (via the C-ABI binding) and
+through the CPU oracle, on the same seeded inputs."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_rope_gb300 as pk
+from paged_kv_cache_rope_gb300 import workloads as W
+
+BF16_TOL = 1e-2       # max abs error vs the fp64 oracle, bf16 pool
+FP8_TOL = 4e-2        # max abs error vs the oracle on the unquantised (bf16) values
+FP8_DEQ_TOL = 1e-2    # max abs error vs the oracle on the dequantised FP8 pool
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    return t.numpy()
+
+
+@dataclasses.dataclass
+class GpuResult:
+    pool: torch.Tensor       # pool after the append (device)
+    q_out: torch.Tensor      # rotated q (device)
+    out: torch.Tensor        # attention output (device)
+    error: int               # device error word
+    launches: int
+
+
+def gpu_run(b: W.Batch, device: str = "cuda", attention: bool = True) -> GpuResult:
+    """Append (+ attention) through the C-ABI on a fresh copy of the batch's pool."""
+    pool = pk.KVPool(b.pool.to(device).clone(), b.kv_scale, b.inv_scale)
+    meta = pk.BatchMeta(b.request_types, b.new_len, b.past, b.block_table, device)
+    table = pk.paged_rope_table_build(b.rope_base, b.head_dim, b.max_pos, device)
+    step = pk.PagedAttentionStep(pool, meta, b.num_q_heads, b.head_dim, table)
+    q, k, v = b.q.to(device), b.k.to(device), b.v.to(device)
+    if attention:
+        out = step(q, k, v)
+    else:
+        pk.paged_kv_append_rope(pool, meta, b.num_q_heads, q, k, v, step.q_out, table, step.d_error)
+        out = step.out
+    torch.cuda.synchronize()
+    return GpuResult(pool.data, step.q_out, out, int(step.d_error.item()), step.launches)
+
+
+@dataclasses.dataclass
+class OracleResult:
+    pool: np.ndarray         # write image (bits)
+    q_out: np.ndarray        # bf16 bits [T, Hq*D]
+    out: np.ndarray          # fp64 [T, Hq, D] (NaN for rows not computed)
+    status: int
+
+
+def oracle_run(b: W.Batch, rows=None, unquantised: bool = False) -> OracleResult:
+    """O1 + O2 on the batch.  ``unquantised`` runs an FP8 batch on its bf16 twin pool."""
+    use_twin = unquantised and b.kv_dtype == "fp8"
+    pool_np = bits(b.pool_bf16 if use_twin else b.pool).copy()
+    fp8 = b.kv_dtype == "fp8" and not use_twin
+    cs = oracle.rope_table(b.rope_base, b.head_dim, b.max_pos)
+    st, q_out = oracle.append_rope(
+        new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
+        num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
+        num_blocks=b.num_blocks, kv_fp8=fp8, inv_scale=b.inv_scale, q_bits=bits(b.q),
+        k_bits=bits(b.k), v_bits=bits(b.v), cs=cs, pool=pool_np)
+    q64 = oracle.f32_from_bf16(q_out).astype(np.float64)
+    st2, out = oracle.attention(
+        new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
+        num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
+        num_blocks=b.num_blocks, kv_fp8=fp8, kv_scale=b.kv_scale if fp8 else 1.0, pool=pool_np,
+        q=q64, softmax_scale=b.softmax_scale, rows=rows)
+    return OracleResult(pool_np, q_out, out, st or st2)
+
+
+def gpu_out_f64(res: GpuResult, b: W.Batch) -> np.ndarray:
+    return res.out.float().cpu().numpy().astype(np.float64).reshape(b.num_tokens, b.num_q_heads, b.head_dim)
+
+
+def max_err(gpu: np.ndarray, ref: np.ndarray, rows=None) -> float:
+    if rows is not None:
+        gpu, ref = gpu[rows], ref[rows]
+    assert np.all(np.isfinite(ref))
+    if not np.all(np.isfinite(gpu)):
+        return float("inf")
+    return float(np.max(np.abs(gpu - ref))) if gpu.size else 0.0

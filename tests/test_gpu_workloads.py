@@ -1,0 +1,45 @@
+"""The five synthetic workloads at full size, launched exactly as bench.py launches them:
+bit-exact pool write image everywhere, and attention outputs against the fp64 oracle on every
+row (workloads 1-3) or on a deterministic row sample plus every generation row (4, 5)."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_rope_gb300 import workloads as W
+
+from helpers import BF16_TOL, FP8_DEQ_TOL, FP8_TOL, bits, gpu_out_f64, gpu_run, max_err, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_rows(b: W.Batch, stride: int, tail: int) -> np.ndarray:
+    rows, row = [], 0
+    for r in range(b.num_requests):
+        n = int(b.new_len[r])
+        if b.request_types[r] == W.REQ_CONTEXT:
+            rows += list(range(row, row + n, stride)) + list(range(max(row, row + n - tail), row + n))
+        else:
+            rows.append(row)
+        row += n
+    return np.unique(np.array(rows, dtype=np.int64))
+
+
+@pytest.mark.parametrize("idx,kv_dtype,stride", [
+    (1, "bf16", 1), (2, "bf16", 1), (3, "bf16", 1), (3, "fp8", 1), (4, "bf16", 29), (5, "bf16", 257),
+])
+def test_workload_full_size(idx, kv_dtype, stride):
+    b = W.workload(idx, kv_dtype=kv_dtype, device="cuda")
+    g = gpu_run(b)
+    assert g.error == 0
+    rows = None if stride == 1 else _sample_rows(b, stride, 16)
+    b_host = b.to("cpu")
+    o = oracle_run(b_host, rows=rows)
+    assert o.status == 0
+    assert np.array_equal(bits(g.q_out), o.q_out)
+    assert np.array_equal(bits(g.pool).reshape(-1), o.pool.reshape(-1))
+    got = gpu_out_f64(g, b)
+    if kv_dtype == "bf16":
+        assert max_err(got, o.out, rows) <= BF16_TOL
+    else:
+        assert max_err(got, o.out, rows) <= FP8_DEQ_TOL
+        assert max_err(got, oracle_run(b_host, rows=rows, unquantised=True).out, rows) <= FP8_TOL
