@@ -235,7 +235,7 @@ def run_ours(args):
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     b = W.workload(args.workload, kv_dtype=args.kv_dtype, device=str(dev), poison=False,
-                   seed=args.workload + 1000 * rank)
+                   seed=args.workload + 1000 * rank, max_gen=args.max_gen)
     work = work_of(b)
     pool = pk.KVPool(b.pool, b.kv_scale, b.inv_scale)
     meta = pk.BatchMeta(b.request_types, b.new_len, b.past, b.block_table, dev)
@@ -411,6 +411,8 @@ def main():
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-gen", type=int, default=None,
+                    help="keep only the first N generation requests (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -162,7 +162,8 @@ int choose_kv_chunk(const pkv_batch* b, int C, int Hkv) {
 
 void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
   hp->num_tiles = 0;
-  for (int r = 0; r < hp->C; ++r) hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxTileM - 1) / pkv::kCtxTileM;
+  for (int r = 0; r < hp->C; ++r)
+    hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
   hp->kv_chunk = choose_kv_chunk(b, hp->C, pool->num_kv_heads);
   hp->num_splits = 0;
   hp->max_splits = 0;
@@ -333,6 +334,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.C = hp.C;
   pp.G = hp.G;
   pp.T = hp.T;
+  pp.Hkv = Hkv;
   pp.expect_tiles = hp.num_tiles;
   pp.expect_splits = hp.num_splits;
   pp.kv_chunk = hp.kv_chunk;

@@ -10,16 +10,22 @@
 //
 // The pages' kernel keeps S and O in registers of warp-level MMA fragments.  On sm_103a the
 // contraction runs on tcgen05 with both accumulators in TMEM instead:
-//   CTA = (query head, 128-row query tile of one context request), 6 warps:
-//     warps 0-3  softmax: thread i owns row i (TMEM lane i) -- reads S from TMEM, masks,
-//                online max / sum in base 2 (O is rescaled in TMEM only when the running max
-//                grows by more than 2^8), writes P (bf16) to shared memory, final O / l;
-//     warp 4     TMA producer: Q once, then per 128-key tile the pool pages of K and V through
+//   CTA = (query head, 256 query rows of one context request) = two 128-row Q tiles A and B
+//   that share every K/V tile and take turns on the tensor core; 12 warps (3 warpgroups, with
+//   setmaxnreg moving registers from the control warpgroup to the two softmax warpgroups):
+//     warps 0-3 / 4-7  softmax of tile A / B: thread i owns row i (TMEM lane i).  It reads its
+//                S row from TMEM in one pass (128 registers), masks by select, keeps the running
+//                max / sum in base 2 (O is rescaled in TMEM only when the max grows by more than
+//                2^8), and writes P as bf16 back into the first 64 columns of its own S buffer;
+//     warp 8     TMA producer: Q once, then per 128-key tile the pool pages of K and V through
 //                the block table (one box per page and 64-wide head-dim half);
-//     warp 5     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM S buffers, then
-//                O += P_{j-1} V_{j-1}; completion is signalled with tcgen05.commit on mbarriers.
-//   TMEM: S0 | S1 | O  (128 + 128 + D columns of 128 lanes, 512 allocated).
-//   Shared memory (128-byte swizzle, K-major Q/K/P, MN-major V): Q, K[2], V[2], P[2].
+//     warp 9     TMEM owner and MMA issuer (warps 10-11 only complete the warpgroup), in the order
+//                  S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
+//                so one tile's softmax overlaps the other tile's MMAs.  PV takes P straight from
+//                TMEM (A operand in tensor memory) and V from shared memory (MN-major).
+//   TMEM columns: S_A | S_B | O_A | O_B (4 x 128 of 128 lanes).  tcgen05 work issued by one
+//   thread completes in order, so a commit after S_X(j) also covers PV_X(j-1): the softmax of
+//   tile j may rescale O_X as soon as S_X(j) has landed.
 // Rows past the request's end and keys past the causal limit are masked by select (never by
 // arithmetic on the loaded values); V rows past the sequence end are zeroed before PV, so
 // stale or poisoned pool slots cannot reach the output.  Every wait is bounded.
@@ -32,41 +38,39 @@
 namespace pkv {
 namespace {
 
-constexpr int kSoftmaxWarps = 4;
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 12 * 32;  // three warpgroups: softmax A, softmax B, producer + MMA (+2 idle)
+// Registers: 168 per thread at launch (64512 per CTA).  The softmax warpgroups take 216 each and
+// the producer / MMA warpgroup keeps 64: 2 * 128 * 216 + 128 * 64 = 63488 <= 64512.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could exceed 2^8
 
 template <int D>
 struct CtxSmem {
-  static constexpr int kHalf = 128 * 128;                    // one 64-wide half of a 128-row tile
-  static constexpr int kQ = (D / 64) * kHalf;                 // Q tile
-  static constexpr int kKV = (D / 64) * kHalf;                // one K or V stage
-  static constexpr int kP = 2 * kHalf;                        // P tile (128 keys)
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQ;
-  static constexpr int kVOff = kKOff + 2 * kKV;
-  static constexpr int kPOff = kVOff + 2 * kKV;
-  static constexpr int kBarOff = kPOff + 2 * kP;
+  static constexpr int kHalf = 128 * 128;         // one 64-wide half of a 128-row tile (bytes)
+  static constexpr int kTile = (D / 64) * kHalf;  // one Q tile or one K / V stage
+  static constexpr int kQOff = 0;                 // Q_A, Q_B
+  static constexpr int kKOff = 2 * kTile;         // K[2]
+  static constexpr int kVOff = 4 * kTile;         // V[2]
+  static constexpr int kBarOff = 6 * kTile;
   static constexpr int kBarBytes = 256;
   static constexpr int kBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
 };
 
-// barrier indices
 enum {
   BAR_Q = 0,
-  BAR_KFULL = 1,   // +2
+  BAR_KFULL = 1,   // +2 stages
   BAR_KEMPTY = 3,  // +2
   BAR_VFULL = 5,   // +2
   BAR_VEMPTY = 7,  // +2
-  BAR_SFULL = 9,   // +2
-  BAR_SFREE = 11,  // +2
-  BAR_PFULL = 13,  // +2
-  BAR_PFREE = 15,  // +2
-  BAR_MMADONE = 17,
-  NUM_BARS = 18
+  BAR_SFULL = 9,   // +2 Q tiles
+  BAR_PFULL = 11,  // +2
+  BAR_ODONE = 13,  // +2
+  BAR_MMADONE = 15,
+  NUM_BARS = 16
 };
 
 template <int D>
@@ -87,32 +91,36 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   const int hq = blockIdx.x;
   const int hk = hq / p.group;
 
-  // ---- which context request / query tile (heaviest tiles first) ----
-  const int tile = p.num_tiles - 1 - static_cast<int>(blockIdx.y);
+  // ---- which context request / pair of query tiles (heaviest first) ----
+  const int unit = p.num_tiles - 1 - static_cast<int>(blockIdx.y);
   int lo = 0, hi = p.C - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.tile_prefix + mid) <= tile) lo = mid;
+    if (__ldg(p.tile_prefix + mid) <= unit) lo = mid;
     else hi = mid - 1;
   }
   const int r = lo;
-  const int i0 = (tile - __ldg(p.tile_prefix + r)) * kCtxTileM;
+  const int i0 = (unit - __ldg(p.tile_prefix + r)) * kCtxRowsPerCta;
   const int n_r = __ldg(p.ctx_len + r);
   const int past = __ldg(p.past + r);
-  const int n_valid = min(kCtxTileM, n_r - i0);
   const int row0 = __ldg(p.cu_q + r) + i0;
   const int L_r = past + n_r;
-  if (n_valid <= 0 || tile < 0) {  // plan disagrees with the launch
+  // valid rows and KV tiles of query tiles A (0) and B (1); scalars, not arrays, so that a
+  // runtime tile index never forces them into local memory
+  const int nv0 = max(0, min(128, n_r - i0)), nv1 = max(0, min(128, n_r - i0 - 128));
+  const int nkt0 = nv0 > 0 ? (past + i0 + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
+  const int nkt1 = nv1 > 0 ? (past + i0 + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
+  if (nv0 <= 0 || unit < 0) {  // plan disagrees with the launch
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
     return;
   }
-  const int kv_len = past + i0 + n_valid;  // keys visible to the last valid row
-  const int n_kv_tiles = (kv_len + kCtxTileN - 1) / kCtxTileN;
+  const bool hasB = nv1 > 0;
+  const int nT = hasB ? nkt1 : nkt0;       // KV tiles this CTA streams
+  const int zero_x = (nkt0 == nT) ? 0 : 1;  // first user of the last V tile zeroes its tail
 
   const uint32_t sQ = base_s + L::kQOff;
-  auto sK = [&](int st) { return base_s + L::kKOff + st * L::kKV; };
-  auto sV = [&](int st) { return base_s + L::kVOff + st * L::kKV; };
-  auto sP = [&](int st) { return base_s + L::kPOff + st * L::kP; };
+  auto sK = [&](int st) { return base_s + L::kKOff + st * L::kTile; };
+  auto sV = [&](int st) { return base_s + L::kVOff + st * L::kTile; };
 
   // ---- set-up: barriers, TMEM ----
   if (threadIdx.x == 0) {
@@ -123,9 +131,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       tc::mbar_init(bar(BAR_VFULL + s), 1);
       tc::mbar_init(bar(BAR_VEMPTY + s), 1);
       tc::mbar_init(bar(BAR_SFULL + s), 1);
-      tc::mbar_init(bar(BAR_SFREE + s), kSoftmaxWarps * 32);
-      tc::mbar_init(bar(BAR_PFULL + s), kSoftmaxWarps * 32);
-      tc::mbar_init(bar(BAR_PFREE + s), 1);
+      tc::mbar_init(bar(BAR_PFULL + s), 128);
+      tc::mbar_init(bar(BAR_ODONE + s), 1);
     }
     tc::mbar_init(bar(BAR_MMADONE), 1);
     *abort_flag = 0;
@@ -143,7 +150,6 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
 
   auto fail = [&]() {
     flag_error(p.d_error, PKV_DEVERR_TIMEOUT);
@@ -156,220 +162,243 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   };
   auto warp_abort = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0) != 0; };
 
-  if (warp == kProducerWarp) {
-    // ======================= TMA producer =======================
-    if (lane == 0) {
-      const int32_t* tbl = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
-      const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
-      const int pages_per_tile = kCtxTileN / box_rows;
-      const int n_pages_seq = (L_r + p.B - 1) / p.B;
-      tc::mbar_arrive_expect_tx(bar(BAR_Q), kCtxTileM * D * 2);
-      for (int dh = 0; dh < D / 64; ++dh)
-        tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(BAR_Q), 0, dh, hq, row0);
-      int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < n_kv_tiles && !*abort_flag; ++j) {
-        const int st = j & 1;
-        // pages of this tile that exist in the sequence and have a valid id
-        int pages[kCtxTileN / 16];
-        int n_ok = 0;
-        for (int pp = 0; pp < pages_per_tile; ++pp) {
-          const int lb = (j * kCtxTileN) / p.B + pp;  // B <= 128: whole pages per tile
-          int pg = -1;
-          if (lb < n_pages_seq && lb < p.max_blocks) {
-            pg = __ldg(tbl + lb);
-            if (pg < 0 || pg >= p.NB) {
-              flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
-              pg = -1;
+  if (warp >= 8) {
+    // one setmaxnreg instruction for all four warps of the control warpgroup
+    tc::regs_dec<kRegsControl>();
+    if (warp == kProducerWarp) {
+      // ======================= TMA producer =======================
+      if (lane == 0) {
+        const int32_t* tbl = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
+        const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
+        const int pages_per_tile = kCtxTileN / box_rows;
+        const int n_pages_seq = (L_r + p.B - 1) / p.B;
+        tc::mbar_arrive_expect_tx(bar(BAR_Q), (hasB ? 2 : 1) * 128 * D * 2);
+        for (int x = 0; x < (hasB ? 2 : 1); ++x)
+          for (int dh = 0; dh < D / 64; ++dh)
+            tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(BAR_Q), 0, dh, hq, row0 + 128 * x);
+        int issued_k = 0, issued_v = 0;
+        for (int j = 0; j < nT && !*abort_flag; ++j) {
+          const int st = j & 1;
+          int pages[kCtxTileN / 16];
+          int n_ok = 0;
+          for (int pp = 0; pp < pages_per_tile; ++pp) {
+            const int lb = (j * kCtxTileN) / p.B + pp;  // B <= 128: whole pages per tile
+            int pg = -1;
+            if (lb < n_pages_seq && lb < p.max_blocks) {
+              pg = __ldg(tbl + lb);
+              if (pg < 0 || pg >= p.NB) {
+                flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+                pg = -1;
+              }
+            }
+            pages[pp] = pg;
+            n_ok += pg >= 0;
+          }
+          const uint32_t bytes = static_cast<uint32_t>(n_ok) * box_rows * D * 2;
+          if (j >= 2 && !tc::mbar_wait(bar(BAR_KEMPTY + st), ((j - 2) >> 1) & 1)) { fail(); break; }
+          tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
+          for (int pp = 0; pp < pages_per_tile; ++pp) {
+            if (pages[pp] < 0) continue;
+            for (int dh = 0; dh < D / 64; ++dh)
+              tc::tma_load_4d(sK(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_KFULL + st), 0, dh, hk,
+                              (pages[pp] * 2 + 0) * p.B);
+          }
+          ++issued_k;
+          if (j >= 2 && !tc::mbar_wait(bar(BAR_VEMPTY + st), ((j - 2) >> 1) & 1)) { fail(); break; }
+          tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
+          for (int pp = 0; pp < pages_per_tile; ++pp) {
+            if (pages[pp] < 0) continue;
+            for (int dh = 0; dh < D / 64; ++dh)
+              tc::tma_load_4d(sV(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_VFULL + st), 0, dh, hk,
+                              (pages[pp] * 2 + 1) * p.B);
+          }
+          ++issued_v;
+        }
+        if (*abort_flag) {  // let copies already in flight land before the CTA winds down
+          for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
+            tc::mbar_wait(bar(BAR_KFULL + (j & 1)), (j >> 1) & 1, 200000000LL);
+          for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
+            tc::mbar_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1, 200000000LL);
+          tc::mbar_wait(bar(BAR_Q), 0, 200000000LL);
+        }
+      }
+    } else if (warp == kMmaWarp) {
+      // ======================= MMA issuer =======================
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
+        constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
+        auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
+        auto last_user = [&](int j) { return (hasB && j < nkt1) ? 1 : 0; };
+        auto issue_s = [&](int j, int x) {
+          const int st = j & 1;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = tc::sdesc_sw128(sQ + x * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = tc::sdesc_sw128(sK(st) + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(tmem + 128 * x, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(BAR_SFULL + x));
+          if (x == last_user(j)) tc::mma_commit(bar(BAR_KEMPTY + st));
+        };
+        bool ok = tc::mbar_wait(bar(BAR_Q), 0) && tc::mbar_wait(bar(BAR_KFULL + 0), 0);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_s(0, 0);
+          if (hasB) issue_s(0, 1);
+        }
+        for (int j = 0; ok && j < nT && !*abort_flag; ++j) {
+          bool v_ready = false;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!uses(j, x)) continue;
+            if (!tc::mbar_wait(bar(BAR_PFULL + x), j & 1)) { ok = false; break; }
+            if (!v_ready) {
+              if (!tc::mbar_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+              v_ready = true;
+            }
+            tc::fence_after_sync();
+  #pragma unroll
+            for (int kk = 0; kk < kCtxTileN / 16; ++kk) {
+              const uint64_t b = tc::sdesc_sw128(sV(j & 1) + kk * 16 * 128, L::kHalf, 1024);
+              tc::mma_bf16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (x == last_user(j)) tc::mma_commit(bar(BAR_VEMPTY + (j & 1)));
+            if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
+            if (uses(j + 1, x)) {
+              if (!tc::mbar_wait(bar(BAR_KFULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) { ok = false; break; }
+              tc::fence_after_sync();
+              issue_s(j + 1, x);
             }
           }
-          pages[pp] = pg;
-          n_ok += pg >= 0;
         }
-        const uint32_t bytes = static_cast<uint32_t>(n_ok) * box_rows * D * 2;
-        if (j >= 2 && !tc::mbar_wait(bar(BAR_KEMPTY + st), ((j - 2) >> 1) & 1)) { fail(); break; }
-        tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
-        for (int pp = 0; pp < pages_per_tile; ++pp) {
-          if (pages[pp] < 0) continue;
-          const int row = (pages[pp] * 2 + 0) * p.B;
-          for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sK(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_KFULL + st), 0, dh, hk,
-                            row);
-        }
-        ++issued_k;
-        if (j >= 2 && !tc::mbar_wait(bar(BAR_VEMPTY + st), ((j - 2) >> 1) & 1)) { fail(); break; }
-        tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
-        for (int pp = 0; pp < pages_per_tile; ++pp) {
-          if (pages[pp] < 0) continue;
-          const int row = (pages[pp] * 2 + 1) * p.B;
-          for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sV(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_VFULL + st), 0, dh, hk,
-                            row);
-        }
-        ++issued_v;
+        if (!ok) fail();
+        tc::mma_commit(bar(BAR_MMADONE));
+        tc::mbar_wait(bar(BAR_MMADONE), 0, 200000000LL);  // nothing of ours still runs on TMEM
       }
-      if (*abort_flag) {  // let copies already in flight land before the CTA winds down
-        for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
-          tc::mbar_wait(bar(BAR_KFULL + (j & 1)), (j >> 1) & 1, 200000000LL);
-        for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
-          tc::mbar_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1, 200000000LL);
-        tc::mbar_wait(bar(BAR_Q), 0, 200000000LL);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
-      constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
-      auto issue_pv = [&](int jj) -> bool {
-        const int st = jj & 1;
-        if (!tc::mbar_wait(bar(BAR_PFULL + st), (jj >> 1) & 1)) return false;
-        if (!tc::mbar_wait(bar(BAR_VFULL + st), (jj >> 1) & 1)) return false;
-        tc::fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < kCtxTileN / 16; ++kk) {
-          const uint64_t a = tc::sdesc_sw128(sP(st) + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = tc::sdesc_sw128(sV(st) + kk * 16 * 128, L::kHalf, 1024);
-          tc::mma_bf16_ss(tO, a, b, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(bar(BAR_PFREE + st));
-        tc::mma_commit(bar(BAR_VEMPTY + st));
-        return true;
-      };
-      bool ok = tc::mbar_wait(bar(BAR_Q), 0);
-      for (int j = 0; ok && j < n_kv_tiles && !*abort_flag; ++j) {
-        const int st = j & 1;
-        if (!tc::mbar_wait(bar(BAR_KFULL + st), (j >> 1) & 1)) { ok = false; break; }
-        if (j >= 2 && !tc::mbar_wait(bar(BAR_SFREE + st), ((j - 2) >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = tc::sdesc_sw128(sQ + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = tc::sdesc_sw128(sK(st) + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tS0 + st * kCtxTileN, a, b, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(bar(BAR_SFULL + st));
-        tc::mma_commit(bar(BAR_KEMPTY + st));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
-      }
-      if (ok && !*abort_flag) ok = issue_pv(n_kv_tiles - 1);
-      if (!ok) fail();
-      tc::mma_commit(bar(BAR_MMADONE));
-      tc::mbar_wait(bar(BAR_MMADONE), 0, 200000000LL);  // nothing of ours still runs on TMEM
     }
   } else {
-    // ======================= softmax warps =======================
-    const int row = warp * 32 + lane;                   // tile row == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int q_pos = past + i0 + min(row, n_valid - 1);  // padding rows mirror the last row
+    // ======================= softmax warpgroups =======================
+    tc::regs_inc<kRegsSoftmax>();
+    const int x = warp >> 2;                 // Q tile A (0) or B (1)
+    const int row = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 128 * x + lane_off;
+    const uint32_t tO = tmem + 256 + 128 * x + lane_off;
+    const int nvx = x ? nv1 : nv0, nk = x ? nkt1 : nkt0;
+    const int q_pos = past + i0 + 128 * x + min(row, max(nvx, 1) - 1);  // padding rows mirror the last row
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv_tiles; ++j) {
-      const int st = j & 1;
-      if (warp_abort() || !warp_wait(bar(BAR_SFULL + st), (j >> 1) & 1)) { ok = false; break; }
+    for (int j = 0; j < nk; ++j) {
+      if (warp_abort() || !warp_wait(bar(BAR_SFULL + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      const uint32_t tS = tS0 + st * kCtxTileN + lane_off;
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      tc::tmem_ld32_async(tS + 0, v0);
+      tc::tmem_ld32_async(tS + 32, v1);
+      tc::tmem_ld32_async(tS + 64, v2);
+      tc::tmem_ld32_async(tS + 96, v3);
+      tc::tmem_wait_ld_dep(v0);
+      tc::reg_dep(v1);
+      tc::reg_dep(v2);
+      tc::reg_dep(v3);
       const int lim = q_pos - j * kCtxTileN;  // key column c is visible iff c <= lim
-      // pass 1: row max of the visible, scaled scores
-      float mx = -INFINITY;
-#pragma unroll
-      for (int cc = 0; cc < kCtxTileN / 32; ++cc) {
-        uint32_t v[32];
-        tc::tmem_ld32(tS + cc * 32, v);
+      if (__any_sync(0xffffffffu, lim < kCtxTileN - 1)) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float s = __uint_as_float(v[e]) * sl2;
-          mx = (cc * 32 + e <= lim) ? fmaxf(mx, s) : mx;
+          v0[e] = e <= lim ? v0[e] : __float_as_uint(-INFINITY);
+          v1[e] = 32 + e <= lim ? v1[e] : __float_as_uint(-INFINITY);
+          v2[e] = 64 + e <= lim ? v2[e] : __float_as_uint(-INFINITY);
+          v3[e] = 96 + e <= lim ? v3[e] : __float_as_uint(-INFINITY);
         }
       }
-      const float m_new = fmaxf(m_run, mx);
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        mx[0] = fmaxf(mx[0], __uint_as_float(v0[e]));
+        mx[1] = fmaxf(mx[1], __uint_as_float(v1[e]));
+        mx[2] = fmaxf(mx[2], __uint_as_float(v2[e]));
+        mx[3] = fmaxf(mx[3], __uint_as_float(v3[e]));
+      }
+      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
       float m_use = m_run;
       if (j == 0) {
-        m_use = m_new;  // first tile: O is still empty
+        m_use = m_new;  // O is still empty
       } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
-        // the whole warp rescales (lanes below the threshold too, each to its own new max);
-        // O must hold every earlier P V before it is rescaled
-        if (!warp_wait(bar(BAR_PFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
+        // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
         const float f = exp2f(m_run - m_new);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t v[32];
-          tc::tmem_ld32(tO + lane_off + cc * 32, v);
+          uint32_t o[32];
+          tc::tmem_ld32(tO + cc * 32, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-          tc::tmem_st32(tO + lane_off + cc * 32, v);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+          tc::tmem_st32(tO + cc * 32, o);
         }
-        tc::tmem_wait_st();
         l_run *= f;
         m_use = m_new;
       }
       m_run = m_use;
-      // P buffer `st` is free once P_{j-2} V_{j-2} has completed
-      if (j >= 2 && !warp_wait(bar(BAR_PFREE + st), ((j - 2) >> 1) & 1)) { ok = false; break; }
-      // pass 2: P = exp2(s - m) for visible keys, 0 otherwise; bf16 into the swizzled P tile
-      uint8_t* prow = base + (sP(st) - base_s) + row * 128;
-#pragma unroll
-      for (int cc = 0; cc < kCtxTileN / 32; ++cc) {
-        uint32_t v[32];
-        tc::tmem_ld32(tS + cc * 32, v);
+      // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      auto emit = [&](uint32_t(&v)[32], int c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int c = cc * 32 + e;
-          const float p0 = (c <= lim) ? exp2f(__uint_as_float(v[e]) * sl2 - m_use) : 0.f;
-          const float p1 = (c + 1 <= lim) ? exp2f(__uint_as_float(v[e + 1]) * sl2 - m_use) : 0.f;
-          l_run += p0 + p1;
+          const float p0 = exp2f(fmaf(__uint_as_float(v[e]), sl2, -m_use));
+          const float p1 = exp2f(fmaf(__uint_as_float(v[e + 1]), sl2, -m_use));
+          ls[c] += p0 + p1;
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
-        // 32 keys = 4 chunks of 16 bytes in key-half (cc >> 1), chunks (cc & 1) * 4 .. +3
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = (cc & 1) * 4 + k;
-          uint4* dst = reinterpret_cast<uint4*>(prow + (cc >> 1) * L::kHalf + ((chunk ^ (row & 7)) << 4));
-          *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
-      }
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar(BAR_SFREE + st));
-      if (j == n_kv_tiles - 1) {
-        // zero V rows past the end of the sequence (stale or unloaded slots)
-        if (!warp_wait(bar(BAR_VFULL + st), (j >> 1) & 1)) { ok = false; break; }
+        tc::tmem_st16(tS + 16 * c, pk);
+      };
+      emit(v0, 0);
+      emit(v1, 1);
+      emit(v2, 2);
+      emit(v3, 3);
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tc::tmem_wait_st();
+      if (j == nT - 1 && x == zero_x) {
+        // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
+        if (!warp_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
         if (j * kCtxTileN + row >= L_r) {
-          uint8_t* vrow = base + (sV(st) - base_s) + row * 128;
+          uint8_t* vrow = base + (sV(j & 1) - base_s) + row * 128;
 #pragma unroll
           for (int dh = 0; dh < D / 64; ++dh)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               reinterpret_cast<uint4*>(vrow + dh * L::kHalf)[k] = make_uint4(0u, 0u, 0u, 0u);
         }
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(bar(BAR_PFULL + st));
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar(BAR_PFULL + x));
     }
     if (!ok) fail();
     // ---- epilogue: O / l -> bf16 rows ----
-    const int jl = n_kv_tiles - 1;
-    if (ok && !warp_abort() && warp_wait(bar(BAR_PFREE + (jl & 1)), (jl >> 1) & 1)) {
-      tc::fence_after_sync();
-      const float inv_l = 1.f / l_run;
-      uint16_t* orow = p.out + static_cast<int64_t>(row0 + row) * p.out_stride + static_cast<int64_t>(hq) * D;
+    if (nk > 0) {
+      if (ok && !warp_abort() && warp_wait(bar(BAR_ODONE + x), 0)) {
+        tc::fence_after_sync();
+        const float inv_l = 1.f / l_run;
+        const int grow = row0 + 128 * x + row;
+        uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(hq) * D;
+        const bool store = row < nvx && grow < p.T;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t v[32];
-        tc::tmem_ld32(tO + lane_off + cc * 32, v);
-        if (row < n_valid && row0 + row < p.T) {
-          uint32_t pk[16];
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t v[32];
+          tc::tmem_ld32(tO + cc * 32, v);
+          if (store) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+            for (int e = 0; e < 32; e += 2)
+              pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            reinterpret_cast<uint4*>(orow + cc * 32)[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            for (int k = 0; k < 4; ++k)
+              reinterpret_cast<uint4*>(orow + cc * 32)[k] =
+                  make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
         }
+      } else if (ok) {
+        fail();
       }
-    } else if (ok) {
-      fail();
     }
   }
 

@@ -16,7 +16,9 @@
 //   * each KV head is read once for its whole GQA query group: S^T = K Q^T and
 //     O^T += V^T P^T run on mma.sync m16n8k16 with the group (up to 8 heads per n-tile) on N;
 //   * online softmax in base 2 with warp-shuffle column maxima; warps merge in shared memory;
-//   * splits of one request are merged by combine_kernel with a log-sum-exp rescale.
+//   * the splits of one request are merged by combine_kernel with a log-sum-exp rescale (a
+//     separate launch: merging inside the decode kernel's last CTA per pair was measured slower,
+//     since those merges hold SM slots that would otherwise stream KV).
 // FP8 pools: codes convert exactly to f16 (cvt e4m3x2 -> f16x2); Q is scaled by a power of two
 // into f16 range, and the per-pool scale is applied to scores and outputs in fp32.
 #include <math.h>
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       const int n = __ldg(p.ctx_len + r);
       x.x = n;
       if (r < C) {
-        x.y = (n + kCtxTileM - 1) / kCtxTileM;
+        x.y = (n + kCtxRowsPerCta - 1) / kCtxRowsPerCta;
       } else {
         x.z = (__ldg(p.past + r) + 1 + chunk - 1) / chunk;
         bad |= n != 1;
@@ -119,7 +121,7 @@ struct DecodeCfg {
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one of K or V
-  static constexpr int kStages = FP8 ? 6 : 3;
+  static constexpr int kStages = FP8 ? 4 : 3;  // 64 / 96 KB per CTA: 3 / 2 CTAs per SM
   static constexpr int kWarpBytes = kStages * 2 * kTileBytes;
   static constexpr int kSmemBytes = kWarps * kWarpBytes;
 };
@@ -464,11 +466,11 @@ decode_splitkv_kernel(DecodeParams p) {
 }
 
 // --------------------------------------------------------------------------------------------
-// log-sum-exp combine of the splits of each generation request
+// log-sum-exp merge of the splits: one warp per (generation request, query head), lane i owns
+// 4 consecutive head dims; splits are streamed with an online max so one pass suffices
 // --------------------------------------------------------------------------------------------
 constexpr int kCombineWarps = 4;
 
-// One warp per (generation request, query head); lane i owns 4 consecutive head dims.
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParams p) {
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
@@ -477,29 +479,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
   const int first = __ldg(p.split_prefix + gr);
   const int S = __ldg(p.split_prefix + gr + 1) - first;
   if (S <= 1) return;  // written directly by the decode kernel
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + static_cast<int64_t>(first) * p.Hq + hq;
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[static_cast<int64_t>(s) * p.Hq].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const int D = p.D;
   const bool active = lane < D / 4;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + static_cast<int64_t>(first) * p.Hq + hq;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(first) * p.Hq + hq) * D) + lane;
   const int64_t stride4 = static_cast<int64_t>(p.Hq) * D / 4;
+  float M = -INFINITY, lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int s = 0; s < S; ++s) {
     const float2 m_l = ml[static_cast<int64_t>(s) * p.Hq];
-    const float f = exp2f(m_l.x - M);
-    lsum += f * m_l.y;
-    if (active) {
-      const float4 v = po[s * stride4];
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
-    }
+    const float4 v = active ? po[s * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float Mn = fmaxf(M, m_l.x);
+    const float a = exp2f(M - Mn), b = exp2f(m_l.x - Mn);
+    acc.x = acc.x * a + v.x * b;
+    acc.y = acc.y * a + v.y * b;
+    acc.z = acc.z * a + v.z * b;
+    acc.w = acc.w * a + v.w * b;
+    lsum = lsum * a + m_l.y * b;
+    M = Mn;
   }
   if (active) {
     const float inv = 1.f / lsum;
@@ -528,6 +526,12 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s) {
+  const int64_t warps = static_cast<int64_t>(p.G) * p.Hq;
+  combine_kernel<<<static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches) {
   cudaError_t e;
   const int nt = p.group > 8 ? 2 : 1;
@@ -540,12 +544,6 @@ cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* 
   }
   if (e == cudaSuccess && launches) ++*launches;
   return e;
-}
-
-cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s) {
-  const int64_t warps = static_cast<int64_t>(p.G) * p.Hq;
-  combine_kernel<<<static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace pkv

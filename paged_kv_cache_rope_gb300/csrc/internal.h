@@ -11,13 +11,14 @@
 namespace pkv {
 
 constexpr int kCtxTileM = 128;   // query rows per context-attention tile (tcgen05 M)
+constexpr int kCtxRowsPerCta = 256;  // a context CTA owns two query tiles
 constexpr int kCtxTileN = 128;   // keys per context-attention KV tile
 constexpr int kDecodeTile = 16;  // tokens per decode warp tile (mma.sync M)
 
 // Device-side plan written by plan_kernel into the front of the workspace (int32 words).
 struct PlanLayout {
   int64_t cu_q;          // [R + 1]  exclusive prefix of context_lengths
-  int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxTileM) over context requests
+  int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxRowsPerCta) over context requests
   int64_t split_prefix;  // [G + 1]  prefix of ceil(L_r / kv_chunk) over generation requests
   int64_t int_words;     // total int32 words of the plan
   int64_t part_o;        // byte offset of fp32 partial outputs [num_splits, Hq, D]
@@ -46,7 +47,7 @@ struct AppendParams {
 };
 
 struct PlanParams {
-  int32_t R, C, G, T, expect_tiles, expect_splits, kv_chunk;
+  int32_t R, C, G, T, Hkv, expect_tiles, expect_splits, kv_chunk;
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words

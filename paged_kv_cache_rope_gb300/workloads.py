@@ -179,33 +179,40 @@ WORKLOADS = {
 
 
 def workload(idx: int, *, kv_dtype: str = "bf16", device: str = "cpu", poison: bool = True,
-             seed: int | None = None) -> Batch:
-    """The five synthetic workloads (seed = workload index unless given)."""
+             seed: int | None = None, max_gen: int | None = None) -> Batch:
+    """The five synthetic workloads (seed = workload index unless given).  ``max_gen`` keeps
+    only the first generation requests (smaller captures for profiling)."""
     seed = idx if seed is None else seed
     rng = np.random.default_rng(1000 + seed)
+
+    def _mk(**kw):
+        if max_gen is not None:
+            kw["gen"] = list(kw["gen"])[:max_gen]
+        return make_batch(**kw)
+
     if idx == 1:  # 1 context (37 new, 0 cached) + 1 decode (53 cached + 1 new); 16-page pool
-        return make_batch(name=WORKLOADS[1], ctx=[(37, 0)], gen=[54], num_q_heads=4,
+        return _mk(name=WORKLOADS[1], ctx=[(37, 0)], gen=[54], num_q_heads=4,
                           num_kv_heads=2, head_dim=64, tokens_per_block=16, kv_dtype=kv_dtype,
                           rope_base=1e4, seed=seed, device=device, poison=poison, num_blocks=16)
     if idx == 2:  # 64 decodes, MHA 32/32, L ~ U[512, 4096], block 64
         gen = rng.integers(512, 4096, size=64, endpoint=True).tolist()
-        return make_batch(name=WORKLOADS[2], ctx=[], gen=gen, num_q_heads=32, num_kv_heads=32,
+        return _mk(name=WORKLOADS[2], ctx=[], gen=gen, num_q_heads=32, num_kv_heads=32,
                           head_dim=128, tokens_per_block=64, kv_dtype=kv_dtype, seed=seed,
                           device=device, poison=poison)
     if idx == 3:  # 256 decodes, GQA 64/8, L log-uniform 128..8192, block 32
         gen = np.clip(_log_uniform_int(rng, 128, 8192, 256), 128, 8192).tolist()
-        return make_batch(name=WORKLOADS[3], ctx=[], gen=gen, num_q_heads=64, num_kv_heads=8,
+        return _mk(name=WORKLOADS[3], ctx=[], gen=gen, num_q_heads=64, num_kv_heads=8,
                           head_dim=128, tokens_per_block=32, kv_dtype=kv_dtype, seed=seed,
                           device=device, poison=poison)
     if idx == 4:  # 4 chunked contexts (1024 new, 0..3072 cached, multiple of 64) + 128 decodes
         ctx = [(1024, int(64 * rng.integers(0, 48, endpoint=True))) for _ in range(4)]
         gen = rng.integers(256, 4096, size=128, endpoint=True).tolist()
-        return make_batch(name=WORKLOADS[4], ctx=ctx, gen=gen, num_q_heads=32, num_kv_heads=8,
+        return _mk(name=WORKLOADS[4], ctx=ctx, gen=gen, num_q_heads=32, num_kv_heads=8,
                           head_dim=128, tokens_per_block=64, kv_dtype=kv_dtype, seed=seed,
                           device=device, poison=poison)
     if idx == 5:  # 16384-token prefill + 8 decodes with L ~ U[32768, 131072], RoPE base 5e5
         gen = rng.integers(32768, 131072, size=8, endpoint=True).tolist()
-        return make_batch(name=WORKLOADS[5], ctx=[(16384, 0)], gen=gen, num_q_heads=32,
+        return _mk(name=WORKLOADS[5], ctx=[(16384, 0)], gen=gen, num_q_heads=32,
                           num_kv_heads=8, head_dim=128, tokens_per_block=64, kv_dtype=kv_dtype,
                           rope_base=5e5, seed=seed, device=device, poison=poison)
     raise ValueError(f"unknown workload {idx}")
