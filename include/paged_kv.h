@@ -176,6 +176,26 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
                             float softmax_scale, void* workspace, size_t workspace_bytes,
                             int32_t* d_error, pkv_stream_t stream);
 
+/*
+ * paged_attention_forward without a caller workspace.  The pages have no counterpart: this is
+ * an addition for callers that cannot allocate device memory where they call attention (a
+ * plugin whose host framework owns all device memory and offers no workspace hook, or a
+ * latency-critical loop that forbids allocator calls).  Same arguments and results as
+ * paged_attention_forward minus the workspace; the scratch comes from one file-scope device
+ * buffer of PKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until exit.
+ *   - A batch needing more scratch than that (paged_attention_workspace_size) returns
+ *     PKV_ERR_WORKSPACE and launches nothing.  The call allocates nothing itself.
+ *   - The first call on each device looks the buffer's device address up (cudaGetSymbolAddress
+ *     with that device current) and caches it; make that first call before any stream capture.
+ *   - All calls share the buffer and leave their data in it; nothing in it has to start at zero,
+ *     but calls whose kernels overlap on the GPU (several streams or threads) race on it, so
+ *     serialise them on one stream.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (64u << 20)
+int paged_attention_forward_noalloc(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
+                                    const void* q_rot, int64_t q_row_stride, void* out, float softmax_scale,
+                                    int32_t* d_error, pkv_stream_t stream);
+
 /* Number of kernels the last successful call of either entry point on this thread enqueued. */
 int32_t paged_kv_last_launch_count(void);
 

@@ -41,6 +41,7 @@ EXPORTS = (
     "paged_kv_append_rope",
     "paged_attention_workspace_size",
     "paged_attention_forward",
+    "paged_attention_forward_noalloc",
     "paged_kv_last_launch_count",
     "paged_kv_last_launch_name",
     "paged_kv_set_kernel_events",
@@ -89,6 +90,8 @@ def lib() -> C.CDLL:
         L.paged_attention_workspace_size.restype = sz
         L.paged_attention_forward.argtypes = [P, P, i32, P, i64, P, C.c_float, P, sz, P, P]
         L.paged_attention_forward.restype = C.c_int
+        L.paged_attention_forward_noalloc.argtypes = [P, P, i32, P, i64, P, C.c_float, P, P]
+        L.paged_attention_forward_noalloc.restype = C.c_int
         L.paged_kv_last_launch_count.argtypes = []
         L.paged_kv_last_launch_count.restype = i32
         L.paged_kv_last_launch_name.argtypes = [i32]
@@ -218,6 +221,24 @@ def paged_attention_forward(pool: KVPool, batch: BatchMeta, num_q_heads: int, q_
         float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(d_error), _stream_ptr(stream))
     _check(code, "paged_attention_forward")
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def paged_attention_forward_noalloc(pool: KVPool, batch: BatchMeta, num_q_heads: int,
+                                    q_rot: torch.Tensor, out: torch.Tensor, softmax_scale: float,
+                                    d_error: torch.Tensor, stream=None) -> None:
+    """paged_attention_forward on the library's own static scratch buffer, for callers that
+    cannot allocate a workspace (see include/paged_kv.h).  Batches needing more than
+    NOALLOC_SCRATCH_BYTES of scratch raise; concurrent calls on different streams race."""
+    assert q_rot.dtype == torch.bfloat16 and q_rot.stride(1) == 1
+    assert out.dtype == torch.bfloat16 and out.is_contiguous()
+    pc, bc = pool.c(), batch.c()
+    code = lib().paged_attention_forward_noalloc(
+        C.byref(pc), C.byref(bc), int(num_q_heads), _ptr(q_rot), q_rot.stride(0), _ptr(out),
+        float(softmax_scale), _ptr(d_error), _stream_ptr(stream))
+    _check(code, "paged_attention_forward_noalloc")
 
 
 def last_launch_count() -> int:

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpaged_kv.so")
-SOURCES = ["api.cpp", "append_rope.cu", "decode_attn.cu", "context_attn.cu"]
+SOURCES = ["api.cpp", "append_rope.cu", "decode_attn.cu", "context_attn.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "internal.h", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
