@@ -148,8 +148,9 @@ int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t n
 
 /*
  * Workspace bytes paged_attention_forward needs for this pool geometry, batch and head count
- * (device plan + fp32 split-KV partials; [NOTES] 五 5.1: the runtime checks that the scratch
- * workspace is large enough).  0 on invalid arguments.
+ * ([NOTES] 五 5.1: the runtime checks that the scratch workspace is large enough): the device
+ * plan, fp32 split-KV partials, and for FP8 pools with context requests a bf16 staging copy of
+ * those requests' pages.  0 on invalid arguments.
  */
 size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* batch,
                                       int32_t num_q_heads);
@@ -168,8 +169,9 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  *   workspace    device, at least paged_attention_workspace_size bytes, 256-byte aligned;
  *                its contents need not be initialised and are scratch after the call
  *   d_error      device int32 error bits as above
- * Context rows use a tcgen05/TMEM tensor-core kernel, generation rows a split-KV decode kernel
- * plus a log-sum-exp combine; all launches go to `stream`.  T == 0 is a no-op.
+ * Context rows use a tcgen05/TMEM tensor-core kernel (for FP8 pools after staging the context
+ * requests' pages as exact bf16 code values in the workspace), generation rows a split-KV decode
+ * kernel plus a log-sum-exp combine; all launches go to `stream`.  T == 0 is a no-op.
  */
 int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
                             const void* q_rot, int64_t q_row_stride, void* out,
@@ -200,7 +202,7 @@ int paged_attention_forward_noalloc(const pkv_pool* pool, const pkv_batch* batch
 int32_t paged_kv_last_launch_count(void);
 
 /* Name of the i-th kernel the last call on this thread enqueued ("append_rope", "plan",
- * "context_attn", "decode_splitkv", "combine"), or NULL when i is out of range. */
+ * "stage_fp8", "context_attn", "decode_splitkv", "combine"), or NULL when i is out of range. */
 const char* paged_kv_last_launch_name(int32_t i);
 
 /*

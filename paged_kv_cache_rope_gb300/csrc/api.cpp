@@ -161,6 +161,7 @@ int choose_kv_chunk(const pkv_batch* b, int C, int Hkv) {
 }
 
 void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
+  const bool staging = pool->dtype == PKV_FP8_E4M3 && hp->C > 0;
   hp->num_tiles = 0;
   for (int r = 0; r < hp->C; ++r)
     hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
@@ -176,12 +177,20 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   L.cu_q = 0;
   L.tile_prefix = L.cu_q + hp->R + 1;
   L.split_prefix = L.tile_prefix + hp->C + 1;
-  L.int_words = L.split_prefix + hp->G + 1;
+  L.stage_prefix = L.split_prefix + hp->G + 1;
+  L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
+  L.int_words = L.stage_tbl + (staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
+  L.stage_pages = 0;
+  if (staging)
+    for (int r = 0; r < hp->C; ++r)
+      L.stage_pages += (b->h_past_kv_lengths[r] + b->h_context_lengths[r] + pool->tokens_per_block - 1) /
+                       pool->tokens_per_block;
   const int64_t int_bytes = (L.int_words * 4 + 255) / 256 * 256;
   const int64_t D = pool->head_dim;
   L.part_o = int_bytes;
   L.part_ml = L.part_o + (static_cast<int64_t>(hp->num_splits) * Hq * D * 4 + 255) / 256 * 256;
-  L.total_bytes = L.part_ml + (static_cast<int64_t>(hp->num_splits) * Hq * 2 * 4 + 255) / 256 * 256;
+  L.stage_pool = L.part_ml + (static_cast<int64_t>(hp->num_splits) * Hq * 2 * 4 + 255) / 256 * 256;
+  L.total_bytes = L.stage_pool + (L.stage_pages * 2 * pool->tokens_per_block * pool->num_kv_heads * D * 2 + 255) / 256 * 256;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
@@ -321,7 +330,6 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   if (q_row_stride < static_cast<int64_t>(num_q_heads) * D) return PKV_ERR_INVALID_ARGUMENT;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARGUMENT;
   const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-  if (fp8 && hp.C > 0) return PKV_ERR_UNSUPPORTED;  // context kernel reads bf16 pools only
   plan_attention(pool, batch, num_q_heads, &hp);
   if (!workspace || workspace_bytes < static_cast<size_t>(hp.lay.total_bytes)) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGNMENT;
@@ -335,6 +343,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.G = hp.G;
   pp.T = hp.T;
   pp.Hkv = Hkv;
+  pp.B = pool->tokens_per_block;
+  pp.expect_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
   pp.expect_tiles = hp.num_tiles;
   pp.expect_splits = hp.num_splits;
   pp.kv_chunk = hp.kv_chunk;
@@ -354,10 +364,41 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   ++launches;
 
   if (hp.C > 0) {
+    // FP8 pools: stage the context requests' pages as bf16 first (exact values, own table)
+    const void* ctx_pool = pool->pool;
+    const int32_t* ctx_tbl = batch->d_block_offsets;
+    int64_t ctx_blocks = pool->num_blocks;
+    if (fp8) {
+      pkv::StageParams sp{};
+      sp.C = hp.C;
+      sp.B = pool->tokens_per_block;
+      sp.Hkv = Hkv;
+      sp.D = D;
+      sp.NB = pool->num_blocks;
+      sp.max_blocks = batch->max_blocks_per_seq;
+      sp.total_pages = static_cast<int32_t>(hp.lay.stage_pages);
+      sp.ctx_len = batch->d_context_lengths;
+      sp.past = batch->d_past_kv_lengths;
+      sp.tbl = batch->d_block_offsets;
+      sp.stage_prefix = ws + hp.lay.stage_prefix;
+      sp.stage_tbl = ws + hp.lay.stage_tbl;
+      sp.pool = static_cast<const uint8_t*>(pool->pool);
+      sp.stage_pool = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + hp.lay.stage_pool);
+      sp.d_error = d_error;
+      {
+        LaunchScope ls(launches, "stage_fp8", s);
+        e = pkv::launch_stage_fp8(sp, s);
+      }
+      if (e != cudaSuccess) return PKV_ERR_CUDA;
+      ++launches;
+      ctx_pool = sp.stage_pool;
+      ctx_tbl = sp.stage_tbl;
+      ctx_blocks = hp.lay.stage_pages;
+    }
     CUtensorMap qmap, kvmap;
     if (!encode_rows_map(&qmap, q_rot, D, num_q_heads, hp.T, q_row_stride * 2, pkv::kCtxTileM)) return PKV_ERR_CUDA;
-    const int64_t pool_rows = static_cast<int64_t>(pool->num_blocks) * 2 * pool->tokens_per_block;
-    if (!encode_rows_map(&kvmap, pool->pool, D, Hkv, pool_rows, static_cast<int64_t>(Hkv) * D * 2,
+    const int64_t pool_rows = ctx_blocks * 2 * pool->tokens_per_block;
+    if (!encode_rows_map(&kvmap, ctx_pool, D, Hkv, pool_rows, static_cast<int64_t>(Hkv) * D * 2,
                          std::min(pool->tokens_per_block, pkv::kCtxTileN)))
       return PKV_ERR_CUDA;
     pkv::ContextParams cp{};
@@ -368,22 +409,23 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.group = num_q_heads / Hkv;
     cp.D = D;
     cp.B = pool->tokens_per_block;
-    cp.NB = pool->num_blocks;
+    cp.NB = static_cast<int32_t>(ctx_blocks);
     cp.max_blocks = batch->max_blocks_per_seq;
     cp.num_tiles = hp.num_tiles;
     cp.cu_q = ws + hp.lay.cu_q;
     cp.tile_prefix = ws + hp.lay.tile_prefix;
     cp.ctx_len = batch->d_context_lengths;
     cp.past = batch->d_past_kv_lengths;
-    cp.tbl = batch->d_block_offsets;
-    cp.pool = static_cast<const uint8_t*>(pool->pool);
+    cp.tbl = ctx_tbl;
+    cp.pool = static_cast<const uint8_t*>(ctx_pool);
     cp.out = static_cast<uint16_t*>(out);
     cp.out_stride = static_cast<int64_t>(num_q_heads) * D;
-    cp.scale_log2 = scale_log2;
+    cp.scale_log2 = fp8 ? scale_log2 * pool->kv_scale_quant_orig : scale_log2;
+    cp.out_scale = fp8 ? pool->kv_scale_quant_orig : 1.0f;
     cp.d_error = d_error;
     {
       LaunchScope ls(launches, "context_attn", s);
-      e = pkv::launch_context(cp, &qmap, &kvmap, fp8, s);
+      e = pkv::launch_context(cp, &qmap, &kvmap, false, s);
     }
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     ++launches;

@@ -26,6 +26,9 @@
 //   TMEM columns: S_A | S_B | O_A | O_B (4 x 128 of 128 lanes).  tcgen05 work issued by one
 //   thread completes in order, so a commit after S_X(j) also covers PV_X(j-1): the softmax of
 //   tile j may rescale O_X as soon as S_X(j) has landed.
+// FP8 pools: stage_fp8_kernel first copies the context requests' pages into a bf16 staging pool
+// (exact code values) with its own block table; this kernel then runs unchanged on it, with the
+// pool scale folded into the score scale and into the output scale.
 // Rows past the request's end and keys past the causal limit are masked by select (never by
 // arithmetic on the loaded values); V rows past the sequence end are zeroed before PV, so
 // stale or poisoned pool slots cannot reach the output.  Every wait is bounded.
@@ -377,7 +380,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     if (nk > 0) {
       if (ok && !warp_abort() && warp_wait(bar(BAR_ODONE + x), 0)) {
         tc::fence_after_sync();
-        const float inv_l = 1.f / l_run;
+        const float inv_l = p.out_scale / l_run;
         const int grow = row0 + 128 * x + row;
         uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(hq) * D;
         const bool store = row < nvx && grow < p.T;
@@ -411,7 +414,56 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   }
 }
 
+// ---- FP8 pools: stage the context requests' pages as bf16 (exact code values) ----
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads) stage_fp8_kernel(const StageParams p) {
+  const int gp = blockIdx.x;  // staging page
+  int lo = 0, hi = p.C - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.stage_prefix + mid) <= gp) lo = mid;
+    else hi = mid - 1;
+  }
+  const int r = lo, lb = gp - __ldg(p.stage_prefix + r);
+  const int n_pages = (__ldg(p.past + r) + __ldg(p.ctx_len + r) + p.B - 1) / p.B;
+  if (lb < 0 || lb >= n_pages || lb >= p.max_blocks) {  // plan disagrees with the launch
+    if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+    return;
+  }
+  int page = __ldg(p.tbl + static_cast<int64_t>(r) * p.max_blocks + lb);
+  const bool ok = page >= 0 && page < p.NB;
+  if (threadIdx.x == 0) {
+    p.stage_tbl[static_cast<int64_t>(r) * p.max_blocks + lb] = gp;
+    if (!ok) flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+  }
+  const int64_t page_elems = static_cast<int64_t>(2) * p.B * p.Hkv * p.D;  // K and V of one page
+  const uint4* src = reinterpret_cast<const uint4*>(p.pool + (ok ? page : 0) * page_elems);
+  uint4* dst = reinterpret_cast<uint4*>(p.stage_pool + gp * page_elems);
+  for (int64_t i = threadIdx.x; i < page_elems / 16; i += kStageThreads) {
+    uint4 c = ok ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> (16 * h)));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        o[2 * k + h] = pack_bf16x2(f.x, f.y);  // exact: every E4M3 value is a bf16 value
+      }
+    }
+    dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s) {
+  stage_fp8_kernel<<<p.total_pages, kStageThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, bool fp8,
                            cudaStream_t s) {

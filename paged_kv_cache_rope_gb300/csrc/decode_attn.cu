@@ -33,80 +33,84 @@ namespace {
 // --------------------------------------------------------------------------------------------
 constexpr int kPlanThreads = 256;
 
-// One pass over the requests: exclusive prefix sums of (new tokens, context query tiles,
-// generation splits) at once, so the whole plan costs a single sweep of block-wide scans.
+// One pass over the requests: exclusive prefix sums of (new tokens, context units of
+// kCtxRowsPerCta rows, generation splits, staged FP8 context pages) at once, so the whole plan
+// costs a single sweep of block-wide scans.
+__device__ __forceinline__ int4 shfl_up4(int4 v, int o) {
+  return make_int4(__shfl_up_sync(0xffffffffu, v.x, o), __shfl_up_sync(0xffffffffu, v.y, o),
+                   __shfl_up_sync(0xffffffffu, v.z, o), __shfl_up_sync(0xffffffffu, v.w, o));
+}
+__device__ __forceinline__ int4 add4(int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ int4 sub4(int4 a, int4 b) { return make_int4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
-  __shared__ int3 s_warp[kPlanThreads / 32];
-  __shared__ int3 s_carry;
+  __shared__ int4 s_warp[kPlanThreads / 32];
+  __shared__ int4 s_carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int32_t* cu = p.ws + p.lay.cu_q;
   int32_t* tiles = p.ws + p.lay.tile_prefix;
   int32_t* splits = p.ws + p.lay.split_prefix;
+  int32_t* stage = p.ws + p.lay.stage_prefix;
+  const bool staging = p.expect_stage_pages > 0;
   const int C = p.C, chunk = p.kv_chunk;
   bool bad = false;
-  if (tid == 0) s_carry = make_int3(0, 0, 0);
+  if (tid == 0) s_carry = make_int4(0, 0, 0, 0);
   __syncthreads();
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + tid;
-    int3 x = make_int3(0, 0, 0);
+    int4 x = make_int4(0, 0, 0, 0);
     if (r < p.R) {
       const int n = __ldg(p.ctx_len + r);
       x.x = n;
       if (r < C) {
         x.y = (n + kCtxRowsPerCta - 1) / kCtxRowsPerCta;
+        if (staging) x.w = (__ldg(p.past + r) + n + p.B - 1) / p.B;
       } else {
         x.z = (__ldg(p.past + r) + 1 + chunk - 1) / chunk;
         bad |= n != 1;
       }
     }
-    int3 incl = x;
+    int4 incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, incl.x, o);
-      const int b = __shfl_up_sync(0xffffffffu, incl.y, o);
-      const int c = __shfl_up_sync(0xffffffffu, incl.z, o);
-      if (lane >= o) {
-        incl.x += a;
-        incl.y += b;
-        incl.z += c;
-      }
+      const int4 y = shfl_up4(incl, o);
+      if (lane >= o) incl = add4(incl, y);
     }
     if (lane == 31) s_warp[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-      const int3 w = lane < kPlanThreads / 32 ? s_warp[lane] : make_int3(0, 0, 0);
-      int3 wi = w;
+      const int4 w = lane < kPlanThreads / 32 ? s_warp[lane] : make_int4(0, 0, 0, 0);
+      int4 wi = w;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, wi.x, o);
-        const int b = __shfl_up_sync(0xffffffffu, wi.y, o);
-        const int c = __shfl_up_sync(0xffffffffu, wi.z, o);
-        if (lane >= o) {
-          wi.x += a;
-          wi.y += b;
-          wi.z += c;
-        }
+        const int4 y = shfl_up4(wi, o);
+        if (lane >= o) wi = add4(wi, y);
       }
-      if (lane < kPlanThreads / 32) s_warp[lane] = make_int3(wi.x - w.x, wi.y - w.y, wi.z - w.z);
+      if (lane < kPlanThreads / 32) s_warp[lane] = sub4(wi, w);
     }
     __syncthreads();
-    const int3 cy = s_carry, wo = s_warp[wid];
-    const int ex = cy.x + wo.x + incl.x - x.x, ey = cy.y + wo.y + incl.y - x.y, ez = cy.z + wo.z + incl.z - x.z;
+    const int4 ex = add4(add4(s_carry, s_warp[wid]), sub4(incl, x));
     if (r < p.R) {
-      cu[r] = ex;
-      if (r < C) tiles[r] = ey;
-      else splits[r - C] = ez;
+      cu[r] = ex.x;
+      if (r < C) {
+        tiles[r] = ex.y;
+        if (staging) stage[r] = ex.w;
+      } else {
+        splits[r - C] = ex.z;
+      }
     }
     __syncthreads();
-    if (tid == kPlanThreads - 1) s_carry = make_int3(ex + x.x, ey + x.y, ez + x.z);
+    if (tid == kPlanThreads - 1) s_carry = add4(ex, x);
     __syncthreads();
   }
   if (tid == 0) {
-    const int3 t = s_carry;
+    const int4 t = s_carry;
     cu[p.R] = t.x;
     tiles[C] = t.y;
     splits[p.G] = t.z;
-    bad |= (t.x != p.T) || (t.y != p.expect_tiles) || (t.z != p.expect_splits);
+    if (staging) stage[C] = t.w;
+    bad |= (t.x != p.T) || (t.y != p.expect_tiles) || (t.z != p.expect_splits) ||
+           (staging && t.w != p.expect_stage_pages);
   }
   if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
 }
@@ -114,6 +118,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 // --------------------------------------------------------------------------------------------
 // split-KV decode
 // --------------------------------------------------------------------------------------------
+// Tuning knobs (compile-time): cp.async ring depth per warp, and how FP8 codes become f16.
+#ifndef PKV_DECODE_STAGES_BF16
+#define PKV_DECODE_STAGES_BF16 3  // 96 KB per CTA at D = 128: 2 CTAs per SM
+#endif
+#ifndef PKV_DECODE_STAGES_FP8
+#define PKV_DECODE_STAGES_FP8 3   // 48 KB per CTA at D = 128: 4 CTAs per SM (measured best)
+#endif
+#ifndef PKV_FP8_INT_CONVERT
+#define PKV_FP8_INT_CONVERT 1     // 1: integer bit placement, 0: cvt.rn.f16x2.e4m3x2
+#endif
+
 template <int D, bool FP8>
 struct DecodeCfg {
   static constexpr int kWarps = 4;
@@ -121,7 +136,7 @@ struct DecodeCfg {
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one of K or V
-  static constexpr int kStages = FP8 ? 4 : 3;  // 64 / 96 KB per CTA: 3 / 2 CTAs per SM
+  static constexpr int kStages = FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16;
   static constexpr int kWarpBytes = kStages * 2 * kTileBytes;
   static constexpr int kSmemBytes = kWarps * kWarpBytes;
 };
@@ -139,6 +154,27 @@ __device__ __forceinline__ int swz_v(int row, int c) {
   else if constexpr (D == 128) return c ^ (((row >> 1) & 3) << 1);
   else return c ^ (((row >> 1) & 1) << 1);
 }
+
+// Two E4M3 codes -> f16x2.  Integer form: with byte b in bits 15:8 of a half, the f16 with
+// sign b7, exponent field b6..b3 (one bit narrower than f16's) and mantissa b2..b0 is exactly
+// value(b) * 2^-8 (normals and subnormals alike, since both formats are binary with the same
+// mantissa alignment); bytes 0 and 2 of `x` are ignored.  The 2^8 is folded into the fp32
+// scales applied after the MMAs.
+constexpr float kFp8IntUnscale = PKV_FP8_INT_CONVERT ? 256.0f : 1.0f;
+__device__ __forceinline__ uint32_t e4m3_pair_bits_to_f16x2(uint32_t x) {
+  return (x & 0x80008000u) | ((x & 0x7F007F00u) >> 1);
+}
+// codes (byte lo_sel of x, byte hi_sel of y) of a word pair -> f16x2 (times 2^-8 in int form)
+__device__ __forceinline__ uint32_t fp8_pair_to_f16x2(uint32_t x, uint32_t y, uint32_t sel) {
+#if PKV_FP8_INT_CONVERT
+  return e4m3_pair_bits_to_f16x2(__byte_perm(x, y, sel));
+#else
+  const uint32_t two = __byte_perm(x, y, sel) ;  // code lo in byte 1, code hi in byte 3
+  return e4m3x2_to_f16x2(static_cast<uint16_t>(((two >> 8) & 0xFF) | ((two >> 16) & 0xFF00)));
+#endif
+}
+// selector putting byte i of x into byte 1 and byte j of the pair into byte 3
+__host__ __device__ constexpr uint32_t pair_sel(uint32_t i, uint32_t j) { return (j << 12) | (i << 4); }
 
 template <int D, bool FP8, int NT>
 __global__ void __launch_bounds__(DecodeCfg<D, FP8>::kThreads)
@@ -214,8 +250,8 @@ decode_splitkv_kernel(DecodeParams p) {
       const float down = 1.f / up;
       const float d0 = __shfl_sync(0xffffffffu, down, (2 * q4) * 4);
       const float d1 = __shfl_sync(0xffffffffu, down, (2 * q4 + 1) * 4);
-      colscale[nt][0] = d0 * p.kv_scale * p.scale_log2;
-      colscale[nt][1] = d1 * p.kv_scale * p.scale_log2;
+      colscale[nt][0] = d0 * kFp8IntUnscale * p.kv_scale * p.scale_log2;
+      colscale[nt][1] = d1 * kFp8IntUnscale * p.kv_scale * p.scale_log2;
     }
   }
 
@@ -309,12 +345,12 @@ decode_splitkv_kernel(DecodeParams p) {
       for (int kk = 0; kk < KS; ++kk) {
         const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2]);
         const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2]);
-        const uint32_t lo_w = w0[kk & 3], hi_w = w1[kk & 3];
+        const uint32_t lo_w = w0[kk & 3], hi_w = w1[kk & 3];  // rows g8 and g8 + 8
         uint32_t a[4];
-        a[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo_w & 0xFFFF));
-        a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo_w >> 16));
-        a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi_w & 0xFFFF));
-        a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi_w >> 16));
+        a[0] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(0, 1));
+        a[2] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(2, 3));
+        a[1] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(0, 1));
+        a[3] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(2, 3));
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
       }
@@ -380,18 +416,16 @@ decode_splitkv_kernel(DecodeParams p) {
         for (int i = 0; i < 4; ++i)
           w[i] = *reinterpret_cast<const uint32_t*>(sVp + rows[i] * Cfg::kRowBytes +
                                                     (swz_v<D, FP8>(rows[i], c) << 4) + in_chunk);
-        // 4x4 byte transpose: dj = (w0.bj, w1.bj, w2.bj, w3.bj) = dim j at tokens 2q,2q+1,2q+8,2q+9
-        const uint32_t x0 = __byte_perm(w[0], w[1], 0x5140), x1 = __byte_perm(w[0], w[1], 0x7362);
-        const uint32_t y0 = __byte_perm(w[2], w[3], 0x5140), y1 = __byte_perm(w[2], w[3], 0x7362);
-        const uint32_t dj[4] = {__byte_perm(x0, y0, 0x5410), __byte_perm(x0, y0, 0x7632),
-                                __byte_perm(x1, y1, 0x5410), __byte_perm(x1, y1, 0x7632)};
+        // dim j of this lane's 4 dims, at tokens (2q, 2q+1) from words w0, w1 and (2q+8, 2q+9)
+        // from w2, w3: one byte permute gathers the pair, which converts in place
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
+          const uint32_t j0 = 2 * half, j1 = 2 * half + 1;
           uint32_t a[4];
-          a[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half] & 0xFFFF));
-          a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half + 1] & 0xFFFF));
-          a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half] >> 16));
-          a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(dj[2 * half + 1] >> 16));
+          a[0] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j0, 4 + j0));
+          a[1] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j1, 4 + j1));
+          a[2] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j0, 4 + j0));
+          a[3] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j1, 4 + j1));
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[nt][0], pb[nt][1]);
         }
@@ -450,7 +484,7 @@ decode_splitkv_kernel(DecodeParams p) {
       acc += f * sm_o[(w * HN + hl) * D + d];
       lsum += f * sm_l[w * HN + hl];
     }
-    acc *= p.kv_scale;
+    acc *= FP8 ? p.kv_scale * kFp8IntUnscale : p.kv_scale;
     if (num_splits == 1) {
       __nv_bfloat16 b = __float2bfloat16_rn(acc / lsum);
       p.out[static_cast<int64_t>(qrow) * p.Hq * D + (hq0 + hl) * D + d] = *reinterpret_cast<uint16_t*>(&b);
@@ -466,16 +500,17 @@ decode_splitkv_kernel(DecodeParams p) {
 }
 
 // --------------------------------------------------------------------------------------------
-// log-sum-exp merge of the splits: one warp per (generation request, query head), lane i owns
-// 4 consecutive head dims; splits are streamed with an online max so one pass suffices
+// log-sum-exp merge of the splits: one CTA of 4 warps per (generation request, query head); warp
+// w streams splits w, w+4, ... with an online max (lane i owns 4 consecutive head dims), then
+// the four partial results are merged through shared memory
 // --------------------------------------------------------------------------------------------
 constexpr int kCombineWarps = 4;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParams p) {
-  const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-  const int gr = w / p.Hq, hq = w - gr * p.Hq;
-  if (gr >= p.G) return;
+  __shared__ float4 s_acc[kCombineWarps][32];
+  __shared__ float2 s_ml[kCombineWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gr = blockIdx.x / p.Hq, hq = blockIdx.x - gr * p.Hq;
   const int first = __ldg(p.split_prefix + gr);
   const int S = __ldg(p.split_prefix + gr + 1) - first;
   if (S <= 1) return;  // written directly by the decode kernel
@@ -486,8 +521,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
   const int64_t stride4 = static_cast<int64_t>(p.Hq) * D / 4;
   float M = -INFINITY, lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = 0; s < S; ++s) {
+#pragma unroll 4
+  for (int s = warp; s < S; s += kCombineWarps) {
     const float2 m_l = ml[static_cast<int64_t>(s) * p.Hq];
     const float4 v = active ? po[s * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float Mn = fmaxf(M, m_l.x);
@@ -499,12 +534,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
     lsum = lsum * a + m_l.y * b;
     M = Mn;
   }
-  if (active) {
-    const float inv = 1.f / lsum;
-    const int64_t qrow = p.gen_row0 + gr;
-    uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    *reinterpret_cast<uint2*>(p.out + qrow * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
+  s_acc[warp][lane] = acc;
+  if (lane == 0) s_ml[warp] = make_float2(M, lsum);
+  __syncthreads();
+  if (warp != 0 || !active) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, s_ml[w].x);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    const float f = exp2f(s_ml[w].x - Mt);  // a warp with no splits has M = -inf: f = 0
+    const float4 a4 = s_acc[w][lane];
+    o.x += f * a4.x;
+    o.y += f * a4.y;
+    o.z += f * a4.z;
+    o.w += f * a4.w;
+    lt += f * s_ml[w].y;
   }
+  const float inv = 1.f / lt;
+  const int64_t qrow = p.gen_row0 + gr;
+  uint2 packed = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
+  *reinterpret_cast<uint2*>(p.out + qrow * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
 }
 
 template <int D, bool FP8, int NT>
@@ -527,8 +579,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s) {
-  const int64_t warps = static_cast<int64_t>(p.G) * p.Hq;
-  combine_kernel<<<static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0, s>>>(p);
+  combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(p.G) * p.Hq), kCombineWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -20,9 +20,13 @@ struct PlanLayout {
   int64_t cu_q;          // [R + 1]  exclusive prefix of context_lengths
   int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxRowsPerCta) over context requests
   int64_t split_prefix;  // [G + 1]  prefix of ceil(L_r / kv_chunk) over generation requests
+  int64_t stage_prefix;  // [C + 1]  FP8 pools: prefix of the context requests' page counts
+  int64_t stage_tbl;     // [C * max_blocks] FP8 pools: block table into the bf16 staging pool
   int64_t int_words;     // total int32 words of the plan
   int64_t part_o;        // byte offset of fp32 partial outputs [num_splits, Hq, D]
   int64_t part_ml;       // byte offset of fp32 (m, l) pairs   [num_splits, Hq, 2]
+  int64_t stage_pool;    // byte offset of the bf16 staging pool [stage_pages, 2, B, Hkv, D]
+  int64_t stage_pages;   // pages in the staging pool (0 unless FP8 pool with context requests)
   int64_t total_bytes;
 };
 
@@ -47,7 +51,7 @@ struct AppendParams {
 };
 
 struct PlanParams {
-  int32_t R, C, G, T, Hkv, expect_tiles, expect_splits, kv_chunk;
+  int32_t R, C, G, T, Hkv, B, expect_tiles, expect_splits, kv_chunk, expect_stage_pages;
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words
@@ -82,6 +86,21 @@ struct ContextParams {
   uint16_t* out;
   int64_t out_stride;
   float scale_log2;
+  float out_scale;          // multiplies O at the end (the FP8 dequantisation scale, else 1)
+  int32_t* d_error;
+};
+
+// FP8 pools with context requests: copies the context requests' pages into a bf16 staging pool
+// holding each code's exact value (every E4M3 value is a bf16 value), with its own block table.
+struct StageParams {
+  int32_t C, B, Hkv, D, NB, max_blocks, total_pages;
+  const int32_t* ctx_len;
+  const int32_t* past;
+  const int32_t* tbl;
+  const int32_t* stage_prefix;
+  int32_t* stage_tbl;
+  const uint8_t* pool;
+  uint16_t* stage_pool;
   int32_t* d_error;
 };
 
@@ -89,6 +108,7 @@ cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches);
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map,
                            bool fp8, cudaStream_t s);

@@ -70,15 +70,22 @@ CONTEXT = [
 ]
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
 @pytest.mark.parametrize("case", CONTEXT, ids=[c[0] for c in CONTEXT])
-def test_context_matches_oracle(case):
+def test_context_matches_oracle(case, kv_dtype):
     name, ctx, gen, Hq, Hkv, D, B = case
-    b = _batch(name, ctx, gen, Hq, Hkv, D, B)
+    b = _batch(name, ctx, gen, Hq, Hkv, D, B, kv_dtype)
     g = gpu_run(b)
     assert g.error == 0
     o = oracle_run(b)
     assert o.status == 0
-    assert max_err(gpu_out_f64(g, b), o.out) <= BF16_TOL
+    got = gpu_out_f64(g, b)
+    if kv_dtype == "bf16":
+        assert max_err(got, o.out) <= BF16_TOL
+    else:  # FP8 pool: context pages are staged as exact bf16 code values first
+        assert max_err(got, o.out) <= FP8_DEQ_TOL
+        unq = oracle_run(b, unquantised=True).out
+        assert max_err(got, unq) <= max_err(o.out, unq) + FP8_DEQ_TOL
 
 
 def test_deterministic_and_page_permutation_invariant():
@@ -115,3 +122,5 @@ def test_launch_counts():
     b = _batch("launches", [(100, 0)], [5000, 20], 8, 2, 128, 64)
     g = gpu_run(b)
     assert g.launches == 5  # append, plan, context, decode, combine
+    g8 = gpu_run(_batch("launches8", [(100, 0)], [5000, 20], 8, 2, 128, 64, "fp8"))
+    assert g8.launches == 6  # append, plan, stage_fp8, context, decode, combine
