@@ -220,12 +220,21 @@ def barrier(world):
 
 
 def reduce_max(x: float, world: int) -> float:
+    """Max over ranks (the slowest rank's time); NCCL reduces on the GPU, gloo on the host."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(work_per_rank: float, ms_total_per_rank: float, steps: int, world: int) -> tuple[float, float]:
+    """Weak scaling: every rank processes its own batch of the same shape.  Returns (ms per
+    step of the slowest rank, whole-job units per second = world * work / that time)."""
+    ms_step = reduce_max(ms_total_per_rank, world) / steps
+    return ms_step, world * work_per_rank / (ms_step * 1e-3)
 
 
 def run_ours(args):
@@ -273,8 +282,7 @@ def run_ours(args):
         stop.record()
         torch.cuda.synchronize()
     barrier(world)
-    ms_total = reduce_max(start.elapsed_time(stop), world)
-    ms_step = ms_total / args.steps
+    ms_step, _ = aggregate(1.0, start.elapsed_time(stop), args.steps, world)
     err = int(step.d_error.item())
     if err:
         raise SystemExit(f"device error word {err} during the timed region")
@@ -283,6 +291,34 @@ def run_ours(args):
     for j, n in enumerate(fwd_names):
         kern_ms[n] = statistics.fmean(e.elapsed_ms(j) for e in ev_fwd)
     kern_ms["append_rope"] = statistics.fmean(e.elapsed_ms(0) for e in ev_app)
+
+    # ---- the same step captured once into a CUDA graph and replayed (launch overhead gone) ----
+    graph = None
+    try:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            step(q, k, v)
+        torch.cuda.current_stream().wait_stream(gs)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            step(q, k, v)
+        for _ in range(3):
+            cg.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            cg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        g_ms, _ = aggregate(1.0, g0.elapsed_time(g1), args.steps, world)
+        graph = {"ms_per_step": g_ms, "launches_per_step": launches_per_step}
+        del cg
+    except Exception as exc:  # capture is a measurement extra, never a reason to fail the bench
+        graph = {"error": str(exc)[:200]}
 
     # ---- e2e through the public API: host q/k/v in pinned memory, output copied back ----
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
@@ -318,6 +354,10 @@ def run_ours(args):
         value = world * work["ctx_flops"] / (ms_step * 1e-3) / 1e12
         e2e_value = world * work["ctx_flops"] / (e2e_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
+    if graph and "ms_per_step" in graph:
+        w = work["decode_kv_bytes"] or work["ctx_flops"]
+        graph["value"] = world * w / (graph["ms_per_step"] * 1e-3) / (1e9 if work["decode_kv_bytes"] else 1e12)
+        graph["tokens_per_s"] = world * work["tokens"] / (graph["ms_per_step"] * 1e-3)
     if dominant == "decode_splitkv":
         ach = work["decode_bytes"] / (kern_ms["decode_splitkv"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": pk_["hbm"], "unit": "GB/s",
@@ -359,6 +399,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
+        "graph": graph,
         "kernels": kernels,
         "roofline": roof,
         "clocks": sampler.summary(),

@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
   __shared__ int32_t s_warp[kAppendThreads / 32];
   __shared__ int32_t s_carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  pdl_wait();
   if (tid == 0) s_carry = 0;
   __syncthreads();
   for (int base = 0; base < p.R; base += kAppendThreads) {
@@ -205,14 +206,9 @@ cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const size_t smem = sizeof(int32_t) * (p.R + 1);
-  if (fp8) {
-    if (smem > 48 * 1024) cudaFuncSetAttribute(append_rope_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    append_rope_kernel<true><<<static_cast<unsigned>(blocks), kAppendThreads, smem, s>>>(p);
-  } else {
-    if (smem > 48 * 1024) cudaFuncSetAttribute(append_rope_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    append_rope_kernel<false><<<static_cast<unsigned>(blocks), kAppendThreads, smem, s>>>(p);
-  }
-  return cudaGetLastError();
+  auto kern = fp8 ? append_rope_kernel<true> : append_rope_kernel<false>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kAppendThreads), smem, s, p);
 }
 
 }  // namespace pkv

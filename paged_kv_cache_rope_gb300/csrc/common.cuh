@@ -17,6 +17,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so that it may start
+// while the previous kernel on the stream drains; it must wait here before touching memory that
+// earlier work produces.  A no-op when launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ void flag_error(int32_t* d_error, uint32_t bits) {
   if (d_error) atomicOr(reinterpret_cast<unsigned int*>(d_error), bits);
 }

@@ -93,6 +93,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.x;
   const int hk = hq / p.group;
+  pdl_wait();
 
   // ---- which context request / pair of query tiles (heaviest first) ----
   const int unit = p.num_tiles - 1 - static_cast<int>(blockIdx.y);
@@ -419,6 +420,7 @@ constexpr int kStageThreads = 256;
 
 __global__ void __launch_bounds__(kStageThreads) stage_fp8_kernel(const StageParams p) {
   const int gp = blockIdx.x;  // staging page
+  pdl_wait();
   int lo = 0, hi = p.C - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
@@ -461,8 +463,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_fp8_kernel(const StagePar
 }  // namespace
 
 cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s) {
-  stage_fp8_kernel<<<p.total_pages, kStageThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(stage_fp8_kernel, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
 }
 
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, bool fp8,
@@ -475,13 +476,11 @@ cudaError_t launch_context(const ContextParams& p, const void* q_map, const void
   if (p.D == 128) {
     e = cudaFuncSetAttribute(context_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<128>::kBytes);
     if (e != cudaSuccess) return e;
-    context_attn_kernel<128><<<grid, kThreads, CtxSmem<128>::kBytes, s>>>(p, qm, km);
-  } else {
-    e = cudaFuncSetAttribute(context_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<64>::kBytes);
-    if (e != cudaSuccess) return e;
-    context_attn_kernel<64><<<grid, kThreads, CtxSmem<64>::kBytes, s>>>(p, qm, km);
+    return launch_pdl(context_attn_kernel<128>, grid, dim3(kThreads), CtxSmem<128>::kBytes, s, p, qm, km);
   }
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(context_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<64>::kBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(context_attn_kernel<64>, grid, dim3(kThreads), CtxSmem<64>::kBytes, s, p, qm, km);
 }
 
 }  // namespace pkv

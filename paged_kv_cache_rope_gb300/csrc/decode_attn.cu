@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   const bool staging = p.expect_stage_pages > 0;
   const int C = p.C, chunk = p.kv_chunk;
   bool bad = false;
+  pdl_wait();
   if (tid == 0) s_carry = make_int4(0, 0, 0, 0);
   __syncthreads();
   for (int base = 0; base < p.R; base += kPlanThreads) {
@@ -188,6 +189,7 @@ decode_splitkv_kernel(DecodeParams p) {
 
   // ---- which generation request and split this CTA owns ----
   if (item >= p.total_splits) return;
+  pdl_wait();
   int lo = 0, hi = p.G - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
@@ -511,6 +513,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
   __shared__ float2 s_ml[kCombineWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gr = blockIdx.x / p.Hq, hq = blockIdx.x - gr * p.Hq;
+  pdl_wait();
   const int first = __ldg(p.split_prefix + gr);
   const int S = __ldg(p.split_prefix + gr + 1) - first;
   if (S <= 1) return;  // written directly by the decode kernel
@@ -566,21 +569,18 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   static_assert(Cfg::kSmemBytes >= Cfg::kWarps * NT * 8 * (D + 2) * 4, "merge buffer must fit");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.total_splits, p.Hkv);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.total_splits, p.Hkv), dim3(Cfg::kThreads), Cfg::kSmemBytes, s, p);
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
 }
 
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s) {
-  combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(p.G) * p.Hq), kCombineWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(p.G) * p.Hq)),
+                    dim3(kCombineWarps * 32), 0, s, p);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches) {

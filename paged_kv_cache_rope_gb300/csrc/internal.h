@@ -104,6 +104,23 @@ struct StageParams {
   int32_t* d_error;
 };
 
+// Launch `kernel` with programmatic stream serialisation (it may begin while the previous
+// kernel on the stream drains; the kernel itself waits with griddepcontrol.wait).
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches);

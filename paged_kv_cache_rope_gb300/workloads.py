@@ -183,7 +183,7 @@ def workload(idx: int, *, kv_dtype: str = "bf16", device: str = "cpu", poison: b
     """The five synthetic workloads (seed = workload index unless given).  ``max_gen`` keeps
     only the first generation requests (smaller captures for profiling)."""
     seed = idx if seed is None else seed
-    rng = np.random.default_rng(1000 + seed)
+    rng = np.random.default_rng(1000 + idx)  # lengths depend on the workload only, values on seed
 
     def _mk(**kw):
         if max_gen is not None:

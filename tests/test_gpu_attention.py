@@ -124,3 +124,23 @@ def test_launch_counts():
     assert g.launches == 5  # append, plan, context, decode, combine
     g8 = gpu_run(_batch("launches8", [(100, 0)], [5000, 20], 8, 2, 128, 64, "fp8"))
     assert g8.launches == 6  # append, plan, stage_fp8, context, decode, combine
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_prefix_shared_pages(kv_dtype):
+    """Prefix reuse: several requests' block tables point at the same physical pages for a
+    common cached prefix (read-only); each request's own new tokens land in pages of its own."""
+    ctx = [(70, 96)] if kv_dtype == "bf16" else []
+    b = _batch("shared_" + kv_dtype, ctx, [200, 150, 97], 8, 2, 128, 32, kv_dtype)
+    tbl = b.block_table.copy()
+    donor = b.num_requests - 1  # the 97-token decode: its first 3 pages hold 96 cached tokens
+    for r in range(b.num_requests - 1):
+        tbl[r, :3] = tbl[donor, :3]
+    b2 = dataclasses.replace(b, block_table=tbl)
+    g = gpu_run(b2)
+    assert g.error == 0
+    o = oracle_run(b2)
+    assert o.status == 0
+    tol = BF16_TOL if kv_dtype == "bf16" else FP8_DEQ_TOL
+    assert max_err(gpu_out_f64(g, b2), o.out) <= tol
+    assert np.array_equal(bits(g.pool).reshape(-1), o.pool.reshape(-1))
