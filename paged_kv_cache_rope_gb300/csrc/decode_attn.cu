@@ -124,7 +124,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 #define PKV_DECODE_STAGES_BF16 3  // 96 KB per CTA at D = 128: 2 CTAs per SM
 #endif
 #ifndef PKV_DECODE_STAGES_FP8
-#define PKV_DECODE_STAGES_FP8 3   // 48 KB per CTA at D = 128: 4 CTAs per SM (measured best)
+#define PKV_DECODE_STAGES_FP8 2   // ring slots of SUB_FP8 tiles: 64 KB per CTA at D = 128
+#endif
+#ifndef PKV_DECODE_SUB_FP8
+#define PKV_DECODE_SUB_FP8 2      // 16-token tiles consumed per iteration (FP8)
+#endif
+#ifndef PKV_DECODE_SUB_BF16
+#define PKV_DECODE_SUB_BF16 1     // 16-token tiles consumed per iteration (bf16)
 #endif
 #ifndef PKV_FP8_INT_CONVERT
 #define PKV_FP8_INT_CONVERT 1     // 1: integer bit placement, 0: cvt.rn.f16x2.e4m3x2
@@ -136,9 +142,11 @@ struct DecodeCfg {
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
   static constexpr int kChunksPerRow = kRowBytes / 16;
-  static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one of K or V
+  static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one 16-token tile of K or V
+  static constexpr int kSub = FP8 ? PKV_DECODE_SUB_FP8 : PKV_DECODE_SUB_BF16;
+  static constexpr int kSlotBytes = 2 * kSub * kTileBytes;      // K then V of kSub tiles
   static constexpr int kStages = FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16;
-  static constexpr int kWarpBytes = kStages * 2 * kTileBytes;
+  static constexpr int kWarpBytes = kStages * kSlotBytes;
   static constexpr int kSmemBytes = kWarps * kWarpBytes;
 };
 
@@ -272,164 +280,207 @@ decode_splitkv_kernel(DecodeParams p) {
   const int32_t* tbl_r = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
   const int64_t row_pitch = static_cast<int64_t>(p.Hkv) * Cfg::kRowBytes;  // bytes between slots
   const int64_t kv_pitch = static_cast<int64_t>(p.B) * row_pitch;           // K -> V in a page
+  const int log2B = 31 - __clz(p.B);                                        // B is a power of two
+  constexpr int SUB = Cfg::kSub;
+  const int w_begin = t_begin + my_first * kDecodeTile;
+  const int w_end = min(t_end, w_begin + my_n * kDecodeTile);  // this warp's tokens
+  const int n_iter = (my_n + SUB - 1) / SUB;
 
-  auto load_tile = [&](int tile, int stage) {
-    const int t0 = t_begin + (my_first + tile) * kDecodeTile;
-    const int lb = t0 / p.B, slot0 = t0 - lb * p.B;
-    int page = lb < p.max_blocks ? __ldg(tbl_r + lb) : -1;
-    bool page_ok = page >= 0 && page < p.NB;
+  // per-lane pieces of the 16-row tile copy that do not change from tile to tile
+  constexpr int kCopies = Cfg::kChunksPerRow / 2;
+  int cp_row[kCopies];
+  uint32_t cp_dk[kCopies], cp_dv[kCopies], cp_src[kCopies];
+#pragma unroll
+  for (int i = 0; i < kCopies; ++i) {
+    const int c_lin = lane + 32 * i;
+    const int row = c_lin / Cfg::kChunksPerRow, c = c_lin % Cfg::kChunksPerRow;
+    cp_row[i] = row;
+    cp_src[i] = static_cast<uint32_t>(row * row_pitch + c * 16);
+    cp_dk[i] = row * Cfg::kRowBytes + (swz_k<D, FP8>(row, c) << 4);
+    cp_dv[i] = row * Cfg::kRowBytes + (swz_v<D, FP8>(row, c) << 4);
+  }
+
+  auto load_tile = [&](int tile, uint32_t sK, uint32_t sV) {  // one 16-token tile into (sK, sV)
+    const int t0 = w_begin + tile * kDecodeTile;
+    const int lb = t0 >> log2B, slot0 = t0 & (p.B - 1);
+    int page = (t0 < w_end && lb < p.max_blocks) ? __ldg(tbl_r + lb) : 0;
+    const bool page_ok = page >= 0 && page < p.NB;
     if (!page_ok) {
       if (lane == 0) flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
       page = 0;
     }
     const uint8_t* kbase = p.pool + (static_cast<int64_t>(page) * 2 * kv_pitch) +
                            static_cast<int64_t>(slot0) * row_pitch + static_cast<int64_t>(h) * Cfg::kRowBytes;
-    const uint32_t sK = wbuf_s + stage * 2 * Cfg::kTileBytes;
-    const uint32_t sV = sK + Cfg::kTileBytes;
 #pragma unroll
-    for (int i = 0; i < Cfg::kChunksPerRow / 2; ++i) {
-      const int c_lin = lane + 32 * i;
-      const int row = c_lin / Cfg::kChunksPerRow, c = c_lin % Cfg::kChunksPerRow;
-      const bool ok = page_ok && (t0 + row < t_end);
-      const uint8_t* src = kbase + row * row_pitch + c * 16;
-      cp_async_16(sK + row * Cfg::kRowBytes + (swz_k<D, FP8>(row, c) << 4), ok ? src : p.pool, ok ? 16u : 0u);
-      cp_async_16(sV + row * Cfg::kRowBytes + (swz_v<D, FP8>(row, c) << 4), ok ? src + kv_pitch : p.pool,
-                  ok ? 16u : 0u);
+    for (int i = 0; i < kCopies; ++i) {
+      const bool ok = page_ok && (t0 + cp_row[i] < w_end);
+      const uint8_t* src = kbase + cp_src[i];
+      cp_async_16(sK + cp_dk[i], ok ? src : p.pool, ok ? 16u : 0u);
+      cp_async_16(sV + cp_dv[i], ok ? src + kv_pitch : p.pool, ok ? 16u : 0u);
     }
+  };
+  auto load_slot = [&](int it, int slot) {  // SUB consecutive tiles of this warp
+    const uint32_t base = wbuf_s + slot * Cfg::kSlotBytes;
+#pragma unroll
+    for (int u = 0; u < SUB; ++u)
+      load_tile(it * SUB + u, base + u * Cfg::kTileBytes, base + (SUB + u) * Cfg::kTileBytes);
   };
 
   constexpr int S = Cfg::kStages;
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
-    if (s < my_n) load_tile(s, s);
+    if (s < n_iter) load_slot(s, s);
     cp_async_commit();
   }
 
-  for (int it = 0; it < my_n; ++it) {
+  for (int it = 0; it < n_iter; ++it) {
     cp_async_wait<S - 2>();
     __syncwarp();
     {
       const int nxt = it + S - 1;
-      if (nxt < my_n) load_tile(nxt, nxt % S);
+      if (nxt < n_iter) load_slot(nxt, nxt % S);
       cp_async_commit();
     }
-    const int stage = it % S;
-    const uint32_t sK = wbuf_s + stage * 2 * Cfg::kTileBytes;
-    const uint32_t sV = sK + Cfg::kTileBytes;
-    const int t0 = t_begin + (my_first + it) * kDecodeTile;
+    const int slot = it % S;
+    const uint32_t sK0 = wbuf_s + slot * Cfg::kSlotBytes;
+    const uint32_t sV0 = sK0 + SUB * Cfg::kTileBytes;
+    const int t0 = w_begin + it * SUB * kDecodeTile;
 
-    // ---- S^T[16 tokens x 8 heads] = K Q^T ----
-    float sacc[NT][4];
+    // ---- S^T[16 tokens x 8 heads] = K Q^T for each sub-tile ----
+    float sacc[SUB][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-    if constexpr (!FP8) {
-      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+    for (int u = 0; u < SUB; ++u)
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        uint32_t a[4];
-        ldmatrix_x4(a, sK + row * Cfg::kRowBytes + (swz_k<D, FP8>(row, 2 * kk + (lane >> 4)) << 4));
+      for (int nt = 0; nt < NT; ++nt) sacc[u][nt][0] = sacc[u][nt][1] = sacc[u][nt][2] = sacc[u][nt][3] = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-      }
-    } else {
-      constexpr int CPL = D / 64;  // 16-byte chunks per lane per row
-      uint4 kw[2][CPL];
-      const uint8_t* sKp = wbuf + stage * 2 * Cfg::kTileBytes;
+    for (int u = 0; u < SUB; ++u) {
+      const uint32_t sK = sK0 + u * Cfg::kTileBytes;
+      if constexpr (!FP8) {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int rs = 0; rs < 2; ++rs) {
-        const int row = g8 + 8 * rs;
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a[4];
+          ldmatrix_x4(a, sK + row * Cfg::kRowBytes + (swz_k<D, FP8>(row, 2 * kk + (lane >> 4)) << 4));
 #pragma unroll
-        for (int i = 0; i < CPL; ++i)
-          kw[rs][i] = *reinterpret_cast<const uint4*>(sKp + row * Cfg::kRowBytes +
-                                                      (swz_k<D, FP8>(row, q4 * CPL + i) << 4));
-      }
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
+      } else {
+        constexpr int CPL = D / 64;  // 16-byte chunks per lane per row
+        uint4 kw[2][CPL];
+        const uint8_t* sKp = wbuf + (sK - wbuf_s);
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2]);
-        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2]);
-        const uint32_t lo_w = w0[kk & 3], hi_w = w1[kk & 3];  // rows g8 and g8 + 8
-        uint32_t a[4];
-        a[0] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(0, 1));
-        a[2] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(2, 3));
-        a[1] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(0, 1));
-        a[3] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(2, 3));
+        for (int rs = 0; rs < 2; ++rs) {
+          const int row = g8 + 8 * rs;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          for (int i = 0; i < CPL; ++i)
+            kw[rs][i] = *reinterpret_cast<const uint4*>(sKp + row * Cfg::kRowBytes +
+                                                        (swz_k<D, FP8>(row, q4 * CPL + i) << 4));
+        }
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2]);
+          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2]);
+          const uint32_t lo_w = w0[kk & 3], hi_w = w1[kk & 3];  // rows g8 and g8 + 8
+          uint32_t a[4];
+          a[0] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(0, 1));
+          a[2] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(2, 3));
+          a[1] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(0, 1));
+          a[3] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(2, 3));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
       }
     }
 
-    // ---- online softmax over this tile (columns 2*q4, 2*q4+1; rows g8, g8+8) ----
-    uint32_t pb[NT][2];
-    const bool r0_ok = t0 + g8 < t_end, r1_ok = t0 + g8 + 8 < t_end;
+    // ---- online softmax over the SUB sub-tiles (columns 2*q4, 2*q4+1) ----
+    uint32_t pb[SUB][NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float s0 = r0_ok ? sacc[nt][0] * colscale[nt][0] : -INFINITY;
-      float s1 = r0_ok ? sacc[nt][1] * colscale[nt][1] : -INFINITY;
-      float s2 = r1_ok ? sacc[nt][2] * colscale[nt][0] : -INFINITY;
-      float s3 = r1_ok ? sacc[nt][3] * colscale[nt][1] : -INFINITY;
-      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+      float sv[SUB][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < SUB; ++u) {
+        const bool r0_ok = t0 + u * kDecodeTile + g8 < w_end, r1_ok = t0 + u * kDecodeTile + g8 + 8 < w_end;
+        sv[u][0] = r0_ok ? sacc[u][nt][0] * colscale[nt][0] : -INFINITY;
+        sv[u][1] = r0_ok ? sacc[u][nt][1] * colscale[nt][1] : -INFINITY;
+        sv[u][2] = r1_ok ? sacc[u][nt][2] * colscale[nt][0] : -INFINITY;
+        sv[u][3] = r1_ok ? sacc[u][nt][3] * colscale[nt][1] : -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(sv[u][0], sv[u][2]));
+        mx1 = fmaxf(mx1, fmaxf(sv[u][1], sv[u][3]));
+      }
 #pragma unroll
       for (int msk = 4; msk < 32; msk <<= 1) {
         mx0 = warp_max_xor(mx0, msk);
         mx1 = warp_max_xor(mx1, msk);
       }
       const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-      const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
-      const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
-      const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
-      l_run[nt][0] = l_run[nt][0] * al0 + p0 + p2;
-      l_run[nt][1] = l_run[nt][1] * al1 + p1 + p3;
-      m_run[nt][0] = mn0;
-      m_run[nt][1] = mn1;
+      if (__any_sync(0xffffffffu, mn0 != m_run[nt][0] || mn1 != m_run[nt][1])) {
+        const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+        l_run[nt][0] *= al0;
+        l_run[nt][1] *= al1;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        o[nt][mt][0] *= al0;
-        o[nt][mt][1] *= al1;
-        o[nt][mt][2] *= al0;
-        o[nt][mt][3] *= al1;
+        for (int mt = 0; mt < KS; ++mt) {
+          o[nt][mt][0] *= al0;
+          o[nt][mt][1] *= al1;
+          o[nt][mt][2] *= al0;
+          o[nt][mt][3] *= al1;
+        }
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
       }
-      if constexpr (!FP8) {
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
-      } else {
-        pb[nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
-        pb[nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+#pragma unroll
+      for (int u = 0; u < SUB; ++u) {
+        const float p0 = exp2f(sv[u][0] - mn0), p1 = exp2f(sv[u][1] - mn1);
+        const float p2 = exp2f(sv[u][2] - mn0), p3 = exp2f(sv[u][3] - mn1);
+        l_run[nt][0] += p0 + p2;
+        l_run[nt][1] += p1 + p3;
+        if constexpr (!FP8) {
+          pb[u][nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+          pb[u][nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+        } else {
+          pb[u][nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
+          pb[u][nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+        }
       }
     }
 
-    // ---- O^T[D x 8 heads] += V^T P^T ----
-    if constexpr (!FP8) {
-      const int row = (lane & 7) + (lane >> 4) * 8;
+    // ---- O^T[D x 8 heads] += V^T P^T for each sub-tile ----
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, sV + row * Cfg::kRowBytes + (swz_v<D, FP8>(row, 2 * mt + ((lane >> 3) & 1)) << 4));
+    for (int u = 0; u < SUB; ++u) {
+      const uint32_t sV = sV0 + u * Cfg::kTileBytes;
+      if constexpr (!FP8) {
+        const int row = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
-      }
-    } else {
-      const uint8_t* sVp = wbuf + stage * 2 * Cfg::kTileBytes + Cfg::kTileBytes;
-      const int rows[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
-#pragma unroll
-      for (int pp = 0; pp < D / 32; ++pp) {
-        const int c = 2 * pp + (g8 >> 2), in_chunk = (4 * g8) & 15;
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          w[i] = *reinterpret_cast<const uint32_t*>(sVp + rows[i] * Cfg::kRowBytes +
-                                                    (swz_v<D, FP8>(rows[i], c) << 4) + in_chunk);
-        // dim j of this lane's 4 dims, at tokens (2q, 2q+1) from words w0, w1 and (2q+8, 2q+9)
-        // from w2, w3: one byte permute gathers the pair, which converts in place
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t j0 = 2 * half, j1 = 2 * half + 1;
+        for (int mt = 0; mt < KS; ++mt) {
           uint32_t a[4];
-          a[0] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j0, 4 + j0));
-          a[1] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j1, 4 + j1));
-          a[2] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j0, 4 + j0));
-          a[3] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j1, 4 + j1));
+          ldmatrix_x4_trans(a, sV + row * Cfg::kRowBytes + (swz_v<D, FP8>(row, 2 * mt + ((lane >> 3) & 1)) << 4));
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb[u][nt][0], pb[u][nt][1]);
+        }
+      } else {
+        const uint8_t* sVp = wbuf + (sV - wbuf_s);
+        const int rows[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+#pragma unroll
+        for (int pp = 0; pp < D / 32; ++pp) {
+          const int c = 2 * pp + (g8 >> 2), in_chunk = (4 * g8) & 15;
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = *reinterpret_cast<const uint32_t*>(sVp + rows[i] * Cfg::kRowBytes +
+                                                      (swz_v<D, FP8>(rows[i], c) << 4) + in_chunk);
+          // dim j of this lane's 4 dims, at tokens (2q, 2q+1) from words w0, w1 and (2q+8, 2q+9)
+          // from w2, w3: one byte permute gathers the pair, which converts in place
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t j0 = 2 * half, j1 = 2 * half + 1;
+            uint32_t a[4];
+            a[0] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j0, 4 + j0));
+            a[1] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j1, 4 + j1));
+            a[2] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j0, 4 + j0));
+            a[3] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j1, 4 + j1));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[u][nt][0], pb[u][nt][1]);
+          }
         }
       }
     }
