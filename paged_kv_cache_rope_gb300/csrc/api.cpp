@@ -149,15 +149,22 @@ int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPla
   return PKV_OK;
 }
 
+#ifndef PKV_DECODE_SPLIT_KB
+#define PKV_DECODE_SPLIT_KB 512  // largest K+V byte count one decode CTA streams (measured best)
+#endif
+
 // Decode split length (tokens, multiple of 16): about 4 CTAs per SM over the whole batch, each
-// CTA streaming 64..512 tokens of one KV head.
-int choose_kv_chunk(const pkv_batch* b, int C, int Hkv) {
+// CTA streaming at most PKV_DECODE_SPLIT_KB of K+V (1024 tokens of a bf16 head of 128 dims,
+// 2048 of an FP8 one), so per-CTA set-up is amortised over the same bytes for either dtype.
+int choose_kv_chunk(const pkv_pool* pool, const pkv_batch* b, int C) {
   int64_t total = 0;
   for (int r = C; r < b->num_requests; ++r) total += b->h_past_kv_lengths[r] + 1;
   const int64_t target = static_cast<int64_t>(device_sm_count()) * 4;
-  int64_t chunk = (total * Hkv + target - 1) / std::max<int64_t>(target, 1);
+  int64_t chunk = (total * pool->num_kv_heads + target - 1) / std::max<int64_t>(target, 1);
   chunk = (chunk + 15) / 16 * 16;
-  return static_cast<int>(std::min<int64_t>(512, std::max<int64_t>(64, chunk)));
+  const int64_t token_bytes = 2LL * pool->head_dim * (pool->dtype == PKV_FP8_E4M3 ? 1 : 2);
+  const int64_t cap = std::max<int64_t>(64, (PKV_DECODE_SPLIT_KB * 1024LL / token_bytes) / 16 * 16);
+  return static_cast<int>(std::min<int64_t>(cap, std::max<int64_t>(64, chunk)));
 }
 
 void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
@@ -165,7 +172,7 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   hp->num_tiles = 0;
   for (int r = 0; r < hp->C; ++r)
     hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
-  hp->kv_chunk = choose_kv_chunk(b, hp->C, pool->num_kv_heads);
+  hp->kv_chunk = choose_kv_chunk(pool, b, hp->C);
   hp->num_splits = 0;
   hp->max_splits = 0;
   for (int r = hp->C; r < hp->R; ++r) {

@@ -73,6 +73,29 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D(16x8, fp32) += A(16x32) * B(32x8), E4M3 operands (4 codes per register).
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> two E4M3 codes (RNE, saturating), x.x in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// x ~= hi + lo with hi = e4m3(x) and lo = e4m3(x - hi) (two codes per output, low byte first):
+// about 8 significant bits between them, so a pair of E4M3 MMAs reproduces a bf16 operand.
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi2, uint32_t& lo2) {
+  hi2 = f32x2_to_e4m3x2(x0, x1);
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(hi2), __NV_E4M3);
+  const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  lo2 = f32x2_to_e4m3x2(x0 - hv.x, x1 - hv.y);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

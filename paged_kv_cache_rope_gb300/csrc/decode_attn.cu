@@ -19,8 +19,11 @@
 //   * the splits of one request are merged by combine_kernel with a log-sum-exp rescale (a
 //     separate launch: merging inside the decode kernel's last CTA per pair was measured slower,
 //     since those merges hold SM slots that would otherwise stream KV).
-// FP8 pools: codes convert exactly to f16 (cvt e4m3x2 -> f16x2); Q is scaled by a power of two
-// into f16 range, and the per-pool scale is applied to scores and outputs in fp32.
+// FP8 pools: the codes feed mma.sync m16n8k32 E4M3 directly (K as stored, V after a 4x4 byte
+// transpose in registers); Q (scaled by a power of two) and P (times 256) are each split into
+// hi + lo E4M3 codes and both halves are multiplied into the same fp32 accumulator, which keeps
+// about 8 significant bits of each -- the precision of a bf16 operand -- with no per-element
+// conversion of the pool.  The per-pool scale is applied to scores and outputs in fp32.
 #include <math.h>
 
 #include "common.cuh"
@@ -119,21 +122,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 // --------------------------------------------------------------------------------------------
 // split-KV decode
 // --------------------------------------------------------------------------------------------
-// Tuning knobs (compile-time): cp.async ring depth per warp, and how FP8 codes become f16.
+// Tuning knobs (compile-time): cp.async ring depth per warp and tiles per iteration.
 #ifndef PKV_DECODE_STAGES_BF16
 #define PKV_DECODE_STAGES_BF16 3  // 96 KB per CTA at D = 128: 2 CTAs per SM
 #endif
 #ifndef PKV_DECODE_STAGES_FP8
 #define PKV_DECODE_STAGES_FP8 2   // ring slots of SUB_FP8 tiles: 64 KB per CTA at D = 128
 #endif
-#ifndef PKV_DECODE_SUB_FP8
-#define PKV_DECODE_SUB_FP8 2      // 16-token tiles consumed per iteration (FP8)
-#endif
 #ifndef PKV_DECODE_SUB_BF16
 #define PKV_DECODE_SUB_BF16 1     // 16-token tiles consumed per iteration (bf16)
-#endif
-#ifndef PKV_FP8_INT_CONVERT
-#define PKV_FP8_INT_CONVERT 1     // 1: integer bit placement, 0: cvt.rn.f16x2.e4m3x2
 #endif
 
 template <int D, bool FP8>
@@ -143,7 +140,7 @@ struct DecodeCfg {
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one 16-token tile of K or V
-  static constexpr int kSub = FP8 ? PKV_DECODE_SUB_FP8 : PKV_DECODE_SUB_BF16;
+  static constexpr int kSub = FP8 ? 2 : PKV_DECODE_SUB_BF16;  // FP8: PV takes 32 tokens per MMA
   static constexpr int kSlotBytes = 2 * kSub * kTileBytes;      // K then V of kSub tiles
   static constexpr int kStages = FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16;
   static constexpr int kWarpBytes = kStages * kSlotBytes;
@@ -164,26 +161,15 @@ __device__ __forceinline__ int swz_v(int row, int c) {
   else return c ^ (((row >> 1) & 1) << 1);
 }
 
-// Two E4M3 codes -> f16x2.  Integer form: with byte b in bits 15:8 of a half, the f16 with
-// sign b7, exponent field b6..b3 (one bit narrower than f16's) and mantissa b2..b0 is exactly
-// value(b) * 2^-8 (normals and subnormals alike, since both formats are binary with the same
-// mantissa alignment); bytes 0 and 2 of `x` are ignored.  The 2^8 is folded into the fp32
-// scales applied after the MMAs.
-constexpr float kFp8IntUnscale = PKV_FP8_INT_CONVERT ? 256.0f : 1.0f;
-__device__ __forceinline__ uint32_t e4m3_pair_bits_to_f16x2(uint32_t x) {
-  return (x & 0x80008000u) | ((x & 0x7F007F00u) >> 1);
+// 4x4 byte transpose: word j of the result holds byte j of w0, w1, w2, w3 (in that order).
+__device__ __forceinline__ void transpose4x4_bytes(const uint32_t (&w)[4], uint32_t (&d)[4]) {
+  const uint32_t x0 = __byte_perm(w[0], w[1], 0x5140), x1 = __byte_perm(w[0], w[1], 0x7362);
+  const uint32_t y0 = __byte_perm(w[2], w[3], 0x5140), y1 = __byte_perm(w[2], w[3], 0x7362);
+  d[0] = __byte_perm(x0, y0, 0x5410);
+  d[1] = __byte_perm(x0, y0, 0x7632);
+  d[2] = __byte_perm(x1, y1, 0x5410);
+  d[3] = __byte_perm(x1, y1, 0x7632);
 }
-// codes (byte lo_sel of x, byte hi_sel of y) of a word pair -> f16x2 (times 2^-8 in int form)
-__device__ __forceinline__ uint32_t fp8_pair_to_f16x2(uint32_t x, uint32_t y, uint32_t sel) {
-#if PKV_FP8_INT_CONVERT
-  return e4m3_pair_bits_to_f16x2(__byte_perm(x, y, sel));
-#else
-  const uint32_t two = __byte_perm(x, y, sel) ;  // code lo in byte 1, code hi in byte 3
-  return e4m3x2_to_f16x2(static_cast<uint16_t>(((two >> 8) & 0xFF) | ((two >> 16) & 0xFF00)));
-#endif
-}
-// selector putting byte i of x into byte 1 and byte j of the pair into byte 3
-__host__ __device__ constexpr uint32_t pair_sel(uint32_t i, uint32_t j) { return (j << 12) | (i << 4); }
 
 template <int D, bool FP8, int NT>
 __global__ void __launch_bounds__(DecodeCfg<D, FP8>::kThreads)
@@ -221,7 +207,11 @@ decode_splitkv_kernel(DecodeParams p) {
   const uint16_t* qbase = p.q + static_cast<int64_t>(qrow) * p.q_stride;
 
   // ---- Q fragments (B operand of S^T = K Q^T): column n = query head h*group + nt*8 + g8 ----
-  uint32_t qb[NT][KS][2];
+  // bf16: k16 fragments.  FP8 pool: k32 E4M3 fragments of q * 2^e split as hi + lo codes; the
+  // lane holds head dims [q4*D/4, (q4+1)*D/4) and k-step kk takes its bytes 8kk .. 8kk+7.
+  constexpr int QW = FP8 ? D / 32 : KS;  // k-steps
+  uint32_t qb[NT][QW][2];
+  uint32_t ql[NT][FP8 ? QW : 1][2];
   float colscale[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -236,7 +226,6 @@ decode_splitkv_kernel(DecodeParams p) {
       }
       colscale[nt][0] = colscale[nt][1] = p.scale_log2;
     } else {
-      // this lane holds head-dim slice [q4*D/4, (q4+1)*D/4); k-step kk uses 4 consecutive dims
       float x[D / 4];
       float amax = 0.f;
 #pragma unroll
@@ -250,18 +239,25 @@ decode_splitkv_kernel(DecodeParams p) {
       amax = warp_max_xor(amax, 2);
       int ex = 0;
       if (amax > 0.f) frexpf(amax, &ex);
-      const float up = ldexpf(1.f, 8 - ex);  // amax * up lies in [128, 256)
+      const float up = ldexpf(1.f, 8 - ex);  // amax * up lies in [128, 256), inside E4M3's 448
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        qb[nt][kk][0] = pack_f16x2(x[4 * kk] * up, x[4 * kk + 1] * up);
-        qb[nt][kk][1] = pack_f16x2(x[4 * kk + 2] * up, x[4 * kk + 3] * up);
+      for (int kk = 0; kk < QW; ++kk) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const float* xs = x + 8 * kk + 4 * b;
+          uint32_t h01, l01, h23, l23;
+          split_e4m3x2(xs[0] * up, xs[1] * up, h01, l01);
+          split_e4m3x2(xs[2] * up, xs[3] * up, h23, l23);
+          qb[nt][kk][b] = h01 | (h23 << 16);
+          ql[nt][kk][b] = l01 | (l23 << 16);
+        }
       }
       // score columns 2*q4, 2*q4+1 belong to heads held by lanes (2*q4)*4 and (2*q4+1)*4
       const float down = 1.f / up;
       const float d0 = __shfl_sync(0xffffffffu, down, (2 * q4) * 4);
       const float d1 = __shfl_sync(0xffffffffu, down, (2 * q4 + 1) * 4);
-      colscale[nt][0] = d0 * kFp8IntUnscale * p.kv_scale * p.scale_log2;
-      colscale[nt][1] = d1 * kFp8IntUnscale * p.kv_scale * p.scale_log2;
+      colscale[nt][0] = d0 * p.kv_scale * p.scale_log2;
+      colscale[nt][1] = d1 * p.kv_scale * p.scale_log2;
     }
   }
 
@@ -377,23 +373,22 @@ decode_splitkv_kernel(DecodeParams p) {
                                                         (swz_k<D, FP8>(row, q4 * CPL + i) << 4));
         }
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2]);
-          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2]);
-          const uint32_t lo_w = w0[kk & 3], hi_w = w1[kk & 3];  // rows g8 and g8 + 8
-          uint32_t a[4];
-          a[0] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(0, 1));
-          a[2] = fp8_pair_to_f16x2(lo_w, lo_w, pair_sel(2, 3));
-          a[1] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(0, 1));
-          a[3] = fp8_pair_to_f16x2(hi_w, hi_w, pair_sel(2, 3));
+        for (int kk = 0; kk < QW; ++kk) {  // K codes feed the E4M3 MMA as they are
+          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][(2 * kk) >> 2]);
+          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][(2 * kk) >> 2]);
+          const uint32_t a[4] = {w0[(2 * kk) & 3], w1[(2 * kk) & 3], w0[(2 * kk + 1) & 3], w1[(2 * kk + 1) & 3]};
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_e4m3_16832(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+            mma_e4m3_16832(sacc[u][nt], a, ql[nt][kk][0], ql[nt][kk][1]);
+          }
         }
       }
     }
 
     // ---- online softmax over the SUB sub-tiles (columns 2*q4, 2*q4+1) ----
-    uint32_t pb[SUB][NT][2];
+    uint32_t pb[SUB][NT][2];     // bf16: k16 P^T fragments per sub-tile
+    uint32_t p8[NT][2][2];       // FP8: [hi/lo][sub-tile] E4M3 P^T words (k32 over both sub-tiles)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float sv[SUB][4];
@@ -438,17 +433,25 @@ decode_splitkv_kernel(DecodeParams p) {
           pb[u][nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
           pb[u][nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
         } else {
-          pb[u][nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
-          pb[u][nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+          // 256 * p as hi + lo E4M3 codes, one (hi | lo << 8) 16-bit element per value, so the
+          // 8x8 16-bit transpose moves each value whole: lane (g, q) then holds tokens 2q, 2q+1
+          // (upper rows) and 2q+8, 2q+9 (lower rows) of head g
+          uint32_t h01, l01, h23, l23;
+          split_e4m3x2(p0 * 256.f, p1 * 256.f, h01, l01);
+          split_e4m3x2(p2 * 256.f, p3 * 256.f, h23, l23);
+          const uint32_t up_t = movmatrix_trans(__byte_perm(h01, l01, 0x5140));
+          const uint32_t lo_t = movmatrix_trans(__byte_perm(h23, l23, 0x5140));
+          p8[nt][0][u] = __byte_perm(up_t, lo_t, 0x6420);  // hi codes of tokens 2q, 2q+1, 2q+8, 2q+9
+          p8[nt][1][u] = __byte_perm(up_t, lo_t, 0x7531);  // lo codes
         }
       }
     }
 
-    // ---- O^T[D x 8 heads] += V^T P^T for each sub-tile ----
+    // ---- O^T[D x 8 heads] += V^T P^T ----
+    if constexpr (!FP8) {
 #pragma unroll
-    for (int u = 0; u < SUB; ++u) {
-      const uint32_t sV = sV0 + u * Cfg::kTileBytes;
-      if constexpr (!FP8) {
+      for (int u = 0; u < SUB; ++u) {
+        const uint32_t sV = sV0 + u * Cfg::kTileBytes;
         const int row = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
@@ -457,29 +460,32 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb[u][nt][0], pb[u][nt][1]);
         }
-      } else {
-        const uint8_t* sVp = wbuf + (sV - wbuf_s);
-        const int rows[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+      }
+    } else {
+      // V^T fragments (m = head dim, k = the 32 tokens in P^T's order): for each sub-tile the lane
+      // reads 4 dims of tokens 2q, 2q+1, 2q+8, 2q+9 and transposes them to one word per dim
+      const int rows[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
 #pragma unroll
-        for (int pp = 0; pp < D / 32; ++pp) {
-          const int c = 2 * pp + (g8 >> 2), in_chunk = (4 * g8) & 15;
+      for (int pp = 0; pp < D / 32; ++pp) {
+        const int c = 2 * pp + (g8 >> 2), in_chunk = (4 * g8) & 15;
+        uint32_t dj[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint8_t* sVp = wbuf + (sV0 - wbuf_s) + u * Cfg::kTileBytes;
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             w[i] = *reinterpret_cast<const uint32_t*>(sVp + rows[i] * Cfg::kRowBytes +
                                                       (swz_v<D, FP8>(rows[i], c) << 4) + in_chunk);
-          // dim j of this lane's 4 dims, at tokens (2q, 2q+1) from words w0, w1 and (2q+8, 2q+9)
-          // from w2, w3: one byte permute gathers the pair, which converts in place
+          transpose4x4_bytes(w, dj[u]);
+        }
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t j0 = 2 * half, j1 = 2 * half + 1;
-            uint32_t a[4];
-            a[0] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j0, 4 + j0));
-            a[1] = fp8_pair_to_f16x2(w[0], w[1], pair_sel(j1, 4 + j1));
-            a[2] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j0, 4 + j0));
-            a[3] = fp8_pair_to_f16x2(w[2], w[3], pair_sel(j1, 4 + j1));
+        for (int half = 0; half < 2; ++half) {  // dims 32pp + 4g + 2half + {0, 1}
+          const uint32_t a[4] = {dj[0][2 * half], dj[0][2 * half + 1], dj[1][2 * half], dj[1][2 * half + 1]};
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[u][nt][0], pb[u][nt][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][0][0], p8[nt][0][1]);
+            mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][1][0], p8[nt][1][1]);
           }
         }
       }
@@ -537,7 +543,7 @@ decode_splitkv_kernel(DecodeParams p) {
       acc += f * sm_o[(w * HN + hl) * D + d];
       lsum += f * sm_l[w * HN + hl];
     }
-    acc *= FP8 ? p.kv_scale * kFp8IntUnscale : p.kv_scale;
+    acc *= FP8 ? p.kv_scale * (1.f / 256.f) : p.kv_scale;  // FP8: P entered the MMA as 256 p
     if (num_splits == 1) {
       __nv_bfloat16 b = __float2bfloat16_rn(acc / lsum);
       p.out[static_cast<int64_t>(qrow) * p.Hq * D + (hq0 + hl) * D + d] = *reinterpret_cast<uint16_t*>(&b);
