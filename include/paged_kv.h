@@ -147,6 +147,38 @@ int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t n
                          int32_t* d_error, pkv_stream_t stream);
 
 /*
+ * Variants of the append (adg.csdn.net/69730cc6 section 1.1: RoPE variants and QK LayerNorm;
+ * [ARCH] kernel list: fused QK-norm + RoPE).  Fields:
+ *   rope_style     PKV_ROPE_NEOX (rotate-half pairs (x_j, x_{j+r/2})) or PKV_ROPE_GPTJ
+ *                  (interleaved pairs (x_{2j}, x_{2j+1})), j < r/2
+ *   rotary_dim     r: rotated dims per head, a multiple of 16 and <= head_dim (0 = head_dim);
+ *                  dims >= r are copied unchanged; the RoPE table must then be built with
+ *                  head_dim = r (r/2 (cos, sin) pairs per position, theta_j = base^(-2j/r))
+ *   q_norm_weight  device fp32 [head_dim]: RMSNorm each query head before rotating it,
+ *                  y = x / sqrt(mean(x^2) + norm_eps) * w; NULL = no norm
+ *   k_norm_weight  the same for key heads (V is never normalised or rotated)
+ *   norm_eps       epsilon of the norms
+ * With a norm the sum of squares is an fp32 reduction across lanes, so results agree with an
+ * exact computation to rounding (not bit for bit); without one they are the fixed fp32
+ * recipe of paged_kv_append_rope.
+ */
+typedef enum { PKV_ROPE_NEOX = 0, PKV_ROPE_GPTJ = 1 } pkv_rope_style;
+typedef struct pkv_append_opts {
+  int32_t rope_style;
+  int32_t rotary_dim;
+  const float* q_norm_weight;
+  const float* k_norm_weight;
+  float norm_eps;
+} pkv_append_opts;
+
+/* paged_kv_append_rope with the variants above; opts == NULL is paged_kv_append_rope. */
+int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
+                            const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                            const void* v, int64_t v_row_stride, void* q_out, int64_t q_out_row_stride,
+                            const float* rope_table, int32_t max_pos, const pkv_append_opts* opts,
+                            int32_t* d_error, pkv_stream_t stream);
+
+/*
  * Workspace bytes paged_attention_forward needs for this pool geometry, batch and head count
  * ([NOTES] 五 5.1: the runtime checks that the scratch workspace is large enough): the device
  * plan, fp32 split-KV partials, and for FP8 pools with context requests a bf16 staging copy of

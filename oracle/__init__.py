@@ -49,6 +49,10 @@ def lib():
         L.orc_append_rope.argtypes = [i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                       P, i64, P, i64, P, i64, P, i32, P, i64, P]
         L.orc_append_rope.restype = C.c_int
+        L.orc_append_rope_ex.argtypes = [i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                         P, i64, P, i64, P, i64, P, i32, i32, i32, P, P, f64,
+                                         P, i64, P]
+        L.orc_append_rope_ex.restype = C.c_int
         L.orc_attention.argtypes = [i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, P,
                                     P, f64, P, i64, P]
         L.orc_attention.restype = C.c_int
@@ -155,6 +159,35 @@ def append_rope(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_d
         _ptr(q_bits), int(q_bits.shape[1]) if T else 0, _ptr(k_bits), int(k_bits.shape[1]) if T else 0,
         _ptr(v_bits), int(v_bits.shape[1]) if T else 0, _ptr(cs), int(cs.shape[0]),
         _ptr(q_out), int(q_out.shape[1]), _ptr(pool))
+    return int(st), q_out
+
+
+def append_rope_ex(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim,
+                   tokens_per_block, num_blocks, kv_fp8, inv_scale, q_bits, k_bits, v_bits, cs,
+                   pool, style=0, rotary_dim=0, q_norm_w=None, k_norm_w=None, norm_eps=1e-6,
+                   q_out=None):
+    """O1 with the variants: style 0 rotate-half / 1 interleaved, rotary_dim (0 = head_dim),
+    optional RMSNorm weights for q and k heads.  ``cs`` has rotary_dim / 2 pairs per row."""
+    new_len = np.ascontiguousarray(new_len, dtype=np.int32)
+    past = np.ascontiguousarray(past, dtype=np.int32)
+    tbl = np.ascontiguousarray(block_table, dtype=np.int32)
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    cs = np.ascontiguousarray(cs, dtype=np.float32)
+    T = int(new_len.sum())
+    if q_out is None:
+        q_out = np.zeros((T, num_q_heads * head_dim), dtype=np.uint16)
+    qw = None if q_norm_w is None else np.ascontiguousarray(q_norm_w, dtype=np.float32)
+    kw = None if k_norm_w is None else np.ascontiguousarray(k_norm_w, dtype=np.float32)
+    st = lib().orc_append_rope_ex(
+        int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
+        int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
+        int(num_blocks), int(bool(kv_fp8)), float(inv_scale),
+        _ptr(q_bits), int(q_bits.shape[1]) if T else 0, _ptr(k_bits), int(k_bits.shape[1]) if T else 0,
+        _ptr(v_bits), int(v_bits.shape[1]) if T else 0, _ptr(cs), int(cs.shape[0]), int(style),
+        int(rotary_dim), None if qw is None else _ptr(qw), None if kw is None else _ptr(kw),
+        float(norm_eps), _ptr(q_out), int(q_out.shape[1]), _ptr(pool))
     return int(st), q_out
 
 

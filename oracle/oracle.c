@@ -323,3 +323,93 @@ void orc_f32_to_e4m3_array(const float* x, int64_t n, uint8_t* out) {
 void orc_e4m3_to_f64_array(const uint8_t* c, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_to_f64(c[i]);
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* Variants of the append (adg.csdn.net/69730cc6 section 1.1: several RoPE variants, QK       */
+/* LayerNorm; "TensorRT-LLM 源码完全拆解(一)" kernel list: fused QK-norm + RoPE).  Readings:     */
+/*   style 0 = GPT-NeoX rotate-half: pairs (x_j, x_{j+r/2}), j < r/2;                          */
+/*   style 1 = GPT-J interleaved:    pairs (x_{2j}, x_{2j+1}), j < r/2;                         */
+/*   r = rotary dims (a multiple of 16, <= D), theta_j = base^(-2j/r); dims >= r pass through;  */
+/*   QK-norm = RMSNorm over each q / k head before the rotation:                               */
+/*     y_d = fp32(fp32(x_d * inv_rms) * w_d), inv_rms = fp32(1 / sqrt(mean(x^2) + eps)),        */
+/*   the mean taken in fp64 (the reference value; the kernel sums in fp32, so outputs with      */
+/*   QK-norm agree to rounding, not bit for bit).  V is never normalised or rotated.            */
+/* ------------------------------------------------------------------------------------------ */
+static void rotate_variant(const float* x, int32_t D, int32_t rot, int32_t style, const float* cs_row, float* y) {
+  for (int d = 0; d < D; ++d) y[d] = x[d];
+  int half = rot / 2;
+  for (int j = 0; j < half; ++j) {
+    int ia = style == 0 ? j : 2 * j;
+    int ib = style == 0 ? j + half : 2 * j + 1;
+    float c = cs_row[2 * j], s = cs_row[2 * j + 1];
+    float a = x[ia], b = x[ib];
+    float bs = b * s, as = a * s;
+    y[ia] = fmaf(a, c, -bs);
+    y[ib] = fmaf(b, c, as);
+  }
+}
+
+static void rms_norm(float* x, int32_t D, const float* w, double eps) {
+  double ss = 0.0;
+  for (int d = 0; d < D; ++d) ss += (double)x[d] * (double)x[d];
+  float inv = (float)(1.0 / sqrt(ss / D + eps));
+  for (int d = 0; d < D; ++d) {
+    float t = x[d] * inv;
+    x[d] = t * w[d];
+  }
+}
+
+int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+                       const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
+                       int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                       int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                       int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
+                       int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
+                       double norm_eps, uint16_t* q_out, int64_t q_out_stride, void* pool) {
+  int D = head_dim, B = tokens_per_block, Hkv = num_kv_heads;
+  int rot = rotary_dim > 0 ? rotary_dim : D;
+  int status = ORC_OK;
+  float* x = (float*)malloc(sizeof(float) * D);
+  float* y = (float*)malloc(sizeof(float) * D);
+  int64_t row = 0;
+  for (int r = 0; r < num_requests; ++r) {
+    for (int i = 0; i < new_len[r]; ++i, ++row) {
+      int64_t pos = (int64_t)past[r] + i;
+      if (pos >= max_pos) { status = ORC_ERR_BAD_ARG; continue; }
+      const float* cs_row = cs + (size_t)pos * (rot / 2) * 2;
+      for (int h = 0; h < num_q_heads; ++h) {
+        for (int d = 0; d < D; ++d) x[d] = orc_bf16_to_f32(q[row * q_stride + (int64_t)h * D + d]);
+        if (q_norm_w) rms_norm(x, D, q_norm_w, norm_eps);
+        rotate_variant(x, D, rot, style, cs_row, y);
+        for (int d = 0; d < D; ++d) q_out[row * q_out_stride + (int64_t)h * D + d] = orc_f32_to_bf16(y[d]);
+      }
+      int logical_block = (int)(pos / B), slot = (int)(pos % B);
+      int blk = logical_block < max_blocks_per_seq
+                    ? block_table[(size_t)r * max_blocks_per_seq + logical_block] : -1;
+      if (blk < 0 || blk >= num_blocks) { status = ORC_ERR_BAD_PAGE; continue; }
+      for (int h = 0; h < Hkv; ++h) {
+        for (int d = 0; d < D; ++d) x[d] = orc_bf16_to_f32(k[row * k_stride + (int64_t)h * D + d]);
+        if (k_norm_w) rms_norm(x, D, k_norm_w, norm_eps);
+        rotate_variant(x, D, rot, style, cs_row, y);
+        for (int d = 0; d < D; ++d) {
+          uint16_t vb = v[row * v_stride + (int64_t)h * D + d];
+          size_t ik = pool_index(blk, 0, slot, h, d, B, Hkv, D);
+          size_t iv = pool_index(blk, 1, slot, h, d, B, Hkv, D);
+          if (kv_is_fp8) {
+            uint8_t* p8 = (uint8_t*)pool;
+            p8[ik] = orc_f32_to_e4m3(y[d] * inv_scale);
+            p8[iv] = orc_f32_to_e4m3(orc_bf16_to_f32(vb) * inv_scale);
+          } else {
+            uint16_t* p16 = (uint16_t*)pool;
+            p16[ik] = orc_f32_to_bf16(y[d]);
+            p16[iv] = vb;
+          }
+        }
+      }
+    }
+  }
+  free(x);
+  free(y);
+  return status;
+}

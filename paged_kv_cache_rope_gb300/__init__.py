@@ -39,6 +39,7 @@ EXPORTS = (
     "paged_rope_table_bytes",
     "paged_rope_table_build",
     "paged_kv_append_rope",
+    "paged_kv_append_rope_ex",
     "paged_attention_workspace_size",
     "paged_attention_forward",
     "paged_attention_forward_noalloc",
@@ -86,6 +87,8 @@ def lib() -> C.CDLL:
         L.paged_rope_table_build.restype = C.c_int
         L.paged_kv_append_rope.argtypes = [P, P, i32, P, i64, P, i64, P, i64, P, i64, P, i32, P, P]
         L.paged_kv_append_rope.restype = C.c_int
+        L.paged_kv_append_rope_ex.argtypes = [P, P, i32, P, i64, P, i64, P, i64, P, i64, P, i32, P, P, P]
+        L.paged_kv_append_rope_ex.restype = C.c_int
         L.paged_attention_workspace_size.argtypes = [P, P, i32]
         L.paged_attention_workspace_size.restype = sz
         L.paged_attention_forward.argtypes = [P, P, i32, P, i64, P, C.c_float, P, sz, P, P]
@@ -203,6 +206,37 @@ def paged_kv_append_rope(pool: KVPool, batch: BatchMeta, num_q_heads: int, q: to
         _ptr(v), v.stride(0), _ptr(q_out), q_out.stride(0), _ptr(rope_table),
         int(rope_table.shape[0]), _ptr(d_error), _stream_ptr(stream))
     _check(code, "paged_kv_append_rope")
+
+
+PKV_ROPE_NEOX = 0
+PKV_ROPE_GPTJ = 1
+
+
+class PkvAppendOpts(C.Structure):
+    _fields_ = [("rope_style", C.c_int32), ("rotary_dim", C.c_int32), ("q_norm_weight", C.c_void_p),
+                ("k_norm_weight", C.c_void_p), ("norm_eps", C.c_float)]
+
+
+def paged_kv_append_rope_ex(pool: KVPool, batch: BatchMeta, num_q_heads: int, q: torch.Tensor,
+                            k: torch.Tensor, v: torch.Tensor, q_out: torch.Tensor,
+                            rope_table: torch.Tensor, d_error: torch.Tensor, *, rope_style: int = 0,
+                            rotary_dim: int = 0, q_norm_weight: torch.Tensor | None = None,
+                            k_norm_weight: torch.Tensor | None = None, norm_eps: float = 1e-6,
+                            stream=None) -> None:
+    """Append with RoPE variants (rotate-half / interleaved, partial rotary) and optional
+    RMSNorm of q / k heads; ``rope_table`` must have rotary_dim / 2 pairs per position."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_out", q_out)):
+        assert t.dtype == torch.bfloat16 and t.dim() == 2 and t.stride(1) == 1, name
+    for w in (q_norm_weight, k_norm_weight):
+        assert w is None or (w.dtype == torch.float32 and w.is_contiguous())
+    opts = PkvAppendOpts(int(rope_style), int(rotary_dim), _ptr(q_norm_weight), _ptr(k_norm_weight),
+                         float(norm_eps))
+    pc, bc = pool.c(), batch.c()
+    code = lib().paged_kv_append_rope_ex(
+        C.byref(pc), C.byref(bc), int(num_q_heads), _ptr(q), q.stride(0), _ptr(k), k.stride(0),
+        _ptr(v), v.stride(0), _ptr(q_out), q_out.stride(0), _ptr(rope_table),
+        int(rope_table.shape[0]), C.byref(opts), _ptr(d_error), _stream_ptr(stream))
+    _check(code, "paged_kv_append_rope_ex")
 
 
 def paged_attention_workspace_size(pool: KVPool, batch: BatchMeta, num_q_heads: int) -> int:

@@ -258,6 +258,14 @@ int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t n
                          int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
                          int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
                          int32_t max_pos, int32_t* d_error, pkv_stream_t stream) {
+  return paged_kv_append_rope_ex(pool, batch, num_q_heads, q, q_row_stride, k, k_row_stride, v, v_row_stride,
+                                 q_out, q_out_row_stride, rope_table, max_pos, nullptr, d_error, stream);
+}
+
+int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q,
+                            int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                            int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
+                            int32_t max_pos, const pkv_append_opts* opts, int32_t* d_error, pkv_stream_t stream) {
   g_last_launches = 0;
   int st = validate_pool(pool);
   if (st) return st;
@@ -277,6 +285,14 @@ int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t n
   for (int r = 0; r < hp.R; ++r)
     if (static_cast<int64_t>(batch->h_past_kv_lengths[r]) + batch->h_context_lengths[r] > max_pos) return PKV_ERR_CAPACITY;
   if (hp.R > 12000) return PKV_ERR_UNSUPPORTED;  // in-CTA prefix scan keeps R + 1 ints in shared memory
+  const int style = opts ? opts->rope_style : PKV_ROPE_NEOX;
+  const int rot = (opts && opts->rotary_dim) ? opts->rotary_dim : D;
+  if (style != PKV_ROPE_NEOX && style != PKV_ROPE_GPTJ) return PKV_ERR_UNSUPPORTED;
+  if (rot < 16 || rot > D || (rot & 15)) return PKV_ERR_UNSUPPORTED;
+  if (opts && ((opts->q_norm_weight && !aligned16(opts->q_norm_weight)) ||
+               (opts->k_norm_weight && !aligned16(opts->k_norm_weight))))
+    return PKV_ERR_ALIGNMENT;
+  if (opts && !(opts->norm_eps >= 0.f && std::isfinite(opts->norm_eps))) return PKV_ERR_INVALID_ARGUMENT;
 
   pkv::AppendParams p{};
   p.R = hp.R;
@@ -297,6 +313,11 @@ int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t n
   p.q_out_stride = q_out_row_stride;
   p.rope = reinterpret_cast<const float2*>(rope_table);
   p.max_pos = max_pos;
+  p.style = style;
+  p.rot = rot;
+  p.q_norm_w = opts ? opts->q_norm_weight : nullptr;
+  p.k_norm_w = opts ? opts->k_norm_weight : nullptr;
+  p.norm_eps = opts ? opts->norm_eps : 0.f;
   p.pool = pool->pool;
   p.inv_scale = pool->kv_scale_orig_quant;
   p.ctx_len = batch->d_context_lengths;

@@ -6,8 +6,10 @@
 // embedding); "TensorRT-LLM 源码完全拆解(一)", "KVCacheManager 的三个对外接口" (pool layout
 // [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim]).
 //
-// HBM-bound.  One thread handles 8 rotation pairs (x_j .. x_{j+7}, x_{j+D/2} .. x_{j+D/2+7}) of
-// one head of one token: two 16-byte loads, two 16-byte stores (8-byte stores into an FP8 pool).
+// HBM-bound.  One thread handles 16 elements of one head of one token (8 rotation pairs, or a
+// pass-through part of a partially rotated head): two 16-byte loads, two 16-byte stores (8-byte
+// stores into an FP8 pool).  Variants: rotate-half or interleaved pairs, partial rotary dims,
+// and an optional RMSNorm of q / k heads reduced across the head's lanes with shuffles.
 // Threads of a warp cover consecutive heads of the same token, so every row read and written
 // is a run of full 32-byte sectors.  The token -> request map comes from an in-CTA prefix scan
 // of context_lengths (no workspace needed).
@@ -30,16 +32,16 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// Rotate 8 pairs with the fixed fp32 recipe: y_lo = fma(lo, c, -(hi*s)), y_hi = fma(hi, c, lo*s).
-__device__ __forceinline__ void rotate8(const U16x8& lo, const U16x8& hi, const float2* cs,
+// Rotate 8 rotate-half pairs (lo[e], hi[e]) with the fixed fp32 recipe:
+// y_lo = fma(lo, c, -(hi*s)), y_hi = fma(hi, c, lo*s).
+__device__ __forceinline__ void rotate8(const float (&lo)[8], const float (&hi)[8], const float2* cs,
                                         float (&ylo)[8], float (&yhi)[8]) {
   const float4* cs4 = reinterpret_cast<const float4*>(cs);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     float4 t = __ldg(cs4 + e);
-    float c0 = t.x, s0 = t.y, c1 = t.z, s1 = t.w;
-    float a0 = bf16_bits_to_f32(lo.v[2 * e]), b0 = bf16_bits_to_f32(hi.v[2 * e]);
-    float a1 = bf16_bits_to_f32(lo.v[2 * e + 1]), b1 = bf16_bits_to_f32(hi.v[2 * e + 1]);
+    const float c0 = t.x, s0 = t.y, c1 = t.z, s1 = t.w;
+    const float a0 = lo[2 * e], b0 = hi[2 * e], a1 = lo[2 * e + 1], b1 = hi[2 * e + 1];
     ylo[2 * e] = __fmaf_rn(a0, c0, -__fmul_rn(b0, s0));
     yhi[2 * e] = __fmaf_rn(b0, c0, __fmul_rn(a0, s0));
     ylo[2 * e + 1] = __fmaf_rn(a1, c1, -__fmul_rn(b1, s1));
@@ -116,16 +118,22 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
     return;
   }
 
-  const int D = p.D, half = D >> 1, per_head = D >> 4;  // 8-pair tasks per head
+  // Each lane handles 16 elements of one head of one token: two groups of 8 (A and B) whose
+  // place depends on the rope style; heads of a token are consecutive tasks, so the lanes of one
+  // head are D/16 consecutive lanes of a warp (D/16 divides 32) -- the norm reduces over them.
+  const int D = p.D, per_head = D >> 4;
+  const int rot_tasks = p.rot >> 4, rhalf = p.rot >> 1;
   const int tasks_per_token = (p.Hq + 2 * p.Hkv) * per_head;
   const int64_t total = static_cast<int64_t>(p.T) * tasks_per_token;
   const size_t esz = FP8 ? 1 : 2;
-  for (int64_t gi = static_cast<int64_t>(blockIdx.x) * kAppendThreads + tid; gi < total;
-       gi += static_cast<int64_t>(gridDim.x) * kAppendThreads) {
-    const int token = static_cast<int>(gi / tasks_per_token);
-    int task = static_cast<int>(gi - static_cast<int64_t>(token) * tasks_per_token);
-    // request of this token: largest r with s_cu[r] <= token
-    int lo = 0, hi = p.R - 1;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kAppendThreads;
+  for (int64_t wbase = static_cast<int64_t>(blockIdx.x) * kAppendThreads + (tid & ~31); wbase < total;
+       wbase += stride) {  // warp-uniform loop: inactive lanes still join the norm shuffles
+    const int64_t gi = wbase + lane;
+    const bool active = gi < total;
+    const int token = active ? static_cast<int>(gi / tasks_per_token) : 0;
+    int task = active ? static_cast<int>(gi - static_cast<int64_t>(token) * tasks_per_token) : 0;
+    int lo = 0, hi = p.R - 1;  // request of this token: largest r with s_cu[r] <= token
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
       if (s_cu[mid] <= token) lo = mid;
@@ -133,59 +141,118 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
     }
     const int r = lo;
     const int pos = __ldg(p.past + r) + (token - s_cu[r]);
-    if (pos < 0 || pos >= p.max_pos) {  // device lengths disagree with the host-checked ones
+    bool ok = active;
+    if (active && (pos < 0 || pos >= p.max_pos)) {  // device lengths disagree with the host-checked ones
       flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
-      continue;
+      ok = false;
     }
-    const float2* cs = p.rope + static_cast<size_t>(pos) * half;
-    if (task < p.Hq * per_head) {  // ---- Q head: rotate, bf16 out ----
-      const int h = task / per_head, j0 = (task - h * per_head) * 8;
-      const uint16_t* src = p.q + token * p.q_stride + h * D;
-      U16x8 lo8 = *reinterpret_cast<const U16x8*>(src + j0);
-      U16x8 hi8 = *reinterpret_cast<const U16x8*>(src + half + j0);
-      float ylo[8], yhi[8];
-      rotate8(lo8, hi8, cs + j0, ylo, yhi);
+    // kind: 0 = q, 1 = k, 2 = v; head h; task t within the head
+    int kind = 0;
+    if (task >= p.Hq * per_head) {
+      task -= p.Hq * per_head;
+      kind = 1;
+      if (task >= p.Hkv * per_head) {
+        task -= p.Hkv * per_head;
+        kind = 2;
+      }
+    }
+    const int h = task / per_head, t = task - h * per_head;
+    const bool rotate = kind != 2 && t < rot_tasks;
+    int offA, offB;  // element offsets of the two 8-element groups inside the head
+    if (p.style == 0 && t < rot_tasks) {
+      offA = 8 * t;
+      offB = rhalf + 8 * t;
+    } else {
+      const int base = (p.style == 0) ? p.rot + 16 * (t - rot_tasks) : 16 * t;
+      offA = base;
+      offB = base + 8;
+    }
+    const uint16_t* src = (kind == 0 ? p.q + token * p.q_stride : kind == 1 ? p.k + token * p.k_stride
+                                                                          : p.v + token * p.v_stride) +
+                          h * D;
+    U16x8 a8 = {}, b8 = {};
+    if (ok) {
+      a8 = *reinterpret_cast<const U16x8*>(src + offA);
+      b8 = *reinterpret_cast<const U16x8*>(src + offB);
+    }
+    float xa[8], xb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      xa[e] = bf16_bits_to_f32(a8.v[e]);
+      xb[e] = bf16_bits_to_f32(b8.v[e]);
+    }
+    // ---- optional RMSNorm of q / k heads (uniform per warp group of D/16 lanes) ----
+    const float* nw = kind == 0 ? p.q_norm_w : kind == 1 ? p.k_norm_w : nullptr;
+    if (__any_sync(0xffffffffu, nw != nullptr)) {  // every lane shuffles; xor stays inside a head
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = __fmaf_rn(xa[e], xa[e], __fmaf_rn(xb[e], xb[e], ss));
+      for (int m = 1; m < per_head; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      if (nw != nullptr) {
+        const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), p.norm_eps)));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          xa[e] = __fmul_rn(__fmul_rn(xa[e], inv), __ldg(nw + offA + e));
+          xb[e] = __fmul_rn(__fmul_rn(xb[e], inv), __ldg(nw + offB + e));
+        }
+      }
+    }
+    if (!ok) continue;
+    // ---- rotation: the fixed fp32 recipe y_a = fma(a, c, -(b*s)), y_b = fma(b, c, a*s) ----
+    float ya[8], yb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ya[e] = xa[e];
+      yb[e] = xb[e];
+    }
+    if (rotate) {
+      const float2* cs = p.rope + static_cast<size_t>(pos) * rhalf + 8 * t;
+      if (p.style == 0) {
+        rotate8(xa, xb, cs, ya, yb);
+      } else {
+        float c[8], sn[8];
+        const float4* cs4 = reinterpret_cast<const float4*>(cs);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 f = __ldg(cs4 + e);
+          c[2 * e] = f.x;
+          sn[2 * e] = f.y;
+          c[2 * e + 1] = f.z;
+          sn[2 * e + 1] = f.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {  // pairs (xa[2e], xa[2e+1]) then (xb[2e], xb[2e+1])
+          ya[2 * e] = __fmaf_rn(xa[2 * e], c[e], -__fmul_rn(xa[2 * e + 1], sn[e]));
+          ya[2 * e + 1] = __fmaf_rn(xa[2 * e + 1], c[e], __fmul_rn(xa[2 * e], sn[e]));
+          yb[2 * e] = __fmaf_rn(xb[2 * e], c[4 + e], -__fmul_rn(xb[2 * e + 1], sn[4 + e]));
+          yb[2 * e + 1] = __fmaf_rn(xb[2 * e + 1], c[4 + e], __fmul_rn(xb[2 * e], sn[4 + e]));
+        }
+      }
+    }
+    if (kind == 0) {
       uint16_t* dst = p.q_out + token * p.q_out_stride + h * D;
-      *reinterpret_cast<U16x8*>(dst + j0) = to_bf16x8(ylo);
-      *reinterpret_cast<U16x8*>(dst + half + j0) = to_bf16x8(yhi);
+      *reinterpret_cast<U16x8*>(dst + offA) = to_bf16x8(ya);
+      *reinterpret_cast<U16x8*>(dst + offB) = to_bf16x8(yb);
       continue;
     }
-    task -= p.Hq * per_head;
-    const int is_v = task >= p.Hkv * per_head;
-    if (is_v) task -= p.Hkv * per_head;
-    const int h = task / per_head, j0 = (task - h * per_head) * 8;
-    const int lb = pos / p.B, slot = pos - lb * p.B;
+    const int lb = pos >> (31 - __clz(p.B)), slot = pos & (p.B - 1);
     const int page = lb < p.max_blocks ? __ldg(p.tbl + static_cast<size_t>(r) * p.max_blocks + lb) : -1;
     if (page < 0 || page >= p.NB) {
       flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
       continue;
     }
+    const int is_v = kind == 2;
     const size_t elem = ((static_cast<size_t>(page) * 2 + is_v) * p.B + slot) * p.Hkv * D + static_cast<size_t>(h) * D;
     uint8_t* dst = static_cast<uint8_t*>(p.pool) + elem * esz;
-    const uint16_t* src = (is_v ? p.v + token * p.v_stride : p.k + token * p.k_stride) + h * D;
-    U16x8 lo8 = *reinterpret_cast<const U16x8*>(src + j0);
-    U16x8 hi8 = *reinterpret_cast<const U16x8*>(src + half + j0);
-    float ylo[8], yhi[8];
-    if (!is_v) {
-      rotate8(lo8, hi8, cs + j0, ylo, yhi);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ylo[e] = bf16_bits_to_f32(lo8.v[e]);
-        yhi[e] = bf16_bits_to_f32(hi8.v[e]);
-      }
-    }
     if constexpr (FP8) {
-      *reinterpret_cast<uint2*>(dst + j0) = to_e4m3x8(ylo, p.inv_scale);
-      *reinterpret_cast<uint2*>(dst + half + j0) = to_e4m3x8(yhi, p.inv_scale);
+      *reinterpret_cast<uint2*>(dst + offA) = to_e4m3x8(ya, p.inv_scale);
+      *reinterpret_cast<uint2*>(dst + offB) = to_e4m3x8(yb, p.inv_scale);
+    } else if (is_v) {  // V is stored as given
+      *reinterpret_cast<U16x8*>(dst + 2 * offA) = a8;
+      *reinterpret_cast<U16x8*>(dst + 2 * offB) = b8;
     } else {
-      if (is_v) {  // V is stored as given
-        *reinterpret_cast<U16x8*>(dst + 2 * j0) = lo8;
-        *reinterpret_cast<U16x8*>(dst + 2 * (half + j0)) = hi8;
-      } else {
-        *reinterpret_cast<U16x8*>(dst + 2 * j0) = to_bf16x8(ylo);
-        *reinterpret_cast<U16x8*>(dst + 2 * (half + j0)) = to_bf16x8(yhi);
-      }
+      *reinterpret_cast<U16x8*>(dst + 2 * offA) = to_bf16x8(ya);
+      *reinterpret_cast<U16x8*>(dst + 2 * offB) = to_bf16x8(yb);
     }
   }
 }

@@ -40,8 +40,12 @@ struct AppendParams {
   int64_t v_stride;
   uint16_t* q_out;
   int64_t q_out_stride;
-  const float2* rope;  // [max_pos, D/2]
+  const float2* rope;  // [max_pos, rot/2]
   int32_t max_pos;
+  int32_t style, rot;  // rope style (0 rotate-half, 1 interleaved), rotated dims per head
+  const float* q_norm_w;  // RMSNorm weights [D] or null
+  const float* k_norm_w;
+  float norm_eps;
   void* pool;
   float inv_scale;
   const int32_t* ctx_len;

@@ -434,3 +434,101 @@ def test_temperature_example_from_the_pages():
         assert np.max(np.abs(probs - exact)) < 1e-12
         if asserted:
             assert [round(float(p), 2) for p in probs] == printed
+
+
+# ----------------------------------------------------------------------------------------------
+# append variants: RoPE styles, partial rotary, QK RMSNorm
+# ----------------------------------------------------------------------------------------------
+
+def _variant_append(b, pool_np, **kw):
+    rot = kw.get("rotary_dim", 0) or b.head_dim
+    cs = oracle.rope_table(b.rope_base, rot, b.max_pos)
+    return oracle.append_rope_ex(
+        new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
+        num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
+        num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8", inv_scale=b.inv_scale,
+        q_bits=_np_bits(b.q), k_bits=_np_bits(b.k), v_bits=_np_bits(b.v), cs=cs, pool=pool_np, **kw)
+
+
+def test_variant_defaults_equal_plain_append():
+    b = _small_mixed()
+    p1, p2 = _np_bits(b.pool).copy(), _np_bits(b.pool).copy()
+    _, q1 = _run_append(b, p1)
+    _, q2 = _variant_append(b, p2)
+    assert np.array_equal(q1, q2) and np.array_equal(p1, p2)
+
+
+def test_gptj_interleaved_unit_vectors():
+    """Interleaved pairs: e_{2j} -> cos at 2j, sin at 2j+1; e_{2j+1} -> -sin at 2j, cos at 2j+1."""
+    D, p = 64, 23
+    b = W.make_batch(name="gptj", ctx=[], gen=[p + 1], num_q_heads=1, num_kv_heads=1, head_dim=D,
+                     tokens_per_block=16, seed=2)
+    cs = oracle.rope_table(b.rope_base, D, p + 1)
+    for j in (0, 7, D // 2 - 1):
+        for which, expect in ((2 * j, (cs[p, j, 0], cs[p, j, 1])), (2 * j + 1, (-cs[p, j, 1], cs[p, j, 0]))):
+            e = np.zeros((1, D), np.float32)
+            e[0, which] = 1.0
+            import dataclasses
+            bb = dataclasses.replace(b, q=torch.from_numpy(e).to(torch.bfloat16))
+            _, q_out = _variant_append(bb, _np_bits(b.pool).copy(), style=1)
+            got = oracle.f32_from_bf16(q_out[0])
+            ref = np.zeros(D, np.float32)
+            ref[2 * j], ref[2 * j + 1] = expect
+            assert np.array_equal(got, oracle.f32_from_bf16(oracle.bf16_from_f32(ref)))
+
+
+@pytest.mark.parametrize("style", [0, 1])
+def test_partial_rotary_passes_the_tail_through(style):
+    b = _small_mixed()
+    rot = 32
+    pool = _np_bits(b.pool).copy()
+    _, q_out = _variant_append(b, pool, style=style, rotary_dim=rot)
+    qb = _np_bits(b.q)
+    D = b.head_dim
+    q3 = q_out.reshape(b.num_tokens, b.num_q_heads, D)
+    q_in = qb.reshape(b.num_tokens, b.num_q_heads, D)
+    assert np.array_equal(q3[:, :, rot:], q_in[:, :, rot:])  # untouched dims, bit for bit
+    # the rotated part equals a standalone rotation of the first rot dims as a head of size rot
+    cs = oracle.rope_table(b.rope_base, rot, b.max_pos)
+    row = 0
+    for r in range(b.num_requests):
+        for i in range(int(b.new_len[r])):
+            pos = int(b.past[r]) + i
+            for h in range(b.num_q_heads):
+                x = oracle.f32_from_bf16(q_in[row, h, :rot])
+                if style == 0:
+                    ref = oracle.rope32(x, cs[pos])
+                else:  # interleaved = rotate-half applied to the de-interleaved vector
+                    perm = np.concatenate([np.arange(0, rot, 2), np.arange(1, rot, 2)])
+                    y = oracle.rope32(x[perm], cs[pos])
+                    ref = np.empty_like(y)
+                    ref[perm] = y
+                assert np.array_equal(q3[row, h, :rot], oracle.bf16_from_f32(ref))
+            row += 1
+
+
+def test_qk_rmsnorm_matches_formula_and_scale_invariance():
+    b = W.make_batch(name="norm", ctx=[(9, 0)], gen=[], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                     tokens_per_block=16, seed=8)  # past 0: position i, no rotation at row 0
+    rng = np.random.default_rng(8)
+    qw, kw = rng.uniform(0.5, 1.5, 64).astype(np.float32), rng.uniform(0.5, 1.5, 64).astype(np.float32)
+    pool = _np_bits(b.pool).copy()
+    _, q_out = _variant_append(b, pool, q_norm_w=qw, k_norm_w=kw, norm_eps=1e-6)
+    x = torch.from_numpy(oracle.f32_from_bf16(_np_bits(b.q)[0]).astype(np.float64)).reshape(4, 64)
+    ref = x / torch.sqrt((x * x).mean(-1, keepdim=True) + 1e-6) * torch.from_numpy(qw).double()
+    got = oracle.f32_from_bf16(q_out[0]).reshape(4, 64).astype(np.float64)
+    ulp = np.spacing(np.abs(ref.numpy()).astype(np.float32)).astype(np.float64) * 2**16  # 1 bf16 ulp
+    assert np.all(np.abs(got - ref.numpy()) <= ulp)
+    # RMSNorm is invariant to scaling the input by a power of two (exact in every format here)
+    import dataclasses
+    b4 = dataclasses.replace(b, q=(b.q.float() * 4).to(torch.bfloat16), k=(b.k.float() * 4).to(torch.bfloat16),
+                             v=(b.v.float() * 4).to(torch.bfloat16))
+    pool4 = _np_bits(b.pool).copy()
+    _, q_out4 = _variant_append(b4, pool4, q_norm_w=qw, k_norm_w=kw, norm_eps=0.0)
+    pool1 = _np_bits(b.pool).copy()
+    _, q_out1 = _variant_append(b, pool1, q_norm_w=qw, k_norm_w=kw, norm_eps=0.0)
+    assert np.array_equal(q_out4, q_out1)
+    view4 = pool4.reshape(b.num_blocks, 2, 16, 2, 64)
+    view1 = pool1.reshape(b.num_blocks, 2, 16, 2, 64)
+    assert np.array_equal(view4[:, 0], view1[:, 0])        # K normalised: identical
+    assert not np.array_equal(view4[:, 1], view1[:, 1])    # V is never normalised (stays 4x)
