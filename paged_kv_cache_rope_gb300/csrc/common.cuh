@@ -111,6 +111,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// 2^x with the MUFU instruction alone (flush-to-zero; relative error ~2^-22, and results below
+// 2^-126 -- probabilities of masked or vanishing keys -- become 0).  -inf gives 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float warp_max_xor(float v, int mask) {
   return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, mask));
 }

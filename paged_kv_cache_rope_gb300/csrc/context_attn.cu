@@ -328,7 +328,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         m_use = m_new;  // O is still empty
       } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
         // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
-        const float f = exp2f(m_run - m_new);
+        const float f = ex2_approx(m_run - m_new);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -347,8 +347,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = exp2f(fmaf(__uint_as_float(v[e]), sl2, -m_use));
-          const float p1 = exp2f(fmaf(__uint_as_float(v[e + 1]), sl2, -m_use));
+          const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m_use));
           ls[c] += p0 + p1;
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }

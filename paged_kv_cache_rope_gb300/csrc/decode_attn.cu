@@ -410,7 +410,7 @@ decode_splitkv_kernel(DecodeParams p) {
       }
       const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
       if (__any_sync(0xffffffffu, mn0 != m_run[nt][0] || mn1 != m_run[nt][1])) {
-        const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+        const float al0 = ex2_approx(m_run[nt][0] - mn0), al1 = ex2_approx(m_run[nt][1] - mn1);
         l_run[nt][0] *= al0;
         l_run[nt][1] *= al1;
 #pragma unroll
@@ -425,8 +425,8 @@ decode_splitkv_kernel(DecodeParams p) {
       }
 #pragma unroll
       for (int u = 0; u < SUB; ++u) {
-        const float p0 = exp2f(sv[u][0] - mn0), p1 = exp2f(sv[u][1] - mn1);
-        const float p2 = exp2f(sv[u][2] - mn0), p3 = exp2f(sv[u][3] - mn1);
+        const float p0 = ex2_approx(sv[u][0] - mn0), p1 = ex2_approx(sv[u][1] - mn1);
+        const float p2 = ex2_approx(sv[u][2] - mn0), p3 = ex2_approx(sv[u][3] - mn1);
         l_run[nt][0] += p0 + p2;
         l_run[nt][1] += p1 + p3;
         if constexpr (!FP8) {
@@ -539,7 +539,7 @@ decode_splitkv_kernel(DecodeParams p) {
     float acc = 0.f, lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < Cfg::kWarps; ++w) {
-      const float f = exp2f(sm_m[w * HN + hl] - M);
+      const float f = ex2_approx(sm_m[w * HN + hl] - M);
       acc += f * sm_o[(w * HN + hl) * D + d];
       lsum += f * sm_l[w * HN + hl];
     }
@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
     const float2 m_l = ml[static_cast<int64_t>(s) * p.Hq];
     const float4 v = active ? po[s * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float Mn = fmaxf(M, m_l.x);
-    const float a = exp2f(M - Mn), b = exp2f(m_l.x - Mn);
+    const float a = ex2_approx(M - Mn), b = ex2_approx(m_l.x - Mn);
     acc.x = acc.x * a + v.x * b;
     acc.y = acc.y * a + v.y * b;
     acc.z = acc.z * a + v.z * b;
@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
   float lt = 0.f;
 #pragma unroll
   for (int w = 0; w < kCombineWarps; ++w) {
-    const float f = exp2f(s_ml[w].x - Mt);  // a warp with no splits has M = -inf: f = 0
+    const float f = ex2_approx(s_ml[w].x - Mt);  // a warp with no splits has M = -inf: f = 0
     const float4 a4 = s_acc[w][lane];
     o.x += f * a4.x;
     o.y += f * a4.y;
