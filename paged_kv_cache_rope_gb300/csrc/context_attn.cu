@@ -316,11 +316,11 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        mx[0] = fmaxf(mx[0], __uint_as_float(v0[e]));
-        mx[1] = fmaxf(mx[1], __uint_as_float(v1[e]));
-        mx[2] = fmaxf(mx[2], __uint_as_float(v2[e]));
-        mx[3] = fmaxf(mx[3], __uint_as_float(v3[e]));
+      for (int e = 0; e < 32; e += 2) {
+        mx[0] = max3f(mx[0], __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
+        mx[1] = max3f(mx[1], __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
+        mx[2] = max3f(mx[2], __uint_as_float(v2[e]), __uint_as_float(v2[e + 1]));
+        mx[3] = max3f(mx[3], __uint_as_float(v3[e]), __uint_as_float(v3[e + 1]));
       }
       const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
       float m_use = m_run;
@@ -342,15 +342,16 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       }
       m_run = m_use;
       // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
       auto emit = [&](uint32_t(&v)[32], int c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m_use));
-          ls[c] += p0 + p1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
+          const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
+          const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+          ls[c] = fadd2(ls[c], pv);
+          pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
         }
         tc::tmem_st16(tS + 16 * c, pk);
       };
@@ -358,7 +359,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       emit(v1, 1);
       emit(v2, 2);
       emit(v3, 3);
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+      l_run += lsum.x + lsum.y;
       tc::tmem_wait_st();
       if (j == nT - 1 && x == zero_x) {
         // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
