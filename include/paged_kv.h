@@ -16,9 +16,11 @@
  *   - All pointers named d_* and all tensor pointers (q, k, v, q_out, out, pool, rope table,
  *     workspace, error word) are DEVICE pointers; h_* pointers are HOST pointers.
  *   - The caller owns every buffer.  The library allocates no device memory, keeps no state
- *     between calls other than cached device attributes, and never synchronises the stream:
- *     each call only enqueues kernels on `stream` and returns (same-stream FIFO ordering as in
- *     [NOTES] 五 "完整的推理流程", 5.2 CPU/GPU Overlap).
+ *     between calls other than cached device attributes and one auxiliary stream with two
+ *     events per device (created on first use, see paged_attention_forward), and never
+ *     synchronises a stream: each call only enqueues kernels and returns, and its effects are
+ *     ordered on `stream` like one kernel's (same-stream FIFO ordering as in [NOTES] 五
+ *     "完整的推理流程", 5.2 CPU/GPU Overlap).
  *   - Return value: PKV_OK (0) or a negative PKV_ERR_* detected on the host before anything
  *     was enqueued.  Errors only the device can see (a page id outside [0, num_blocks), a
  *     bounded wait that ran out) are OR-ed as PKV_DEVERR_* bits into the caller's device int
@@ -203,7 +205,14 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  *   d_error      device int32 error bits as above
  * Context rows use a tcgen05/TMEM tensor-core kernel (for FP8 pools after staging the context
  * requests' pages as exact bf16 code values in the workspace), generation rows a split-KV decode
- * kernel plus a log-sum-exp combine; all launches go to `stream`.  T == 0 is a no-op.
+ * kernel plus a log-sum-exp combine.  When the batch has both kinds of rows, the generation
+ * kernels run on the library's auxiliary stream for this device (highest stream priority),
+ * forked from `stream` by an event after the planning kernel and joined back into it before
+ * the call returns, so that they share the GPU with the context kernel; every other launch goes
+ * to `stream`.  The auxiliary stream is created by the first such call that is not made under
+ * stream capture (calls made before that, and calls made while paged_kv_set_kernel_events is
+ * set, run everything on `stream`); the fork and join are captured like any other stream work.
+ * T == 0 is a no-op.
  */
 int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
                             const void* q_rot, int64_t q_row_stride, void* out,
@@ -241,7 +250,9 @@ const char* paged_kv_last_launch_name(int32_t i);
  * Optional per-kernel timing for profiling harnesses.  `events` points to 2 * max_kernels
  * cudaEvent_t handles (created by the caller, host array owned by the caller and kept alive
  * while set).  Every later call on this thread records events[2i] on the stream just before
- * its i-th kernel and events[2i + 1] just after it, for i < max_kernels.  NULL turns it off.
+ * its i-th kernel and events[2i + 1] just after it, for i < max_kernels.  While events are
+ * set, every kernel of a call goes to the caller's stream (no overlap of context and generation
+ * kernels), so that each pair brackets one kernel alone.  NULL turns it off.
  * Returns PKV_OK or PKV_ERR_INVALID_ARGUMENT.
  */
 int paged_kv_set_kernel_events(void* const* events, int32_t max_kernels);

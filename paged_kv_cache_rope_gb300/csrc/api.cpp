@@ -1,6 +1,7 @@
 // api.cpp -- C-ABI front end of libpaged_kv.so: argument validation, launch planning and
-// dispatch.  Everything here runs on the host and only enqueues work on the caller's stream;
-// no device memory is allocated and the stream is never synchronised.
+// dispatch.  Everything here runs on the host and only enqueues work on the caller's stream
+// (and, for mixed batches, on an auxiliary stream forked from and joined back into it); no
+// device memory is allocated and no stream is ever synchronised.
 //
 // Dispatch follows "TensorRT-LLM 1.0 源码学习笔记" 6.1 "两者分工": context requests (input length
 // > 1, and chunked-context requests) go to the flash-attention style tensor-core kernel,
@@ -184,7 +185,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   L.cu_q = 0;
   L.tile_prefix = L.cu_q + hp->R + 1;
   L.split_prefix = L.tile_prefix + hp->C + 1;
-  L.stage_prefix = L.split_prefix + hp->G + 1;
+  L.unit_order = L.split_prefix + hp->G + 1;
+  L.stage_prefix = L.unit_order + hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
   L.int_words = L.stage_tbl + (staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
   L.stage_pages = 0;
@@ -201,6 +203,63 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// A batch with both context and generation rows runs its generation kernels (HBM-bound) on an
+// auxiliary stream of the device's highest priority, beside the context kernel (tensor-bound)
+// on the caller's stream; the auxiliary stream is forked from and joined back into the
+// caller's stream with events.  Whenever an SM frees up, pending generation CTAs are placed
+// first, so the long context units fill the rest of the machine.  (Measured against the
+// context kernel on the auxiliary stream, at default or high priority: this order gave the
+// shortest mixed steps.)  One stream and event pair per device, created on first use and kept
+// for the life of the process; `lock` is held from the fork's record to the join's wait so
+// that calls from several host threads never interleave on the shared events.
+struct AuxStream {
+  std::mutex lock;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+
+AuxStream* aux_stream_for_current_device(cudaStream_t caller) {
+  static AuxStream aux[64];
+  static std::mutex create_lock;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  AuxStream* a = &aux[dev];
+  std::lock_guard<std::mutex> g(create_lock);
+  if (!a->tried) {
+    // creating a stream is not a stream operation, but stay clear of it while the caller's
+    // stream is being captured: such a call keeps the single-stream order until the next
+    // uncaptured call has created the pair
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+    a->tried = true;
+    int lo = 0, hi = 0;
+    cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (cudaStreamCreateWithPriority(&a->stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a->join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      a->stream = nullptr;
+    }
+  }
+  return a->stream ? a : nullptr;
+}
+
+// Joins the auxiliary stream back into the caller's stream when the call returns, on error
+// paths too, so that a capture never ends with forked work left over.
+struct AuxJoin {
+  AuxStream* aux;
+  cudaStream_t caller;
+  bool join() {
+    if (!aux) return true;
+    const bool ok = cudaEventRecord(aux->join, aux->stream) == cudaSuccess &&
+                    cudaStreamWaitEvent(caller, aux->join, 0) == cudaSuccess;
+    aux = nullptr;
+    return ok;
+  }
+  ~AuxJoin() { join(); }
+};
 
 }  // namespace
 
@@ -372,6 +431,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.T = hp.T;
   pp.Hkv = Hkv;
   pp.B = pool->tokens_per_block;
+  pp.Hq = num_q_heads;
   pp.expect_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
   pp.expect_tiles = hp.num_tiles;
   pp.expect_splits = hp.num_splits;
@@ -390,6 +450,21 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   }
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   ++launches;
+
+  // generation work on the auxiliary stream when a context kernel runs beside it; while the
+  // caller has per-kernel timing events set, every kernel stays on `stream` so that each pair
+  // of events brackets one kernel's own work
+  AuxStream* aux = (hp.C > 0 && hp.G > 0 && !g_events) ? aux_stream_for_current_device(s) : nullptr;
+  std::unique_lock<std::mutex> aux_hold;
+  const cudaStream_t cs = s;  // context kernels
+  cudaStream_t gs = s;        // generation kernels
+  if (aux) {
+    aux_hold = std::unique_lock<std::mutex>(aux->lock);
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess) return PKV_ERR_CUDA;
+    gs = aux->stream;
+  }
+  AuxJoin aux_join{aux, s};
 
   if (hp.C > 0) {
     // FP8 pools: stage the context requests' pages as bf16 first (exact values, own table)
@@ -414,8 +489,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       sp.stage_pool = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + hp.lay.stage_pool);
       sp.d_error = d_error;
       {
-        LaunchScope ls(launches, "stage_fp8", s);
-        e = pkv::launch_stage_fp8(sp, s);
+        LaunchScope ls(launches, "stage_fp8", cs);
+        e = pkv::launch_stage_fp8(sp, cs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;
@@ -442,6 +517,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.num_tiles = hp.num_tiles;
     cp.cu_q = ws + hp.lay.cu_q;
     cp.tile_prefix = ws + hp.lay.tile_prefix;
+    cp.unit_order = ws + hp.lay.unit_order;
     cp.ctx_len = batch->d_context_lengths;
     cp.past = batch->d_past_kv_lengths;
     cp.tbl = ctx_tbl;
@@ -452,8 +528,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.out_scale = fp8 ? pool->kv_scale_quant_orig : 1.0f;
     cp.d_error = d_error;
     {
-      LaunchScope ls(launches, "context_attn", s);
-      e = pkv::launch_context(cp, &qmap, &kvmap, false, s);
+      LaunchScope ls(launches, "context_attn", cs);
+      e = pkv::launch_context(cp, &qmap, &kvmap, false, cs);
     }
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     ++launches;
@@ -486,20 +562,21 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_ml);
     dp.d_error = d_error;
     {
-      LaunchScope ls(launches, "decode_splitkv", s);
-      e = pkv::launch_decode(dp, fp8, s, nullptr);
+      LaunchScope ls(launches, "decode_splitkv", gs);
+      e = pkv::launch_decode(dp, fp8, gs, nullptr);
     }
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     ++launches;
     if (hp.max_splits > 1) {
       {
-        LaunchScope ls(launches, "combine", s);
-        e = pkv::launch_combine(dp, s);
+        LaunchScope ls(launches, "combine", gs);
+        e = pkv::launch_combine(dp, gs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;
     }
   }
+  if (!aux_join.join()) return PKV_ERR_CUDA;  // later work on the caller's stream sees every row
   g_last_launches = launches;
   return PKV_OK;
 }

@@ -95,8 +95,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   const int hk = hq / p.group;
   pdl_wait();
 
-  // ---- which context request / pair of query tiles (heaviest first) ----
-  const int unit = p.num_tiles - 1 - static_cast<int>(blockIdx.y);
+  // ---- which context request / pair of query tiles ----
+  const int unit = __ldg(p.unit_order + blockIdx.y);  // longest units launch first
   int lo = 0, hi = p.C - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
@@ -114,7 +114,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   const int nv0 = max(0, min(128, n_r - i0)), nv1 = max(0, min(128, n_r - i0 - 128));
   const int nkt0 = nv0 > 0 ? (past + i0 + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
   const int nkt1 = nv1 > 0 ? (past + i0 + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
-  if (nv0 <= 0 || unit < 0) {  // plan disagrees with the launch
+  if (nv0 <= 0 || unit < 0 || unit >= p.num_tiles) {  // plan disagrees with the launch
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
     return;
   }

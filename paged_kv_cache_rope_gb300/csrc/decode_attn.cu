@@ -117,6 +117,58 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
            (staging && t.w != p.expect_stage_pages);
   }
   if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+
+  // ---- context units, most KV tiles first: a counting sort by tile count (descending) ----
+  const int U = p.expect_tiles;
+  int32_t* order = p.ws + p.lay.unit_order;
+  if (__syncthreads_or(bad)) {  // lengths disagree with the host plan: identity order, in range
+    for (int u = tid; u < U; u += kPlanThreads) order[u] = u;
+    return;
+  }
+  if (U <= 0) return;
+  constexpr int kBins = 2048;  // units with more tiles share the top bin
+  __shared__ int32_t s_hist[kBins];
+  __shared__ int32_t s_part[kPlanThreads];
+  for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
+  __syncthreads();  // tiles[] (this block's global writes) and the zeroed histogram are visible
+  auto unit_cost = [&](int u) {
+    int lo = 0, hi = C - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tiles[mid] <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    const int n = __ldg(p.ctx_len + lo), i0 = (u - tiles[lo]) * kCtxRowsPerCta;
+    const int keys = __ldg(p.past + lo) + i0 + min(kCtxRowsPerCta, n - i0);
+    return min(kBins - 1, (keys + kCtxTileN - 1) / kCtxTileN);
+  };
+  for (int u = tid; u < U; u += kPlanThreads) atomicAdd(&s_hist[kBins - 1 - unit_cost(u)], 1);
+  __syncthreads();
+  // exclusive scan of the (reversed) histogram: each thread owns kBins / kPlanThreads bins
+  constexpr int kPer = kBins / kPlanThreads;
+  int own = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) own += s_hist[tid * kPer + i];
+  s_part[tid] = own;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int t = 0; t < kPlanThreads; ++t) {
+      const int v = s_part[t];
+      s_part[t] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  int run = s_part[tid];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int v = s_hist[tid * kPer + i];
+    s_hist[tid * kPer + i] = run;
+    run += v;
+  }
+  __syncthreads();
+  for (int u = tid; u < U; u += kPlanThreads) order[atomicAdd(&s_hist[kBins - 1 - unit_cost(u)], 1)] = u;
 }
 
 // --------------------------------------------------------------------------------------------

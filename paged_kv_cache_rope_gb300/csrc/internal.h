@@ -20,6 +20,7 @@ struct PlanLayout {
   int64_t cu_q;          // [R + 1]  exclusive prefix of context_lengths
   int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxRowsPerCta) over context requests
   int64_t split_prefix;  // [G + 1]  prefix of ceil(L_r / kv_chunk) over generation requests
+  int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
   int64_t stage_prefix;  // [C + 1]  FP8 pools: prefix of the context requests' page counts
   int64_t stage_tbl;     // [C * max_blocks] FP8 pools: block table into the bf16 staging pool
   int64_t int_words;     // total int32 words of the plan
@@ -56,6 +57,7 @@ struct AppendParams {
 
 struct PlanParams {
   int32_t R, C, G, T, Hkv, B, expect_tiles, expect_splits, kv_chunk, expect_stage_pages;
+  int32_t Hq;
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words
@@ -83,6 +85,7 @@ struct ContextParams {
   int32_t C, T, Hq, Hkv, group, D, B, NB, max_blocks, num_tiles;
   const int32_t* cu_q;
   const int32_t* tile_prefix;
+  const int32_t* unit_order;  // [num_tiles] launch order of the context units
   const int32_t* ctx_len;
   const int32_t* past;
   const int32_t* tbl;

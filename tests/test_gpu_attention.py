@@ -102,6 +102,22 @@ def test_deterministic_and_page_permutation_invariant():
     assert torch.equal(g1.pool[torch.from_numpy(perm).cuda()].view(torch.int16), g3.pool.view(torch.int16))
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_overlapped_and_serial_schedules_agree(kv_dtype):
+    """A mixed batch runs its generation kernels on the library's auxiliary stream beside the
+    context kernel; with per-kernel timing events set, everything runs on the caller's stream.
+    Each output row is written by one kernel either way, so the two must agree bit for bit."""
+    b = _batch("overlap_" + kv_dtype, [(300, 64), (40, 0)], [900, 45, 3000, 1], 16, 4, 128, 32, kv_dtype)
+    overlapped = gpu_run(b)
+    with pk.KernelEvents(8):
+        serial = gpu_run(b)
+    assert overlapped.error == 0 and serial.error == 0
+    assert torch.equal(overlapped.out, serial.out)
+    o = oracle_run(b)
+    tol = BF16_TOL if kv_dtype == "bf16" else FP8_DEQ_TOL
+    assert max_err(gpu_out_f64(overlapped, b), o.out) <= tol
+
+
 def test_decode_bad_page_sets_error_word():
     b = _batch("badread", [], [100, 300], 8, 2, 128, 32)
     tbl = b.block_table.copy()
@@ -130,8 +146,7 @@ def test_launch_counts():
 def test_prefix_shared_pages(kv_dtype):
     """Prefix reuse: several requests' block tables point at the same physical pages for a
     common cached prefix (read-only); each request's own new tokens land in pages of its own."""
-    ctx = [(70, 96)] if kv_dtype == "bf16" else []
-    b = _batch("shared_" + kv_dtype, ctx, [200, 150, 97], 8, 2, 128, 32, kv_dtype)
+    b = _batch("shared_" + kv_dtype, [(70, 96)], [200, 150, 97], 8, 2, 128, 32, kv_dtype)
     tbl = b.block_table.copy()
     donor = b.num_requests - 1  # the 97-token decode: its first 3 pages hold 96 cached tokens
     for r in range(b.num_requests - 1):

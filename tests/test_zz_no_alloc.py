@@ -32,9 +32,8 @@ def _setup(b: W.Batch):
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
 def test_noalloc_matches_regular_entry_point_twice(kv_dtype):
-    # contexts only with bf16 pools (the context kernel reads bf16); decodes long enough to split
-    ctx = [(300, 64), (37, 0)] if kv_dtype == "bf16" else []
-    b = W.make_batch(name="noalloc", ctx=ctx, gen=[5, 700, 3000, 129], num_q_heads=16, num_kv_heads=4,
+    # two chunked/fresh contexts and decodes long enough to split
+    b = W.make_batch(name="noalloc", ctx=[(300, 64), (37, 0)], gen=[5, 700, 3000, 129], num_q_heads=16, num_kv_heads=4,
                      head_dim=128, tokens_per_block=32, kv_dtype=kv_dtype, seed=21)
     pool, meta, q_out, err = _setup(b)
     ref = torch.empty(b.num_tokens, b.num_q_heads * b.head_dim, dtype=torch.bfloat16, device="cuda")
