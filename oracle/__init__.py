@@ -10,7 +10,9 @@ Functions (all on host numpy arrays):
   rope_table                        fp32 (cos, sin) table computed in fp64
   rope32 / rope64                   GPT-NeoX rotate-half rotation (fp32 recipe / exact fp64)
   append_rope                       O1 write image: q_out rows and pool bytes after the append
+  append_rope_ex                    O1 with RoPE variants, QK-norm and draft-token position offsets
   attention                         O2 fp64 causal GQA attention read through the block table
+                                    (optionally with packed masks for draft-token requests)
 Each C function cites its page and section in oracle.c.
 """
 from __future__ import annotations
@@ -56,6 +58,13 @@ def lib():
         L.orc_attention.argtypes = [i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, P,
                                     P, f64, P, i64, P]
         L.orc_attention.restype = C.c_int
+        L.orc_append_rope_spec.argtypes = [i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                           P, i64, P, i64, P, i64, P, i32, i32, i32, P, P, f64,
+                                           P, P, i64, P]
+        L.orc_append_rope_spec.restype = C.c_int
+        L.orc_attention_spec.argtypes = [i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, P,
+                                         P, f64, P, i64, i32, P, i32, P]
+        L.orc_attention_spec.restype = C.c_int
         L.orc_f32_to_bf16_array.argtypes = [P, i64, P]
         L.orc_f32_to_bf16_array.restype = None
         L.orc_f32_to_e4m3_array.argtypes = [P, i64, P]
@@ -165,9 +174,11 @@ def append_rope(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_d
 def append_rope_ex(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim,
                    tokens_per_block, num_blocks, kv_fp8, inv_scale, q_bits, k_bits, v_bits, cs,
                    pool, style=0, rotary_dim=0, q_norm_w=None, k_norm_w=None, norm_eps=1e-6,
-                   q_out=None):
+                   pos_offset=None, q_out=None):
     """O1 with the variants: style 0 rotate-half / 1 interleaved, rotary_dim (0 = head_dim),
-    optional RMSNorm weights for q and k heads.  ``cs`` has rotary_dim / 2 pairs per row."""
+    optional RMSNorm weights for q and k heads.  ``cs`` has rotary_dim / 2 pairs per row.
+    ``pos_offset`` (int32 [T], one per packed row) rotates row (r, i) for position
+    past_r + pos_offset[row] instead of past_r + i; the slot stays past_r + i."""
     new_len = np.ascontiguousarray(new_len, dtype=np.int32)
     past = np.ascontiguousarray(past, dtype=np.int32)
     tbl = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -180,22 +191,30 @@ def append_rope_ex(*, new_len, past, block_table, num_q_heads, num_kv_heads, hea
         q_out = np.zeros((T, num_q_heads * head_dim), dtype=np.uint16)
     qw = None if q_norm_w is None else np.ascontiguousarray(q_norm_w, dtype=np.float32)
     kw = None if k_norm_w is None else np.ascontiguousarray(k_norm_w, dtype=np.float32)
-    st = lib().orc_append_rope_ex(
-        int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
-        int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
-        int(num_blocks), int(bool(kv_fp8)), float(inv_scale),
-        _ptr(q_bits), int(q_bits.shape[1]) if T else 0, _ptr(k_bits), int(k_bits.shape[1]) if T else 0,
-        _ptr(v_bits), int(v_bits.shape[1]) if T else 0, _ptr(cs), int(cs.shape[0]), int(style),
-        int(rotary_dim), None if qw is None else _ptr(qw), None if kw is None else _ptr(kw),
-        float(norm_eps), _ptr(q_out), int(q_out.shape[1]), _ptr(pool))
+    common = (int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
+              int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
+              int(num_blocks), int(bool(kv_fp8)), float(inv_scale),
+              _ptr(q_bits), int(q_bits.shape[1]) if T else 0, _ptr(k_bits), int(k_bits.shape[1]) if T else 0,
+              _ptr(v_bits), int(v_bits.shape[1]) if T else 0, _ptr(cs), int(cs.shape[0]), int(style),
+              int(rotary_dim), None if qw is None else _ptr(qw), None if kw is None else _ptr(kw),
+              float(norm_eps))
+    if pos_offset is None:
+        st = lib().orc_append_rope_ex(*common, _ptr(q_out), int(q_out.shape[1]), _ptr(pool))
+    else:
+        off = np.ascontiguousarray(pos_offset, dtype=np.int32)
+        assert off.shape == (T,)
+        st = lib().orc_append_rope_spec(*common, _ptr(off), _ptr(q_out), int(q_out.shape[1]), _ptr(pool))
     return int(st), q_out
 
 
 def attention(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim,
               tokens_per_block, num_blocks, kv_fp8, kv_scale, pool, q, softmax_scale,
-              rows=None):
+              rows=None, num_contexts=None, gen_mask=None):
     """O2 fp64 attention.  ``q`` is float64 [T, Hq, D] (or [T, Hq*D]); returns
-    (status, out float64 [T, Hq, D]); rows not in ``rows`` (when given) are NaN."""
+    (status, out float64 [T, Hq, D]); rows not in ``rows`` (when given) are NaN.
+    ``gen_mask`` (uint32 [generation rows, words], with ``num_contexts``) gives each token of a
+    generation request the new tokens of its request it may see (bit j of word j // 32; the
+    token itself is always seen); without it every request is causal."""
     new_len = np.ascontiguousarray(new_len, dtype=np.int32)
     past = np.ascontiguousarray(past, dtype=np.int32)
     tbl = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -207,9 +226,15 @@ def attention(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim
         rows_p, n = _ptr(rows), int(rows.shape[0])
     else:
         rows_p, n = None, T
-    st = lib().orc_attention(
-        int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
-        int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
-        int(num_blocks), int(bool(kv_fp8)), float(kv_scale), _ptr(pool), _ptr(q),
-        float(softmax_scale), rows_p, n, _ptr(out))
+    common = (int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
+              int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
+              int(num_blocks), int(bool(kv_fp8)), float(kv_scale), _ptr(pool), _ptr(q),
+              float(softmax_scale), rows_p, n)
+    if gen_mask is None:
+        st = lib().orc_attention(*common, _ptr(out))
+    else:
+        m = np.ascontiguousarray(gen_mask, dtype=np.uint32)
+        C_ = int(num_contexts)
+        assert m.ndim == 2 and m.shape[0] == T - int(new_len[:C_].sum())
+        st = lib().orc_attention_spec(*common, C_, _ptr(m), int(m.shape[1]), _ptr(out))
     return int(st), out

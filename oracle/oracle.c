@@ -235,17 +235,32 @@ static double pool_value(const void* pool, int kv_is_fp8, double kv_scale, size_
   return (double)orc_bf16_to_f32(((const uint16_t*)pool)[idx]);
 }
 
-int orc_attention(int32_t num_requests, const int32_t* new_len, const int32_t* past,
-                  const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
-                  int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                  int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
-                  const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
-                  double* out) {
+/* Keys visible to query i of request r: every cached key t < past_r, and the new key
+ * past_r + j (j < new_len[r]) when j <= i -- plain causal order.  A generation request of
+ * several new tokens (draft tokens verified in one step: [REPORT] 1.4 "推测解码技术",
+ * spec_decoding_generation_lengths / spec_decoding_packed_mask; [ARCH] "还有哪些值得一提的模块",
+ * the Medusa candidate tree) may instead carry a packed mask row per token: bit j of word j / 32
+ * set means "sees new token j"; the token always sees itself.  gen_mask is indexed by the
+ * token's place among the generation rows (packed row - rows of the context requests). */
+static int attention_core(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+                          const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
+                          int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
+                          const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
+                          int32_t num_contexts, const uint32_t* gen_mask, int32_t mask_words,
+                          double* out) {
   int D = head_dim, B = tokens_per_block, Hkv = num_kv_heads;
   int group = num_q_heads / num_kv_heads;
   if (group * num_kv_heads != num_q_heads) return ORC_ERR_BAD_ARG;
-  int64_t T = 0;
-  for (int r = 0; r < num_requests; ++r) T += new_len[r];
+  int64_t T = 0, ctx_rows = 0;
+  for (int r = 0; r < num_requests; ++r) {
+    T += new_len[r];
+    if (r < num_contexts) ctx_rows += new_len[r];
+  }
+  if (gen_mask) {
+    for (int r = num_contexts; r < num_requests; ++r)
+      if (new_len[r] > 32 * mask_words) return ORC_ERR_BAD_ARG;
+  }
   /* request of each packed row, and its index inside the request */
   int32_t* row_req = (int32_t*)malloc(sizeof(int32_t) * (T > 0 ? T : 1));
   int32_t* row_idx = (int32_t*)malloc(sizeof(int32_t) * (T > 0 ? T : 1));
@@ -260,14 +275,20 @@ int orc_attention(int32_t num_requests, const int32_t* new_len, const int32_t* p
   for (int64_t w = 0; w < n; ++w) {
     for (int h = 0; h < num_q_heads; ++h) {
       int64_t row = rows ? rows[w] : w;
-      int r = row_req[row];
-      int64_t L = (int64_t)past[r] + row_idx[row] + 1; /* keys 0 .. past + i */
+      int r = row_req[row], i = row_idx[row];
+      const uint32_t* mrow = (gen_mask && r >= num_contexts) ? gen_mask + (row - ctx_rows) * mask_words : NULL;
+      /* keys 0 .. past + i (causal), or every key of the request when a mask row decides */
+      int64_t L = mrow ? (int64_t)past[r] + new_len[r] : (int64_t)past[r] + i + 1;
       int hk = h / group;
       const double* qv = q + (row * num_q_heads + h) * (int64_t)D;
       double* o = out + (row * num_q_heads + h) * (int64_t)D;
       double* s = (double*)malloc(sizeof(double) * L);
       int bad = 0;
       for (int64_t t = 0; t < L && !bad; ++t) {
+        if (mrow && t >= past[r]) {
+          int j = (int)(t - past[r]);
+          if (j != i && !((mrow[j / 32] >> (j % 32)) & 1u)) { s[t] = -INFINITY; continue; }
+        }
         int lb = (int)(t / B);
         int blk = lb < max_blocks_per_seq ? block_table[(size_t)r * max_blocks_per_seq + lb] : -1;
         if (blk < 0 || blk >= num_blocks) { bad = 1; break; }
@@ -300,6 +321,30 @@ int orc_attention(int32_t num_requests, const int32_t* new_len, const int32_t* p
   free(row_req);
   free(row_idx);
   return status;
+}
+
+int orc_attention(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+                  const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                  int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
+                  int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
+                  const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
+                  double* out) {
+  return attention_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
+                        num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, kv_scale, pool,
+                        q, softmax_scale, rows, num_rows, num_requests, NULL, 0, out);
+}
+
+/* O2 with packed masks for the generation requests (requests num_contexts .. R-1). */
+int orc_attention_spec(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+                       const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
+                       int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
+                       const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
+                       int32_t num_contexts, const uint32_t* gen_mask, int32_t mask_words,
+                       double* out) {
+  return attention_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
+                        num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, kv_scale, pool,
+                        q, softmax_scale, rows, num_rows, num_contexts, gen_mask, mask_words, out);
 }
 
 int orc_num_threads(void) {
@@ -359,14 +404,15 @@ static void rms_norm(float* x, int32_t D, const float* w, double eps) {
   }
 }
 
-int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+static int append_core(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                        const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
                        int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
                        int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
                        int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
                        int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
-                       double norm_eps, uint16_t* q_out, int64_t q_out_stride, void* pool) {
+                       double norm_eps, const int32_t* pos_offset, uint16_t* q_out,
+                       int64_t q_out_stride, void* pool) {
   int D = head_dim, B = tokens_per_block, Hkv = num_kv_heads;
   int rot = rotary_dim > 0 ? rotary_dim : D;
   int status = ORC_OK;
@@ -375,9 +421,12 @@ int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32
   int64_t row = 0;
   for (int r = 0; r < num_requests; ++r) {
     for (int i = 0; i < new_len[r]; ++i, ++row) {
-      int64_t pos = (int64_t)past[r] + i;
-      if (pos >= max_pos) { status = ORC_ERR_BAD_ARG; continue; }
-      const float* cs_row = cs + (size_t)pos * (rot / 2) * 2;
+      int64_t pos = (int64_t)past[r] + i; /* where the token is stored */
+      int64_t off = pos_offset ? pos_offset[row] : i;
+      if (off < 0 || off >= new_len[r]) { status = ORC_ERR_BAD_ARG; continue; }
+      int64_t rpos = (int64_t)past[r] + off; /* the position its rotation uses */
+      if (pos >= max_pos || rpos >= max_pos) { status = ORC_ERR_BAD_ARG; continue; }
+      const float* cs_row = cs + (size_t)rpos * (rot / 2) * 2;
       for (int h = 0; h < num_q_heads; ++h) {
         for (int d = 0; d < D; ++d) x[d] = orc_bf16_to_f32(q[row * q_stride + (int64_t)h * D + d]);
         if (q_norm_w) rms_norm(x, D, q_norm_w, norm_eps);
@@ -412,4 +461,39 @@ int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32
   free(x);
   free(y);
   return status;
+}
+
+int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+                       const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
+                       int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                       int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                       int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
+                       int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
+                       double norm_eps, uint16_t* q_out, int64_t q_out_stride, void* pool) {
+  return append_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, inv_scale, q,
+                     q_stride, k, k_stride, v, v_stride, cs, max_pos, style, rotary_dim, q_norm_w,
+                     k_norm_w, norm_eps, NULL, q_out, q_out_stride, pool);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* O1 for draft tokens ([REPORT] 1.4 "推测解码技术", spec_decoding_position_offsets): packed row  */
+/* `row` (request r, index i) is still stored at slot past_r + i, but rotated for position      */
+/* past_r + pos_offset[row] (its depth in the candidate tree); 0 <= pos_offset[row] < new_len[r] */
+/* or the token is skipped with ORC_ERR_BAD_ARG.  pos_offset holds one entry per packed row.     */
+/* ------------------------------------------------------------------------------------------ */
+int orc_append_rope_spec(int32_t num_requests, const int32_t* new_len, const int32_t* past,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
+                         int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                         int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                         int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
+                         int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
+                         double norm_eps, const int32_t* pos_offset, uint16_t* q_out,
+                         int64_t q_out_stride, void* pool) {
+  return append_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
+                     num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, inv_scale, q,
+                     q_stride, k, k_stride, v, v_stride, cs, max_pos, style, rotary_dim, q_norm_w,
+                     k_norm_w, norm_eps, pos_offset, q_out, q_out_stride, pool);
 }

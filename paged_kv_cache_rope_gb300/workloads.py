@@ -8,7 +8,8 @@ CUDA library and the CPU oracle are fed from here.
 Batch structure (page "TensorRT-LLM 源码完全拆解(一)", sections "AttentionMetadata 的字段与它的含义"
 and "KVCacheManager 的三个对外接口"; page adg.csdn.net/69730cc6, section 1.3):
   * requests are packed with no padding, context requests first, generation requests after;
-  * request r brings ``new_len[r]`` tokens (1 for generation) on top of ``past[r]`` cached ones;
+  * request r brings ``new_len[r]`` tokens (1 for generation, or several draft tokens to verify)
+    on top of ``past[r]`` cached ones;
   * the pool is ``[num_blocks, 2, tokens_per_block, num_kv_heads, head_dim]`` (K at index 0,
     V at index 1) and ``block_table[r, j]`` is the physical page of logical block j.
 
@@ -53,6 +54,11 @@ class Batch:
     pool_bf16: torch.Tensor | None  # fp8 batches: the unquantised bf16 twin of ``pool``
     kv_scale: float               # dequantisation multiplier (amax / 448), 1.0 for bf16
     inv_scale: float              # fp32(1 / kv_scale), the quantisation multiplier
+    # draft-token trees (generation requests of several tokens), else None: per generation
+    # row, the RoPE position offset (depth in the tree) and the packed mask row (bit j of word
+    # j // 32: the row's token sees new token j of its request -- its ancestors and itself)
+    position_offsets: np.ndarray | None = None  # int32 [T_gen]
+    packed_mask: np.ndarray | None = None       # uint32 [T_gen, words]
 
     @property
     def num_requests(self) -> int:
@@ -71,6 +77,10 @@ class Batch:
         return (self.past + self.new_len).astype(np.int64)
 
     @property
+    def num_ctx_tokens(self) -> int:
+        return int(self.new_len[:self.num_contexts].sum())
+
+    @property
     def max_pos(self) -> int:
         return int(self.kv_lengths.max()) if self.num_requests else 1
 
@@ -84,17 +94,22 @@ class Batch:
                                    pool=f(self.pool), pool_bf16=f(self.pool_bf16))
 
 
-def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list[int], num_q_heads: int,
+def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list, num_q_heads: int,
                num_kv_heads: int, head_dim: int, tokens_per_block: int, kv_dtype: str = "bf16",
                rope_base: float = 1e4, seed: int = 0, device: str = "cpu", poison: bool = True,
                extra_blocks: float = 0.1, min_spare_blocks: int = 4,
-               num_blocks: int | None = None) -> Batch:
-    """``ctx``: (new tokens, cached tokens) per context request; ``gen``: KV length per
-    generation request, counting this step's token (so ``past = L - 1``)."""
+               num_blocks: int | None = None, draft_tree: bool = False) -> Batch:
+    """``ctx``: (new tokens, cached tokens) per context request; ``gen``: per generation
+    request either its KV length counting this step's one token (so ``past = L - 1``), or a
+    pair (draft tokens, cached tokens) for a request verifying several tokens at once.
+    ``draft_tree`` draws a seeded random candidate tree per generation request (token 0 the
+    root, each later token a child of an earlier one) and fills ``position_offsets`` and
+    ``packed_mask``; without it the draft tokens form a chain (plain causal order)."""
     assert kv_dtype in ("bf16", "fp8")
     B, Hkv, D = tokens_per_block, num_kv_heads, head_dim
-    new_len = np.array([n for n, _ in ctx] + [1] * len(gen), dtype=np.int32)
-    past = np.array([p for _, p in ctx] + [L - 1 for L in gen], dtype=np.int32)
+    gen = [(1, L - 1) if np.ndim(L) == 0 else (int(L[0]), int(L[1])) for L in gen]
+    new_len = np.array([n for n, _ in ctx] + [n for n, _ in gen], dtype=np.int32)
+    past = np.array([p for _, p in ctx] + [p for _, p in gen], dtype=np.int32)
     types = np.array([REQ_CONTEXT] * len(ctx) + [REQ_GENERATION] * len(gen), dtype=np.int32)
     R = len(new_len)
     kv_len = past.astype(np.int64) + new_len
@@ -111,6 +126,24 @@ def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list[int], num_q_h
     for r in range(R):
         table[r, :pages[r]] = perm[off:off + pages[r]]
         off += pages[r]
+
+    offsets = mask = None
+    if draft_tree:
+        words = max(1, -(-max([n for n, _ in gen] + [1]) // 32))
+        offsets = np.zeros(sum(n for n, _ in gen), dtype=np.int32)
+        mask = np.zeros((offsets.shape[0], words), dtype=np.uint32)
+        trng = np.random.default_rng(seed + 7919)
+        row = 0
+        for n, _ in gen:
+            parent = [-1] + [int(trng.integers(0, i)) for i in range(1, n)]
+            for i in range(n):
+                a, depth = i, 0
+                while a >= 0:  # the token and its ancestors
+                    mask[row + i, a // 32] |= np.uint32(1 << (a % 32))
+                    a = parent[a]
+                    depth += 1
+                offsets[row + i] = depth - 1
+            row += n
 
     gen_t = torch.Generator(device=device)
     gen_t.manual_seed(seed)
@@ -146,7 +179,7 @@ def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list[int], num_q_h
 
     if kv_dtype == "bf16":
         return Batch(name, Hq, Hkv, D, B, num_blocks, kv_dtype, rope_base, types, new_len,
-                     past, table, q, k, v, bf16_pool, None, 1.0, 1.0)
+                     past, table, q, k, v, bf16_pool, None, 1.0, 1.0, offsets, mask)
 
     # FP8 pool: one per-tensor scale, amax over every K/V value drawn (history and new k/v)
     amax = max(float(hist.float().abs().max()) if n_hist else 0.0,
@@ -160,7 +193,7 @@ def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list[int], num_q_h
     fp8_pool[tok_blk, 0, tok_slot] = codes[:, 0]
     fp8_pool[tok_blk, 1, tok_slot] = codes[:, 1]
     return Batch(name, Hq, Hkv, D, B, num_blocks, kv_dtype, rope_base, types, new_len, past,
-                 table, q, k, v, fp8_pool, bf16_pool, kv_scale, inv_scale)
+                 table, q, k, v, fp8_pool, bf16_pool, kv_scale, inv_scale, offsets, mask)
 
 
 # --- the five workloads ------------------------------------------------------------------------

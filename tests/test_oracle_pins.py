@@ -532,3 +532,180 @@ def test_qk_rmsnorm_matches_formula_and_scale_invariance():
     view1 = pool1.reshape(b.num_blocks, 2, 16, 2, 64)
     assert np.array_equal(view4[:, 0], view1[:, 0])        # K normalised: identical
     assert not np.array_equal(view4[:, 1], view1[:, 1])    # V is never normalised (stays 4x)
+
+
+# ----------------------------------------------------------------------------------------------
+# draft tokens: generation requests of several tokens with position offsets and packed masks
+# (page adg.csdn.net/69730cc6, section 1.4: generation lengths, position offsets, packed mask)
+# ----------------------------------------------------------------------------------------------
+
+def _draft_offsets_all_rows(b: W.Batch) -> np.ndarray:
+    """Per packed row: index i for context rows, the batch's offset for generation rows."""
+    ctx = [np.arange(int(n), dtype=np.int32) for n in b.new_len[:b.num_contexts]]
+    gen = [b.position_offsets] if b.position_offsets is not None else [
+        np.concatenate([np.arange(int(n), dtype=np.int32) for n in b.new_len[b.num_contexts:]])]
+    return np.concatenate(ctx + gen).astype(np.int32)
+
+
+def _draft_append(b: W.Batch, pool_np, pos_offset=None, spare_pos=0):
+    cs = oracle.rope_table(b.rope_base, b.head_dim, b.max_pos + spare_pos)
+    return oracle.append_rope_ex(
+        new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
+        num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
+        num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8", inv_scale=b.inv_scale,
+        q_bits=_np_bits(b.q), k_bits=_np_bits(b.k), v_bits=_np_bits(b.v), cs=cs, pool=pool_np,
+        pos_offset=_draft_offsets_all_rows(b) if pos_offset is None else pos_offset)
+
+
+def _draft_attention(b: W.Batch, pool_np, q64, gen_mask):
+    return oracle.attention(
+        new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
+        num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
+        num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8", kv_scale=b.kv_scale, pool=pool_np,
+        q=q64, softmax_scale=b.softmax_scale, num_contexts=b.num_contexts, gen_mask=gen_mask)
+
+
+def _draft_batch(kv_dtype="bf16", seed=31, tree=True):
+    return W.make_batch(name="draft", ctx=[(19, 5)], gen=[23, (6, 40), (37, 3), (1, 17)],
+                        num_q_heads=4, num_kv_heads=2, head_dim=64, tokens_per_block=16,
+                        kv_dtype=kv_dtype, seed=seed, draft_tree=tree)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("seed", [31, 32])
+def test_draft_tree_attention_matches_sdpa_with_unpacked_mask(kv_dtype, seed):
+    """Brute force: the visible-key set of every row rebuilt with numpy's own little-endian bit
+    unpacking of the packed words (cached keys always, new key j when its bit is set or j is the
+    row itself; context rows causal), then torch SDPA in fp64 over gathered K/V."""
+    b = _draft_batch(kv_dtype, seed)
+    pool = _np_bits(b.pool).copy()
+    st, q_out = _draft_append(b, pool)
+    assert st == 0
+    T, Hq, D, Hkv, B = b.num_tokens, b.num_q_heads, b.head_dim, b.num_kv_heads, b.tokens_per_block
+    q64 = oracle.f32_from_bf16(q_out).astype(np.float64).reshape(T, Hq, D)
+    st, out = _draft_attention(b, pool, q64, b.packed_mask)
+    assert st == 0
+    bits = np.unpackbits(b.packed_mask.astype("<u4").view(np.uint8), axis=1, bitorder="little").astype(bool)
+    if kv_dtype == "fp8":
+        vals = torch.from_numpy(oracle.e4m3_decode(pool)) * b.kv_scale
+    else:
+        vals = torch.from_numpy(oracle.f32_from_bf16(pool).astype(np.float64))
+    pool5 = vals.reshape(b.num_blocks, 2, B, Hkv, D)
+    row, grow = 0, 0
+    for r in range(b.num_requests):
+        n, P = int(b.new_len[r]), int(b.past[r])
+        t = torch.arange(P + n)
+        blk = torch.from_numpy(b.block_table[r]).long()[t // B]
+        K = pool5[blk, 0, t % B].repeat_interleave(Hq // Hkv, dim=1).permute(1, 0, 2)
+        V = pool5[blk, 1, t % B].repeat_interleave(Hq // Hkv, dim=1).permute(1, 0, 2)
+        Q = torch.from_numpy(q64[row:row + n]).permute(1, 0, 2)
+        if r < b.num_contexts:
+            mask = t[None, :] <= (P + torch.arange(n))[:, None]
+        else:
+            mask = torch.zeros(n, P + n, dtype=torch.bool)
+            mask[:, :P] = True
+            mask[:, P:] = torch.from_numpy(bits[grow:grow + n, :n].copy())
+            mask[torch.arange(n), P + torch.arange(n)] = True
+            grow += n
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=b.softmax_scale)
+        assert np.max(np.abs(out[row:row + n] - ref.permute(1, 0, 2).numpy())) < 1e-12
+        row += n
+
+
+def test_draft_chain_mask_equals_causal_across_words():
+    """A chain written out as explicit bits (j <= i, 40 tokens: two words per row) must give
+    exactly the plain causal result: pins the word (j // 32) and bit (j % 32) addressing."""
+    b = _draft_batch(tree=False)
+    pool = _np_bits(b.pool).copy()
+    st, q_out = _draft_append(b, pool)
+    assert st == 0
+    q64 = oracle.f32_from_bf16(q_out).astype(np.float64).reshape(b.num_tokens, b.num_q_heads, b.head_dim)
+    _, causal = _draft_attention(b, pool, q64, None)
+    gen_n = [int(n) for n in b.new_len[b.num_contexts:]]
+    mask = np.zeros((sum(gen_n), 2), dtype=np.uint32)
+    row = 0
+    for n in gen_n:
+        for i in range(n):
+            for j in range(i + 1):
+                mask[row + i, j // 32] |= np.uint32(1 << (j % 32))
+        row += n
+    st, explicit = _draft_attention(b, pool, q64, mask)
+    assert st == 0 and np.array_equal(causal, explicit)
+    # and a chain's rows equal the rows of the same tokens sent as a chunked context request
+    r = b.num_contexts + 2  # the 37-token request
+    import dataclasses
+    rows = slice(int(b.new_len[:r].sum()), int(b.new_len[:r + 1].sum()))
+    as_ctx = dataclasses.replace(b, request_types=np.int32([W.REQ_CONTEXT]), new_len=b.new_len[r:r + 1],
+                                 past=b.past[r:r + 1], block_table=b.block_table[r:r + 1],
+                                 q=b.q[rows], k=b.k[rows], v=b.v[rows], position_offsets=None,
+                                 packed_mask=None)
+    pool2 = _np_bits(b.pool).copy()
+    st, q2 = _run_append(as_ctx, pool2)
+    q2 = oracle.f32_from_bf16(q2).astype(np.float64).reshape(-1, b.num_q_heads, b.head_dim)
+    _, out2 = _oracle_attention(as_ctx, pool2, q2)
+    assert np.array_equal(out2, causal[rows])
+
+
+def test_draft_self_only_mask_equals_one_token_requests():
+    """Candidates that are all alternatives for the next position (offset 0, no bits set: each
+    sees the cache and itself) equal one-token generation requests, one per candidate, whose
+    single new token lands at slot `past` -- bit for bit."""
+    import dataclasses
+    n, P = 5, 37
+    b = W.make_batch(name="siblings", ctx=[], gen=[(n, P)], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                     tokens_per_block=16, seed=8)
+    b = dataclasses.replace(b, position_offsets=np.zeros(n, np.int32), packed_mask=np.zeros((n, 1), np.uint32))
+    pool = _np_bits(b.pool).copy()
+    st, q_out = _draft_append(b, pool)
+    assert st == 0
+    q64 = oracle.f32_from_bf16(q_out).astype(np.float64).reshape(n, 4, 64)
+    st, out = _draft_attention(b, pool, q64, b.packed_mask)
+    assert st == 0
+    for i in range(n):
+        one = dataclasses.replace(b, new_len=np.int32([1]), past=np.int32([P]), q=b.q[i:i + 1], k=b.k[i:i + 1],
+                                  v=b.v[i:i + 1], position_offsets=None, packed_mask=None)
+        pool1 = _np_bits(b.pool).copy()
+        st, q1 = _run_append(one, pool1)
+        assert st == 0 and np.array_equal(q1[0], q_out[i])
+        _, o1 = _oracle_attention(one, pool1, oracle.f32_from_bf16(q1).astype(np.float64).reshape(1, 4, 64))
+        assert np.array_equal(o1[0], out[i])
+
+
+def test_draft_position_offsets_rotate_like_a_token_at_that_position():
+    """Token i with offset o is rotated exactly as a lone token at position past + o, but is
+    stored at slot past + i."""
+    import dataclasses
+    n, P, offs = 6, 50, [0, 1, 1, 2, 2, 3]
+    b = W.make_batch(name="offsets", ctx=[], gen=[(n, P)], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                     tokens_per_block=16, seed=9)
+    b = dataclasses.replace(b, position_offsets=np.int32(offs))
+    pool = _np_bits(b.pool).copy()
+    st, q_out = _draft_append(b, pool)
+    assert st == 0
+    view = pool.reshape(b.num_blocks, 2, 16, 2, 64)
+    for i, o in enumerate(offs):
+        one = dataclasses.replace(b, new_len=np.int32([1]), past=np.int32([P + o]), q=b.q[i:i + 1],
+                                  k=b.k[i:i + 1], v=b.v[i:i + 1], position_offsets=None)
+        pool1 = _np_bits(b.pool).copy()
+        st, q1 = _run_append(one, pool1)
+        assert st == 0 and np.array_equal(q1[0], q_out[i])
+        v1 = pool1.reshape(view.shape)
+        s_one, s_draft = P + o, P + i
+        k_one = v1[b.block_table[0, s_one // 16], :, s_one % 16]
+        k_draft = view[b.block_table[0, s_draft // 16], :, s_draft % 16]
+        assert np.array_equal(k_one, k_draft)  # K (rotated at P + o) and V, at slot P + i
+
+
+def test_draft_position_offset_out_of_range_is_rejected():
+    import dataclasses
+    b = W.make_batch(name="badoff", ctx=[], gen=[(4, 20)], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                     tokens_per_block=16, seed=10)
+    for bad in (4, -1):
+        b2 = dataclasses.replace(b, position_offsets=np.int32([0, 1, bad, 2]))
+        pool = _np_bits(b.pool).copy()
+        st, _ = _draft_append(b2, pool, spare_pos=16)  # the table itself would cover past + 4
+        assert st == -2
+        view, before = pool.reshape(b.num_blocks, 2, 16, 2, 64), _np_bits(b.pool).reshape(b.num_blocks, 2, 16, 2, 64)
+        s = 22  # the skipped token's slot keeps its poison
+        blk = b.block_table[0, s // 16]
+        assert np.array_equal(view[blk, :, s % 16], before[blk, :, s % 16])
