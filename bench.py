@@ -49,7 +49,7 @@ def work_of(b) -> dict:
     gen = b.request_types == 1
     L = (b.past + b.new_len).astype(np.int64)
     dec_kv = int(np.sum(L[gen]) * 2 * Hkv * D * esz)
-    dec_qo = int(gen.sum()) * 2 * Hq * D * 2
+    dec_qo = int(np.sum(b.new_len[gen])) * 2 * Hq * D * 2  # q read + out write per generation row
     ctx_flops = 0
     for r in np.nonzero(~gen)[0]:
         n, P = int(b.new_len[r]), int(b.past[r])

@@ -45,9 +45,10 @@ typedef struct CUstream_st* pkv_stream_t; /* == cudaStream_t; NULL = legacy defa
 #define PKV_OK 0
 #define PKV_ERR_INVALID_ARGUMENT (-1) /* NULL pointer, negative or inconsistent count          */
 #define PKV_ERR_UNSUPPORTED (-2)      /* head_dim not 64/128, tokens_per_block not 16..128,
-                                         Hq not a multiple of Hkv, group > 16, bad dtype       */
+                                         Hq not a multiple of Hkv, bad dtype                   */
 #define PKV_ERR_BATCH_ORDER (-3)      /* a context request after a generation request, or a
-                                         generation request with context_length != 1          */
+                                         generation request with context_length outside
+                                         1 .. PKV_MAX_GEN_TOKENS                               */
 #define PKV_ERR_CAPACITY (-4)         /* past + new exceeds max_blocks_per_seq * tokens_per_block
                                          or the RoPE table's max_pos                           */
 #define PKV_ERR_ALIGNMENT (-5)        /* pointer or row stride not 16-byte aligned            */
@@ -58,6 +59,12 @@ typedef struct CUstream_st* pkv_stream_t; /* == cudaStream_t; NULL = legacy defa
 #define PKV_DEVERR_BAD_PAGE 1u        /* block-table entry outside [0, num_blocks): skipped     */
 #define PKV_DEVERR_TIMEOUT 2u         /* a bounded mbarrier / TMA wait gave up                   */
 #define PKV_DEVERR_PLAN_MISMATCH 4u   /* device metadata disagrees with the host copies         */
+#define PKV_DEVERR_BAD_OFFSET 8u      /* a draft-token position offset outside [0, context_length):
+                                         that token is skipped by the append                   */
+
+/* Most new tokens one generation request may bring in one step (draft tokens under
+ * verification, [REPORT] 1.4 "推测解码技术": spec_decoding_max_generation_length). */
+#define PKV_MAX_GEN_TOKENS 64
 
 /* ---- KV-pool element type ([ARCH] "KVCacheManager 的三个对外接口": kv_cache_dtype) --------- */
 typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
@@ -95,6 +102,20 @@ typedef struct pkv_pool {
  * The host and device copies must hold the same values; the host copies plan the launch, the
  * device copies are what the kernels read (a disagreement is flagged PKV_DEVERR_PLAN_MISMATCH
  * where it is detectable).  Two requests may share a page read-only (prefix reuse).
+ *
+ * Draft tokens ([REPORT] 1.4 "推测解码技术": spec_decoding_generation_lengths, _position_offsets,
+ * _packed_mask; [NOTES] 3.2 "Draft Token 裁剪": draft tokens verified by the large model in one
+ * pass; [ARCH] "还有哪些值得一提的模块": the Medusa candidate tree): a generation request may bring
+ * 1 .. PKV_MAX_GEN_TOKENS new tokens.  Its token i is stored at slot past + i like any new
+ * token.  The two optional arrays below are indexed by a token's place among the generation
+ * rows, k = packed row - (rows of the context requests):
+ *   d_position_offsets[k]  the token is rotated for position past + offset instead of past + i
+ *                          (its depth in the candidate tree); 0 <= offset < context_length,
+ *                          otherwise PKV_DEVERR_BAD_OFFSET and the token is not written.
+ *                          NULL: offset = i.  Context rows always use past + i.
+ *   d_packed_mask[k * mask_words + j / 32] bit j % 32: the token sees new token j of its request.
+ *                          It always sees itself and every cached token (t < past).  NULL:
+ *                          plain causal order among the new tokens (token i sees j <= i).
  */
 typedef struct pkv_batch {
   int32_t num_requests;       /* R = num_contexts + number of generation requests             */
@@ -107,6 +128,10 @@ typedef struct pkv_batch {
   const int32_t* d_context_lengths; /* device copy of h_context_lengths                       */
   const int32_t* d_past_kv_lengths; /* device copy of h_past_kv_lengths                       */
   const int32_t* d_block_offsets;   /* device [R, max_blocks_per_seq] page ids                */
+  const int32_t* d_position_offsets; /* device [T_gen] or NULL (draft tokens, see above)      */
+  const uint32_t* d_packed_mask;     /* device [T_gen, mask_words] or NULL (see above)         */
+  int32_t mask_words;                /* words per mask row: >= ceil(longest generation
+                                        request / 32) when d_packed_mask is set, else ignored  */
 } pkv_batch;
 
 /*
@@ -127,7 +152,9 @@ int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float
  * RoPE + append ([NOTES] 二.2 "KVCacheManager 详解": the attention op writes each new token's
  * K/V into the pages named by the block table; [ARCH] "AttentionMetadata 的字段与它的含义":
  * the backend may apply RoPE itself when position_ids is None; [NOTES] 6.4 "量化": quantise
- * on write).  For every packed row (request r, index i, position p = past_r + i):
+ * on write).  For every packed row (request r, index i, slot position s = past_r + i, page
+ * block_offsets[r][s / B], slot s % B; rotation position p = s, or past_r + offset for draft
+ * tokens with d_position_offsets set):
  *   q_out[row, h*D:(h+1)*D] = bf16(rope(q[row, h*D:(h+1)*D], p))          for h < Hq
  *   pool[page, 0, slot, h, :] = bf16(rope(k[row, h*D:...], p))            for h < Hkv
  *   pool[page, 1, slot, h, :] = v[row, h*D:...]
@@ -139,7 +166,8 @@ int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float
  *   q_out        device bf16 [T, q_out_row_stride]; may equal q (in-place, same stride)
  *   rope_table   device fp32 table from paged_rope_table_build, max_pos rows
  *   d_error      device int32, PKV_DEVERR_* bits OR-ed in (bad page: that token's pool write
- *                is skipped, q_out is still written)
+ *                is skipped, q_out is still written; bad draft offset: nothing of that token
+ *                is written)
  * Every pool byte not addressed by a new token is left untouched.  T == 0 is a no-op.
  */
 int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads,
@@ -195,9 +223,13 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  * the generation (paged attention) path; 6.2 "Flash Attention算法核心"; 6.3 "Paged Attention
  * Kernel 内部"; [ARCH] "AttentionMetadata 的字段与它的含义": flattened (num_tokens, heads*D)
  * tensors).  For packed row (r, i), query head h, KV head h / (Hq/Hkv), position p = past_r + i:
- *   out[row, h*D:(h+1)*D] = sum_{t <= p} softmax_t(softmax_scale * <q_rot[row,h], K_t>) V_t
+ *   out[row, h*D:(h+1)*D] = sum_{t in V(r,i)} softmax_t(softmax_scale * <q_rot[row,h], K_t>) V_t
  * with K_t, V_t read through the block table (FP8 pool: value = code * kv_scale_quant_orig),
- * fp32 accumulation, bf16 output.
+ * fp32 accumulation, bf16 output.  The visible keys V(r, i) are t <= p (causal), except for
+ * generation requests with d_packed_mask set: every t < past_r, plus past_r + j for the new
+ * tokens j that the token's mask row selects, plus the token itself.  Generation requests of
+ * several tokens use the decode kernel with (token, query head) pairs of one KV head as the
+ * columns of its score tile, so the KV stream is still read once per KV head.
  *   q_rot        device bf16 [T, q_row_stride] rotated queries (q_out of the append)
  *   out          device bf16 [T, Hq*D] (row stride Hq*D)
  *   workspace    device, at least paged_attention_workspace_size bytes, 256-byte aligned;

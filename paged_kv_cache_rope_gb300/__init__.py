@@ -33,6 +33,8 @@ PKV_REQ_GENERATION = 1
 PKV_DEVERR_BAD_PAGE = 1
 PKV_DEVERR_TIMEOUT = 2
 PKV_DEVERR_PLAN_MISMATCH = 4
+PKV_DEVERR_BAD_OFFSET = 8
+PKV_MAX_GEN_TOKENS = 64
 
 # the C ABI's exported symbols (include/paged_kv.h)
 EXPORTS = (
@@ -62,7 +64,9 @@ class PkvBatch(C.Structure):
                 ("num_tokens", C.c_int32), ("max_blocks_per_seq", C.c_int32),
                 ("h_request_types", C.c_void_p), ("h_context_lengths", C.c_void_p),
                 ("h_past_kv_lengths", C.c_void_p), ("d_context_lengths", C.c_void_p),
-                ("d_past_kv_lengths", C.c_void_p), ("d_block_offsets", C.c_void_p)]
+                ("d_past_kv_lengths", C.c_void_p), ("d_block_offsets", C.c_void_p),
+                ("d_position_offsets", C.c_void_p), ("d_packed_mask", C.c_void_p),
+                ("mask_words", C.c_int32)]
 
 
 class PagedKVError(RuntimeError):
@@ -151,7 +155,11 @@ class KVPool:
 class BatchMeta:
     """Host and device copies of one inflight batch's metadata (context requests first)."""
 
-    def __init__(self, request_types, context_lengths, past_kv_lengths, block_offsets, device):
+    def __init__(self, request_types, context_lengths, past_kv_lengths, block_offsets, device,
+                 position_offsets=None, packed_mask=None):
+        """``position_offsets`` (int32 [generation rows]) and ``packed_mask`` (uint32
+        [generation rows, words]) describe draft tokens of generation requests that bring
+        several new tokens; both optional."""
         self.h_request_types = np.ascontiguousarray(request_types, dtype=np.int32)
         self.h_context_lengths = np.ascontiguousarray(context_lengths, dtype=np.int32)
         self.h_past_kv_lengths = np.ascontiguousarray(past_kv_lengths, dtype=np.int32)
@@ -162,6 +170,15 @@ class BatchMeta:
         self.d_context_lengths = torch.from_numpy(self.h_context_lengths.copy()).to(device)
         self.d_past_kv_lengths = torch.from_numpy(self.h_past_kv_lengths.copy()).to(device)
         self.d_block_offsets = torch.from_numpy(tbl.copy()).to(device)
+        self.d_position_offsets = self.d_packed_mask = None
+        self.mask_words = 0
+        if position_offsets is not None:
+            off = np.ascontiguousarray(position_offsets, dtype=np.int32).reshape(-1)
+            self.d_position_offsets = torch.from_numpy(off.copy()).to(device)
+        if packed_mask is not None:
+            m = np.ascontiguousarray(packed_mask, dtype=np.uint32)
+            self.mask_words = int(m.shape[1])
+            self.d_packed_mask = torch.from_numpy(m.view(np.int32).copy()).to(device)
 
     @property
     def num_requests(self) -> int:
@@ -180,7 +197,10 @@ class BatchMeta:
         return PkvBatch(R, self.num_contexts, self.num_tokens, int(self.h_block_offsets.shape[1]),
                         self.h_request_types.ctypes.data, self.h_context_lengths.ctypes.data,
                         self.h_past_kv_lengths.ctypes.data, self.d_context_lengths.data_ptr(),
-                        self.d_past_kv_lengths.data_ptr(), self.d_block_offsets.data_ptr())
+                        self.d_past_kv_lengths.data_ptr(), self.d_block_offsets.data_ptr(),
+                        None if self.d_position_offsets is None else self.d_position_offsets.data_ptr(),
+                        None if self.d_packed_mask is None else self.d_packed_mask.data_ptr(),
+                        self.mask_words)
 
 
 # --- entry points --------------------------------------------------------------------------

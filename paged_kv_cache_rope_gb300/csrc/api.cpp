@@ -93,8 +93,9 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int D, int heads, int64
 }
 
 struct HostPlan {
-  int R = 0, C = 0, G = 0, T = 0, ctx_tokens = 0;
+  int R = 0, C = 0, G = 0, T = 0, ctx_tokens = 0, max_gen_tokens = 0;
   int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
+  int decode_nt = 1, num_items = 0, num_parts = 0;  // decode n-tiles per CTA, CTAs per KV head, partial rows
   pkv::PlanLayout lay{};
 };
 
@@ -117,7 +118,6 @@ int validate_pool(const pkv_pool* pool) {
 int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
   if (!b) return PKV_ERR_INVALID_ARGUMENT;
   if (Hq <= 0 || Hq % pool->num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
-  if (Hq / pool->num_kv_heads > 16) return PKV_ERR_UNSUPPORTED;
   const int R = b->num_requests, C = b->num_contexts;
   if (R < 0 || C < 0 || C > R || b->num_tokens < 0) return PKV_ERR_INVALID_ARGUMENT;
   hp->R = R;
@@ -131,6 +131,7 @@ int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPla
     return PKV_ERR_INVALID_ARGUMENT;
   const int64_t cap = static_cast<int64_t>(b->max_blocks_per_seq) * pool->tokens_per_block;
   int64_t T = 0, ctx_tokens = 0;
+  int max_gen = 0;
   for (int r = 0; r < R; ++r) {
     const int type = b->h_request_types[r];
     const int n = b->h_context_lengths[r], past = b->h_past_kv_lengths[r];
@@ -139,14 +140,17 @@ int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPla
       if (type != PKV_REQ_CONTEXT) return PKV_ERR_BATCH_ORDER;
       ctx_tokens += n;
     } else {
-      if (type != PKV_REQ_GENERATION || n != 1) return PKV_ERR_BATCH_ORDER;
+      if (type != PKV_REQ_GENERATION || n > PKV_MAX_GEN_TOKENS) return PKV_ERR_BATCH_ORDER;
+      max_gen = std::max(max_gen, n);
     }
     if (static_cast<int64_t>(past) + n > cap) return PKV_ERR_CAPACITY;
     if (static_cast<int64_t>(past) + n > INT32_MAX / 2) return PKV_ERR_CAPACITY;
     T += n;
   }
   if (T != b->num_tokens) return PKV_ERR_INVALID_ARGUMENT;
+  if (b->d_packed_mask && (b->mask_words <= 0 || 32LL * b->mask_words < max_gen)) return PKV_ERR_INVALID_ARGUMENT;
   hp->ctx_tokens = static_cast<int>(ctx_tokens);
+  hp->max_gen_tokens = max_gen;
   return PKV_OK;
 }
 
@@ -159,7 +163,7 @@ int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPla
 // 2048 of an FP8 one), so per-CTA set-up is amortised over the same bytes for either dtype.
 int choose_kv_chunk(const pkv_pool* pool, const pkv_batch* b, int C) {
   int64_t total = 0;
-  for (int r = C; r < b->num_requests; ++r) total += b->h_past_kv_lengths[r] + 1;
+  for (int r = C; r < b->num_requests; ++r) total += b->h_past_kv_lengths[r] + b->h_context_lengths[r];
   const int64_t target = static_cast<int64_t>(device_sm_count()) * 4;
   int64_t chunk = (total * pool->num_kv_heads + target - 1) / std::max<int64_t>(target, 1);
   chunk = (chunk + 15) / 16 * 16;
@@ -174,18 +178,29 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   for (int r = 0; r < hp->C; ++r)
     hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
   hp->kv_chunk = choose_kv_chunk(pool, b, hp->C);
-  hp->num_splits = 0;
-  hp->max_splits = 0;
+  // decode score-tile columns are (token, query head) pairs of one KV head: 8 or 16 per CTA,
+  // and a request whose pairs do not fit takes several column groups per split
+  const int group = Hq / pool->num_kv_heads;
+  hp->decode_nt = static_cast<int64_t>(hp->max_gen_tokens) * group > 8 ? 2 : 1;
+  const int cols = 8 * hp->decode_nt;
+  hp->num_splits = hp->max_splits = hp->num_items = hp->num_parts = 0;
   for (int r = hp->C; r < hp->R; ++r) {
-    const int s = (b->h_past_kv_lengths[r] + 1 + hp->kv_chunk - 1) / hp->kv_chunk;
+    const int n = b->h_context_lengths[r];
+    const int s = (b->h_past_kv_lengths[r] + n + hp->kv_chunk - 1) / hp->kv_chunk;
     hp->num_splits += s;
+    hp->num_items += s * ((n * group + cols - 1) / cols);
+    hp->num_parts += s * n;
     hp->max_splits = std::max(hp->max_splits, s);
   }
   pkv::PlanLayout& L = hp->lay;
   L.cu_q = 0;
   L.tile_prefix = L.cu_q + hp->R + 1;
   L.split_prefix = L.tile_prefix + hp->C + 1;
-  L.unit_order = L.split_prefix + hp->G + 1;
+  L.item_prefix = L.split_prefix + hp->G + 1;
+  L.part_prefix = L.item_prefix + hp->G + 1;
+  L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
+  L.row_map = L.item_map + 2LL * hp->num_items;
+  L.unit_order = L.row_map + 2LL * (hp->T - hp->ctx_tokens);
   L.stage_prefix = L.unit_order + hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
   L.int_words = L.stage_tbl + (staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
@@ -197,8 +212,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   const int64_t int_bytes = (L.int_words * 4 + 255) / 256 * 256;
   const int64_t D = pool->head_dim;
   L.part_o = int_bytes;
-  L.part_ml = L.part_o + (static_cast<int64_t>(hp->num_splits) * Hq * D * 4 + 255) / 256 * 256;
-  L.stage_pool = L.part_ml + (static_cast<int64_t>(hp->num_splits) * Hq * 2 * 4 + 255) / 256 * 256;
+  L.part_ml = L.part_o + (static_cast<int64_t>(hp->num_parts) * Hq * D * 4 + 255) / 256 * 256;
+  L.stage_pool = L.part_ml + (static_cast<int64_t>(hp->num_parts) * Hq * 2 * 4 + 255) / 256 * 256;
   L.total_bytes = L.stage_pool + (L.stage_pages * 2 * pool->tokens_per_block * pool->num_kv_heads * D * 2 + 255) / 256 * 256;
 }
 
@@ -382,6 +397,8 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
   p.ctx_len = batch->d_context_lengths;
   p.past = batch->d_past_kv_lengths;
   p.tbl = batch->d_block_offsets;
+  p.pos_off = batch->d_position_offsets;
+  p.gen_row0 = hp.ctx_tokens;
   p.d_error = d_error;
   reset_names();
   cudaError_t e;
@@ -432,6 +449,12 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.Hkv = Hkv;
   pp.B = pool->tokens_per_block;
   pp.Hq = num_q_heads;
+  pp.group = num_q_heads / Hkv;
+  pp.cols_per_cta = 8 * hp.decode_nt;
+  pp.expect_items = hp.num_items;
+  pp.expect_parts = hp.num_parts;
+  pp.gen_row0 = hp.ctx_tokens;
+  pp.gen_rows = hp.T - hp.ctx_tokens;
   pp.expect_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
   pp.expect_tiles = hp.num_tiles;
   pp.expect_splits = hp.num_splits;
@@ -548,7 +571,10 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.max_blocks = batch->max_blocks_per_seq;
     dp.kv_chunk = hp.kv_chunk;
     dp.gen_row0 = hp.ctx_tokens;
-    dp.total_splits = hp.num_splits;
+    dp.gen_rows = hp.T - hp.ctx_tokens;
+    dp.total_items = hp.num_items;
+    dp.total_parts = hp.num_parts;
+    dp.nt = hp.decode_nt;
     dp.pool = static_cast<const uint8_t*>(pool->pool);
     dp.kv_scale = fp8 ? pool->kv_scale_quant_orig : 1.0f;
     dp.scale_log2 = scale_log2;
@@ -556,8 +582,15 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.q_stride = q_row_stride;
     dp.out = static_cast<uint16_t*>(out);
     dp.past = batch->d_past_kv_lengths;
+    dp.new_len = batch->d_context_lengths;
     dp.tbl = batch->d_block_offsets;
+    dp.cu_q = ws + hp.lay.cu_q;
     dp.split_prefix = ws + hp.lay.split_prefix;
+    dp.item_map = reinterpret_cast<const int2*>(ws + hp.lay.item_map);
+    dp.row_map = reinterpret_cast<const int2*>(ws + hp.lay.row_map);
+    dp.part_prefix = ws + hp.lay.part_prefix;
+    dp.mask = batch->d_packed_mask;
+    dp.mask_words = batch->d_packed_mask ? batch->mask_words : 0;
     dp.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_o);
     dp.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_ml);
     dp.d_error = d_error;
@@ -570,7 +603,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     if (hp.max_splits > 1) {
       {
         LaunchScope ls(launches, "combine", gs);
-        e = pkv::launch_combine(dp, gs);
+        e = pkv::launch_combine(dp, hp.max_splits, gs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;

@@ -9,7 +9,9 @@
 // HBM-bound.  One thread handles 16 elements of one head of one token (8 rotation pairs, or a
 // pass-through part of a partially rotated head): two 16-byte loads, two 16-byte stores (8-byte
 // stores into an FP8 pool).  Variants: rotate-half or interleaved pairs, partial rotary dims,
-// and an optional RMSNorm of q / k heads reduced across the head's lanes with shuffles.
+// an optional RMSNorm of q / k heads reduced across the head's lanes with shuffles, and
+// draft tokens rotated for past + offset (adg.csdn.net/69730cc6 section 1.4,
+// spec_decoding_position_offsets) while stored at slot past + i.
 // Threads of a warp cover consecutive heads of the same token, so every row read and written
 // is a run of full 32-byte sectors.  The token -> request map comes from an in-CTA prefix scan
 // of context_lengths (no workspace needed).
@@ -140,10 +142,20 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
       else hi = mid - 1;
     }
     const int r = lo;
-    const int pos = __ldg(p.past + r) + (token - s_cu[r]);
+    const int past_r = __ldg(p.past + r);
+    const int pos = past_r + (token - s_cu[r]);  // slot position
+    int rpos = pos;                               // rotation position
     bool ok = active;
-    if (active && (pos < 0 || pos >= p.max_pos)) {  // device lengths disagree with the host-checked ones
-      flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+    if (active && p.pos_off != nullptr && token >= p.gen_row0) {  // a draft token
+      const int off = __ldg(p.pos_off + (token - p.gen_row0));
+      if (off < 0 || off >= __ldg(p.ctx_len + r)) {
+        flag_error(p.d_error, PKV_DEVERR_BAD_OFFSET);
+        ok = false;
+      }
+      rpos = past_r + off;
+    }
+    if (ok && (pos < 0 || pos >= p.max_pos || rpos < 0 || rpos >= p.max_pos)) {
+      flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree with the host-checked ones
       ok = false;
     }
     // kind: 0 = q, 1 = k, 2 = v; head h; task t within the head
@@ -206,7 +218,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
       yb[e] = xb[e];
     }
     if (rotate) {
-      const float2* cs = p.rope + static_cast<size_t>(pos) * rhalf + 8 * t;
+      const float2* cs = p.rope + static_cast<size_t>(rpos) * rhalf + 8 * t;
       if (p.style == 0) {
         rotate8(xa, xb, cs, ya, yb);
       } else {

@@ -37,8 +37,8 @@ namespace {
 constexpr int kPlanThreads = 256;
 
 // One pass over the requests: exclusive prefix sums of (new tokens, context units of
-// kCtxRowsPerCta rows, generation splits, staged FP8 context pages) at once, so the whole plan
-// costs a single sweep of block-wide scans.
+// kCtxRowsPerCta rows, generation splits, staged FP8 context pages, decode CTAs, partial rows)
+// at once, so the whole plan costs a single sweep of block-wide scans.
 __device__ __forceinline__ int4 shfl_up4(int4 v, int o) {
   return make_int4(__shfl_up_sync(0xffffffffu, v.x, o), __shfl_up_sync(0xffffffffu, v.y, o),
                    __shfl_up_sync(0xffffffffu, v.z, o), __shfl_up_sync(0xffffffffu, v.w, o));
@@ -46,75 +46,113 @@ __device__ __forceinline__ int4 shfl_up4(int4 v, int o) {
 __device__ __forceinline__ int4 add4(int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 __device__ __forceinline__ int4 sub4(int4 a, int4 b) { return make_int4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
 
+// Block-wide exclusive scan of a pair of int4 values per thread (one chunk of kPlanThreads
+// requests); returns the exclusive prefix within the chunk plus the running carry.
+struct Int8v {
+  int4 a, b;
+};
+__device__ __forceinline__ Int8v scan_chunk(const Int8v x, Int8v* s_warp, const Int8v& carry, int lane, int wid) {
+  Int8v incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int4 ya = shfl_up4(incl.a, o), yb = shfl_up4(incl.b, o);
+    if (lane >= o) {
+      incl.a = add4(incl.a, ya);
+      incl.b = add4(incl.b, yb);
+    }
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int4 z = make_int4(0, 0, 0, 0);
+    const Int8v w = lane < kPlanThreads / 32 ? s_warp[lane] : Int8v{z, z};
+    Int8v wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int4 ya = shfl_up4(wi.a, o), yb = shfl_up4(wi.b, o);
+      if (lane >= o) {
+        wi.a = add4(wi.a, ya);
+        wi.b = add4(wi.b, yb);
+      }
+    }
+    if (lane < kPlanThreads / 32) s_warp[lane] = Int8v{sub4(wi.a, w.a), sub4(wi.b, w.b)};
+  }
+  __syncthreads();
+  const Int8v sw = s_warp[wid];
+  return Int8v{add4(add4(carry.a, sw.a), sub4(incl.a, x.a)), add4(add4(carry.b, sw.b), sub4(incl.b, x.b))};
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
-  __shared__ int4 s_warp[kPlanThreads / 32];
-  __shared__ int4 s_carry;
+  __shared__ Int8v s_warp[kPlanThreads / 32];
+  __shared__ Int8v s_carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int32_t* cu = p.ws + p.lay.cu_q;
   int32_t* tiles = p.ws + p.lay.tile_prefix;
   int32_t* splits = p.ws + p.lay.split_prefix;
+  int32_t* items = p.ws + p.lay.item_prefix;
+  int32_t* parts = p.ws + p.lay.part_prefix;
+  int2* item_map = reinterpret_cast<int2*>(p.ws + p.lay.item_map);
+  int2* row_map = reinterpret_cast<int2*>(p.ws + p.lay.row_map);
   int32_t* stage = p.ws + p.lay.stage_prefix;
   const bool staging = p.expect_stage_pages > 0;
-  const int C = p.C, chunk = p.kv_chunk;
+  const int C = p.C, chunk = p.kv_chunk, cols = p.cols_per_cta;
   bool bad = false;
   pdl_wait();
-  if (tid == 0) s_carry = make_int4(0, 0, 0, 0);
+  const int4 z4 = make_int4(0, 0, 0, 0);
+  if (tid == 0) s_carry = Int8v{z4, z4};
   __syncthreads();
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + tid;
-    int4 x = make_int4(0, 0, 0, 0);
+    // a: (new tokens, context units, generation splits, staged FP8 context pages)
+    // b: (decode CTAs per KV head, partial-result rows, -, -)
+    Int8v x{z4, z4};
     if (r < p.R) {
       const int n = __ldg(p.ctx_len + r);
-      x.x = n;
+      x.a.x = n;
       if (r < C) {
-        x.y = (n + kCtxRowsPerCta - 1) / kCtxRowsPerCta;
-        if (staging) x.w = (__ldg(p.past + r) + n + p.B - 1) / p.B;
+        x.a.y = (n + kCtxRowsPerCta - 1) / kCtxRowsPerCta;
+        if (staging) x.a.w = (__ldg(p.past + r) + n + p.B - 1) / p.B;
       } else {
-        x.z = (__ldg(p.past + r) + 1 + chunk - 1) / chunk;
-        bad |= n != 1;
+        bad |= n < 1 || n > PKV_MAX_GEN_TOKENS;
+        const int sr = (__ldg(p.past + r) + n + chunk - 1) / chunk;
+        x.a.z = sr;
+        x.b.x = sr * ((n * p.group + cols - 1) / cols);
+        x.b.y = sr * n;
       }
     }
-    int4 incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int4 y = shfl_up4(incl, o);
-      if (lane >= o) incl = add4(incl, y);
-    }
-    if (lane == 31) s_warp[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      const int4 w = lane < kPlanThreads / 32 ? s_warp[lane] : make_int4(0, 0, 0, 0);
-      int4 wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int4 y = shfl_up4(wi, o);
-        if (lane >= o) wi = add4(wi, y);
-      }
-      if (lane < kPlanThreads / 32) s_warp[lane] = sub4(wi, w);
-    }
-    __syncthreads();
-    const int4 ex = add4(add4(s_carry, s_warp[wid]), sub4(incl, x));
+    const Int8v ex = scan_chunk(x, s_warp, s_carry, lane, wid);
     if (r < p.R) {
-      cu[r] = ex.x;
+      cu[r] = ex.a.x;
       if (r < C) {
-        tiles[r] = ex.y;
-        if (staging) stage[r] = ex.w;
+        tiles[r] = ex.a.y;
+        if (staging) stage[r] = ex.a.w;
       } else {
-        splits[r - C] = ex.z;
+        const int gr = r - C;
+        splits[gr] = ex.a.z;
+        items[gr] = ex.b.x;
+        parts[gr] = ex.b.y;
+        // direct maps for the decode CTAs and the combine rows (no searches there)
+        for (int it = 0; it < x.b.x && ex.b.x + it < p.expect_items; ++it) item_map[ex.b.x + it] = make_int2(gr, it);
+        for (int i = 0; i < x.a.x; ++i) {
+          const int row = ex.a.x + i - p.gen_row0;
+          if (row >= 0 && row < p.gen_rows) row_map[row] = make_int2(gr, i);
+        }
       }
     }
     __syncthreads();
-    if (tid == kPlanThreads - 1) s_carry = add4(ex, x);
+    if (tid == kPlanThreads - 1) s_carry = Int8v{add4(ex.a, x.a), add4(ex.b, x.b)};
     __syncthreads();
   }
   if (tid == 0) {
-    const int4 t = s_carry;
-    cu[p.R] = t.x;
-    tiles[C] = t.y;
-    splits[p.G] = t.z;
-    if (staging) stage[C] = t.w;
-    bad |= (t.x != p.T) || (t.y != p.expect_tiles) || (t.z != p.expect_splits) ||
-           (staging && t.w != p.expect_stage_pages);
+    const Int8v t = s_carry;
+    cu[p.R] = t.a.x;
+    tiles[C] = t.a.y;
+    splits[p.G] = t.a.z;
+    items[p.G] = t.b.x;
+    parts[p.G] = t.b.y;
+    if (staging) stage[C] = t.a.w;
+    bad |= (t.a.x != p.T) || (t.a.y != p.expect_tiles) || (t.a.z != p.expect_splits) ||
+           (t.b.x != p.expect_items) || (t.b.y != p.expect_parts) || (staging && t.a.w != p.expect_stage_pages);
   }
   if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
 
@@ -233,32 +271,62 @@ decode_splitkv_kernel(DecodeParams p) {
   const int g8 = lane >> 2, q4 = lane & 3;  // fragment row group / column pair
   const int item = blockIdx.x, h = blockIdx.y;
 
-  // ---- which generation request and split this CTA owns ----
-  if (item >= p.total_splits) return;
+  // ---- which generation request, split and column group this CTA owns ----
+  // Columns of the score tile are (token i, query head h*group + hl) pairs of this KV head,
+  // c = i*group + hl; a CTA takes HN of them (column group cg).
+  constexpr int HN = NT * 8;
+  if (item >= p.total_items) return;
   pdl_wait();
-  int lo = 0, hi = p.G - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.split_prefix + mid) <= item) lo = mid;
-    else hi = mid - 1;
-  }
-  const int gr = lo, r = p.C + gr;
-  const int s_idx = item - __ldg(p.split_prefix + gr);
+  const int2 im = p.item_map[item];  // written by the plan kernel earlier on the stream
+  const int gr = min(max(im.x, 0), p.G - 1), r = p.C + gr, local = im.y;
+  const int n_new = __ldg(p.new_len + r);
+  const int ncols = n_new * p.group;
+  const int n_cg = (ncols + HN - 1) / HN;
+  const int s_idx = local / max(n_cg, 1), cg = local - s_idx * n_cg;
   const int num_splits = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
-  const int L = __ldg(p.past + r) + 1;
+  const int past = __ldg(p.past + r);
+  const int L = past + n_new;
   const int t_begin = s_idx * p.kv_chunk;
   const int t_end = min(L, t_begin + p.kv_chunk);
-  if (s_idx >= num_splits || t_begin >= t_end) {
+  if (local < 0 || s_idx >= num_splits || t_begin >= t_end || n_new < 1 || n_new > PKV_MAX_GEN_TOKENS) {
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
     return;
   }
   const int n_tiles = (t_end - t_begin + kDecodeTile - 1) / kDecodeTile;
   const int my_first = (warp * n_tiles) / Cfg::kWarps;
   const int my_n = ((warp + 1) * n_tiles) / Cfg::kWarps - my_first;
-  const int qrow = p.gen_row0 + gr;
-  const uint16_t* qbase = p.q + static_cast<int64_t>(qrow) * p.q_stride;
+  const int row0 = __ldg(p.cu_q + r);  // packed row of the request's token 0
+  const int col0 = cg * HN;
+  const int64_t part_row0 = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new;
+  if (row0 < p.gen_row0 || row0 + n_new > p.gen_row0 + p.gen_rows || part_row0 + n_new > p.total_parts) {
+    if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
+    return;
+  }
 
-  // ---- Q fragments (B operand of S^T = K Q^T): column n = query head h*group + nt*8 + g8 ----
+  // which new keys (past + j) the lane's accumulator columns (2*q4 + {0,1} of each n-tile) see:
+  // bit j; a column past the last pair sees everything (its result is discarded)
+  uint64_t vis[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = col0 + nt * 8 + 2 * q4 + j;
+      uint64_t v = ~0ull;
+      if (c < ncols) {
+        const int i = c / p.group;
+        if (p.mask != nullptr) {
+          const uint32_t* mrow = p.mask + static_cast<int64_t>(row0 + i - p.gen_row0) * p.mask_words;
+          v = __ldg(mrow);
+          if (n_new > 32 && p.mask_words > 1) v |= static_cast<uint64_t>(__ldg(mrow + 1)) << 32;
+          v |= 1ull << i;
+        } else {
+          v = (2ull << i) - 1;  // j <= i (i = 63 wraps to all ones)
+        }
+      }
+      vis[nt][j] = v;
+    }
+
+  // ---- Q fragments (B operand of S^T = K Q^T): column n = col0 + nt*8 + g8 ----
   // bf16: k16 fragments.  FP8 pool: k32 E4M3 fragments of q * 2^e split as hi + lo codes; the
   // lane holds head dims [q4*D/4, (q4+1)*D/4) and k-step kk takes its bytes 8kk .. 8kk+7.
   constexpr int QW = FP8 ? D / 32 : KS;  // k-steps
@@ -267,9 +335,10 @@ decode_splitkv_kernel(DecodeParams p) {
   float colscale[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int hl = nt * 8 + g8;
-    const bool valid = hl < p.group;
-    const uint16_t* qh = qbase + static_cast<int64_t>(h * p.group + (valid ? hl : 0)) * D;
+    const int c = col0 + nt * 8 + g8;
+    const bool valid = c < ncols;
+    const int ci = valid ? c / p.group : 0, hl = valid ? c - ci * p.group : 0;
+    const uint16_t* qh = p.q + static_cast<int64_t>(row0 + ci) * p.q_stride + static_cast<int64_t>(h * p.group + hl) * D;
     if constexpr (!FP8) {
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
@@ -447,11 +516,19 @@ decode_splitkv_kernel(DecodeParams p) {
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int u = 0; u < SUB; ++u) {
-        const bool r0_ok = t0 + u * kDecodeTile + g8 < w_end, r1_ok = t0 + u * kDecodeTile + g8 + 8 < w_end;
-        sv[u][0] = r0_ok ? sacc[u][nt][0] * colscale[nt][0] : -INFINITY;
-        sv[u][1] = r0_ok ? sacc[u][nt][1] * colscale[nt][1] : -INFINITY;
-        sv[u][2] = r1_ok ? sacc[u][nt][2] * colscale[nt][0] : -INFINITY;
-        sv[u][3] = r1_ok ? sacc[u][nt][3] * colscale[nt][1] : -INFINITY;
+        const int ta = t0 + u * kDecodeTile + g8, tb = ta + 8;
+        bool ok[4] = {ta < w_end, ta < w_end, tb < w_end, tb < w_end};
+        if (t0 + (u + 1) * kDecodeTile > past) {  // the tile holds new keys: apply visibility
+          const int ja = ta - past, jb = tb - past;
+          ok[0] = ok[0] && (ja < 0 || ((vis[nt][0] >> ja) & 1ull));
+          ok[1] = ok[1] && (ja < 0 || ((vis[nt][1] >> ja) & 1ull));
+          ok[2] = ok[2] && (jb < 0 || ((vis[nt][0] >> jb) & 1ull));
+          ok[3] = ok[3] && (jb < 0 || ((vis[nt][1] >> jb) & 1ull));
+        }
+        sv[u][0] = ok[0] ? sacc[u][nt][0] * colscale[nt][0] : -INFINITY;
+        sv[u][1] = ok[1] ? sacc[u][nt][1] * colscale[nt][1] : -INFINITY;
+        sv[u][2] = ok[2] ? sacc[u][nt][2] * colscale[nt][0] : -INFINITY;
+        sv[u][3] = ok[3] ? sacc[u][nt][3] * colscale[nt][1] : -INFINITY;
         mx0 = fmaxf(mx0, fmaxf(sv[u][0], sv[u][2]));
         mx1 = fmaxf(mx1, fmaxf(sv[u][1], sv[u][3]));
       }
@@ -460,9 +537,11 @@ decode_splitkv_kernel(DecodeParams p) {
         mx0 = warp_max_xor(mx0, msk);
         mx1 = warp_max_xor(mx1, msk);
       }
+      // a column that has seen no visible key yet keeps m = -inf; its exponents use base 0
       const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+      const float eb0 = mn0 == -INFINITY ? 0.f : mn0, eb1 = mn1 == -INFINITY ? 0.f : mn1;
       if (__any_sync(0xffffffffu, mn0 != m_run[nt][0] || mn1 != m_run[nt][1])) {
-        const float al0 = ex2_approx(m_run[nt][0] - mn0), al1 = ex2_approx(m_run[nt][1] - mn1);
+        const float al0 = ex2_approx(m_run[nt][0] - eb0), al1 = ex2_approx(m_run[nt][1] - eb1);
         l_run[nt][0] *= al0;
         l_run[nt][1] *= al1;
 #pragma unroll
@@ -477,8 +556,8 @@ decode_splitkv_kernel(DecodeParams p) {
       }
 #pragma unroll
       for (int u = 0; u < SUB; ++u) {
-        const float p0 = ex2_approx(sv[u][0] - mn0), p1 = ex2_approx(sv[u][1] - mn1);
-        const float p2 = ex2_approx(sv[u][2] - mn0), p3 = ex2_approx(sv[u][3] - mn1);
+        const float p0 = ex2_approx(sv[u][0] - eb0), p1 = ex2_approx(sv[u][1] - eb1);
+        const float p2 = ex2_approx(sv[u][2] - eb0), p3 = ex2_approx(sv[u][3] - eb1);
         l_run[nt][0] += p0 + p2;
         l_run[nt][1] += p1 + p3;
         if constexpr (!FP8) {
@@ -557,7 +636,6 @@ decode_splitkv_kernel(DecodeParams p) {
       l_run[nt][j] = v;
     }
   __syncthreads();  // every warp is done with its ring; reuse shared memory for the merge
-  constexpr int HN = NT * 8;
   float* sm_o = reinterpret_cast<float*>(smem);             // [warps][HN][D]
   float* sm_m = sm_o + Cfg::kWarps * HN * D;                 // [warps][HN]
   float* sm_l = sm_m + Cfg::kWarps * HN;                     // [warps][HN]
@@ -583,24 +661,27 @@ decode_splitkv_kernel(DecodeParams p) {
   }
   __syncthreads();
   const int64_t hq0 = static_cast<int64_t>(h) * p.group;
-  for (int idx = threadIdx.x; idx < p.group * D; idx += Cfg::kThreads) {
-    const int hl = idx / D, d = idx - hl * D;
+  const int n_here = min(HN, ncols - col0);  // valid columns of this CTA
+  for (int idx = threadIdx.x; idx < n_here * D; idx += Cfg::kThreads) {
+    const int cl = idx / D, d = idx - cl * D;
+    const int c = col0 + cl, ci = c / p.group, hl = c - ci * p.group;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < Cfg::kWarps; ++w) M = fmaxf(M, sm_m[w * HN + hl]);
+    for (int w = 0; w < Cfg::kWarps; ++w) M = fmaxf(M, sm_m[w * HN + cl]);
+    const float Mb = M == -INFINITY ? 0.f : M;  // no visible key in this split (draft masks)
     float acc = 0.f, lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < Cfg::kWarps; ++w) {
-      const float f = ex2_approx(sm_m[w * HN + hl] - M);
-      acc += f * sm_o[(w * HN + hl) * D + d];
-      lsum += f * sm_l[w * HN + hl];
+      const float f = ex2_approx(sm_m[w * HN + cl] - Mb);
+      acc += f * sm_o[(w * HN + cl) * D + d];
+      lsum += f * sm_l[w * HN + cl];
     }
     acc *= FP8 ? p.kv_scale * (1.f / 256.f) : p.kv_scale;  // FP8: P entered the MMA as 256 p
     if (num_splits == 1) {
       __nv_bfloat16 b = __float2bfloat16_rn(acc / lsum);
-      p.out[static_cast<int64_t>(qrow) * p.Hq * D + (hq0 + hl) * D + d] = *reinterpret_cast<uint16_t*>(&b);
+      p.out[static_cast<int64_t>(row0 + ci) * p.Hq * D + (hq0 + hl) * D + d] = *reinterpret_cast<uint16_t*>(&b);
     } else {
-      const int64_t pi = static_cast<int64_t>(item) * p.Hq + hq0 + hl;
+      const int64_t pi = (part_row0 + ci) * p.Hq + hq0 + hl;
       p.part_o[pi * D + d] = acc;
       if (d == 0) {
         p.part_ml[pi * 2] = M;
@@ -611,34 +692,43 @@ decode_splitkv_kernel(DecodeParams p) {
 }
 
 // --------------------------------------------------------------------------------------------
-// log-sum-exp merge of the splits: one CTA of 4 warps per (generation request, query head); warp
-// w streams splits w, w+4, ... with an online max (lane i owns 4 consecutive head dims), then
-// the four partial results are merged through shared memory
+// log-sum-exp merge of the splits: one CTA of W warps (4, 8 or 16, by the largest split count)
+// per (generation row, query head); warp w streams splits w, w+W, ... with an online max (lane
+// i owns 4 consecutive head dims), then the W partial results are merged through shared memory
 // --------------------------------------------------------------------------------------------
-constexpr int kCombineWarps = 4;
-
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParams p) {
-  __shared__ float4 s_acc[kCombineWarps][32];
-  __shared__ float2 s_ml[kCombineWarps];
+template <int W>  // warps per CTA: more for requests with many splits
+__global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
+  __shared__ float4 s_acc[W][32];
+  __shared__ float2 s_ml[W];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gr = blockIdx.x / p.Hq, hq = blockIdx.x - gr * p.Hq;
+  const int grow = blockIdx.x / p.Hq, hq = blockIdx.x - grow * p.Hq;  // generation row, query head
   pdl_wait();
-  const int first = __ldg(p.split_prefix + gr);
-  const int S = __ldg(p.split_prefix + gr + 1) - first;
+  const int row = p.gen_row0 + grow;
+  const int2 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
+  const int gr = min(max(rm.x, 0), p.G - 1), r = p.C + gr, i = rm.y;
+  const int S = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
   if (S <= 1) return;  // written directly by the decode kernel
+  const int n_new = __ldg(p.new_len + r);
+  if (i < 0 || i >= n_new || static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(S) * n_new > p.total_parts) {
+    if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
+    return;
+  }
   const int D = p.D;
   const bool active = lane < D / 4;
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + static_cast<int64_t>(first) * p.Hq + hq;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(first) * p.Hq + hq) * D) + lane;
-  const int64_t stride4 = static_cast<int64_t>(p.Hq) * D / 4;
+  // partial row of split s: part_prefix[gr] + s * n_new + i
+  const int64_t first = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + i;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + first * p.Hq + hq;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (first * p.Hq + hq) * D) + lane;
+  const int64_t stride_ml = static_cast<int64_t>(n_new) * p.Hq, stride4 = stride_ml * D / 4;
   float M = -INFINITY, lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int s = warp; s < S; s += kCombineWarps) {
-    const float2 m_l = ml[static_cast<int64_t>(s) * p.Hq];
+  for (int s = warp; s < S; s += W) {
+    const float2 m_l = ml[s * stride_ml];
     const float4 v = active ? po[s * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float Mn = fmaxf(M, m_l.x);
-    const float a = ex2_approx(M - Mn), b = ex2_approx(m_l.x - Mn);
+    const float Mb = Mn == -INFINITY ? 0.f : Mn;  // splits with no visible key (draft masks)
+    const float a = ex2_approx(M - Mb), b = ex2_approx(m_l.x - Mb);
     acc.x = acc.x * a + v.x * b;
     acc.y = acc.y * a + v.y * b;
     acc.z = acc.z * a + v.z * b;
@@ -652,11 +742,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
   if (warp != 0 || !active) return;
   float Mt = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, s_ml[w].x);
+  for (int w = 0; w < W; ++w) Mt = fmaxf(Mt, s_ml[w].x);
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float lt = 0.f;
 #pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) {
+  for (int w = 0; w < W; ++w) {
     const float f = ex2_approx(s_ml[w].x - Mt);  // a warp with no splits has M = -inf: f = 0
     const float4 a4 = s_acc[w][lane];
     o.x += f * a4.x;
@@ -666,9 +756,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(DecodeParam
     lt += f * s_ml[w].y;
   }
   const float inv = 1.f / lt;
-  const int64_t qrow = p.gen_row0 + gr;
   uint2 packed = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
-  *reinterpret_cast<uint2*>(p.out + qrow * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
+  *reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(row) * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
 }
 
 template <int D, bool FP8, int NT>
@@ -678,7 +767,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   static_assert(Cfg::kSmemBytes >= Cfg::kWarps * NT * 8 * (D + 2) * 4, "merge buffer must fit");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(p.total_splits, p.Hkv), dim3(Cfg::kThreads), Cfg::kSmemBytes, s, p);
+  return launch_pdl(kern, dim3(p.total_items, p.Hkv), dim3(Cfg::kThreads), Cfg::kSmemBytes, s, p);
 }
 
 }  // namespace
@@ -687,14 +776,17 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p);
 }
 
-cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s) {
-  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(p.G) * p.Hq)),
-                    dim3(kCombineWarps * 32), 0, s, p);
+cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.gen_rows) * p.Hq));
+  // about 8 splits per warp, 4 to 16 warps
+  if (max_splits > 64) return launch_pdl(combine_kernel<16>, grid, dim3(16 * 32), 0, s, p);
+  if (max_splits > 32) return launch_pdl(combine_kernel<8>, grid, dim3(8 * 32), 0, s, p);
+  return launch_pdl(combine_kernel<4>, grid, dim3(4 * 32), 0, s, p);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches) {
   cudaError_t e;
-  const int nt = p.group > 8 ? 2 : 1;
+  const int nt = p.nt;
   if (p.D == 128) {
     if (fp8) e = nt == 1 ? launch_decode_t<128, true, 1>(p, s) : launch_decode_t<128, true, 2>(p, s);
     else e = nt == 1 ? launch_decode_t<128, false, 1>(p, s) : launch_decode_t<128, false, 2>(p, s);

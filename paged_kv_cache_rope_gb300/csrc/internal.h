@@ -19,13 +19,17 @@ constexpr int kDecodeTile = 16;  // tokens per decode warp tile (mma.sync M)
 struct PlanLayout {
   int64_t cu_q;          // [R + 1]  exclusive prefix of context_lengths
   int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxRowsPerCta) over context requests
-  int64_t split_prefix;  // [G + 1]  prefix of ceil(L_r / kv_chunk) over generation requests
+  int64_t split_prefix;  // [G + 1]  prefix of S_r = ceil(L_r / kv_chunk) over generation requests
+  int64_t item_prefix;   // [G + 1]  prefix of S_r * column groups_r (decode CTAs per KV head)
+  int64_t part_prefix;   // [G + 1]  prefix of S_r * n_r (partial-result rows per query head)
+  int64_t item_map;      // [num_items] int2 (generation request, item index within it)
+  int64_t row_map;       // [generation rows] int2 (generation request, token index within it)
   int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
   int64_t stage_prefix;  // [C + 1]  FP8 pools: prefix of the context requests' page counts
   int64_t stage_tbl;     // [C * max_blocks] FP8 pools: block table into the bf16 staging pool
   int64_t int_words;     // total int32 words of the plan
-  int64_t part_o;        // byte offset of fp32 partial outputs [num_splits, Hq, D]
-  int64_t part_ml;       // byte offset of fp32 (m, l) pairs   [num_splits, Hq, 2]
+  int64_t part_o;        // byte offset of fp32 partial outputs [num_parts, Hq, D]
+  int64_t part_ml;       // byte offset of fp32 (m, l) pairs   [num_parts, Hq, 2]
   int64_t stage_pool;    // byte offset of the bf16 staging pool [stage_pages, 2, B, Hkv, D]
   int64_t stage_pages;   // pages in the staging pool (0 unless FP8 pool with context requests)
   int64_t total_bytes;
@@ -52,12 +56,17 @@ struct AppendParams {
   const int32_t* ctx_len;
   const int32_t* past;
   const int32_t* tbl;
+  const int32_t* pos_off;  // draft-token rotation offsets [T - gen_row0] or null
+  int32_t gen_row0;        // first packed row of the generation requests
   int32_t* d_error;
 };
 
 struct PlanParams {
   int32_t R, C, G, T, Hkv, B, expect_tiles, expect_splits, kv_chunk, expect_stage_pages;
-  int32_t Hq;
+  int32_t Hq, group;
+  int32_t cols_per_cta;  // decode score-tile columns per CTA: (token, query head) pairs
+  int32_t expect_items, expect_parts;
+  int32_t gen_row0, gen_rows;  // first packed row and number of rows of the generation requests
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words
@@ -66,7 +75,10 @@ struct PlanParams {
 };
 
 struct DecodeParams {
-  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, gen_row0, total_splits;
+  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, gen_row0, total_items;
+  int32_t gen_rows;         // packed rows of the generation requests (T - gen_row0)
+  int32_t total_parts;      // partial-result rows the workspace holds (per query head)
+  int32_t nt;               // n-tiles of 8 columns per decode CTA (1 or 2)
   const uint8_t* pool;
   float kv_scale;           // dequantisation multiplier (1 for bf16)
   float scale_log2;         // softmax_scale * log2(e)
@@ -74,8 +86,15 @@ struct DecodeParams {
   int64_t q_stride;
   uint16_t* out;            // [T, Hq*D] bf16
   const int32_t* past;
+  const int32_t* new_len;   // context_lengths
   const int32_t* tbl;
+  const int32_t* cu_q;
   const int32_t* split_prefix;
+  const int2* item_map;
+  const int2* row_map;
+  const int32_t* part_prefix;
+  const uint32_t* mask;     // draft-token packed mask rows [gen_rows, mask_words] or null
+  int32_t mask_words;
   float* part_o;
   float* part_ml;
   int32_t* d_error;
@@ -131,7 +150,7 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches);
-cudaError_t launch_combine(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s);
 cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map,

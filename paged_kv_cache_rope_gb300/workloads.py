@@ -208,13 +208,15 @@ WORKLOADS = {
     3: "decode_llama70b_gqa",
     4: "inflight_mixed_chunked",
     5: "long_context_16k_prefill",
+    6: "spec_decode_tree_gqa",
 }
 
 
 def workload(idx: int, *, kv_dtype: str = "bf16", device: str = "cpu", poison: bool = True,
              seed: int | None = None, max_gen: int | None = None) -> Batch:
-    """The five synthetic workloads (seed = workload index unless given).  ``max_gen`` keeps
-    only the first generation requests (smaller captures for profiling)."""
+    """The synthetic workloads (seed = workload index unless given): 1-5 shaped like the pages'
+    configurations, 6 a draft-token verification batch.  ``max_gen`` keeps only the first
+    generation requests (smaller captures for profiling)."""
     seed = idx if seed is None else seed
     rng = np.random.default_rng(1000 + idx)  # lengths depend on the workload only, values on seed
 
@@ -248,4 +250,9 @@ def workload(idx: int, *, kv_dtype: str = "bf16", device: str = "cpu", poison: b
         return _mk(name=WORKLOADS[5], ctx=[(16384, 0)], gen=gen, num_q_heads=32,
                           num_kv_heads=8, head_dim=128, tokens_per_block=64, kv_dtype=kv_dtype,
                           rope_base=5e5, seed=seed, device=device, poison=poison)
+    if idx == 6:  # 64 generation requests verifying 8-token draft trees, GQA 64/8, L ~ U[1024, 4096]
+        past = rng.integers(1024 - 8, 4096 - 8, size=64, endpoint=True).tolist()
+        return _mk(name=WORKLOADS[6], ctx=[], gen=[(8, int(p)) for p in past], num_q_heads=64,
+                   num_kv_heads=8, head_dim=128, tokens_per_block=32, kv_dtype=kv_dtype, seed=seed,
+                   device=device, poison=poison, draft_tree=True)
     raise ValueError(f"unknown workload {idx}")

@@ -65,7 +65,7 @@ def _fwd(L, pool, batch, Hq=32, q=0x10000, out=0x20000, ws=0x30000, ws_bytes=1 <
     (dict(B=24), -2),
     (dict(dtype=7), -2),
     (dict(types=(1, 0), lens=(1, 5), past=(9, 0)), -3),   # generation before context
-    (dict(lens=(5, 2)), -3),                               # generation with 2 tokens
+    (dict(lens=(5, 65), mb=8), -3),                        # generation beyond 64 draft tokens
     (dict(past=(0, 300)), -4),                             # exceeds 4 blocks x 64
 ])
 def test_host_rejects_bad_batches(L, mutate, code):
@@ -76,7 +76,7 @@ def test_host_rejects_bad_batches(L, mutate, code):
 def test_host_rejects_bad_heads_alignment_workspace(L):
     pool, batch, keep = _descs()
     assert _fwd(L, pool, batch, Hq=12) == -2          # 12 % 8 != 0
-    assert _fwd(L, pool, batch, Hq=256) == -2         # group 32 > 16
+    assert L.paged_attention_workspace_size(C.byref(pool), C.byref(batch), 256) > 0  # any group size plans
     assert _fwd(L, pool, batch, q=0x10004) == -5      # misaligned q
     assert _fwd(L, pool, batch, ws=0) == -6           # no workspace
     assert _fwd(L, pool, batch, ws_bytes=16) == -6    # too small
@@ -94,3 +94,15 @@ def test_append_rejects_capacity_of_rope_table(L):
     code = L.paged_kv_append_rope(C.byref(pool), C.byref(batch), 32, 0x10000, 32 * 128, 0x20000, 8 * 128,
                                   0x30000, 8 * 128, 0x10000, 32 * 128, 0x40000, 8, 0x5000, None)
     assert code == -4   # past 9 + 1 > max_pos 8
+
+
+def test_host_checks_draft_mask_words(L):
+    pool, batch, keep = _descs(lens=(5, 40), mb=4)
+    batch.d_packed_mask = 0x6000
+    batch.mask_words = 0
+    assert _fwd(L, pool, batch) == -1                 # a mask needs words
+    batch.mask_words = 1
+    assert _fwd(L, pool, batch) == -1                 # 40 draft tokens need two words per row
+    assert L.paged_attention_workspace_size(C.byref(pool), C.byref(batch), 32) == 0
+    batch.mask_words = 2
+    assert L.paged_attention_workspace_size(C.byref(pool), C.byref(batch), 32) > 0

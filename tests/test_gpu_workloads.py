@@ -1,6 +1,7 @@
-"""The five synthetic workloads at full size, launched exactly as bench.py launches them:
-bit-exact pool write image everywhere, and attention outputs against the fp64 oracle on every
-row (workloads 1-3) or on a deterministic row sample plus every generation row (4, 5)."""
+"""The synthetic workloads at full size, launched exactly as bench.py launches them: bit-exact
+pool write image everywhere, and attention outputs against the fp64 oracle on every row
+(workloads 1-3 and the draft-token batch 6) or on a deterministic row sample plus every
+generation row (4, 5)."""
 import numpy as np
 import pytest
 import torch
@@ -19,13 +20,14 @@ def _sample_rows(b: W.Batch, stride: int, tail: int) -> np.ndarray:
         if b.request_types[r] == W.REQ_CONTEXT:
             rows += list(range(row, row + n, stride)) + list(range(max(row, row + n - tail), row + n))
         else:
-            rows.append(row)
+            rows += list(range(row, row + n))  # every generation row (several for draft tokens)
         row += n
     return np.unique(np.array(rows, dtype=np.int64))
 
 
 @pytest.mark.parametrize("idx,kv_dtype,stride", [
     (1, "bf16", 1), (2, "bf16", 1), (3, "bf16", 1), (3, "fp8", 1), (4, "bf16", 29), (5, "bf16", 257),
+    (6, "bf16", 1), (6, "fp8", 1),
 ])
 def test_workload_full_size(idx, kv_dtype, stride):
     b = W.workload(idx, kv_dtype=kv_dtype, device="cuda")
