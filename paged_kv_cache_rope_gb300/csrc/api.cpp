@@ -95,7 +95,8 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int D, int heads, int64
 struct HostPlan {
   int R = 0, C = 0, G = 0, T = 0, ctx_tokens = 0, max_gen_tokens = 0;
   int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
-  int decode_nt = 1, num_items = 0, num_parts = 0;  // decode n-tiles per CTA, CTAs per KV head, partial rows
+  int decode_nt = 1, num_items = 0, num_parts = 0;  // narrow decode n-tiles per CTA, CTAs per KV head, partial rows
+  int num_witems = 0;                                // wide decode CTAs per KV head
   pkv::PlanLayout lay{};
 };
 
@@ -178,17 +179,25 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   for (int r = 0; r < hp->C; ++r)
     hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
   hp->kv_chunk = choose_kv_chunk(pool, b, hp->C);
-  // decode score-tile columns are (token, query head) pairs of one KV head: 8 or 16 per CTA,
-  // and a request whose pairs do not fit takes several column groups per split
+  // decode score-tile columns are (token, query head) pairs of one KV head.  Requests with at
+  // most kDecodeNarrowMaxCols of them take the narrow kernel (8 or 16 columns per CTA, the
+  // split's tiles shared out among the warps); wider ones the wide kernel (64 columns per CTA,
+  // one per warp-column set, every warp over every tile), in as many column groups as needed.
   const int group = Hq / pool->num_kv_heads;
-  hp->decode_nt = static_cast<int64_t>(hp->max_gen_tokens) * group > 8 ? 2 : 1;
-  const int cols = 8 * hp->decode_nt;
-  hp->num_splits = hp->max_splits = hp->num_items = hp->num_parts = 0;
+  int max_narrow = 0;
   for (int r = hp->C; r < hp->R; ++r) {
-    const int n = b->h_context_lengths[r];
+    const int cols_r = b->h_context_lengths[r] * group;
+    if (cols_r <= pkv::kDecodeNarrowMaxCols) max_narrow = std::max(max_narrow, cols_r);
+  }
+  hp->decode_nt = max_narrow > 8 ? 2 : 1;
+  const int cols = 8 * hp->decode_nt;
+  hp->num_splits = hp->max_splits = hp->num_items = hp->num_witems = hp->num_parts = 0;
+  for (int r = hp->C; r < hp->R; ++r) {
+    const int n = b->h_context_lengths[r], cols_r = n * group;
     const int s = (b->h_past_kv_lengths[r] + n + hp->kv_chunk - 1) / hp->kv_chunk;
     hp->num_splits += s;
-    hp->num_items += s * ((n * group + cols - 1) / cols);
+    if (cols_r <= pkv::kDecodeNarrowMaxCols) hp->num_items += s * ((cols_r + cols - 1) / cols);
+    else hp->num_witems += s * ((cols_r + pkv::kDecodeWideCols - 1) / pkv::kDecodeWideCols);
     hp->num_parts += s * n;
     hp->max_splits = std::max(hp->max_splits, s);
   }
@@ -199,7 +208,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   L.item_prefix = L.split_prefix + hp->G + 1;
   L.part_prefix = L.item_prefix + hp->G + 1;
   L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
-  L.row_map = L.item_map + 2LL * hp->num_items;
+  L.witem_map = L.item_map + 2LL * hp->num_items;
+  L.row_map = L.witem_map + 2LL * hp->num_witems;
   L.unit_order = L.row_map + 2LL * (hp->T - hp->ctx_tokens);
   L.stage_prefix = L.unit_order + hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
@@ -453,6 +463,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.cols_per_cta = 8 * hp.decode_nt;
   pp.expect_items = hp.num_items;
   pp.expect_parts = hp.num_parts;
+  pp.expect_witems = hp.num_witems;
   pp.gen_row0 = hp.ctx_tokens;
   pp.gen_rows = hp.T - hp.ctx_tokens;
   pp.expect_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
@@ -573,6 +584,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.gen_row0 = hp.ctx_tokens;
     dp.gen_rows = hp.T - hp.ctx_tokens;
     dp.total_items = hp.num_items;
+    dp.total_witems = hp.num_witems;
     dp.total_parts = hp.num_parts;
     dp.nt = hp.decode_nt;
     dp.pool = static_cast<const uint8_t*>(pool->pool);
@@ -587,6 +599,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.cu_q = ws + hp.lay.cu_q;
     dp.split_prefix = ws + hp.lay.split_prefix;
     dp.item_map = reinterpret_cast<const int2*>(ws + hp.lay.item_map);
+    dp.witem_map = reinterpret_cast<const int2*>(ws + hp.lay.witem_map);
     dp.row_map = reinterpret_cast<const int2*>(ws + hp.lay.row_map);
     dp.part_prefix = ws + hp.lay.part_prefix;
     dp.mask = batch->d_packed_mask;
@@ -594,12 +607,22 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_o);
     dp.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + hp.lay.part_ml);
     dp.d_error = d_error;
-    {
-      LaunchScope ls(launches, "decode_splitkv", gs);
-      e = pkv::launch_decode(dp, fp8, gs, nullptr);
+    if (hp.num_items > 0) {
+      {
+        LaunchScope ls(launches, "decode_splitkv", gs);
+        e = pkv::launch_decode(dp, fp8, false, gs);
+      }
+      if (e != cudaSuccess) return PKV_ERR_CUDA;
+      ++launches;
     }
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
-    ++launches;
+    if (hp.num_witems > 0) {
+      {
+        LaunchScope ls(launches, "decode_splitkv_wide", gs);
+        e = pkv::launch_decode(dp, fp8, true, gs);
+      }
+      if (e != cudaSuccess) return PKV_ERR_CUDA;
+      ++launches;
+    }
     if (hp.max_splits > 1) {
       {
         LaunchScope ls(launches, "combine", gs);

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   int32_t* parts = p.ws + p.lay.part_prefix;
   int2* item_map = reinterpret_cast<int2*>(p.ws + p.lay.item_map);
   int2* row_map = reinterpret_cast<int2*>(p.ws + p.lay.row_map);
+  int2* witem_map = reinterpret_cast<int2*>(p.ws + p.lay.witem_map);
   int32_t* stage = p.ws + p.lay.stage_prefix;
   const bool staging = p.expect_stage_pages > 0;
   const int C = p.C, chunk = p.kv_chunk, cols = p.cols_per_cta;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + tid;
     // a: (new tokens, context units, generation splits, staged FP8 context pages)
-    // b: (decode CTAs per KV head, partial-result rows, -, -)
+    // b: (narrow decode CTAs per KV head, partial-result rows, wide decode CTAs per KV head, -)
     Int8v x{z4, z4};
     if (r < p.R) {
       const int n = __ldg(p.ctx_len + r);
@@ -114,9 +115,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         if (staging) x.a.w = (__ldg(p.past + r) + n + p.B - 1) / p.B;
       } else {
         bad |= n < 1 || n > PKV_MAX_GEN_TOKENS;
-        const int sr = (__ldg(p.past + r) + n + chunk - 1) / chunk;
+        const int sr = (__ldg(p.past + r) + n + chunk - 1) / chunk, ncols = n * p.group;
         x.a.z = sr;
-        x.b.x = sr * ((n * p.group + cols - 1) / cols);
+        if (ncols <= kDecodeNarrowMaxCols) x.b.x = sr * ((ncols + cols - 1) / cols);
+        else x.b.z = sr * ((ncols + kDecodeWideCols - 1) / kDecodeWideCols);
         x.b.y = sr * n;
       }
     }
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         parts[gr] = ex.b.y;
         // direct maps for the decode CTAs and the combine rows (no searches there)
         for (int it = 0; it < x.b.x && ex.b.x + it < p.expect_items; ++it) item_map[ex.b.x + it] = make_int2(gr, it);
+        for (int it = 0; it < x.b.z && ex.b.z + it < p.expect_witems; ++it) witem_map[ex.b.z + it] = make_int2(gr, it);
         for (int i = 0; i < x.a.x; ++i) {
           const int row = ex.a.x + i - p.gen_row0;
           if (row >= 0 && row < p.gen_rows) row_map[row] = make_int2(gr, i);
@@ -152,7 +155,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     parts[p.G] = t.b.y;
     if (staging) stage[C] = t.a.w;
     bad |= (t.a.x != p.T) || (t.a.y != p.expect_tiles) || (t.a.z != p.expect_splits) ||
-           (t.b.x != p.expect_items) || (t.b.y != p.expect_parts) || (staging && t.a.w != p.expect_stage_pages);
+           (t.b.x != p.expect_items) || (t.b.y != p.expect_parts) || (t.b.z != p.expect_witems) ||
+           (staging && t.a.w != p.expect_stage_pages);
   }
   if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
 
@@ -223,18 +227,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 #define PKV_DECODE_SUB_BF16 1     // 16-token tiles consumed per iteration (bf16)
 #endif
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool WIDE>
 struct DecodeCfg {
+  // Narrow (WIDE = false): each warp streams its own share of the split's tiles through a ring
+  // of its own, all warps on the same columns, merged at the end.  Wide: the CTA's warps share
+  // one ring and each owns 8*NT columns of its own over every tile (no merge).
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one 16-token tile of K or V
-  static constexpr int kSub = FP8 ? 2 : PKV_DECODE_SUB_BF16;  // FP8: PV takes 32 tokens per MMA
+  static constexpr int kSub = (FP8 || WIDE) ? 2 : PKV_DECODE_SUB_BF16;  // FP8: PV takes 32 tokens per MMA
   static constexpr int kSlotBytes = 2 * kSub * kTileBytes;      // K then V of kSub tiles
-  static constexpr int kStages = FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16;
-  static constexpr int kWarpBytes = kStages * kSlotBytes;
-  static constexpr int kSmemBytes = kWarps * kWarpBytes;
+  static constexpr int kStages = WIDE ? 4 : (FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16);
+  static constexpr int kRingBytes = kStages * kSlotBytes;       // one ring
+  static constexpr int kRingsBytes = (WIDE ? 1 : kWarps) * kRingBytes;
+  static constexpr int kLoaders = WIDE ? kThreads : 32;          // threads filling one ring
 };
 
 // Physical 16-byte chunk of logical chunk c in tile row `row` (bank-conflict-free layouts for
@@ -261,10 +269,10 @@ __device__ __forceinline__ void transpose4x4_bytes(const uint32_t (&w)[4], uint3
   d[3] = __byte_perm(x1, y1, 0x7632);
 }
 
-template <int D, bool FP8, int NT>
-__global__ void __launch_bounds__(DecodeCfg<D, FP8>::kThreads)
+template <int D, bool FP8, int NT, bool WIDE>
+__global__ void __launch_bounds__(DecodeCfg<D, FP8, WIDE>::kThreads)
 decode_splitkv_kernel(DecodeParams p) {
-  using Cfg = DecodeCfg<D, FP8>;
+  using Cfg = DecodeCfg<D, FP8, WIDE>;
   constexpr int KS = D / 16;  // k-steps over the head dim / m-tiles of O^T
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -273,15 +281,16 @@ decode_splitkv_kernel(DecodeParams p) {
 
   // ---- which generation request, split and column group this CTA owns ----
   // Columns of the score tile are (token i, query head h*group + hl) pairs of this KV head,
-  // c = i*group + hl; a CTA takes HN of them (column group cg).
+  // c = i*group + hl; a CTA takes HNC of them (column group cg), a warp HN.
   constexpr int HN = NT * 8;
-  if (item >= p.total_items) return;
+  constexpr int HNC = WIDE ? Cfg::kWarps * HN : HN;
+  if (item >= (WIDE ? p.total_witems : p.total_items)) return;
   pdl_wait();
-  const int2 im = p.item_map[item];  // written by the plan kernel earlier on the stream
+  const int2 im = (WIDE ? p.witem_map : p.item_map)[item];  // written by the plan kernel
   const int gr = min(max(im.x, 0), p.G - 1), r = p.C + gr, local = im.y;
   const int n_new = __ldg(p.new_len + r);
   const int ncols = n_new * p.group;
-  const int n_cg = (ncols + HN - 1) / HN;
+  const int n_cg = (ncols + HNC - 1) / HNC;
   const int s_idx = local / max(n_cg, 1), cg = local - s_idx * n_cg;
   const int num_splits = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
   const int past = __ldg(p.past + r);
@@ -293,10 +302,12 @@ decode_splitkv_kernel(DecodeParams p) {
     return;
   }
   const int n_tiles = (t_end - t_begin + kDecodeTile - 1) / kDecodeTile;
-  const int my_first = (warp * n_tiles) / Cfg::kWarps;
-  const int my_n = ((warp + 1) * n_tiles) / Cfg::kWarps - my_first;
+  const int my_first = WIDE ? 0 : (warp * n_tiles) / Cfg::kWarps;
+  const int my_n = WIDE ? n_tiles : ((warp + 1) * n_tiles) / Cfg::kWarps - my_first;
   const int row0 = __ldg(p.cu_q + r);  // packed row of the request's token 0
-  const int col0 = cg * HN;
+  const int col0 = cg * HNC;                        // the CTA's first column
+  const int wcol0 = col0 + (WIDE ? warp * HN : 0);  // this warp's first column
+  const bool warp_cols = wcol0 < ncols;             // wide: a warp past the last pair only loads
   const int64_t part_row0 = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new;
   if (row0 < p.gen_row0 || row0 + n_new > p.gen_row0 + p.gen_rows || part_row0 + n_new > p.total_parts) {
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
@@ -310,7 +321,7 @@ decode_splitkv_kernel(DecodeParams p) {
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int c = col0 + nt * 8 + 2 * q4 + j;
+      const int c = wcol0 + nt * 8 + 2 * q4 + j;
       uint64_t v = ~0ull;
       if (c < ncols) {
         const int i = c / p.group;
@@ -326,7 +337,7 @@ decode_splitkv_kernel(DecodeParams p) {
       vis[nt][j] = v;
     }
 
-  // ---- Q fragments (B operand of S^T = K Q^T): column n = col0 + nt*8 + g8 ----
+  // ---- Q fragments (B operand of S^T = K Q^T): column n = wcol0 + nt*8 + g8 ----
   // bf16: k16 fragments.  FP8 pool: k32 E4M3 fragments of q * 2^e split as hi + lo codes; the
   // lane holds head dims [q4*D/4, (q4+1)*D/4) and k-step kk takes its bytes 8kk .. 8kk+7.
   constexpr int QW = FP8 ? D / 32 : KS;  // k-steps
@@ -335,7 +346,7 @@ decode_splitkv_kernel(DecodeParams p) {
   float colscale[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int c = col0 + nt * 8 + g8;
+    const int c = wcol0 + nt * 8 + g8;
     const bool valid = c < ncols;
     const int ci = valid ? c / p.group : 0, hl = valid ? c - ci * p.group : 0;
     const uint16_t* qh = p.q + static_cast<int64_t>(row0 + ci) * p.q_stride + static_cast<int64_t>(h * p.group + hl) * D;
@@ -392,7 +403,7 @@ decode_splitkv_kernel(DecodeParams p) {
     for (int mt = 0; mt < KS; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
   }
 
-  uint8_t* wbuf = smem + warp * Cfg::kWarpBytes;
+  uint8_t* wbuf = smem + (WIDE ? 0 : warp * Cfg::kRingBytes);
   const uint32_t wbuf_s = smem_u32(wbuf);
   const int32_t* tbl_r = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
   const int64_t row_pitch = static_cast<int64_t>(p.Hkv) * Cfg::kRowBytes;  // bytes between slots
@@ -403,15 +414,18 @@ decode_splitkv_kernel(DecodeParams p) {
   const int w_end = min(t_end, w_begin + my_n * kDecodeTile);  // this warp's tokens
   const int n_iter = (my_n + SUB - 1) / SUB;
 
-  // per-lane pieces of the 16-row tile copy that do not change from tile to tile
-  constexpr int kCopies = Cfg::kChunksPerRow / 2;
+  // per-thread pieces of the 16-row tile copy that do not change from tile to tile (a narrow
+  // warp fills its own ring, the whole CTA fills the wide ring)
+  constexpr int kTileChunks = kDecodeTile * Cfg::kChunksPerRow;
+  constexpr int kCopies = (kTileChunks + Cfg::kLoaders - 1) / Cfg::kLoaders;
+  const int loader = WIDE ? static_cast<int>(threadIdx.x) : lane;
   int cp_row[kCopies];
   uint32_t cp_dk[kCopies], cp_dv[kCopies], cp_src[kCopies];
 #pragma unroll
   for (int i = 0; i < kCopies; ++i) {
-    const int c_lin = lane + 32 * i;
+    const int c_lin = min(loader + Cfg::kLoaders * i, kTileChunks - 1);
     const int row = c_lin / Cfg::kChunksPerRow, c = c_lin % Cfg::kChunksPerRow;
-    cp_row[i] = row;
+    cp_row[i] = loader + Cfg::kLoaders * i < kTileChunks ? row : kDecodeTile;  // kDecodeTile: no copy
     cp_src[i] = static_cast<uint32_t>(row * row_pitch + c * 16);
     cp_dk[i] = row * Cfg::kRowBytes + (swz_k<D, FP8>(row, c) << 4);
     cp_dv[i] = row * Cfg::kRowBytes + (swz_v<D, FP8>(row, c) << 4);
@@ -423,20 +437,21 @@ decode_splitkv_kernel(DecodeParams p) {
     int page = (t0 < w_end && lb < p.max_blocks) ? __ldg(tbl_r + lb) : 0;
     const bool page_ok = page >= 0 && page < p.NB;
     if (!page_ok) {
-      if (lane == 0) flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+      if (loader == 0) flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
       page = 0;
     }
     const uint8_t* kbase = p.pool + (static_cast<int64_t>(page) * 2 * kv_pitch) +
                            static_cast<int64_t>(slot0) * row_pitch + static_cast<int64_t>(h) * Cfg::kRowBytes;
 #pragma unroll
     for (int i = 0; i < kCopies; ++i) {
+      if (kTileChunks % Cfg::kLoaders != 0 && cp_row[i] >= kDecodeTile) continue;  // no chunk left
       const bool ok = page_ok && (t0 + cp_row[i] < w_end);
       const uint8_t* src = kbase + cp_src[i];
       cp_async_16(sK + cp_dk[i], ok ? src : p.pool, ok ? 16u : 0u);
       cp_async_16(sV + cp_dv[i], ok ? src + kv_pitch : p.pool, ok ? 16u : 0u);
     }
   };
-  auto load_slot = [&](int it, int slot) {  // SUB consecutive tiles of this warp
+  auto load_slot = [&](int it, int slot) {  // SUB consecutive tiles of this ring
     const uint32_t base = wbuf_s + slot * Cfg::kSlotBytes;
 #pragma unroll
     for (int u = 0; u < SUB; ++u)
@@ -452,12 +467,14 @@ decode_splitkv_kernel(DecodeParams p) {
 
   for (int it = 0; it < n_iter; ++it) {
     cp_async_wait<S - 2>();
-    __syncwarp();
+    if constexpr (WIDE) __syncthreads();  // slot `it` filled by all; slot it-1 free for reuse
+    else __syncwarp();
     {
       const int nxt = it + S - 1;
       if (nxt < n_iter) load_slot(nxt, nxt % S);
       cp_async_commit();
     }
+    if (WIDE && !warp_cols) continue;  // warp-uniform: no columns of its own
     const int slot = it % S;
     const uint32_t sK0 = wbuf_s + slot * Cfg::kSlotBytes;
     const uint32_t sV0 = sK0 + SUB * Cfg::kTileBytes;
@@ -661,20 +678,25 @@ decode_splitkv_kernel(DecodeParams p) {
   }
   __syncthreads();
   const int64_t hq0 = static_cast<int64_t>(h) * p.group;
-  const int n_here = min(HN, ncols - col0);  // valid columns of this CTA
+  const int n_here = min(HNC, ncols - col0);  // valid columns of this CTA
   for (int idx = threadIdx.x; idx < n_here * D; idx += Cfg::kThreads) {
     const int cl = idx / D, d = idx - cl * D;
     const int c = col0 + cl, ci = c / p.group, hl = c - ci * p.group;
-    float M = -INFINITY;
+    float M = -INFINITY, acc = 0.f, lsum = 0.f;
+    if constexpr (WIDE) {  // column cl belongs to warp cl / HN, which saw the whole split
+      M = sm_m[cl];
+      acc = sm_o[cl * D + d];
+      lsum = sm_l[cl];
+    } else {
 #pragma unroll
-    for (int w = 0; w < Cfg::kWarps; ++w) M = fmaxf(M, sm_m[w * HN + cl]);
-    const float Mb = M == -INFINITY ? 0.f : M;  // no visible key in this split (draft masks)
-    float acc = 0.f, lsum = 0.f;
+      for (int w = 0; w < Cfg::kWarps; ++w) M = fmaxf(M, sm_m[w * HN + cl]);
+      const float Mb = M == -INFINITY ? 0.f : M;  // no visible key in this split (draft masks)
 #pragma unroll
-    for (int w = 0; w < Cfg::kWarps; ++w) {
-      const float f = ex2_approx(sm_m[w * HN + cl] - Mb);
-      acc += f * sm_o[(w * HN + cl) * D + d];
-      lsum += f * sm_l[w * HN + cl];
+      for (int w = 0; w < Cfg::kWarps; ++w) {
+        const float f = ex2_approx(sm_m[w * HN + cl] - Mb);
+        acc += f * sm_o[(w * HN + cl) * D + d];
+        lsum += f * sm_l[w * HN + cl];
+      }
     }
     acc *= FP8 ? p.kv_scale * (1.f / 256.f) : p.kv_scale;  // FP8: P entered the MMA as 256 p
     if (num_splits == 1) {
@@ -760,14 +782,16 @@ __global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
   *reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(row) * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
 }
 
-template <int D, bool FP8, int NT>
+template <int D, bool FP8, int NT, bool WIDE>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
-  using Cfg = DecodeCfg<D, FP8>;
-  auto kern = decode_splitkv_kernel<D, FP8, NT>;
-  static_assert(Cfg::kSmemBytes >= Cfg::kWarps * NT * 8 * (D + 2) * 4, "merge buffer must fit");
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  using Cfg = DecodeCfg<D, FP8, WIDE>;
+  auto kern = decode_splitkv_kernel<D, FP8, NT, WIDE>;
+  constexpr int kMerge = Cfg::kWarps * NT * 8 * (D + 2) * 4;  // the epilogue's staging
+  constexpr int kSmem = Cfg::kRingsBytes > kMerge ? Cfg::kRingsBytes : kMerge;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(p.total_items, p.Hkv), dim3(Cfg::kThreads), Cfg::kSmemBytes, s, p);
+  const int items = WIDE ? p.total_witems : p.total_items;
+  return launch_pdl(kern, dim3(items, p.Hkv), dim3(Cfg::kThreads), kSmem, s, p);
 }
 
 }  // namespace
@@ -784,18 +808,18 @@ cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s
   return launch_pdl(combine_kernel<4>, grid, dim3(4 * 32), 0, s, p);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches) {
-  cudaError_t e;
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, bool wide, cudaStream_t s) {
+  if (wide) {  // 16 columns per warp, 64 per CTA
+    if (p.D == 128) return fp8 ? launch_decode_t<128, true, 2, true>(p, s) : launch_decode_t<128, false, 2, true>(p, s);
+    return fp8 ? launch_decode_t<64, true, 2, true>(p, s) : launch_decode_t<64, false, 2, true>(p, s);
+  }
   const int nt = p.nt;
   if (p.D == 128) {
-    if (fp8) e = nt == 1 ? launch_decode_t<128, true, 1>(p, s) : launch_decode_t<128, true, 2>(p, s);
-    else e = nt == 1 ? launch_decode_t<128, false, 1>(p, s) : launch_decode_t<128, false, 2>(p, s);
-  } else {
-    if (fp8) e = nt == 1 ? launch_decode_t<64, true, 1>(p, s) : launch_decode_t<64, true, 2>(p, s);
-    else e = nt == 1 ? launch_decode_t<64, false, 1>(p, s) : launch_decode_t<64, false, 2>(p, s);
+    if (fp8) return nt == 1 ? launch_decode_t<128, true, 1, false>(p, s) : launch_decode_t<128, true, 2, false>(p, s);
+    return nt == 1 ? launch_decode_t<128, false, 1, false>(p, s) : launch_decode_t<128, false, 2, false>(p, s);
   }
-  if (e == cudaSuccess && launches) ++*launches;
-  return e;
+  if (fp8) return nt == 1 ? launch_decode_t<64, true, 1, false>(p, s) : launch_decode_t<64, true, 2, false>(p, s);
+  return nt == 1 ? launch_decode_t<64, false, 1, false>(p, s) : launch_decode_t<64, false, 2, false>(p, s);
 }
 
 }  // namespace pkv

@@ -14,6 +14,10 @@ constexpr int kCtxTileM = 128;   // query rows per context-attention tile (tcgen
 constexpr int kCtxRowsPerCta = 256;  // a context CTA owns two query tiles
 constexpr int kCtxTileN = 128;   // keys per context-attention KV tile
 constexpr int kDecodeTile = 16;  // tokens per decode warp tile (mma.sync M)
+// Generation requests whose score tile has at most this many (token, query head) columns run
+// on the narrow decode kernel, wider ones (draft tokens, large query groups) on the wide one.
+constexpr int kDecodeNarrowMaxCols = 16;
+constexpr int kDecodeWideCols = 64;  // columns per wide-decode CTA (4 warps x 16)
 
 // Device-side plan written by plan_kernel into the front of the workspace (int32 words).
 struct PlanLayout {
@@ -23,6 +27,7 @@ struct PlanLayout {
   int64_t item_prefix;   // [G + 1]  prefix of S_r * column groups_r (decode CTAs per KV head)
   int64_t part_prefix;   // [G + 1]  prefix of S_r * n_r (partial-result rows per query head)
   int64_t item_map;      // [num_items] int2 (generation request, item index within it)
+  int64_t witem_map;     // [num_witems] the same for the wide decode kernel's CTAs
   int64_t row_map;       // [generation rows] int2 (generation request, token index within it)
   int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
   int64_t stage_prefix;  // [C + 1]  FP8 pools: prefix of the context requests' page counts
@@ -65,7 +70,7 @@ struct PlanParams {
   int32_t R, C, G, T, Hkv, B, expect_tiles, expect_splits, kv_chunk, expect_stage_pages;
   int32_t Hq, group;
   int32_t cols_per_cta;  // decode score-tile columns per CTA: (token, query head) pairs
-  int32_t expect_items, expect_parts;
+  int32_t expect_items, expect_parts, expect_witems;
   int32_t gen_row0, gen_rows;  // first packed row and number of rows of the generation requests
   const int32_t* ctx_len;
   const int32_t* past;
@@ -75,7 +80,7 @@ struct PlanParams {
 };
 
 struct DecodeParams {
-  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, gen_row0, total_items;
+  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, gen_row0, total_items, total_witems;
   int32_t gen_rows;         // packed rows of the generation requests (T - gen_row0)
   int32_t total_parts;      // partial-result rows the workspace holds (per query head)
   int32_t nt;               // n-tiles of 8 columns per decode CTA (1 or 2)
@@ -91,6 +96,7 @@ struct DecodeParams {
   const int32_t* cu_q;
   const int32_t* split_prefix;
   const int2* item_map;
+  const int2* witem_map;
   const int2* row_map;
   const int32_t* part_prefix;
   const uint32_t* mask;     // draft-token packed mask rows [gen_rows, mask_words] or null
@@ -149,7 +155,9 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 
 cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, cudaStream_t s, int* launches);
+// wide = false: requests with at most 16 score columns (KV split across warps); true: wider
+// requests (columns split across warps, 64 per CTA).
+cudaError_t launch_decode(const DecodeParams& p, bool fp8, bool wide, cudaStream_t s);
 cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s);
 cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
