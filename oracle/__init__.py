@@ -30,7 +30,8 @@ _LIB = None
 def lib():
     global _LIB
     if _LIB is None:
-        path = _build.build()
+        # a mutated build of oracle.c can be swapped in by the planted-mistake tests
+        path = os.environ.get("PKV_ORACLE_LIB") or _build.build()
         L = C.CDLL(path)
         P = C.c_void_p
         i32, i64, f32, f64 = C.c_int32, C.c_int64, C.c_float, C.c_double
