@@ -7,6 +7,7 @@ this package imports nothing from it: the two sides share only the seeded input 
 Functions (all on host numpy arrays):
   bf16_from_f32 / f32_from_bf16     IEEE round-to-nearest-even bf16
   e4m3_encode / e4m3_decode         OCP FP8 E4M3, RNE with saturation to +-448
+  int8_encode                       INT8 codes: nearest integer, ties to even, saturating
   rope_table                        fp32 (cos, sin) table computed in fp64
   rope32 / rope64                   GPT-NeoX rotate-half rotation (fp32 recipe / exact fp64)
   append_rope                       O1 write image: q_out rows and pool bytes after the append
@@ -70,6 +71,8 @@ def lib():
         L.orc_f32_to_bf16_array.restype = None
         L.orc_f32_to_e4m3_array.argtypes = [P, i64, P]
         L.orc_f32_to_e4m3_array.restype = None
+        L.orc_f32_to_int8_array.argtypes = [P, i64, P]
+        L.orc_f32_to_int8_array.restype = None
         L.orc_e4m3_to_f64_array.argtypes = [P, i64, P]
         L.orc_e4m3_to_f64_array.restype = None
         L.orc_num_threads.argtypes = []
@@ -119,6 +122,20 @@ def e4m3_encode(x) -> np.ndarray:
     return out.reshape(shape)
 
 
+def int8_encode(x) -> np.ndarray:
+    """fp32 values -> int8 codes: nearest integer, ties to even, saturated to [-128, 127]."""
+    shape = np.shape(x)
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).reshape(-1)
+    out = np.empty(x.shape, dtype=np.int8)
+    lib().orc_f32_to_int8_array(_ptr(x), int(x.size), _ptr(out))
+    return out.reshape(shape)
+
+
+def _kind(kv_fp8, kv_int8) -> int:
+    """Pool element type for the C side: 0 bf16, 1 FP8 E4M3, 2 INT8."""
+    return 2 if kv_int8 else int(bool(kv_fp8))
+
+
 # --- RoPE -------------------------------------------------------------------------------------
 
 def rope_table(base: float, head_dim: int, max_pos: int) -> np.ndarray:
@@ -148,7 +165,7 @@ def rope64(x: np.ndarray, base: float, pos: int) -> np.ndarray:
 
 def append_rope(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim,
                 tokens_per_block, num_blocks, kv_fp8, inv_scale, q_bits, k_bits, v_bits, cs,
-                pool, q_out=None):
+                pool, q_out=None, kv_int8=False):
     """O1 write image.  Updates ``pool`` (uint16 bf16 bits or uint8 e4m3 codes, any shape,
     C-contiguous) in place and returns (status, q_out bits [T, Hq*D])."""
     new_len = np.ascontiguousarray(new_len, dtype=np.int32)
@@ -165,7 +182,7 @@ def append_rope(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_d
     st = lib().orc_append_rope(
         int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
         int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
-        int(num_blocks), int(bool(kv_fp8)), float(inv_scale),
+        int(num_blocks), _kind(kv_fp8, kv_int8), float(inv_scale),
         _ptr(q_bits), int(q_bits.shape[1]) if T else 0, _ptr(k_bits), int(k_bits.shape[1]) if T else 0,
         _ptr(v_bits), int(v_bits.shape[1]) if T else 0, _ptr(cs), int(cs.shape[0]),
         _ptr(q_out), int(q_out.shape[1]), _ptr(pool))
@@ -175,7 +192,7 @@ def append_rope(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_d
 def append_rope_ex(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim,
                    tokens_per_block, num_blocks, kv_fp8, inv_scale, q_bits, k_bits, v_bits, cs,
                    pool, style=0, rotary_dim=0, q_norm_w=None, k_norm_w=None, norm_eps=1e-6,
-                   pos_offset=None, q_out=None):
+                   pos_offset=None, q_out=None, kv_int8=False):
     """O1 with the variants: style 0 rotate-half / 1 interleaved, rotary_dim (0 = head_dim),
     optional RMSNorm weights for q and k heads.  ``cs`` has rotary_dim / 2 pairs per row.
     ``pos_offset`` (int32 [T], one per packed row) rotates row (r, i) for position
@@ -194,7 +211,7 @@ def append_rope_ex(*, new_len, past, block_table, num_q_heads, num_kv_heads, hea
     kw = None if k_norm_w is None else np.ascontiguousarray(k_norm_w, dtype=np.float32)
     common = (int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
               int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
-              int(num_blocks), int(bool(kv_fp8)), float(inv_scale),
+              int(num_blocks), _kind(kv_fp8, kv_int8), float(inv_scale),
               _ptr(q_bits), int(q_bits.shape[1]) if T else 0, _ptr(k_bits), int(k_bits.shape[1]) if T else 0,
               _ptr(v_bits), int(v_bits.shape[1]) if T else 0, _ptr(cs), int(cs.shape[0]), int(style),
               int(rotary_dim), None if qw is None else _ptr(qw), None if kw is None else _ptr(kw),
@@ -210,7 +227,7 @@ def append_rope_ex(*, new_len, past, block_table, num_q_heads, num_kv_heads, hea
 
 def attention(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim,
               tokens_per_block, num_blocks, kv_fp8, kv_scale, pool, q, softmax_scale,
-              rows=None, num_contexts=None, gen_mask=None):
+              rows=None, num_contexts=None, gen_mask=None, kv_int8=False):
     """O2 fp64 attention.  ``q`` is float64 [T, Hq, D] (or [T, Hq*D]); returns
     (status, out float64 [T, Hq, D]); rows not in ``rows`` (when given) are NaN.
     ``gen_mask`` (uint32 [generation rows, words], with ``num_contexts``) gives each token of a
@@ -229,7 +246,7 @@ def attention(*, new_len, past, block_table, num_q_heads, num_kv_heads, head_dim
         rows_p, n = None, T
     common = (int(new_len.shape[0]), _ptr(new_len), _ptr(past), _ptr(tbl), int(tbl.shape[1]),
               int(num_q_heads), int(num_kv_heads), int(head_dim), int(tokens_per_block),
-              int(num_blocks), int(bool(kv_fp8)), float(kv_scale), _ptr(pool), _ptr(q),
+              int(num_blocks), _kind(kv_fp8, kv_int8), float(kv_scale), _ptr(pool), _ptr(q),
               float(softmax_scale), rows_p, n)
     if gen_mask is None:
         st = lib().orc_attention(*common, _ptr(out))

@@ -27,6 +27,7 @@
  *   - The rotation is done in fp32 from an fp32 (cos, sin) table that is computed in fp64 and
  *     rounded once:  y_j = fma(x_j, c, -(x_{j+D/2}*s)),  y_{j+D/2} = fma(x_{j+D/2}, c, x_j*s).
  *     This fixes every rounding, so the written pool bytes are a single exact value.
+ *   - kv_kind selects the pool's element type: 0 bf16, 1 FP8 E4M3, 2 INT8.
  *   - FP8 is OCP E4M3 (bias 7, max normal 448, no infinities, NaN = S.1111.111), encoded
  *     round-to-nearest-even with saturation to +-448; code = e4m3(fp32(x * inv_scale)),
  *     value = code * scale, one scale per pool.
@@ -111,6 +112,25 @@ uint8_t orc_f32_to_e4m3(float x) {
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* INT8 ("INT8 KV Cache": the cache stored as 8-bit integers, quantised on write with            */
+/* kv_scale_orig_quant and turned back into real values with kv_scale_quant_orig on read --     */
+/* "TensorRT-LLM 1.0 源码学习笔记" 6.4 "量化").  Reading: the nearest integer, ties to the even    */
+/* one, saturated to [-128, 127]; NaN encodes as 0.  value = code * scale.                       */
+/* ------------------------------------------------------------------------------------------ */
+int8_t orc_f32_to_int8(float x) {
+  if (isnan(x)) return 0;
+  double a = (double)x;
+  if (a >= 127.0) return 127;
+  if (a <= -128.0) return -128;
+  double f = floor(a), diff = a - f;
+  double n;
+  if (diff > 0.5) n = f + 1.0;
+  else if (diff < 0.5) n = f;
+  else n = (fmod(f, 2.0) == 0.0) ? f : f + 1.0; /* exact tie: the even neighbour */
+  return (int8_t)n;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* RoPE (GPT-NeoX rotate-half).                                                               */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -171,7 +191,7 @@ static size_t pool_index(int blk, int kv, int slot, int h, int d, int B, int Hkv
 int orc_append_rope(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                     const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                     int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                    int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                    int32_t num_blocks, int32_t kv_kind, float inv_scale, const uint16_t* q,
                     int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
                     int64_t v_stride, const float* cs, int32_t max_pos, uint16_t* q_out,
                     int64_t q_out_stride, void* pool) {
@@ -204,10 +224,14 @@ int orc_append_rope(int32_t num_requests, const int32_t* new_len, const int32_t*
           uint16_t vb = v[row * v_stride + (int64_t)h * D + d];
           size_t ik = pool_index(blk, 0, slot, h, d, B, Hkv, D);
           size_t iv = pool_index(blk, 1, slot, h, d, B, Hkv, D);
-          if (kv_is_fp8) {
+          if (kv_kind == 1) {
             uint8_t* p8 = (uint8_t*)pool;
             p8[ik] = orc_f32_to_e4m3(y[d] * inv_scale);
             p8[iv] = orc_f32_to_e4m3(orc_bf16_to_f32(vb) * inv_scale);
+          } else if (kv_kind == 2) {
+            int8_t* p8 = (int8_t*)pool;
+            p8[ik] = orc_f32_to_int8(y[d] * inv_scale);
+            p8[iv] = orc_f32_to_int8(orc_bf16_to_f32(vb) * inv_scale);
           } else {
             uint16_t* p16 = (uint16_t*)pool;
             p16[ik] = orc_f32_to_bf16(y[d]);
@@ -226,12 +250,13 @@ int orc_append_rope(int32_t num_requests, const int32_t* new_len, const int32_t*
 /* O2: attention in fp64 over the pool, per the definition                                    */
 /*   out[row, h, :] = sum_t softmax_t(scale * <q[row, h, :], K_t>) V_t,  t = 0 .. past_r + i,  */
 /* with K_t, V_t read through the block table (page tbl[r][t / B], slot t % B) and decoded     */
-/* exactly (bf16 -> double; e4m3 code -> value * kv_scale).  q is given in fp64 [T, Hq, D].    */
+/* exactly (bf16 -> double; e4m3 or int8 code -> value * kv_scale).  q is fp64 [T, Hq, D].      */
 /* rows == NULL computes every row; otherwise only the listed packed-row indices.              */
 /* Returns ORC_ERR_BAD_PAGE if a needed page id is out of range (that row is left as NaN).     */
 /* ------------------------------------------------------------------------------------------ */
-static double pool_value(const void* pool, int kv_is_fp8, double kv_scale, size_t idx) {
-  if (kv_is_fp8) return orc_e4m3_to_f64(((const uint8_t*)pool)[idx]) * kv_scale;
+static double pool_value(const void* pool, int kv_kind, double kv_scale, size_t idx) {
+  if (kv_kind == 1) return orc_e4m3_to_f64(((const uint8_t*)pool)[idx]) * kv_scale;
+  if (kv_kind == 2) return (double)((const int8_t*)pool)[idx] * kv_scale;
   return (double)orc_bf16_to_f32(((const uint16_t*)pool)[idx]);
 }
 
@@ -245,7 +270,7 @@ static double pool_value(const void* pool, int kv_is_fp8, double kv_scale, size_
 static int attention_core(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                           const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                          int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
+                          int32_t num_blocks, int32_t kv_kind, double kv_scale, const void* pool,
                           const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
                           int32_t num_contexts, const uint32_t* gen_mask, int32_t mask_words,
                           double* out) {
@@ -294,7 +319,7 @@ static int attention_core(int32_t num_requests, const int32_t* new_len, const in
         if (blk < 0 || blk >= num_blocks) { bad = 1; break; }
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-          dot += qv[d] * pool_value(pool, kv_is_fp8, kv_scale, pool_index(blk, 0, (int)(t % B), hk, d, B, Hkv, D));
+          dot += qv[d] * pool_value(pool, kv_kind, kv_scale, pool_index(blk, 0, (int)(t % B), hk, d, B, Hkv, D));
         s[t] = softmax_scale * dot;
       }
       if (bad) {
@@ -313,7 +338,7 @@ static int attention_core(int32_t num_requests, const int32_t* new_len, const in
         int blk = block_table[(size_t)r * max_blocks_per_seq + (int)(t / B)];
         double w_t = s[t] / z;
         for (int d = 0; d < D; ++d)
-          o[d] += w_t * pool_value(pool, kv_is_fp8, kv_scale, pool_index(blk, 1, (int)(t % B), hk, d, B, Hkv, D));
+          o[d] += w_t * pool_value(pool, kv_kind, kv_scale, pool_index(blk, 1, (int)(t % B), hk, d, B, Hkv, D));
       }
       free(s);
     }
@@ -326,11 +351,11 @@ static int attention_core(int32_t num_requests, const int32_t* new_len, const in
 int orc_attention(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                   const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                   int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                  int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
+                  int32_t num_blocks, int32_t kv_kind, double kv_scale, const void* pool,
                   const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
                   double* out) {
   return attention_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
-                        num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, kv_scale, pool,
+                        num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_kind, kv_scale, pool,
                         q, softmax_scale, rows, num_rows, num_requests, NULL, 0, out);
 }
 
@@ -338,12 +363,12 @@ int orc_attention(int32_t num_requests, const int32_t* new_len, const int32_t* p
 int orc_attention_spec(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                        const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                       int32_t num_blocks, int32_t kv_is_fp8, double kv_scale, const void* pool,
+                       int32_t num_blocks, int32_t kv_kind, double kv_scale, const void* pool,
                        const double* q, double softmax_scale, const int64_t* rows, int64_t num_rows,
                        int32_t num_contexts, const uint32_t* gen_mask, int32_t mask_words,
                        double* out) {
   return attention_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
-                        num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, kv_scale, pool,
+                        num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_kind, kv_scale, pool,
                         q, softmax_scale, rows, num_rows, num_contexts, gen_mask, mask_words, out);
 }
 
@@ -363,6 +388,10 @@ void orc_f32_to_bf16_array(const float* x, int64_t n, uint16_t* out) {
 
 void orc_f32_to_e4m3_array(const float* x, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_e4m3(x[i]);
+}
+
+void orc_f32_to_int8_array(const float* x, int64_t n, int8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_int8(x[i]);
 }
 
 void orc_e4m3_to_f64_array(const uint8_t* c, int64_t n, double* out) {
@@ -407,7 +436,7 @@ static void rms_norm(float* x, int32_t D, const float* w, double eps) {
 static int append_core(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                        const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                       int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                       int32_t num_blocks, int32_t kv_kind, float inv_scale, const uint16_t* q,
                        int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
                        int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
                        int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
@@ -445,10 +474,14 @@ static int append_core(int32_t num_requests, const int32_t* new_len, const int32
           uint16_t vb = v[row * v_stride + (int64_t)h * D + d];
           size_t ik = pool_index(blk, 0, slot, h, d, B, Hkv, D);
           size_t iv = pool_index(blk, 1, slot, h, d, B, Hkv, D);
-          if (kv_is_fp8) {
+          if (kv_kind == 1) {
             uint8_t* p8 = (uint8_t*)pool;
             p8[ik] = orc_f32_to_e4m3(y[d] * inv_scale);
             p8[iv] = orc_f32_to_e4m3(orc_bf16_to_f32(vb) * inv_scale);
+          } else if (kv_kind == 2) {
+            int8_t* p8 = (int8_t*)pool;
+            p8[ik] = orc_f32_to_int8(y[d] * inv_scale);
+            p8[iv] = orc_f32_to_int8(orc_bf16_to_f32(vb) * inv_scale);
           } else {
             uint16_t* p16 = (uint16_t*)pool;
             p16[ik] = orc_f32_to_bf16(y[d]);
@@ -466,13 +499,13 @@ static int append_core(int32_t num_requests, const int32_t* new_len, const int32
 int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                        const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                       int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                       int32_t num_blocks, int32_t kv_kind, float inv_scale, const uint16_t* q,
                        int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
                        int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
                        int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
                        double norm_eps, uint16_t* q_out, int64_t q_out_stride, void* pool) {
   return append_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
-                     num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, inv_scale, q,
+                     num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_kind, inv_scale, q,
                      q_stride, k, k_stride, v, v_stride, cs, max_pos, style, rotary_dim, q_norm_w,
                      k_norm_w, norm_eps, NULL, q_out, q_out_stride, pool);
 }
@@ -486,14 +519,14 @@ int orc_append_rope_ex(int32_t num_requests, const int32_t* new_len, const int32
 int orc_append_rope_spec(int32_t num_requests, const int32_t* new_len, const int32_t* past,
                          const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t tokens_per_block,
-                         int32_t num_blocks, int32_t kv_is_fp8, float inv_scale, const uint16_t* q,
+                         int32_t num_blocks, int32_t kv_kind, float inv_scale, const uint16_t* q,
                          int64_t q_stride, const uint16_t* k, int64_t k_stride, const uint16_t* v,
                          int64_t v_stride, const float* cs, int32_t max_pos, int32_t style,
                          int32_t rotary_dim, const float* q_norm_w, const float* k_norm_w,
                          double norm_eps, const int32_t* pos_offset, uint16_t* q_out,
                          int64_t q_out_stride, void* pool) {
   return append_core(num_requests, new_len, past, block_table, max_blocks_per_seq, num_q_heads,
-                     num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_is_fp8, inv_scale, q,
+                     num_kv_heads, head_dim, tokens_per_block, num_blocks, kv_kind, inv_scale, q,
                      q_stride, k, k_stride, v, v_stride, cs, max_pos, style, rotary_dim, q_norm_w,
                      k_norm_w, norm_eps, pos_offset, q_out, q_out_stride, pool);
 }

@@ -28,6 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libpaged_kv.so")
 PKV_OK = 0
 PKV_BF16 = 0
 PKV_FP8_E4M3 = 1
+PKV_INT8 = 2
 PKV_REQ_CONTEXT = 0
 PKV_REQ_GENERATION = 1
 PKV_DEVERR_BAD_PAGE = 1
@@ -131,8 +132,9 @@ def _ptr(t: torch.Tensor | None) -> int | None:
 
 @dataclasses.dataclass
 class KVPool:
-    """One layer's paged KV pool [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim]
-    (bf16, or uint8 holding E4M3 codes with one per-pool scale)."""
+    """One layer's paged KV pool [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim]:
+    bf16; uint8 / float8_e4m3fn holding E4M3 codes; or int8 codes -- the 8-bit kinds with one
+    per-pool scale."""
     data: torch.Tensor
     kv_scale_quant_orig: float = 1.0
     kv_scale_orig_quant: float = 1.0
@@ -140,15 +142,21 @@ class KVPool:
     def __post_init__(self):
         assert self.data.dim() == 5 and self.data.shape[1] == 2, "pool must be [NB, 2, B, Hkv, D]"
         assert self.data.is_contiguous()
-        assert self.data.dtype in (torch.bfloat16, torch.uint8, torch.float8_e4m3fn)
+        assert self.data.dtype in (torch.bfloat16, torch.uint8, torch.float8_e4m3fn, torch.int8)
+
+    @property
+    def dtype(self) -> int:
+        if self.data.dtype == torch.bfloat16:
+            return PKV_BF16
+        return PKV_INT8 if self.data.dtype == torch.int8 else PKV_FP8_E4M3
 
     @property
     def fp8(self) -> bool:
-        return self.data.dtype != torch.bfloat16
+        return self.dtype == PKV_FP8_E4M3
 
     def c(self) -> PkvPool:
         NB, _, B, Hkv, D = self.data.shape
-        return PkvPool(self.data.data_ptr(), PKV_FP8_E4M3 if self.fp8 else PKV_BF16, NB, B, Hkv, D,
+        return PkvPool(self.data.data_ptr(), self.dtype, NB, B, Hkv, D,
                        float(self.kv_scale_quant_orig), float(self.kv_scale_orig_quant))
 
 

@@ -16,8 +16,8 @@ and "KVCacheManager 的三个对外接口"; page adg.csdn.net/69730cc6, section 
 Recipe: lengths as stated per workload; page placement is a seeded random permutation of all
 pool pages (pages never referenced stay unused); q, k, v and the cached K/V history are i.i.d.
 N(0, 1) rounded to bf16; the history is treated as already rotated.  Pool slots holding no
-cached token are poisoned with NaN (bf16 0x7FC0, e4m3 0x7F) when ``poison`` is set, else zero,
-and unused block-table entries are -1.
+cached token are poisoned with NaN (bf16 0x7FC0, e4m3 0x7F; int8, having no NaN, -128) when
+``poison`` is set, else zero, and unused block-table entries are -1.
 """
 from __future__ import annotations
 
@@ -29,6 +29,7 @@ import torch
 
 BF16_NAN = 0x7FC0
 E4M3_NAN = 0x7F
+INT8_POISON = -128  # int8 has no NaN: unused slots hold the most negative code
 REQ_CONTEXT = 0
 REQ_GENERATION = 1
 
@@ -41,7 +42,7 @@ class Batch:
     head_dim: int
     tokens_per_block: int
     num_blocks: int
-    kv_dtype: str                 # "bf16" or "fp8"
+    kv_dtype: str                 # "bf16", "fp8" or "int8"
     rope_base: float
     request_types: np.ndarray     # int32 [R]
     new_len: np.ndarray           # int32 [R]
@@ -50,9 +51,9 @@ class Batch:
     q: torch.Tensor               # bf16 [T, Hq*D]
     k: torch.Tensor               # bf16 [T, Hkv*D]
     v: torch.Tensor               # bf16 [T, Hkv*D]
-    pool: torch.Tensor            # [NB, 2, B, Hkv, D], bf16 or uint8 (e4m3 codes)
-    pool_bf16: torch.Tensor | None  # fp8 batches: the unquantised bf16 twin of ``pool``
-    kv_scale: float               # dequantisation multiplier (amax / 448), 1.0 for bf16
+    pool: torch.Tensor            # [NB, 2, B, Hkv, D], bf16, uint8 (e4m3 codes) or int8 codes
+    pool_bf16: torch.Tensor | None  # 8-bit batches: the unquantised bf16 twin of ``pool``
+    kv_scale: float               # dequantisation multiplier (amax / 448 or amax / 127), 1 for bf16
     inv_scale: float              # fp32(1 / kv_scale), the quantisation multiplier
     # draft-token trees (generation requests of several tokens), else None: per generation
     # row, the RoPE position offset (depth in the tree) and the packed mask row (bit j of word
@@ -105,7 +106,7 @@ def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list, num_q_heads:
     ``draft_tree`` draws a seeded random candidate tree per generation request (token 0 the
     root, each later token a child of an earlier one) and fills ``position_offsets`` and
     ``packed_mask``; without it the draft tokens form a chain (plain causal order)."""
-    assert kv_dtype in ("bf16", "fp8")
+    assert kv_dtype in ("bf16", "fp8", "int8")
     B, Hkv, D = tokens_per_block, num_kv_heads, head_dim
     gen = [(1, L - 1) if np.ndim(L) == 0 else (int(L[0]), int(L[1])) for L in gen]
     new_len = np.array([n for n, _ in ctx] + [n for n, _ in gen], dtype=np.int32)
@@ -181,12 +182,20 @@ def make_batch(*, name: str, ctx: list[tuple[int, int]], gen: list, num_q_heads:
         return Batch(name, Hq, Hkv, D, B, num_blocks, kv_dtype, rope_base, types, new_len,
                      past, table, q, k, v, bf16_pool, None, 1.0, 1.0, offsets, mask)
 
-    # FP8 pool: one per-tensor scale, amax over every K/V value drawn (history and new k/v)
+    # 8-bit pool: one per-tensor scale, amax over every K/V value drawn (history and new k/v)
     amax = max(float(hist.float().abs().max()) if n_hist else 0.0,
                float(k.float().abs().max()) if T else 0.0,
                float(v.float().abs().max()) if T else 0.0, 1e-30)
-    kv_scale = float(np.float32(amax / 448.0))
+    kv_scale = float(np.float32(amax / (127.0 if kv_dtype == "int8" else 448.0)))
     inv_scale = float(np.float32(1.0 / kv_scale))
+    if kv_dtype == "int8":  # history codes by torch's round-half-even and a clamp
+        codes = (hist.float() * inv_scale).round().clamp(-128.0, 127.0).to(torch.int8)
+        i8_pool = torch.empty(num_blocks, 2, B, Hkv, D, dtype=torch.int8, device=device)
+        i8_pool.fill_(INT8_POISON if poison else 0)
+        i8_pool[tok_blk, 0, tok_slot] = codes[:, 0]
+        i8_pool[tok_blk, 1, tok_slot] = codes[:, 1]
+        return Batch(name, Hq, Hkv, D, B, num_blocks, kv_dtype, rope_base, types, new_len, past,
+                     table, q, k, v, i8_pool, bf16_pool, kv_scale, inv_scale, offsets, mask)
     codes = (hist.float() * inv_scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
     fp8_pool = torch.empty(num_blocks, 2, B, Hkv, D, dtype=torch.uint8, device=device)
     fp8_pool.fill_(E4M3_NAN if poison else 0)

@@ -13,6 +13,8 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 MUTATIONS = {
     "bf16_round_up_on_ties": ("return (uint16_t)((lo & 1u) ? lo + 1 : lo);", "return (uint16_t)(lo + 1);"),
+    "int8_ties_away": ("else n = (fmod(f, 2.0) == 0.0) ? f : f + 1.0;", "else n = f + 1.0;"),
+    "int8_symmetric_clamp": ("if (a <= -128.0) return -128;", "if (a <= -127.0) return -127;"),
     "e4m3_overflow_to_nan": ("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 448.0) return (uint8_t)(sign | 0x7F);"),
     "rope_sign": ("    y[j] = fmaf(a, c, -bs);", "    y[j] = fmaf(a, c, bs);"),
     "rope_pairs_swapped": ("    float a = x[j], b = x[j + half];", "    float b = x[j], a = x[j + half];"),

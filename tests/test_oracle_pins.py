@@ -81,6 +81,19 @@ def test_e4m3_saturates_and_nan():
     assert oracle.e4m3_encode(np.float32([np.nan]))[0] == 0x7F
 
 
+def test_int8_encode_matches_torch_round_and_clamp():
+    """torch.round rounds halves to even, then clamp to [-128, 127] -- an independent route."""
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.normal(0, 30, 200_000), rng.uniform(-200, 200, 100_000)]).astype(np.float32)
+    ties = np.arange(-140, 140, dtype=np.float32) + np.float32(0.5)  # every exact half in range
+    x = np.concatenate([x, ties, np.float32([0.0, -0.0, 127.0, -128.0, 127.49, -128.49, 1e9, -np.inf, np.inf])])
+    ours = oracle.int8_encode(x)
+    ref = torch.from_numpy(x.copy()).double().round().clamp(-128, 127).to(torch.int8).numpy()
+    assert np.array_equal(ours, ref)
+    assert oracle.int8_encode(np.float32([np.nan]))[0] == 0
+    assert oracle.int8_encode(np.float32([0.5, 1.5, 2.5, -2.5, 126.5])).tolist() == [0, 2, 2, -2, 126]
+
+
 # ----------------------------------------------------------------------------------------------
 # RoPE
 # ----------------------------------------------------------------------------------------------
@@ -180,7 +193,8 @@ def _run_append(b: W.Batch, pool_np: np.ndarray):
         new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
         num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
         num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8", inv_scale=b.inv_scale,
-        q_bits=_np_bits(b.q), k_bits=_np_bits(b.k), v_bits=_np_bits(b.v), cs=cs, pool=pool_np)
+        q_bits=_np_bits(b.q), k_bits=_np_bits(b.k), v_bits=_np_bits(b.v), cs=cs, pool=pool_np,
+        kv_int8=b.kv_dtype == "int8")
 
 
 def _small_mixed(kv_dtype="bf16", seed=11):
@@ -189,7 +203,7 @@ def _small_mixed(kv_dtype="bf16", seed=11):
                         seed=seed)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 def test_write_image_addresses_and_untouched_bytes(kv_dtype):
     b = _small_mixed(kv_dtype)
     before = _np_bits(b.pool).copy()
@@ -213,9 +227,13 @@ def test_write_image_addresses_and_untouched_bytes(kv_dtype):
                 if kv_dtype == "bf16":
                     kref = torch.from_numpy(krot).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
                     vref = vb[row, h * D:(h + 1) * D]
-                else:
+                elif kv_dtype == "fp8":
                     enc = lambda a: torch.from_numpy((a * np.float32(b.inv_scale)).astype(np.float32)).to(
                         torch.float8_e4m3fn).view(torch.uint8).numpy()
+                    kref, vref = enc(krot), enc(vval)
+                else:
+                    enc = lambda a: torch.from_numpy((a * np.float32(b.inv_scale)).astype(np.float32)).round().clamp(
+                        -128, 127).to(torch.int8).numpy()
                     kref, vref = enc(krot), enc(vval)
                 assert np.array_equal(view5[blk, 0, slot, h], kref)
                 assert np.array_equal(view5[blk, 1, slot, h], vref)
@@ -265,7 +283,7 @@ def _oracle_attention(b: W.Batch, pool_np, q64, rows=None, kv_fp8=None, kv_scale
         num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
         num_blocks=b.num_blocks, kv_fp8=(b.kv_dtype == "fp8") if kv_fp8 is None else kv_fp8,
         kv_scale=b.kv_scale if kv_scale is None else kv_scale, pool=pool_np, q=q64,
-        softmax_scale=b.softmax_scale, rows=rows)
+        softmax_scale=b.softmax_scale, rows=rows, kv_int8=b.kv_dtype == "int8" and kv_fp8 is None)
 
 
 def _after_append(b):
@@ -282,6 +300,8 @@ def _sdpa_reference(b: W.Batch, pool_np, q64):
     D, Hkv, Hq, B = b.head_dim, b.num_kv_heads, b.num_q_heads, b.tokens_per_block
     if b.kv_dtype == "fp8":
         vals = torch.from_numpy(oracle.e4m3_decode(pool_np)) * b.kv_scale
+    elif b.kv_dtype == "int8":
+        vals = torch.from_numpy(pool_np.astype(np.float64)) * b.kv_scale
     else:
         vals = torch.from_numpy(oracle.f32_from_bf16(pool_np).astype(np.float64))
     pool5 = vals.reshape(b.num_blocks, 2, B, Hkv, D)
@@ -304,7 +324,7 @@ def _sdpa_reference(b: W.Batch, pool_np, q64):
     return np.concatenate(outs, axis=0)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("seed", [11, 12])
 def test_attention_matches_sdpa_bruteforce(kv_dtype, seed):
     b = _small_mixed(kv_dtype, seed)
