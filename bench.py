@@ -1,6 +1,6 @@
 """Benchmark of one inflight-batch layer step (RoPE + append, then paged attention) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--kv-dtype bf16|fp8]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--kv-dtype bf16|fp8|int8]
                     [--impl ours|reference] [--no-cpu-baseline]
 
 A step is the whole hot path over one batch: paged_kv_append_rope + paged_attention_forward
@@ -44,7 +44,7 @@ METRIC = "decode attn KV GB/s (% of HBM peak); prefill TFLOP/s (% BF16 peak); to
 def work_of(b) -> dict:
     """Decode KV bytes (each KV head read once per request), context flops (causal part only,
     2 flops per MAC for QK^T and PV), append bytes."""
-    esz = 1 if b.kv_dtype == "fp8" else 2
+    esz = 1 if b.kv_dtype != "bf16" else 2
     D, Hq, Hkv = b.head_dim, b.num_q_heads, b.num_kv_heads
     gen = b.request_types == 1
     L = (b.past + b.new_len).astype(np.int64)
@@ -161,24 +161,29 @@ class OracleSample:
         self.cs = oracle.rope_table(b.rope_base, b.head_dim, b.max_pos)
         self.gen = [r for r in range(b.num_requests) if b.request_types[r] == 1]
         self.row_of = np.concatenate([[0], np.cumsum(b.new_len)[:-1]]).astype(np.int64)
+        self.gen_row0 = int(b.new_len[:b.num_contexts].sum())
         self.i = 0
-        self.esz = 1 if b.kv_dtype == "fp8" else 2
+        self.esz = 1 if b.kv_dtype != "bf16" else 2
 
     def step(self) -> int:
-        """Process one generation request; returns the KV bytes it read."""
+        """Process one generation request (all of its tokens); returns the KV bytes it read."""
         b, o = self.b, self.oracle
         r = self.gen[self.i % len(self.gen)]
         self.i += 1
-        row = int(self.row_of[r])
-        sl = slice(row, row + 1)
+        row, n = int(self.row_of[r]), int(b.new_len[r])
+        sl = slice(row, row + n)
+        g = slice(row - self.gen_row0, row - self.gen_row0 + n)  # rows of the draft-token arrays
         kw = dict(new_len=b.new_len[r:r + 1], past=b.past[r:r + 1], block_table=b.block_table[r:r + 1],
                   num_q_heads=b.num_q_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
-                  tokens_per_block=b.tokens_per_block, num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8")
-        st, q_out = o.append_rope(**kw, inv_scale=b.inv_scale, q_bits=self.q[sl], k_bits=self.k[sl],
-                                  v_bits=self.v[sl], cs=self.cs, pool=self.pool)
+                  tokens_per_block=b.tokens_per_block, num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8",
+                  kv_int8=b.kv_dtype == "int8")
+        st, q_out = o.append_rope_ex(**kw, inv_scale=b.inv_scale, q_bits=self.q[sl], k_bits=self.k[sl],
+                                     v_bits=self.v[sl], cs=self.cs, pool=self.pool,
+                                     pos_offset=None if b.position_offsets is None else b.position_offsets[g])
         q64 = o.f32_from_bf16(q_out).astype(np.float64)
-        o.attention(**kw, kv_scale=b.kv_scale, pool=self.pool, q=q64, softmax_scale=b.softmax_scale)
-        L = int(b.past[r]) + 1
+        o.attention(**kw, kv_scale=b.kv_scale, pool=self.pool, q=q64, softmax_scale=b.softmax_scale,
+                    num_contexts=0, gen_mask=None if b.packed_mask is None else b.packed_mask[g])
+        L = int(b.past[r]) + n
         return L * 2 * b.num_kv_heads * b.head_dim * self.esz
 
 
@@ -382,7 +387,7 @@ def run_ours(args):
         ach = work["ctx_flops"] / (kern_ms["context_attn"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": pk_["bf16"], "unit": "TFLOP/s",
                 "frac": ach / pk_["bf16"], "kernel": "context_attn", "peak_source": pk_["src"]}
-    roof["traffic"] = ncu_traffic(dominant, b.name + ("_fp8" if b.kv_dtype == "fp8" else ""))
+    roof["traffic"] = ncu_traffic(dominant, b.name + ("" if b.kv_dtype == "bf16" else "_" + b.kv_dtype))
 
     kernels = {}
     for n, ms in kern_ms.items():
@@ -401,7 +406,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else "fp8-e4m3 KV / bf16 q",
+        "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "fp8-e4m3 KV / bf16 q", "int8": "int8 KV / bf16 q"}[b.kv_dtype],
         "data": "synthetic (seeded N(0,1) q/k/v and cached KV, random page placement)",
         "config": {"workload": b.name, "requests": b.num_requests, "contexts": b.num_contexts,
                    "num_tokens": b.num_tokens, "num_q_heads": b.num_q_heads,
@@ -467,7 +472,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"])
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8", "int8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-gen", type=int, default=None,

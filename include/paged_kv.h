@@ -66,8 +66,9 @@ typedef struct CUstream_st* pkv_stream_t; /* == cudaStream_t; NULL = legacy defa
  * verification, [REPORT] 1.4 "推测解码技术": spec_decoding_max_generation_length). */
 #define PKV_MAX_GEN_TOKENS 64
 
-/* ---- KV-pool element type ([ARCH] "KVCacheManager 的三个对外接口": kv_cache_dtype) --------- */
-typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
+/* ---- KV-pool element type ([ARCH] "KVCacheManager 的三个对外接口": kv_cache_dtype; [NOTES] 6.4
+ * "量化": FP8 and "INT8 KV Cache") ------------------------------------------------------------- */
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_INT8 = 2 } pkv_dtype;
 
 /* ---- request phase ([REPORT] 1.1 host_request_types) --------------------------------------- */
 typedef enum { PKV_REQ_CONTEXT = 0, PKV_REQ_GENERATION = 1 } pkv_req_type;
@@ -75,9 +76,9 @@ typedef enum { PKV_REQ_CONTEXT = 0, PKV_REQ_GENERATION = 1 } pkv_req_type;
 /*
  * One layer's KV pool.  Layout [num_blocks, 2, tokens_per_block, num_kv_heads, head_dim],
  * row-major, K at index 0 and V at index 1 of dim 1 ([ARCH] "KVCacheManager 的三个对外接口",
- * get_buffers).  Element type bf16, or one byte per element (OCP FP8 E4M3) with one scale for
- * the whole pool ([NOTES] 6.4 "量化": quantise on write with kv_scale_orig_quant, dequantise on
- * read with kv_scale_quant_orig).
+ * get_buffers).  Element type bf16, or one byte per element (OCP FP8 E4M3 or int8 codes) with
+ * one scale for the whole pool ([NOTES] 6.4 "量化": quantise on write with kv_scale_orig_quant,
+ * dequantise on read with kv_scale_quant_orig).
  */
 typedef struct pkv_pool {
   void* pool;                /* device, 16-byte aligned                                        */
@@ -86,9 +87,10 @@ typedef struct pkv_pool {
   int32_t tokens_per_block;  /* 16, 32, 64 or 128                                               */
   int32_t num_kv_heads;      /* Hkv                                                            */
   int32_t head_dim;          /* D: 64 or 128                                                   */
-  float kv_scale_quant_orig; /* FP8: dequantisation multiplier (value = code * this); ignored for bf16 */
-  float kv_scale_orig_quant; /* FP8: quantisation multiplier (code = e4m3(x * this)), normally
-                                (float)(1 / kv_scale_quant_orig); ignored for bf16            */
+  float kv_scale_quant_orig; /* 8-bit pools: dequantisation multiplier (value = code * this);
+                                ignored for bf16                                               */
+  float kv_scale_orig_quant; /* 8-bit pools: quantisation multiplier (code = enc(x * this)),
+                                normally (float)(1 / kv_scale_quant_orig); ignored for bf16    */
 } pkv_pool;
 
 /*
@@ -158,7 +160,9 @@ int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float
  *   q_out[row, h*D:(h+1)*D] = bf16(rope(q[row, h*D:(h+1)*D], p))          for h < Hq
  *   pool[page, 0, slot, h, :] = bf16(rope(k[row, h*D:...], p))            for h < Hkv
  *   pool[page, 1, slot, h, :] = v[row, h*D:...]
- * (FP8 pool: e4m3(x * kv_scale_orig_quant) with round-to-nearest-even, saturating to +-448.)
+ * (FP8 pool: e4m3(x * kv_scale_orig_quant) with round-to-nearest-even, saturating to +-448;
+ * INT8 pool: the nearest integer to x * kv_scale_orig_quant, ties to even, saturated to
+ * [-128, 127].)
  * rope(x, p): y_j = x_j c - x_{j+D/2} s, y_{j+D/2} = x_{j+D/2} c + x_j s, (c, s) = table[p][j],
  * evaluated in fp32 as fma(x_j, c, -(x_{j+D/2} * s)) and fma(x_{j+D/2}, c, x_j * s).
  *   q, k, v      device bf16 rows [T, Hq*D], [T, Hkv*D], [T, Hkv*D] with row strides in
@@ -211,8 +215,8 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
 /*
  * Workspace bytes paged_attention_forward needs for this pool geometry, batch and head count
  * ([NOTES] 五 5.1: the runtime checks that the scratch workspace is large enough): the device
- * plan, fp32 split-KV partials, and for FP8 pools with context requests a bf16 staging copy of
- * those requests' pages.  0 on invalid arguments.
+ * plan, fp32 split-KV partials, and for 8-bit pools with context requests a bf16 staging copy
+ * of those requests' pages.  0 on invalid arguments.
  */
 size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* batch,
                                       int32_t num_q_heads);
@@ -224,7 +228,7 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  * Kernel 内部"; [ARCH] "AttentionMetadata 的字段与它的含义": flattened (num_tokens, heads*D)
  * tensors).  For packed row (r, i), query head h, KV head h / (Hq/Hkv), position p = past_r + i:
  *   out[row, h*D:(h+1)*D] = sum_{t in V(r,i)} softmax_t(softmax_scale * <q_rot[row,h], K_t>) V_t
- * with K_t, V_t read through the block table (FP8 pool: value = code * kv_scale_quant_orig),
+ * with K_t, V_t read through the block table (8-bit pool: value = code * kv_scale_quant_orig),
  * fp32 accumulation, bf16 output.  The visible keys V(r, i) are t <= p (causal), except for
  * generation requests with d_packed_mask set: every t < past_r, plus past_r + j for the new
  * tokens j that the token's mask row selects, plus the token itself.  Generation requests of
@@ -235,7 +239,7 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  *   workspace    device, at least paged_attention_workspace_size bytes, 256-byte aligned;
  *                its contents need not be initialised and are scratch after the call
  *   d_error      device int32 error bits as above
- * Context rows use a tcgen05/TMEM tensor-core kernel (for FP8 pools after staging the context
+ * Context rows use a tcgen05/TMEM tensor-core kernel (for 8-bit pools after staging the context
  * requests' pages as exact bf16 code values in the workspace), generation rows a split-KV decode
  * kernel plus a log-sum-exp combine.  When the batch has both kinds of rows, the generation
  * kernels run on the library's auxiliary stream for this device (highest stream priority),
@@ -275,7 +279,7 @@ int paged_attention_forward_noalloc(const pkv_pool* pool, const pkv_batch* batch
 int32_t paged_kv_last_launch_count(void);
 
 /* Name of the i-th kernel the last call on this thread enqueued ("append_rope", "plan",
- * "stage_fp8", "context_attn", "decode_splitkv", "decode_splitkv_wide", "combine"), or NULL
+ * "stage_q8", "context_attn", "decode_splitkv", "decode_splitkv_wide", "combine"), or NULL
  * when i is out of range. */
 const char* paged_kv_last_launch_name(int32_t i);
 

@@ -102,13 +102,13 @@ struct HostPlan {
 
 int validate_pool(const pkv_pool* pool) {
   if (!pool || !pool->pool) return PKV_ERR_INVALID_ARGUMENT;
-  if (pool->dtype != PKV_BF16 && pool->dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (pool->dtype != PKV_BF16 && pool->dtype != PKV_FP8_E4M3 && pool->dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
   if (pool->num_blocks <= 0 || pool->num_kv_heads <= 0) return PKV_ERR_INVALID_ARGUMENT;
   const int B = pool->tokens_per_block;
   if (B != 16 && B != 32 && B != 64 && B != 128) return PKV_ERR_UNSUPPORTED;
   if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (!aligned16(pool->pool)) return PKV_ERR_ALIGNMENT;
-  if (pool->dtype == PKV_FP8_E4M3 &&
+  if (pool->dtype != PKV_BF16 &&
       !(std::isfinite(pool->kv_scale_quant_orig) && std::isfinite(pool->kv_scale_orig_quant) &&
         pool->kv_scale_quant_orig > 0.f && pool->kv_scale_orig_quant > 0.f))
     return PKV_ERR_INVALID_ARGUMENT;
@@ -168,13 +168,13 @@ int choose_kv_chunk(const pkv_pool* pool, const pkv_batch* b, int C) {
   const int64_t target = static_cast<int64_t>(device_sm_count()) * 4;
   int64_t chunk = (total * pool->num_kv_heads + target - 1) / std::max<int64_t>(target, 1);
   chunk = (chunk + 15) / 16 * 16;
-  const int64_t token_bytes = 2LL * pool->head_dim * (pool->dtype == PKV_FP8_E4M3 ? 1 : 2);
+  const int64_t token_bytes = 2LL * pool->head_dim * (pool->dtype != PKV_BF16 ? 1 : 2);
   const int64_t cap = std::max<int64_t>(64, (PKV_DECODE_SPLIT_KB * 1024LL / token_bytes) / 16 * 16);
   return static_cast<int>(std::min<int64_t>(cap, std::max<int64_t>(64, chunk)));
 }
 
 void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
-  const bool staging = pool->dtype == PKV_FP8_E4M3 && hp->C > 0;
+  const bool staging = pool->dtype != PKV_BF16 && hp->C > 0;
   hp->num_tiles = 0;
   for (int r = 0; r < hp->C; ++r)
     hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
@@ -414,7 +414,7 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
   cudaError_t e;
   {
     LaunchScope ls(0, "append_rope", reinterpret_cast<cudaStream_t>(stream));
-    e = pkv::launch_append(p, pool->dtype == PKV_FP8_E4M3, reinterpret_cast<cudaStream_t>(stream));
+    e = pkv::launch_append(p, pool->dtype, reinterpret_cast<cudaStream_t>(stream));
   }
   if (e == cudaSuccess) g_last_launches = 1;
   return cuda_status(e);
@@ -443,7 +443,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   if (!aligned16(q_rot) || !aligned16(out) || (q_row_stride & 7)) return PKV_ERR_ALIGNMENT;
   if (q_row_stride < static_cast<int64_t>(num_q_heads) * D) return PKV_ERR_INVALID_ARGUMENT;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARGUMENT;
-  const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+  const bool q8 = pool->dtype != PKV_BF16;  // 8-bit codes with one pool scale
   plan_attention(pool, batch, num_q_heads, &hp);
   if (!workspace || workspace_bytes < static_cast<size_t>(hp.lay.total_bytes)) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGNMENT;
@@ -501,13 +501,14 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   AuxJoin aux_join{aux, s};
 
   if (hp.C > 0) {
-    // FP8 pools: stage the context requests' pages as bf16 first (exact values, own table)
+    // 8-bit pools: stage the context requests' pages as bf16 first (exact values, own table)
     const void* ctx_pool = pool->pool;
     const int32_t* ctx_tbl = batch->d_block_offsets;
     int64_t ctx_blocks = pool->num_blocks;
-    if (fp8) {
+    if (q8) {
       pkv::StageParams sp{};
       sp.C = hp.C;
+      sp.kv_dtype = pool->dtype;
       sp.B = pool->tokens_per_block;
       sp.Hkv = Hkv;
       sp.D = D;
@@ -523,8 +524,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       sp.stage_pool = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + hp.lay.stage_pool);
       sp.d_error = d_error;
       {
-        LaunchScope ls(launches, "stage_fp8", cs);
-        e = pkv::launch_stage_fp8(sp, cs);
+        LaunchScope ls(launches, "stage_q8", cs);
+        e = pkv::launch_stage_q8(sp, cs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;
@@ -558,8 +559,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.pool = static_cast<const uint8_t*>(ctx_pool);
     cp.out = static_cast<uint16_t*>(out);
     cp.out_stride = static_cast<int64_t>(num_q_heads) * D;
-    cp.scale_log2 = fp8 ? scale_log2 * pool->kv_scale_quant_orig : scale_log2;
-    cp.out_scale = fp8 ? pool->kv_scale_quant_orig : 1.0f;
+    cp.scale_log2 = q8 ? scale_log2 * pool->kv_scale_quant_orig : scale_log2;
+    cp.out_scale = q8 ? pool->kv_scale_quant_orig : 1.0f;
     cp.d_error = d_error;
     {
       LaunchScope ls(launches, "context_attn", cs);
@@ -588,7 +589,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.total_parts = hp.num_parts;
     dp.nt = hp.decode_nt;
     dp.pool = static_cast<const uint8_t*>(pool->pool);
-    dp.kv_scale = fp8 ? pool->kv_scale_quant_orig : 1.0f;
+    dp.kv_scale = q8 ? pool->kv_scale_quant_orig : 1.0f;
     dp.scale_log2 = scale_log2;
     dp.q = static_cast<const uint16_t*>(q_rot);
     dp.q_stride = q_row_stride;
@@ -610,7 +611,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     if (hp.num_items > 0) {
       {
         LaunchScope ls(launches, "decode_splitkv", gs);
-        e = pkv::launch_decode(dp, fp8, false, gs);
+        e = pkv::launch_decode(dp, pool->dtype, false, gs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;
@@ -618,7 +619,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     if (hp.num_witems > 0) {
       {
         LaunchScope ls(launches, "decode_splitkv_wide", gs);
-        e = pkv::launch_decode(dp, fp8, true, gs);
+        e = pkv::launch_decode(dp, pool->dtype, true, gs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;

@@ -8,7 +8,7 @@
 //
 // HBM-bound.  One thread handles 16 elements of one head of one token (8 rotation pairs, or a
 // pass-through part of a partially rotated head): two 16-byte loads, two 16-byte stores (8-byte
-// stores into an FP8 pool).  Variants: rotate-half or interleaved pairs, partial rotary dims,
+// stores into an FP8 or INT8 pool).  Variants: rotate-half or interleaved pairs, partial rotary dims,
 // an optional RMSNorm of q / k heads reduced across the head's lanes with shuffles, and
 // draft tokens rotated for past + offset (adg.csdn.net/69730cc6 section 1.4,
 // spec_decoding_position_offsets) while stored at slot past + i.
@@ -75,7 +75,25 @@ __device__ __forceinline__ uint2 to_e4m3x8(const float (&y)[8], float inv_scale)
   return make_uint2(w[0], w[1]);
 }
 
-template <bool FP8>
+// 8 fp32 values * inv_scale -> 8 int8 codes: nearest integer, ties to even, saturated to
+// [-128, 127] (NaN -> 0), packed little-endian.
+__device__ __forceinline__ uint2 to_int8x8(const float (&y)[8], float inv_scale) {
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float f = __fmul_rn(y[4 * h + e], inv_scale);
+      const int c = min(max(__float2int_rn(f), -128), 127);
+      acc |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * e);
+    }
+    w[h] = acc;
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+template <int KVK>  // pool element kind: 0 bf16, 1 E4M3 codes, 2 int8 codes
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParams p) {
   extern __shared__ int32_t s_cu[];  // [R + 1] exclusive prefix of context_lengths
   // ---- block-wide exclusive scan of context_lengths (chunks of blockDim.x) ----
@@ -127,7 +145,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
   const int rot_tasks = p.rot >> 4, rhalf = p.rot >> 1;
   const int tasks_per_token = (p.Hq + 2 * p.Hkv) * per_head;
   const int64_t total = static_cast<int64_t>(p.T) * tasks_per_token;
-  const size_t esz = FP8 ? 1 : 2;
+  const size_t esz = KVK != 0 ? 1 : 2;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kAppendThreads;
   for (int64_t wbase = static_cast<int64_t>(blockIdx.x) * kAppendThreads + (tid & ~31); wbase < total;
        wbase += stride) {  // warp-uniform loop: inactive lanes still join the norm shuffles
@@ -256,7 +274,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
     const int is_v = kind == 2;
     const size_t elem = ((static_cast<size_t>(page) * 2 + is_v) * p.B + slot) * p.Hkv * D + static_cast<size_t>(h) * D;
     uint8_t* dst = static_cast<uint8_t*>(p.pool) + elem * esz;
-    if constexpr (FP8) {
+    if constexpr (KVK == 2) {
+      *reinterpret_cast<uint2*>(dst + offA) = to_int8x8(ya, p.inv_scale);
+      *reinterpret_cast<uint2*>(dst + offB) = to_int8x8(yb, p.inv_scale);
+    } else if constexpr (KVK == 1) {
       *reinterpret_cast<uint2*>(dst + offA) = to_e4m3x8(ya, p.inv_scale);
       *reinterpret_cast<uint2*>(dst + offB) = to_e4m3x8(yb, p.inv_scale);
     } else if (is_v) {  // V is stored as given
@@ -271,7 +292,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
 
 }  // namespace
 
-cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s) {
+cudaError_t launch_append(const AppendParams& p, int kv_dtype, cudaStream_t s) {
   static int num_sms = 0;
   if (num_sms == 0) {
     int dev = 0;
@@ -285,7 +306,9 @@ cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const size_t smem = sizeof(int32_t) * (p.R + 1);
-  auto kern = fp8 ? append_rope_kernel<true> : append_rope_kernel<false>;
+  auto kern = kv_dtype == PKV_FP8_E4M3 ? append_rope_kernel<1>
+              : kv_dtype == PKV_INT8   ? append_rope_kernel<2>
+                                       : append_rope_kernel<0>;
   if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kAppendThreads), smem, s, p);
 }

@@ -111,6 +111,25 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// Four int8 codes (byte j = code j) -> two f16x2 with lo = (code0, code1), hi = (code2, code3),
+// each value 1152 + code exactly: with the sign bit flipped a byte reads u = code + 128, and the
+// f16 pattern 0x64:u is 1024 + u (f16 values are spaced exactly 1 apart in [1024, 2048)).
+__device__ __forceinline__ void i8x4_to_f16x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+}
+// The same with the bias removed: lo, hi hold the codes themselves (exact in f16).
+__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  i8x4_to_f16x2_biased(w, lo, hi);
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+  __half2 l = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+  __half2 h = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+}
+constexpr float kI8Bias = 1152.f;
+
 // 2^x with the MUFU instruction alone (flush-to-zero; relative error ~2^-22, and results below
 // 2^-126 -- probabilities of masked or vanishing keys -- become 0).  -inf gives 0.
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -26,9 +26,9 @@
 //   TMEM columns: S_A | S_B | O_A | O_B (4 x 128 of 128 lanes).  tcgen05 work issued by one
 //   thread completes in order, so a commit after S_X(j) also covers PV_X(j-1): the softmax of
 //   tile j may rescale O_X as soon as S_X(j) has landed.
-// FP8 pools: stage_fp8_kernel first copies the context requests' pages into a bf16 staging pool
-// (exact code values) with its own block table; this kernel then runs unchanged on it, with the
-// pool scale folded into the score scale and into the output scale.
+// 8-bit pools (E4M3 or int8 codes): stage_q8_kernel first copies the context requests' pages
+// into a bf16 staging pool (exact code values) with its own block table; this kernel then runs
+// unchanged on it, with the pool scale folded into the score scale and into the output scale.
 // Rows past the request's end and keys past the causal limit are masked by select (never by
 // arithmetic on the loaded values); V rows past the sequence end are zeroed before PV, so
 // stale or poisoned pool slots cannot reach the output.  Every wait is bounded.
@@ -417,10 +417,11 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   }
 }
 
-// ---- FP8 pools: stage the context requests' pages as bf16 (exact code values) ----
+// ---- 8-bit pools: stage the context requests' pages as bf16 (exact code values) ----
 constexpr int kStageThreads = 256;
 
-__global__ void __launch_bounds__(kStageThreads) stage_fp8_kernel(const StageParams p) {
+template <bool I8>  // false: E4M3 codes, true: int8 codes
+__global__ void __launch_bounds__(kStageThreads) stage_q8_kernel(const StageParams p) {
   const int gp = blockIdx.x;  // staging page
   pdl_wait();
   int lo = 0, hi = p.C - 1;
@@ -452,9 +453,14 @@ __global__ void __launch_bounds__(kStageThreads) stage_fp8_kernel(const StagePar
     for (int k = 0; k < 4; ++k) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> (16 * h)));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        o[2 * k + h] = pack_bf16x2(f.x, f.y);  // exact: every E4M3 value is a bf16 value
+        if constexpr (I8) {  // exact: every int8 is a bf16 value (8 significant bits)
+          const int c0 = static_cast<int8_t>(w[k] >> (16 * h)), c1 = static_cast<int8_t>(w[k] >> (16 * h + 8));
+          o[2 * k + h] = pack_bf16x2(static_cast<float>(c0), static_cast<float>(c1));
+        } else {
+          const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> (16 * h)));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          o[2 * k + h] = pack_bf16x2(f.x, f.y);  // exact: every E4M3 value is a bf16 value
+        }
       }
     }
     dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -464,8 +470,9 @@ __global__ void __launch_bounds__(kStageThreads) stage_fp8_kernel(const StagePar
 
 }  // namespace
 
-cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s) {
-  return launch_pdl(stage_fp8_kernel, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
+cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s) {
+  if (p.kv_dtype == PKV_INT8) return launch_pdl(stage_q8_kernel<true>, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
+  return launch_pdl(stage_q8_kernel<false>, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
 }
 
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, bool fp8,

@@ -24,6 +24,10 @@
 // hi + lo E4M3 codes and both halves are multiplied into the same fp32 accumulator, which keeps
 // about 8 significant bits of each -- the precision of a bf16 operand -- with no per-element
 // conversion of the pool.  The per-pool scale is applied to scores and outputs in fp32.
+// INT8 pools: the codes become exact f16 values in registers (sign bit flipped into the
+// mantissa of 1024.0: a permute and a packed subtract per two codes) and run on
+// mma.sync m16n8k16 f16 with Q and P in f16; V keeps its +1152 bias through the MMA, which
+// comes off at the end as 1152 times the row sum of the same rounded P.
 #include <math.h>
 
 #include "common.cuh"
@@ -227,19 +231,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 #define PKV_DECODE_SUB_BF16 1     // 16-token tiles consumed per iteration (bf16)
 #endif
 
-template <int D, bool FP8, bool WIDE>
+// Pool element kinds of the decode kernel (the pkv_dtype values).
+constexpr int kKvBf16 = 0, kKvE4m3 = 1, kKvInt8 = 2;
+
+template <int D, int KVK, bool WIDE>
 struct DecodeCfg {
   // Narrow (WIDE = false): each warp streams its own share of the split's tiles through a ring
   // of its own, all warps on the same columns, merged at the end.  Wide: the CTA's warps share
   // one ring and each owns 8*NT columns of its own over every tile (no merge).
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+  static constexpr bool kBytes = KVK != kKvBf16;  // one byte per element (E4M3 or INT8 codes)
+  static constexpr int kRowBytes = D * (kBytes ? 1 : 2);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kTileBytes = kDecodeTile * kRowBytes;  // one 16-token tile of K or V
-  static constexpr int kSub = (FP8 || WIDE) ? 2 : PKV_DECODE_SUB_BF16;  // FP8: PV takes 32 tokens per MMA
+  static constexpr int kSub = (kBytes || WIDE) ? 2 : PKV_DECODE_SUB_BF16;  // E4M3: PV takes 32 tokens per MMA
   static constexpr int kSlotBytes = 2 * kSub * kTileBytes;      // K then V of kSub tiles
-  static constexpr int kStages = WIDE ? 4 : (FP8 ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16);
+  static constexpr int kStages = WIDE ? 4 : (kBytes ? PKV_DECODE_STAGES_FP8 : PKV_DECODE_STAGES_BF16);
   static constexpr int kRingBytes = kStages * kSlotBytes;       // one ring
   static constexpr int kRingsBytes = (WIDE ? 1 : kWarps) * kRingBytes;
   static constexpr int kLoaders = WIDE ? kThreads : 32;          // threads filling one ring
@@ -247,14 +255,14 @@ struct DecodeCfg {
 
 // Physical 16-byte chunk of logical chunk c in tile row `row` (bank-conflict-free layouts for
 // the fragment loads below; each is a bijection inside a row).
-template <int D, bool FP8>
+template <int D, bool BYTES>
 __device__ __forceinline__ int swz_k(int row, int c) {
-  if constexpr (FP8 && D == 64) return c ^ (row & 3);
+  if constexpr (BYTES && D == 64) return c ^ (row & 3);
   else return c ^ (row & 7);
 }
-template <int D, bool FP8>
+template <int D, bool BYTES>
 __device__ __forceinline__ int swz_v(int row, int c) {
-  if constexpr (!FP8) return c ^ (row & 7);
+  if constexpr (!BYTES) return c ^ (row & 7);
   else if constexpr (D == 128) return c ^ (((row >> 1) & 3) << 1);
   else return c ^ (((row >> 1) & 1) << 1);
 }
@@ -269,10 +277,11 @@ __device__ __forceinline__ void transpose4x4_bytes(const uint32_t (&w)[4], uint3
   d[3] = __byte_perm(x1, y1, 0x7632);
 }
 
-template <int D, bool FP8, int NT, bool WIDE>
-__global__ void __launch_bounds__(DecodeCfg<D, FP8, WIDE>::kThreads)
+template <int D, int KVK, int NT, bool WIDE>
+__global__ void __launch_bounds__(DecodeCfg<D, KVK, WIDE>::kThreads)
 decode_splitkv_kernel(DecodeParams p) {
-  using Cfg = DecodeCfg<D, FP8, WIDE>;
+  using Cfg = DecodeCfg<D, KVK, WIDE>;
+  constexpr bool BYTES = Cfg::kBytes, FP8 = KVK == kKvE4m3, I8 = KVK == kKvInt8;
   constexpr int KS = D / 16;  // k-steps over the head dim / m-tiles of O^T
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -340,6 +349,8 @@ decode_splitkv_kernel(DecodeParams p) {
   // ---- Q fragments (B operand of S^T = K Q^T): column n = wcol0 + nt*8 + g8 ----
   // bf16: k16 fragments.  FP8 pool: k32 E4M3 fragments of q * 2^e split as hi + lo codes; the
   // lane holds head dims [q4*D/4, (q4+1)*D/4) and k-step kk takes its bytes 8kk .. 8kk+7.
+  // INT8 pool: k16 f16 fragments of q * 2^e over the same per-lane segment, k-step kk taking its
+  // elements 4kk .. 4kk+3 (the K codes are converted to f16 in the same order).
   constexpr int QW = FP8 ? D / 32 : KS;  // k-steps
   uint32_t qb[NT][QW][2];
   uint32_t ql[NT][FP8 ? QW : 1][2];
@@ -350,7 +361,7 @@ decode_splitkv_kernel(DecodeParams p) {
     const bool valid = c < ncols;
     const int ci = valid ? c / p.group : 0, hl = valid ? c - ci * p.group : 0;
     const uint16_t* qh = p.q + static_cast<int64_t>(row0 + ci) * p.q_stride + static_cast<int64_t>(h * p.group + hl) * D;
-    if constexpr (!FP8) {
+    if constexpr (!BYTES) {
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         qb[nt][kk][0] = valid ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * q4) : 0u;
@@ -371,17 +382,26 @@ decode_splitkv_kernel(DecodeParams p) {
       amax = warp_max_xor(amax, 2);
       int ex = 0;
       if (amax > 0.f) frexpf(amax, &ex);
-      const float up = ldexpf(1.f, 8 - ex);  // amax * up lies in [128, 256), inside E4M3's 448
+      // E4M3: amax * up in [128, 256), inside E4M3's 448; f16: in [2^13, 2^14), far from 65504
+      const float up = ldexpf(1.f, (I8 ? 14 : 8) - ex);
+      if constexpr (I8) {
 #pragma unroll
-      for (int kk = 0; kk < QW; ++kk) {
+        for (int kk = 0; kk < KS; ++kk) {
+          qb[nt][kk][0] = pack_f16x2(x[4 * kk] * up, x[4 * kk + 1] * up);
+          qb[nt][kk][1] = pack_f16x2(x[4 * kk + 2] * up, x[4 * kk + 3] * up);
+        }
+      } else {
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const float* xs = x + 8 * kk + 4 * b;
-          uint32_t h01, l01, h23, l23;
-          split_e4m3x2(xs[0] * up, xs[1] * up, h01, l01);
-          split_e4m3x2(xs[2] * up, xs[3] * up, h23, l23);
-          qb[nt][kk][b] = h01 | (h23 << 16);
-          ql[nt][kk][b] = l01 | (l23 << 16);
+        for (int kk = 0; kk < QW; ++kk) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const float* xs = x + 8 * kk + 4 * b;
+            uint32_t h01, l01, h23, l23;
+            split_e4m3x2(xs[0] * up, xs[1] * up, h01, l01);
+            split_e4m3x2(xs[2] * up, xs[3] * up, h23, l23);
+            qb[nt][kk][b] = h01 | (h23 << 16);
+            ql[nt][kk][b] = l01 | (l23 << 16);
+          }
         }
       }
       // score columns 2*q4, 2*q4+1 belong to heads held by lanes (2*q4)*4 and (2*q4+1)*4
@@ -427,8 +447,8 @@ decode_splitkv_kernel(DecodeParams p) {
     const int row = c_lin / Cfg::kChunksPerRow, c = c_lin % Cfg::kChunksPerRow;
     cp_row[i] = loader + Cfg::kLoaders * i < kTileChunks ? row : kDecodeTile;  // kDecodeTile: no copy
     cp_src[i] = static_cast<uint32_t>(row * row_pitch + c * 16);
-    cp_dk[i] = row * Cfg::kRowBytes + (swz_k<D, FP8>(row, c) << 4);
-    cp_dv[i] = row * Cfg::kRowBytes + (swz_v<D, FP8>(row, c) << 4);
+    cp_dk[i] = row * Cfg::kRowBytes + (swz_k<D, BYTES>(row, c) << 4);
+    cp_dv[i] = row * Cfg::kRowBytes + (swz_v<D, BYTES>(row, c) << 4);
   }
 
   auto load_tile = [&](int tile, uint32_t sK, uint32_t sV) {  // one 16-token tile into (sK, sV)
@@ -489,12 +509,12 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
     for (int u = 0; u < SUB; ++u) {
       const uint32_t sK = sK0 + u * Cfg::kTileBytes;
-      if constexpr (!FP8) {
+      if constexpr (!BYTES) {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           uint32_t a[4];
-          ldmatrix_x4(a, sK + row * Cfg::kRowBytes + (swz_k<D, FP8>(row, 2 * kk + (lane >> 4)) << 4));
+          ldmatrix_x4(a, sK + row * Cfg::kRowBytes + (swz_k<D, BYTES>(row, 2 * kk + (lane >> 4)) << 4));
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
@@ -508,17 +528,30 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
           for (int i = 0; i < CPL; ++i)
             kw[rs][i] = *reinterpret_cast<const uint4*>(sKp + row * Cfg::kRowBytes +
-                                                        (swz_k<D, FP8>(row, q4 * CPL + i) << 4));
+                                                        (swz_k<D, BYTES>(row, q4 * CPL + i) << 4));
         }
+        if constexpr (FP8) {
 #pragma unroll
-        for (int kk = 0; kk < QW; ++kk) {  // K codes feed the E4M3 MMA as they are
-          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][(2 * kk) >> 2]);
-          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][(2 * kk) >> 2]);
-          const uint32_t a[4] = {w0[(2 * kk) & 3], w1[(2 * kk) & 3], w0[(2 * kk + 1) & 3], w1[(2 * kk + 1) & 3]};
+          for (int kk = 0; kk < QW; ++kk) {  // K codes feed the E4M3 MMA as they are
+            const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][(2 * kk) >> 2]);
+            const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][(2 * kk) >> 2]);
+            const uint32_t a[4] = {w0[(2 * kk) & 3], w1[(2 * kk) & 3], w0[(2 * kk + 1) & 3], w1[(2 * kk + 1) & 3]};
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_e4m3_16832(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-            mma_e4m3_16832(sacc[u][nt], a, ql[nt][kk][0], ql[nt][kk][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_e4m3_16832(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+              mma_e4m3_16832(sacc[u][nt], a, ql[nt][kk][0], ql[nt][kk][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {  // INT8 codes -> exact f16, four per word
+            const uint32_t w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2])[kk & 3];
+            const uint32_t w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2])[kk & 3];
+            uint32_t a[4];
+            i8x4_to_f16x2(w0, a[0], a[2]);
+            i8x4_to_f16x2(w1, a[1], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
           }
         }
       }
@@ -575,12 +608,24 @@ decode_splitkv_kernel(DecodeParams p) {
       for (int u = 0; u < SUB; ++u) {
         const float p0 = ex2_approx(sv[u][0] - eb0), p1 = ex2_approx(sv[u][1] - eb1);
         const float p2 = ex2_approx(sv[u][2] - eb0), p3 = ex2_approx(sv[u][3] - eb1);
-        l_run[nt][0] += p0 + p2;
-        l_run[nt][1] += p1 + p3;
-        if constexpr (!FP8) {
+        if constexpr (!BYTES) {
+          l_run[nt][0] += p0 + p2;
+          l_run[nt][1] += p1 + p3;
           pb[u][nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
           pb[u][nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+        } else if constexpr (I8) {
+          // f16 P; the row sums take the rounded values the MMA multiplies, so that the bias
+          // of the V codes (1152 per unit weight) comes off exactly as 1152 * l at the end
+          const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
+          const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+          const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+          l_run[nt][0] += r01.x + r23.x;
+          l_run[nt][1] += r01.y + r23.y;
+          pb[u][nt][0] = movmatrix_trans(h01);
+          pb[u][nt][1] = movmatrix_trans(h23);
         } else {
+          l_run[nt][0] += p0 + p2;
+          l_run[nt][1] += p1 + p3;
           // 256 * p as hi + lo E4M3 codes, one (hi | lo << 8) 16-bit element per value, so the
           // 8x8 16-bit transpose moves each value whole: lane (g, q) then holds tokens 2q, 2q+1
           // (upper rows) and 2q+8, 2q+9 (lower rows) of head g
@@ -596,7 +641,7 @@ decode_splitkv_kernel(DecodeParams p) {
     }
 
     // ---- O^T[D x 8 heads] += V^T P^T ----
-    if constexpr (!FP8) {
+    if constexpr (!BYTES) {
 #pragma unroll
       for (int u = 0; u < SUB; ++u) {
         const uint32_t sV = sV0 + u * Cfg::kTileBytes;
@@ -604,7 +649,7 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           uint32_t a[4];
-          ldmatrix_x4_trans(a, sV + row * Cfg::kRowBytes + (swz_v<D, FP8>(row, 2 * mt + ((lane >> 3) & 1)) << 4));
+          ldmatrix_x4_trans(a, sV + row * Cfg::kRowBytes + (swz_v<D, BYTES>(row, 2 * mt + ((lane >> 3) & 1)) << 4));
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb[u][nt][0], pb[u][nt][1]);
         }
@@ -624,17 +669,30 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             w[i] = *reinterpret_cast<const uint32_t*>(sVp + rows[i] * Cfg::kRowBytes +
-                                                      (swz_v<D, FP8>(rows[i], c) << 4) + in_chunk);
+                                                      (swz_v<D, BYTES>(rows[i], c) << 4) + in_chunk);
           transpose4x4_bytes(w, dj[u]);
         }
+        if constexpr (FP8) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {  // dims 32pp + 4g + 2half + {0, 1}
-          const uint32_t a[4] = {dj[0][2 * half], dj[0][2 * half + 1], dj[1][2 * half], dj[1][2 * half + 1]};
+          for (int half = 0; half < 2; ++half) {  // dims 32pp + 4g + 2half + {0, 1}
+            const uint32_t a[4] = {dj[0][2 * half], dj[0][2 * half + 1], dj[1][2 * half], dj[1][2 * half + 1]};
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][0][0], p8[nt][0][1]);
-            mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][1][0], p8[nt][1][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][0][0], p8[nt][0][1]);
+              mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][1][0], p8[nt][1][1]);
+            }
           }
+        } else {  // per 16-token sub-tile: dims 32pp + 4g + 2half + {0, 1} as rows
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t a[4];
+              i8x4_to_f16x2_biased(dj[u][2 * half], a[0], a[2]);
+              i8x4_to_f16x2_biased(dj[u][2 * half + 1], a[1], a[3]);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[u][nt][0], pb[u][nt][1]);
+            }
         }
       }
     }
@@ -671,7 +729,7 @@ decode_splitkv_kernel(DecodeParams p) {
       for (int j = 0; j < 4; ++j) {
         const int rho = g8 + 8 * (j >> 1);
         int d;
-        if constexpr (!FP8) d = 16 * mt + rho;
+        if constexpr (!BYTES) d = 16 * mt + rho;
         else d = 32 * (mt >> 1) + 4 * (rho & 7) + 2 * (mt & 1) + (rho >> 3);
         sm_o[(warp * HN + nt * 8 + 2 * q4 + (j & 1)) * D + d] = o[nt][mt][j];
       }
@@ -698,6 +756,7 @@ decode_splitkv_kernel(DecodeParams p) {
         lsum += f * sm_l[w * HN + cl];
       }
     }
+    if constexpr (I8) acc -= kI8Bias * lsum;  // the V codes entered the MMA as 1152 + code
     acc *= FP8 ? p.kv_scale * (1.f / 256.f) : p.kv_scale;  // FP8: P entered the MMA as 256 p
     if (num_splits == 1) {
       __nv_bfloat16 b = __float2bfloat16_rn(acc / lsum);
@@ -782,10 +841,10 @@ __global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
   *reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(row) * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
 }
 
-template <int D, bool FP8, int NT, bool WIDE>
+template <int D, int KVK, int NT, bool WIDE>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
-  using Cfg = DecodeCfg<D, FP8, WIDE>;
-  auto kern = decode_splitkv_kernel<D, FP8, NT, WIDE>;
+  using Cfg = DecodeCfg<D, KVK, WIDE>;
+  auto kern = decode_splitkv_kernel<D, KVK, NT, WIDE>;
   constexpr int kMerge = Cfg::kWarps * NT * 8 * (D + 2) * 4;  // the epilogue's staging
   constexpr int kSmem = Cfg::kRingsBytes > kMerge ? Cfg::kRingsBytes : kMerge;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -808,18 +867,19 @@ cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s
   return launch_pdl(combine_kernel<4>, grid, dim3(4 * 32), 0, s, p);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, bool wide, cudaStream_t s) {
+template <int KVK>
+cudaError_t launch_decode_kind(const DecodeParams& p, bool wide, cudaStream_t s) {
   if (wide) {  // 16 columns per warp, 64 per CTA
-    if (p.D == 128) return fp8 ? launch_decode_t<128, true, 2, true>(p, s) : launch_decode_t<128, false, 2, true>(p, s);
-    return fp8 ? launch_decode_t<64, true, 2, true>(p, s) : launch_decode_t<64, false, 2, true>(p, s);
+    return p.D == 128 ? launch_decode_t<128, KVK, 2, true>(p, s) : launch_decode_t<64, KVK, 2, true>(p, s);
   }
-  const int nt = p.nt;
-  if (p.D == 128) {
-    if (fp8) return nt == 1 ? launch_decode_t<128, true, 1, false>(p, s) : launch_decode_t<128, true, 2, false>(p, s);
-    return nt == 1 ? launch_decode_t<128, false, 1, false>(p, s) : launch_decode_t<128, false, 2, false>(p, s);
-  }
-  if (fp8) return nt == 1 ? launch_decode_t<64, true, 1, false>(p, s) : launch_decode_t<64, true, 2, false>(p, s);
-  return nt == 1 ? launch_decode_t<64, false, 1, false>(p, s) : launch_decode_t<64, false, 2, false>(p, s);
+  if (p.D == 128) return p.nt == 1 ? launch_decode_t<128, KVK, 1, false>(p, s) : launch_decode_t<128, KVK, 2, false>(p, s);
+  return p.nt == 1 ? launch_decode_t<64, KVK, 1, false>(p, s) : launch_decode_t<64, KVK, 2, false>(p, s);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int kv_dtype, bool wide, cudaStream_t s) {
+  if (kv_dtype == PKV_FP8_E4M3) return launch_decode_kind<kKvE4m3>(p, wide, s);
+  if (kv_dtype == PKV_INT8) return launch_decode_kind<kKvInt8>(p, wide, s);
+  return launch_decode_kind<kKvBf16>(p, wide, s);
 }
 
 }  // namespace pkv

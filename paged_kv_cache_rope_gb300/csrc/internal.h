@@ -30,8 +30,8 @@ struct PlanLayout {
   int64_t witem_map;     // [num_witems] the same for the wide decode kernel's CTAs
   int64_t row_map;       // [generation rows] int2 (generation request, token index within it)
   int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
-  int64_t stage_prefix;  // [C + 1]  FP8 pools: prefix of the context requests' page counts
-  int64_t stage_tbl;     // [C * max_blocks] FP8 pools: block table into the bf16 staging pool
+  int64_t stage_prefix;  // [C + 1]  8-bit pools: prefix of the context requests' page counts
+  int64_t stage_tbl;     // [C * max_blocks] 8-bit pools: block table into the bf16 staging pool
   int64_t int_words;     // total int32 words of the plan
   int64_t part_o;        // byte offset of fp32 partial outputs [num_parts, Hq, D]
   int64_t part_ml;       // byte offset of fp32 (m, l) pairs   [num_parts, Hq, 2]
@@ -122,10 +122,12 @@ struct ContextParams {
   int32_t* d_error;
 };
 
-// FP8 pools with context requests: copies the context requests' pages into a bf16 staging pool
-// holding each code's exact value (every E4M3 value is a bf16 value), with its own block table.
+// 8-bit pools with context requests: copies the context requests' pages into a bf16 staging
+// pool holding each code's exact value (every E4M3 value and every int8 is a bf16 value), with
+// its own block table.
 struct StageParams {
   int32_t C, B, Hkv, D, NB, max_blocks, total_pages;
+  int32_t kv_dtype;  // PKV_FP8_E4M3 or PKV_INT8
   const int32_t* ctx_len;
   const int32_t* past;
   const int32_t* tbl;
@@ -153,13 +155,13 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, int kv_dtype, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // wide = false: requests with at most 16 score columns (KV split across warps); true: wider
 // requests (columns split across warps, 64 per CTA).
-cudaError_t launch_decode(const DecodeParams& p, bool fp8, bool wide, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int kv_dtype, bool wide, cudaStream_t s);
 cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s);
-cudaError_t launch_stage_fp8(const StageParams& p, cudaStream_t s);
+cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map,
                            bool fp8, cudaStream_t s);

@@ -13,7 +13,8 @@ from paged_kv_cache_rope_gb300 import workloads as W
 
 BF16_TOL = 1e-2       # max abs error vs the fp64 oracle, bf16 pool
 FP8_TOL = 4e-2        # the FP8-pool bar, taken against the fp64 oracle on the same FP8 pool
-FP8_DEQ_TOL = 1e-2    # what the kernels are held to against that oracle (tighter than FP8_TOL)
+FP8_DEQ_TOL = 1e-2    # what the kernels are held to against that oracle (tighter than FP8_TOL);
+                      # INT8 pools are held to the same bar against the oracle on the INT8 pool
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -60,15 +61,16 @@ class OracleResult:
 
 
 def oracle_run(b: W.Batch, rows=None, unquantised: bool = False) -> OracleResult:
-    """O1 + O2 on the batch.  ``unquantised`` runs an FP8 batch on its bf16 twin pool."""
-    use_twin = unquantised and b.kv_dtype == "fp8"
+    """O1 + O2 on the batch.  ``unquantised`` runs an 8-bit batch on its bf16 twin pool."""
+    use_twin = unquantised and b.kv_dtype != "bf16"
     pool_np = bits(b.pool_bf16 if use_twin else b.pool).copy()
     fp8 = b.kv_dtype == "fp8" and not use_twin
+    i8 = b.kv_dtype == "int8" and not use_twin
     cs = oracle.rope_table(b.rope_base, b.head_dim, b.max_pos)
     args = dict(new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
                 num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
                 num_blocks=b.num_blocks, kv_fp8=fp8, inv_scale=b.inv_scale, q_bits=bits(b.q),
-                k_bits=bits(b.k), v_bits=bits(b.v), cs=cs, pool=pool_np)
+                k_bits=bits(b.k), v_bits=bits(b.v), cs=cs, pool=pool_np, kv_int8=i8)
     if b.position_offsets is None:
         st, q_out = oracle.append_rope(**args)
     else:  # draft tokens: context rows keep i, generation rows take the batch's offsets
@@ -78,9 +80,9 @@ def oracle_run(b: W.Batch, rows=None, unquantised: bool = False) -> OracleResult
     st2, out = oracle.attention(
         new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
         num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
-        num_blocks=b.num_blocks, kv_fp8=fp8, kv_scale=b.kv_scale if fp8 else 1.0, pool=pool_np,
+        num_blocks=b.num_blocks, kv_fp8=fp8, kv_scale=b.kv_scale if (fp8 or i8) else 1.0, pool=pool_np,
         q=q64, softmax_scale=b.softmax_scale, rows=rows, num_contexts=b.num_contexts,
-        gen_mask=b.packed_mask)
+        gen_mask=b.packed_mask, kv_int8=i8)
     return OracleResult(pool_np, q_out, out, st or st2)
 
 

@@ -24,7 +24,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_append_bit_exact(case, kv_dtype):
     name, ctx, gen, Hq, Hkv, D, B = case

@@ -34,7 +34,7 @@ DECODE = [
 ]
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("case", DECODE, ids=[c[0] for c in DECODE])
 def test_decode_matches_oracle(case, kv_dtype):
     name, gen, Hq, Hkv, D, B = case
@@ -47,10 +47,10 @@ def test_decode_matches_oracle(case, kv_dtype):
     if kv_dtype == "bf16":
         assert max_err(got, o.out) <= BF16_TOL
     else:
-        # kernel arithmetic: against the oracle on the same (dequantised) FP8 pool
+        # kernel arithmetic: against the oracle on the same (dequantised) 8-bit pool
         assert max_err(got, o.out) <= FP8_DEQ_TOL
         # quantisation: against the unquantised values the kernel may add at most the kernel
-        # tolerance to the error E4M3 itself causes (measured exactly by the oracle)
+        # tolerance to the error the 8-bit codes themselves cause (measured exactly by the oracle)
         unq = oracle_run(b, unquantised=True).out
         inherent = max_err(o.out, unq)
         assert max_err(got, unq) <= inherent + FP8_DEQ_TOL
@@ -70,7 +70,7 @@ CONTEXT = [
 ]
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("case", CONTEXT, ids=[c[0] for c in CONTEXT])
 def test_context_matches_oracle(case, kv_dtype):
     name, ctx, gen, Hq, Hkv, D, B = case
@@ -82,7 +82,7 @@ def test_context_matches_oracle(case, kv_dtype):
     got = gpu_out_f64(g, b)
     if kv_dtype == "bf16":
         assert max_err(got, o.out) <= BF16_TOL
-    else:  # FP8 pool: context pages are staged as exact bf16 code values first
+    else:  # 8-bit pool: context pages are staged as exact bf16 code values first
         assert max_err(got, o.out) <= FP8_DEQ_TOL
         unq = oracle_run(b, unquantised=True).out
         assert max_err(got, unq) <= max_err(o.out, unq) + FP8_DEQ_TOL
@@ -102,7 +102,7 @@ def test_deterministic_and_page_permutation_invariant():
     assert torch.equal(g1.pool[torch.from_numpy(perm).cuda()].view(torch.int16), g3.pool.view(torch.int16))
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 def test_overlapped_and_serial_schedules_agree(kv_dtype):
     """A mixed batch runs its generation kernels on the library's auxiliary stream beside the
     context kernel; with per-kernel timing events set, everything runs on the caller's stream.
@@ -139,10 +139,10 @@ def test_launch_counts():
     g = gpu_run(b)
     assert g.launches == 5  # append, plan, context, decode, combine
     g8 = gpu_run(_batch("launches8", [(100, 0)], [5000, 20], 8, 2, 128, 64, "fp8"))
-    assert g8.launches == 6  # append, plan, stage_fp8, context, decode, combine
+    assert g8.launches == 6  # append, plan, stage_q8, context, decode, combine
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 def test_prefix_shared_pages(kv_dtype):
     """Prefix reuse: several requests' block tables point at the same physical pages for a
     common cached prefix (read-only); each request's own new tokens land in pages of its own."""

@@ -34,7 +34,7 @@ def _batch(case, kv_dtype):
                         tokens_per_block=B, kv_dtype=kv_dtype, seed=len(name) * 7 + 3, draft_tree=tree)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_draft_tokens_match_oracle(case, kv_dtype):
     b = _batch(case, kv_dtype)

@@ -13,7 +13,7 @@ from helpers import bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 def test_graph_replay_matches_direct(kv_dtype):
     b = W.make_batch(name="graph", ctx=[(150, 40)], gen=[700, 33, 2000], num_q_heads=16, num_kv_heads=4,
                      head_dim=128, tokens_per_block=32, kv_dtype=kv_dtype, seed=31)

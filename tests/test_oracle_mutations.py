@@ -20,8 +20,8 @@ MUTATIONS = {
     "rope_pairs_swapped": ("    float a = x[j], b = x[j + half];", "    float b = x[j], a = x[j + half];"),
     "gqa_map": ("      int hk = h / group;", "      int hk = h % num_kv_heads;"),
     "causal_drops_diagonal": ("(int64_t)past[r] + i + 1;", "(int64_t)past[r] + i;"),
-    "scores_read_v": ("dot += qv[d] * pool_value(pool, kv_is_fp8, kv_scale, pool_index(blk, 0,",
-                      "dot += qv[d] * pool_value(pool, kv_is_fp8, kv_scale, pool_index(blk, 1,"),
+    "scores_read_v": ("dot += qv[d] * pool_value(pool, kv_kind, kv_scale, pool_index(blk, 0,",
+                      "dot += qv[d] * pool_value(pool, kv_kind, kv_scale, pool_index(blk, 1,"),
     "page_slot_off_by_one": ("int logical_block = (int)(pos / B), slot = (int)(pos % B);\n      int blk = logical_block < max_blocks_per_seq\n                    ? block_table[(size_t)r * max_blocks_per_seq + logical_block] : -1;\n      if (blk < 0 || blk >= num_blocks) {\n        status",
                              "int logical_block = (int)(pos / B), slot = (int)((pos + 1) % B);\n      int blk = logical_block < max_blocks_per_seq\n                    ? block_table[(size_t)r * max_blocks_per_seq + logical_block] : -1;\n      if (blk < 0 || blk >= num_blocks) {\n        status"),
     "draft_mask_word": ("mrow[j / 32] >> (j % 32)", "mrow[0] >> (j % 32)"),

@@ -30,7 +30,7 @@ def _setup(b: W.Batch):
     return pool, meta, q_out, err
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 def test_noalloc_matches_regular_entry_point_twice(kv_dtype):
     # two chunked/fresh contexts and decodes long enough to split
     b = W.make_batch(name="noalloc", ctx=[(300, 64), (37, 0)], gen=[5, 700, 3000, 129], num_q_heads=16, num_kv_heads=4,
