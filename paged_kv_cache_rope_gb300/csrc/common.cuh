@@ -130,6 +130,12 @@ __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
 }
 constexpr float kI8Bias = 1152.f;
 
+// Four E4M3 codes (byte j = code j) -> two exact f16x2, lo = (code0, code1), hi = (code2, code3).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_to_f16x2(static_cast<uint16_t>(w));
+  hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+
 // 2^x with the MUFU instruction alone (flush-to-zero; relative error ~2^-22, and results below
 // 2^-126 -- probabilities of masked or vanishing keys -- become 0).  -inf gives 0.
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -281,7 +281,14 @@ template <int D, int KVK, int NT, bool WIDE>
 __global__ void __launch_bounds__(DecodeCfg<D, KVK, WIDE>::kThreads)
 decode_splitkv_kernel(DecodeParams p) {
   using Cfg = DecodeCfg<D, KVK, WIDE>;
-  constexpr bool BYTES = Cfg::kBytes, FP8 = KVK == kKvE4m3, I8 = KVK == kKvInt8;
+  constexpr bool BYTES = Cfg::kBytes, I8 = KVK == kKvInt8;
+  // 8-bit codes either become exact f16 values in registers and run on f16 MMAs (INT8 always;
+  // E4M3 in the wide kernel), or feed E4M3 MMAs directly with hi/lo-split Q and P (E4M3 in the
+  // narrow kernel).  Measured: the hardware E4M3 -> f16 conversion made the narrow kernel 8%
+  // slower than the E4M3 MMAs, while in the wide kernel, whose four sets of hi/lo fragments
+  // overflow the register file, converting was 17% faster.
+  constexpr bool F16 = I8 || (KVK == kKvE4m3 && WIDE);
+  constexpr bool FP8 = KVK == kKvE4m3 && !F16;
   constexpr int KS = D / 16;  // k-steps over the head dim / m-tiles of O^T
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -383,8 +390,8 @@ decode_splitkv_kernel(DecodeParams p) {
       int ex = 0;
       if (amax > 0.f) frexpf(amax, &ex);
       // E4M3: amax * up in [128, 256), inside E4M3's 448; f16: in [2^13, 2^14), far from 65504
-      const float up = ldexpf(1.f, (I8 ? 14 : 8) - ex);
-      if constexpr (I8) {
+      const float up = ldexpf(1.f, (F16 ? 14 : 8) - ex);
+      if constexpr (F16) {
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           qb[nt][kk][0] = pack_f16x2(x[4 * kk] * up, x[4 * kk + 1] * up);
@@ -544,12 +551,17 @@ decode_splitkv_kernel(DecodeParams p) {
           }
         } else {
 #pragma unroll
-          for (int kk = 0; kk < KS; ++kk) {  // INT8 codes -> exact f16, four per word
+          for (int kk = 0; kk < KS; ++kk) {  // 8-bit codes -> exact f16, four per word
             const uint32_t w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk >> 2])[kk & 3];
             const uint32_t w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk >> 2])[kk & 3];
             uint32_t a[4];
-            i8x4_to_f16x2(w0, a[0], a[2]);
-            i8x4_to_f16x2(w1, a[1], a[3]);
+            if constexpr (I8) {
+              i8x4_to_f16x2(w0, a[0], a[2]);
+              i8x4_to_f16x2(w1, a[1], a[3]);
+            } else {
+              e4m3x4_to_f16x2(w0, a[0], a[2]);
+              e4m3x4_to_f16x2(w1, a[1], a[3]);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
           }
@@ -613,7 +625,7 @@ decode_splitkv_kernel(DecodeParams p) {
           l_run[nt][1] += p1 + p3;
           pb[u][nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
           pb[u][nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
-        } else if constexpr (I8) {
+        } else if constexpr (F16) {
           // f16 P; the row sums take the rounded values the MMA multiplies, so that the bias
           // of the V codes (1152 per unit weight) comes off exactly as 1152 * l at the end
           const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
@@ -688,8 +700,13 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t a[4];
-              i8x4_to_f16x2_biased(dj[u][2 * half], a[0], a[2]);
-              i8x4_to_f16x2_biased(dj[u][2 * half + 1], a[1], a[3]);
+              if constexpr (I8) {
+                i8x4_to_f16x2_biased(dj[u][2 * half], a[0], a[2]);
+                i8x4_to_f16x2_biased(dj[u][2 * half + 1], a[1], a[3]);
+              } else {
+                e4m3x4_to_f16x2(dj[u][2 * half], a[0], a[2]);
+                e4m3x4_to_f16x2(dj[u][2 * half + 1], a[1], a[3]);
+              }
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * pp + half], a, pb[u][nt][0], pb[u][nt][1]);
             }
