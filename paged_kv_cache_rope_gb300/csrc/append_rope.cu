@@ -8,7 +8,8 @@
 //
 // HBM-bound.  One thread handles 16 elements of one head of one token (8 rotation pairs, or a
 // pass-through part of a partially rotated head): two 16-byte loads, two 16-byte stores (8-byte
-// stores into an FP8 or INT8 pool).  Variants: rotate-half or interleaved pairs, partial rotary dims,
+// stores into an FP8 or INT8 pool).  (A warp-per-token layout with the rotation coefficients
+// loaded once per token measured no faster.)  Variants: rotate-half or interleaved pairs, partial rotary dims,
 // an optional RMSNorm of q / k heads reduced across the head's lanes with shuffles, and
 // draft tokens rotated for past + offset (adg.csdn.net/69730cc6 section 1.4,
 // spec_decoding_position_offsets) while stored at slot past + i.
@@ -144,15 +145,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
   const int D = p.D, per_head = D >> 4;
   const int rot_tasks = p.rot >> 4, rhalf = p.rot >> 1;
   const int tasks_per_token = (p.Hq + 2 * p.Hkv) * per_head;
-  const int64_t total = static_cast<int64_t>(p.T) * tasks_per_token;
+  const int total = p.T * tasks_per_token;  // < 2^31, checked on the host
+  const int lph = 31 - __clz(per_head);      // per_head is 4 or 8
   const size_t esz = KVK != 0 ? 1 : 2;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kAppendThreads;
-  for (int64_t wbase = static_cast<int64_t>(blockIdx.x) * kAppendThreads + (tid & ~31); wbase < total;
+  const int stride = gridDim.x * kAppendThreads;
+  for (int wbase = blockIdx.x * kAppendThreads + (tid & ~31); wbase < total;
        wbase += stride) {  // warp-uniform loop: inactive lanes still join the norm shuffles
-    const int64_t gi = wbase + lane;
+    const int gi = wbase + lane;
     const bool active = gi < total;
-    const int token = active ? static_cast<int>(gi / tasks_per_token) : 0;
-    int task = active ? static_cast<int>(gi - static_cast<int64_t>(token) * tasks_per_token) : 0;
+    const int token = active ? gi / tasks_per_token : 0;
+    int task = active ? gi - token * tasks_per_token : 0;
     int lo = 0, hi = p.R - 1;  // request of this token: largest r with s_cu[r] <= token
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
         kind = 2;
       }
     }
-    const int h = task / per_head, t = task - h * per_head;
+    const int h = task >> lph, t = task & (per_head - 1);
     const bool rotate = kind != 2 && t < rot_tasks;
     int offA, offB;  // element offsets of the two 8-element groups inside the head
     if (p.style == 0 && t < rot_tasks) {
@@ -301,6 +303,7 @@ cudaError_t launch_append(const AppendParams& p, int kv_dtype, cudaStream_t s) {
     if (num_sms <= 0) num_sms = 152;
   }
   const int64_t tasks = static_cast<int64_t>(p.T) * (p.Hq + 2 * p.Hkv) * (p.D / 16);
+  if (tasks + kAppendThreads * 8LL * num_sms >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // int32 task index
   int64_t blocks = (tasks + kAppendThreads - 1) / kAppendThreads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // grid-stride beyond 8 CTAs per SM
   if (blocks > cap) blocks = cap;
