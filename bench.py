@@ -264,7 +264,7 @@ def run_ours(args):
     names = ["append_rope"] + fwd_names
     launches_per_step = len(names)
     # generation rows run on the narrow and/or the wide decode kernel: together they read the KV
-    dec_names = [n for n in ("decode_splitkv", "decode_splitkv_wide") if n in fwd_names]
+    dec_names = [n for n in ("decode_splitkv", "decode_splitkv_wide", "decode_tc") if n in fwd_names]
     dominant = "+".join(dec_names) if work["decode_kv_bytes"] else "context_attn"
 
     for _ in range(args.warmup):

@@ -279,7 +279,8 @@ int paged_attention_forward_noalloc(const pkv_pool* pool, const pkv_batch* batch
 int32_t paged_kv_last_launch_count(void);
 
 /* Name of the i-th kernel the last call on this thread enqueued ("append_rope", "plan",
- * "stage_q8", "context_attn", "decode_splitkv", "decode_splitkv_wide", "combine"), or NULL
+ * "stage_q8", "context_attn", "decode_splitkv", "decode_splitkv_wide", "decode_tc", "combine"),
+ * or NULL
  * when i is out of range. */
 const char* paged_kv_last_launch_name(int32_t i);
 

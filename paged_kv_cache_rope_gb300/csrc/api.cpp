@@ -78,13 +78,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 4-D bf16 map (64-wide head-dim half, head-dim halves, heads, rows) with a 128-byte swizzle;
 // box = one 64-wide half of `box_rows` rows of one head.
 bool encode_rows_map(CUtensorMap* map, const void* base, int D, int heads, int64_t rows, int64_t row_bytes,
-                     int box_rows) {
+                     int box_rows, int box_heads = 1) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(row_bytes)};
-  cuuint32_t box[4] = {64, 1, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -97,6 +97,8 @@ struct HostPlan {
   int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
   int decode_nt = 1, num_items = 0, num_parts = 0;  // narrow decode n-tiles per CTA, CTAs per KV head, partial rows
   int num_witems = 0;                                // wide decode CTAs per KV head
+  int num_titems = 0;                                // tensor-core generation CTAs per KV head
+  bool tc_wide = false;                              // wide requests take the tensor-core kernel
   pkv::PlanLayout lay{};
 };
 
@@ -181,22 +183,34 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   hp->kv_chunk = choose_kv_chunk(pool, b, hp->C);
   // decode score-tile columns are (token, query head) pairs of one KV head.  Requests with at
   // most kDecodeNarrowMaxCols of them take the narrow kernel (8 or 16 columns per CTA, the
-  // split's tiles shared out among the warps); wider ones the wide kernel (64 columns per CTA,
-  // one per warp-column set, every warp over every tile), in as many column groups as needed.
+  // split's tiles shared out among the warps).  Wider ones (draft tokens, large query groups)
+  // take the tensor-core kernel when the pool is bf16 and a 128-row tile holds whole groups
+  // (rows = pairs, 128 per CTA; splits of whole 128-key tiles), else the wide mma.sync kernel
+  // (64 columns per CTA, every warp over every tile), in as many column groups as needed.
   const int group = Hq / pool->num_kv_heads;
   int max_narrow = 0;
+  bool any_wide = false;
   for (int r = hp->C; r < hp->R; ++r) {
     const int cols_r = b->h_context_lengths[r] * group;
     if (cols_r <= pkv::kDecodeNarrowMaxCols) max_narrow = std::max(max_narrow, cols_r);
+    else any_wide = true;
   }
+  hp->tc_wide = any_wide && pool->dtype == PKV_BF16 && group <= 128 && 128 % group == 0;
+#ifndef PKV_TC_MIN_CHUNK
+#define PKV_TC_MIN_CHUNK 2048
+#endif
+  if (hp->tc_wide)  // whole 128-key tiles per split, and enough of them to amortise a CTA's set-up
+    hp->kv_chunk = std::max<int>(PKV_TC_MIN_CHUNK,
+                                 (hp->kv_chunk + pkv::kTcChunkAlign - 1) / pkv::kTcChunkAlign * pkv::kTcChunkAlign);
   hp->decode_nt = max_narrow > 8 ? 2 : 1;
   const int cols = 8 * hp->decode_nt;
-  hp->num_splits = hp->max_splits = hp->num_items = hp->num_witems = hp->num_parts = 0;
+  hp->num_splits = hp->max_splits = hp->num_items = hp->num_witems = hp->num_titems = hp->num_parts = 0;
   for (int r = hp->C; r < hp->R; ++r) {
     const int n = b->h_context_lengths[r], cols_r = n * group;
     const int s = (b->h_past_kv_lengths[r] + n + hp->kv_chunk - 1) / hp->kv_chunk;
     hp->num_splits += s;
     if (cols_r <= pkv::kDecodeNarrowMaxCols) hp->num_items += s * ((cols_r + cols - 1) / cols);
+    else if (hp->tc_wide) hp->num_titems += s * ((cols_r + pkv::kCtxTileM - 1) / pkv::kCtxTileM);
     else hp->num_witems += s * ((cols_r + pkv::kDecodeWideCols - 1) / pkv::kDecodeWideCols);
     hp->num_parts += s * n;
     hp->max_splits = std::max(hp->max_splits, s);
@@ -209,7 +223,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   L.part_prefix = L.item_prefix + hp->G + 1;
   L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
   L.witem_map = L.item_map + 2LL * hp->num_items;
-  L.row_map = L.witem_map + 2LL * hp->num_witems;
+  L.titem_map = L.witem_map + 2LL * hp->num_witems;
+  L.row_map = L.titem_map + 2LL * hp->num_titems;
   L.unit_order = L.row_map + 2LL * (hp->T - hp->ctx_tokens);
   L.stage_prefix = L.unit_order + hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
@@ -464,6 +479,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.expect_items = hp.num_items;
   pp.expect_parts = hp.num_parts;
   pp.expect_witems = hp.num_witems;
+  pp.expect_titems = hp.num_titems;
+  pp.tc_wide = hp.tc_wide ? 1 : 0;
   pp.gen_row0 = hp.ctx_tokens;
   pp.gen_rows = hp.T - hp.ctx_tokens;
   pp.expect_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
@@ -620,6 +637,55 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       {
         LaunchScope ls(launches, "decode_splitkv_wide", gs);
         e = pkv::launch_decode(dp, pool->dtype, true, gs);
+      }
+      if (e != cudaSuccess) return PKV_ERR_CUDA;
+      ++launches;
+    }
+    if (hp.num_titems > 0) {
+      // wide generation requests on the tensor-core kernel: a Q box is g heads x 128/g tokens,
+      // i.e. 128 (token, head) rows of one KV head
+      const int group = num_q_heads / Hkv;
+      CUtensorMap qmap_g, kvmap_g;
+      if (!encode_rows_map(&qmap_g, q_rot, D, num_q_heads, hp.T, q_row_stride * 2, pkv::kCtxTileM / group, group))
+        return PKV_ERR_CUDA;
+      if (!encode_rows_map(&kvmap_g, pool->pool, D, Hkv, static_cast<int64_t>(pool->num_blocks) * 2 * pool->tokens_per_block,
+                           static_cast<int64_t>(Hkv) * D * 2, std::min(pool->tokens_per_block, pkv::kCtxTileN)))
+        return PKV_ERR_CUDA;
+      pkv::ContextParams tp{};
+      tp.C = hp.C;
+      tp.T = hp.T;
+      tp.Hq = num_q_heads;
+      tp.Hkv = Hkv;
+      tp.group = group;
+      tp.D = D;
+      tp.B = pool->tokens_per_block;
+      tp.NB = pool->num_blocks;
+      tp.max_blocks = batch->max_blocks_per_seq;
+      tp.cu_q = ws + hp.lay.cu_q;
+      tp.ctx_len = batch->d_context_lengths;
+      tp.past = batch->d_past_kv_lengths;
+      tp.tbl = batch->d_block_offsets;
+      tp.pool = static_cast<const uint8_t*>(pool->pool);
+      tp.out = static_cast<uint16_t*>(out);
+      tp.out_stride = static_cast<int64_t>(num_q_heads) * D;
+      tp.scale_log2 = scale_log2;
+      tp.out_scale = 1.0f;
+      tp.d_error = d_error;
+      tp.G = hp.G;
+      tp.gen_row0 = hp.ctx_tokens;
+      tp.kv_chunk = hp.kv_chunk;
+      tp.num_titems = hp.num_titems;
+      tp.total_parts = hp.num_parts;
+      tp.titem_map = reinterpret_cast<const int2*>(ws + hp.lay.titem_map);
+      tp.split_prefix = ws + hp.lay.split_prefix;
+      tp.part_prefix = ws + hp.lay.part_prefix;
+      tp.mask = batch->d_packed_mask;
+      tp.mask_words = batch->d_packed_mask ? batch->mask_words : 0;
+      tp.part_o = dp.part_o;
+      tp.part_ml = dp.part_ml;
+      {
+        LaunchScope ls(launches, "decode_tc", gs);
+        e = pkv::launch_context(tp, &qmap_g, &kvmap_g, true, gs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;

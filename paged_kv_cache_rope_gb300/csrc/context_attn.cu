@@ -51,36 +51,45 @@ constexpr uint32_t kRegsControl = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could exceed 2^8
 
-template <int D>
+// Context: Q_A, Q_B, K[2], V[2].  Generation: one Q tile (A and B share it), K[3], V[3] -- a
+// deeper ring, since each K / V tile has one consumer and the two halves alternate.
+template <int D, bool DEC>
 struct CtxSmem {
   static constexpr int kHalf = 128 * 128;         // one 64-wide half of a 128-row tile (bytes)
   static constexpr int kTile = (D / 64) * kHalf;  // one Q tile or one K / V stage
-  static constexpr int kQOff = 0;                 // Q_A, Q_B
-  static constexpr int kKOff = 2 * kTile;         // K[2]
-  static constexpr int kVOff = 4 * kTile;         // V[2]
-  static constexpr int kBarOff = 6 * kTile;
+  static constexpr int kStages = DEC ? 3 : 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = (DEC ? 1 : 2) * kTile;
+  static constexpr int kVOff = kKOff + kStages * kTile;
+  static constexpr int kBarOff = kVOff + kStages * kTile;
   static constexpr int kBarBytes = 256;
   static constexpr int kBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+  static_assert(kBytes <= 232448, "shared memory per CTA");
 };
 
 enum {
   BAR_Q = 0,
-  BAR_KFULL = 1,   // +2 stages
-  BAR_KEMPTY = 3,  // +2
-  BAR_VFULL = 5,   // +2
-  BAR_VEMPTY = 7,  // +2
-  BAR_SFULL = 9,   // +2 Q tiles
-  BAR_PFULL = 11,  // +2
-  BAR_ODONE = 13,  // +2
-  BAR_MMADONE = 15,
-  NUM_BARS = 16
+  BAR_KFULL = 1,   // +3 stages
+  BAR_KEMPTY = 4,  // +3
+  BAR_VFULL = 7,   // +3
+  BAR_VEMPTY = 10, // +3
+  BAR_SFULL = 13,  // +2 Q tiles
+  BAR_PFULL = 15,  // +2
+  BAR_ODONE = 17,  // +2
+  BAR_MMADONE = 19,
+  BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
+  NUM_BARS = 21
 };
 
-template <int D>
+template <int D, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
 context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap kv_map) {
-  using L = CtxSmem<D>;
+  using L = CtxSmem<D, DEC>;
+  constexpr int S = L::kStages;
+  // ring stage and phase of the g-th K / V tile of the stream
+  auto stg = [](int g) { return g % S; };
+  auto phs = [](int g) { return (g / S) & 1; };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -91,36 +100,81 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * NUM_BARS + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = blockIdx.x;
-  const int hk = hq / p.group;
   pdl_wait();
 
-  // ---- which context request / pair of query tiles ----
-  const int unit = __ldg(p.unit_order + blockIdx.y);  // longest units launch first
-  int lo = 0, hi = p.C - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.tile_prefix + mid) <= unit) lo = mid;
-    else hi = mid - 1;
+  // ---- the work item ----
+  // Context (DEC = false): CTA = (query head hq, unit of 256 rows of one context request); keys
+  // 0 .. the causal limit of each row.
+  // Generation (DEC = true): CTA = (generation request, KV head hk, split of the keys, group of
+  // 256 rows); rows are the (token i, query head hk*g + hl) pairs r = i*g + hl of the request's
+  // new tokens, keys kt0 .. kend-1 of the split, visibility per draft-token mask; partial
+  // results go to the split workspace when the request has several splits.
+  int hq = 0, hk, r, past, L_r, nv0, nv1, nkt0, nkt1, kt0 = 0, kend, q_row = 0, i0 = 0;
+  int gr = 0, n_new = 0, s_idx = 0, num_splits = 1, pr0 = 0, tok0 = 0;
+  bool item_ok;
+  if constexpr (!DEC) {
+    hq = blockIdx.x;
+    hk = hq / p.group;
+    const int unit = __ldg(p.unit_order + blockIdx.y);  // longest units launch first
+    int lo = 0, hi = p.C - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.tile_prefix + mid) <= unit) lo = mid;
+      else hi = mid - 1;
+    }
+    r = lo;
+    i0 = (unit - __ldg(p.tile_prefix + r)) * kCtxRowsPerCta;
+    const int n_r = __ldg(p.ctx_len + r);
+    past = __ldg(p.past + r);
+    q_row = __ldg(p.cu_q + r) + i0;
+    L_r = past + n_r;
+    kend = L_r;
+    // valid rows and KV tiles of query tiles A (0) and B (1); scalars, not arrays, so that a
+    // runtime tile index never forces them into local memory
+    nv0 = max(0, min(128, n_r - i0));
+    nv1 = max(0, min(128, n_r - i0 - 128));
+    nkt0 = nv0 > 0 ? (past + i0 + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
+    nkt1 = nv1 > 0 ? (past + i0 + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
+    item_ok = nv0 > 0 && unit >= 0 && unit < p.num_tiles;
+  } else {
+    hk = blockIdx.y;
+    const int2 im = p.titem_map[blockIdx.x];
+    gr = min(max(im.x, 0), p.G - 1);
+    r = p.C + gr;
+    n_new = __ldg(p.ctx_len + r);
+    past = __ldg(p.past + r);
+    L_r = past + n_new;
+    const int rows = n_new * p.group;
+    const int n_rg = (rows + kCtxTileM - 1) / kCtxTileM;
+    s_idx = im.y / max(n_rg, 1);
+    const int rg = im.y - s_idx * n_rg;
+    num_splits = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
+    kt0 = s_idx * p.kv_chunk;
+    kend = min(L_r, kt0 + p.kv_chunk);
+    pr0 = rg * kCtxTileM;  // first (token, head) pair of the CTA: one Q tile of 128 pairs
+    tok0 = __ldg(p.cu_q + r);
+    q_row = tok0 + pr0 / p.group;
+    nv0 = max(0, min(128, rows - pr0));
+    // both halves of the pipeline serve the same rows: A takes the split's even KV tiles, B the
+    // odd ones, each with its own S, P, O and softmax state, merged at the end
+    const int nk = (kend - kt0 + kCtxTileN - 1) / kCtxTileN;
+    nkt0 = (nk + 1) / 2;
+    nkt1 = nk / 2;
+    nv1 = nkt1 > 0 ? nv0 : 0;
+    item_ok = im.y >= 0 && s_idx < num_splits && kt0 < kend && nv0 > 0 && n_new >= 1 &&
+              n_new <= PKV_MAX_GEN_TOKENS && tok0 >= p.gen_row0 && tok0 + n_new <= p.T &&
+              static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(num_splits) * n_new <= p.total_parts;
   }
-  const int r = lo;
-  const int i0 = (unit - __ldg(p.tile_prefix + r)) * kCtxRowsPerCta;
-  const int n_r = __ldg(p.ctx_len + r);
-  const int past = __ldg(p.past + r);
-  const int row0 = __ldg(p.cu_q + r) + i0;
-  const int L_r = past + n_r;
-  // valid rows and KV tiles of query tiles A (0) and B (1); scalars, not arrays, so that a
-  // runtime tile index never forces them into local memory
-  const int nv0 = max(0, min(128, n_r - i0)), nv1 = max(0, min(128, n_r - i0 - 128));
-  const int nkt0 = nv0 > 0 ? (past + i0 + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
-  const int nkt1 = nv1 > 0 ? (past + i0 + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
-  if (nv0 <= 0 || unit < 0 || unit >= p.num_tiles) {  // plan disagrees with the launch
+  if (!item_ok) {  // plan disagrees with the launch
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
     return;
   }
   const bool hasB = nv1 > 0;
-  const int nT = hasB ? nkt1 : nkt0;       // KV tiles this CTA streams
-  const int zero_x = (nkt0 == nT) ? 0 : 1;  // first user of the last V tile zeroes its tail
+  // KV tiles this CTA streams; the first user of the last V tile zeroes its tail
+  const int nT = DEC ? nkt0 + nkt1 : (hasB ? nkt1 : nkt0);
+  const int zero_x = DEC ? (nT - 1) & 1 : ((nkt0 == nT) ? 0 : 1);
+  // tile j of Q tile x: which K / V tile of the stream (ring stage, phase), and which Q slot
+  auto gtile = [&](int j, int x) { return DEC ? 2 * j + x : j; };
 
   const uint32_t sQ = base_s + L::kQOff;
   auto sK = [&](int st) { return base_s + L::kKOff + st * L::kTile; };
@@ -129,16 +183,19 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   // ---- set-up: barriers, TMEM ----
   if (threadIdx.x == 0) {
     tc::mbar_init(bar(BAR_Q), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar(BAR_KFULL + s), 1);
       tc::mbar_init(bar(BAR_KEMPTY + s), 1);
       tc::mbar_init(bar(BAR_VFULL + s), 1);
       tc::mbar_init(bar(BAR_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(BAR_SFULL + s), 1);
       tc::mbar_init(bar(BAR_PFULL + s), 128);
       tc::mbar_init(bar(BAR_ODONE + s), 1);
     }
     tc::mbar_init(bar(BAR_MMADONE), 1);
+    tc::mbar_init(bar(BAR_MERGE), 128);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -176,17 +233,19 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
         const int pages_per_tile = kCtxTileN / box_rows;
         const int n_pages_seq = (L_r + p.B - 1) / p.B;
-        tc::mbar_arrive_expect_tx(bar(BAR_Q), (hasB ? 2 : 1) * 128 * D * 2);
-        for (int x = 0; x < (hasB ? 2 : 1); ++x)
+        const int n_q = (hasB && !DEC) ? 2 : 1;  // generation: one Q tile shared by A and B
+        tc::mbar_arrive_expect_tx(bar(BAR_Q), n_q * 128 * D * 2);
+        for (int x = 0; x < n_q; ++x)
           for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(BAR_Q), 0, dh, hq, row0 + 128 * x);
+            tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(BAR_Q), 0, dh, DEC ? hk * p.group : hq,
+                            DEC ? q_row + (128 / p.group) * x : q_row + 128 * x);
         int issued_k = 0, issued_v = 0;
         for (int j = 0; j < nT && !*abort_flag; ++j) {
-          const int st = j & 1;
+          const int st = stg(j);
           int pages[kCtxTileN / 16];
           int n_ok = 0;
           for (int pp = 0; pp < pages_per_tile; ++pp) {
-            const int lb = (j * kCtxTileN) / p.B + pp;  // B <= 128: whole pages per tile
+            const int lb = (kt0 + j * kCtxTileN) / p.B + pp;  // B <= 128: whole pages per tile
             int pg = -1;
             if (lb < n_pages_seq && lb < p.max_blocks) {
               pg = __ldg(tbl + lb);
@@ -199,7 +258,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             n_ok += pg >= 0;
           }
           const uint32_t bytes = static_cast<uint32_t>(n_ok) * box_rows * D * 2;
-          if (j >= 2 && !tc::mbar_wait(bar(BAR_KEMPTY + st), ((j - 2) >> 1) & 1)) { fail(); break; }
+          if (j >= S && !tc::mbar_wait(bar(BAR_KEMPTY + st), phs(j - S))) { fail(); break; }
           tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
           for (int pp = 0; pp < pages_per_tile; ++pp) {
             if (pages[pp] < 0) continue;
@@ -208,7 +267,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
                               (pages[pp] * 2 + 0) * p.B);
           }
           ++issued_k;
-          if (j >= 2 && !tc::mbar_wait(bar(BAR_VEMPTY + st), ((j - 2) >> 1) & 1)) { fail(); break; }
+          if (j >= S && !tc::mbar_wait(bar(BAR_VEMPTY + st), phs(j - S))) { fail(); break; }
           tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
           for (int pp = 0; pp < pages_per_tile; ++pp) {
             if (pages[pp] < 0) continue;
@@ -219,10 +278,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           ++issued_v;
         }
         if (*abort_flag) {  // let copies already in flight land before the CTA winds down
-          for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
-            tc::mbar_wait(bar(BAR_KFULL + (j & 1)), (j >> 1) & 1, 200000000LL);
-          for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
-            tc::mbar_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1, 200000000LL);
+          for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
+            tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
+          for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
+            tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
           tc::mbar_wait(bar(BAR_Q), 0, 200000000LL);
         }
       }
@@ -232,43 +291,58 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
         constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
         auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
+        // context: A and B share every K / V tile (the last one to use it frees it); generation:
+        // each tile has one user
         auto last_user = [&](int j) { return (hasB && j < nkt1) ? 1 : 0; };
+        auto frees = [&](int j, int x) { return DEC || x == last_user(j); };
+        auto kfull = [&](int j, int x) {
+          const int g = gtile(j, x);
+          return tc::mbar_wait(bar(BAR_KFULL + stg(g)), phs(g));
+        };
         auto issue_s = [&](int j, int x) {
-          const int st = j & 1;
+          const int st = stg(gtile(j, x));
+          const uint32_t qx = DEC ? 0 : x;
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = tc::sdesc_sw128(sQ + x * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
+            const uint64_t a = tc::sdesc_sw128(sQ + qx * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
             const uint64_t b = tc::sdesc_sw128(sK(st) + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
             tc::mma_bf16_ss(tmem + 128 * x, a, b, idesc_s, kk > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(BAR_SFULL + x));
-          if (x == last_user(j)) tc::mma_commit(bar(BAR_KEMPTY + st));
+          if (frees(j, x)) tc::mma_commit(bar(BAR_KEMPTY + st));
         };
-        bool ok = tc::mbar_wait(bar(BAR_Q), 0) && tc::mbar_wait(bar(BAR_KFULL + 0), 0);
+        bool ok = tc::mbar_wait(bar(BAR_Q), 0) && kfull(0, 0);
         if (ok) {
           tc::fence_after_sync();
           issue_s(0, 0);
-          if (hasB) issue_s(0, 1);
+          if (hasB) {
+            if (DEC) ok = kfull(0, 1);  // B's first tile is the stream's second
+            if (ok) {
+              tc::fence_after_sync();
+              issue_s(0, 1);
+            }
+          }
         }
         for (int j = 0; ok && j < nT && !*abort_flag; ++j) {
           bool v_ready = false;
           for (int x = 0; x < 2 && ok; ++x) {
             if (!uses(j, x)) continue;
+            const int g = gtile(j, x);
             if (!tc::mbar_wait(bar(BAR_PFULL + x), j & 1)) { ok = false; break; }
             if (!v_ready) {
-              if (!tc::mbar_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
-              v_ready = true;
+              if (!tc::mbar_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
+              v_ready = !DEC;  // context: B reuses A's tile
             }
             tc::fence_after_sync();
   #pragma unroll
             for (int kk = 0; kk < kCtxTileN / 16; ++kk) {
-              const uint64_t b = tc::sdesc_sw128(sV(j & 1) + kk * 16 * 128, L::kHalf, 1024);
+              const uint64_t b = tc::sdesc_sw128(sV(stg(g)) + kk * 16 * 128, L::kHalf, 1024);
               tc::mma_bf16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
             }
-            if (x == last_user(j)) tc::mma_commit(bar(BAR_VEMPTY + (j & 1)));
+            if (frees(j, x)) tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
             if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
             if (uses(j + 1, x)) {
-              if (!tc::mbar_wait(bar(BAR_KFULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) { ok = false; break; }
+              if (!kfull(j + 1, x)) { ok = false; break; }
               tc::fence_after_sync();
               issue_s(j + 1, x);
             }
@@ -289,6 +363,24 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     const uint32_t tO = tmem + 256 + 128 * x + lane_off;
     const int nvx = x ? nv1 : nv0, nk = x ? nkt1 : nkt0;
     const int q_pos = past + i0 + 128 * x + min(row, max(nvx, 1) - 1);  // padding rows mirror the last row
+    // generation rows: the row's token and the new keys it sees (bit j: key past + j)
+    uint64_t vis = ~0ull;
+    int tok_i = 0, hl = 0;
+    if constexpr (DEC) {
+      const int pr = pr0 + row;  // A and B hold the same rows
+      if (row < nvx) {
+        tok_i = pr / p.group;
+        hl = pr - tok_i * p.group;
+        if (p.mask != nullptr) {
+          const uint32_t* mrow = p.mask + static_cast<int64_t>(tok0 + tok_i - p.gen_row0) * p.mask_words;
+          vis = __ldg(mrow);
+          if (n_new > 32 && p.mask_words > 1) vis |= static_cast<uint64_t>(__ldg(mrow + 1)) << 32;
+          vis |= 1ull << tok_i;
+        } else {
+          vis = (2ull << tok_i) - 1;  // j <= i (i = 63 wraps to all ones)
+        }
+      }
+    }
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -304,14 +396,38 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       tc::reg_dep(v1);
       tc::reg_dep(v2);
       tc::reg_dep(v3);
-      const int lim = q_pos - j * kCtxTileN;  // key column c is visible iff c <= lim
-      if (__any_sync(0xffffffffu, lim < kCtxTileN - 1)) {
+      if constexpr (!DEC) {
+        const int lim = q_pos - j * kCtxTileN;  // key column c is visible iff c <= lim
+        if (__any_sync(0xffffffffu, lim < kCtxTileN - 1)) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          v0[e] = e <= lim ? v0[e] : __float_as_uint(-INFINITY);
-          v1[e] = 32 + e <= lim ? v1[e] : __float_as_uint(-INFINITY);
-          v2[e] = 64 + e <= lim ? v2[e] : __float_as_uint(-INFINITY);
-          v3[e] = 96 + e <= lim ? v3[e] : __float_as_uint(-INFINITY);
+          for (int e = 0; e < 32; ++e) {
+            v0[e] = e <= lim ? v0[e] : __float_as_uint(-INFINITY);
+            v1[e] = 32 + e <= lim ? v1[e] : __float_as_uint(-INFINITY);
+            v2[e] = 64 + e <= lim ? v2[e] : __float_as_uint(-INFINITY);
+            v3[e] = 96 + e <= lim ? v3[e] : __float_as_uint(-INFINITY);
+          }
+        }
+      } else {
+        const int tb = kt0 + gtile(j, x) * kCtxTileN;  // key of column 0
+        if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
+          // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
+          // keys this row's token sees (bits of vis), nothing at or past the split's end
+          auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
+          auto word = [&](int w) {
+            const int t0 = tb + 32 * w, sh = t0 - past;
+            uint32_t nv = 0u;
+            if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
+            else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
+            return (low(past - t0) | nv) & low(kend - t0);
+          };
+          const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+            v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
+            v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
+            v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
+          }
         }
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -343,7 +459,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       m_run = m_use;
       // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
       float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+      const float m_base = m_use == -INFINITY ? 0.f : m_use;  // no visible key yet (generation splits)
+      const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
       auto emit = [&](uint32_t(&v)[32], int c) {
         uint32_t pk[16];
 #pragma unroll
@@ -362,11 +479,12 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
       l_run += lsum.x + lsum.y;
       tc::tmem_wait_st();
-      if (j == nT - 1 && x == zero_x) {
+      if (gtile(j, x) == nT - 1 && x == zero_x) {
         // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
-        if (!warp_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
-        if (j * kCtxTileN + row >= L_r) {
-          uint8_t* vrow = base + (sV(j & 1) - base_s) + row * 128;
+        const int g = nT - 1;
+        if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
+        if (kt0 + g * kCtxTileN + row >= kend) {
+          uint8_t* vrow = base + (sV(stg(g)) - base_s) + row * 128;
 #pragma unroll
           for (int dh = 0; dh < D / 64; ++dh)
 #pragma unroll
@@ -383,23 +501,93 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     if (nk > 0) {
       if (ok && !warp_abort() && warp_wait(bar(BAR_ODONE + x), 0)) {
         tc::fence_after_sync();
-        const float inv_l = p.out_scale / l_run;
-        const int grow = row0 + 128 * x + row;
-        uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(hq) * D;
-        const bool store = row < nvx && grow < p.T;
+        if constexpr (!DEC) {
+          const float inv_l = p.out_scale / l_run;
+          const int grow = q_row + 128 * x + row;
+          uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(hq) * D;
+          const bool store = row < nvx && grow < p.T;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t v[32];
-          tc::tmem_ld32(tO + cc * 32, v);
-          if (store) {
-            uint32_t pk[16];
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            tc::tmem_ld32(tO + cc * 32, v);
+            if (store) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+              for (int e = 0; e < 32; e += 2)
+                pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              reinterpret_cast<uint4*>(orow + cc * 32)[k] =
-                  make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+              for (int k = 0; k < 4; ++k)
+                reinterpret_cast<uint4*>(orow + cc * 32)[k] =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
+          }
+        } else {
+          // the two halves of the split's keys: B hands its (m, l) over through shared memory
+          // (the K ring is idle once both halves are done) and A merges O_A and O_B from TMEM
+          float* xch = reinterpret_cast<float*>(base + (sK(0) - base_s));  // [2][128]
+          if (x == 1) {
+            xch[row] = m_run;
+            xch[128 + row] = l_run;
+            tc::mbar_arrive(bar(BAR_MERGE));
+          } else {
+            float mB = -INFINITY, lB = 0.f;
+            bool merged = true;
+            if (nkt1 > 0) {
+              merged = warp_wait(bar(BAR_MERGE), 0);
+              if (merged) {
+                tc::fence_after_sync();
+                mB = xch[row];
+                lB = xch[128 + row];
+              }
+            }
+            if (!merged) {
+              ok = false;
+            } else {
+              const float M = fmaxf(m_run, mB), Mb = M == -INFINITY ? 0.f : M;
+              const float fA = ex2_approx(m_run - Mb), fB = ex2_approx(mB - Mb);
+              const float l = fA * l_run + fB * lB;
+              const bool store = row < nvx;
+              const int64_t head = static_cast<int64_t>(hk) * p.group + hl;
+              const bool whole = num_splits == 1;  // else a partial result for the combine
+              const float sA = whole ? fA * p.out_scale / l : fA * p.out_scale;
+              const float sB = whole ? fB * p.out_scale / l : fB * p.out_scale;
+              uint16_t* orow = p.out + static_cast<int64_t>(tok0 + tok_i) * p.out_stride + head * D;
+              const int64_t pi =
+                  (static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new + tok_i) * p.Hq +
+                  head;
+              float* prow = p.part_o + pi * D;
+#pragma unroll
+              for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t va[32], vb[32];
+                tc::tmem_ld32(tO + cc * 32, va);
+                if (nkt1 > 0) {
+                  tc::tmem_ld32(tO + 128 + cc * 32, vb);  // O_B, same lanes
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) vb[e] = 0u;
+                }
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(va[e]) * sA + __uint_as_float(vb[e]) * sB;
+                if (store && whole) {
+                  uint32_t pk[16];
+#pragma unroll
+                  for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o[e], o[e + 1]);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k)
+                    reinterpret_cast<uint4*>(orow + cc * 32)[k] =
+                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                } else if (store) {
+#pragma unroll
+                  for (int k = 0; k < 8; ++k)
+                    reinterpret_cast<float4*>(prow + cc * 32)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                }
+              }
+              if (store && !whole) {
+                p.part_ml[pi * 2] = M;
+                p.part_ml[pi * 2 + 1] = l;
+              }
+            }
           }
         }
       } else if (ok) {
@@ -475,21 +663,20 @@ cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s) {
   return launch_pdl(stage_q8_kernel<false>, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
 }
 
-cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, bool fp8,
-                           cudaStream_t s) {
-  if (fp8) return cudaErrorNotSupported;
+template <int D, bool DEC>
+cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, cudaStream_t s) {
+  auto kern = context_attn_kernel<D, DEC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<D, DEC>::kBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid = DEC ? dim3(p.num_titems, p.Hkv) : dim3(p.Hq, p.num_tiles);
+  return launch_pdl(kern, grid, dim3(kThreads), CtxSmem<D, DEC>::kBytes, s, p, qm, km);
+}
+
+cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, bool dec, cudaStream_t s) {
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
-  dim3 grid(p.Hq, p.num_tiles);
-  cudaError_t e;
-  if (p.D == 128) {
-    e = cudaFuncSetAttribute(context_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<128>::kBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(context_attn_kernel<128>, grid, dim3(kThreads), CtxSmem<128>::kBytes, s, p, qm, km);
-  }
-  e = cudaFuncSetAttribute(context_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<64>::kBytes);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(context_attn_kernel<64>, grid, dim3(kThreads), CtxSmem<64>::kBytes, s, p, qm, km);
+  if (p.D == 128) return dec ? launch_context_t<128, true>(p, qm, km, s) : launch_context_t<128, false>(p, qm, km, s);
+  return dec ? launch_context_t<64, true>(p, qm, km, s) : launch_context_t<64, false>(p, qm, km, s);
 }
 
 }  // namespace pkv

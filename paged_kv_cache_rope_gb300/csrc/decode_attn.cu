@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   int2* item_map = reinterpret_cast<int2*>(p.ws + p.lay.item_map);
   int2* row_map = reinterpret_cast<int2*>(p.ws + p.lay.row_map);
   int2* witem_map = reinterpret_cast<int2*>(p.ws + p.lay.witem_map);
+  int2* titem_map = reinterpret_cast<int2*>(p.ws + p.lay.titem_map);
   int32_t* stage = p.ws + p.lay.stage_prefix;
   const bool staging = p.expect_stage_pages > 0;
   const int C = p.C, chunk = p.kv_chunk, cols = p.cols_per_cta;
@@ -109,7 +110,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + tid;
     // a: (new tokens, context units, generation splits, staged FP8 context pages)
-    // b: (narrow decode CTAs per KV head, partial-result rows, wide decode CTAs per KV head, -)
+    // b: (narrow decode CTAs per KV head, partial-result rows, wide decode CTAs per KV head,
+    //     tensor-core generation CTAs per KV head)
     Int8v x{z4, z4};
     if (r < p.R) {
       const int n = __ldg(p.ctx_len + r);
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int sr = (__ldg(p.past + r) + n + chunk - 1) / chunk, ncols = n * p.group;
         x.a.z = sr;
         if (ncols <= kDecodeNarrowMaxCols) x.b.x = sr * ((ncols + cols - 1) / cols);
+        else if (p.tc_wide) x.b.w = sr * ((ncols + kCtxTileM - 1) / kCtxTileM);
         else x.b.z = sr * ((ncols + kDecodeWideCols - 1) / kDecodeWideCols);
         x.b.y = sr * n;
       }
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         // direct maps for the decode CTAs and the combine rows (no searches there)
         for (int it = 0; it < x.b.x && ex.b.x + it < p.expect_items; ++it) item_map[ex.b.x + it] = make_int2(gr, it);
         for (int it = 0; it < x.b.z && ex.b.z + it < p.expect_witems; ++it) witem_map[ex.b.z + it] = make_int2(gr, it);
+        for (int it = 0; it < x.b.w && ex.b.w + it < p.expect_titems; ++it) titem_map[ex.b.w + it] = make_int2(gr, it);
         for (int i = 0; i < x.a.x; ++i) {
           const int row = ex.a.x + i - p.gen_row0;
           if (row >= 0 && row < p.gen_rows) row_map[row] = make_int2(gr, i);
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (staging) stage[C] = t.a.w;
     bad |= (t.a.x != p.T) || (t.a.y != p.expect_tiles) || (t.a.z != p.expect_splits) ||
            (t.b.x != p.expect_items) || (t.b.y != p.expect_parts) || (t.b.z != p.expect_witems) ||
+           (t.b.w != p.expect_titems) ||
            (staging && t.a.w != p.expect_stage_pages);
   }
   if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
@@ -794,6 +799,54 @@ decode_splitkv_kernel(DecodeParams p) {
 // per (generation row, query head); warp w streams splits w, w+W, ... with an online max (lane
 // i owns 4 consecutive head dims), then the W partial results are merged through shared memory
 // --------------------------------------------------------------------------------------------
+// Few splits: one warp per (generation row, query head), kCombinePairs pairs per CTA, each warp
+// an online log-sum-exp over all the row's splits (lane i owns 4 consecutive head dims).
+constexpr int kCombinePairs = 8;
+
+__global__ void __launch_bounds__(kCombinePairs * 32) combine_warp_kernel(DecodeParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * kCombinePairs + warp;
+  pdl_wait();
+  if (pair >= static_cast<int64_t>(p.gen_rows) * p.Hq) return;
+  const int grow = static_cast<int>(pair / p.Hq), hq = static_cast<int>(pair - static_cast<int64_t>(grow) * p.Hq);
+  const int row = p.gen_row0 + grow;
+  const int2 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
+  const int gr = min(max(rm.x, 0), p.G - 1), r = p.C + gr, i = rm.y;
+  const int S = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
+  if (S <= 1) return;  // written directly by the decode kernel
+  const int n_new = __ldg(p.new_len + r);
+  if (i < 0 || i >= n_new || static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(S) * n_new > p.total_parts) {
+    if (lane == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
+    return;
+  }
+  const int D = p.D;
+  const bool active = lane < D / 4;
+  const int64_t first = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + i;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + first * p.Hq + hq;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (first * p.Hq + hq) * D) + lane;
+  const int64_t stride_ml = static_cast<int64_t>(n_new) * p.Hq, stride4 = stride_ml * D / 4;
+  float M = -INFINITY, lsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = 0; s < S; ++s) {
+    const float2 m_l = ml[s * stride_ml];
+    const float4 v = active ? po[s * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float Mn = fmaxf(M, m_l.x);
+    const float Mb = Mn == -INFINITY ? 0.f : Mn;  // splits with no visible key (draft masks)
+    const float a = ex2_approx(M - Mb), b = ex2_approx(m_l.x - Mb);
+    acc.x = acc.x * a + v.x * b;
+    acc.y = acc.y * a + v.y * b;
+    acc.z = acc.z * a + v.z * b;
+    acc.w = acc.w * a + v.w * b;
+    lsum = lsum * a + m_l.y * b;
+    M = Mn;
+  }
+  if (!active) return;
+  const float inv = 1.f / lsum;
+  uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  *reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(row) * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
+}
+
 template <int W>  // warps per CTA: more for requests with many splits
 __global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
   __shared__ float4 s_acc[W][32];
@@ -878,6 +931,11 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
 
 cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.gen_rows) * p.Hq));
+  if (max_splits <= kCombinePairs) {  // one warp per (row, head)
+    const int64_t pairs = static_cast<int64_t>(p.gen_rows) * p.Hq;
+    return launch_pdl(combine_warp_kernel, dim3(static_cast<unsigned>((pairs + kCombinePairs - 1) / kCombinePairs)),
+                      dim3(kCombinePairs * 32), 0, s, p);
+  }
   // about 8 splits per warp, 4 to 16 warps
   if (max_splits > 64) return launch_pdl(combine_kernel<16>, grid, dim3(16 * 32), 0, s, p);
   if (max_splits > 32) return launch_pdl(combine_kernel<8>, grid, dim3(8 * 32), 0, s, p);

@@ -18,6 +18,7 @@ constexpr int kDecodeTile = 16;  // tokens per decode warp tile (mma.sync M)
 // on the narrow decode kernel, wider ones (draft tokens, large query groups) on the wide one.
 constexpr int kDecodeNarrowMaxCols = 16;
 constexpr int kDecodeWideCols = 64;  // columns per wide-decode CTA (4 warps x 16)
+constexpr int kTcChunkAlign = 128;   // split length multiple when generation rows use the tensor-core kernel
 
 // Device-side plan written by plan_kernel into the front of the workspace (int32 words).
 struct PlanLayout {
@@ -28,6 +29,7 @@ struct PlanLayout {
   int64_t part_prefix;   // [G + 1]  prefix of S_r * n_r (partial-result rows per query head)
   int64_t item_map;      // [num_items] int2 (generation request, item index within it)
   int64_t witem_map;     // [num_witems] the same for the wide decode kernel's CTAs
+  int64_t titem_map;     // [num_titems] the same for the tensor-core kernel's generation CTAs
   int64_t row_map;       // [generation rows] int2 (generation request, token index within it)
   int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
   int64_t stage_prefix;  // [C + 1]  8-bit pools: prefix of the context requests' page counts
@@ -70,7 +72,8 @@ struct PlanParams {
   int32_t R, C, G, T, Hkv, B, expect_tiles, expect_splits, kv_chunk, expect_stage_pages;
   int32_t Hq, group;
   int32_t cols_per_cta;  // decode score-tile columns per CTA: (token, query head) pairs
-  int32_t expect_items, expect_parts, expect_witems;
+  int32_t expect_items, expect_parts, expect_witems, expect_titems;
+  int32_t tc_wide;             // wide requests run on the tensor-core kernel (bf16 pool, 128 % group == 0)
   int32_t gen_row0, gen_rows;  // first packed row and number of rows of the generation requests
   const int32_t* ctx_len;
   const int32_t* past;
@@ -120,6 +123,16 @@ struct ContextParams {
   float scale_log2;
   float out_scale;          // multiplies O at the end (the FP8 dequantisation scale, else 1)
   int32_t* d_error;
+  // generation mode (wide generation requests on the tensor-core kernel): CTA = titem_map
+  // entry (generation request, split x row group) x KV head
+  int32_t G, gen_row0, kv_chunk, num_titems, mask_words;
+  int64_t total_parts;
+  const int2* titem_map;
+  const int32_t* split_prefix;
+  const int32_t* part_prefix;
+  const uint32_t* mask;
+  float* part_o;
+  float* part_ml;
 };
 
 // 8-bit pools with context requests: copies the context requests' pages into a bf16 staging
@@ -163,7 +176,9 @@ cudaError_t launch_decode(const DecodeParams& p, int kv_dtype, bool wide, cudaSt
 cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s);
 cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
+// dec = false: context units; true: wide generation requests (rows = (token, head) pairs of one
+// KV head, q_map boxes g heads x 128/g tokens, partial results for split requests).
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map,
-                           bool fp8, cudaStream_t s);
+                           bool dec, cudaStream_t s);
 
 }  // namespace pkv
