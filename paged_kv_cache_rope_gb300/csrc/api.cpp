@@ -224,8 +224,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
   L.witem_map = L.item_map + 2LL * hp->num_items;
   L.titem_map = L.witem_map + 2LL * hp->num_witems;
-  L.row_map = L.titem_map + 2LL * hp->num_titems;
-  L.unit_order = L.row_map + 2LL * (hp->T - hp->ctx_tokens);
+  L.row_map = (L.titem_map + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
+  L.unit_order = L.row_map + 4LL * (hp->T - hp->ctx_tokens);
   L.stage_prefix = L.unit_order + hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
   L.int_words = L.stage_tbl + (staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
@@ -618,7 +618,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.split_prefix = ws + hp.lay.split_prefix;
     dp.item_map = reinterpret_cast<const int2*>(ws + hp.lay.item_map);
     dp.witem_map = reinterpret_cast<const int2*>(ws + hp.lay.witem_map);
-    dp.row_map = reinterpret_cast<const int2*>(ws + hp.lay.row_map);
+    dp.row_map = reinterpret_cast<const int4*>(ws + hp.lay.row_map);
     dp.part_prefix = ws + hp.lay.part_prefix;
     dp.mask = batch->d_packed_mask;
     dp.mask_words = batch->d_packed_mask ? batch->mask_words : 0;

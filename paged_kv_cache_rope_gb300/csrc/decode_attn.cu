@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   int32_t* items = p.ws + p.lay.item_prefix;
   int32_t* parts = p.ws + p.lay.part_prefix;
   int2* item_map = reinterpret_cast<int2*>(p.ws + p.lay.item_map);
-  int2* row_map = reinterpret_cast<int2*>(p.ws + p.lay.row_map);
+  int4* row_map = reinterpret_cast<int4*>(p.ws + p.lay.row_map);
   int2* witem_map = reinterpret_cast<int2*>(p.ws + p.lay.witem_map);
   int2* titem_map = reinterpret_cast<int2*>(p.ws + p.lay.titem_map);
   int32_t* stage = p.ws + p.lay.stage_prefix;
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         for (int it = 0; it < x.b.w && ex.b.w + it < p.expect_titems; ++it) titem_map[ex.b.w + it] = make_int2(gr, it);
         for (int i = 0; i < x.a.x; ++i) {
           const int row = ex.a.x + i - p.gen_row0;
-          if (row >= 0 && row < p.gen_rows) row_map[row] = make_int2(gr, i);
+          // (splits, partial row of split 0, rows between splits, token index)
+          if (row >= 0 && row < p.gen_rows) row_map[row] = make_int4(x.a.z, ex.b.y + i, x.a.x, i);
         }
       }
     }
@@ -810,18 +811,16 @@ __global__ void __launch_bounds__(kCombinePairs * 32) combine_warp_kernel(Decode
   if (pair >= static_cast<int64_t>(p.gen_rows) * p.Hq) return;
   const int grow = static_cast<int>(pair / p.Hq), hq = static_cast<int>(pair - static_cast<int64_t>(grow) * p.Hq);
   const int row = p.gen_row0 + grow;
-  const int2 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
-  const int gr = min(max(rm.x, 0), p.G - 1), r = p.C + gr, i = rm.y;
-  const int S = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
+  const int4 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
+  const int S = rm.x, n_new = rm.z, i = rm.w;
   if (S <= 1) return;  // written directly by the decode kernel
-  const int n_new = __ldg(p.new_len + r);
-  if (i < 0 || i >= n_new || static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(S) * n_new > p.total_parts) {
+  const int64_t first = rm.y;  // partial row of split 0; split s: first + s * n_new
+  if (i < 0 || i >= n_new || first < 0 || first + static_cast<int64_t>(S - 1) * n_new >= p.total_parts) {
     if (lane == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
     return;
   }
   const int D = p.D;
   const bool active = lane < D / 4;
-  const int64_t first = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + i;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + first * p.Hq + hq;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + (first * p.Hq + hq) * D) + lane;
   const int64_t stride_ml = static_cast<int64_t>(n_new) * p.Hq, stride4 = stride_ml * D / 4;
@@ -855,19 +854,16 @@ __global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
   const int grow = blockIdx.x / p.Hq, hq = blockIdx.x - grow * p.Hq;  // generation row, query head
   pdl_wait();
   const int row = p.gen_row0 + grow;
-  const int2 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
-  const int gr = min(max(rm.x, 0), p.G - 1), r = p.C + gr, i = rm.y;
-  const int S = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
+  const int4 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
+  const int S = rm.x, n_new = rm.z, i = rm.w;
   if (S <= 1) return;  // written directly by the decode kernel
-  const int n_new = __ldg(p.new_len + r);
-  if (i < 0 || i >= n_new || static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(S) * n_new > p.total_parts) {
+  const int64_t first = rm.y;  // partial row of split 0; split s: first + s * n_new
+  if (i < 0 || i >= n_new || first < 0 || first + static_cast<int64_t>(S - 1) * n_new >= p.total_parts) {
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
     return;
   }
   const int D = p.D;
   const bool active = lane < D / 4;
-  // partial row of split s: part_prefix[gr] + s * n_new + i
-  const int64_t first = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + i;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + first * p.Hq + hq;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + (first * p.Hq + hq) * D) + lane;
   const int64_t stride_ml = static_cast<int64_t>(n_new) * p.Hq, stride4 = stride_ml * D / 4;

@@ -30,7 +30,8 @@ struct PlanLayout {
   int64_t item_map;      // [num_items] int2 (generation request, item index within it)
   int64_t witem_map;     // [num_witems] the same for the wide decode kernel's CTAs
   int64_t titem_map;     // [num_titems] the same for the tensor-core kernel's generation CTAs
-  int64_t row_map;       // [generation rows] int2 (generation request, token index within it)
+  int64_t row_map;       // [generation rows] int4 (splits, partial row of split 0, rows between
+                         // splits = the request's new tokens, token index), 16-byte aligned
   int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
   int64_t stage_prefix;  // [C + 1]  8-bit pools: prefix of the context requests' page counts
   int64_t stage_tbl;     // [C * max_blocks] 8-bit pools: block table into the bf16 staging pool
@@ -100,7 +101,7 @@ struct DecodeParams {
   const int32_t* split_prefix;
   const int2* item_map;
   const int2* witem_map;
-  const int2* row_map;
+  const int4* row_map;
   const int32_t* part_prefix;
   const uint32_t* mask;     // draft-token packed mask rows [gen_rows, mask_words] or null
   int32_t mask_words;
