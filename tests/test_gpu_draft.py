@@ -25,6 +25,11 @@ CASES = [
     ("chain_gqa16", [], [(2, 64), (3, 4100), 700], 32, 2, 128, 128, False),
     ("group32_single", [], [900, 33, 4097], 64, 2, 128, 64, False),
     ("mixed_ctx_tree", [(200, 64), (31, 0)], [(6, 500), 1200, (9, 2500)], 16, 4, 128, 32, True),
+    # tensor-core generation mode: one head per row (g = 1), several 128-row groups per request
+    ("tree_mha_d64_64tok", [], [(64, 300), (20, 5000), 70], 4, 4, 64, 16, True),
+    ("tree_gqa8_row_groups", [], [(20, 700), (64, 2000), (16, 4100)], 16, 2, 128, 32, True),
+    # a group that does not divide 128 keeps the mma.sync wide kernel even on a bf16 pool
+    ("tree_gqa6_mma_wide", [], [(5, 300), (9, 1000), 77], 12, 2, 128, 32, True),
 ]
 
 
