@@ -29,6 +29,14 @@
 // 8-bit pools (E4M3 or int8 codes): stage_q8_kernel first copies the context requests' pages
 // into a bf16 staging pool (exact code values) with its own block table; this kernel then runs
 // unchanged on it, with the pool scale folded into the score scale and into the output scale.
+// Generation mode (DEC, bf16 pools, generation requests with more (token, query head) pairs
+// than the mma.sync decode kernel's columns): a 128-row tile is 128/g draft tokens x the g query
+// heads of one KV head (the Q box spans g heads), so each K / V tile serves the whole group;
+// the two softmax warpgroups take the even and the odd KV tiles of one split of kv_chunk keys
+// against the same Q tile; at the end B hands its (max, sum) over through shared memory, A
+// merges O_A and O_B from TMEM and writes the output row (one split) or a partial row for the
+// combine kernel.  Visibility of the new keys comes from the
+// draft-token mask words (bitmaps per row), applied only to the tiles that hold new keys.
 // Rows past the request's end and keys past the causal limit are masked by select (never by
 // arithmetic on the loaded values); V rows past the sequence end are zeroed before PV, so
 // stale or poisoned pool slots cannot reach the output.  Every wait is bounded.

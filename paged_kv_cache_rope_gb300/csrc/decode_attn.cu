@@ -6,25 +6,33 @@
 // softmax, weighted sum of V) and 6.1 "两者分工" (generation = input length 1);
 // "TensorRT-LLM 源码完全拆解(一)", "AttentionMetadata 的字段与它的含义" (packed rows, host and
 // device copies of the lengths); "TensorRT-LLM框架概述" (intelliparadigm.com) section 1: decode
-// is bound by memory bandwidth.
+// is bound by memory bandwidth; adg.csdn.net/69730cc6 section 1.4 (draft tokens: several new
+// tokens per generation request, position offsets, packed masks).
 //
 // Redesign for GB300 (the pages' kernel gives one CTA per (request, head); here):
 //   * the work unit is (generation request, KV head, split of kv_chunk tokens), so short and
 //     long requests both fill 152 SMs;
-//   * a CTA's warps each stream their own run of 16-token tiles with a cp.async ring through
-//     shared memory (zero-fill past the sequence end), one block-table lookup per tile;
-//   * each KV head is read once for its whole GQA query group: S^T = K Q^T and
-//     O^T += V^T P^T run on mma.sync m16n8k16 with the group (up to 8 heads per n-tile) on N;
-//   * online softmax in base 2 with warp-shuffle column maxima; warps merge in shared memory;
-//   * the splits of one request are merged by combine_kernel with a log-sum-exp rescale (a
+//   * the score tile's columns are the (token, query head) pairs of one KV head, so each KV head
+//     is read once for its whole GQA query group and all of the request's draft tokens:
+//     S^T = K Q^T and O^T += V^T P^T run on mma.sync with the pairs on N;
+//   * narrow kernel (<= 16 columns): a CTA's warps each stream their own run of 16-token tiles
+//     with a cp.async ring through shared memory (zero-fill past the sequence end, one
+//     block-table lookup per tile) and merge in shared memory at the end;
+//     wide kernel (more columns, 8-bit pools or groups that do not divide 128; bf16 pools with
+//     such requests otherwise take the tcgen05 kernel's generation mode): the warps share one
+//     ring and each owns 16 columns over every tile;
+//   * online softmax in base 2 with warp-shuffle column maxima; draft-token visibility as a
+//     64-bit mask per column, applied only to tiles that hold new keys;
+//   * the splits of one request are merged by a combine kernel with a log-sum-exp rescale (a
 //     separate launch: merging inside the decode kernel's last CTA per pair was measured slower,
 //     since those merges hold SM slots that would otherwise stream KV).
-// FP8 pools: the codes feed mma.sync m16n8k32 E4M3 directly (K as stored, V after a 4x4 byte
+// FP8 pools (narrow kernel): the codes feed mma.sync m16n8k32 E4M3 directly (K as stored, V after a 4x4 byte
 // transpose in registers); Q (scaled by a power of two) and P (times 256) are each split into
 // hi + lo E4M3 codes and both halves are multiplied into the same fp32 accumulator, which keeps
 // about 8 significant bits of each -- the precision of a bf16 operand -- with no per-element
 // conversion of the pool.  The per-pool scale is applied to scores and outputs in fp32.
-// INT8 pools: the codes become exact f16 values in registers (sign bit flipped into the
+// INT8 pools, and FP8 pools in the wide kernel: the codes become exact f16 values in
+// registers (E4M3 by the hardware conversion; INT8 with the sign bit flipped into the
 // mantissa of 1024.0: a permute and a packed subtract per two codes) and run on
 // mma.sync m16n8k16 f16 with Q and P in f16; V keeps its +1152 bias through the MMA, which
 // comes off at the end as 1152 times the row sum of the same rounded P.
@@ -513,7 +521,7 @@ decode_splitkv_kernel(DecodeParams p) {
     const uint32_t sV0 = sK0 + SUB * Cfg::kTileBytes;
     const int t0 = w_begin + it * SUB * kDecodeTile;
 
-    // ---- S^T[16 tokens x 8 heads] = K Q^T for each sub-tile ----
+    // ---- S^T[16 tokens x 8 columns] = K Q^T for each sub-tile ----
     float sacc[SUB][NT][4];
 #pragma unroll
     for (int u = 0; u < SUB; ++u)
@@ -658,7 +666,7 @@ decode_splitkv_kernel(DecodeParams p) {
       }
     }
 
-    // ---- O^T[D x 8 heads] += V^T P^T ----
+    // ---- O^T[D x 8 columns] += V^T P^T ----
     if constexpr (!BYTES) {
 #pragma unroll
       for (int u = 0; u < SUB; ++u) {
