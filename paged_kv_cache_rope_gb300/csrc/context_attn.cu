@@ -250,12 +250,13 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         int issued_k = 0, issued_v = 0;
         for (int j = 0; j < nT && !*abort_flag; ++j) {
           const int st = stg(j);
-          int pages[kCtxTileN / 16];
+          int pages[kCtxTileN / 16];  // compile-time indices only: stays in registers
           int n_ok = 0;
-          for (int pp = 0; pp < pages_per_tile; ++pp) {
+#pragma unroll
+          for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
             const int lb = (kt0 + j * kCtxTileN) / p.B + pp;  // B <= 128: whole pages per tile
             int pg = -1;
-            if (lb < n_pages_seq && lb < p.max_blocks) {
+            if (pp < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
               pg = __ldg(tbl + lb);
               if (pg < 0 || pg >= p.NB) {
                 flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
@@ -268,7 +269,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           const uint32_t bytes = static_cast<uint32_t>(n_ok) * box_rows * D * 2;
           if (j >= S && !tc::mbar_wait(bar(BAR_KEMPTY + st), phs(j - S))) { fail(); break; }
           tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
-          for (int pp = 0; pp < pages_per_tile; ++pp) {
+#pragma unroll
+          for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
             if (pages[pp] < 0) continue;
             for (int dh = 0; dh < D / 64; ++dh)
               tc::tma_load_4d(sK(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_KFULL + st), 0, dh, hk,
@@ -277,7 +279,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           ++issued_k;
           if (j >= S && !tc::mbar_wait(bar(BAR_VEMPTY + st), phs(j - S))) { fail(); break; }
           tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
-          for (int pp = 0; pp < pages_per_tile; ++pp) {
+#pragma unroll
+          for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
             if (pages[pp] < 0) continue;
             for (int dh = 0; dh < D / 64; ++dh)
               tc::tma_load_4d(sV(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_VFULL + st), 0, dh, hk,
@@ -331,7 +334,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             }
           }
         }
-        for (int j = 0; ok && j < nT && !*abort_flag; ++j) {
+        // no abort-flag poll per tile: a shared-memory load here sits on the critical path
+        // (P ready -> next MMA); if another warp gave up, the waits below run out instead
+        for (int j = 0; ok && j < nT; ++j) {
           bool v_ready = false;
           for (int x = 0; x < 2 && ok; ++x) {
             if (!uses(j, x)) continue;
@@ -393,7 +398,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
-      if (warp_abort() || !warp_wait(bar(BAR_SFULL + x), j & 1)) { ok = false; break; }
+      if (!warp_wait(bar(BAR_SFULL + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
       uint32_t v0[32], v1[32], v2[32], v3[32];
       tc::tmem_ld32_async(tS + 0, v0);
