@@ -234,40 +234,45 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   if (warp >= 8) {
     // one setmaxnreg instruction for all four warps of the control warpgroup
     tc::regs_dec<kRegsControl>();
+    // The producer and MMA warps run their loops with all 32 lanes (waits and control flow
+    // warp-uniform) and let one elected lane issue the TMA copies / MMAs: a warp that sits
+    // diverged on one lane gets issue slots far less often next to a busy softmax warp on the
+    // same sub-partition, and the tensor pipe then runs dry between MMA batches.
     if (warp == kProducerWarp) {
       // ======================= TMA producer =======================
-      if (lane == 0) {
-        const int32_t* tbl = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
-        const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
-        const int pages_per_tile = kCtxTileN / box_rows;
-        const int n_pages_seq = (L_r + p.B - 1) / p.B;
-        const int n_q = (hasB && !DEC) ? 2 : 1;  // generation: one Q tile shared by A and B
+      const int32_t* tbl = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
+      const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
+      const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
+      const int n_pages_seq = (L_r + p.B - 1) / p.B;
+      const int n_q = (hasB && !DEC) ? 2 : 1;  // generation: one Q tile shared by A and B
+      if (tc::elect_one()) {
         tc::mbar_arrive_expect_tx(bar(BAR_Q), n_q * 128 * D * 2);
         for (int x = 0; x < n_q; ++x)
           for (int dh = 0; dh < D / 64; ++dh)
             tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(BAR_Q), 0, dh, DEC ? hk * p.group : hq,
                             DEC ? q_row + (128 / p.group) * x : q_row + 128 * x);
-        int issued_k = 0, issued_v = 0;
-        for (int j = 0; j < nT && !*abort_flag; ++j) {
-          const int st = stg(j);
-          int pages[kCtxTileN / 16];  // compile-time indices only: stays in registers
-          int n_ok = 0;
-#pragma unroll
-          for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
-            const int lb = (kt0 + j * kCtxTileN) / p.B + pp;  // B <= 128: whole pages per tile
-            int pg = -1;
-            if (pp < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
-              pg = __ldg(tbl + lb);
-              if (pg < 0 || pg >= p.NB) {
-                flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
-                pg = -1;
-              }
-            }
-            pages[pp] = pg;
-            n_ok += pg >= 0;
+      }
+      __syncwarp();
+      int issued_k = 0, issued_v = 0;
+      bool pok = true;
+      for (int j = 0; j < nT && !warp_abort(); ++j) {
+        const int st = stg(j);
+        // lane pp < pages_per_tile looks up page pp of the tile (B <= 128: whole pages per tile)
+        const int lb = (kt0 + j * kCtxTileN) / p.B + lane;
+        int pg = -1;
+        if (lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
+          pg = __ldg(tbl + lb);
+          if (pg < 0 || pg >= p.NB) {
+            flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+            pg = -1;
           }
-          const uint32_t bytes = static_cast<uint32_t>(n_ok) * box_rows * D * 2;
-          if (j >= S && !tc::mbar_wait(bar(BAR_KEMPTY + st), phs(j - S))) { fail(); break; }
+        }
+        const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * 2;
+        int pages[kCtxTileN / 16];
+#pragma unroll
+        for (int pp = 0; pp < kCtxTileN / 16; ++pp) pages[pp] = __shfl_sync(0xffffffffu, pg, pp);
+        if (j >= S && !warp_wait(bar(BAR_KEMPTY + st), phs(j - S))) { pok = false; break; }
+        if (tc::elect_one()) {
           tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
 #pragma unroll
           for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
@@ -276,8 +281,11 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
               tc::tma_load_4d(sK(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_KFULL + st), 0, dh, hk,
                               (pages[pp] * 2 + 0) * p.B);
           }
-          ++issued_k;
-          if (j >= S && !tc::mbar_wait(bar(BAR_VEMPTY + st), phs(j - S))) { fail(); break; }
+        }
+        __syncwarp();
+        ++issued_k;
+        if (j >= S && !warp_wait(bar(BAR_VEMPTY + st), phs(j - S))) { pok = false; break; }
+        if (tc::elect_one()) {
           tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
 #pragma unroll
           for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
@@ -286,34 +294,39 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
               tc::tma_load_4d(sV(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_VFULL + st), 0, dh, hk,
                               (pages[pp] * 2 + 1) * p.B);
           }
-          ++issued_v;
         }
-        if (*abort_flag) {  // let copies already in flight land before the CTA winds down
-          for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
-            tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
-          for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
-            tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
-          tc::mbar_wait(bar(BAR_Q), 0, 200000000LL);
-        }
+        __syncwarp();
+        ++issued_v;
+      }
+      if (!pok && lane == 0) fail();
+      __syncwarp();
+      if (warp_abort()) {  // let copies already in flight land before the CTA winds down
+        for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
+          tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
+        for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
+          tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
+        tc::mbar_wait(bar(BAR_Q), 0, 200000000LL);
       }
     } else if (warp == kMmaWarp) {
       // ======================= MMA issuer =======================
-      if (lane == 0) {
-        constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
-        constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
-        auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
-        // context: A and B share every K / V tile (the last one to use it frees it); generation:
-        // each tile has one user
-        auto last_user = [&](int j) { return (hasB && j < nkt1) ? 1 : 0; };
-        auto frees = [&](int j, int x) { return DEC || x == last_user(j); };
-        auto kfull = [&](int j, int x) {
-          const int g = gtile(j, x);
-          return tc::mbar_wait(bar(BAR_KFULL + stg(g)), phs(g));
-        };
-        auto issue_s = [&](int j, int x) {
-          const int st = stg(gtile(j, x));
-          const uint32_t qx = DEC ? 0 : x;
-  #pragma unroll
+      // tcgen05.commit tracks the MMAs of the thread that issues it: elect.sync on a converged
+      // warp picks the same (lowest) lane every time, so MMAs and commits share one thread.
+      constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
+      constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
+      auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
+      // context: A and B share every K / V tile (the last one to use it frees it); generation:
+      // each tile has one user
+      auto last_user = [&](int j) { return (hasB && j < nkt1) ? 1 : 0; };
+      auto frees = [&](int j, int x) { return DEC || x == last_user(j); };
+      auto kfull = [&](int j, int x) {
+        const int g = gtile(j, x);
+        return warp_wait(bar(BAR_KFULL + stg(g)), phs(g));
+      };
+      auto issue_s = [&](int j, int x) {
+        const int st = stg(gtile(j, x));
+        const uint32_t qx = DEC ? 0 : x;
+        if (tc::elect_one()) {
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t a = tc::sdesc_sw128(sQ + qx * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
             const uint64_t b = tc::sdesc_sw128(sK(st) + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
@@ -321,50 +334,57 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           }
           tc::mma_commit(bar(BAR_SFULL + x));
           if (frees(j, x)) tc::mma_commit(bar(BAR_KEMPTY + st));
-        };
-        bool ok = tc::mbar_wait(bar(BAR_Q), 0) && kfull(0, 0);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_s(0, 0);
-          if (hasB) {
-            if (DEC) ok = kfull(0, 1);  // B's first tile is the stream's second
-            if (ok) {
-              tc::fence_after_sync();
-              issue_s(0, 1);
-            }
+        }
+        __syncwarp();
+      };
+      bool ok = warp_wait(bar(BAR_Q), 0) && kfull(0, 0);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_s(0, 0);
+        if (hasB) {
+          if (DEC) ok = kfull(0, 1);  // B's first tile is the stream's second
+          if (ok) {
+            tc::fence_after_sync();
+            issue_s(0, 1);
           }
         }
-        // no abort-flag poll per tile: a shared-memory load here sits on the critical path
-        // (P ready -> next MMA); if another warp gave up, the waits below run out instead
-        for (int j = 0; ok && j < nT; ++j) {
-          bool v_ready = false;
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (!uses(j, x)) continue;
-            const int g = gtile(j, x);
-            if (!tc::mbar_wait(bar(BAR_PFULL + x), j & 1)) { ok = false; break; }
-            if (!v_ready) {
-              if (!tc::mbar_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
-              v_ready = !DEC;  // context: B reuses A's tile
-            }
-            tc::fence_after_sync();
-  #pragma unroll
+      }
+      // no abort-flag poll per tile: a shared-memory load here sits on the critical path
+      // (P ready -> next MMA); if another warp gave up, the waits below run out instead
+      for (int j = 0; ok && j < nT; ++j) {
+        bool v_ready = false;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!uses(j, x)) continue;
+          const int g = gtile(j, x);
+          if (!warp_wait(bar(BAR_PFULL + x), j & 1)) { ok = false; break; }
+          if (!v_ready) {
+            if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
+            v_ready = !DEC;  // context: B reuses A's tile
+          }
+          tc::fence_after_sync();
+          if (tc::elect_one()) {
+#pragma unroll
             for (int kk = 0; kk < kCtxTileN / 16; ++kk) {
               const uint64_t b = tc::sdesc_sw128(sV(stg(g)) + kk * 16 * 128, L::kHalf, 1024);
               tc::mma_bf16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
             }
             if (frees(j, x)) tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
             if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
-            if (uses(j + 1, x)) {
-              if (!kfull(j + 1, x)) { ok = false; break; }
-              tc::fence_after_sync();
-              issue_s(j + 1, x);
-            }
+          }
+          __syncwarp();
+          if (uses(j + 1, x)) {
+            if (!kfull(j + 1, x)) { ok = false; break; }
+            tc::fence_after_sync();
+            issue_s(j + 1, x);
           }
         }
-        if (!ok) fail();
+      }
+      if (!ok && lane == 0) fail();
+      if (tc::elect_one()) {
         tc::mma_commit(bar(BAR_MMADONE));
         tc::mbar_wait(bar(BAR_MMADONE), 0, 200000000LL);  // nothing of ours still runs on TMEM
       }
+      __syncwarp();
     }
   } else {
     // ======================= softmax warpgroups =======================
