@@ -199,7 +199,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(BAR_SFULL + s), 1);
-      tc::mbar_init(bar(BAR_PFULL + s), 128);
+      tc::mbar_init(bar(BAR_PFULL + s), 4);  // one arrive per softmax warp
       tc::mbar_init(bar(BAR_ODONE + s), 1);
     }
     tc::mbar_init(bar(BAR_MMADONE), 1);
@@ -526,8 +526,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         }
         tc::fence_proxy_async_smem();
       }
+      // one arrive per warp after the warp has synchronised (fewer atomics on one word)
       tc::fence_before_sync();
-      tc::mbar_arrive(bar(BAR_PFULL + x));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar(BAR_PFULL + x));
     }
     if (!ok) fail();
     // ---- epilogue: O / l -> bf16 rows ----
