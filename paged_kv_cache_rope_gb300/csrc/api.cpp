@@ -225,8 +225,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   L.witem_map = L.item_map + 2LL * hp->num_items;
   L.titem_map = L.witem_map + 2LL * hp->num_witems;
   L.row_map = (L.titem_map + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
-  L.unit_order = L.row_map + 4LL * (hp->T - hp->ctx_tokens);
-  L.stage_prefix = L.unit_order + hp->num_tiles;
+  L.unit_info = L.row_map + 4LL * (hp->T - hp->ctx_tokens);  // int4 entries: 16-byte aligned
+  L.stage_prefix = L.unit_info + 4LL * hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
   L.int_words = L.stage_tbl + (staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
   L.stage_pages = 0;
@@ -552,6 +552,9 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     }
     CUtensorMap qmap, kvmap;
     if (!encode_rows_map(&qmap, q_rot, D, num_q_heads, hp.T, q_row_stride * 2, pkv::kCtxTileM)) return PKV_ERR_CUDA;
+    CUtensorMap omap;  // output rows [T, Hq * D] (packed), for the full tiles' TMA stores
+    if (!encode_rows_map(&omap, out, D, num_q_heads, hp.T, static_cast<int64_t>(num_q_heads) * D * 2, pkv::kCtxTileM))
+      return PKV_ERR_CUDA;
     const int64_t pool_rows = ctx_blocks * 2 * pool->tokens_per_block;
     if (!encode_rows_map(&kvmap, ctx_pool, D, Hkv, pool_rows, static_cast<int64_t>(Hkv) * D * 2,
                          std::min(pool->tokens_per_block, pkv::kCtxTileN)))
@@ -569,7 +572,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.num_tiles = hp.num_tiles;
     cp.cu_q = ws + hp.lay.cu_q;
     cp.tile_prefix = ws + hp.lay.tile_prefix;
-    cp.unit_order = ws + hp.lay.unit_order;
+    cp.unit_info = reinterpret_cast<const int4*>(ws + hp.lay.unit_info);
     cp.ctx_len = batch->d_context_lengths;
     cp.past = batch->d_past_kv_lengths;
     cp.tbl = ctx_tbl;
@@ -581,7 +584,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.d_error = d_error;
     {
       LaunchScope ls(launches, "context_attn", cs);
-      e = pkv::launch_context(cp, &qmap, &kvmap, false, cs);
+      e = pkv::launch_context(cp, &qmap, &kvmap, &omap, false, cs);
     }
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     ++launches;
@@ -685,7 +688,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       tp.part_ml = dp.part_ml;
       {
         LaunchScope ls(launches, "decode_tc", gs);
-        e = pkv::launch_context(tp, &qmap_g, &kvmap_g, true, gs);
+        e = pkv::launch_context(tp, &qmap_g, &kvmap_g, &qmap_g, true, gs);  // no output map in generation mode
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;

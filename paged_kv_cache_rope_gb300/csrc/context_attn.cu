@@ -92,7 +92,7 @@ enum {
 template <int D, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
 context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
-                    const __grid_constant__ CUtensorMap kv_map) {
+                    const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
   using L = CtxSmem<D, DEC>;
   constexpr int S = L::kStages;
   // ring stage and phase of the g-th K / V tile of the stream
@@ -108,6 +108,41 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * NUM_BARS + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- set-up: barriers, TMEM (reads nothing earlier kernels write, so it runs before the
+  // grid-dependency wait and overlaps the previous kernel's tail) ----
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar(BAR_Q), 1);
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(bar(BAR_KFULL + s), 1);
+      tc::mbar_init(bar(BAR_KEMPTY + s), 1);
+      tc::mbar_init(bar(BAR_VFULL + s), 1);
+      tc::mbar_init(bar(BAR_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(BAR_SFULL + s), 1);
+      tc::mbar_init(bar(BAR_PFULL + s), 4);  // one arrive per softmax warp
+      tc::mbar_init(bar(BAR_ODONE + s), 1);
+    }
+    tc::mbar_init(bar(BAR_MMADONE), 1);
+    tc::mbar_init(bar(BAR_MERGE), 128);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(base_s + L::kBarOff + 8 * NUM_BARS, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tc::prefetch_tmap(&q_map);
+    tc::prefetch_tmap(&kv_map);
+    if (!DEC) tc::prefetch_tmap(&out_map);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
   pdl_wait();
 
   // ---- the work item ----
@@ -123,27 +158,23 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   if constexpr (!DEC) {
     hq = blockIdx.x;
     hk = hq / p.group;
-    const int unit = __ldg(p.unit_order + blockIdx.y);  // longest units launch first
-    int lo = 0, hi = p.C - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.tile_prefix + mid) <= unit) lo = mid;
-      else hi = mid - 1;
-    }
-    r = lo;
-    i0 = (unit - __ldg(p.tile_prefix + r)) * kCtxRowsPerCta;
-    const int n_r = __ldg(p.ctx_len + r);
-    past = __ldg(p.past + r);
-    q_row = __ldg(p.cu_q + r) + i0;
-    L_r = past + n_r;
+    // the plan's descriptor of the unit, longest units first: (request, first q row,
+    // past + first row, rows of the request from the first row on); rows are counted from the
+    // unit's first row, so `past` below is the key position of that row and i0 stays 0
+    const int4 u = __ldg(p.unit_info + blockIdx.y);
+    r = u.x;
+    q_row = u.y;
+    past = u.z;
+    const int n_rem = u.w;
+    L_r = past + n_rem;
     kend = L_r;
     // valid rows and KV tiles of query tiles A (0) and B (1); scalars, not arrays, so that a
     // runtime tile index never forces them into local memory
-    nv0 = max(0, min(128, n_r - i0));
-    nv1 = max(0, min(128, n_r - i0 - 128));
-    nkt0 = nv0 > 0 ? (past + i0 + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
-    nkt1 = nv1 > 0 ? (past + i0 + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
-    item_ok = nv0 > 0 && unit >= 0 && unit < p.num_tiles;
+    nv0 = max(0, min(128, n_rem));
+    nv1 = max(0, min(128, n_rem - 128));
+    nkt0 = nv0 > 0 ? (past + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
+    nkt1 = nv1 > 0 ? (past + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
+    item_ok = nv0 > 0 && r >= 0 && r < p.C && past >= 0 && q_row >= 0 && q_row + nv0 + nv1 <= p.T;
   } else {
     hk = blockIdx.y;
     const int2 im = p.titem_map[blockIdx.x];
@@ -173,10 +204,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
               n_new <= PKV_MAX_GEN_TOKENS && tok0 >= p.gen_row0 && tok0 + n_new <= p.T &&
               static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(num_splits) * n_new <= p.total_parts;
   }
-  if (!item_ok) {  // plan disagrees with the launch
-    if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
-    return;
-  }
+  if (!item_ok && threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
   const bool hasB = nv1 > 0;
   // KV tiles this CTA streams; the first user of the last V tile zeroes its tail
   const int nT = DEC ? nkt0 + nkt1 : (hasB ? nkt1 : nkt0);
@@ -187,38 +215,6 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   const uint32_t sQ = base_s + L::kQOff;
   auto sK = [&](int st) { return base_s + L::kKOff + st * L::kTile; };
   auto sV = [&](int st) { return base_s + L::kVOff + st * L::kTile; };
-
-  // ---- set-up: barriers, TMEM ----
-  if (threadIdx.x == 0) {
-    tc::mbar_init(bar(BAR_Q), 1);
-    for (int s = 0; s < S; ++s) {
-      tc::mbar_init(bar(BAR_KFULL + s), 1);
-      tc::mbar_init(bar(BAR_KEMPTY + s), 1);
-      tc::mbar_init(bar(BAR_VFULL + s), 1);
-      tc::mbar_init(bar(BAR_VEMPTY + s), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(bar(BAR_SFULL + s), 1);
-      tc::mbar_init(bar(BAR_PFULL + s), 4);  // one arrive per softmax warp
-      tc::mbar_init(bar(BAR_ODONE + s), 1);
-    }
-    tc::mbar_init(bar(BAR_MMADONE), 1);
-    tc::mbar_init(bar(BAR_MERGE), 128);
-    *abort_flag = 0;
-    tc::fence_barrier_init();
-  }
-  if (warp == kMmaWarp) {
-    tc::tmem_alloc(base_s + L::kBarOff + 8 * NUM_BARS, kTmemCols);
-    tc::tmem_relinquish();
-  }
-  if (warp == kProducerWarp && lane == 0) {
-    tc::prefetch_tmap(&q_map);
-    tc::prefetch_tmap(&kv_map);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
 
   auto fail = [&]() {
     flag_error(p.d_error, PKV_DEVERR_TIMEOUT);
@@ -231,7 +227,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   };
   auto warp_abort = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0) != 0; };
 
-  if (warp >= 8) {
+  if (!item_ok) {
+    // nothing to do: fall through to the teardown (TMEM is already allocated)
+  } else if (warp >= 8) {
     // one setmaxnreg instruction for all four warps of the control warpgroup
     tc::regs_dec<kRegsControl>();
     // The producer and MMA warps run their loops with all 32 lanes (waits and control flow
@@ -539,21 +537,44 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         if constexpr (!DEC) {
           const float inv_l = p.out_scale / l_run;
           const int grow = q_row + 128 * x + row;
+          // a full tile of 128 rows leaves through shared memory and two TMA stores (one per
+          // 64-wide half): each thread's own row would otherwise be 16 stores spread over 128
+          // different output rows per warp instruction; a partial tile (the end of a request,
+          // whose next rows belong to another request) keeps the per-row stores
+          const bool full = nvx == 128 && q_row + 128 * x + 128 <= p.T;
+          const uint32_t sO = sQ + x * L::kTile;  // this tile's Q slot: all of its S MMAs are done
           uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(hq) * D;
           const bool store = row < nvx && grow < p.T;
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t v[32];
             tc::tmem_ld32(tO + cc * 32, v);
-            if (store) {
-              uint32_t pk[16];
+            uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 32; e += 2)
-                pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+            for (int e = 0; e < 32; e += 2)
+              pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+            if (full) {
+              // 128-byte swizzle of the TMA box: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+              const uint32_t rbase = sO + (cc >> 1) * L::kHalf + row * 128;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + k) ^ static_cast<uint32_t>(row & 7);
+                st_shared_v4(rbase + chunk * 16, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+              }
+            } else if (store) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 reinterpret_cast<uint4*>(orow + cc * 32)[k] =
                     make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
+          }
+          if (full) {
+            tc::fence_proxy_async_smem();
+            tc::named_sync(1 + x, 128);  // the tile's four warps have written their rows
+            if ((warp & 3) == 0 && lane == 0) {
+              for (int dh = 0; dh < D / 64; ++dh) tc::tma_store_4d(&out_map, sO + dh * L::kHalf, 0, dh, hq, q_row + 128 * x);
+              tc::bulk_commit();
+              tc::bulk_wait_read0();
             }
           }
         } else {
@@ -699,19 +720,22 @@ cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s) {
 }
 
 template <int D, bool DEC>
-cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, cudaStream_t s) {
+cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& om,
+                             cudaStream_t s) {
   auto kern = context_attn_kernel<D, DEC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<D, DEC>::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid = DEC ? dim3(p.num_titems, p.Hkv) : dim3(p.Hq, p.num_tiles);
-  return launch_pdl(kern, grid, dim3(kThreads), CtxSmem<D, DEC>::kBytes, s, p, qm, km);
+  return launch_pdl(kern, grid, dim3(kThreads), CtxSmem<D, DEC>::kBytes, s, p, qm, km, om);
 }
 
-cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, bool dec, cudaStream_t s) {
+cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map, bool dec,
+                           cudaStream_t s) {
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
-  if (p.D == 128) return dec ? launch_context_t<128, true>(p, qm, km, s) : launch_context_t<128, false>(p, qm, km, s);
-  return dec ? launch_context_t<64, true>(p, qm, km, s) : launch_context_t<64, false>(p, qm, km, s);
+  const CUtensorMap& om = *static_cast<const CUtensorMap*>(out_map);
+  if (p.D == 128) return dec ? launch_context_t<128, true>(p, qm, km, om, s) : launch_context_t<128, false>(p, qm, km, om, s);
+  return dec ? launch_context_t<64, true>(p, qm, km, om, s) : launch_context_t<64, false>(p, qm, km, om, s);
 }
 
 }  // namespace pkv

@@ -179,10 +179,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
 
   // ---- context units, most KV tiles first: a counting sort by tile count (descending) ----
+  // Each slot gets the unit's descriptor (request, first q row, past + first row, rows left), so
+  // a context CTA reads one int4 instead of searching the tile prefix itself.
   const int U = p.expect_tiles;
-  int32_t* order = p.ws + p.lay.unit_order;
-  if (__syncthreads_or(bad)) {  // lengths disagree with the host plan: identity order, in range
-    for (int u = tid; u < U; u += kPlanThreads) order[u] = u;
+  int4* order = reinterpret_cast<int4*>(p.ws + p.lay.unit_info);
+  if (__syncthreads_or(bad)) {  // lengths disagree with the host plan: empty units (rejected)
+    for (int u = tid; u < U; u += kPlanThreads) order[u] = make_int4(0, 0, 0, 0);
     return;
   }
   if (U <= 0) return;
@@ -191,18 +193,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ int32_t s_part[kPlanThreads];
   for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
   __syncthreads();  // tiles[] (this block's global writes) and the zeroed histogram are visible
-  auto unit_cost = [&](int u) {
+  auto unit_desc = [&](int u) {
     int lo = 0, hi = C - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (tiles[mid] <= u) lo = mid;
       else hi = mid - 1;
     }
-    const int n = __ldg(p.ctx_len + lo), i0 = (u - tiles[lo]) * kCtxRowsPerCta;
-    const int keys = __ldg(p.past + lo) + i0 + min(kCtxRowsPerCta, n - i0);
+    const int i0 = (u - tiles[lo]) * kCtxRowsPerCta;
+    return make_int4(lo, cu[lo] + i0, __ldg(p.past + lo) + i0, __ldg(p.ctx_len + lo) - i0);
+  };
+  auto unit_cost = [&](const int4 d) {
+    const int keys = d.z + min(kCtxRowsPerCta, d.w);
     return min(kBins - 1, (keys + kCtxTileN - 1) / kCtxTileN);
   };
-  for (int u = tid; u < U; u += kPlanThreads) atomicAdd(&s_hist[kBins - 1 - unit_cost(u)], 1);
+  for (int u = tid; u < U; u += kPlanThreads) atomicAdd(&s_hist[kBins - 1 - unit_cost(unit_desc(u))], 1);
   __syncthreads();
   // exclusive scan of the (reversed) histogram: each thread owns kBins / kPlanThreads bins
   constexpr int kPer = kBins / kPlanThreads;
@@ -228,7 +233,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     run += v;
   }
   __syncthreads();
-  for (int u = tid; u < U; u += kPlanThreads) order[atomicAdd(&s_hist[kBins - 1 - unit_cost(u)], 1)] = u;
+  for (int u = tid; u < U; u += kPlanThreads) {
+    const int4 d = unit_desc(u);
+    order[atomicAdd(&s_hist[kBins - 1 - unit_cost(d)], 1)] = d;
+  }
 }
 
 // --------------------------------------------------------------------------------------------

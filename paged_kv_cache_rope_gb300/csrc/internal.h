@@ -32,7 +32,8 @@ struct PlanLayout {
   int64_t titem_map;     // [num_titems] the same for the tensor-core kernel's generation CTAs
   int64_t row_map;       // [generation rows] int4 (splits, partial row of split 0, rows between
                          // splits = the request's new tokens, token index), 16-byte aligned
-  int64_t unit_order;    // [num context units] unit ids, most KV tiles first (longest-first)
+  int64_t unit_info;     // [num context units] int4 (request, first q row, past + first row,
+                         // rows left), most KV tiles first (longest-first launch order)
   int64_t stage_prefix;  // [C + 1]  8-bit pools: prefix of the context requests' page counts
   int64_t stage_tbl;     // [C * max_blocks] 8-bit pools: block table into the bf16 staging pool
   int64_t int_words;     // total int32 words of the plan
@@ -114,7 +115,8 @@ struct ContextParams {
   int32_t C, T, Hq, Hkv, group, D, B, NB, max_blocks, num_tiles;
   const int32_t* cu_q;
   const int32_t* tile_prefix;
-  const int32_t* unit_order;  // [num_tiles] launch order of the context units
+  const int4* unit_info;      // [num_tiles] context units in launch order: (request r, first
+                              // q row, past_r + first row, rows of the request from there on)
   const int32_t* ctx_len;
   const int32_t* past;
   const int32_t* tbl;
@@ -179,7 +181,9 @@ cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
 // dec = false: context units; true: wide generation requests (rows = (token, head) pairs of one
 // KV head, q_map boxes g heads x 128/g tokens, partial results for split requests).
-cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map,
+// out_map: the output rows as a tiled map (box 128 rows x 64 columns of one head) for the
+// context tiles' TMA stores; unused by the generation mode.
+cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map,
                            bool dec, cudaStream_t s);
 
 }  // namespace pkv
