@@ -320,15 +320,20 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         const int g = gtile(j, x);
         return warp_wait(bar(BAR_KFULL + stg(g)), phs(g));
       };
+      // Descriptors are built once per operand tile and advanced by adding the byte offset / 16
+      // (the start address occupies the low bits and never carries out inside a tile): this
+      // warp competes for issue slots with a busy softmax warp, so every instruction counts.
+      const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dq1 = tc::sdesc_sw128(sQ + L::kTile, 16, 1024);
       auto issue_s = [&](int j, int x) {
         const int st = stg(gtile(j, x));
-        const uint32_t qx = DEC ? 0 : x;
+        const uint64_t a0 = (DEC || x == 0) ? dq0 : dq1;
+        const uint64_t b0 = tc::sdesc_sw128(sK(st), 16, 1024);
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = tc::sdesc_sw128(sQ + qx * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = tc::sdesc_sw128(sK(st) + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(tmem + 128 * x, a, b, idesc_s, kk > 0 ? 1u : 0u);
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4);
+            tc::mma_bf16_ss(tmem + 128 * x, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(BAR_SFULL + x));
           if (frees(j, x)) tc::mma_commit(bar(BAR_KEMPTY + st));
@@ -350,7 +355,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       // no abort-flag poll per tile: a shared-memory load here sits on the critical path
       // (P ready -> next MMA); if another warp gave up, the waits below run out instead
       for (int j = 0; ok && j < nT; ++j) {
-        bool v_ready = false;
+        bool v_ready = false, k_ready = false;  // context: B reuses the tiles A waited for
         for (int x = 0; x < 2 && ok; ++x) {
           if (!uses(j, x)) continue;
           const int g = gtile(j, x);
@@ -360,18 +365,19 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             v_ready = !DEC;  // context: B reuses A's tile
           }
           tc::fence_after_sync();
+          const uint64_t v0 = tc::sdesc_sw128(sV(stg(g)), L::kHalf, 1024);
           if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kCtxTileN / 16; ++kk) {
-              const uint64_t b = tc::sdesc_sw128(sV(stg(g)) + kk * 16 * 128, L::kHalf, 1024);
-              tc::mma_bf16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kCtxTileN / 16; ++kk)
+              tc::mma_bf16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk, v0 + static_cast<uint64_t>(kk * 16 * 128 / 16),
+                              idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
             if (frees(j, x)) tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
             if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
           }
           __syncwarp();
           if (uses(j + 1, x)) {
-            if (!kfull(j + 1, x)) { ok = false; break; }
+            if (!k_ready && !kfull(j + 1, x)) { ok = false; break; }
+            k_ready = !DEC;
             tc::fence_after_sync();
             issue_s(j + 1, x);
           }
