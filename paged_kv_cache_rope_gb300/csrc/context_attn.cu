@@ -330,10 +330,16 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         const uint64_t a0 = (DEC || x == 0) ? dq0 : dq1;
         const uint64_t b0 = tc::sdesc_sw128(sK(st), 16, 1024);
         if (tc::elect_one()) {
+          if constexpr (D == 128) {
+            // steps kk: ((kk / 4) * 16 KB + (kk % 4) * 32 B) / 16
+            tc::mma_bf16_ss_x8<0, 2, 4, 6, L::kHalf / 16, L::kHalf / 16 + 2, L::kHalf / 16 + 4, L::kHalf / 16 + 6>(
+                tmem + 128 * x, a0, b0, idesc_s, 0u);
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4);
-            tc::mma_bf16_ss(tmem + 128 * x, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4);
+              tc::mma_bf16_ss(tmem + 128 * x, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
           }
           tc::mma_commit(bar(BAR_SFULL + x));
           if (frees(j, x)) tc::mma_commit(bar(BAR_KEMPTY + st));
@@ -367,10 +373,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           tc::fence_after_sync();
           const uint64_t v0 = tc::sdesc_sw128(sV(stg(g)), L::kHalf, 1024);
           if (tc::elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < kCtxTileN / 16; ++kk)
-              tc::mma_bf16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk, v0 + static_cast<uint64_t>(kk * 16 * 128 / 16),
-                              idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
+            tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
             if (frees(j, x)) tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
             if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
           }

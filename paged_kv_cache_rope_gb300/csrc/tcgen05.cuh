@@ -154,6 +154,48 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Eight K=16 steps of one 128 x N x 128 product in one statement (one predicate set-up): A and
+// B advance by the given per-step descriptor increments (16-byte units).  The first step
+// accumulates into D only when `accumulate` is non-zero, the others always.
+template <uint32_t A0, uint32_t A1, uint32_t A2, uint32_t A3, uint32_t A4, uint32_t A5, uint32_t A6, uint32_t A7>
+__device__ __forceinline__ void mma_bf16_ss_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 a, b;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      " add.s64 a, %1, %5;\n add.s64 b, %2, %5;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.s64 a, %1, %6;\n add.s64 b, %2, %6;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.s64 a, %1, %7;\n add.s64 b, %2, %7;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.s64 a, %1, %8;\n add.s64 b, %2, %8;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.s64 a, %1, %9;\n add.s64 b, %2, %9;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.s64 a, %1, %10;\n add.s64 b, %2, %10;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.s64 a, %1, %11;\n add.s64 b, %2, %11;\n tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(A1), "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6),
+      "n"(A7)
+      : "memory");
+  (void)A0;
+}
+// Eight K=16 steps of P(TMEM) x V: A (TMEM) advances 8 columns per step, B by `BSTEP`
+// descriptor units (16 bytes).
+template <uint32_t BSTEP>
+__device__ __forceinline__ void mma_bf16_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 b;\n .reg .b32 a;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " add.u32 a, %1, 8;\n add.s64 b, %2, %5;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 16;\n add.s64 b, %2, %6;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 24;\n add.s64 b, %2, %7;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 32;\n add.s64 b, %2, %8;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 40;\n add.s64 b, %2, %9;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 48;\n add.s64 b, %2, %10;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 56;\n add.s64 b, %2, %11;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP),
+      "n"(4 * BSTEP), "n"(5 * BSTEP), "n"(6 * BSTEP), "n"(7 * BSTEP)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
                : "memory");
