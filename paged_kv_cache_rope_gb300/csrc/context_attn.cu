@@ -266,33 +266,23 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           }
         }
         const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * 2;
-        int pages[kCtxTileN / 16];
-#pragma unroll
-        for (int pp = 0; pp < kCtxTileN / 16; ++pp) pages[pp] = __shfl_sync(0xffffffffu, pg, pp);
+        // one lane registers the tile's bytes, then every lane with a page issues its own copies
+        // (no shuffles, no serial issue loop on one lane)
+        const uint32_t koff = static_cast<uint32_t>(lane * box_rows * 128);
         if (j >= S && !warp_wait(bar(BAR_KEMPTY + st), phs(j - S))) { pok = false; break; }
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
-#pragma unroll
-          for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
-            if (pages[pp] < 0) continue;
-            for (int dh = 0; dh < D / 64; ++dh)
-              tc::tma_load_4d(sK(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_KFULL + st), 0, dh, hk,
-                              (pages[pp] * 2 + 0) * p.B);
-          }
-        }
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
+        __syncwarp();
+        if (pg >= 0)
+          for (int dh = 0; dh < D / 64; ++dh)
+            tc::tma_load_4d(sK(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_KFULL + st), 0, dh, hk, (pg * 2 + 0) * p.B);
         __syncwarp();
         ++issued_k;
         if (j >= S && !warp_wait(bar(BAR_VEMPTY + st), phs(j - S))) { pok = false; break; }
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
-#pragma unroll
-          for (int pp = 0; pp < kCtxTileN / 16; ++pp) {
-            if (pages[pp] < 0) continue;
-            for (int dh = 0; dh < D / 64; ++dh)
-              tc::tma_load_4d(sV(st) + dh * L::kHalf + pp * box_rows * 128, &kv_map, bar(BAR_VFULL + st), 0, dh, hk,
-                              (pages[pp] * 2 + 1) * p.B);
-          }
-        }
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
+        __syncwarp();
+        if (pg >= 0)
+          for (int dh = 0; dh < D / 64; ++dh)
+            tc::tma_load_4d(sV(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_VFULL + st), 0, dh, hk, (pg * 2 + 1) * p.B);
         __syncwarp();
         ++issued_v;
       }
