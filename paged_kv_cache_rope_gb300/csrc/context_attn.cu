@@ -315,10 +315,14 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       // warp competes for issue slots with a busy softmax warp, so every instruction counts.
       const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
       const uint64_t dq1 = tc::sdesc_sw128(sQ + L::kTile, 16, 1024);
+      // per-stage K / V descriptors: stages are L::kTile apart, i.e. kTile / 16 descriptor units
+      const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
+      const uint64_t dv0 = tc::sdesc_sw128(sV(0), L::kHalf, 1024);
+      auto stage_off = [](int st) { return static_cast<uint64_t>(st) * (L::kTile / 16); };
       auto issue_s = [&](int j, int x) {
         const int st = stg(gtile(j, x));
         const uint64_t a0 = (DEC || x == 0) ? dq0 : dq1;
-        const uint64_t b0 = tc::sdesc_sw128(sK(st), 16, 1024);
+        const uint64_t b0 = dk0 + stage_off(st);
         if (tc::elect_one()) {
           if constexpr (D == 128) {
             // steps kk: ((kk / 4) * 16 KB + (kk % 4) * 32 B) / 16
@@ -361,7 +365,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             v_ready = !DEC;  // context: B reuses A's tile
           }
           tc::fence_after_sync();
-          const uint64_t v0 = tc::sdesc_sw128(sV(stg(g)), L::kHalf, 1024);
+          const uint64_t v0 = dv0 + stage_off(stg(g));
           if (tc::elect_one()) {
             static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
             tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
