@@ -199,9 +199,19 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
 #ifndef PKV_TC_MIN_CHUNK
 #define PKV_TC_MIN_CHUNK 2048
 #endif
-  if (hp->tc_wide)  // whole 128-key tiles per split, and enough of them to amortise a CTA's set-up
-    hp->kv_chunk = std::max<int>(PKV_TC_MIN_CHUNK,
-                                 (hp->kv_chunk + pkv::kTcChunkAlign - 1) / pkv::kTcChunkAlign * pkv::kTcChunkAlign);
+  if (hp->tc_wide) {
+    // whole 128-key tiles per split, enough of them to amortise a CTA's set-up, and about two
+    // waves of the (one-per-SM) tensor-core CTAs: a longer split costs nothing there while every
+    // extra split adds partial rows and a combine pass (measured on 64 requests x 8 draft
+    // tokens: no split at all ran the kernel as fast and saved the 17 us combine)
+    int64_t total = 0;
+    for (int r = hp->C; r < hp->R; ++r) total += b->h_past_kv_lengths[r] + b->h_context_lengths[r];
+    const int64_t waves2 = 2LL * device_sm_count();
+    const int64_t tc_chunk = (total * pool->num_kv_heads + waves2 - 1) / waves2;
+    hp->kv_chunk = static_cast<int>(std::max<int64_t>(
+        PKV_TC_MIN_CHUNK, (std::max<int64_t>(tc_chunk, hp->kv_chunk) + pkv::kTcChunkAlign - 1) / pkv::kTcChunkAlign *
+                              pkv::kTcChunkAlign));
+  }
   hp->decode_nt = max_narrow > 8 ? 2 : 1;
   const int cols = 8 * hp->decode_nt;
   hp->num_splits = hp->max_splits = hp->num_items = hp->num_witems = hp->num_titems = hp->num_parts = 0;
