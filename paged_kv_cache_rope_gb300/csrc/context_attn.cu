@@ -18,11 +18,18 @@
 //                max / sum in base 2 (O is rescaled in TMEM only when the max grows by more than
 //                2^8), and writes P as bf16 back into the first 64 columns of its own S buffer;
 //     warp 8     TMA producer: Q once, then per 128-key tile the pool pages of K and V through
-//                the block table (one box per page and 64-wide head-dim half);
+//                the block table (lane i looks up and loads page i: one box per page and
+//                64-wide head-dim half);
 //     warp 9     TMEM owner and MMA issuer (warps 10-11 only complete the warpgroup), in the order
 //                  S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
 //                so one tile's softmax overlaps the other tile's MMAs.  PV takes P straight from
 //                TMEM (A operand in tensor memory) and V from shared memory (MN-major).
+//   Warps 8 and 9 share their sub-partitions with busy softmax warps and get few issue slots,
+//   so they run converged, one elect.sync lane issues, and an 8-step MMA batch is a single
+//   inline-asm statement over descriptors built once per operand tile: every instruction they
+//   spend between MMA batches leaves the tensor pipe idle.
+//   A full 128-row output tile is written into its own (finished) Q slot and leaves with two
+//   TMA stores; per-thread row stores would scatter each warp instruction over 32 rows.
 //   TMEM columns: S_A | S_B | O_A | O_B (4 x 128 of 128 lanes).  tcgen05 work issued by one
 //   thread completes in order, so a commit after S_X(j) also covers PV_X(j-1): the softmax of
 //   tile j may rescale O_X as soon as S_X(j) has landed.
