@@ -92,6 +92,21 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int D, int heads, int64
   return r == CUDA_SUCCESS;
 }
 
+// 8-bit pool rows of D one-byte codes: dims (D, heads, rows), box D x 1 head x box_rows, with
+// the 128-byte swizzle (D = 128: one row per swizzle span).
+bool encode_raw8_map(CUtensorMap* map, const void* base, int D, int heads, int64_t rows, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads) * D};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct HostPlan {
   int R = 0, C = 0, G = 0, T = 0, ctx_tokens = 0, max_gen_tokens = 0;
   int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
@@ -195,7 +210,9 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
     if (cols_r <= pkv::kDecodeNarrowMaxCols) max_narrow = std::max(max_narrow, cols_r);
     else any_wide = true;
   }
-  hp->tc_wide = any_wide && pool->dtype == PKV_BF16 && group <= 128 && 128 % group == 0;
+  // the tensor-core generation mode: bf16 pools, and 8-bit pools at head_dim 128 (their codes
+  // are converted to f16 in shared memory)
+  hp->tc_wide = any_wide && group <= 128 && 128 % group == 0 && (pool->dtype == PKV_BF16 || pool->head_dim == 128);
 #ifndef PKV_TC_MIN_CHUNK
 #define PKV_TC_MIN_CHUNK 2048
 #endif
@@ -661,8 +678,10 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       CUtensorMap qmap_g, kvmap_g;
       if (!encode_rows_map(&qmap_g, q_rot, D, num_q_heads, hp.T, q_row_stride * 2, pkv::kCtxTileM / group, group))
         return PKV_ERR_CUDA;
-      if (!encode_rows_map(&kvmap_g, pool->pool, D, Hkv, static_cast<int64_t>(pool->num_blocks) * 2 * pool->tokens_per_block,
-                           static_cast<int64_t>(Hkv) * D * 2, std::min(pool->tokens_per_block, pkv::kCtxTileN)))
+      const int64_t pool_rows_g = static_cast<int64_t>(pool->num_blocks) * 2 * pool->tokens_per_block;
+      const int box_rows_g = std::min(pool->tokens_per_block, pkv::kCtxTileN);
+      if (q8 ? !encode_raw8_map(&kvmap_g, pool->pool, D, Hkv, pool_rows_g, box_rows_g)
+             : !encode_rows_map(&kvmap_g, pool->pool, D, Hkv, pool_rows_g, static_cast<int64_t>(Hkv) * D * 2, box_rows_g))
         return PKV_ERR_CUDA;
       pkv::ContextParams tp{};
       tp.C = hp.C;
@@ -681,8 +700,9 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       tp.pool = static_cast<const uint8_t*>(pool->pool);
       tp.out = static_cast<uint16_t*>(out);
       tp.out_stride = static_cast<int64_t>(num_q_heads) * D;
-      tp.scale_log2 = scale_log2;
-      tp.out_scale = 1.0f;
+      tp.scale_log2 = q8 ? scale_log2 * pool->kv_scale_quant_orig : scale_log2;
+      tp.out_scale = q8 ? pool->kv_scale_quant_orig : 1.0f;
+      tp.kv_dtype = pool->dtype;
       tp.d_error = d_error;
       tp.G = hp.G;
       tp.gen_row0 = hp.ctx_tokens;

@@ -68,18 +68,26 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could
 
 // Context: Q_A, Q_B, K[2], V[2].  Generation: one Q tile (A and B share it), K[3], V[3] -- a
 // deeper ring, since each K / V tile has one consumer and the two halves alternate.
-template <int D, bool DEC>
+// Generation with an 8-bit pool (KV != 0): Q, K[2], V[2] as f16, plus a ring of the raw codes
+// (K[2], V[2]) that TMA fills and the converter warps turn into f16, and the per-row Q scales.
+template <int D, bool DEC, int KV = 0>
 struct CtxSmem {
+  static constexpr bool kQ8 = KV != 0;
   static constexpr int kHalf = 128 * 128;         // one 64-wide half of a 128-row tile (bytes)
   static constexpr int kTile = (D / 64) * kHalf;  // one Q tile or one K / V stage
-  static constexpr int kStages = DEC ? 3 : 2;
+  static constexpr int kStages = (DEC && !kQ8) ? 3 : 2;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = (DEC ? 1 : 2) * kTile;
   static constexpr int kVOff = kKOff + kStages * kTile;
-  static constexpr int kBarOff = kVOff + kStages * kTile;
+  static constexpr int kRawTile = 128 * D;        // 128 rows of D one-byte codes
+  static constexpr int kRawKOff = kVOff + kStages * kTile;
+  static constexpr int kRawVOff = kRawKOff + (kQ8 ? 2 : 0) * kRawTile;
+  static constexpr int kBarOff = kRawVOff + (kQ8 ? 2 : 0) * kRawTile;
   static constexpr int kBarBytes = 256;
-  static constexpr int kBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+  static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 2^(e_row - 14) of Q row
+  static constexpr int kBytes = kQScaleOff + (kQ8 ? 128 * 4 : 0) + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
+  static_assert(!kQ8 || (DEC && D == 128), "8-bit codes only in the generation mode at head_dim 128");
 };
 
 enum {
@@ -93,14 +101,23 @@ enum {
   BAR_ODONE = 17,  // +2
   BAR_MMADONE = 19,
   BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
-  NUM_BARS = 21
+  BAR_RAWK = 21,   // +2: 8-bit generation mode, raw K codes landed (TMA)
+  BAR_RAWV = 23,   // +2: raw V codes landed
+  BAR_RAWEMPTY = 25, // +2: converters done reading a raw stage
+  BAR_QRAW = 27,   // the bf16 Q tile landed (the converters turn it into scaled f16)
+  NUM_BARS = 28
 };
+constexpr int kConvWarp0 = 10;  // 8-bit generation mode: warps 10 and 11 convert codes to f16
+constexpr int kConvWarps = 2;
 
-template <int D, bool DEC>
+template <int D, bool DEC, int KV>
 __global__ void __launch_bounds__(kThreads, 1)
 context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
-  using L = CtxSmem<D, DEC>;
+  using L = CtxSmem<D, DEC, KV>;
+  // 8-bit pool in the generation mode: the producer lands raw codes, warps 10-11 convert them
+  // (and Q, scaled per row) to f16, and every MMA runs kind::f16 on f16 operands
+  constexpr bool Q8 = L::kQ8;
   constexpr int S = L::kStages;
   // ring stage and phase of the g-th K / V tile of the stream
   auto stg = [](int g) { return g % S; };
@@ -119,12 +136,22 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   // ---- set-up: barriers, TMEM (reads nothing earlier kernels write, so it runs before the
   // grid-dependency wait and overlaps the previous kernel's tail) ----
   if (threadIdx.x == 0) {
-    tc::mbar_init(bar(BAR_Q), 1);
+    // Q / K / V ready: the producer's transaction arrive, or (8-bit) one arrive per converter warp
+    const uint32_t ready_count = Q8 ? kConvWarps : 1;
+    tc::mbar_init(bar(BAR_Q), ready_count);
     for (int s = 0; s < S; ++s) {
-      tc::mbar_init(bar(BAR_KFULL + s), 1);
+      tc::mbar_init(bar(BAR_KFULL + s), ready_count);
       tc::mbar_init(bar(BAR_KEMPTY + s), 1);
-      tc::mbar_init(bar(BAR_VFULL + s), 1);
+      tc::mbar_init(bar(BAR_VFULL + s), ready_count);
       tc::mbar_init(bar(BAR_VEMPTY + s), 1);
+    }
+    if (Q8) {
+      for (int s = 0; s < 2; ++s) {
+        tc::mbar_init(bar(BAR_RAWK + s), 1);
+        tc::mbar_init(bar(BAR_RAWV + s), 1);
+        tc::mbar_init(bar(BAR_RAWEMPTY + s), kConvWarps);
+      }
+      tc::mbar_init(bar(BAR_QRAW), 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(BAR_SFULL + s), 1);
@@ -250,11 +277,12 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
       const int n_pages_seq = (L_r + p.B - 1) / p.B;
       const int n_q = (hasB && !DEC) ? 2 : 1;  // generation: one Q tile shared by A and B
+      const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: the converters make Q f16 first
       if (tc::elect_one()) {
-        tc::mbar_arrive_expect_tx(bar(BAR_Q), n_q * 128 * D * 2);
+        tc::mbar_arrive_expect_tx(bar(q_bar), n_q * 128 * D * 2);
         for (int x = 0; x < n_q; ++x)
           for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(BAR_Q), 0, dh, DEC ? hk * p.group : hq,
+            tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, DEC ? hk * p.group : hq,
                             DEC ? q_row + (128 / p.group) * x : q_row + 128 * x);
       }
       __syncwarp();
@@ -272,7 +300,29 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             pg = -1;
           }
         }
-        const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * 2;
+        const uint32_t bytes =
+            static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
+        if constexpr (Q8) {
+          // raw codes of page `lane` into the raw ring; the converters free a stage after
+          // reading both its K and V
+          const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
+          if (j >= 2 && !warp_wait(bar(BAR_RAWEMPTY + (j & 1)), ((j - 2) >> 1) & 1)) { pok = false; break; }
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(bar(BAR_RAWK + (j & 1)), bytes);
+            tc::mbar_arrive_expect_tx(bar(BAR_RAWV + (j & 1)), bytes);
+          }
+          __syncwarp();
+          if (pg >= 0) {
+            tc::tma_load_3d(base_s + L::kRawKOff + (j & 1) * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + (j & 1)), 0,
+                            hk, (pg * 2 + 0) * p.B);
+            tc::tma_load_3d(base_s + L::kRawVOff + (j & 1) * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + (j & 1)), 0,
+                            hk, (pg * 2 + 1) * p.B);
+          }
+          __syncwarp();
+          ++issued_k;
+          ++issued_v;
+          continue;
+        }
         // one lane registers the tile's bytes, then every lane with a page issues its own copies
         // (no shuffles, no serial issue loop on one lane)
         const uint32_t koff = static_cast<uint32_t>(lane * box_rows * 128);
@@ -296,18 +346,25 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       if (!pok && lane == 0) fail();
       __syncwarp();
       if (warp_abort()) {  // let copies already in flight land before the CTA winds down
-        for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
-          tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
-        for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
-          tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
-        tc::mbar_wait(bar(BAR_Q), 0, 200000000LL);
+        if constexpr (Q8) {
+          for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j) {
+            tc::mbar_wait(bar(BAR_RAWK + (j & 1)), (j >> 1) & 1, 200000000LL);
+            tc::mbar_wait(bar(BAR_RAWV + (j & 1)), (j >> 1) & 1, 200000000LL);
+          }
+        } else {
+          for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
+            tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
+          for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
+            tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
+        }
+        tc::mbar_wait(bar(q_bar), 0, 200000000LL);
       }
     } else if (warp == kMmaWarp) {
       // ======================= MMA issuer =======================
       // tcgen05.commit tracks the MMAs of the thread that issues it: elect.sync on a converged
       // warp picks the same (lowest) lane every time, so MMAs and commits share one thread.
-      constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
-      constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
+      constexpr uint32_t idesc_s = Q8 ? tc::idesc_f16(128, kCtxTileN, 0) : tc::idesc_bf16(128, kCtxTileN, 0);
+      constexpr uint32_t idesc_o = Q8 ? tc::idesc_f16(128, D, 1) : tc::idesc_bf16(128, D, 1);
       auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
       // context: A and B share every K / V tile (the last one to use it frees it); generation:
       // each tile has one user
@@ -394,6 +451,99 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         tc::mbar_wait(bar(BAR_MMADONE), 0, 200000000LL);  // nothing of ours still runs on TMEM
       }
       __syncwarp();
+    } else if (Q8 && warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
+      // ======================= code -> f16 converters (8-bit pool) =======================
+      // Thread ct owns tile rows ct and ct + 64.  Raw rows are 128 codes in the 128-byte swizzle
+      // TMA wrote (16-byte chunk j at j ^ (row % 8)); each chunk becomes two f16 chunks of the
+      // K-major 128-byte-swizzled layout the MMAs read, in 64-wide head-dim halves.
+      const int ct = (warp - kConvWarp0) * 32 + lane;
+      auto cvt_rows = [&](uint32_t raw_off, uint32_t dst_s) {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = ct + 64 * rr;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 w = *reinterpret_cast<const uint4*>(base + raw_off + r * 128 + ((j ^ (r & 7)) << 4));
+            uint32_t f[8];
+            if constexpr (KV == PKV_INT8) {
+              i8x4_to_f16x2(w.x, f[0], f[1]);
+              i8x4_to_f16x2(w.y, f[2], f[3]);
+              i8x4_to_f16x2(w.z, f[4], f[5]);
+              i8x4_to_f16x2(w.w, f[6], f[7]);
+            } else {
+              e4m3x4_to_f16x2(w.x, f[0], f[1]);
+              e4m3x4_to_f16x2(w.y, f[2], f[3]);
+              e4m3x4_to_f16x2(w.z, f[4], f[5]);
+              e4m3x4_to_f16x2(w.w, f[6], f[7]);
+            }
+            const uint32_t drow = dst_s + (j >> 2) * L::kHalf + r * 128;
+            const uint32_t c0 = static_cast<uint32_t>(2 * (j & 3));
+            st_shared_v4(drow + ((c0 ^ static_cast<uint32_t>(r & 7)) << 4), f[0], f[1], f[2], f[3]);
+            st_shared_v4(drow + (((c0 + 1) ^ static_cast<uint32_t>(r & 7)) << 4), f[4], f[5], f[6], f[7]);
+          }
+        }
+      };
+      bool cok = warp_wait(bar(BAR_QRAW), 0);
+      if (cok) {
+        // Q rows: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
+        // below f16's 65504), in place; the softmax multiplies its scores by 2^(e - 14)
+        float* qscale = reinterpret_cast<float*>(base + L::kQScaleOff);
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = ct + 64 * rr;
+          float amax = 0.f;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 w =
+                *reinterpret_cast<const uint4*>(base + L::kQOff + (c >> 3) * L::kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
+          }
+          int ex = 0;
+          if (amax > 0.f) frexpf(amax, &ex);
+          const float up = ldexpf(1.f, 14 - ex);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+            const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
+            st_shared_v4(a, h[0], h[1], h[2], h[3]);
+          }
+          qscale[r] = 1.f / up;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
+      }
+      for (int g = 0; cok && g < nT; ++g) {
+        const int st = g & 1, ph = (g >> 1) & 1, ph_prev = ((g - 2) >> 1) & 1;
+        if (!warp_wait(bar(BAR_RAWK + st), ph) || (g >= 2 && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) {
+          cok = false;
+          break;
+        }
+        cvt_rows(L::kRawKOff + st * L::kRawTile, sK(st));
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(BAR_KFULL + st));
+        if (!warp_wait(bar(BAR_RAWV + st), ph) || (g >= 2 && !warp_wait(bar(BAR_VEMPTY + st), ph_prev))) {
+          cok = false;
+          break;
+        }
+        cvt_rows(L::kRawVOff + st * L::kRawTile, sV(st));
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(bar(BAR_VFULL + st));
+          tc::mbar_arrive(bar(BAR_RAWEMPTY + st));
+        }
+      }
+      if (!cok && lane == 0) fail();
     }
   } else {
     // ======================= softmax warpgroups =======================
@@ -423,10 +573,14 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         }
       }
     }
-    const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
+    float sl2 = p.scale_log2;
     bool ok = true;
-    for (int j = 0; j < nk; ++j) {
+    if constexpr (Q8) {  // Q row was scaled by 2^(14 - e) when it became f16
+      ok = warp_wait(bar(BAR_Q), 0);
+      if (ok) sl2 *= reinterpret_cast<const float*>(base + L::kQScaleOff)[row];
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; ok && j < nk; ++j) {
       if (!warp_wait(bar(BAR_SFULL + x), j & 1)) { ok = false; break; }
       tc::fence_after_sync();
       uint32_t v0[32], v1[32], v2[32], v3[32];
@@ -510,7 +664,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
           const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
           ls[c] = fadd2(ls[c], pv);
-          pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
+          pk[e >> 1] = Q8 ? pack_f16x2(pv.x, pv.y) : pack_bf16x2(pv.x, pv.y);
         }
         tc::tmem_st16(tS + 16 * c, pk);
       };
@@ -730,14 +884,15 @@ cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s) {
   return launch_pdl(stage_q8_kernel<false>, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
 }
 
-template <int D, bool DEC>
+template <int D, bool DEC, int KV>
 cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& om,
                              cudaStream_t s) {
-  auto kern = context_attn_kernel<D, DEC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CtxSmem<D, DEC>::kBytes);
+  auto kern = context_attn_kernel<D, DEC, KV>;
+  constexpr int bytes = CtxSmem<D, DEC, KV>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const dim3 grid = DEC ? dim3(p.num_titems, p.Hkv) : dim3(p.Hq, p.num_tiles);
-  return launch_pdl(kern, grid, dim3(kThreads), CtxSmem<D, DEC>::kBytes, s, p, qm, km, om);
+  return launch_pdl(kern, grid, dim3(kThreads), bytes, s, p, qm, km, om);
 }
 
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map, bool dec,
@@ -745,8 +900,14 @@ cudaError_t launch_context(const ContextParams& p, const void* q_map, const void
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
   const CUtensorMap& om = *static_cast<const CUtensorMap*>(out_map);
-  if (p.D == 128) return dec ? launch_context_t<128, true>(p, qm, km, om, s) : launch_context_t<128, false>(p, qm, km, om, s);
-  return dec ? launch_context_t<64, true>(p, qm, km, om, s) : launch_context_t<64, false>(p, qm, km, om, s);
+  if (dec && p.kv_dtype != PKV_BF16) {  // 8-bit codes, converted in shared memory (head_dim 128)
+    if (p.D != 128) return cudaErrorInvalidValue;
+    return p.kv_dtype == PKV_INT8 ? launch_context_t<128, true, PKV_INT8>(p, qm, km, om, s)
+                                  : launch_context_t<128, true, PKV_FP8_E4M3>(p, qm, km, om, s);
+  }
+  if (p.D == 128)
+    return dec ? launch_context_t<128, true, 0>(p, qm, km, om, s) : launch_context_t<128, false, 0>(p, qm, km, om, s);
+  return dec ? launch_context_t<64, true, 0>(p, qm, km, om, s) : launch_context_t<64, false, 0>(p, qm, km, om, s);
 }
 
 }  // namespace pkv

@@ -129,6 +129,8 @@ struct ContextParams {
   // generation mode (wide generation requests on the tensor-core kernel): CTA = titem_map
   // entry (generation request, split x row group) x KV head
   int32_t G, gen_row0, kv_chunk, num_titems, mask_words;
+  int32_t kv_dtype;         // generation mode: pool element kind (pkv_dtype); 8-bit codes are
+                            // converted to f16 in shared memory (head_dim 128 only)
   int64_t total_parts;
   const int2* titem_map;
   const int32_t* split_prefix;

@@ -59,6 +59,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 // Tiled store shared -> global (bulk async group of the issuing thread).  The x coordinate
 // (c0) must keep the 16-byte rule; no coordinate may be negative.
 __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1, int c2, int c3) {
@@ -134,6 +141,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
          | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// The same with f16 A and B (both operands f16: kind::f16 takes one element type for A and B).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn_major) {
+  return idesc_bf16(M, N, b_mn_major) & ~((1u << 7) | (1u << 10));
 }
 
 // ---- MMA ---------------------------------------------------------------------------------------
