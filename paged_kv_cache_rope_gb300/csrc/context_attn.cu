@@ -103,12 +103,12 @@ enum {
   BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
   BAR_RAWK = 21,   // +2: 8-bit generation mode, raw K codes landed (TMA)
   BAR_RAWV = 23,   // +2: raw V codes landed
-  BAR_RAWEMPTY = 25, // +2: converters done reading a raw stage
-  BAR_QRAW = 27,   // the bf16 Q tile landed (the converters turn it into scaled f16)
-  NUM_BARS = 28
+  BAR_RAWKEMPTY = 25, // +2: the K converter is done reading a raw K stage
+  BAR_RAWVEMPTY = 27, // +2: the V converter is done reading a raw V stage
+  BAR_QRAW = 29,   // the bf16 Q tile landed (the converters turn it into scaled f16)
+  NUM_BARS = 30
 };
-constexpr int kConvWarp0 = 10;  // 8-bit generation mode: warps 10 and 11 convert codes to f16
-constexpr int kConvWarps = 2;
+
 
 template <int D, bool DEC, int KV>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -136,8 +136,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   // ---- set-up: barriers, TMEM (reads nothing earlier kernels write, so it runs before the
   // grid-dependency wait and overlaps the previous kernel's tail) ----
   if (threadIdx.x == 0) {
-    // Q / K / V ready: the producer's transaction arrive, or (8-bit) one arrive per converter warp
-    const uint32_t ready_count = Q8 ? kConvWarps : 1;
+    // Q / K / V ready: the producer's transaction arrive, or (8-bit) one arrive per warp of the
+    // softmax warpgroup that converted them
+    const uint32_t ready_count = Q8 ? 4 : 1;
     tc::mbar_init(bar(BAR_Q), ready_count);
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar(BAR_KFULL + s), ready_count);
@@ -149,7 +150,8 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       for (int s = 0; s < 2; ++s) {
         tc::mbar_init(bar(BAR_RAWK + s), 1);
         tc::mbar_init(bar(BAR_RAWV + s), 1);
-        tc::mbar_init(bar(BAR_RAWEMPTY + s), kConvWarps);
+        tc::mbar_init(bar(BAR_RAWKEMPTY + s), 4);
+        tc::mbar_init(bar(BAR_RAWVEMPTY + s), 4);
       }
       tc::mbar_init(bar(BAR_QRAW), 1);
     }
@@ -303,23 +305,25 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         const uint32_t bytes =
             static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
         if constexpr (Q8) {
-          // raw codes of page `lane` into the raw ring; the converters free a stage after
-          // reading both its K and V
+          // raw codes of page `lane` into the raw rings; K and V stages are freed separately (a
+          // V stage waits for the PV two tiles back, a K stage only for the converter)
           const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
-          if (j >= 2 && !warp_wait(bar(BAR_RAWEMPTY + (j & 1)), ((j - 2) >> 1) & 1)) { pok = false; break; }
-          if (lane == 0) {
-            tc::mbar_arrive_expect_tx(bar(BAR_RAWK + (j & 1)), bytes);
-            tc::mbar_arrive_expect_tx(bar(BAR_RAWV + (j & 1)), bytes);
-          }
+          const int rs = j & 1, rph = ((j - 2) >> 1) & 1;
+          if (j >= 2 && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) { pok = false; break; }
+          if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWK + rs), bytes);
           __syncwarp();
-          if (pg >= 0) {
-            tc::tma_load_3d(base_s + L::kRawKOff + (j & 1) * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + (j & 1)), 0,
-                            hk, (pg * 2 + 0) * p.B);
-            tc::tma_load_3d(base_s + L::kRawVOff + (j & 1) * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + (j & 1)), 0,
-                            hk, (pg * 2 + 1) * p.B);
-          }
+          if (pg >= 0)
+            tc::tma_load_3d(base_s + L::kRawKOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + rs), 0, hk,
+                            (pg * 2 + 0) * p.B);
           __syncwarp();
           ++issued_k;
+          if (j >= 2 && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) { pok = false; break; }
+          if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWV + rs), bytes);
+          __syncwarp();
+          if (pg >= 0)
+            tc::tma_load_3d(base_s + L::kRawVOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + rs), 0, hk,
+                            (pg * 2 + 1) * p.B);
+          __syncwarp();
           ++issued_v;
           continue;
         }
@@ -347,10 +351,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       __syncwarp();
       if (warp_abort()) {  // let copies already in flight land before the CTA winds down
         if constexpr (Q8) {
-          for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j) {
+          for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
             tc::mbar_wait(bar(BAR_RAWK + (j & 1)), (j >> 1) & 1, 200000000LL);
+          for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
             tc::mbar_wait(bar(BAR_RAWV + (j & 1)), (j >> 1) & 1, 200000000LL);
-          }
         } else {
           for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
             tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
@@ -451,99 +455,6 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         tc::mbar_wait(bar(BAR_MMADONE), 0, 200000000LL);  // nothing of ours still runs on TMEM
       }
       __syncwarp();
-    } else if (Q8 && warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
-      // ======================= code -> f16 converters (8-bit pool) =======================
-      // Thread ct owns tile rows ct and ct + 64.  Raw rows are 128 codes in the 128-byte swizzle
-      // TMA wrote (16-byte chunk j at j ^ (row % 8)); each chunk becomes two f16 chunks of the
-      // K-major 128-byte-swizzled layout the MMAs read, in 64-wide head-dim halves.
-      const int ct = (warp - kConvWarp0) * 32 + lane;
-      auto cvt_rows = [&](uint32_t raw_off, uint32_t dst_s) {
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int r = ct + 64 * rr;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 w = *reinterpret_cast<const uint4*>(base + raw_off + r * 128 + ((j ^ (r & 7)) << 4));
-            uint32_t f[8];
-            if constexpr (KV == PKV_INT8) {
-              i8x4_to_f16x2(w.x, f[0], f[1]);
-              i8x4_to_f16x2(w.y, f[2], f[3]);
-              i8x4_to_f16x2(w.z, f[4], f[5]);
-              i8x4_to_f16x2(w.w, f[6], f[7]);
-            } else {
-              e4m3x4_to_f16x2(w.x, f[0], f[1]);
-              e4m3x4_to_f16x2(w.y, f[2], f[3]);
-              e4m3x4_to_f16x2(w.z, f[4], f[5]);
-              e4m3x4_to_f16x2(w.w, f[6], f[7]);
-            }
-            const uint32_t drow = dst_s + (j >> 2) * L::kHalf + r * 128;
-            const uint32_t c0 = static_cast<uint32_t>(2 * (j & 3));
-            st_shared_v4(drow + ((c0 ^ static_cast<uint32_t>(r & 7)) << 4), f[0], f[1], f[2], f[3]);
-            st_shared_v4(drow + (((c0 + 1) ^ static_cast<uint32_t>(r & 7)) << 4), f[4], f[5], f[6], f[7]);
-          }
-        }
-      };
-      bool cok = warp_wait(bar(BAR_QRAW), 0);
-      if (cok) {
-        // Q rows: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
-        // below f16's 65504), in place; the softmax multiplies its scores by 2^(e - 14)
-        float* qscale = reinterpret_cast<float*>(base + L::kQScaleOff);
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int r = ct + 64 * rr;
-          float amax = 0.f;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint4 w =
-                *reinterpret_cast<const uint4*>(base + L::kQOff + (c >> 3) * L::kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
-          }
-          int ex = 0;
-          if (amax > 0.f) frexpf(amax, &ex);
-          const float up = ldexpf(1.f, 14 - ex);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-            const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
-            st_shared_v4(a, h[0], h[1], h[2], h[3]);
-          }
-          qscale[r] = 1.f / up;
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
-      }
-      for (int g = 0; cok && g < nT; ++g) {
-        const int st = g & 1, ph = (g >> 1) & 1, ph_prev = ((g - 2) >> 1) & 1;
-        if (!warp_wait(bar(BAR_RAWK + st), ph) || (g >= 2 && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) {
-          cok = false;
-          break;
-        }
-        cvt_rows(L::kRawKOff + st * L::kRawTile, sK(st));
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(BAR_KFULL + st));
-        if (!warp_wait(bar(BAR_RAWV + st), ph) || (g >= 2 && !warp_wait(bar(BAR_VEMPTY + st), ph_prev))) {
-          cok = false;
-          break;
-        }
-        cvt_rows(L::kRawVOff + st * L::kRawTile, sV(st));
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(bar(BAR_VFULL + st));
-          tc::mbar_arrive(bar(BAR_RAWEMPTY + st));
-        }
-      }
-      if (!cok && lane == 0) fail();
     }
   } else {
     // ======================= softmax warpgroups =======================
@@ -575,9 +486,99 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     }
     float sl2 = p.scale_log2;
     bool ok = true;
-    if constexpr (Q8) {  // Q row was scaled by 2^(14 - e) when it became f16
-      ok = warp_wait(bar(BAR_Q), 0);
-      if (ok) sl2 *= reinterpret_cast<const float*>(base + L::kQScaleOff)[row];
+    // ---- 8-bit pool: this warpgroup turns the raw codes of its own tiles into f16 ----
+    // Thread `row` converts tile row `row`: 128 codes in the 128-byte swizzle TMA wrote (16-byte
+    // chunk j at j ^ (row % 8)) become 16 f16 chunks of the K-major 128-byte-swizzled layout the
+    // MMAs read, in 64-wide head-dim halves.  E4M3 codes become f16 by bit placement (sign to bit
+    // 15, exponent and mantissa to bits 7..13): exactly code x 2^-8 for every finite code,
+    // subnormals included, with the 2^8 folded into the score and output scales.  INT8 codes
+    // become exact f16 integers.  A warpgroup converts its next tile right after handing over
+    // its P, while its own PV and the other warpgroup's MMAs run.
+    auto cvt_row = [&](uint32_t raw_off, uint32_t dst_s) {
+#pragma unroll
+      for (int jc = 0; jc < 8; ++jc) {
+        const uint4 w = *reinterpret_cast<const uint4*>(base + raw_off + row * 128 + ((jc ^ (row & 7)) << 4));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        uint32_t f[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if constexpr (KV == PKV_INT8) {
+            i8x4_to_f16x2(wv[k], f[2 * k], f[2 * k + 1]);
+          } else {
+            const uint32_t x0 = __byte_perm(wv[k], 0u, 0x1404), x1 = __byte_perm(wv[k], 0u, 0x3424);  // codes << 8
+            f[2 * k] = (x0 & 0x80008000u) | ((x0 >> 1) & 0x3F803F80u);
+            f[2 * k + 1] = (x1 & 0x80008000u) | ((x1 >> 1) & 0x3F803F80u);
+          }
+        }
+        const uint32_t drow = dst_s + (jc >> 2) * L::kHalf + row * 128;
+        const uint32_t c0 = static_cast<uint32_t>(2 * (jc & 3));
+        st_shared_v4(drow + ((c0 ^ static_cast<uint32_t>(row & 7)) << 4), f[0], f[1], f[2], f[3]);
+        st_shared_v4(drow + (((c0 + 1) ^ static_cast<uint32_t>(row & 7)) << 4), f[4], f[5], f[6], f[7]);
+      }
+    };
+    // tile g of the stream (this warpgroup's parity): K into f16 stage g % 2 once the stage's
+    // previous S is done, then V once its previous PV is done; each step frees a raw stage
+    auto convert_tile = [&](int g) {
+      const int st = g & 1, ph = (g >> 1) & 1, ph_prev = ((g - 2) >> 1) & 1;
+      if (!warp_wait(bar(BAR_RAWK + st), ph) || (g >= 2 && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) return false;
+      cvt_row(L::kRawKOff + st * L::kRawTile, sK(st));
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(bar(BAR_KFULL + st));
+        tc::mbar_arrive(bar(BAR_RAWKEMPTY + st));
+      }
+      if (!warp_wait(bar(BAR_RAWV + st), ph) || (g >= 2 && !warp_wait(bar(BAR_VEMPTY + st), ph_prev))) return false;
+      cvt_row(L::kRawVOff + st * L::kRawTile, sV(st));
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(bar(BAR_VFULL + st));
+        tc::mbar_arrive(bar(BAR_RAWVEMPTY + st));
+      }
+      return true;
+    };
+    if constexpr (Q8) {
+      float* qscale = reinterpret_cast<float*>(base + L::kQScaleOff);
+      if (x == 0) {
+        // Q row `row`: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
+        // below f16's 65504), in place; the scores take 2^(e - 14) back
+        ok = warp_wait(bar(BAR_QRAW), 0);
+        if (ok) {
+          float amax = 0.f;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (c >> 3) * L::kHalf + row * 128 +
+                                                            (((c & 7) ^ (row & 7)) << 4));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
+          }
+          int ex = 0;
+          if (amax > 0.f) frexpf(amax, &ex);
+          const float up = ldexpf(1.f, 14 - ex);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+            const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
+            st_shared_v4(a, h[0], h[1], h[2], h[3]);
+          }
+          qscale[row] = 1.f / up;
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
+        }
+      }
+      if (ok && nk > 0) ok = convert_tile(x);  // this warpgroup's first tile
+      if (ok) ok = warp_wait(bar(BAR_Q), 0);
+      if (ok) sl2 *= qscale[row];
+      if (KV == PKV_FP8_E4M3) sl2 *= 256.f;  // K entered as code x 2^-8
     }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; ok && j < nk; ++j) {
@@ -693,6 +694,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(bar(BAR_PFULL + x));
+      if constexpr (Q8) {  // the warpgroup's next tile, while its PV and the other tile's MMAs run
+        if (j + 1 < nk && !convert_tile(gtile(j + 1, x))) { ok = false; break; }
+      }
     }
     if (!ok) fail();
     // ---- epilogue: O / l -> bf16 rows ----
@@ -770,8 +774,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
               const bool store = row < nvx;
               const int64_t head = static_cast<int64_t>(hk) * p.group + hl;
               const bool whole = num_splits == 1;  // else a partial result for the combine
-              const float sA = whole ? fA * p.out_scale / l : fA * p.out_scale;
-              const float sB = whole ? fB * p.out_scale / l : fB * p.out_scale;
+              // E4M3 V entered the MMA as code x 2^-8
+              const float osc = p.out_scale * ((Q8 && KV == PKV_FP8_E4M3) ? 256.f : 1.f);
+              const float sA = whole ? fA * osc / l : fA * osc;
+              const float sB = whole ? fB * osc / l : fB * osc;
               uint16_t* orow = p.out + static_cast<int64_t>(tok0 + tok_i) * p.out_stride + head * D;
               const int64_t pi =
                   (static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new + tok_i) * p.Hq +
