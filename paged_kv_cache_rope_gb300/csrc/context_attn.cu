@@ -489,11 +489,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     // ---- 8-bit pool: this warpgroup turns the raw codes of its own tiles into f16 ----
     // Thread `row` converts tile row `row`: 128 codes in the 128-byte swizzle TMA wrote (16-byte
     // chunk j at j ^ (row % 8)) become 16 f16 chunks of the K-major 128-byte-swizzled layout the
-    // MMAs read, in 64-wide head-dim halves.  E4M3 codes become f16 by bit placement (sign to bit
-    // 15, exponent and mantissa to bits 7..13): exactly code x 2^-8 for every finite code,
-    // subnormals included, with the 2^8 folded into the score and output scales.  INT8 codes
-    // become exact f16 integers.  A warpgroup converts its next tile right after handing over
-    // its P, while its own PV and the other warpgroup's MMAs run.
+    // MMAs read, in 64-wide head-dim halves.  Both code kinds are exact in f16: E4M3 through the
+    // hardware conversion (measured 4% faster here than placing the bits with integer ops),
+    // INT8 as integers.  A warpgroup converts its next tile right after handing over its P,
+    // while its own PV and the other warpgroup's MMAs run.
     auto cvt_row = [&](uint32_t raw_off, uint32_t dst_s) {
 #pragma unroll
       for (int jc = 0; jc < 8; ++jc) {
@@ -505,9 +504,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           if constexpr (KV == PKV_INT8) {
             i8x4_to_f16x2(wv[k], f[2 * k], f[2 * k + 1]);
           } else {
-            const uint32_t x0 = __byte_perm(wv[k], 0u, 0x1404), x1 = __byte_perm(wv[k], 0u, 0x3424);  // codes << 8
-            f[2 * k] = (x0 & 0x80008000u) | ((x0 >> 1) & 0x3F803F80u);
-            f[2 * k + 1] = (x1 & 0x80008000u) | ((x1 >> 1) & 0x3F803F80u);
+            e4m3x4_to_f16x2(wv[k], f[2 * k], f[2 * k + 1]);
           }
         }
         const uint32_t drow = dst_s + (jc >> 2) * L::kHalf + row * 128;
@@ -578,7 +575,6 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       if (ok && nk > 0) ok = convert_tile(x);  // this warpgroup's first tile
       if (ok) ok = warp_wait(bar(BAR_Q), 0);
       if (ok) sl2 *= qscale[row];
-      if (KV == PKV_FP8_E4M3) sl2 *= 256.f;  // K entered as code x 2^-8
     }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; ok && j < nk; ++j) {
@@ -774,8 +770,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
               const bool store = row < nvx;
               const int64_t head = static_cast<int64_t>(hk) * p.group + hl;
               const bool whole = num_splits == 1;  // else a partial result for the combine
-              // E4M3 V entered the MMA as code x 2^-8
-              const float osc = p.out_scale * ((Q8 && KV == PKV_FP8_E4M3) ? 256.f : 1.f);
+              const float osc = p.out_scale;
               const float sA = whole ? fA * osc / l : fA * osc;
               const float sB = whole ? fB * osc / l : fB * osc;
               uint16_t* orow = p.out + static_cast<int64_t>(tok0 + tok_i) * p.out_stride + head * D;
