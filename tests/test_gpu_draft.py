@@ -1,9 +1,11 @@
 """Generation requests of several draft tokens (page adg.csdn.net/69730cc6, section 1.4: generation
 lengths, position offsets, packed mask; the Medusa candidate tree on page "TensorRT-LLM 源码完全
 拆解(一)") through the C-ABI against the fp64 oracle: draft tokens rotated for past + offset and
-stored at past + i (bit-exact pool and q_out), attention under chain (causal) or tree masks on
-the split-KV decode kernel, whose score-tile columns are (token, query head) pairs of one KV
-head -- several column groups per split when they do not fit one CTA."""
+stored at past + i (bit-exact pool and q_out), attention under chain (causal) or tree masks.
+Narrow requests run on the split-KV decode kernel, whose score-tile columns are (token, query
+head) pairs of one KV head; wider ones on the tcgen05 kernel's generation mode (rows = those
+pairs; 8-bit pools at head_dim 128 have their codes converted to f16 in shared memory) or, for
+groups that do not divide 128 and 8-bit pools at head_dim 64, on the wide mma.sync kernel."""
 import dataclasses
 
 import numpy as np
@@ -28,7 +30,7 @@ CASES = [
     # tensor-core generation mode: one head per row (g = 1), several 128-row groups per request
     ("tree_mha_d64_64tok", [], [(64, 300), (20, 5000), 70], 4, 4, 64, 16, True),
     ("tree_gqa8_row_groups", [], [(20, 700), (64, 2000), (16, 4100)], 16, 2, 128, 32, True),
-    # a group that does not divide 128 keeps the mma.sync wide kernel even on a bf16 pool
+    # a group that does not divide 128 keeps the mma.sync wide kernel on every pool
     ("tree_gqa6_mma_wide", [], [(5, 300), (9, 1000), 77], 12, 2, 128, 32, True),
 ]
 
