@@ -241,7 +241,10 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  *   d_error      device int32 error bits as above
  * Context rows use a tcgen05/TMEM tensor-core kernel (for 8-bit pools after staging the context
  * requests' pages as exact bf16 code values in the workspace), generation rows a split-KV decode
- * kernel plus a log-sum-exp combine.  When the batch has both kinds of rows, the generation
+ * kernel plus a log-sum-exp combine.  Generation requests with more (token, query head) pairs
+ * than the decode kernel's narrow columns run on the tensor-core kernel's generation mode when
+ * the query group divides 128 and the pool is bf16, or 8-bit at head_dim 128 (codes converted
+ * to f16 in shared memory); otherwise on a wide split-KV decode kernel.  When the batch has both kinds of rows, the generation
  * kernels run on the library's auxiliary stream for this device (highest stream priority),
  * forked from `stream` by an event after the planning kernel and joined back into it before
  * the call returns, so that they share the GPU with the context kernel; every other launch goes
