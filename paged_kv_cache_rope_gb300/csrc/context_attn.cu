@@ -36,8 +36,11 @@
 // 8-bit pools (E4M3 or int8 codes): stage_q8_kernel first copies the context requests' pages
 // into a bf16 staging pool (exact code values) with its own block table; this kernel then runs
 // unchanged on it, with the pool scale folded into the score scale and into the output scale.
-// Generation mode (DEC, bf16 pools, generation requests with more (token, query head) pairs
-// than the mma.sync decode kernel's columns): a 128-row tile is 128/g draft tokens x the g query
+// Generation mode (DEC: generation requests with more (token, query head) pairs than the
+// mma.sync decode kernel's columns; bf16 pools, or 8-bit pools at head_dim 128 whose codes TMA
+// lands raw and the softmax warpgroup that will read a tile converts to f16 in shared memory,
+// with Q made f16 under a power-of-two scale per row and every MMA kind::f16): a 128-row tile
+// is 128/g draft tokens x the g query
 // heads of one KV head (the Q box spans g heads), so each K / V tile serves the whole group;
 // the two softmax warpgroups take the even and the odd KV tiles of one split of kv_chunk keys
 // against the same Q tile; at the end B hands its (max, sum) over through shared memory, A
