@@ -121,6 +121,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   // 8-bit pool in the generation mode: the producer lands raw codes, warps 10-11 convert them
   // (and Q, scaled per row) to f16, and every MMA runs kind::f16 on f16 operands
   constexpr bool Q8 = L::kQ8;
+  // E4M3 pools: scores on kind::f8f6f4 straight from the raw K codes, with Q split into hi + lo
+  // E4M3 codes (about 8 significant bits together); only V is converted to f16
+  constexpr bool F8S = KV == PKV_FP8_E4M3;
   constexpr int S = L::kStages;
   // ring stage and phase of the g-th K / V tile of the stream
   auto stg = [](int g) { return g % S; };
@@ -153,7 +156,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       for (int s = 0; s < 2; ++s) {
         tc::mbar_init(bar(BAR_RAWK + s), 1);
         tc::mbar_init(bar(BAR_RAWV + s), 1);
-        tc::mbar_init(bar(BAR_RAWKEMPTY + s), 4);
+        tc::mbar_init(bar(BAR_RAWKEMPTY + s), F8S ? 1 : 4);
         tc::mbar_init(bar(BAR_RAWVEMPTY + s), 4);
       }
       tc::mbar_init(bar(BAR_QRAW), 1);
@@ -379,6 +382,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       auto frees = [&](int j, int x) { return DEC || x == last_user(j); };
       auto kfull = [&](int j, int x) {
         const int g = gtile(j, x);
+        if constexpr (F8S) return warp_wait(bar(BAR_RAWK + (g & 1)), (g >> 1) & 1);  // raw codes landed
         return warp_wait(bar(BAR_KFULL + stg(g)), phs(g));
       };
       // Descriptors are built once per operand tile and advanced by adding the byte offset / 16
@@ -394,6 +398,25 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         const int st = stg(gtile(j, x));
         const uint64_t a0 = (DEC || x == 0) ? dq0 : dq1;
         const uint64_t b0 = dk0 + stage_off(st);
+        if constexpr (F8S) {
+          // Q hi and lo tiles (one 128-byte row of codes per Q row) sit in the f16 K stage 0
+          // area; K is the raw tile: four K=32 steps of 32 bytes, hi then lo
+          const int g = gtile(j, x);
+          const uint64_t aq = tc::sdesc_sw128(sK(0), 16, 1024);
+          const uint64_t bk = tc::sdesc_sw128(base_s + L::kRawKOff + (g & 1) * L::kRawTile, 16, 1024);
+          constexpr uint64_t kLo = 128 * 128 / 16;  // lo tile: 16 KB after hi
+          if (tc::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_e4m3_ss(tmem + 128 * x, aq + 2 * kk, bk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3_ss(tmem + 128 * x, aq + kLo + 2 * kk, bk + 2 * kk, idesc_s, 1u);
+            tc::mma_commit(bar(BAR_SFULL + x));
+            tc::mma_commit(bar(BAR_RAWKEMPTY + (g & 1)));  // the raw K stage may be refilled
+          }
+          __syncwarp();
+          return;
+        }
         if (tc::elect_one()) {
           if constexpr (D == 128) {
             // steps kk: ((kk / 4) * 16 KB + (kk % 4) * 32 B) / 16
@@ -520,13 +543,15 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     // previous S is done, then V once its previous PV is done; each step frees a raw stage
     auto convert_tile = [&](int g) {
       const int st = g & 1, ph = (g >> 1) & 1, ph_prev = ((g - 2) >> 1) & 1;
-      if (!warp_wait(bar(BAR_RAWK + st), ph) || (g >= 2 && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) return false;
-      cvt_row(L::kRawKOff + st * L::kRawTile, sK(st));
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(bar(BAR_KFULL + st));
-        tc::mbar_arrive(bar(BAR_RAWKEMPTY + st));
+      if constexpr (!F8S) {  // E4M3 scores read the raw K codes themselves
+        if (!warp_wait(bar(BAR_RAWK + st), ph) || (g >= 2 && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) return false;
+        cvt_row(L::kRawKOff + st * L::kRawTile, sK(st));
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(bar(BAR_KFULL + st));
+          tc::mbar_arrive(bar(BAR_RAWKEMPTY + st));
+        }
       }
       if (!warp_wait(bar(BAR_RAWV + st), ph) || (g >= 2 && !warp_wait(bar(BAR_VEMPTY + st), ph_prev))) return false;
       cvt_row(L::kRawVOff + st * L::kRawTile, sV(st));
@@ -557,17 +582,46 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
           }
           int ex = 0;
           if (amax > 0.f) frexpf(amax, &ex);
-          const float up = ldexpf(1.f, 14 - ex);
+          // f16: |q| * up in [2^13, 2^14); E4M3 hi + lo: |q| * up in [128, 256), under 448
+          const float up = ldexpf(1.f, (F8S ? 8 : 14) - ex);
+          if constexpr (F8S) {
+            // code chunk jc (16 codes = q elements 16 jc ..) from bf16 chunks 2 (jc % 4) and
+            // 2 (jc % 4) + 1 of head-dim half jc / 4; hi tile at sK(0), lo tile 16 KB after it
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-            const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[4];
+            for (int jc = 0; jc < 8; ++jc) {
+              uint32_t hw[4], lw[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
-            st_shared_v4(a, h[0], h[1], h[2], h[3]);
+              for (int hc = 0; hc < 2; ++hc) {
+                const int c = 2 * (jc & 3) + hc;
+                const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (jc >> 2) * L::kHalf + row * 128 +
+                                                                ((c ^ (row & 7)) << 4));
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int k = 0; k < 4; k += 2) {
+                  uint32_t h0, l0, h1, l1;
+                  split_e4m3x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up, h0, l0);
+                  split_e4m3x2(__uint_as_float(u[k + 1] << 16) * up, __uint_as_float(u[k + 1] & 0xFFFF0000u) * up, h1,
+                               l1);
+                  hw[2 * hc + (k >> 1)] = (h0 & 0xFFFFu) | (h1 << 16);
+                  lw[2 * hc + (k >> 1)] = (l0 & 0xFFFFu) | (l1 << 16);
+                }
+              }
+              const uint32_t off = static_cast<uint32_t>(row * 128 + ((jc ^ (row & 7)) << 4));
+              st_shared_v4(sK(0) + off, hw[0], hw[1], hw[2], hw[3]);
+              st_shared_v4(sK(0) + 128 * 128 + off, lw[0], lw[1], lw[2], lw[3]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+              const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
+              const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+              uint32_t h[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
+              st_shared_v4(a, h[0], h[1], h[2], h[3]);
+            }
           }
           qscale[row] = 1.f / up;
           tc::fence_proxy_async_smem();
