@@ -38,9 +38,11 @@
 // unchanged on it, with the pool scale folded into the score scale and into the output scale.
 // Generation mode (DEC: generation requests with more (token, query head) pairs than the
 // mma.sync decode kernel's columns; bf16 pools, or 8-bit pools at head_dim 128 whose codes TMA
-// lands raw and the softmax warpgroup that will read a tile converts to f16 in shared memory,
-// with Q made f16 under a power-of-two scale per row and every MMA kind::f16): a 128-row tile
-// is 128/g draft tokens x the g query
+// lands raw: E4M3 scores run on kind::f8f6f4 from the raw K codes against Q split into hi + lo
+// E4M3 tiles, INT8 K is converted to f16 with Q made f16, and V is converted to f16 for a
+// kind::f16 PV -- each conversion by the softmax warpgroup that will read the tile; Q takes a
+// power-of-two scale per row that the scores give back): a 128-row tile is 128/g draft tokens
+// x the g query
 // heads of one KV head (the Q box spans g heads), so each K / V tile serves the whole group;
 // the two softmax warpgroups take the even and the odd KV tiles of one split of kv_chunk keys
 // against the same Q tile; at the end B hands its (max, sum) over through shared memory, A
