@@ -73,8 +73,9 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could
 
 // Context: Q_A, Q_B, K[2], V[2].  Generation: one Q tile (A and B share it), K[3], V[3] -- a
 // deeper ring, since each K / V tile has one consumer and the two halves alternate.
-// Generation with an 8-bit pool (KV != 0): Q, K[2], V[2] as f16, plus a ring of the raw codes
-// (K[2], V[2]) that TMA fills and the converter warps turn into f16, and the per-row Q scales.
+// Generation with an 8-bit pool (KV != 0): Q, K[2], V[2] (f16; for E4M3 the K[0] area holds the
+// hi and lo E4M3 Q tiles instead), a ring of the raw codes (K[2], V[2]) that TMA fills and the
+// softmax warpgroups convert, and the per-row Q scales.
 template <int D, bool DEC, int KV = 0>
 struct CtxSmem {
   static constexpr bool kQ8 = KV != 0;
@@ -89,7 +90,7 @@ struct CtxSmem {
   static constexpr int kRawVOff = kRawKOff + (kQ8 ? 2 : 0) * kRawTile;
   static constexpr int kBarOff = kRawVOff + (kQ8 ? 2 : 0) * kRawTile;
   static constexpr int kBarBytes = 256;
-  static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 2^(e_row - 14) of Q row
+  static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 1 / (Q row's power-of-two scale)
   static constexpr int kBytes = kQScaleOff + (kQ8 ? 128 * 4 : 0) + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
   static_assert(!kQ8 || (DEC && D == 128), "8-bit codes only in the generation mode at head_dim 128");
@@ -108,9 +109,9 @@ enum {
   BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
   BAR_RAWK = 21,   // +2: 8-bit generation mode, raw K codes landed (TMA)
   BAR_RAWV = 23,   // +2: raw V codes landed
-  BAR_RAWKEMPTY = 25, // +2: the K converter is done reading a raw K stage
-  BAR_RAWVEMPTY = 27, // +2: the V converter is done reading a raw V stage
-  BAR_QRAW = 29,   // the bf16 Q tile landed (the converters turn it into scaled f16)
+  BAR_RAWKEMPTY = 25, // +2: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
+  BAR_RAWVEMPTY = 27, // +2: a raw V stage has been converted
+  BAR_QRAW = 29,   // the bf16 Q tile landed (warpgroup A rescales and re-encodes it)
   NUM_BARS = 30
 };
 
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
   using L = CtxSmem<D, DEC, KV>;
-  // 8-bit pool in the generation mode: the producer lands raw codes, warps 10-11 convert them
-  // (and Q, scaled per row) to f16, and every MMA runs kind::f16 on f16 operands
+  // 8-bit pool in the generation mode: the producer lands raw codes and the softmax warpgroups
+  // convert what the MMAs cannot read as stored (Q, V, and INT8 K)
   constexpr bool Q8 = L::kQ8;
   // E4M3 pools: scores on kind::f8f6f4 straight from the raw K codes, with Q split into hi + lo
   // E4M3 codes (about 8 significant bits together); only V is converted to f16
