@@ -288,7 +288,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
       const int n_pages_seq = (L_r + p.B - 1) / p.B;
       const int n_q = (hasB && !DEC) ? 2 : 1;  // generation: one Q tile shared by A and B
-      const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: the converters make Q f16 first
+      const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: warpgroup A re-encodes Q first
       if (tc::elect_one()) {
         tc::mbar_arrive_expect_tx(bar(q_bar), n_q * 128 * D * 2);
         for (int x = 0; x < n_q; ++x)
@@ -315,7 +315,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
         if constexpr (Q8) {
           // raw codes of page `lane` into the raw rings; K and V stages are freed separately (a
-          // V stage waits for the PV two tiles back, a K stage only for the converter)
+          // V stage waits for the PV two tiles back, a K stage only for its S or conversion)
           const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
           const int rs = j & 1, rph = ((j - 2) >> 1) & 1;
           if (j >= 2 && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) { pok = false; break; }
