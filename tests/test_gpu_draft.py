@@ -30,6 +30,8 @@ CASES = [
     # tensor-core generation mode: one head per row (g = 1), several 128-row groups per request
     ("tree_mha_d64_64tok", [], [(64, 300), (20, 5000), 70], 4, 4, 64, 16, True),
     ("tree_gqa8_row_groups", [], [(20, 700), (64, 2000), (16, 4100)], 16, 2, 128, 32, True),
+    # 16-token pages: eight pages per 128-key tile (one TMA box per producer lane)
+    ("tree_gqa4_d128_b16", [], [(6, 900), (12, 2600), 40], 16, 4, 128, 16, True),
     # a group that does not divide 128 keeps the mma.sync wide kernel on every pool
     ("tree_gqa6_mma_wide", [], [(5, 300), (9, 1000), 77], 12, 2, 128, 32, True),
 ]
