@@ -201,8 +201,8 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   // split's tiles shared out among the warps).  Wider ones (draft tokens, large query groups)
   // take the tensor-core kernel when a 128-row tile holds whole groups and the pool is bf16 or
   // 8-bit at head_dim 128 (rows = pairs, 128 per CTA; splits of whole 128-key tiles), else the
-  // wide mma.sync kernel
-  // (64 columns per CTA, every warp over every tile), in as many column groups as needed.
+  // wide mma.sync kernel (64 columns per CTA, every warp over every tile), in as many column
+  // groups as needed.
   const int group = Hq / pool->num_kv_heads;
   int max_narrow = 0;
   bool any_wide = false;
