@@ -52,18 +52,34 @@ def _fingerprint(verbose_ptxas: bool) -> str:
     return h.hexdigest()
 
 
+# The self-test build: the same sources with the producer of the context kernel issuing no K / V
+# copies and every bounded wait given about a millisecond, so that a test can watch a wait run
+# out and the kernel wind down (error bit set, TMEM freed, the context still usable).  Only the
+# tests build and load it; it is never part of libpaged_kv.so.
+SELFTEST_LIB = os.path.join(PKG, "libpaged_kv_selftest.so")
+SELFTEST_DEFS = ["-DPKV_SELFTEST", "-DPKV_WAIT_BUDGET=2000000LL"]
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "libpaged_kv.stamp")
-    fp = _fingerprint(verbose_ptxas)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == fp:
-        return LIB
+    return _build_lib(LIB, BUILD, [], force, verbose_ptxas)
+
+
+def build_selftest(force: bool = False) -> str:
+    return _build_lib(SELFTEST_LIB, os.path.join(BUILD, "selftest"), SELFTEST_DEFS, force, False)
+
+
+def _build_lib(lib: str, build_dir: str, defs: list[str], force: bool, verbose_ptxas: bool) -> str:
+    os.makedirs(build_dir, exist_ok=True)
+    stamp = os.path.join(build_dir, os.path.basename(lib) + ".stamp")
+    fp = _fingerprint(verbose_ptxas) + " ".join(defs)
+    if not force and os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read() == fp:
+        return lib
     nvcc = _nvcc()
-    flags = _flags(verbose_ptxas)
+    flags = _flags(verbose_ptxas) + defs
 
     def compile_one(name: str) -> str:
         src = os.path.join(CSRC, name)
-        obj = os.path.join(BUILD, name + ".o")
+        obj = os.path.join(build_dir, name + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -74,15 +90,15 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as fh:
         fh.write(fp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -299,7 +299,17 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       __syncwarp();
       int issued_k = 0, issued_v = 0;
       bool pok = true;
-      for (int j = 0; j < nT && !warp_abort(); ++j) {
+#ifdef PKV_SELFTEST
+      // Self-test build only (compiled by the tests, never into libpaged_kv.so): the producer
+      // issues no K / V copy, so the MMA warp's wait for the first K tile and the softmax warps'
+      // waits for their first S run out after the short self-test budget and the CTA winds down
+      // through the timeout path below.  Q has landed before the teardown: no copy in flight.
+      const int n_issue = 0;
+      tc::mbar_wait(bar(q_bar), 0);
+#else
+      const int n_issue = nT;
+#endif
+      for (int j = 0; j < n_issue && !warp_abort(); ++j) {
         const int st = stg(j);
         // lane pp < pages_per_tile looks up page pp of the tile (B <= 128: whole pages per tile)
         const int lb = (kt0 + j * kCtxTileN) / p.B + lane;

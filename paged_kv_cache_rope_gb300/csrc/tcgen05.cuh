@@ -33,8 +33,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Clock budget of a bounded wait: about one second at the GB300's SM clock.  The self-test
+// build of the library (built only by the tests) sets a budget of about a millisecond.
+#ifndef PKV_WAIT_BUDGET
+#define PKV_WAIT_BUDGET 2000000000LL
+#endif
 // Wait for the phase with the given parity to complete; gives up after ~`budget` SM clocks.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long budget = 2000000000LL) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long budget = PKV_WAIT_BUDGET) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
