@@ -1,7 +1,7 @@
 """Benchmark of one inflight-batch layer step (RoPE + append, then paged attention) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--kv-dtype bf16|fp8|int8]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-sub]
 
 A step is the whole hot path over one batch: paged_kv_append_rope + paged_attention_forward
 (plan, context tensor-core kernel, split-KV decode, log-sum-exp combine), inputs resident in HBM.
@@ -11,9 +11,14 @@ flush is needed between steps.  With N > 1 (torchrun) every rank runs its own ba
 shape (requests are independent, so the path shards with no exchange) and ``value`` is the sum
 over ranks of the work divided by the slowest rank's time.
 
-Printed (rank 0): one JSON line with value, e2e (same metric through the public API with the
-step's q/k/v copied host->device and the output copied back inside the timed region), the
-dominant kernel's roofline, clocks sampled during the timed region and the CPU oracle baseline.
+Printed (rank 0): one JSON line with value (decode KV GB/s of the default workload), e2e (same
+metric through the public API with the step's q/k/v copied host->device and the output copied
+back inside the timed region), the roofline of the kernel that takes the most time, clocks
+sampled during the timed region and the CPU oracle baseline.  The default run adds ``sub``: the
+same measurement on the other workloads of the metric -- the 16384-token prefill (prefill
+TFLOP/s of the context kernel), the inflight mixed batch with bf16 and FP8 pools, the 70B-like
+GQA decode with bf16 and FP8 pools, and the tiny mixed batch (launch overhead) -- each with its
+per-kernel fractions of the measured and the nominal peaks and its own clocks.
 ``--impl reference`` times the CPU oracle itself on a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -35,6 +40,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode attn KV GB/s (% of HBM peak); prefill TFLOP/s (% BF16 peak); tokens/s"
+
+# Nominal GB300 figures (context for the measured fractions): HBM3e bandwidth and dense bf16
+# tensor throughput per GPU.
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+# kernels that read the generation requests' KV (together they move the decode bytes)
+DECODE_KERNELS = ("decode_splitkv", "decode_splitkv_wide", "decode_tc")
 
 
 # --------------------------------------------------------------------------------------------
@@ -82,6 +95,57 @@ def ncu_traffic(kernel: str, workload: str):
             except ValueError:
                 return None
     return None
+
+
+def kernel_rates(work: dict, kern_ms: dict, pk_: dict) -> dict:
+    """Per-kernel time and, where the kernel has algorithmic work of its own, its rate and its
+    fraction of the measured peak (``frac_*``) and of the nominal GB300 peak (``*_nominal``).
+    The decode kernels share the decode bytes: each gets a rate only when it is the only one."""
+    dec = [n for n in DECODE_KERNELS if n in kern_ms]
+    out = {}
+    for n, ms in kern_ms.items():
+        d = {"us": ms * 1e3}
+        if n in dec and len(dec) == 1 and work["decode_kv_bytes"]:
+            gbs = work["decode_bytes"] / (ms * 1e-3) / 1e9
+            d.update({"GB/s": gbs, "frac_hbm": gbs / pk_["hbm"], "frac_hbm_nominal": gbs / NOMINAL_HBM_GBS})
+        elif n == "context_attn" and work["ctx_flops"]:
+            tf = work["ctx_flops"] / (ms * 1e-3) / 1e12
+            d.update({"TFLOP/s": tf, "frac_bf16": tf / pk_["bf16"], "frac_bf16_sustained": tf / pk_["bf16_sustained"],
+                      "frac_bf16_nominal": tf / NOMINAL_BF16_TFLOPS})
+        elif n == "append_rope":
+            gbs = work["append_bytes"] / (ms * 1e-3) / 1e9
+            d.update({"GB/s": gbs, "frac_hbm": gbs / pk_["hbm"], "frac_hbm_nominal": gbs / NOMINAL_HBM_GBS})
+        out[n] = d
+    return out
+
+
+def roofline_of(work: dict, kern_ms: dict, pk_: dict, workload: str) -> dict:
+    """Roofline of the kernel class that takes the most time in the step: the decode kernels
+    (together, HBM), the context kernel (bf16 tensor) or the append (HBM)."""
+    classes = {}
+    dec = [n for n in DECODE_KERNELS if n in kern_ms]
+    if dec and work["decode_kv_bytes"]:
+        classes["+".join(dec)] = sum(kern_ms[n] for n in dec)
+    if "context_attn" in kern_ms and work["ctx_flops"]:
+        classes["context_attn"] = kern_ms["context_attn"]
+    if "append_rope" in kern_ms:
+        classes["append_rope"] = kern_ms["append_rope"]
+    kernel = max(classes, key=classes.get)
+    ms = classes[kernel]
+    if kernel == "context_attn":
+        ach = work["ctx_flops"] / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk_["bf16"], "unit": "TFLOP/s", "frac": ach / pk_["bf16"],
+                "peak_nominal": NOMINAL_BF16_TFLOPS, "frac_nominal": ach / NOMINAL_BF16_TFLOPS,
+                "frac_sustained": ach / pk_["bf16_sustained"]}
+    else:
+        nbytes = work["append_bytes"] if kernel == "append_rope" else work["decode_bytes"]
+        ach = nbytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk_["hbm"], "unit": "GB/s", "frac": ach / pk_["hbm"],
+                "peak_nominal": NOMINAL_HBM_GBS, "frac_nominal": ach / NOMINAL_HBM_GBS}
+    roof.update({"kernel": kernel, "us_per_launch": ms * 1e3, "peak_source": pk_["src"],
+                 "share_of_serial_step": ms / sum(kern_ms.values())})
+    roof["traffic"] = ncu_traffic(kernel, workload)
+    return roof
 
 
 # --------------------------------------------------------------------------------------------
@@ -143,8 +207,13 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------------------------
-# CPU oracle baseline (bounded sample)
+# CPU oracle baseline (bounded samples)
 # --------------------------------------------------------------------------------------------
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
 
 class OracleSample:
     """The CPU oracle on one generation request at a time (write image of its token, then fp64
@@ -154,10 +223,8 @@ class OracleSample:
         import oracle
         self.oracle = oracle
         self.b = b
-        bits = lambda t: (t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-                          if t.dtype == torch.bfloat16 else t.detach().cpu().contiguous().numpy())
-        self.pool = bits(b.pool)
-        self.q, self.k, self.v = bits(b.q), bits(b.k), bits(b.v)
+        self.pool = _bits(b.pool)
+        self.q, self.k, self.v = _bits(b.q), _bits(b.k), _bits(b.v)
         self.cs = oracle.rope_table(b.rope_base, b.head_dim, b.max_pos)
         self.gen = [r for r in range(b.num_requests) if b.request_types[r] == 1]
         self.row_of = np.concatenate([[0], np.cumsum(b.new_len)[:-1]]).astype(np.int64)
@@ -187,17 +254,59 @@ class OracleSample:
         return L * 2 * b.num_kv_heads * b.head_dim * self.esz
 
 
-def cpu_baseline(b, budget_s: float = 12.0) -> dict:
+def oracle_context_rate(b, stride: int) -> dict:
+    """The CPU oracle on the context rows of a batch: the write image of every new token, then
+    fp64 attention (all query heads) of every ``stride``-th context row; the rate is the causal
+    flops of those rows over the attention's wall time."""
+    import oracle as o
+    pool = _bits(b.pool).copy()
+    cs = o.rope_table(b.rope_base, b.head_dim, b.max_pos)
+    kw = dict(new_len=b.new_len, past=b.past, block_table=b.block_table, num_q_heads=b.num_q_heads,
+              num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, tokens_per_block=b.tokens_per_block,
+              num_blocks=b.num_blocks, kv_fp8=b.kv_dtype == "fp8", kv_int8=b.kv_dtype == "int8")
+    st, q_out = o.append_rope(**kw, inv_scale=b.inv_scale, q_bits=_bits(b.q), k_bits=_bits(b.k),
+                              v_bits=_bits(b.v), cs=cs, pool=pool)
+    q64 = o.f32_from_bf16(q_out).astype(np.float64)
+    rows, flops, row0 = [], 0, 0
+    for r in range(b.num_contexts):
+        n, P = int(b.new_len[r]), int(b.past[r])
+        for i in range(0, n, stride):
+            rows.append(row0 + i)
+            flops += 4 * b.head_dim * b.num_q_heads * (P + i + 1)
+        row0 += n
+    t0 = time.perf_counter()
+    o.attention(**kw, kv_scale=b.kv_scale, pool=pool, q=q64, softmax_scale=b.softmax_scale,
+                rows=np.array(rows, dtype=np.int64))
+    dt = time.perf_counter() - t0
+    return {"tflops": flops / dt / 1e12, "rows": len(rows), "seconds": dt, "flops": flops}
+
+
+def cpu_baseline(b, ctx_batches=(), budget_s: float = 8.0) -> dict:
+    """The oracle as it stands on the host cores: generation requests of the main workload
+    (``value``, GB/s) and, for each batch in ``ctx_batches`` ((name, batch, row stride)), its
+    context rows (TFLOP/s, sampled every stride-th row and extrapolated to the full prefill)."""
     s = OracleSample(b)
     s.step()  # build / load the oracle outside the timing
     t0, nbytes, n = time.perf_counter(), 0, 0
-    while time.perf_counter() - t0 < budget_s and n < 4 * len(s.gen):
+    while time.perf_counter() - t0 < budget_s and n < 40 * len(s.gen):
         nbytes += s.step()
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": s.oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} generation requests of the workload (all heads each), fp64 oracle "
-                      f"write image + attention, {dt:.1f} s wall"}
+    res = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": s.oracle.num_threads(), "kind": "oracle",
+           "sample": f"{n} generation requests of the workload (all heads each), fp64 oracle "
+                     f"write image + attention, {dt:.1f} s wall"}
+    ctx = {}
+    for name, cb, stride in ctx_batches:
+        c = oracle_context_rate(cb, stride)
+        full = work_of(cb)["ctx_flops"]
+        ctx[name] = {"value": c["tflops"], "unit": "TFLOP/s", "extrapolated": stride > 1,
+                     "sample": f"every {stride}th context row ({c['rows']} rows, all {cb.num_q_heads} query "
+                               f"heads), fp64 attention over the pool after the write image, "
+                               f"{c['seconds']:.1f} s wall",
+                     "full_prefill_s_extrapolated": full / (c["tflops"] * 1e12)}
+    if ctx:
+        res["context"] = ctx
+    return res
 
 
 # --------------------------------------------------------------------------------------------
@@ -242,17 +351,28 @@ def aggregate(work_per_rank: float, ms_total_per_rank: float, steps: int, world:
     return ms_step, world * work_per_rank / (ms_step * 1e-3)
 
 
-def run_ours(args):
+class Ctx:
+    def __init__(self, world, rank, local):
+        self.world, self.rank, self.local = world, rank, local
+        self.dev = torch.device("cuda", local)
+        self.gpu_index = torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local
+
+
+def measure(cx: Ctx, workload: int, kv_dtype: str, steps: int, warmup: int, *, graph: bool = True,
+            e2e: bool = False, max_gen: int | None = None) -> dict:
+    """Times K steps of one workload: the step as a whole (default streams), the same K steps with
+    per-kernel events (every kernel on the caller's stream), optionally graph replay and the
+    end-to-end loop through the public API with host inputs.  Returns the raw measurements."""
     import paged_kv_cache_rope_gb300 as pk
     from paged_kv_cache_rope_gb300 import workloads as W
 
-    world, rank, local = dist_setup()
-    dev = torch.device("cuda", local)
-    b = W.workload(args.workload, kv_dtype=args.kv_dtype, device=str(dev), poison=False,
-                   seed=args.workload + 1000 * rank, max_gen=args.max_gen)
+    world, dev = cx.world, cx.dev
+    b = W.workload(workload, kv_dtype=kv_dtype, device=str(dev), poison=False,
+                   seed=workload + 1000 * cx.rank, max_gen=max_gen)
     work = work_of(b)
     pool = pk.KVPool(b.pool, b.kv_scale, b.inv_scale)
-    meta = pk.BatchMeta(b.request_types, b.new_len, b.past, b.block_table, dev)
+    meta = pk.BatchMeta(b.request_types, b.new_len, b.past, b.block_table, dev,
+                        position_offsets=b.position_offsets, packed_mask=b.packed_mask)
     table = pk.paged_rope_table_build(b.rope_base, b.head_dim, b.max_pos, dev)
     step = pk.PagedAttentionStep(pool, meta, b.num_q_heads, b.head_dim, table)
     q, k, v = b.q, b.k, b.v
@@ -261,13 +381,9 @@ def run_ours(args):
     step(q, k, v)
     torch.cuda.synchronize()
     fwd_names = pk.last_launch_names()
-    names = ["append_rope"] + fwd_names
-    launches_per_step = len(names)
-    # generation rows run on the narrow and/or the wide decode kernel: together they read the KV
-    dec_names = [n for n in ("decode_splitkv", "decode_splitkv_wide", "decode_tc") if n in fwd_names]
-    dominant = "+".join(dec_names) if work["decode_kv_bytes"] else "context_attn"
+    launches_per_step = 1 + len(fwd_names)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step(q, k, v)
     torch.cuda.synchronize()
 
@@ -275,16 +391,16 @@ def run_ours(args):
     # recorded by the library around each launch; while events are set the library keeps every
     # kernel on the caller's stream (no context/generation overlap), so that each pair of events
     # brackets one kernel's own work.
-    ev_app = [pk.KernelEvents(1) for _ in range(args.steps)]
-    ev_fwd = [pk.KernelEvents(len(fwd_names)) for _ in range(args.steps)]
+    ev_app = [pk.KernelEvents(1) for _ in range(steps)]
+    ev_fwd = [pk.KernelEvents(len(fwd_names)) for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    sampler = ClockSampler(cx.gpu_index)
     barrier(world)
     torch.cuda.synchronize()
     with sampler:
         start.record()
-        for i in range(args.steps):
+        for _ in range(steps):
             pk.paged_kv_append_rope(pool, meta, step.Hq, q, k, v, step.q_out, table, step.d_error)
             pk.paged_attention_forward(pool, meta, step.Hq, step.q_out, step.out, step.softmax_scale,
                                        step.workspace, step.d_error)
@@ -292,7 +408,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         k0.record()
-        for i in range(args.steps):
+        for i in range(steps):
             with ev_app[i]:
                 pk.paged_kv_append_rope(pool, meta, step.Hq, q, k, v, step.q_out, table, step.d_error)
             with ev_fwd[i]:
@@ -301,96 +417,140 @@ def run_ours(args):
         k1.record()
         torch.cuda.synchronize()
     barrier(world)
-    ms_step, _ = aggregate(1.0, start.elapsed_time(stop), args.steps, world)
-    ms_serial, _ = aggregate(1.0, k0.elapsed_time(k1), args.steps, world)
+    ms_step, _ = aggregate(1.0, start.elapsed_time(stop), steps, world)
+    ms_serial, _ = aggregate(1.0, k0.elapsed_time(k1), steps, world)
     err = int(step.d_error.item())
     if err:
-        raise SystemExit(f"device error word {err} during the timed region")
+        raise SystemExit(f"device error word {err} during the timed region ({b.name})")
 
-    kern_ms = {}
+    kern_ms = {"append_rope": statistics.fmean(e.elapsed_ms(0) for e in ev_app)}
     for j, n in enumerate(fwd_names):
         kern_ms[n] = statistics.fmean(e.elapsed_ms(j) for e in ev_fwd)
-    kern_ms["append_rope"] = statistics.fmean(e.elapsed_ms(0) for e in ev_app)
+
+    res = dict(b=b, work=work, ms_step=ms_step, ms_serial=ms_serial, kern_ms=kern_ms, fwd_names=fwd_names,
+               launches_per_step=launches_per_step, clocks=sampler.summary(), graph=None, e2e=None)
 
     # ---- the same step captured once into a CUDA graph and replayed (launch overhead gone) ----
-    graph = None
-    try:
-        gs = torch.cuda.Stream()
-        gs.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(gs):
-            step(q, k, v)
-        torch.cuda.current_stream().wait_stream(gs)
-        torch.cuda.synchronize()
-        cg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cg):
-            step(q, k, v)
-        for _ in range(3):
-            cg.replay()
-        torch.cuda.synchronize()
-        barrier(world)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record()
-        for _ in range(args.steps):
-            cg.replay()
-        g1.record()
-        torch.cuda.synchronize()
-        g_ms, _ = aggregate(1.0, g0.elapsed_time(g1), args.steps, world)
-        graph = {"ms_per_step": g_ms, "launches_per_step": launches_per_step}
-        del cg
-    except Exception as exc:  # capture is a measurement extra, never a reason to fail the bench
-        graph = {"error": str(exc)[:200]}
+    if graph:
+        try:
+            gs = torch.cuda.Stream()
+            gs.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(gs):
+                step(q, k, v)
+            torch.cuda.current_stream().wait_stream(gs)
+            torch.cuda.synchronize()
+            cg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(cg):
+                step(q, k, v)
+            for _ in range(3):
+                cg.replay()
+            torch.cuda.synchronize()
+            barrier(world)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record()
+            for _ in range(steps):
+                cg.replay()
+            g1.record()
+            torch.cuda.synchronize()
+            g_ms, _ = aggregate(1.0, g0.elapsed_time(g1), steps, world)
+            res["graph"] = {"ms_per_step": g_ms, "launches_per_step": launches_per_step}
+            del cg
+        except Exception as exc:  # capture is a measurement extra, never a reason to fail the bench
+            res["graph"] = {"error": str(exc)[:200]}
 
     # ---- e2e through the public API: host q/k/v in pinned memory, output copied back ----
     # Every step copies its q/k/v from pinned host memory and its output back to the host.  The
     # copies run on a second stream, double-buffered, so that step i's output and step i+2's
     # inputs move while step i+1 computes (as a serving loop would run it); two step objects
     # share the pool and own separate output buffers.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    dbuf = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
-    steps2 = [step, pk.PagedAttentionStep(pool, meta, b.num_q_heads, b.head_dim, table)]
-    hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    xs = torch.cuda.Stream()
-    cs = torch.cuda.current_stream()
-    e2e_steps = max(10, args.steps // 4)
+    if e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        dbuf = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
+        steps2 = [step, pk.PagedAttentionStep(pool, meta, b.num_q_heads, b.head_dim, table)]
+        hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        xs = torch.cuda.Stream()
+        cs = torch.cuda.current_stream()
+        e2e_steps = max(10, steps // 4)
 
-    def run_e2e(n: int) -> None:
-        h2d_ev = [torch.cuda.Event(), torch.cuda.Event()]
-        done_ev = [torch.cuda.Event(), torch.cuda.Event()]
-        with torch.cuda.stream(xs):
-            xs.wait_stream(cs)
-            for i in range(min(2, n)):
-                for d, h in zip(dbuf[i], (hq, hk, hv)):
-                    d.copy_(h, non_blocking=True)
-                h2d_ev[i].record(xs)
-        for i in range(n):
-            bi = i & 1
-            cs.wait_event(h2d_ev[bi])
-            steps2[bi](*dbuf[bi])
-            done_ev[bi].record(cs)
+        def run_e2e(n: int) -> None:
+            h2d_ev = [torch.cuda.Event(), torch.cuda.Event()]
+            done_ev = [torch.cuda.Event(), torch.cuda.Event()]
             with torch.cuda.stream(xs):
-                xs.wait_event(done_ev[bi])
-                hout.copy_(steps2[bi].out, non_blocking=True)
-                if i + 2 < n:
-                    for d, h in zip(dbuf[bi], (hq, hk, hv)):
+                xs.wait_stream(cs)
+                for i in range(min(2, n)):
+                    for d, h in zip(dbuf[i], (hq, hk, hv)):
                         d.copy_(h, non_blocking=True)
-                    h2d_ev[bi].record(xs)
-        cs.wait_stream(xs)
+                    h2d_ev[i].record(xs)
+            for i in range(n):
+                bi = i & 1
+                cs.wait_event(h2d_ev[bi])
+                steps2[bi](*dbuf[bi])
+                done_ev[bi].record(cs)
+                with torch.cuda.stream(xs):
+                    xs.wait_event(done_ev[bi])
+                    hout.copy_(steps2[bi].out, non_blocking=True)
+                    if i + 2 < n:
+                        for d, h in zip(dbuf[bi], (hq, hk, hv)):
+                            d.copy_(h, non_blocking=True)
+                        h2d_ev[bi].record(xs)
+            cs.wait_stream(xs)
 
-    run_e2e(3)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.perf_counter()
-    e0.record()
-    run_e2e(e2e_steps)
-    e1.record()
-    torch.cuda.synchronize()
-    wall_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    e2e_ms = reduce_max(max(e0.elapsed_time(e1) / e2e_steps, wall_ms), world)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = hout.numel() * hout.element_size()
+        run_e2e(3)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record()
+        run_e2e(e2e_steps)
+        e1.record()
+        torch.cuda.synchronize()
+        wall_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+        e2e_ms = reduce_max(max(e0.elapsed_time(e1) / e2e_steps, wall_ms), world)
+        res["e2e"] = {"ms_per_step": e2e_ms, "h2d": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
+                      "d2h": hout.numel() * hout.element_size()}
+        del steps2, dbuf
+    del step, pool, meta, table
+    return res
 
+
+def sub_record(m: dict, world: int, pk_: dict) -> dict:
+    """The sub-record of one workload: step times, tokens/s, per-kernel rates and fractions, the
+    dominant kernel's roofline and the clocks of its timed region."""
+    b, work = m["b"], m["work"]
+    wname = b.name + ("" if b.kv_dtype == "bf16" else "_" + b.kv_dtype)
+    rec = {"workload": b.name, "kv_dtype": b.kv_dtype, "requests": b.num_requests, "contexts": b.num_contexts,
+           "num_tokens": b.num_tokens, "ms_per_step": m["ms_step"], "ms_per_step_serial": m["ms_serial"],
+           "tokens_per_s": world * work["tokens"] / (m["ms_step"] * 1e-3),
+           "kernels": kernel_rates(work, m["kern_ms"], pk_), "roofline": roofline_of(work, m["kern_ms"], pk_, wname),
+           "clocks": m["clocks"]}
+    if work["ctx_flops"]:
+        rec["prefill_TFLOP/s"] = rec["kernels"]["context_attn"]["TFLOP/s"]
+        rec["prefill_frac_bf16"] = rec["kernels"]["context_attn"]["frac_bf16"]
+    if m["graph"] is not None:
+        rec["graph"] = m["graph"]
+    return rec
+
+
+# the workloads of the metric besides the default one: (key, workload, kv dtype)
+SUB_WORKLOADS = (
+    ("prefill_16k", 5, "bf16"),
+    ("mixed", 4, "bf16"),
+    ("mixed_fp8", 4, "fp8"),
+    ("decode_gqa", 3, "bf16"),
+    ("decode_gqa_fp8", 3, "fp8"),
+    ("tiny", 1, "bf16"),
+)
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    cx = Ctx(world, rank, local)
     pk_ = peaks()
+    m = measure(cx, args.workload, args.kv_dtype, args.steps, args.warmup, graph=True, e2e=True,
+                max_gen=args.max_gen)
+    b, work = m["b"], m["work"]
+    ms_step = m["ms_step"]
+    e2e_ms = m["e2e"]["ms_per_step"]
     if work["decode_kv_bytes"]:
         value = world * work["decode_kv_bytes"] / (ms_step * 1e-3) / 1e9
         e2e_value = world * work["decode_kv_bytes"] / (e2e_ms * 1e-3) / 1e9
@@ -399,34 +559,12 @@ def run_ours(args):
         value = world * work["ctx_flops"] / (ms_step * 1e-3) / 1e12
         e2e_value = world * work["ctx_flops"] / (e2e_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
+    graph = m["graph"]
     if graph and "ms_per_step" in graph:
         w = work["decode_kv_bytes"] or work["ctx_flops"]
         graph["value"] = world * w / (graph["ms_per_step"] * 1e-3) / (1e9 if work["decode_kv_bytes"] else 1e12)
         graph["tokens_per_s"] = world * work["tokens"] / (graph["ms_per_step"] * 1e-3)
-    if dominant != "context_attn":
-        dec_ms = sum(kern_ms[n] for n in dec_names)
-        ach = work["decode_bytes"] / (dec_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": pk_["hbm"], "unit": "GB/s",
-                "frac": ach / pk_["hbm"], "kernel": dominant, "peak_source": pk_["src"]}
-    else:
-        ach = work["ctx_flops"] / (kern_ms["context_attn"] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": pk_["bf16"], "unit": "TFLOP/s",
-                "frac": ach / pk_["bf16"], "kernel": "context_attn", "peak_source": pk_["src"]}
-    roof["traffic"] = ncu_traffic(dominant, b.name + ("" if b.kv_dtype == "bf16" else "_" + b.kv_dtype))
-
-    kernels = {}
-    for n, ms in kern_ms.items():
-        d = {"us": ms * 1e3}
-        if n in dec_names and len(dec_names) == 1:
-            d["GB/s"] = work["decode_bytes"] / (ms * 1e-3) / 1e9
-            d["frac_hbm"] = d["GB/s"] / pk_["hbm"]
-        elif n == "context_attn":
-            d["TFLOP/s"] = work["ctx_flops"] / (ms * 1e-3) / 1e12
-            d["frac_bf16"] = d["TFLOP/s"] / pk_["bf16"]
-        elif n == "append_rope":
-            d["GB/s"] = work["append_bytes"] / (ms * 1e-3) / 1e9
-            d["frac_hbm"] = d["GB/s"] / pk_["hbm"]
-        kernels[n] = d
+    wname = b.name + ("" if b.kv_dtype == "bf16" else "_" + b.kv_dtype)
 
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -442,18 +580,43 @@ def run_ours(args):
                    "parallelism": f"dp{world} (independent batches per GPU)"},
         "tokens_per_s": world * work["tokens"] / (ms_step * 1e-3),
         "pct_of_hbm_peak": 100.0 * value / pk_["hbm"] if unit == "GB/s" else None,
-        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
-        "gpu_launches": launches_per_step * args.steps,
+        "pct_of_hbm_nominal": 100.0 * value / NOMINAL_HBM_GBS if unit == "GB/s" else None,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": m["e2e"]["h2d"],
+                "d2h_bytes_per_step": m["e2e"]["d2h"], "ms_per_step": e2e_ms},
+        "gpu_launches": m["launches_per_step"] * args.steps,
         "graph": graph,
-        "kernels": kernels,
+        "kernels": kernel_rates(work, m["kern_ms"], pk_),
         "kernels_timed": "second loop of the same K steps, per-kernel events, all kernels on one stream",
-        "ms_per_step_serial": ms_serial,
-        "roofline": roof,
-        "clocks": sampler.summary(),
+        "ms_per_step_serial": m["ms_serial"],
+        "roofline": roofline_of(work, m["kern_ms"], pk_, wname),
+        "clocks": m["clocks"],
+        "peaks": {"hbm_gbs": pk_["hbm"], "bf16_tflops": pk_["bf16"], "bf16_tflops_sustained": pk_["bf16_sustained"],
+                  "source": pk_["src"], "hbm_gbs_nominal": NOMINAL_HBM_GBS, "bf16_tflops_nominal": NOMINAL_BF16_TFLOPS},
     }
+    del m
+    torch.cuda.empty_cache()
+
+    ctx_cpu = []
+    if not args.no_sub and args.workload == 2 and args.max_gen is None:
+        # the rest of the metric, measured in the same run: the prefill TFLOP/s half on the 16K
+        # prefill, the mixed inflight batch, the GQA decode, the tiny batch's launch overhead
+        sub_steps = max(3, min(args.steps, 20))
+        subs = {}
+        for key, wl, kd in SUB_WORKLOADS:
+            ms = measure(cx, wl, kd, sub_steps, args.warmup, graph=True, e2e=False)
+            subs[key] = sub_record(ms, world, pk_)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline and key in ("prefill_16k", "mixed"):
+                ctx_cpu.append((key, ms["b"], 16 if key == "prefill_16k" else 2))
+            del ms
+            torch.cuda.empty_cache()
+        line["sub"] = subs
+        line["sub_steps"] = sub_steps
+        pf = subs["prefill_16k"]["kernels"]["context_attn"]
+        line["prefill"] = {"workload": subs["prefill_16k"]["workload"], "TFLOP/s": pf["TFLOP/s"],
+                           "frac_bf16": pf["frac_bf16"], "frac_bf16_sustained": pf["frac_bf16_sustained"],
+                           "frac_bf16_nominal": pf["frac_bf16_nominal"], "us_per_launch": pf["us"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(b.to("cpu"))
+        line["cpu_baseline"] = cpu_baseline(b.to("cpu"), [(k, cb.to("cpu"), s) for k, cb, s in ctx_cpu])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -500,6 +663,7 @@ def main():
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8", "int8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="only the main workload (no sub-records)")
     ap.add_argument("--max-gen", type=int, default=None,
                     help="keep only the first N generation requests (profiling captures)")
     args = ap.parse_args()

@@ -42,3 +42,23 @@ def test_eight_bit_pools_move_half_the_decode_bytes():
     wi = bench.work_of(W.workload(3, kv_dtype="int8", poison=False, max_gen=8))
     assert 2 * w8["decode_kv_bytes"] == wb["decode_kv_bytes"] == 2 * wi["decode_kv_bytes"]
     assert w8["ctx_flops"] == wb["ctx_flops"] == 0
+
+
+def test_roofline_follows_the_kernel_that_takes_the_most_time():
+    """The reported roofline belongs to the kernel class with the largest measured time: the
+    context kernel on a prefill-heavy step, the decode kernels (together) on a decode step."""
+    pk_ = dict(hbm=6000.0, bf16=2000.0, bf16_sustained=1800.0, src="test")
+    work = dict(decode_kv_bytes=6e8, decode_bytes=6.1e8, ctx_flops=2e12, append_bytes=1e8, tokens=100)
+    prefill_heavy = {"append_rope": 0.05, "plan": 0.01, "context_attn": 1.3, "decode_splitkv": 0.4}
+    r = bench.roofline_of(work, prefill_heavy, pk_, "none")
+    assert r["kernel"] == "context_attn" and r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 2e12 / 1.3e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / 2000.0) < 1e-12
+    assert abs(r["frac_nominal"] - r["achieved"] / bench.NOMINAL_BF16_TFLOPS) < 1e-12
+    decode_heavy = {"append_rope": 0.05, "context_attn": 0.1, "decode_splitkv": 0.3, "decode_tc": 0.2}
+    r = bench.roofline_of(work, decode_heavy, pk_, "none")
+    assert r["kernel"] == "decode_splitkv+decode_tc" and r["bound"] == "hbm"
+    assert abs(r["achieved"] - 6.1e8 / 0.5e-3 / 1e9) < 1e-9
+    k = bench.kernel_rates(work, decode_heavy, pk_)
+    assert "GB/s" not in k["decode_splitkv"]  # two decode kernels share the bytes
+    assert abs(k["context_attn"]["frac_bf16_nominal"] - 2e12 / 0.1e-3 / 1e12 / bench.NOMINAL_BF16_TFLOPS) < 1e-12
