@@ -359,7 +359,7 @@ class Ctx:
 
 
 def measure(cx: Ctx, workload: int, kv_dtype: str, steps: int, warmup: int, *, graph: bool = True,
-            e2e: bool = False, max_gen: int | None = None) -> dict:
+            e2e: bool = False, bucket: bool = False, max_gen: int | None = None) -> dict:
     """Times K steps of one workload: the step as a whole (default streams), the same K steps with
     per-kernel events (every kernel on the caller's stream), optionally graph replay and the
     end-to-end loop through the public API with host inputs.  Returns the raw measurements."""
@@ -428,7 +428,8 @@ def measure(cx: Ctx, workload: int, kv_dtype: str, steps: int, warmup: int, *, g
         kern_ms[n] = statistics.fmean(e.elapsed_ms(j) for e in ev_fwd)
 
     res = dict(b=b, work=work, ms_step=ms_step, ms_serial=ms_serial, kern_ms=kern_ms, fwd_names=fwd_names,
-               launches_per_step=launches_per_step, clocks=sampler.summary(), graph=None, e2e=None)
+               launches_per_step=launches_per_step, clocks=sampler.summary(), graph=None, e2e=None,
+               bucket_graph=None)
 
     # ---- the same step captured once into a CUDA graph and replayed (launch overhead gone) ----
     if graph:
@@ -457,6 +458,42 @@ def measure(cx: Ctx, workload: int, kv_dtype: str, steps: int, warmup: int, *, g
             del cg
         except Exception as exc:  # capture is a measurement extra, never a reason to fail the bench
             res["graph"] = {"error": str(exc)[:200]}
+
+    # ---- the same step on a padding bucket: one graph for every batch of the bucket ----
+    # The bucket holds this batch's request slots and rows, with the KV-length limit rounded up
+    # to a multiple of 1024 tokens; the replays run this batch through it.
+    if bucket and graph:
+        try:
+            B = b.tokens_per_block
+            max_kv = int(-(-int(b.kv_lengths.max()) // 1024) * 1024)
+            bk = pk.Bucket(context_slots=b.num_contexts, generation_slots=b.num_requests - b.num_contexts,
+                           max_tokens=b.num_tokens, max_context_tokens=b.num_ctx_tokens, max_kv_len=max_kv,
+                           max_gen_tokens=int(b.new_len[b.num_contexts:].max()) if b.num_requests > b.num_contexts else 1,
+                           max_blocks_per_seq=-(-max_kv // B))
+            btable = pk.paged_rope_table_build(b.rope_base, b.head_dim, max(max_kv, b.max_pos), dev)
+            bstep = pk.PagedAttentionBucketStep(pool, bk, b.num_q_heads, b.head_dim, btable,
+                                                draft=b.position_offsets is not None)
+            bstep.load(b.request_types, b.new_len, b.past, b.block_table, q, k, v,
+                       position_offsets=b.position_offsets, packed_mask=b.packed_mask)
+            bstep.capture()
+            for _ in range(3):
+                bstep.replay()
+            torch.cuda.synchronize()
+            barrier(world)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record()
+            for _ in range(steps):
+                bstep.replay()
+            g1.record()
+            torch.cuda.synchronize()
+            if int(bstep.d_error.item()):
+                raise RuntimeError(f"device error word {int(bstep.d_error.item())} in the bucket replay")
+            g_ms, _ = aggregate(1.0, g0.elapsed_time(g1), steps, world)
+            res["bucket_graph"] = {"ms_per_step": g_ms, "max_kv_len": max_kv, "slots": bk.slots,
+                                   "max_tokens": bk.max_tokens}
+            del bstep
+        except Exception as exc:  # a measurement extra, never a reason to fail the bench
+            res["bucket_graph"] = {"error": str(exc)[:200]}
 
     # ---- e2e through the public API: host q/k/v in pinned memory, output copied back ----
     # Every step copies its q/k/v from pinned host memory and its output back to the host.  The
@@ -528,6 +565,8 @@ def sub_record(m: dict, world: int, pk_: dict) -> dict:
         rec["prefill_frac_bf16"] = rec["kernels"]["context_attn"]["frac_bf16"]
     if m["graph"] is not None:
         rec["graph"] = m["graph"]
+    if m["bucket_graph"] is not None:
+        rec["bucket_graph"] = m["bucket_graph"]
     return rec
 
 
@@ -603,7 +642,7 @@ def run_ours(args):
         sub_steps = max(3, min(args.steps, 20))
         subs = {}
         for key, wl, kd in SUB_WORKLOADS:
-            ms = measure(cx, wl, kd, sub_steps, args.warmup, graph=True, e2e=False)
+            ms = measure(cx, wl, kd, sub_steps, args.warmup, graph=True, e2e=False, bucket=key in ("tiny", "mixed"))
             subs[key] = sub_record(ms, world, pk_)
             if rank == 0 and world == 1 and not args.no_cpu_baseline and key in ("prefill_16k", "mixed"):
                 ctx_cpu.append((key, ms["b"], 16 if key == "prefill_16k" else 2))

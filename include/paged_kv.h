@@ -61,6 +61,8 @@ typedef struct CUstream_st* pkv_stream_t; /* == cudaStream_t; NULL = legacy defa
 #define PKV_DEVERR_PLAN_MISMATCH 4u   /* device metadata disagrees with the host copies         */
 #define PKV_DEVERR_BAD_OFFSET 8u      /* a draft-token position offset outside [0, context_length):
                                          that token is skipped by the append                   */
+#define PKV_DEVERR_BUCKET 16u         /* bucket calls: the batch in the device arrays does not
+                                         fit its bucket; nothing after the append runs          */
 
 /* Most new tokens one generation request may bring in one step (draft tokens under
  * verification, [REPORT] 1.4 "推测解码技术": spec_decoding_max_generation_length). */
@@ -257,6 +259,62 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
                             const void* q_rot, int64_t q_row_stride, void* out,
                             float softmax_scale, void* workspace, size_t workspace_bytes,
                             int32_t* d_error, pkv_stream_t stream);
+
+/*
+ * Padding buckets for CUDA-graph replay ([NOTES] 五 5.2 "CUDA graph": a captured graph is only
+ * replayed when the batch has the shape it was captured with, so batch shapes are padded to a
+ * few fixed buckets to raise the hit rate; [ARCH] "AttentionMetadata 的字段与它的含义":
+ * create_cuda_graph_metadata allocates the metadata tensors once and never again after warm-up).
+ *
+ * The *_bucket entry points take every launch shape from the bucket and the pkv_batch's slot
+ * counts, never from the lengths: the lengths are read on the device only.  So one capture of a
+ * step serves every batch of the bucket -- the caller rewrites the device arrays (lengths, block
+ * table, draft-token arrays) and the input rows between replays.  In the pkv_batch given to
+ * them:
+ *   num_requests        request slots R (fixed); num_contexts = C context slots 0 .. C-1,
+ *                       slots C .. R-1 generation slots
+ *   num_tokens          row capacity: the rows of q / k / v / q_out / out; a batch uses the
+ *                       first sum(context_lengths) rows, packed in slot order
+ *   max_blocks_per_seq  block-table row length (fixed)
+ *   h_* arrays          ignored (may be NULL)
+ *   d_context_lengths   per slot, the new tokens this step; 0 = an empty slot (no rows, no work)
+ *   d_past_kv_lengths, d_block_offsets, d_position_offsets, d_packed_mask: as in pkv_batch (the
+ *                       draft-token arrays indexed by generation row, with capacity for the
+ *                       bucket's largest batch)
+ * Each step's batch must fit the bucket: at most max_context_tokens rows in context slots,
+ * past + new <= max_kv_len for every slot, at most max_gen_tokens new tokens per generation
+ * slot, at most num_tokens rows.  The device checks this; a batch that does not fit sets
+ * PKV_DEVERR_BUCKET and the attention writes nothing (the append may already have written its
+ * tokens).  Grids are sized for the bucket's largest batch: the spare CTAs of a smaller batch
+ * read the plan's counts and exit at once.
+ */
+typedef struct pkv_bucket {
+  int32_t max_context_tokens; /* rows of the context slots together, at most (0: no contexts) */
+  int32_t max_kv_len;         /* past + new of any slot, at most (<= max_blocks_per_seq * B)   */
+  int32_t max_gen_tokens;     /* new tokens of a generation slot, 1 .. PKV_MAX_GEN_TOKENS      */
+} pkv_bucket;
+
+/* Workspace bytes of paged_attention_forward_bucket for this pool, slot layout and bucket
+ * (enough for any batch of the bucket).  0 on invalid arguments. */
+size_t paged_attention_bucket_workspace_size(const pkv_pool* pool, const pkv_batch* batch, const pkv_bucket* bucket,
+                                             int32_t num_q_heads);
+
+/* paged_kv_append_rope over a bucket (see above): the same arithmetic and layouts; the RoPE
+ * table must hold max_kv_len positions.  Returns a host-detected PKV_ERR_* as the plain call
+ * does; batch-dependent errors are the device's (PKV_DEVERR_*). */
+int paged_kv_append_rope_bucket(const pkv_pool* pool, const pkv_batch* batch, const pkv_bucket* bucket,
+                                int32_t num_q_heads, const void* q, int64_t q_row_stride, const void* k,
+                                int64_t k_row_stride, const void* v, int64_t v_row_stride, void* q_out,
+                                int64_t q_out_row_stride, const float* rope_table, int32_t max_pos,
+                                const pkv_append_opts* opts, int32_t* d_error, pkv_stream_t stream);
+
+/* paged_attention_forward over a bucket (see above); the workspace must hold
+ * paged_attention_bucket_workspace_size bytes.  Output rows past the batch's rows are left
+ * untouched. */
+int paged_attention_forward_bucket(const pkv_pool* pool, const pkv_batch* batch, const pkv_bucket* bucket,
+                                   int32_t num_q_heads, const void* q_rot, int64_t q_row_stride, void* out,
+                                   float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* d_error,
+                                   pkv_stream_t stream);
 
 /*
  * paged_attention_forward without a caller workspace.  The pages have no counterpart: this is

@@ -35,6 +35,7 @@ PKV_DEVERR_BAD_PAGE = 1
 PKV_DEVERR_TIMEOUT = 2
 PKV_DEVERR_PLAN_MISMATCH = 4
 PKV_DEVERR_BAD_OFFSET = 8
+PKV_DEVERR_BUCKET = 16
 PKV_MAX_GEN_TOKENS = 64
 
 # the C ABI's exported symbols (include/paged_kv.h)
@@ -46,6 +47,9 @@ EXPORTS = (
     "paged_attention_workspace_size",
     "paged_attention_forward",
     "paged_attention_forward_noalloc",
+    "paged_attention_bucket_workspace_size",
+    "paged_kv_append_rope_bucket",
+    "paged_attention_forward_bucket",
     "paged_kv_last_launch_count",
     "paged_kv_last_launch_name",
     "paged_kv_set_kernel_events",
@@ -68,6 +72,10 @@ class PkvBatch(C.Structure):
                 ("d_past_kv_lengths", C.c_void_p), ("d_block_offsets", C.c_void_p),
                 ("d_position_offsets", C.c_void_p), ("d_packed_mask", C.c_void_p),
                 ("mask_words", C.c_int32)]
+
+
+class PkvBucket(C.Structure):
+    _fields_ = [("max_context_tokens", C.c_int32), ("max_kv_len", C.c_int32), ("max_gen_tokens", C.c_int32)]
 
 
 class PagedKVError(RuntimeError):
@@ -100,6 +108,12 @@ def lib() -> C.CDLL:
         L.paged_attention_forward.restype = C.c_int
         L.paged_attention_forward_noalloc.argtypes = [P, P, i32, P, i64, P, C.c_float, P, P]
         L.paged_attention_forward_noalloc.restype = C.c_int
+        L.paged_attention_bucket_workspace_size.argtypes = [P, P, P, i32]
+        L.paged_attention_bucket_workspace_size.restype = sz
+        L.paged_kv_append_rope_bucket.argtypes = [P, P, P, i32, P, i64, P, i64, P, i64, P, i64, P, i32, P, P, P]
+        L.paged_kv_append_rope_bucket.restype = C.c_int
+        L.paged_attention_forward_bucket.argtypes = [P, P, P, i32, P, i64, P, C.c_float, P, sz, P, P]
+        L.paged_attention_forward_bucket.restype = C.c_int
         L.paged_kv_last_launch_count.argtypes = []
         L.paged_kv_last_launch_count.restype = i32
         L.paged_kv_last_launch_name.argtypes = [i32]
@@ -362,4 +376,191 @@ class PagedAttentionStep:
         paged_attention_forward(self.pool, self.batch, self.Hq, self.q_out, self.out,
                                 self.softmax_scale, self.workspace, self.d_error, stream)
         self.launches = n + last_launch_count()
+        return self.out
+
+
+# --- padding buckets (one CUDA-graph capture per bucket) -------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class Bucket:
+    """A padding bucket: the largest batch one captured step serves.  ``context_slots`` request
+    slots take context requests and ``generation_slots`` slots generation requests (a slot with
+    no new tokens is empty); at most ``max_tokens`` packed rows, ``max_context_tokens`` of them in
+    context slots; past + new <= ``max_kv_len`` for every request; at most ``max_gen_tokens`` new
+    tokens per generation request; block tables of ``max_blocks_per_seq`` entries."""
+    context_slots: int
+    generation_slots: int
+    max_tokens: int
+    max_context_tokens: int
+    max_kv_len: int
+    max_gen_tokens: int
+    max_blocks_per_seq: int
+
+    @property
+    def slots(self) -> int:
+        return self.context_slots + self.generation_slots
+
+    def c(self) -> PkvBucket:
+        return PkvBucket(self.max_context_tokens, self.max_kv_len, self.max_gen_tokens)
+
+
+class BucketMeta:
+    """Device arrays of one bucket's batch (fixed addresses; rewritten in place per step)."""
+
+    def __init__(self, bucket: Bucket, device, draft: bool = False):
+        R, mb = bucket.slots, bucket.max_blocks_per_seq
+        gen_rows = min(bucket.max_tokens, bucket.generation_slots * bucket.max_gen_tokens)
+        self.bucket = bucket
+        self.d_context_lengths = torch.zeros(R, dtype=torch.int32, device=device)
+        self.d_past_kv_lengths = torch.zeros(R, dtype=torch.int32, device=device)
+        self.d_block_offsets = torch.full((R, mb), -1, dtype=torch.int32, device=device)
+        self.mask_words = max(1, -(-bucket.max_gen_tokens // 32)) if draft else 0
+        self.d_position_offsets = torch.zeros(max(gen_rows, 1), dtype=torch.int32, device=device) if draft else None
+        self.d_packed_mask = (torch.zeros(max(gen_rows, 1), self.mask_words, dtype=torch.int32, device=device)
+                              if draft else None)
+
+    def c(self) -> PkvBatch:
+        b = self.bucket
+        return PkvBatch(b.slots, b.context_slots, b.max_tokens, b.max_blocks_per_seq, None, None, None,
+                        self.d_context_lengths.data_ptr(), self.d_past_kv_lengths.data_ptr(),
+                        self.d_block_offsets.data_ptr(),
+                        None if self.d_position_offsets is None else self.d_position_offsets.data_ptr(),
+                        None if self.d_packed_mask is None else self.d_packed_mask.data_ptr(), self.mask_words)
+
+
+def paged_attention_bucket_workspace_size(pool: KVPool, meta: BucketMeta, num_q_heads: int) -> int:
+    pc, bc, kc = pool.c(), meta.c(), meta.bucket.c()
+    return int(lib().paged_attention_bucket_workspace_size(C.byref(pc), C.byref(bc), C.byref(kc), int(num_q_heads)))
+
+
+def paged_kv_append_rope_bucket(pool: KVPool, meta: BucketMeta, num_q_heads: int, q: torch.Tensor,
+                                k: torch.Tensor, v: torch.Tensor, q_out: torch.Tensor, rope_table: torch.Tensor,
+                                d_error: torch.Tensor, stream=None) -> None:
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_out", q_out)):
+        assert t.dtype == torch.bfloat16 and t.dim() == 2 and t.stride(1) == 1, name
+        assert t.shape[0] >= meta.bucket.max_tokens, name
+    assert rope_table.dtype == torch.float32 and rope_table.is_contiguous()
+    pc, bc, kc = pool.c(), meta.c(), meta.bucket.c()
+    code = lib().paged_kv_append_rope_bucket(
+        C.byref(pc), C.byref(bc), C.byref(kc), int(num_q_heads), _ptr(q), q.stride(0), _ptr(k), k.stride(0),
+        _ptr(v), v.stride(0), _ptr(q_out), q_out.stride(0), _ptr(rope_table), int(rope_table.shape[0]), None,
+        _ptr(d_error), _stream_ptr(stream))
+    _check(code, "paged_kv_append_rope_bucket")
+
+
+def paged_attention_forward_bucket(pool: KVPool, meta: BucketMeta, num_q_heads: int, q_rot: torch.Tensor,
+                                   out: torch.Tensor, softmax_scale: float, workspace: torch.Tensor,
+                                   d_error: torch.Tensor, stream=None) -> None:
+    assert q_rot.dtype == torch.bfloat16 and q_rot.stride(1) == 1
+    assert out.dtype == torch.bfloat16 and out.is_contiguous()
+    pc, bc, kc = pool.c(), meta.c(), meta.bucket.c()
+    code = lib().paged_attention_forward_bucket(
+        C.byref(pc), C.byref(bc), C.byref(kc), int(num_q_heads), _ptr(q_rot), q_rot.stride(0), _ptr(out),
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(d_error),
+        _stream_ptr(stream))
+    _check(code, "paged_attention_forward_bucket")
+
+
+class PagedAttentionBucketStep:
+    """One layer step (append + attention) over a padding bucket, with every buffer -- metadata
+    included -- allocated once, so that the step can be captured into a CUDA graph once and
+    replayed for every batch of the bucket.
+
+    ``load(...)`` writes a batch into the fixed buffers (lengths, block table, draft-token arrays
+    and the q / k / v rows; outside any capture), ``__call__`` enqueues the step, ``capture()``
+    records it into a graph and ``replay()`` runs that graph.  Rows ``[0, num_tokens)`` of
+    ``out`` hold the loaded batch's result."""
+
+    def __init__(self, pool: KVPool, bucket: Bucket, num_q_heads: int, head_dim: int, rope_table: torch.Tensor,
+                 softmax_scale: float | None = None, draft: bool = False):
+        dev = pool.data.device
+        self.pool, self.bucket, self.Hq, self.D = pool, bucket, int(num_q_heads), int(head_dim)
+        self.Hkv = int(pool.data.shape[3])
+        self.rope_table = rope_table
+        self.softmax_scale = softmax_scale if softmax_scale is not None else head_dim ** -0.5
+        self.meta = BucketMeta(bucket, dev, draft)
+        T = bucket.max_tokens
+        self.q = torch.zeros(T, self.Hq * self.D, dtype=torch.bfloat16, device=dev)
+        self.k = torch.zeros(T, self.Hkv * self.D, dtype=torch.bfloat16, device=dev)
+        self.v = torch.zeros(T, self.Hkv * self.D, dtype=torch.bfloat16, device=dev)
+        self.q_out = torch.zeros(T, self.Hq * self.D, dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros(T, self.Hq * self.D, dtype=torch.bfloat16, device=dev)
+        ws = paged_attention_bucket_workspace_size(pool, self.meta, num_q_heads)
+        if ws == 0:
+            raise PagedKVError("paged_attention_bucket_workspace_size: invalid bucket")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.d_error = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.num_tokens = 0
+        self.graph = None
+
+    def load(self, request_types, context_lengths, past_kv_lengths, block_offsets, q, k, v,
+             position_offsets=None, packed_mask=None, stream=None) -> None:
+        """Writes one batch (context requests first, as always) into the bucket's slots: its
+        context requests into the first context slots, its generation requests into the first
+        generation slots, every other slot empty.  Checks on the host that it fits."""
+        bk = self.bucket
+        types = np.asarray(request_types, dtype=np.int32)
+        n = np.asarray(context_lengths, dtype=np.int32)
+        past = np.asarray(past_kv_lengths, dtype=np.int32)
+        tbl = np.asarray(block_offsets, dtype=np.int32).reshape(len(n), -1)
+        nc = int((types == PKV_REQ_CONTEXT).sum())
+        ng = len(n) - nc
+        if not (types[:nc] == PKV_REQ_CONTEXT).all():
+            raise PagedKVError("context requests must come first")
+        if nc > bk.context_slots or ng > bk.generation_slots:
+            raise PagedKVError("more requests than the bucket's slots")
+        T = int(n.sum())
+        if T > bk.max_tokens or int(n[:nc].sum()) > bk.max_context_tokens:
+            raise PagedKVError("more rows than the bucket holds")
+        if len(n) and (int((past + n).max()) > bk.max_kv_len or (ng and int(n[nc:].max()) > bk.max_gen_tokens)):
+            raise PagedKVError("a request exceeds the bucket's limits")
+        if tbl.shape[1] > bk.max_blocks_per_seq:
+            raise PagedKVError("block table wider than the bucket's")
+        R = bk.slots
+        sl_n = np.zeros(R, np.int32)
+        sl_p = np.zeros(R, np.int32)
+        sl_t = np.full((R, bk.max_blocks_per_seq), -1, np.int32)
+        slots = list(range(nc)) + list(range(bk.context_slots, bk.context_slots + ng))
+        sl_n[slots], sl_p[slots] = n, past
+        sl_t[slots, :tbl.shape[1]] = tbl
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self.meta.d_context_lengths.copy_(torch.from_numpy(sl_n), non_blocking=False)
+            self.meta.d_past_kv_lengths.copy_(torch.from_numpy(sl_p), non_blocking=False)
+            self.meta.d_block_offsets.copy_(torch.from_numpy(sl_t), non_blocking=False)
+            if self.meta.d_position_offsets is not None:
+                self.meta.d_position_offsets.zero_()
+                self.meta.d_packed_mask.zero_()
+                if position_offsets is not None:
+                    off = torch.from_numpy(np.ascontiguousarray(position_offsets, dtype=np.int32))
+                    self.meta.d_position_offsets[:off.numel()].copy_(off)
+                if packed_mask is not None:
+                    m = np.ascontiguousarray(packed_mask, dtype=np.uint32)
+                    mt = torch.from_numpy(m.view(np.int32))
+                    self.meta.d_packed_mask[:mt.shape[0], :mt.shape[1]].copy_(mt)
+            for dst, src in ((self.q, q), (self.k, k), (self.v, v)):
+                dst[:T].copy_(src[:T])
+        self.num_tokens = T
+
+    def __call__(self, stream=None) -> torch.Tensor:
+        paged_kv_append_rope_bucket(self.pool, self.meta, self.Hq, self.q, self.k, self.v, self.q_out,
+                                    self.rope_table, self.d_error, stream)
+        paged_attention_forward_bucket(self.pool, self.meta, self.Hq, self.q_out, self.out, self.softmax_scale,
+                                       self.workspace, self.d_error, stream)
+        return self.out
+
+    def capture(self) -> None:
+        """Records the step into a CUDA graph (after one uncaptured warm-up call)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self()
+        self.graph = g
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
         return self.out

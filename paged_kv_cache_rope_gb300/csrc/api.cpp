@@ -107,13 +107,20 @@ bool encode_raw8_map(CUtensorMap* map, const void* base, int D, int heads, int64
   return r == CUDA_SUCCESS;
 }
 
+// The launch plan.  Without a bucket every count is exact (from the host copies of the
+// lengths); with a bucket (dyn) every count is a capacity for the bucket's largest batch and the
+// device plan finds the actual counts.
 struct HostPlan {
   int R = 0, C = 0, G = 0, T = 0, ctx_tokens = 0, max_gen_tokens = 0;
+  int gen_rows = 0;                                  // rows of the generation requests
   int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
   int decode_nt = 1, num_items = 0, num_parts = 0;  // narrow decode n-tiles per CTA, CTAs per KV head, partial rows
   int num_witems = 0;                                // wide decode CTAs per KV head
   int num_titems = 0;                                // tensor-core generation CTAs per KV head
   bool tc_wide = false;                              // wide requests take the tensor-core kernel
+  bool staging = false;                              // 8-bit pool with context rows: stage their pages
+  bool dyn = false;                                  // bucket mode
+  int max_ctx_tokens = 0, max_kv_len = 0;            // bucket limits (dyn)
   pkv::PlanLayout lay{};
 };
 
@@ -179,9 +186,7 @@ int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPla
 // Decode split length (tokens, multiple of 16): about 4 CTAs per SM over the whole batch, each
 // CTA streaming at most PKV_DECODE_SPLIT_KB of K+V (1024 tokens of a bf16 head of 128 dims,
 // 2048 of an FP8 one), so per-CTA set-up is amortised over the same bytes for either dtype.
-int choose_kv_chunk(const pkv_pool* pool, const pkv_batch* b, int C) {
-  int64_t total = 0;
-  for (int r = C; r < b->num_requests; ++r) total += b->h_past_kv_lengths[r] + b->h_context_lengths[r];
+int choose_kv_chunk(const pkv_pool* pool, int64_t total) {
   const int64_t target = static_cast<int64_t>(device_sm_count()) * 4;
   int64_t chunk = (total * pool->num_kv_heads + target - 1) / std::max<int64_t>(target, 1);
   chunk = (chunk + 15) / 16 * 16;
@@ -190,40 +195,28 @@ int choose_kv_chunk(const pkv_pool* pool, const pkv_batch* b, int C) {
   return static_cast<int>(std::min<int64_t>(cap, std::max<int64_t>(64, chunk)));
 }
 
-void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
-  const bool staging = pool->dtype != PKV_BF16 && hp->C > 0;
-  hp->num_tiles = 0;
-  for (int r = 0; r < hp->C; ++r)
-    hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
-  hp->kv_chunk = choose_kv_chunk(pool, b, hp->C);
-  // decode score-tile columns are (token, query head) pairs of one KV head.  Requests with at
-  // most kDecodeNarrowMaxCols of them take the narrow kernel (8 or 16 columns per CTA, the
-  // split's tiles shared out among the warps).  Wider ones (draft tokens, large query groups)
-  // take the tensor-core kernel when a 128-row tile holds whole groups and the pool is bf16 or
-  // 8-bit at head_dim 128 (rows = pairs, 128 per CTA; splits of whole 128-key tiles), else the
-  // wide mma.sync kernel (64 columns per CTA, every warp over every tile), in as many column
-  // groups as needed.
-  const int group = Hq / pool->num_kv_heads;
-  int max_narrow = 0;
-  bool any_wide = false;
-  for (int r = hp->C; r < hp->R; ++r) {
-    const int cols_r = b->h_context_lengths[r] * group;
-    if (cols_r <= pkv::kDecodeNarrowMaxCols) max_narrow = std::max(max_narrow, cols_r);
-    else any_wide = true;
-  }
-  // the tensor-core generation mode: bf16 pools, and 8-bit pools at head_dim 128 (their codes
-  // are converted to f16 in shared memory)
-  hp->tc_wide = any_wide && group <= 128 && 128 % group == 0 && (pool->dtype == PKV_BF16 || pool->head_dim == 128);
 #ifndef PKV_TC_MIN_CHUNK
 #define PKV_TC_MIN_CHUNK 2048
 #endif
+
+// Decode routing and split length, from the generation requests' total KV tokens and the
+// widest narrow request.  Requests with at most kDecodeNarrowMaxCols (token, query head) columns
+// take the narrow kernel (8 or 16 columns per CTA, the split's tiles shared out among the warps).
+// Wider ones (draft tokens, large query groups) take the tensor-core kernel when a 128-row tile
+// holds whole groups and the pool is bf16 or 8-bit at head_dim 128 (rows = pairs, 128 per CTA;
+// splits of whole 128-key tiles), else the wide mma.sync kernel (64 columns per CTA, every warp
+// over every tile), in as many column groups as needed.
+void plan_decode_shape(const pkv_pool* pool, int32_t Hq, int64_t total, int max_narrow, bool any_wide, HostPlan* hp) {
+  const int group = Hq / pool->num_kv_heads;
+  hp->kv_chunk = choose_kv_chunk(pool, total);
+  // the tensor-core generation mode: bf16 pools, and 8-bit pools at head_dim 128 (their codes
+  // are converted to f16 in shared memory)
+  hp->tc_wide = any_wide && group <= 128 && 128 % group == 0 && (pool->dtype == PKV_BF16 || pool->head_dim == 128);
   if (hp->tc_wide) {
     // whole 128-key tiles per split, enough of them to amortise a CTA's set-up, and about two
     // waves of the (one-per-SM) tensor-core CTAs: a longer split costs nothing there while every
     // extra split adds partial rows and a combine pass (measured on 64 requests x 8 draft
     // tokens: no split at all ran the kernel as fast and saved the 17 us combine)
-    int64_t total = 0;
-    for (int r = hp->C; r < hp->R; ++r) total += b->h_past_kv_lengths[r] + b->h_context_lengths[r];
     const int64_t waves2 = 2LL * device_sm_count();
     const int64_t tc_chunk = (total * pool->num_kv_heads + waves2 - 1) / waves2;
     hp->kv_chunk = static_cast<int>(std::max<int64_t>(
@@ -231,6 +224,52 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
                               pkv::kTcChunkAlign));
   }
   hp->decode_nt = max_narrow > 8 ? 2 : 1;
+}
+
+// Workspace layout for the plan's counts and capacities (hp->lay.stage_pages set by the caller).
+void plan_layout(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
+  pkv::PlanLayout& L = hp->lay;
+  L.counts = 0;
+  L.cu_q = L.counts + pkv::kCntWords;
+  L.tile_prefix = L.cu_q + hp->R + 1;
+  L.split_prefix = L.tile_prefix + hp->C + 1;
+  L.item_prefix = L.split_prefix + hp->G + 1;
+  L.part_prefix = L.item_prefix + hp->G + 1;
+  L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
+  L.witem_map = L.item_map + 2LL * hp->num_items;
+  L.titem_map = L.witem_map + 2LL * hp->num_witems;
+  L.row_map = (L.titem_map + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
+  L.unit_info = L.row_map + 4LL * hp->gen_rows;                 // int4 entries: 16-byte aligned
+  L.stage_prefix = L.unit_info + 4LL * hp->num_tiles;
+  L.stage_tbl = L.stage_prefix + (hp->staging ? hp->C + 1 : 0);
+  L.int_words = L.stage_tbl + (hp->staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
+  const int64_t int_bytes = (L.int_words * 4 + 255) / 256 * 256;
+  const int64_t D = pool->head_dim;
+  L.part_o = int_bytes;
+  L.part_ml = L.part_o + (static_cast<int64_t>(hp->num_parts) * Hq * D * 4 + 255) / 256 * 256;
+  L.stage_pool = L.part_ml + (static_cast<int64_t>(hp->num_parts) * Hq * 2 * 4 + 255) / 256 * 256;
+  L.total_bytes = L.stage_pool + (L.stage_pages * 2 * pool->tokens_per_block * pool->num_kv_heads * D * 2 + 255) / 256 * 256;
+}
+
+// Exact plan from the host copies of the lengths.
+void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
+  hp->dyn = false;
+  hp->staging = pool->dtype != PKV_BF16 && hp->C > 0;
+  hp->gen_rows = hp->T - hp->ctx_tokens;
+  hp->num_tiles = 0;
+  for (int r = 0; r < hp->C; ++r)
+    hp->num_tiles += (b->h_context_lengths[r] + pkv::kCtxRowsPerCta - 1) / pkv::kCtxRowsPerCta;
+  const int group = Hq / pool->num_kv_heads;
+  int max_narrow = 0;
+  bool any_wide = false;
+  int64_t total = 0;
+  for (int r = hp->C; r < hp->R; ++r) {
+    const int cols_r = b->h_context_lengths[r] * group;
+    if (cols_r <= pkv::kDecodeNarrowMaxCols) max_narrow = std::max(max_narrow, cols_r);
+    else any_wide = true;
+    total += b->h_past_kv_lengths[r] + b->h_context_lengths[r];
+  }
+  plan_decode_shape(pool, Hq, total, max_narrow, any_wide, hp);
   const int cols = 8 * hp->decode_nt;
   hp->num_splits = hp->max_splits = hp->num_items = hp->num_witems = hp->num_titems = hp->num_parts = 0;
   for (int r = hp->C; r < hp->R; ++r) {
@@ -243,31 +282,70 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
     hp->num_parts += s * n;
     hp->max_splits = std::max(hp->max_splits, s);
   }
-  pkv::PlanLayout& L = hp->lay;
-  L.cu_q = 0;
-  L.tile_prefix = L.cu_q + hp->R + 1;
-  L.split_prefix = L.tile_prefix + hp->C + 1;
-  L.item_prefix = L.split_prefix + hp->G + 1;
-  L.part_prefix = L.item_prefix + hp->G + 1;
-  L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
-  L.witem_map = L.item_map + 2LL * hp->num_items;
-  L.titem_map = L.witem_map + 2LL * hp->num_witems;
-  L.row_map = (L.titem_map + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
-  L.unit_info = L.row_map + 4LL * (hp->T - hp->ctx_tokens);  // int4 entries: 16-byte aligned
-  L.stage_prefix = L.unit_info + 4LL * hp->num_tiles;
-  L.stage_tbl = L.stage_prefix + (staging ? hp->C + 1 : 0);
-  L.int_words = L.stage_tbl + (staging ? static_cast<int64_t>(hp->C) * b->max_blocks_per_seq : 0);
-  L.stage_pages = 0;
-  if (staging)
+  hp->lay.stage_pages = 0;
+  if (hp->staging)
     for (int r = 0; r < hp->C; ++r)
-      L.stage_pages += (b->h_past_kv_lengths[r] + b->h_context_lengths[r] + pool->tokens_per_block - 1) /
-                       pool->tokens_per_block;
-  const int64_t int_bytes = (L.int_words * 4 + 255) / 256 * 256;
-  const int64_t D = pool->head_dim;
-  L.part_o = int_bytes;
-  L.part_ml = L.part_o + (static_cast<int64_t>(hp->num_parts) * Hq * D * 4 + 255) / 256 * 256;
-  L.stage_pool = L.part_ml + (static_cast<int64_t>(hp->num_parts) * Hq * 2 * 4 + 255) / 256 * 256;
-  L.total_bytes = L.stage_pool + (L.stage_pages * 2 * pool->tokens_per_block * pool->num_kv_heads * D * 2 + 255) / 256 * 256;
+      hp->lay.stage_pages += (b->h_past_kv_lengths[r] + b->h_context_lengths[r] + pool->tokens_per_block - 1) /
+                             pool->tokens_per_block;
+  plan_layout(pool, b, Hq, hp);
+}
+
+// Checks a bucket call's slot layout and limits (no lengths are read on the host).
+int validate_bucket(const pkv_pool* pool, const pkv_batch* b, const pkv_bucket* bk, int32_t Hq, HostPlan* hp) {
+  if (!b || !bk) return PKV_ERR_INVALID_ARGUMENT;
+  if (Hq <= 0 || Hq % pool->num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
+  const int R = b->num_requests, C = b->num_contexts, T = b->num_tokens;
+  if (R < 0 || C < 0 || C > R || T < 0) return PKV_ERR_INVALID_ARGUMENT;
+  hp->R = R;
+  hp->C = C;
+  hp->G = R - C;
+  hp->T = T;
+  if (R == 0 || T == 0) return PKV_OK;
+  if (b->max_blocks_per_seq <= 0 || !b->d_context_lengths || !b->d_past_kv_lengths || !b->d_block_offsets)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (bk->max_kv_len < 1 || bk->max_context_tokens < 0 || bk->max_context_tokens > T) return PKV_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(bk->max_kv_len) > static_cast<int64_t>(b->max_blocks_per_seq) * pool->tokens_per_block ||
+      bk->max_kv_len > INT32_MAX / 2)
+    return PKV_ERR_CAPACITY;
+  if (hp->G > 0 && (bk->max_gen_tokens < 1 || bk->max_gen_tokens > PKV_MAX_GEN_TOKENS)) return PKV_ERR_BATCH_ORDER;
+  const int max_gen = hp->G > 0 ? bk->max_gen_tokens : 0;
+  if (b->d_packed_mask && (b->mask_words <= 0 || 32LL * b->mask_words < max_gen)) return PKV_ERR_INVALID_ARGUMENT;
+  hp->dyn = true;
+  hp->max_ctx_tokens = C > 0 ? bk->max_context_tokens : 0;
+  hp->max_kv_len = bk->max_kv_len;
+  hp->max_gen_tokens = max_gen;
+  return PKV_OK;
+}
+
+// Capacities for the largest batch a bucket admits.  Context units: sum_r ceil(n_r / 256) is at
+// most floor(rows / 256) + (context slots).  Generation: at most min(T, G * max_gen) rows, each
+// slot at most ceil(max_kv_len / kv_chunk) splits of one column group (narrow) or
+// ceil(max_gen * g / columns per CTA) groups (wide / tensor-core).
+void plan_attention_bucket(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan* hp) {
+  const int group = Hq / pool->num_kv_heads;
+  hp->staging = pool->dtype != PKV_BF16 && hp->max_ctx_tokens > 0;
+  hp->num_tiles = hp->max_ctx_tokens > 0 ? hp->max_ctx_tokens / pkv::kCtxRowsPerCta + hp->C : 0;
+  hp->ctx_tokens = hp->max_ctx_tokens;
+  hp->gen_rows = static_cast<int>(std::min<int64_t>(hp->T, static_cast<int64_t>(hp->G) * hp->max_gen_tokens));
+  int max_narrow = 0;
+  for (int n = 1; n <= hp->max_gen_tokens; ++n)
+    if (n * group <= pkv::kDecodeNarrowMaxCols) max_narrow = n * group;
+  const bool any_wide = hp->G > 0 && hp->max_gen_tokens * group > pkv::kDecodeNarrowMaxCols;
+  plan_decode_shape(pool, Hq, static_cast<int64_t>(hp->G) * hp->max_kv_len, max_narrow, any_wide, hp);
+  const int s_max = hp->G > 0 ? (hp->max_kv_len + hp->kv_chunk - 1) / hp->kv_chunk : 0;
+  const int wide_cols = hp->max_gen_tokens * group;
+  hp->num_splits = hp->G * s_max;
+  hp->max_splits = s_max;
+  hp->num_items = (hp->G > 0 && group <= pkv::kDecodeNarrowMaxCols) ? hp->G * s_max : 0;
+  hp->num_witems = (any_wide && !hp->tc_wide)
+                       ? hp->G * s_max * ((wide_cols + pkv::kDecodeWideCols - 1) / pkv::kDecodeWideCols)
+                       : 0;
+  hp->num_titems = hp->tc_wide ? hp->G * s_max * ((wide_cols + pkv::kCtxTileM - 1) / pkv::kCtxTileM) : 0;
+  hp->num_parts = s_max * hp->gen_rows;
+  hp->lay.stage_pages =
+      hp->staging ? static_cast<int64_t>(hp->C) * ((hp->max_kv_len + pool->tokens_per_block - 1) / pool->tokens_per_block)
+                  : 0;
+  plan_layout(pool, b, Hq, hp);
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
@@ -329,77 +407,12 @@ struct AuxJoin {
   ~AuxJoin() { join(); }
 };
 
-}  // namespace
-
-extern "C" {
-
-const char* paged_kv_status_string(int status) {
-  switch (status) {
-    case PKV_OK: return "ok";
-    case PKV_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case PKV_ERR_UNSUPPORTED: return "unsupported geometry or dtype";
-    case PKV_ERR_BATCH_ORDER: return "batch order: context requests must come first, generation requests have one token";
-    case PKV_ERR_CAPACITY: return "sequence exceeds block table or RoPE table capacity";
-    case PKV_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
-    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
-    case PKV_ERR_CUDA: return "CUDA runtime or driver call failed";
-    default: return "unknown status";
-  }
-}
-
-int32_t paged_kv_last_launch_count(void) { return g_last_launches; }
-
-const char* paged_kv_last_launch_name(int32_t i) {
-  return (i >= 0 && i < g_last_launches && i < 8) ? g_last_names[i] : nullptr;
-}
-
-int paged_kv_set_kernel_events(void* const* events, int32_t max_kernels) {
-  if (events && max_kernels <= 0) return PKV_ERR_INVALID_ARGUMENT;
-  g_events = events;
-  g_events_n = events ? max_kernels : 0;
-  return PKV_OK;
-}
-
-size_t paged_rope_table_bytes(int32_t head_dim, int32_t max_pos) {
-  if (head_dim <= 0 || max_pos <= 0) return 0;
-  return static_cast<size_t>(max_pos) * static_cast<size_t>(head_dim) * sizeof(float);
-}
-
-int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float* h_table) {
-  if (!h_table || head_dim <= 0 || (head_dim & 1) || max_pos <= 0 || !(base > 0.0)) return PKV_ERR_INVALID_ARGUMENT;
-  const int half = head_dim / 2;
-  std::vector<double> theta(half);
-  for (int j = 0; j < half; ++j) theta[j] = std::pow(base, -(2.0 * static_cast<double>(j)) / static_cast<double>(head_dim));
-  for (int64_t p = 0; p < max_pos; ++p) {
-    float* row = h_table + p * head_dim;
-    for (int j = 0; j < half; ++j) {
-      const double a = static_cast<double>(p) * theta[j];
-      row[2 * j] = static_cast<float>(std::cos(a));
-      row[2 * j + 1] = static_cast<float>(std::sin(a));
-    }
-  }
-  return PKV_OK;
-}
-
-int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q,
-                         int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
-                         int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
-                         int32_t max_pos, int32_t* d_error, pkv_stream_t stream) {
-  return paged_kv_append_rope_ex(pool, batch, num_q_heads, q, q_row_stride, k, k_row_stride, v, v_row_stride,
-                                 q_out, q_out_row_stride, rope_table, max_pos, nullptr, d_error, stream);
-}
-
-int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q,
-                            int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
-                            int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
-                            int32_t max_pos, const pkv_append_opts* opts, int32_t* d_error, pkv_stream_t stream) {
-  g_last_launches = 0;
-  int st = validate_pool(pool);
-  if (st) return st;
-  HostPlan hp;
-  st = validate_batch(pool, batch, num_q_heads, &hp);
-  if (st) return st;
-  if (hp.T == 0) return PKV_OK;
+// The append's argument checks and launch, shared by the exact and the bucket entry points
+// (hp.T is the rows' count or capacity; the lengths themselves are only read on the device).
+int append_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& hp, int32_t num_q_heads, const void* q,
+                int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                void* q_out, int64_t q_out_row_stride, const float* rope_table, int32_t max_pos,
+                const pkv_append_opts* opts, int32_t* d_error, pkv_stream_t stream) {
   const int D = pool->head_dim, Hkv = pool->num_kv_heads;
   if (!q || !k || !v || !q_out || !rope_table || max_pos <= 0) return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(rope_table))
@@ -409,8 +422,6 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
       k_row_stride < static_cast<int64_t>(Hkv) * D || v_row_stride < static_cast<int64_t>(Hkv) * D)
     return PKV_ERR_INVALID_ARGUMENT;
   if (q_out == q && q_out_row_stride != q_row_stride) return PKV_ERR_INVALID_ARGUMENT;
-  for (int r = 0; r < hp.R; ++r)
-    if (static_cast<int64_t>(batch->h_past_kv_lengths[r]) + batch->h_context_lengths[r] > max_pos) return PKV_ERR_CAPACITY;
   if (hp.R > 12000) return PKV_ERR_UNSUPPORTED;  // in-CTA prefix scan keeps R + 1 ints in shared memory
   const int style = opts ? opts->rope_style : PKV_ROPE_NEOX;
   const int rot = (opts && opts->rotary_dim) ? opts->rotary_dim : D;
@@ -423,7 +434,9 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
 
   pkv::AppendParams p{};
   p.R = hp.R;
+  p.C = hp.C;
   p.T = hp.T;
+  p.dyn = hp.dyn ? 1 : 0;
   p.Hq = num_q_heads;
   p.Hkv = Hkv;
   p.D = D;
@@ -451,7 +464,6 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
   p.past = batch->d_past_kv_lengths;
   p.tbl = batch->d_block_offsets;
   p.pos_off = batch->d_position_offsets;
-  p.gen_row0 = hp.ctx_tokens;
   p.d_error = d_error;
   reset_names();
   cudaError_t e;
@@ -463,31 +475,18 @@ int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_
   return cuda_status(e);
 }
 
-size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads) {
-  if (validate_pool(pool)) return 0;
-  HostPlan hp;
-  if (validate_batch(pool, batch, num_q_heads, &hp)) return 0;
-  plan_attention(pool, batch, num_q_heads, &hp);
-  return static_cast<size_t>(hp.lay.total_bytes);
-}
-
-int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q_rot,
-                            int64_t q_row_stride, void* out, float softmax_scale, void* workspace,
-                            size_t workspace_bytes, int32_t* d_error, pkv_stream_t stream) {
-  g_last_launches = 0;
-  int st = validate_pool(pool);
-  if (st) return st;
-  HostPlan hp;
-  st = validate_batch(pool, batch, num_q_heads, &hp);
-  if (st) return st;
-  if (hp.T == 0) return PKV_OK;
+// The attention's argument checks and launches, shared by the exact and the bucket entry
+// points: every grid comes from the plan's counts (exact) or capacities (bucket); the kernels
+// read the device plan's counts and skip what this batch does not use.
+int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& hp, int32_t num_q_heads,
+                 const void* q_rot, int64_t q_row_stride, void* out, float softmax_scale, void* workspace,
+                 size_t workspace_bytes, int32_t* d_error, pkv_stream_t stream) {
   const int D = pool->head_dim, Hkv = pool->num_kv_heads;
   if (!q_rot || !out) return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q_rot) || !aligned16(out) || (q_row_stride & 7)) return PKV_ERR_ALIGNMENT;
   if (q_row_stride < static_cast<int64_t>(num_q_heads) * D) return PKV_ERR_INVALID_ARGUMENT;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARGUMENT;
   const bool q8 = pool->dtype != PKV_BF16;  // 8-bit codes with one pool scale
-  plan_attention(pool, batch, num_q_heads, &hp);
   if (!workspace || workspace_bytes < static_cast<size_t>(hp.lay.total_bytes)) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -504,16 +503,20 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   pp.Hq = num_q_heads;
   pp.group = num_q_heads / Hkv;
   pp.cols_per_cta = 8 * hp.decode_nt;
-  pp.expect_items = hp.num_items;
-  pp.expect_parts = hp.num_parts;
-  pp.expect_witems = hp.num_witems;
-  pp.expect_titems = hp.num_titems;
+  pp.cap_items = hp.num_items;
+  pp.cap_parts = hp.num_parts;
+  pp.cap_witems = hp.num_witems;
+  pp.cap_titems = hp.num_titems;
   pp.tc_wide = hp.tc_wide ? 1 : 0;
-  pp.gen_row0 = hp.ctx_tokens;
-  pp.gen_rows = hp.T - hp.ctx_tokens;
-  pp.expect_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
-  pp.expect_tiles = hp.num_tiles;
-  pp.expect_splits = hp.num_splits;
+  pp.staging = hp.staging ? 1 : 0;
+  pp.gen_rows = hp.gen_rows;
+  pp.dyn = hp.dyn ? 1 : 0;
+  pp.max_ctx_tokens = hp.max_ctx_tokens;
+  pp.max_kv_len = hp.max_kv_len;
+  pp.max_gen_tokens = hp.max_gen_tokens;
+  pp.cap_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
+  pp.cap_tiles = hp.num_tiles;
+  pp.cap_splits = hp.num_splits;
   pp.kv_chunk = hp.kv_chunk;
   pp.ctx_len = batch->d_context_lengths;
   pp.past = batch->d_past_kv_lengths;
@@ -533,7 +536,10 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   // generation work on the auxiliary stream when a context kernel runs beside it; while the
   // caller has per-kernel timing events set, every kernel stays on `stream` so that each pair
   // of events brackets one kernel's own work
-  AuxStream* aux = (hp.C > 0 && hp.G > 0 && !g_events) ? aux_stream_for_current_device(s) : nullptr;
+  const bool has_ctx = hp.num_tiles > 0;
+  const bool has_gen = hp.num_items + hp.num_witems + hp.num_titems > 0;
+  const int32_t* counts = ws + hp.lay.counts;
+  AuxStream* aux = (has_ctx && has_gen && !g_events) ? aux_stream_for_current_device(s) : nullptr;
   std::unique_lock<std::mutex> aux_hold;
   const cudaStream_t cs = s;  // context kernels
   cudaStream_t gs = s;        // generation kernels
@@ -545,7 +551,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   }
   AuxJoin aux_join{aux, s};
 
-  if (hp.C > 0) {
+  if (has_ctx) {
     // 8-bit pools: stage the context requests' pages as bf16 first (exact values, own table)
     const void* ctx_pool = pool->pool;
     const int32_t* ctx_tbl = batch->d_block_offsets;
@@ -568,6 +574,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       sp.pool = static_cast<const uint8_t*>(pool->pool);
       sp.stage_pool = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + hp.lay.stage_pool);
       sp.d_error = d_error;
+      sp.counts = counts;
       {
         LaunchScope ls(launches, "stage_q8", cs);
         e = pkv::launch_stage_q8(sp, cs);
@@ -598,6 +605,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     cp.NB = static_cast<int32_t>(ctx_blocks);
     cp.max_blocks = batch->max_blocks_per_seq;
     cp.num_tiles = hp.num_tiles;
+    cp.counts = counts;
     cp.cu_q = ws + hp.lay.cu_q;
     cp.tile_prefix = ws + hp.lay.tile_prefix;
     cp.unit_info = reinterpret_cast<const int4*>(ws + hp.lay.unit_info);
@@ -618,7 +626,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     ++launches;
   }
 
-  if (hp.G > 0) {
+  if (has_gen) {
     pkv::DecodeParams dp{};
     dp.C = hp.C;
     dp.G = hp.G;
@@ -630,8 +638,8 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
     dp.NB = pool->num_blocks;
     dp.max_blocks = batch->max_blocks_per_seq;
     dp.kv_chunk = hp.kv_chunk;
-    dp.gen_row0 = hp.ctx_tokens;
-    dp.gen_rows = hp.T - hp.ctx_tokens;
+    dp.gen_rows = hp.gen_rows;
+    dp.counts = counts;
     dp.total_items = hp.num_items;
     dp.total_witems = hp.num_witems;
     dp.total_parts = hp.num_parts;
@@ -706,7 +714,7 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
       tp.kv_dtype = pool->dtype;
       tp.d_error = d_error;
       tp.G = hp.G;
-      tp.gen_row0 = hp.ctx_tokens;
+      tp.counts = counts;
       tp.kv_chunk = hp.kv_chunk;
       tp.num_titems = hp.num_titems;
       tp.total_parts = hp.num_parts;
@@ -736,6 +744,149 @@ int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_
   if (!aux_join.join()) return PKV_ERR_CUDA;  // later work on the caller's stream sees every row
   g_last_launches = launches;
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* paged_kv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported geometry or dtype";
+    case PKV_ERR_BATCH_ORDER: return "batch order: context requests must come first, generation requests have one token";
+    case PKV_ERR_CAPACITY: return "sequence exceeds block table or RoPE table capacity";
+    case PKV_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t paged_kv_last_launch_count(void) { return g_last_launches; }
+
+const char* paged_kv_last_launch_name(int32_t i) {
+  return (i >= 0 && i < g_last_launches && i < 8) ? g_last_names[i] : nullptr;
+}
+
+int paged_kv_set_kernel_events(void* const* events, int32_t max_kernels) {
+  if (events && max_kernels <= 0) return PKV_ERR_INVALID_ARGUMENT;
+  g_events = events;
+  g_events_n = events ? max_kernels : 0;
+  return PKV_OK;
+}
+
+size_t paged_rope_table_bytes(int32_t head_dim, int32_t max_pos) {
+  if (head_dim <= 0 || max_pos <= 0) return 0;
+  return static_cast<size_t>(max_pos) * static_cast<size_t>(head_dim) * sizeof(float);
+}
+
+int paged_rope_table_build(double base, int32_t head_dim, int32_t max_pos, float* h_table) {
+  if (!h_table || head_dim <= 0 || (head_dim & 1) || max_pos <= 0 || !(base > 0.0)) return PKV_ERR_INVALID_ARGUMENT;
+  const int half = head_dim / 2;
+  std::vector<double> theta(half);
+  for (int j = 0; j < half; ++j) theta[j] = std::pow(base, -(2.0 * static_cast<double>(j)) / static_cast<double>(head_dim));
+  for (int64_t p = 0; p < max_pos; ++p) {
+    float* row = h_table + p * head_dim;
+    for (int j = 0; j < half; ++j) {
+      const double a = static_cast<double>(p) * theta[j];
+      row[2 * j] = static_cast<float>(std::cos(a));
+      row[2 * j + 1] = static_cast<float>(std::sin(a));
+    }
+  }
+  return PKV_OK;
+}
+
+int paged_kv_append_rope(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q,
+                         int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                         int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
+                         int32_t max_pos, int32_t* d_error, pkv_stream_t stream) {
+  return paged_kv_append_rope_ex(pool, batch, num_q_heads, q, q_row_stride, k, k_row_stride, v, v_row_stride,
+                                 q_out, q_out_row_stride, rope_table, max_pos, nullptr, d_error, stream);
+}
+
+int paged_kv_append_rope_ex(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q,
+                            int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                            int64_t v_row_stride, void* q_out, int64_t q_out_row_stride, const float* rope_table,
+                            int32_t max_pos, const pkv_append_opts* opts, int32_t* d_error, pkv_stream_t stream) {
+  g_last_launches = 0;
+  int st = validate_pool(pool);
+  if (st) return st;
+  HostPlan hp;
+  st = validate_batch(pool, batch, num_q_heads, &hp);
+  if (st) return st;
+  if (hp.T == 0) return PKV_OK;
+  for (int r = 0; r < hp.R; ++r)
+    if (static_cast<int64_t>(batch->h_past_kv_lengths[r]) + batch->h_context_lengths[r] > max_pos) return PKV_ERR_CAPACITY;
+  return append_impl(pool, batch, hp, num_q_heads, q, q_row_stride, k, k_row_stride, v, v_row_stride, q_out,
+                     q_out_row_stride, rope_table, max_pos, opts, d_error, stream);
+}
+
+int paged_kv_append_rope_bucket(const pkv_pool* pool, const pkv_batch* batch, const pkv_bucket* bucket,
+                                int32_t num_q_heads, const void* q, int64_t q_row_stride, const void* k,
+                                int64_t k_row_stride, const void* v, int64_t v_row_stride, void* q_out,
+                                int64_t q_out_row_stride, const float* rope_table, int32_t max_pos,
+                                const pkv_append_opts* opts, int32_t* d_error, pkv_stream_t stream) {
+  g_last_launches = 0;
+  int st = validate_pool(pool);
+  if (st) return st;
+  HostPlan hp;
+  st = validate_bucket(pool, batch, bucket, num_q_heads, &hp);
+  if (st) return st;
+  if (hp.T == 0 || hp.R == 0) return PKV_OK;
+  if (max_pos < bucket->max_kv_len) return PKV_ERR_CAPACITY;  // every position of the bucket has a table row
+  return append_impl(pool, batch, hp, num_q_heads, q, q_row_stride, k, k_row_stride, v, v_row_stride, q_out,
+                     q_out_row_stride, rope_table, max_pos, opts, d_error, stream);
+}
+
+size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads) {
+  if (validate_pool(pool)) return 0;
+  HostPlan hp;
+  if (validate_batch(pool, batch, num_q_heads, &hp)) return 0;
+  plan_attention(pool, batch, num_q_heads, &hp);
+  return static_cast<size_t>(hp.lay.total_bytes);
+}
+
+int paged_attention_forward(const pkv_pool* pool, const pkv_batch* batch, int32_t num_q_heads, const void* q_rot,
+                            int64_t q_row_stride, void* out, float softmax_scale, void* workspace,
+                            size_t workspace_bytes, int32_t* d_error, pkv_stream_t stream) {
+  g_last_launches = 0;
+  int st = validate_pool(pool);
+  if (st) return st;
+  HostPlan hp;
+  st = validate_batch(pool, batch, num_q_heads, &hp);
+  if (st) return st;
+  if (hp.T == 0) return PKV_OK;
+  plan_attention(pool, batch, num_q_heads, &hp);
+  return forward_impl(pool, batch, hp, num_q_heads, q_rot, q_row_stride, out, softmax_scale, workspace,
+                      workspace_bytes, d_error, stream);
+}
+
+size_t paged_attention_bucket_workspace_size(const pkv_pool* pool, const pkv_batch* batch, const pkv_bucket* bucket,
+                                             int32_t num_q_heads) {
+  if (validate_pool(pool)) return 0;
+  HostPlan hp;
+  if (validate_bucket(pool, batch, bucket, num_q_heads, &hp)) return 0;
+  if (hp.R == 0 || hp.T == 0) return 256;
+  plan_attention_bucket(pool, batch, num_q_heads, &hp);
+  return static_cast<size_t>(hp.lay.total_bytes);
+}
+
+int paged_attention_forward_bucket(const pkv_pool* pool, const pkv_batch* batch, const pkv_bucket* bucket,
+                                   int32_t num_q_heads, const void* q_rot, int64_t q_row_stride, void* out,
+                                   float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* d_error,
+                                   pkv_stream_t stream) {
+  g_last_launches = 0;
+  int st = validate_pool(pool);
+  if (st) return st;
+  HostPlan hp;
+  st = validate_bucket(pool, batch, bucket, num_q_heads, &hp);
+  if (st) return st;
+  if (hp.T == 0 || hp.R == 0) return PKV_OK;
+  plan_attention_bucket(pool, batch, num_q_heads, &hp);
+  return forward_impl(pool, batch, hp, num_q_heads, q_rot, q_row_stride, out, softmax_scale, workspace,
+                      workspace_bytes, d_error, stream);
 }
 
 }  // extern "C"

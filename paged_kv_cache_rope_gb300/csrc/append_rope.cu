@@ -104,9 +104,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
   pdl_wait();
   if (tid == 0) s_carry = 0;
   __syncthreads();
+  bool neg = false;
   for (int base = 0; base < p.R; base += kAppendThreads) {
     int r = base + tid;
     int x = r < p.R ? __ldg(p.ctx_len + r) : 0;
+    neg |= x < 0;
     int incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -133,11 +135,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
     __syncthreads();
   }
   if (tid == 0) s_cu[p.R] = s_carry;
-  __syncthreads();
-  if (s_cu[p.R] != p.T) {  // device lengths disagree with the host's token count
-    if (blockIdx.x == 0 && tid == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+  // Without a bucket the device lengths must add up to the host's token count; in a bucket
+  // (p.T = the rows' capacity) the batch may use fewer rows, never more, and empty slots
+  // (no new tokens) own no row
+  const bool bad = __syncthreads_or(neg) != 0 || (p.dyn ? s_cu[p.R] > p.T : s_cu[p.R] != p.T);
+  if (bad) {
+    if (blockIdx.x == 0 && tid == 0) flag_error(p.d_error, p.dyn ? PKV_DEVERR_BUCKET : PKV_DEVERR_PLAN_MISMATCH);
     return;
   }
+  const int T = s_cu[p.R];          // packed rows of this batch
+  const int gen_row0 = s_cu[p.C];   // first row of the generation requests
 
   // Each lane handles 16 elements of one head of one token: two groups of 8 (A and B) whose
   // place depends on the rope style; heads of a token are consecutive tasks, so the lanes of one
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
   const int D = p.D, per_head = D >> 4;
   const int rot_tasks = p.rot >> 4, rhalf = p.rot >> 1;
   const int tasks_per_token = (p.Hq + 2 * p.Hkv) * per_head;
-  const int total = p.T * tasks_per_token;  // < 2^31, checked on the host
+  const int total = T * tasks_per_token;  // < 2^31, checked on the host
   const int lph = 31 - __clz(per_head);      // per_head is 4 or 8
   const size_t esz = KVK != 0 ? 1 : 2;
   const int stride = gridDim.x * kAppendThreads;
@@ -166,8 +173,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendParam
     const int pos = past_r + (token - s_cu[r]);  // slot position
     int rpos = pos;                               // rotation position
     bool ok = active;
-    if (active && p.pos_off != nullptr && token >= p.gen_row0) {  // a draft token
-      const int off = __ldg(p.pos_off + (token - p.gen_row0));
+    if (active && p.pos_off != nullptr && token >= gen_row0) {  // a draft token
+      const int off = __ldg(p.pos_off + (token - gen_row0));
       if (off < 0 || off >= __ldg(p.ctx_len + r)) {
         flag_error(p.d_error, PKV_DEVERR_BAD_OFFSET);
         ok = false;

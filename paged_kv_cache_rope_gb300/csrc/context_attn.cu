@@ -197,10 +197,16 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   // 256 rows); rows are the (token i, query head hk*g + hl) pairs r = i*g + hl of the request's
   // new tokens, keys kt0 .. kend-1 of the split, visibility per draft-token mask; partial
   // results go to the split workspace when the request has several splits.
-  int hq = 0, hk, r, past, L_r, nv0, nv1, nkt0, nkt1, kt0 = 0, kend, q_row = 0, i0 = 0;
+  int hq = 0, hk = 0, r = 0, past = 0, L_r = 0, nv0 = 0, nv1 = 0, nkt0 = 0, nkt1 = 0, kt0 = 0, kend = 0, q_row = 0,
+      i0 = 0;
   int gr = 0, n_new = 0, s_idx = 0, num_splits = 1, pr0 = 0, tok0 = 0;
-  bool item_ok;
-  if constexpr (!DEC) {
+  bool item_ok = false;
+  // the plan's counts: a CTA past this batch's share of the grid (a bucket's spare one) has no
+  // work and goes straight to the teardown
+  const bool idle = static_cast<int>(DEC ? blockIdx.x : blockIdx.y) >= __ldg(p.counts + (DEC ? kCntTitems : kCntUnits));
+  const int gen_row0 = DEC ? __ldg(p.counts + kCntGenRow0) : 0;
+  if (idle) {
+  } else if constexpr (!DEC) {
     hq = blockIdx.x;
     hk = hq / p.group;
     // the plan's descriptor of the unit, longest units first: (request, first q row,
@@ -246,10 +252,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     nkt1 = nk / 2;
     nv1 = nkt1 > 0 ? nv0 : 0;
     item_ok = im.y >= 0 && s_idx < num_splits && kt0 < kend && nv0 > 0 && n_new >= 1 &&
-              n_new <= PKV_MAX_GEN_TOKENS && tok0 >= p.gen_row0 && tok0 + n_new <= p.T &&
+              n_new <= PKV_MAX_GEN_TOKENS && tok0 >= gen_row0 && tok0 + n_new <= p.T &&
               static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(num_splits) * n_new <= p.total_parts;
   }
-  if (!item_ok && threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
+  if (!idle && !item_ok && threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
   const bool hasB = nv1 > 0;
   // KV tiles this CTA streams; the first user of the last V tile zeroes its tail
   const int nT = DEC ? nkt0 + nkt1 : (hasB ? nkt1 : nkt0);
@@ -514,7 +520,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         tok_i = pr / p.group;
         hl = pr - tok_i * p.group;
         if (p.mask != nullptr) {
-          const uint32_t* mrow = p.mask + static_cast<int64_t>(tok0 + tok_i - p.gen_row0) * p.mask_words;
+          const uint32_t* mrow = p.mask + static_cast<int64_t>(tok0 + tok_i - gen_row0) * p.mask_words;
           vis = __ldg(mrow);
           if (n_new > 32 && p.mask_words > 1) vis |= static_cast<uint64_t>(__ldg(mrow + 1)) << 32;
           vis |= 1ull << tok_i;
@@ -904,6 +910,7 @@ template <bool I8>  // false: E4M3 codes, true: int8 codes
 __global__ void __launch_bounds__(kStageThreads) stage_q8_kernel(const StageParams p) {
   const int gp = blockIdx.x;  // staging page
   pdl_wait();
+  if (gp >= __ldg(p.counts + kCntStagePages)) return;  // past this batch's pages (a bucket's spare CTA)
   int lo = 0, hi = p.C - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;

@@ -97,7 +97,10 @@ __device__ __forceinline__ Int8v scan_chunk(const Int8v x, Int8v* s_warp, const 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ Int8v s_warp[kPlanThreads / 32];
   __shared__ Int8v s_carry;
+  __shared__ int32_t s_ctx_rows;
+  __shared__ int32_t s_units;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int32_t* counts = p.ws + p.lay.counts;
   int32_t* cu = p.ws + p.lay.cu_q;
   int32_t* tiles = p.ws + p.lay.tile_prefix;
   int32_t* splits = p.ws + p.lay.split_prefix;
@@ -108,28 +111,51 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   int2* witem_map = reinterpret_cast<int2*>(p.ws + p.lay.witem_map);
   int2* titem_map = reinterpret_cast<int2*>(p.ws + p.lay.titem_map);
   int32_t* stage = p.ws + p.lay.stage_prefix;
-  const bool staging = p.expect_stage_pages > 0;
+  const bool staging = p.staging != 0, dyn = p.dyn != 0;
   const int C = p.C, chunk = p.kv_chunk, cols = p.cols_per_cta;
   bool bad = false;
   pdl_wait();
   const int4 z4 = make_int4(0, 0, 0, 0);
-  if (tid == 0) s_carry = Int8v{z4, z4};
+  if (tid == 0) {
+    s_carry = Int8v{z4, z4};
+    s_ctx_rows = 0;
+  }
   __syncthreads();
+  // rows of the context requests: generation row k is packed row (context rows) + k
+  {
+    int part = 0;
+    for (int r = tid; r < C; r += kPlanThreads) part += max(__ldg(p.ctx_len + r), 0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0 && part) atomicAdd(&s_ctx_rows, part);
+  }
+  __syncthreads();
+  const int gen_row0 = s_ctx_rows;
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + tid;
-    // a: (new tokens, context units, generation splits, staged FP8 context pages)
+    // a: (new tokens, context units, generation splits, staged 8-bit context pages)
     // b: (narrow decode CTAs per KV head, partial-result rows, wide decode CTAs per KV head,
     //     tensor-core generation CTAs per KV head)
+    // Without a bucket every request has new tokens.  In a bucket a slot with none is empty,
+    // and a slot over the bucket's limits rejects the batch (treated as empty meanwhile).
     Int8v x{z4, z4};
     if (r < p.R) {
-      const int n = __ldg(p.ctx_len + r);
+      int n = __ldg(p.ctx_len + r);
+      const int past = __ldg(p.past + r);
+      bool bad_r;
+      if (dyn) {
+        bad_r = n < 0 || past < 0 || past > p.max_kv_len - n || (r >= C && n > p.max_gen_tokens);
+      } else {
+        bad_r = n < 1 || (r >= C && n > PKV_MAX_GEN_TOKENS);
+      }
+      bad |= bad_r;
+      if (bad_r) n = 0;
       x.a.x = n;
       if (r < C) {
         x.a.y = (n + kCtxRowsPerCta - 1) / kCtxRowsPerCta;
-        if (staging) x.a.w = (__ldg(p.past + r) + n + p.B - 1) / p.B;
-      } else {
-        bad |= n < 1 || n > PKV_MAX_GEN_TOKENS;
-        const int sr = (__ldg(p.past + r) + n + chunk - 1) / chunk, ncols = n * p.group;
+        if (staging && n > 0) x.a.w = (past + n + p.B - 1) / p.B;
+      } else if (n > 0) {
+        const int sr = (past + n + chunk - 1) / chunk, ncols = n * p.group;
         x.a.z = sr;
         if (ncols <= kDecodeNarrowMaxCols) x.b.x = sr * ((ncols + cols - 1) / cols);
         else if (p.tc_wide) x.b.w = sr * ((ncols + kCtxTileM - 1) / kCtxTileM);
@@ -148,12 +174,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         splits[gr] = ex.a.z;
         items[gr] = ex.b.x;
         parts[gr] = ex.b.y;
-        // direct maps for the decode CTAs and the combine rows (no searches there)
-        for (int it = 0; it < x.b.x && ex.b.x + it < p.expect_items; ++it) item_map[ex.b.x + it] = make_int2(gr, it);
-        for (int it = 0; it < x.b.z && ex.b.z + it < p.expect_witems; ++it) witem_map[ex.b.z + it] = make_int2(gr, it);
-        for (int it = 0; it < x.b.w && ex.b.w + it < p.expect_titems; ++it) titem_map[ex.b.w + it] = make_int2(gr, it);
+        // direct maps for the decode CTAs and the combine rows (no searches there); the
+        // capacities bound every write
+        for (int it = 0; it < x.b.x && ex.b.x + it < p.cap_items; ++it) item_map[ex.b.x + it] = make_int2(gr, it);
+        for (int it = 0; it < x.b.z && ex.b.z + it < p.cap_witems; ++it) witem_map[ex.b.z + it] = make_int2(gr, it);
+        for (int it = 0; it < x.b.w && ex.b.w + it < p.cap_titems; ++it) titem_map[ex.b.w + it] = make_int2(gr, it);
         for (int i = 0; i < x.a.x; ++i) {
-          const int row = ex.a.x + i - p.gen_row0;
+          const int row = ex.a.x + i - gen_row0;
           // (splits, partial row of split 0, rows between splits, token index)
           if (row >= 0 && row < p.gen_rows) row_map[row] = make_int4(x.a.z, ex.b.y + i, x.a.x, i);
         }
@@ -163,6 +190,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (tid == kPlanThreads - 1) s_carry = Int8v{add4(ex.a, x.a), add4(ex.b, x.b)};
     __syncthreads();
   }
+  bool bad_tot = false;
   if (tid == 0) {
     const Int8v t = s_carry;
     cu[p.R] = t.a.x;
@@ -171,28 +199,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     items[p.G] = t.b.x;
     parts[p.G] = t.b.y;
     if (staging) stage[C] = t.a.w;
-    bad |= (t.a.x != p.T) || (t.a.y != p.expect_tiles) || (t.a.z != p.expect_splits) ||
-           (t.b.x != p.expect_items) || (t.b.y != p.expect_parts) || (t.b.z != p.expect_witems) ||
-           (t.b.w != p.expect_titems) ||
-           (staging && t.a.w != p.expect_stage_pages);
+    const int gen_rows = t.a.x - gen_row0;
+    if (dyn) {  // the bucket's grids must hold this batch
+      bad_tot = t.a.x > p.T || gen_row0 > p.max_ctx_tokens || gen_rows > p.gen_rows || t.a.y > p.cap_tiles ||
+                t.a.z > p.cap_splits || t.b.x > p.cap_items || t.b.y > p.cap_parts || t.b.z > p.cap_witems ||
+                t.b.w > p.cap_titems || t.a.w > p.cap_stage_pages;
+    } else {  // the device lengths must give exactly what the host planned
+      bad_tot = t.a.x != p.T || gen_rows != p.gen_rows || t.a.y != p.cap_tiles || t.a.z != p.cap_splits ||
+                t.b.x != p.cap_items || t.b.y != p.cap_parts || t.b.z != p.cap_witems || t.b.w != p.cap_titems ||
+                (staging && t.a.w != p.cap_stage_pages);
+    }
+    s_units = t.a.y;
   }
-  if (bad) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);
+  const bool any_bad = __syncthreads_or(bad || bad_tot) != 0;
+  if (tid == 0) {
+    // the counts every later kernel of the call reads; a rejected batch runs nothing
+    const Int8v t = s_carry;
+    const int32_t v[kCntWords] = {t.a.x, gen_row0, t.a.x - gen_row0, t.a.y, t.b.x, t.b.z, t.b.w, t.b.y, t.a.w};
+#pragma unroll
+    for (int i = 0; i < kCntWords; ++i) counts[i] = any_bad ? 0 : v[i];
+    if (any_bad) flag_error(p.d_error, dyn ? PKV_DEVERR_BUCKET : PKV_DEVERR_PLAN_MISMATCH);
+  }
+  if (any_bad) return;
 
   // ---- context units, most KV tiles first: a counting sort by tile count (descending) ----
   // Each slot gets the unit's descriptor (request, first q row, past + first row, rows left), so
   // a context CTA reads one int4 instead of searching the tile prefix itself.
-  const int U = p.expect_tiles;
+  const int U = s_units;
   int4* order = reinterpret_cast<int4*>(p.ws + p.lay.unit_info);
-  if (__syncthreads_or(bad)) {  // lengths disagree with the host plan: empty units (rejected)
-    for (int u = tid; u < U; u += kPlanThreads) order[u] = make_int4(0, 0, 0, 0);
-    return;
-  }
   if (U <= 0) return;
   constexpr int kBins = 2048;  // units with more tiles share the top bin
   __shared__ int32_t s_hist[kBins];
   __shared__ int32_t s_part[kPlanThreads];
   for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
   __syncthreads();  // tiles[] (this block's global writes) and the zeroed histogram are visible
+  // the unit's request: the last slot whose unit prefix is <= u (an empty slot shares its
+  // prefix with the next slot, so the search lands on the slot that owns the unit)
   auto unit_desc = [&](int u) {
     int lo = 0, hi = C - 1;
     while (lo < hi) {
@@ -324,6 +366,9 @@ decode_splitkv_kernel(DecodeParams p) {
   constexpr int HNC = WIDE ? Cfg::kWarps * HN : HN;
   if (item >= (WIDE ? p.total_witems : p.total_items)) return;
   pdl_wait();
+  // the plan's counts: CTAs past this batch's share of the grid (a bucket's spare ones) exit
+  if (item >= __ldg(p.counts + (WIDE ? kCntWitems : kCntItems))) return;
+  const int gen_row0 = __ldg(p.counts + kCntGenRow0), gen_rows = __ldg(p.counts + kCntGenRows);
   const int2 im = (WIDE ? p.witem_map : p.item_map)[item];  // written by the plan kernel
   const int gr = min(max(im.x, 0), p.G - 1), r = p.C + gr, local = im.y;
   const int n_new = __ldg(p.new_len + r);
@@ -347,7 +392,7 @@ decode_splitkv_kernel(DecodeParams p) {
   const int wcol0 = col0 + (WIDE ? warp * HN : 0);  // this warp's first column
   const bool warp_cols = wcol0 < ncols;             // wide: a warp past the last pair only loads
   const int64_t part_row0 = static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new;
-  if (row0 < p.gen_row0 || row0 + n_new > p.gen_row0 + p.gen_rows || part_row0 + n_new > p.total_parts) {
+  if (row0 < gen_row0 || row0 + n_new > gen_row0 + gen_rows || part_row0 + n_new > p.total_parts) {
     if (threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // device lengths disagree
     return;
   }
@@ -364,7 +409,7 @@ decode_splitkv_kernel(DecodeParams p) {
       if (c < ncols) {
         const int i = c / p.group;
         if (p.mask != nullptr) {
-          const uint32_t* mrow = p.mask + static_cast<int64_t>(row0 + i - p.gen_row0) * p.mask_words;
+          const uint32_t* mrow = p.mask + static_cast<int64_t>(row0 + i - gen_row0) * p.mask_words;
           v = __ldg(mrow);
           if (n_new > 32 && p.mask_words > 1) v |= static_cast<uint64_t>(__ldg(mrow + 1)) << 32;
           v |= 1ull << i;
@@ -824,9 +869,9 @@ __global__ void __launch_bounds__(kCombinePairs * 32) combine_warp_kernel(Decode
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t pair = static_cast<int64_t>(blockIdx.x) * kCombinePairs + warp;
   pdl_wait();
-  if (pair >= static_cast<int64_t>(p.gen_rows) * p.Hq) return;
+  if (pair >= static_cast<int64_t>(__ldg(p.counts + kCntGenRows)) * p.Hq) return;  // this batch's rows only
   const int grow = static_cast<int>(pair / p.Hq), hq = static_cast<int>(pair - static_cast<int64_t>(grow) * p.Hq);
-  const int row = p.gen_row0 + grow;
+  const int row = __ldg(p.counts + kCntGenRow0) + grow;
   const int4 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
   const int S = rm.x, n_new = rm.z, i = rm.w;
   if (S <= 1) return;  // written directly by the decode kernel
@@ -869,7 +914,8 @@ __global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grow = blockIdx.x / p.Hq, hq = blockIdx.x - grow * p.Hq;  // generation row, query head
   pdl_wait();
-  const int row = p.gen_row0 + grow;
+  if (grow >= __ldg(p.counts + kCntGenRows)) return;  // this batch's rows only
+  const int row = __ldg(p.counts + kCntGenRow0) + grow;
   const int4 rm = p.row_map[grow];  // written by the plan kernel earlier on the stream
   const int S = rm.x, n_new = rm.z, i = rm.w;
   if (S <= 1) return;  // written directly by the decode kernel

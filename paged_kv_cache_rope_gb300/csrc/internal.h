@@ -20,8 +20,28 @@ constexpr int kDecodeNarrowMaxCols = 16;
 constexpr int kDecodeWideCols = 64;  // columns per wide-decode CTA (4 warps x 16)
 constexpr int kTcChunkAlign = 128;   // split length multiple when generation rows use the tensor-core kernel
 
+// Counts the plan kernel derives from the device lengths (int32 words at the front of the
+// workspace).  Every later kernel of the call reads them: a CTA whose index is at or past its
+// kernel's count exits at once.  Without a bucket the counts equal the host's (the grids are
+// sized exactly); with a bucket the grids are sized for the bucket's largest batch and the counts
+// say how much of each grid this step's batch uses.  A batch the plan rejects gets all-zero
+// counts, so nothing runs after the plan.
+enum PlanCount {
+  kCntTokens = 0,      // packed rows of the batch (sum of context_lengths)
+  kCntGenRow0 = 1,     // first packed row of the generation requests (= context rows)
+  kCntGenRows = 2,     // packed rows of the generation requests
+  kCntUnits = 3,       // context units (CTAs per query head of the context kernel)
+  kCntItems = 4,       // narrow decode CTAs per KV head
+  kCntWitems = 5,      // wide decode CTAs per KV head
+  kCntTitems = 6,      // tensor-core generation CTAs per KV head
+  kCntParts = 7,       // split-KV partial rows per query head
+  kCntStagePages = 8,  // 8-bit pools: staged context pages
+  kCntWords = 16
+};
+
 // Device-side plan written by plan_kernel into the front of the workspace (int32 words).
 struct PlanLayout {
+  int64_t counts;        // [kCntWords] PlanCount values
   int64_t cu_q;          // [R + 1]  exclusive prefix of context_lengths
   int64_t tile_prefix;   // [C + 1]  prefix of ceil(n_r / kCtxRowsPerCta) over context requests
   int64_t split_prefix;  // [G + 1]  prefix of S_r = ceil(L_r / kv_chunk) over generation requests
@@ -46,6 +66,8 @@ struct PlanLayout {
 
 struct AppendParams {
   int32_t R, T, Hq, Hkv, D, B, NB, max_blocks;
+  int32_t C;    // context requests (slots 0 .. C-1)
+  int32_t dyn;  // 1: bucket mode -- T is the rows' capacity, the batch may use fewer
   const uint16_t* q;
   int64_t q_stride;
   const uint16_t* k;
@@ -65,18 +87,24 @@ struct AppendParams {
   const int32_t* ctx_len;
   const int32_t* past;
   const int32_t* tbl;
-  const int32_t* pos_off;  // draft-token rotation offsets [T - gen_row0] or null
-  int32_t gen_row0;        // first packed row of the generation requests
+  const int32_t* pos_off;  // draft-token rotation offsets [generation rows] or null
   int32_t* d_error;
 };
 
+// Without a bucket (dyn = 0) the cap_* fields are the exact counts the host planned from its
+// copies of the lengths, and a device count that differs is a plan mismatch.  With a bucket
+// (dyn = 1) they are capacities: the grids' sizes for the bucket's largest batch.
 struct PlanParams {
-  int32_t R, C, G, T, Hkv, B, expect_tiles, expect_splits, kv_chunk, expect_stage_pages;
+  int32_t R, C, G, T, Hkv, B, cap_tiles, cap_splits, kv_chunk, cap_stage_pages;
   int32_t Hq, group;
   int32_t cols_per_cta;  // decode score-tile columns per CTA: (token, query head) pairs
-  int32_t expect_items, expect_parts, expect_witems, expect_titems;
-  int32_t tc_wide;             // wide requests run on the tensor-core kernel (bf16 pool, 128 % group == 0)
-  int32_t gen_row0, gen_rows;  // first packed row and number of rows of the generation requests
+  int32_t cap_items, cap_parts, cap_witems, cap_titems;
+  int32_t tc_wide;   // wide requests run on the tensor-core kernel (bf16 pool, 128 % group == 0)
+  int32_t staging;   // 8-bit pool with context requests: stage their pages
+  int32_t gen_rows;  // generation rows: exact (dyn = 0) or capacity (dyn = 1)
+  int32_t dyn;
+  // bucket limits (dyn = 1): a batch over any of them is rejected (PKV_DEVERR_BUCKET)
+  int32_t max_ctx_tokens, max_kv_len, max_gen_tokens;
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words
@@ -85,9 +113,10 @@ struct PlanParams {
 };
 
 struct DecodeParams {
-  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, gen_row0, total_items, total_witems;
-  int32_t gen_rows;         // packed rows of the generation requests (T - gen_row0)
+  int32_t C, G, Hq, Hkv, group, D, B, NB, max_blocks, kv_chunk, total_items, total_witems;
+  int32_t gen_rows;         // generation rows the combine grid covers (count or capacity)
   int32_t total_parts;      // partial-result rows the workspace holds (per query head)
+  const int32_t* counts;    // the plan's PlanCount words
   int32_t nt;               // n-tiles of 8 columns per decode CTA (1 or 2)
   const uint8_t* pool;
   float kv_scale;           // dequantisation multiplier (1 for bf16)
@@ -113,6 +142,7 @@ struct DecodeParams {
 
 struct ContextParams {
   int32_t C, T, Hq, Hkv, group, D, B, NB, max_blocks, num_tiles;
+  const int32_t* counts;    // the plan's PlanCount words
   const int32_t* cu_q;
   const int32_t* tile_prefix;
   const int4* unit_info;      // [num_tiles] context units in launch order: (request r, first
@@ -128,7 +158,7 @@ struct ContextParams {
   int32_t* d_error;
   // generation mode (wide generation requests on the tensor-core kernel): CTA = titem_map
   // entry (generation request, split x row group) x KV head
-  int32_t G, gen_row0, kv_chunk, num_titems, mask_words;
+  int32_t G, kv_chunk, num_titems, mask_words;
   int32_t kv_dtype;         // generation mode: pool element kind (pkv_dtype); 8-bit codes are
                             // converted to f16 in shared memory (head_dim 128 only)
   int64_t total_parts;
@@ -146,6 +176,7 @@ struct ContextParams {
 struct StageParams {
   int32_t C, B, Hkv, D, NB, max_blocks, total_pages;
   int32_t kv_dtype;  // PKV_FP8_E4M3 or PKV_INT8
+  const int32_t* counts;  // the plan's PlanCount words
   const int32_t* ctx_len;
   const int32_t* past;
   const int32_t* tbl;

@@ -106,3 +106,33 @@ def test_host_checks_draft_mask_words(L):
     assert L.paged_attention_workspace_size(C.byref(pool), C.byref(batch), 32) == 0
     batch.mask_words = 2
     assert L.paged_attention_workspace_size(C.byref(pool), C.byref(batch), 32) > 0
+
+
+def _bucket_descs(C_slots=2, G_slots=6, T=600, mb=16, B=64, dtype=pk.PKV_BF16):
+    pool = pk.PkvPool(0x1000, dtype, 256, B, 8, 128, 1.0, 1.0)
+    batch = pk.PkvBatch(C_slots + G_slots, C_slots, T, mb, None, None, None, 0x2000, 0x3000, 0x4000)
+    return pool, batch
+
+
+def test_bucket_host_checks(L):
+    """Bucket calls read no host lengths (NULL host arrays are fine); the host checks the slot
+    layout and the bucket's limits against the block table, the RoPE table and the draft cap."""
+    pool, batch = _bucket_descs()
+    ok = pk.PkvBucket(512, 1000, 1)
+    assert L.paged_attention_bucket_workspace_size(C.byref(pool), C.byref(batch), C.byref(ok), 32) > 0
+
+    def fwd(bk, Hq=32):
+        return L.paged_attention_forward_bucket(C.byref(pool), C.byref(batch), C.byref(bk), Hq, 0x10000, Hq * 128,
+                                                0x20000, C.c_float(0.088), 0x30000, 1 << 30, 0x5000, None)
+    assert fwd(pk.PkvBucket(512, 16 * 64 + 1, 1)) == -4   # past + new beyond the block table
+    assert fwd(pk.PkvBucket(601, 1000, 1)) == -1          # more context rows than rows
+    assert fwd(pk.PkvBucket(512, 1000, 65)) == -3         # beyond 64 draft tokens
+    assert fwd(pk.PkvBucket(512, 1000, 0)) == -3          # generation slots need >= 1 token
+    assert fwd(ok, Hq=12) == -2
+    small = L.paged_attention_bucket_workspace_size(C.byref(pool), C.byref(batch), C.byref(ok), 32)
+    assert L.paged_attention_forward_bucket(C.byref(pool), C.byref(batch), C.byref(ok), 32, 0x10000, 32 * 128,
+                                            0x20000, C.c_float(0.088), 0x30000, small - 256, 0x5000, None) == -6
+    code = L.paged_kv_append_rope_bucket(C.byref(pool), C.byref(batch), C.byref(ok), 32, 0x10000, 32 * 128,
+                                         0x20000, 8 * 128, 0x30000, 8 * 128, 0x10000, 32 * 128, 0x40000, 999,
+                                         None, 0x5000, None)
+    assert code == -4                                     # the RoPE table must cover max_kv_len
