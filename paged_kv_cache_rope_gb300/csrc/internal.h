@@ -68,6 +68,8 @@ struct AppendParams {
   int32_t R, T, Hq, Hkv, D, B, NB, max_blocks;
   int32_t C;    // context requests (slots 0 .. C-1)
   int32_t dyn;  // 1: bucket mode -- T is the rows' capacity, the batch may use fewer
+  int32_t stages;          // set by the launcher: depth of the shared-memory token ring
+  int32_t consumer_warps;  // set by the launcher: warps that process a token's tasks
   const uint16_t* q;
   int64_t q_stride;
   const uint16_t* k;
