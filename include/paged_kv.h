@@ -15,12 +15,14 @@
  * Conventions shared by every entry point
  *   - All pointers named d_* and all tensor pointers (q, k, v, q_out, out, pool, rope table,
  *     workspace, error word) are DEVICE pointers; h_* pointers are HOST pointers.
- *   - The caller owns every buffer.  The library allocates no device memory, keeps no state
- *     between calls other than cached device attributes and one auxiliary stream with two
- *     events per device (created on first use, see paged_attention_forward), and never
- *     synchronises a stream: each call only enqueues kernels and returns, and its effects are
- *     ordered on `stream` like one kernel's (same-stream FIFO ordering as in [NOTES] 五
- *     "完整的推理流程", 5.2 CPU/GPU Overlap).
+ *   - The caller owns every buffer.  The library allocates no device memory at run time and
+ *     keeps no state between calls other than cached device attributes, one auxiliary stream
+ *     with two events per device (created on first use, see paged_attention_forward) and --
+ *     for paged_attention_forward_noalloc only -- one file-scope device scratch buffer of
+ *     PKV_NOALLOC_SCRATCH_BYTES that exists on every GPU loading the library, with its address
+ *     cached per device.  No call synchronises a stream: each call only enqueues kernels and
+ *     returns, and its effects are ordered on `stream` like one kernel's (same-stream FIFO
+ *     ordering as in [NOTES] 五 "完整的推理流程", 5.2 CPU/GPU Overlap).
  *   - Return value: PKV_OK (0) or a negative PKV_ERR_* detected on the host before anything
  *     was enqueued.  Errors only the device can see (a page id outside [0, num_blocks), a
  *     bounded wait that ran out) are OR-ed as PKV_DEVERR_* bits into the caller's device int

@@ -96,6 +96,12 @@ def bf16_step(x: np.ndarray) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - 7)
 
 
+# Every max_err call of the running test, for the session's parity report (conftest prints
+# it): (test, plain max abs error, error as judged, elements that needed the allowance, elements).
+PARITY_LOG: list[tuple[str, float, float, int, int]] = []
+CURRENT_TEST = ""
+
+
 def max_err(gpu: np.ndarray, ref: np.ndarray, rows=None) -> float:
     """Max abs error of bf16 results against the fp64 oracle, read at the bf16 output's own
     resolution.  Where one bf16 step at the reference value is wider than the 1e-2 bar
@@ -111,4 +117,9 @@ def max_err(gpu: np.ndarray, ref: np.ndarray, rows=None) -> float:
     if not gpu.size:
         return 0.0
     allowance = np.maximum(0.0, bf16_step(ref) - BF16_TOL)
-    return float(np.max(np.abs(gpu - ref) - allowance))
+    diff = np.abs(gpu - ref)
+    judged = float(np.max(diff - allowance))
+    # elements over the plain 1e-2 bar that the allowance brought back under it
+    used = int(np.count_nonzero((diff > BF16_TOL) & (diff - allowance <= BF16_TOL)))
+    PARITY_LOG.append((CURRENT_TEST, float(np.max(diff)), judged, used, int(diff.size)))
+    return judged
