@@ -55,10 +55,13 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         r[4] += 1
     tr = terminalreporter
     tr.section("parity report (max abs error vs the fp64 oracle)")
-    tr.write_line(f"{'test':<92} {'plain':>9} {'judged':>9} {'allow':>6} {'elements':>11}")
+    tr.write_line(f"{'test [compared with]':<104} {'plain':>9} {'judged':>9} {'allow':>6} {'elements':>11}")
     for name, (plain, judged, used, n, calls) in rows.items():
-        tr.write_line(f"{name[-92:]:<92} {plain:9.2e} {judged:9.2e} {used:6d} {n:11d}")
-    tot_used = sum(r[2] for r in rows.values())
-    tot_n = sum(r[3] for r in rows.values())
-    tr.write_line(f"elements over the plain 1e-2 bar brought under it by the bf16-resolution allowance: "
-                  f"{tot_used} of {tot_n}")
+        tr.write_line(f"{name[-104:]:<104} {plain:9.2e} {judged:9.2e} {used:6d} {n:11d}")
+    ours = {k: v for k, v in rows.items() if k.endswith("[oracle]")}
+    tot_used = sum(r[2] for r in ours.values())
+    tot_n = sum(r[3] for r in ours.values())
+    worst = max(ours.items(), key=lambda kv: kv[1][0]) if ours else None
+    tr.write_line(f"results against the oracle on the same pool: {len(ours)} checks, largest plain max abs error "
+                  f"{worst[1][0]:.3e} ({worst[0]}); elements over the plain 1e-2 bar brought under it by the "
+                  f"bf16-resolution allowance: {tot_used} of {tot_n}" if worst else "no checks against the oracle")

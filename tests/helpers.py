@@ -97,12 +97,14 @@ def bf16_step(x: np.ndarray) -> np.ndarray:
 
 
 # Every max_err call of the running test, for the session's parity report (conftest prints
-# it): (test, plain max abs error, error as judged, elements that needed the allowance, elements).
+# it): (test [label], plain max abs error, error as judged, elements that needed the allowance,
+# elements).  Label "oracle": a result against the fp64 oracle on the same pool; "unquantised":
+# against the oracle on the unquantised values of an 8-bit pool (quantisation error included).
 PARITY_LOG: list[tuple[str, float, float, int, int]] = []
 CURRENT_TEST = ""
 
 
-def max_err(gpu: np.ndarray, ref: np.ndarray, rows=None) -> float:
+def max_err(gpu: np.ndarray, ref: np.ndarray, rows=None, label: str = "oracle") -> float:
     """Max abs error of bf16 results against the fp64 oracle, read at the bf16 output's own
     resolution.  Where one bf16 step at the reference value is wider than the 1e-2 bar
     (|ref| >= 2: steps of 2^-6 and more), the part of that step beyond the bar is not counted:
@@ -121,5 +123,5 @@ def max_err(gpu: np.ndarray, ref: np.ndarray, rows=None) -> float:
     judged = float(np.max(diff - allowance))
     # elements over the plain 1e-2 bar that the allowance brought back under it
     used = int(np.count_nonzero((diff > BF16_TOL) & (diff - allowance <= BF16_TOL)))
-    PARITY_LOG.append((CURRENT_TEST, float(np.max(diff)), judged, used, int(diff.size)))
+    PARITY_LOG.append((f"{CURRENT_TEST} [{label}]", float(np.max(diff)), judged, used, int(diff.size)))
     return judged

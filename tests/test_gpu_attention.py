@@ -52,8 +52,8 @@ def test_decode_matches_oracle(case, kv_dtype):
         # quantisation: against the unquantised values the kernel may add at most the kernel
         # tolerance to the error the 8-bit codes themselves cause (measured exactly by the oracle)
         unq = oracle_run(b, unquantised=True).out
-        inherent = max_err(o.out, unq)
-        assert max_err(got, unq) <= inherent + FP8_DEQ_TOL
+        inherent = max_err(o.out, unq, label="unquantised")
+        assert max_err(got, unq, label="unquantised") <= inherent + FP8_DEQ_TOL
 
 
 CONTEXT = [
@@ -85,7 +85,7 @@ def test_context_matches_oracle(case, kv_dtype):
     else:  # 8-bit pool: context pages are staged as exact bf16 code values first
         assert max_err(got, o.out) <= FP8_DEQ_TOL
         unq = oracle_run(b, unquantised=True).out
-        assert max_err(got, unq) <= max_err(o.out, unq) + FP8_DEQ_TOL
+        assert max_err(got, unq, label="unquantised") <= max_err(o.out, unq, label="unquantised") + FP8_DEQ_TOL
 
 
 def test_deterministic_and_page_permutation_invariant():

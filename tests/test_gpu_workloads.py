@@ -48,4 +48,4 @@ def test_workload_full_size(idx, kv_dtype, stride):
         # vs the unquantised values: E4M3 itself moves outputs by up to ~4.3e-2 here (exact
         # fp64 on both pools); the kernel adds at most 1e-2 to that
         unq = oracle_run(b_host, rows=rows, unquantised=True).out
-        assert max_err(got, unq, rows) <= max_err(o.out, unq, rows) + FP8_DEQ_TOL
+        assert max_err(got, unq, rows, label="unquantised") <= max_err(o.out, unq, rows, label="unquantised") + FP8_DEQ_TOL
