@@ -256,18 +256,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   int own = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) own += s_hist[tid * kPer + i];
-  s_part[tid] = own;
+  // block-wide exclusive scan of the per-thread totals: shuffles inside each warp, then the
+  // warps' totals (one warp scans them)
+  int incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_part[wid] = incl;
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int t = 0; t < kPlanThreads; ++t) {
-      const int v = s_part[t];
-      s_part[t] = run;
-      run += v;
+  if (wid == 0) {
+    const int w = lane < kPlanThreads / 32 ? s_part[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
     }
+    if (lane < kPlanThreads / 32) s_part[kPlanThreads / 32 + lane] = wi - w;  // exclusive warp offsets
   }
   __syncthreads();
-  int run = s_part[tid];
+  int run = s_part[kPlanThreads / 32 + wid] + incl - own;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int v = s_hist[tid * kPer + i];
