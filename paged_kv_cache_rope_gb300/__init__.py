@@ -15,6 +15,7 @@ is no fallback path.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import dataclasses
 import os
@@ -523,8 +524,9 @@ class PagedAttentionBucketStep:
         slots = list(range(nc)) + list(range(bk.context_slots, bk.context_slots + ng))
         sl_n[slots], sl_p[slots] = n, past
         sl_t[slots, :tbl.shape[1]] = tbl
-        s = stream if stream is not None else torch.cuda.current_stream()
-        with torch.cuda.stream(s):
+        on_gpu = self.q.device.type == "cuda"
+        s = stream if stream is not None else (torch.cuda.current_stream() if on_gpu else None)
+        with torch.cuda.stream(s) if on_gpu else contextlib.nullcontext():
             self.meta.d_context_lengths.copy_(torch.from_numpy(sl_n), non_blocking=False)
             self.meta.d_past_kv_lengths.copy_(torch.from_numpy(sl_p), non_blocking=False)
             self.meta.d_block_offsets.copy_(torch.from_numpy(sl_t), non_blocking=False)

@@ -60,16 +60,30 @@ def _run(step, b, replay=True, scale=None):
     return _check(step, b, scale)
 
 
-def _fixed_scale(batches):
+def _fixed_scale(batches, kv_dtype):
     """8-bit pools: a captured graph holds the pool's scales, so every batch uses one pair."""
     amax = max(float(b.pool_bf16.float().nan_to_num(0.0).abs().max()) for b in batches)
     amax = max([amax] + [float(t.float().abs().max()) for b in batches for t in (b.k, b.v)])
-    s = float(np.float32(amax / 448.0))
+    s = float(np.float32(amax / (127.0 if kv_dtype == "int8" else 448.0)))
     return s, float(np.float32(1.0 / s))
 
 
+def _encode(pool_bf16, kv_dtype, inv_scale):
+    """The history re-encoded with one scale: e4m3 by torch's cast after a clamp, int8 by
+    round-half-even and a clamp; unused slots keep the poison code."""
+    x = pool_bf16.float().nan_to_num(0.0) * inv_scale
+    unused = pool_bf16.view(torch.int16) == W.BF16_NAN
+    if kv_dtype == "int8":
+        codes = x.round().clamp(-128.0, 127.0).to(torch.int8)
+        codes[unused] = W.INT8_POISON
+    else:
+        codes = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        codes[unused] = W.E4M3_NAN
+    return codes
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "int8"])
 def test_one_graph_serves_batches_of_different_mixes(kv_dtype):
     """Captured once on the first batch, replayed on: the same mix with other lengths, only
     generation requests, only context requests (chunked, with cached prefixes), and one long
@@ -84,12 +98,11 @@ def test_one_graph_serves_batches_of_different_mixes(kv_dtype):
         _batch([(100, 0), (400, 64), (37, 1500)], [], 4, kv_dtype),
         _batch([(1000, 1000)], [2048], 5, kv_dtype),
     ]
-    scale = _fixed_scale(batches) if kv_dtype != "bf16" else None
+    scale = _fixed_scale(batches, kv_dtype) if kv_dtype != "bf16" else None
     if scale is not None:  # re-encode every pool with the one scale the graph holds
         for i, b in enumerate(batches):
-            codes = (b.pool_bf16.float() * scale[1]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
-            codes[b.pool_bf16.view(torch.int16) == W.BF16_NAN] = W.E4M3_NAN
-            batches[i] = dataclasses.replace(b, pool=codes, kv_scale=scale[0], inv_scale=scale[1])
+            batches[i] = dataclasses.replace(b, pool=_encode(b.pool_bf16, kv_dtype, scale[1]),
+                                             kv_scale=scale[0], inv_scale=scale[1])
     b0 = batches[0]
     pool = pk.KVPool(b0.pool.to(DEV).clone(), b0.kv_scale, b0.inv_scale)
     table = pk.paged_rope_table_build(1e4, D, bucket.max_kv_len, DEV)

@@ -15,9 +15,9 @@ def test_bf16_step_is_the_gap_to_the_next_bf16_number():
 
 
 def test_max_err_counts_only_the_step_beyond_the_bar():
-    assert abs(max_err(np.array([0.30]), np.array([0.305])) - 0.005) < 1e-15   # |ref| < 2: plain
-    one_step = max_err(np.array([2.0]), np.array([2.0107]))                      # one step off at 2
+    assert abs(max_err(np.array([0.30]), np.array([0.305]), label="helper pin") - 0.005) < 1e-15   # |ref| < 2: plain
+    one_step = max_err(np.array([2.0]), np.array([2.0107]), label="helper pin")                      # one step off at 2
     assert one_step <= BF16_TOL
-    two_steps = max_err(np.array([2.0]), np.array([2.03]))                       # two steps off
+    two_steps = max_err(np.array([2.0]), np.array([2.03]), label="helper pin")                       # two steps off
     assert two_steps > BF16_TOL
-    assert max_err(np.array([np.nan]), np.array([1.0])) == float("inf")
+    assert max_err(np.array([np.nan]), np.array([1.0]), label="helper pin") == float("inf")
