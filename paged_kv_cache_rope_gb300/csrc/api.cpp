@@ -605,7 +605,9 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
     cp.NB = static_cast<int32_t>(ctx_blocks);
     cp.max_blocks = batch->max_blocks_per_seq;
     cp.num_tiles = hp.num_tiles;
+    cp.num_ctas = device_sm_count();
     cp.counts = counts;
+    cp.cursor = ws + hp.lay.counts + pkv::kCntCursor;
     cp.cu_q = ws + hp.lay.cu_q;
     cp.tile_prefix = ws + hp.lay.tile_prefix;
     cp.unit_info = reinterpret_cast<const int4*>(ws + hp.lay.unit_info);

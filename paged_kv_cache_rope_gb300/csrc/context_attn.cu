@@ -55,6 +55,8 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -903,6 +905,557 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   }
 }
 
+// ---- context mode, persistent: one CTA per SM walks a queue of (unit, query head) items ----
+// The per-item work is that of the context mode above (two 128-row Q tiles sharing every K / V
+// tile, S and O in TMEM, the same softmax); what changes is that a CTA keeps its TMEM, barriers
+// and rings across items, so one item's fill and drain overlap its neighbours:
+//   - the producer claims the next item (an atomic cursor the plan zeroes) as soon as it has
+//     issued the current item's last K / V tile, publishes it through a two-entry ring in
+//     shared memory, and loads the next Q tile into a slot as soon as the slot's last S MMA is
+//     done and the next K / V tiles as soon as stages free up;
+//   - the MMA warp goes from the last PV of one item straight to the first S of the next;
+//   - output tiles leave through their own staging tile (one, handed from epilogue to epilogue
+//     in order), so a Q slot never waits for an output store.
+// The ring counters (K / V stream tile, S / P tile per Q tile, Q loads per slot) run on across
+// items; every phase is derived from them.  Items are claimed longest unit first, as the plan
+// sorted them.
+template <int D>
+struct PersistSmem {
+  static constexpr int kHalf = 128 * 128;
+  static constexpr int kTile = (D / 64) * kHalf;
+  static constexpr int kStages = 2;
+  static constexpr int kQOff = 0;                          // Q_A, Q_B
+  static constexpr int kKOff = 2 * kTile;                  // K ring
+  static constexpr int kVOff = kKOff + kStages * kTile;    // V ring
+  static constexpr int kOOff = kVOff + kStages * kTile;    // output staging tile
+  static constexpr int kBarOff = kOOff + kTile;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+  static_assert(kBytes <= 232448, "shared memory per CTA");
+};
+
+enum {
+  PB_Q = 0,          // +2: Q tile of slot x landed
+  PB_QFREE = 2,      // +2: the last S MMA on slot x is done (the slot may be refilled)
+  PB_KFULL = 4,      // +2 stages
+  PB_KEMPTY = 6,     // +2
+  PB_VFULL = 8,      // +2
+  PB_VEMPTY = 10,    // +2
+  PB_SFULL = 12,     // +2 Q tiles
+  PB_PFULL = 14,     // +2
+  PB_ODONE = 16,     // +2
+  PB_ITEM = 18,      // +2: item ring entry written
+  PB_ITEMFREE = 20,  // +2: item ring entry read by the MMA warp and the eight softmax warps
+  PB_OSTG = 22,      // the staging tile's last store has been read out
+  PB_OWRITTEN = 23,  // +2: the four warps of Q tile x have written the staging tile
+  PB_MMADONE = 25,
+  PB_NUM = 26
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+context_persistent_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
+                          const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
+  using L = PersistSmem<D>;
+  constexpr int S = L::kStages;
+  static_assert(S == 2, "ring stage and phase below are bit operations");
+  // ring stage and phase of the g-th K / V tile of the stream (g >= 0)
+  auto stg = [](int g) { return g & 1; };
+  auto phs = [](int g) { return (g >> 1) & 1; };
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_s - raw_s);
+  const uint32_t bar0 = base_s + L::kBarOff;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L::kBarOff + 8 * PB_NUM);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * PB_NUM + 4);
+  volatile int* s_item = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * PB_NUM + 8);  // [2]
+  static_assert(8 * PB_NUM + 16 <= L::kBarBytes, "barrier area");
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- set-up (before the grid-dependency wait: reads nothing earlier kernels write) ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(PB_Q + s), 1);
+      tc::mbar_init(bar(PB_QFREE + s), 1);
+      tc::mbar_init(bar(PB_KFULL + s), 1);
+      tc::mbar_init(bar(PB_KEMPTY + s), 1);
+      tc::mbar_init(bar(PB_VFULL + s), 1);
+      tc::mbar_init(bar(PB_VEMPTY + s), 1);
+      tc::mbar_init(bar(PB_SFULL + s), 1);
+      tc::mbar_init(bar(PB_PFULL + s), 4);  // one arrive per softmax warp
+      tc::mbar_init(bar(PB_ODONE + s), 1);
+      tc::mbar_init(bar(PB_ITEM + s), 1);
+      tc::mbar_init(bar(PB_ITEMFREE + s), 9);  // the MMA warp and the eight softmax warps
+      tc::mbar_init(bar(PB_OWRITTEN + s), 4);
+    }
+    tc::mbar_init(bar(PB_OSTG), 1);
+    tc::mbar_init(bar(PB_MMADONE), 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(base_s + L::kBarOff + 8 * PB_NUM, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tc::prefetch_tmap(&q_map);
+    tc::prefetch_tmap(&kv_map);
+    tc::prefetch_tmap(&out_map);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();
+
+  const int n_items = __ldg(p.counts + kCntUnits) * p.Hq;
+  // An item: query head hq of unit y (the plan's descriptor: request, first q row, key position
+  // of that row, rows of the request from there on).  Every role derives the same geometry.
+  struct Item {
+    int hq, hk, r, q_row, past, L_r, nv0, nv1, nkt0, nkt1, nT;
+    bool ok, hasB, fullA, fullB;
+  };
+  auto item_of = [&](int w) {
+    Item it;
+    const int y = w / p.Hq;
+    it.hq = w - y * p.Hq;
+    it.hk = it.hq / p.group;
+    const int4 u = __ldg(p.unit_info + y);
+    it.r = u.x;
+    it.q_row = u.y;
+    it.past = u.z;
+    const int n_rem = u.w;
+    it.L_r = it.past + n_rem;
+    it.nv0 = max(0, min(128, n_rem));
+    it.nv1 = max(0, min(128, n_rem - 128));
+    it.nkt0 = it.nv0 > 0 ? (it.past + it.nv0 + kCtxTileN - 1) / kCtxTileN : 0;
+    it.nkt1 = it.nv1 > 0 ? (it.past + 128 + it.nv1 + kCtxTileN - 1) / kCtxTileN : 0;
+    it.ok = it.nv0 > 0 && it.r >= 0 && it.r < p.C && it.past >= 0 && it.q_row >= 0 && it.q_row + it.nv0 + it.nv1 <= p.T;
+    it.hasB = it.nv1 > 0;
+    it.nT = it.ok ? (it.hasB ? it.nkt1 : it.nkt0) : 0;
+    // full output tiles leave through the staging tile and a TMA store, A before B
+    it.fullA = it.ok && it.nv0 == 128 && it.q_row + 128 <= p.T;
+    it.fullB = it.ok && it.nv1 == 128 && it.q_row + 256 <= p.T;
+    return it;
+  };
+
+  const uint32_t sQ = base_s + L::kQOff;
+  const uint32_t sO = base_s + L::kOOff;
+  auto sK = [&](int st) { return base_s + L::kKOff + st * L::kTile; };
+  auto sV = [&](int st) { return base_s + L::kVOff + st * L::kTile; };
+  auto fail = [&]() {
+    flag_error(p.d_error, PKV_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+  auto warp_wait = [&](uint32_t b, uint32_t parity) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(b, parity)) != 0;
+  };
+  auto warp_abort = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0) != 0; };
+  // consumers: item k of this CTA from the ring (-1: no more work), entry handed back
+  auto take_item = [&](int k, int& w) {
+    const int slot = k & 1;
+    if (!warp_wait(bar(PB_ITEM + slot), (k >> 1) & 1)) return false;
+    w = *(s_item + slot);
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar(PB_ITEMFREE + slot));
+    return true;
+  };
+
+  if (warp >= 8) {
+    tc::regs_dec<kRegsControl>();
+    if (warp == kProducerWarp) {
+      // ======================= item queue + TMA producer =======================
+      int w = blockIdx.x;
+      int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items)
+      int nq0 = 0, nq1 = 0;            // Q loads per slot
+      bool pok = true;
+      for (int k = 0; pok; ++k) {
+        const int slot = k & 1;
+        if (k >= 2 && !warp_wait(bar(PB_ITEMFREE + slot), ((k - 2) >> 1) & 1)) { pok = false; break; }
+        const bool more = w < n_items;
+        if (lane == 0) {
+          *(s_item + slot) = more ? w : -1;
+          tc::mbar_arrive(bar(PB_ITEM + slot));
+        }
+        __syncwarp();
+        if (!more) break;
+        const Item it = item_of(w);
+        if (!it.ok) {
+          if (lane == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
+        } else {
+          // Q tiles: slot x once its previous item's last S MMA is done
+          for (int x = 0; x < (it.hasB ? 2 : 1); ++x) {
+            const int n = x ? nq1 : nq0;
+            if (n > 0 && !warp_wait(bar(PB_QFREE + x), (n - 1) & 1)) { pok = false; break; }
+            if (tc::elect_one()) {
+              tc::mbar_arrive_expect_tx(bar(PB_Q + x), 128 * D * 2);
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(PB_Q + x), 0, dh, it.hq,
+                                it.q_row + 128 * x);
+            }
+            __syncwarp();
+            if (x) ++nq1; else ++nq0;
+          }
+          const int32_t* tbl = p.tbl + static_cast<int64_t>(it.r) * p.max_blocks;
+          const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
+          const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
+          const int n_pages_seq = (it.L_r + p.B - 1) / p.B;
+#ifdef PKV_SELFTEST
+          // Self-test build only (compiled by the tests, never into libpaged_kv.so): no K / V
+          // copy is issued, so the MMA warp's wait for the first K tile and the softmax warps'
+          // waits for their first S run out after the short self-test budget and the CTA winds
+          // down through the timeout path; the Q tiles land before the teardown (waited below).
+          const int n_issue = 0;
+#else
+          const int n_issue = it.nT;
+#endif
+          for (int j = 0; pok && j < n_issue; ++j) {
+            if (warp_abort()) { pok = false; break; }
+            const int g = issued_k;  // == issued_v
+            const int st = stg(g);
+            // lane pp < pages_per_tile looks up page pp of the tile (whole pages per tile)
+            const int lb = (j * kCtxTileN) / p.B + lane;
+            int pg = -1;
+            if (lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
+              pg = __ldg(tbl + lb);
+              if (pg < 0 || pg >= p.NB) {
+                flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+                pg = -1;
+              }
+            }
+            const uint32_t bytes =
+                static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * 2;
+            const uint32_t koff = static_cast<uint32_t>(lane * box_rows * 128);
+            if (g >= S && !warp_wait(bar(PB_KEMPTY + st), phs(g - S))) { pok = false; break; }
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(PB_KFULL + st), bytes);
+            __syncwarp();
+            if (pg >= 0)
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_load_4d(sK(st) + dh * L::kHalf + koff, &kv_map, bar(PB_KFULL + st), 0, dh, it.hk,
+                                (pg * 2 + 0) * p.B);
+            __syncwarp();
+            ++issued_k;
+            if (g >= S && !warp_wait(bar(PB_VEMPTY + st), phs(g - S))) { pok = false; break; }
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(PB_VFULL + st), bytes);
+            __syncwarp();
+            if (pg >= 0)
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_load_4d(sV(st) + dh * L::kHalf + koff, &kv_map, bar(PB_VFULL + st), 0, dh, it.hk,
+                                (pg * 2 + 1) * p.B);
+            __syncwarp();
+            ++issued_v;
+          }
+        }
+        if (!pok) break;
+        // claim the next item while this one's tiles are still being consumed
+        int nxt = 0;
+        if (lane == 0) nxt = atomicAdd(p.cursor, 1) + static_cast<int>(gridDim.x);
+        w = __shfl_sync(0xffffffffu, nxt, 0);
+      }
+      if (!pok && lane == 0) fail();
+      __syncwarp();
+      // the last copy into each stage and slot has landed before the CTA can wind down, however
+      // the consumers fare (on the normal path these phases completed long ago)
+      for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
+        tc::mbar_wait(bar(PB_KFULL + stg(j)), phs(j), 200000000LL);
+      for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
+        tc::mbar_wait(bar(PB_VFULL + stg(j)), phs(j), 200000000LL);
+      if (nq0 > 0) tc::mbar_wait(bar(PB_Q + 0), (nq0 - 1) & 1, 200000000LL);
+      if (nq1 > 0) tc::mbar_wait(bar(PB_Q + 1), (nq1 - 1) & 1, 200000000LL);
+    } else if (warp == kMmaWarp) {
+      // ======================= MMA issuer =======================
+      constexpr uint32_t idesc_s = tc::idesc_bf16(128, kCtxTileN, 0);
+      constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, 1);
+      const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dq1 = tc::sdesc_sw128(sQ + L::kTile, 16, 1024);
+      const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
+      const uint64_t dv0 = tc::sdesc_sw128(sV(0), L::kHalf, 1024);
+      auto stage_off = [](int st) { return static_cast<uint64_t>(st) * (L::kTile / 16); };
+      int G = 0;               // K / V stream tiles of earlier items
+      int sc0 = 0, sc1 = 0;    // S / P tiles of earlier items, per Q tile
+      int nq0 = 0, nq1 = 0;    // Q loads consumed per slot
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        int w = -1;
+        if (!take_item(k, w)) { ok = false; break; }
+        if (w < 0) break;
+        const Item it = item_of(w);
+        if (!it.ok) continue;
+        auto uses = [&](int j, int x) { return j < (x ? it.nkt1 : it.nkt0); };
+        auto frees = [&](int j, int x) { return x == ((it.hasB && j < it.nkt1) ? 1 : 0); };
+        auto issue_s = [&](int j, int x) {
+          const int st = stg(G + j);
+          const uint64_t a0 = x == 0 ? dq0 : dq1;
+          const uint64_t b0 = dk0 + stage_off(st);
+          if (tc::elect_one()) {
+            if constexpr (D == 128) {
+              tc::mma_bf16_ss_x8<0, 2, 4, 6, L::kHalf / 16, L::kHalf / 16 + 2, L::kHalf / 16 + 4, L::kHalf / 16 + 6>(
+                  tmem + 128 * x, a0, b0, idesc_s, 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4);
+                tc::mma_bf16_ss(tmem + 128 * x, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+              }
+            }
+            tc::mma_commit(bar(PB_SFULL + x));
+            if (frees(j, x)) tc::mma_commit(bar(PB_KEMPTY + st));
+            if (j == (x ? it.nkt1 : it.nkt0) - 1) tc::mma_commit(bar(PB_QFREE + x));  // the slot's last S
+          }
+          __syncwarp();
+        };
+        // first S of each Q tile: its Q tile and the item's first K tile
+        ok = warp_wait(bar(PB_Q + 0), nq0 & 1) && warp_wait(bar(PB_KFULL + stg(G)), phs(G));
+        ++nq0;
+        if (ok) {
+          tc::fence_after_sync();
+          issue_s(0, 0);
+          if (it.hasB) {
+            ok = warp_wait(bar(PB_Q + 1), nq1 & 1);
+            ++nq1;
+            if (ok) {
+              tc::fence_after_sync();
+              issue_s(0, 1);
+            }
+          }
+        }
+        for (int j = 0; ok && j < it.nT; ++j) {
+          bool v_ready = false, k_ready = false;  // B reuses the tiles A waited for
+          const int g = G + j;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!uses(j, x)) continue;
+            if (!warp_wait(bar(PB_PFULL + x), ((x ? sc1 : sc0) + j) & 1)) { ok = false; break; }
+            if (!v_ready) {
+              if (!warp_wait(bar(PB_VFULL + stg(g)), phs(g))) { ok = false; break; }
+              v_ready = true;
+            }
+            tc::fence_after_sync();
+            const uint64_t v0 = dv0 + stage_off(stg(g));
+            if (tc::elect_one()) {
+              static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
+              tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
+              if (frees(j, x)) tc::mma_commit(bar(PB_VEMPTY + stg(g)));
+              if (j == (x ? it.nkt1 : it.nkt0) - 1) tc::mma_commit(bar(PB_ODONE + x));
+            }
+            __syncwarp();
+            if (uses(j + 1, x)) {
+              if (!k_ready && !warp_wait(bar(PB_KFULL + stg(g + 1)), phs(g + 1))) { ok = false; break; }
+              k_ready = true;
+              tc::fence_after_sync();
+              issue_s(j + 1, x);
+            }
+          }
+        }
+        G += it.nT;
+        sc0 += it.nkt0;
+        if (it.hasB) sc1 += it.nkt1;
+      }
+      if (!ok && lane == 0) fail();
+      if (tc::elect_one()) {
+        tc::mma_commit(bar(PB_MMADONE));
+        tc::mbar_wait(bar(PB_MMADONE), 0, 200000000LL);  // nothing of ours still runs on TMEM
+      }
+      __syncwarp();
+    }
+  } else {
+    // ======================= softmax warpgroups =======================
+    tc::regs_inc<kRegsSoftmax>();
+    const int x = warp >> 2;                 // Q tile A (0) or B (1)
+    const int row = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 128 * x + lane_off;
+    const uint32_t tO = tmem + 256 + 128 * x + lane_off;
+    const float sl2 = p.scale_log2;
+    int G = 0, sc = 0, n_epi = 0;  // stream tiles, this tile's S / P tiles and epilogues so far
+    int n_stg = 0, n_own = 0;      // staging-tile uses so far (both Q tiles), and this tile's own
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      int w = -1;
+      if (!take_item(k, w)) { ok = false; break; }
+      if (w < 0) break;
+      const Item it = item_of(w);
+      if (!it.ok) continue;
+      const int nvx = x ? it.nv1 : it.nv0, nk = x ? it.nkt1 : it.nkt0;
+      const int stg_idx = n_stg + (x ? (it.fullA ? 1 : 0) : 0);  // A's store goes first
+      const bool full = x ? it.fullB : it.fullA;
+      const int zero_x = (it.nkt0 == it.nT) ? 0 : 1;  // first user of the last V tile zeroes its tail
+      const int q_pos = it.past + 128 * x + min(row, max(nvx, 1) - 1);  // padding rows mirror the last row
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; ok && j < nk; ++j) {
+        if (!warp_wait(bar(PB_SFULL + x), (sc + j) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        tc::tmem_ld32_async(tS + 0, v0);
+        tc::tmem_ld32_async(tS + 32, v1);
+        tc::tmem_ld32_async(tS + 64, v2);
+        tc::tmem_ld32_async(tS + 96, v3);
+        tc::tmem_wait_ld_dep(v0);
+        tc::reg_dep(v1);
+        tc::reg_dep(v2);
+        tc::reg_dep(v3);
+        const int lim = q_pos - j * kCtxTileN;  // key column c is visible iff c <= lim
+        if (__any_sync(0xffffffffu, lim < kCtxTileN - 1)) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            v0[e] = e <= lim ? v0[e] : __float_as_uint(-INFINITY);
+            v1[e] = 32 + e <= lim ? v1[e] : __float_as_uint(-INFINITY);
+            v2[e] = 64 + e <= lim ? v2[e] : __float_as_uint(-INFINITY);
+            v3[e] = 96 + e <= lim ? v3[e] : __float_as_uint(-INFINITY);
+          }
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          mx[0] = max3f(mx[0], __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
+          mx[1] = max3f(mx[1], __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
+          mx[2] = max3f(mx[2], __uint_as_float(v2[e]), __uint_as_float(v2[e + 1]));
+          mx[3] = max3f(mx[3], __uint_as_float(v3[e]), __uint_as_float(v3[e + 1]));
+        }
+        const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
+        float m_use = m_run;
+        if (j == 0) {
+          m_use = m_new;  // O is still empty
+        } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
+          const float f = ex2_approx(m_run - m_new);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tc::tmem_st32(tO + cc * 32, o);
+          }
+          l_run *= f;
+          m_use = m_new;
+        }
+        m_run = m_use;
+        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float m_base = m_use == -INFINITY ? 0.f : m_use;
+        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
+        auto emit = [&](uint32_t(&v)[32], int c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
+            const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+            ls[c] = fadd2(ls[c], pv);
+            pk[e >> 1] = pack_bf16x2(pv.x, pv.y);
+          }
+          tc::tmem_st16(tS + 16 * c, pk);
+        };
+        emit(v0, 0);
+        emit(v1, 1);
+        emit(v2, 2);
+        emit(v3, 3);
+        const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+        l_run += lsum.x + lsum.y;
+        tc::tmem_wait_st();
+        if (j == it.nT - 1 && x == zero_x) {
+          // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
+          const int g = G + it.nT - 1;
+          if (!warp_wait(bar(PB_VFULL + stg(g)), phs(g))) { ok = false; break; }
+          if (j * kCtxTileN + row >= it.L_r) {
+            uint8_t* vrow = base + (sV(stg(g)) - base_s) + row * 128;
+#pragma unroll
+            for (int dh = 0; dh < D / 64; ++dh)
+#pragma unroll
+              for (int kq = 0; kq < 8; ++kq)
+                reinterpret_cast<uint4*>(vrow + dh * L::kHalf)[kq] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc::fence_proxy_async_smem();
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(PB_PFULL + x));
+      }
+      if (!ok) break;
+      if (nk > 0) {
+        // ---- epilogue: O / l -> bf16 row ----
+        if (!warp_wait(bar(PB_ODONE + x), n_epi & 1)) { ok = false; break; }
+        ++n_epi;
+        tc::fence_after_sync();
+        const float inv_l = p.out_scale / l_run;
+        // (the next item's first PV on this tile comes after this warp's next P-ready arrive,
+        // which follows these TMEM loads in program order)
+        if (full) {
+          // the staging tile, once the previous store from it has been read out
+          if (stg_idx > 0 && !warp_wait(bar(PB_OSTG), (stg_idx - 1) & 1)) { ok = false; break; }
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            tc::tmem_ld32(tO + cc * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+            // 128-byte swizzle of the TMA box: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+            const uint32_t rbase = sO + (cc >> 1) * L::kHalf + row * 128;
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+              const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + kq) ^ static_cast<uint32_t>(row & 7);
+              st_shared_v4(rbase + chunk * 16, pk[4 * kq], pk[4 * kq + 1], pk[4 * kq + 2], pk[4 * kq + 3]);
+            }
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(bar(PB_OWRITTEN + x));
+          if ((warp & 3) == 0) {
+            // one thread stores the tile once its four warps have written it, waits for the
+            // read-out and hands the staging tile on
+            if (!warp_wait(bar(PB_OWRITTEN + x), n_own & 1)) { ok = false; break; }
+            if (lane == 0) {
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_store_4d(&out_map, sO + dh * L::kHalf, 0, dh, it.hq, it.q_row + 128 * x);
+              tc::bulk_commit();
+              tc::bulk_wait_read0();
+              tc::mbar_arrive(bar(PB_OSTG));
+            }
+            __syncwarp();
+          }
+          ++n_own;
+        } else {
+          // a partial tile (the end of a request, whose next rows belong to another request):
+          // per-row stores
+          const int grow = it.q_row + 128 * x + row;
+          const bool store = row < nvx && grow < p.T;
+          uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(it.hq) * D;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            tc::tmem_ld32(tO + cc * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+            if (store) {
+#pragma unroll
+              for (int kq = 0; kq < 4; ++kq)
+                reinterpret_cast<uint4*>(orow + cc * 32)[kq] =
+                    make_uint4(pk[4 * kq], pk[4 * kq + 1], pk[4 * kq + 2], pk[4 * kq + 3]);
+            }
+          }
+        }
+      }
+      G += it.nT;
+      sc += nk;
+      n_stg += (it.fullA ? 1 : 0) + (it.fullB ? 1 : 0);
+    }
+    if (!ok) fail();
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ---- 8-bit pools: stage the context requests' pages as bf16 (exact code values) ----
 constexpr int kStageThreads = 256;
 
@@ -973,6 +1526,18 @@ cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, cons
   return launch_pdl(kern, grid, dim3(kThreads), bytes, s, p, qm, km, om);
 }
 
+template <int D>
+cudaError_t launch_context_persistent(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km,
+                                      const CUtensorMap& om, cudaStream_t s) {
+  auto kern = context_persistent_kernel<D>;
+  constexpr int bytes = PersistSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  const int64_t items = static_cast<int64_t>(p.num_tiles) * p.Hq;
+  const int grid = static_cast<int>(std::min<int64_t>(items, std::max(p.num_ctas, 1)));
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), bytes, s, p, qm, km, om);
+}
+
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map, bool dec,
                            cudaStream_t s) {
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
@@ -984,8 +1549,8 @@ cudaError_t launch_context(const ContextParams& p, const void* q_map, const void
                                   : launch_context_t<128, true, PKV_FP8_E4M3>(p, qm, km, om, s);
   }
   if (p.D == 128)
-    return dec ? launch_context_t<128, true, 0>(p, qm, km, om, s) : launch_context_t<128, false, 0>(p, qm, km, om, s);
-  return dec ? launch_context_t<64, true, 0>(p, qm, km, om, s) : launch_context_t<64, false, 0>(p, qm, km, om, s);
+    return dec ? launch_context_t<128, true, 0>(p, qm, km, om, s) : launch_context_persistent<128>(p, qm, km, om, s);
+  return dec ? launch_context_t<64, true, 0>(p, qm, km, om, s) : launch_context_persistent<64>(p, qm, km, om, s);
 }
 
 }  // namespace pkv

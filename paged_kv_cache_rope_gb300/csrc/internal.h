@@ -36,6 +36,7 @@ enum PlanCount {
   kCntTitems = 6,      // tensor-core generation CTAs per KV head
   kCntParts = 7,       // split-KV partial rows per query head
   kCntStagePages = 8,  // 8-bit pools: staged context pages
+  kCntCursor = 9,      // work-queue cursor of the context kernel (written as zero by the plan)
   kCntWords = 16
 };
 
@@ -144,7 +145,9 @@ struct DecodeParams {
 
 struct ContextParams {
   int32_t C, T, Hq, Hkv, group, D, B, NB, max_blocks, num_tiles;
+  int32_t num_ctas;         // context mode: persistent CTAs (one per SM at most)
   const int32_t* counts;    // the plan's PlanCount words
+  int32_t* cursor;          // context mode: the counts block's work-queue word
   const int32_t* cu_q;
   const int32_t* tile_prefix;
   const int4* unit_info;      // [num_tiles] context units in launch order: (request r, first
