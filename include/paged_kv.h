@@ -246,7 +246,7 @@ size_t paged_attention_workspace_size(const pkv_pool* pool, const pkv_batch* bat
  * Context rows use a tcgen05/TMEM tensor-core kernel (for 8-bit pools after staging the context
  * requests' pages as exact bf16 code values in the workspace), generation rows a split-KV decode
  * kernel plus a log-sum-exp combine.  Generation requests with more (token, query head) pairs
- * than the decode kernel's narrow columns run on the tensor-core kernel's generation mode when
+ * than the decode kernel's narrow columns run on the tensor-core generation kernel when
  * the query group divides 128 and the pool is bf16, or 8-bit at head_dim 128 (codes converted
  * to f16 in shared memory); otherwise on a wide split-KV decode kernel.  When the batch has both kinds of rows, the generation
  * kernels run on the library's auxiliary stream for this device (highest stream priority),

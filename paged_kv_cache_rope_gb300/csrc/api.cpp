@@ -209,7 +209,7 @@ int choose_kv_chunk(const pkv_pool* pool, int64_t total) {
 void plan_decode_shape(const pkv_pool* pool, int32_t Hq, int64_t total, int max_narrow, bool any_wide, HostPlan* hp) {
   const int group = Hq / pool->num_kv_heads;
   hp->kv_chunk = choose_kv_chunk(pool, total);
-  // the tensor-core generation mode: bf16 pools, and 8-bit pools at head_dim 128 (their codes
+  // the tensor-core generation kernel: bf16 pools, and 8-bit pools at head_dim 128 (their codes
   // are converted to f16 in shared memory)
   hp->tc_wide = any_wide && group <= 128 && 128 % group == 0 && (pool->dtype == PKV_BF16 || pool->head_dim == 128);
   if (hp->tc_wide) {
@@ -622,7 +622,7 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
     cp.d_error = d_error;
     {
       LaunchScope ls(launches, "context_attn", cs);
-      e = pkv::launch_context(cp, &qmap, &kvmap, &omap, false, cs);
+      e = pkv::launch_context(cp, &qmap, &kvmap, &omap, cs);
     }
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     ++launches;
@@ -729,7 +729,7 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
       tp.part_ml = dp.part_ml;
       {
         LaunchScope ls(launches, "decode_tc", gs);
-        e = pkv::launch_context(tp, &qmap_g, &kvmap_g, &qmap_g, true, gs);  // no output map in generation mode
+        e = pkv::launch_gen_tc(tp, &qmap_g, &kvmap_g, gs);
       }
       if (e != cudaSuccess) return PKV_ERR_CUDA;
       ++launches;

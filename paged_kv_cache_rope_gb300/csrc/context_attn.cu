@@ -9,46 +9,54 @@
 // traffic).
 //
 // The pages' kernel keeps S and O in registers of warp-level MMA fragments.  On sm_103a the
-// contraction runs on tcgen05 with both accumulators in TMEM instead:
-//   CTA = (query head, 256 query rows of one context request) = two 128-row Q tiles A and B
-//   that share every K/V tile and take turns on the tensor core; 12 warps (3 warpgroups, with
-//   setmaxnreg moving registers from the control warpgroup to the two softmax warpgroups):
+// contraction runs on tcgen05 with both accumulators in TMEM instead.
+//
+// context_attn_kernel: persistent, one CTA per SM at most.  Work item = (context unit of 256
+// query rows, query head) = two 128-row Q tiles A and B that share every K/V tile and take turns
+// on the tensor core.  A CTA claims items from a queue (longest unit first, as the plan sorted
+// them) and keeps its TMEM, barriers and K/V ring across items.  12 warps (3 warpgroups, with
+// setmaxnreg moving registers from the control warpgroup to the two softmax warpgroups):
 //     warps 0-3 / 4-7  softmax of tile A / B: thread i owns row i (TMEM lane i).  It reads its
 //                S row from TMEM in one pass (128 registers), masks by select, keeps the running
 //                max / sum in base 2 (O is rescaled in TMEM only when the max grows by more than
 //                2^8), and writes P as bf16 back into the first 64 columns of its own S buffer;
-//     warp 8     TMA producer: Q once, then per 128-key tile the pool pages of K and V through
-//                the block table (lane i looks up and loads page i: one box per page and
-//                64-wide head-dim half);
+//     warp 8     item queue and TMA producer: per item Q once per tile, then per 128-key tile
+//                the pool pages of K and V through the block table (lane i looks up and loads
+//                page i: one box per page and 64-wide head-dim half); it claims the next item
+//                as soon as it has issued the current one's last tile;
 //     warp 9     TMEM owner and MMA issuer (warps 10-11 only complete the warpgroup), in the order
 //                  S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
-//                so one tile's softmax overlaps the other tile's MMAs.  PV takes P straight from
-//                TMEM (A operand in tensor memory) and V from shared memory (MN-major).
+//                so one tile's softmax overlaps the other tile's MMAs, and from the last PV of
+//                one item straight on to the first S of the next.  PV takes P straight from TMEM
+//                (A operand in tensor memory) and V from shared memory (MN-major).
 //   Warps 8 and 9 share their sub-partitions with busy softmax warps and get few issue slots,
 //   so they run converged, one elect.sync lane issues, and an 8-step MMA batch is a single
 //   inline-asm statement over descriptors built once per operand tile: every instruction they
 //   spend between MMA batches leaves the tensor pipe idle.
-//   A full 128-row output tile is written into its own (finished) Q slot and leaves with two
-//   TMA stores; per-thread row stores would scatter each warp instruction over 32 rows.
+//   A full 128-row output tile leaves through a staging tile of its own (handed from epilogue to
+//   epilogue in order) and two TMA stores, so no Q slot waits for an output store; per-thread
+//   row stores would scatter each warp instruction over 32 rows.
 //   TMEM columns: S_A | S_B | O_A | O_B (4 x 128 of 128 lanes).  tcgen05 work issued by one
 //   thread completes in order, so a commit after S_X(j) also covers PV_X(j-1): the softmax of
 //   tile j may rescale O_X as soon as S_X(j) has landed.
 // 8-bit pools (E4M3 or int8 codes): stage_q8_kernel first copies the context requests' pages
-// into a bf16 staging pool (exact code values) with its own block table; this kernel then runs
-// unchanged on it, with the pool scale folded into the score scale and into the output scale.
-// Generation mode (DEC: generation requests with more (token, query head) pairs than the
-// mma.sync decode kernel's columns; bf16 pools, or 8-bit pools at head_dim 128 whose codes TMA
-// lands raw: E4M3 scores run on kind::f8f6f4 from the raw K codes against Q split into hi + lo
-// E4M3 tiles, INT8 K is converted to f16 with Q made f16, and V is converted to f16 for a
-// kind::f16 PV -- each conversion by the softmax warpgroup that will read the tile; Q takes a
-// power-of-two scale per row that the scores give back): a 128-row tile is 128/g draft tokens
-// x the g query
-// heads of one KV head (the Q box spans g heads), so each K / V tile serves the whole group;
-// the two softmax warpgroups take the even and the odd KV tiles of one split of kv_chunk keys
-// against the same Q tile; at the end B hands its (max, sum) over through shared memory, A
-// merges O_A and O_B from TMEM and writes the output row (one split) or a partial row for the
-// combine kernel.  Visibility of the new keys comes from the
-// draft-token mask words (bitmaps per row), applied only to the tiles that hold new keys.
+// into a bf16 staging pool (exact code values) with its own block table; the context kernel then
+// runs unchanged on it, with the pool scale folded into the score scale and into the output scale.
+//
+// gen_attn_kernel: generation requests with more (token, query head) pairs than the mma.sync
+// decode kernel's columns, on the same tcgen05 pipeline; bf16 pools, or 8-bit pools at head_dim
+// 128 whose codes TMA lands raw: E4M3 scores run on kind::f8f6f4 from the raw K codes against Q
+// split into hi + lo E4M3 tiles, INT8 K is converted to f16 with Q made f16, and V is converted
+// to f16 for a kind::f16 PV -- each conversion by the softmax warpgroup that will read the tile;
+// Q takes a power-of-two scale per row that the scores give back.  CTA = (request, KV head,
+// split, 128 rows): a 128-row tile is 128/g draft tokens x the g query heads of one KV head (the
+// Q box spans g heads), so each K / V tile serves the whole group; the two softmax warpgroups
+// take the even and the odd KV tiles of one split of kv_chunk keys against the same Q tile; at
+// the end B hands its (max, sum) over through shared memory, A merges O_A and O_B from TMEM and
+// writes the output row (one split) or a partial row for the combine kernel.  Visibility of the
+// new keys comes from the draft-token mask words (bitmaps per row), applied only to the tiles
+// that hold new keys.
+//
 // Rows past the request's end and keys past the causal limit are masked by select (never by
 // arithmetic on the loaded values); V rows past the sequence end are zeroed before PV, so
 // stale or poisoned pool slots cannot reach the output.  Every wait is bounded.
@@ -73,19 +81,19 @@ constexpr uint32_t kRegsControl = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could exceed 2^8
 
-// Context: Q_A, Q_B, K[2], V[2].  Generation: one Q tile (A and B share it), K[3], V[3] -- a
-// deeper ring, since each K / V tile has one consumer and the two halves alternate.
-// Generation with an 8-bit pool (KV != 0): Q, K[2], V[2] (f16; for E4M3 the K[0] area holds the
+// Generation kernel: one Q tile (A and B share it), K[3], V[3] -- each K / V tile has one
+// consumer and the two halves alternate.
+// With an 8-bit pool (KV != 0): Q, K[2], V[2] (f16; for E4M3 the K[0] area holds the
 // hi and lo E4M3 Q tiles instead), a ring of the raw codes (K[2], V[2]) that TMA fills and the
 // softmax warpgroups convert, and the per-row Q scales.
-template <int D, bool DEC, int KV = 0>
-struct CtxSmem {
+template <int D, int KV = 0>
+struct GenSmem {
   static constexpr bool kQ8 = KV != 0;
   static constexpr int kHalf = 128 * 128;         // one 64-wide half of a 128-row tile (bytes)
   static constexpr int kTile = (D / 64) * kHalf;  // one Q tile or one K / V stage
-  static constexpr int kStages = (DEC && !kQ8) ? 3 : 2;
+  static constexpr int kStages = kQ8 ? 2 : 3;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = (DEC ? 1 : 2) * kTile;
+  static constexpr int kKOff = kTile;
   static constexpr int kVOff = kKOff + kStages * kTile;
   static constexpr int kRawTile = 128 * D;        // 128 rows of D one-byte codes
   static constexpr int kRawKOff = kVOff + kStages * kTile;
@@ -95,7 +103,7 @@ struct CtxSmem {
   static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 1 / (Q row's power-of-two scale)
   static constexpr int kBytes = kQScaleOff + (kQ8 ? 128 * 4 : 0) + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
-  static_assert(!kQ8 || (DEC && D == 128), "8-bit codes only in the generation mode at head_dim 128");
+  static_assert(!kQ8 || D == 128, "8-bit codes only at head_dim 128");
 };
 
 enum {
@@ -109,7 +117,7 @@ enum {
   BAR_ODONE = 17,  // +2
   BAR_MMADONE = 19,
   BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
-  BAR_RAWK = 21,   // +2: 8-bit generation mode, raw K codes landed (TMA)
+  BAR_RAWK = 21,   // +2: 8-bit pool, raw K codes landed (TMA)
   BAR_RAWV = 23,   // +2: raw V codes landed
   BAR_RAWKEMPTY = 25, // +2: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
   BAR_RAWVEMPTY = 27, // +2: a raw V stage has been converted
@@ -118,12 +126,12 @@ enum {
 };
 
 
-template <int D, bool DEC, int KV>
+template <int D, int KV>
 __global__ void __launch_bounds__(kThreads, 1)
-context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
-                    const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
-  using L = CtxSmem<D, DEC, KV>;
-  // 8-bit pool in the generation mode: the producer lands raw codes and the softmax warpgroups
+gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
+                const __grid_constant__ CUtensorMap kv_map) {
+  using L = GenSmem<D, KV>;
+  // 8-bit pool: the producer lands raw codes and the softmax warpgroups
   // convert what the MMAs cannot read as stored (Q, V, and INT8 K)
   constexpr bool Q8 = L::kQ8;
   // E4M3 pools: scores on kind::f8f6f4 straight from the raw K codes, with Q split into hi + lo
@@ -183,7 +191,6 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   if (warp == kProducerWarp && lane == 0) {
     tc::prefetch_tmap(&q_map);
     tc::prefetch_tmap(&kv_map);
-    if (!DEC) tc::prefetch_tmap(&out_map);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -193,42 +200,18 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   pdl_wait();
 
   // ---- the work item ----
-  // Context (DEC = false): CTA = (query head hq, unit of 256 rows of one context request); keys
-  // 0 .. the causal limit of each row.
-  // Generation (DEC = true): CTA = (generation request, KV head hk, split of the keys, group of
-  // 256 rows); rows are the (token i, query head hk*g + hl) pairs r = i*g + hl of the request's
-  // new tokens, keys kt0 .. kend-1 of the split, visibility per draft-token mask; partial
-  // results go to the split workspace when the request has several splits.
-  int hq = 0, hk = 0, r = 0, past = 0, L_r = 0, nv0 = 0, nv1 = 0, nkt0 = 0, nkt1 = 0, kt0 = 0, kend = 0, q_row = 0,
-      i0 = 0;
+  // CTA = (generation request, KV head hk, split of the keys, group of 128 rows); rows are the
+  // (token i, query head hk*g + hl) pairs r = i*g + hl of the request's new tokens, keys
+  // kt0 .. kend-1 of the split, visibility per draft-token mask; partial results go to the split
+  // workspace when the request has several splits.
+  int hk = 0, r = 0, past = 0, L_r = 0, nv0 = 0, nv1 = 0, nkt0 = 0, nkt1 = 0, kt0 = 0, kend = 0, q_row = 0;
   int gr = 0, n_new = 0, s_idx = 0, num_splits = 1, pr0 = 0, tok0 = 0;
   bool item_ok = false;
   // the plan's counts: a CTA past this batch's share of the grid (a bucket's spare one) has no
   // work and goes straight to the teardown
-  const bool idle = static_cast<int>(DEC ? blockIdx.x : blockIdx.y) >= __ldg(p.counts + (DEC ? kCntTitems : kCntUnits));
-  const int gen_row0 = DEC ? __ldg(p.counts + kCntGenRow0) : 0;
-  if (idle) {
-  } else if constexpr (!DEC) {
-    hq = blockIdx.x;
-    hk = hq / p.group;
-    // the plan's descriptor of the unit, longest units first: (request, first q row,
-    // past + first row, rows of the request from the first row on); rows are counted from the
-    // unit's first row, so `past` below is the key position of that row and i0 stays 0
-    const int4 u = __ldg(p.unit_info + blockIdx.y);
-    r = u.x;
-    q_row = u.y;
-    past = u.z;
-    const int n_rem = u.w;
-    L_r = past + n_rem;
-    kend = L_r;
-    // valid rows and KV tiles of query tiles A (0) and B (1); scalars, not arrays, so that a
-    // runtime tile index never forces them into local memory
-    nv0 = max(0, min(128, n_rem));
-    nv1 = max(0, min(128, n_rem - 128));
-    nkt0 = nv0 > 0 ? (past + nv0 + kCtxTileN - 1) / kCtxTileN : 0;
-    nkt1 = nv1 > 0 ? (past + 128 + nv1 + kCtxTileN - 1) / kCtxTileN : 0;
-    item_ok = nv0 > 0 && r >= 0 && r < p.C && past >= 0 && q_row >= 0 && q_row + nv0 + nv1 <= p.T;
-  } else {
+  const bool idle = static_cast<int>(blockIdx.x) >= __ldg(p.counts + kCntTitems);
+  const int gen_row0 = __ldg(p.counts + kCntGenRow0);
+  if (!idle) {
     hk = blockIdx.y;
     const int2 im = p.titem_map[blockIdx.x];
     gr = min(max(im.x, 0), p.G - 1);
@@ -259,11 +242,12 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   }
   if (!idle && !item_ok && threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
   const bool hasB = nv1 > 0;
-  // KV tiles this CTA streams; the first user of the last V tile zeroes its tail
-  const int nT = DEC ? nkt0 + nkt1 : (hasB ? nkt1 : nkt0);
-  const int zero_x = DEC ? (nT - 1) & 1 : ((nkt0 == nT) ? 0 : 1);
-  // tile j of Q tile x: which K / V tile of the stream (ring stage, phase), and which Q slot
-  auto gtile = [&](int j, int x) { return DEC ? 2 * j + x : j; };
+  // KV tiles this CTA streams (A the even ones, B the odd ones); the user of the last V tile
+  // zeroes its tail
+  const int nT = nkt0 + nkt1;
+  const int zero_x = (nT - 1) & 1;
+  // tile j of half x: which K / V tile of the stream (ring stage, phase)
+  auto gtile = [&](int j, int x) { return 2 * j + x; };
 
   const uint32_t sQ = base_s + L::kQOff;
   auto sK = [&](int st) { return base_s + L::kKOff + st * L::kTile; };
@@ -295,29 +279,16 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
       const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
       const int n_pages_seq = (L_r + p.B - 1) / p.B;
-      const int n_q = (hasB && !DEC) ? 2 : 1;  // generation: one Q tile shared by A and B
       const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: warpgroup A re-encodes Q first
-      if (tc::elect_one()) {
-        tc::mbar_arrive_expect_tx(bar(q_bar), n_q * 128 * D * 2);
-        for (int x = 0; x < n_q; ++x)
-          for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sQ + x * L::kTile + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, DEC ? hk * p.group : hq,
-                            DEC ? q_row + (128 / p.group) * x : q_row + 128 * x);
+      if (tc::elect_one()) {  // one Q tile (128 / g tokens x the group's g heads), shared by A and B
+        tc::mbar_arrive_expect_tx(bar(q_bar), 128 * D * 2);
+        for (int dh = 0; dh < D / 64; ++dh)
+          tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, hk * p.group, q_row);
       }
       __syncwarp();
       int issued_k = 0, issued_v = 0;
       bool pok = true;
-#ifdef PKV_SELFTEST
-      // Self-test build only (compiled by the tests, never into libpaged_kv.so): the producer
-      // issues no K / V copy, so the MMA warp's wait for the first K tile and the softmax warps'
-      // waits for their first S run out after the short self-test budget and the CTA winds down
-      // through the timeout path below.  Q has landed before the teardown: no copy in flight.
-      const int n_issue = 0;
-      tc::mbar_wait(bar(q_bar), 0);
-#else
-      const int n_issue = nT;
-#endif
-      for (int j = 0; j < n_issue && !warp_abort(); ++j) {
+      for (int j = 0; j < nT && !warp_abort(); ++j) {
         const int st = stg(j);
         // lane pp < pages_per_tile looks up page pp of the tile (B <= 128: whole pages per tile)
         const int lb = (kt0 + j * kCtxTileN) / p.B + lane;
@@ -397,10 +368,6 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       constexpr uint32_t idesc_s = Q8 ? tc::idesc_f16(128, kCtxTileN, 0) : tc::idesc_bf16(128, kCtxTileN, 0);
       constexpr uint32_t idesc_o = Q8 ? tc::idesc_f16(128, D, 1) : tc::idesc_bf16(128, D, 1);
       auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
-      // context: A and B share every K / V tile (the last one to use it frees it); generation:
-      // each tile has one user
-      auto last_user = [&](int j) { return (hasB && j < nkt1) ? 1 : 0; };
-      auto frees = [&](int j, int x) { return DEC || x == last_user(j); };
       auto kfull = [&](int j, int x) {
         const int g = gtile(j, x);
         if constexpr (F8S) return warp_wait(bar(BAR_RAWK + (g & 1)), (g >> 1) & 1);  // raw codes landed
@@ -410,14 +377,13 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       // (the start address occupies the low bits and never carries out inside a tile): this
       // warp competes for issue slots with a busy softmax warp, so every instruction counts.
       const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
-      const uint64_t dq1 = tc::sdesc_sw128(sQ + L::kTile, 16, 1024);
       // per-stage K / V descriptors: stages are L::kTile apart, i.e. kTile / 16 descriptor units
       const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
       const uint64_t dv0 = tc::sdesc_sw128(sV(0), L::kHalf, 1024);
       auto stage_off = [](int st) { return static_cast<uint64_t>(st) * (L::kTile / 16); };
       auto issue_s = [&](int j, int x) {
         const int st = stg(gtile(j, x));
-        const uint64_t a0 = (DEC || x == 0) ? dq0 : dq1;
+        const uint64_t a0 = dq0;  // A and B share the Q tile
         const uint64_t b0 = dk0 + stage_off(st);
         if constexpr (F8S) {
           // Q hi and lo tiles (one 128-byte row of codes per Q row) sit in the f16 K stage 0
@@ -451,7 +417,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
             }
           }
           tc::mma_commit(bar(BAR_SFULL + x));
-          if (frees(j, x)) tc::mma_commit(bar(BAR_KEMPTY + st));
+          tc::mma_commit(bar(BAR_KEMPTY + st));  // each K / V tile has one user
         }
         __syncwarp();
       };
@@ -460,7 +426,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         tc::fence_after_sync();
         issue_s(0, 0);
         if (hasB) {
-          if (DEC) ok = kfull(0, 1);  // B's first tile is the stream's second
+          ok = kfull(0, 1);  // B's first tile is the stream's second
           if (ok) {
             tc::fence_after_sync();
             issue_s(0, 1);
@@ -469,28 +435,23 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       }
       // no abort-flag poll per tile: a shared-memory load here sits on the critical path
       // (P ready -> next MMA); if another warp gave up, the waits below run out instead
-      for (int j = 0; ok && j < nT; ++j) {
-        bool v_ready = false, k_ready = false;  // context: B reuses the tiles A waited for
+      for (int j = 0; ok && j < nkt0; ++j) {
         for (int x = 0; x < 2 && ok; ++x) {
           if (!uses(j, x)) continue;
           const int g = gtile(j, x);
           if (!warp_wait(bar(BAR_PFULL + x), j & 1)) { ok = false; break; }
-          if (!v_ready) {
-            if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
-            v_ready = !DEC;  // context: B reuses A's tile
-          }
+          if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
           tc::fence_after_sync();
           const uint64_t v0 = dv0 + stage_off(stg(g));
           if (tc::elect_one()) {
             static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
             tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
-            if (frees(j, x)) tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
+            tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
             if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
           }
           __syncwarp();
           if (uses(j + 1, x)) {
-            if (!k_ready && !kfull(j + 1, x)) { ok = false; break; }
-            k_ready = !DEC;
+            if (!kfull(j + 1, x)) { ok = false; break; }
             tc::fence_after_sync();
             issue_s(j + 1, x);
           }
@@ -512,11 +473,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     const uint32_t tS = tmem + 128 * x + lane_off;
     const uint32_t tO = tmem + 256 + 128 * x + lane_off;
     const int nvx = x ? nv1 : nv0, nk = x ? nkt1 : nkt0;
-    const int q_pos = past + i0 + 128 * x + min(row, max(nvx, 1) - 1);  // padding rows mirror the last row
-    // generation rows: the row's token and the new keys it sees (bit j: key past + j)
+    // the row's token and the new keys it sees (bit j: key past + j)
     uint64_t vis = ~0ull;
     int tok_i = 0, hl = 0;
-    if constexpr (DEC) {
+    {
       const int pr = pr0 + row;  // A and B hold the same rows
       if (row < nvx) {
         tok_i = pr / p.group;
@@ -667,38 +627,25 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       tc::reg_dep(v1);
       tc::reg_dep(v2);
       tc::reg_dep(v3);
-      if constexpr (!DEC) {
-        const int lim = q_pos - j * kCtxTileN;  // key column c is visible iff c <= lim
-        if (__any_sync(0xffffffffu, lim < kCtxTileN - 1)) {
+      const int tb = kt0 + gtile(j, x) * kCtxTileN;  // key of column 0
+      if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
+        // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
+        // keys this row's token sees (bits of vis), nothing at or past the split's end
+        auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
+        auto word = [&](int w) {
+          const int t0 = tb + 32 * w, sh = t0 - past;
+          uint32_t nv = 0u;
+          if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
+          else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
+          return (low(past - t0) | nv) & low(kend - t0);
+        };
+        const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v0[e] = e <= lim ? v0[e] : __float_as_uint(-INFINITY);
-            v1[e] = 32 + e <= lim ? v1[e] : __float_as_uint(-INFINITY);
-            v2[e] = 64 + e <= lim ? v2[e] : __float_as_uint(-INFINITY);
-            v3[e] = 96 + e <= lim ? v3[e] : __float_as_uint(-INFINITY);
-          }
-        }
-      } else {
-        const int tb = kt0 + gtile(j, x) * kCtxTileN;  // key of column 0
-        if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
-          // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
-          // keys this row's token sees (bits of vis), nothing at or past the split's end
-          auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
-          auto word = [&](int w) {
-            const int t0 = tb + 32 * w, sh = t0 - past;
-            uint32_t nv = 0u;
-            if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
-            else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
-            return (low(past - t0) | nv) & low(kend - t0);
-          };
-          const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
-            v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
-            v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
-            v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
-          }
+        for (int e = 0; e < 32; ++e) {
+          v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+          v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
+          v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
+          v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
         }
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -777,116 +724,71 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     if (nk > 0) {
       if (ok && !warp_abort() && warp_wait(bar(BAR_ODONE + x), 0)) {
         tc::fence_after_sync();
-        if constexpr (!DEC) {
-          const float inv_l = p.out_scale / l_run;
-          const int grow = q_row + 128 * x + row;
-          // a full tile of 128 rows leaves through shared memory and two TMA stores (one per
-          // 64-wide half): each thread's own row would otherwise be 16 stores spread over 128
-          // different output rows per warp instruction; a partial tile (the end of a request,
-          // whose next rows belong to another request) keeps the per-row stores
-          const bool full = nvx == 128 && q_row + 128 * x + 128 <= p.T;
-          const uint32_t sO = sQ + x * L::kTile;  // this tile's Q slot: all of its S MMAs are done
-          uint16_t* orow = p.out + static_cast<int64_t>(grow) * p.out_stride + static_cast<int64_t>(hq) * D;
-          const bool store = row < nvx && grow < p.T;
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t v[32];
-            tc::tmem_ld32(tO + cc * 32, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              pk[e >> 1] = pack_bf16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
-            if (full) {
-              // 128-byte swizzle of the TMA box: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
-              const uint32_t rbase = sO + (cc >> 1) * L::kHalf + row * 128;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + k) ^ static_cast<uint32_t>(row & 7);
-                st_shared_v4(rbase + chunk * 16, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-              }
-            } else if (store) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                reinterpret_cast<uint4*>(orow + cc * 32)[k] =
-                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-            }
-          }
-          if (full) {
-            tc::fence_proxy_async_smem();
-            tc::named_sync(1 + x, 128);  // the tile's four warps have written their rows
-            if ((warp & 3) == 0 && lane == 0) {
-              for (int dh = 0; dh < D / 64; ++dh) tc::tma_store_4d(&out_map, sO + dh * L::kHalf, 0, dh, hq, q_row + 128 * x);
-              tc::bulk_commit();
-              tc::bulk_wait_read0();
-            }
-          }
+        // the two halves of the split's keys: B hands its (m, l) over through shared memory
+        // (the K ring is idle once both halves are done) and A merges O_A and O_B from TMEM
+        float* xch = reinterpret_cast<float*>(base + (sK(0) - base_s));  // [2][128]
+        if (x == 1) {
+          xch[row] = m_run;
+          xch[128 + row] = l_run;
+          tc::mbar_arrive(bar(BAR_MERGE));
         } else {
-          // the two halves of the split's keys: B hands its (m, l) over through shared memory
-          // (the K ring is idle once both halves are done) and A merges O_A and O_B from TMEM
-          float* xch = reinterpret_cast<float*>(base + (sK(0) - base_s));  // [2][128]
-          if (x == 1) {
-            xch[row] = m_run;
-            xch[128 + row] = l_run;
-            tc::mbar_arrive(bar(BAR_MERGE));
+          float mB = -INFINITY, lB = 0.f;
+          bool merged = true;
+          if (nkt1 > 0) {
+            merged = warp_wait(bar(BAR_MERGE), 0);
+            if (merged) {
+              tc::fence_after_sync();
+              mB = xch[row];
+              lB = xch[128 + row];
+            }
+          }
+          if (!merged) {
+            ok = false;
           } else {
-            float mB = -INFINITY, lB = 0.f;
-            bool merged = true;
-            if (nkt1 > 0) {
-              merged = warp_wait(bar(BAR_MERGE), 0);
-              if (merged) {
-                tc::fence_after_sync();
-                mB = xch[row];
-                lB = xch[128 + row];
+            const float M = fmaxf(m_run, mB), Mb = M == -INFINITY ? 0.f : M;
+            const float fA = ex2_approx(m_run - Mb), fB = ex2_approx(mB - Mb);
+            const float l = fA * l_run + fB * lB;
+            const bool store = row < nvx;
+            const int64_t head = static_cast<int64_t>(hk) * p.group + hl;
+            const bool whole = num_splits == 1;  // else a partial result for the combine
+            const float osc = p.out_scale;
+            const float sA = whole ? fA * osc / l : fA * osc;
+            const float sB = whole ? fB * osc / l : fB * osc;
+            uint16_t* orow = p.out + static_cast<int64_t>(tok0 + tok_i) * p.out_stride + head * D;
+            const int64_t pi =
+                (static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new + tok_i) * p.Hq +
+                head;
+            float* prow = p.part_o + pi * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t va[32], vb[32];
+              tc::tmem_ld32(tO + cc * 32, va);
+              if (nkt1 > 0) {
+                tc::tmem_ld32(tO + 128 + cc * 32, vb);  // O_B, same lanes
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) vb[e] = 0u;
+              }
+              float o[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(va[e]) * sA + __uint_as_float(vb[e]) * sB;
+              if (store && whole) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o[e], o[e + 1]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  reinterpret_cast<uint4*>(orow + cc * 32)[k] =
+                      make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+              } else if (store) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  reinterpret_cast<float4*>(prow + cc * 32)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
               }
             }
-            if (!merged) {
-              ok = false;
-            } else {
-              const float M = fmaxf(m_run, mB), Mb = M == -INFINITY ? 0.f : M;
-              const float fA = ex2_approx(m_run - Mb), fB = ex2_approx(mB - Mb);
-              const float l = fA * l_run + fB * lB;
-              const bool store = row < nvx;
-              const int64_t head = static_cast<int64_t>(hk) * p.group + hl;
-              const bool whole = num_splits == 1;  // else a partial result for the combine
-              const float osc = p.out_scale;
-              const float sA = whole ? fA * osc / l : fA * osc;
-              const float sB = whole ? fB * osc / l : fB * osc;
-              uint16_t* orow = p.out + static_cast<int64_t>(tok0 + tok_i) * p.out_stride + head * D;
-              const int64_t pi =
-                  (static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new + tok_i) * p.Hq +
-                  head;
-              float* prow = p.part_o + pi * D;
-#pragma unroll
-              for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t va[32], vb[32];
-                tc::tmem_ld32(tO + cc * 32, va);
-                if (nkt1 > 0) {
-                  tc::tmem_ld32(tO + 128 + cc * 32, vb);  // O_B, same lanes
-                } else {
-#pragma unroll
-                  for (int e = 0; e < 32; ++e) vb[e] = 0u;
-                }
-                float o[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(va[e]) * sA + __uint_as_float(vb[e]) * sB;
-                if (store && whole) {
-                  uint32_t pk[16];
-#pragma unroll
-                  for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o[e], o[e + 1]);
-#pragma unroll
-                  for (int k = 0; k < 4; ++k)
-                    reinterpret_cast<uint4*>(orow + cc * 32)[k] =
-                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                } else if (store) {
-#pragma unroll
-                  for (int k = 0; k < 8; ++k)
-                    reinterpret_cast<float4*>(prow + cc * 32)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
-              }
-              if (store && !whole) {
-                p.part_ml[pi * 2] = M;
-                p.part_ml[pi * 2 + 1] = l;
-              }
+            if (store && !whole) {
+              p.part_ml[pi * 2] = M;
+              p.part_ml[pi * 2 + 1] = l;
             }
           }
         }
@@ -905,10 +807,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   }
 }
 
-// ---- context mode, persistent: one CTA per SM walks a queue of (unit, query head) items ----
-// The per-item work is that of the context mode above (two 128-row Q tiles sharing every K / V
-// tile, S and O in TMEM, the same softmax); what changes is that a CTA keeps its TMEM, barriers
-// and rings across items, so one item's fill and drain overlap its neighbours:
+// ---- context attention: one CTA per SM walks a queue of (unit, query head) items ----
+// A CTA keeps its TMEM, barriers and rings across items, so one item's fill and drain overlap
+// its neighbours:
 //   - the producer claims the next item (an atomic cursor the plan zeroes) as soon as it has
 //     issued the current item's last K / V tile, publishes it through a two-entry ring in
 //     shared memory, and loads the next Q tile into a slot as soon as the slot's last S MMA is
@@ -920,7 +821,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
 // items; every phase is derived from them.  Items are claimed longest unit first, as the plan
 // sorted them.
 template <int D>
-struct PersistSmem {
+struct CtxSmem {
   static constexpr int kHalf = 128 * 128;
   static constexpr int kTile = (D / 64) * kHalf;
   static constexpr int kStages = 2;
@@ -954,9 +855,9 @@ enum {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-context_persistent_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
-                          const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
-  using L = PersistSmem<D>;
+context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
+                    const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap out_map) {
+  using L = CtxSmem<D>;
   constexpr int S = L::kStages;
   static_assert(S == 2, "ring stage and phase below are bit operations");
   // ring stage and phase of the g-th K / V tile of the stream (g >= 0)
@@ -1515,22 +1416,20 @@ cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s) {
   return launch_pdl(stage_q8_kernel<false>, dim3(p.total_pages), dim3(kStageThreads), 0, s, p);
 }
 
-template <int D, bool DEC, int KV>
-cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& om,
-                             cudaStream_t s) {
-  auto kern = context_attn_kernel<D, DEC, KV>;
-  constexpr int bytes = CtxSmem<D, DEC, KV>::kBytes;
+template <int D, int KV>
+cudaError_t launch_gen_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, cudaStream_t s) {
+  auto kern = gen_attn_kernel<D, KV>;
+  constexpr int bytes = GenSmem<D, KV>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid = DEC ? dim3(p.num_titems, p.Hkv) : dim3(p.Hq, p.num_tiles);
-  return launch_pdl(kern, grid, dim3(kThreads), bytes, s, p, qm, km, om);
+  return launch_pdl(kern, dim3(p.num_titems, p.Hkv), dim3(kThreads), bytes, s, p, qm, km);
 }
 
 template <int D>
-cudaError_t launch_context_persistent(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km,
-                                      const CUtensorMap& om, cudaStream_t s) {
-  auto kern = context_persistent_kernel<D>;
-  constexpr int bytes = PersistSmem<D>::kBytes;
+cudaError_t launch_context_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km,
+                             const CUtensorMap& om, cudaStream_t s) {
+  auto kern = context_attn_kernel<D>;
+  constexpr int bytes = CtxSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int64_t items = static_cast<int64_t>(p.num_tiles) * p.Hq;
@@ -1538,19 +1437,22 @@ cudaError_t launch_context_persistent(const ContextParams& p, const CUtensorMap&
   return launch_pdl(kern, dim3(grid), dim3(kThreads), bytes, s, p, qm, km, om);
 }
 
-cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map, bool dec,
+cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map,
                            cudaStream_t s) {
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
   const CUtensorMap& om = *static_cast<const CUtensorMap*>(out_map);
-  if (dec && p.kv_dtype != PKV_BF16) {  // 8-bit codes, converted in shared memory (head_dim 128)
+  return p.D == 128 ? launch_context_t<128>(p, qm, km, om, s) : launch_context_t<64>(p, qm, km, om, s);
+}
+
+cudaError_t launch_gen_tc(const ContextParams& p, const void* q_map, const void* kv_map, cudaStream_t s) {
+  const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
+  const CUtensorMap& km = *static_cast<const CUtensorMap*>(kv_map);
+  if (p.kv_dtype != PKV_BF16) {  // 8-bit codes, converted in shared memory (head_dim 128)
     if (p.D != 128) return cudaErrorInvalidValue;
-    return p.kv_dtype == PKV_INT8 ? launch_context_t<128, true, PKV_INT8>(p, qm, km, om, s)
-                                  : launch_context_t<128, true, PKV_FP8_E4M3>(p, qm, km, om, s);
+    return p.kv_dtype == PKV_INT8 ? launch_gen_t<128, PKV_INT8>(p, qm, km, s) : launch_gen_t<128, PKV_FP8_E4M3>(p, qm, km, s);
   }
-  if (p.D == 128)
-    return dec ? launch_context_t<128, true, 0>(p, qm, km, om, s) : launch_context_persistent<128>(p, qm, km, om, s);
-  return dec ? launch_context_t<64, true, 0>(p, qm, km, om, s) : launch_context_persistent<64>(p, qm, km, om, s);
+  return p.D == 128 ? launch_gen_t<128, 0>(p, qm, km, s) : launch_gen_t<64, 0>(p, qm, km, s);
 }
 
 }  // namespace pkv

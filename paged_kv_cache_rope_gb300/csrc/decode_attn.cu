@@ -19,7 +19,7 @@
 //     with a cp.async ring through shared memory (zero-fill past the sequence end, one
 //     block-table lookup per tile) and merge in shared memory at the end;
 //     wide kernel (more columns, 8-bit pools or groups that do not divide 128; bf16 pools with
-//     such requests otherwise take the tcgen05 kernel's generation mode): the warps share one
+//     such requests otherwise take the tcgen05 generation kernel): the warps share one
 //     ring and each owns 16 columns over every tile;
 //   * online softmax in base 2 with warp-shuffle column maxima; draft-token visibility as a
 //     64-bit mask per column, applied only to tiles that hold new keys;

@@ -161,10 +161,10 @@ struct ContextParams {
   float scale_log2;
   float out_scale;          // multiplies O at the end (the FP8 dequantisation scale, else 1)
   int32_t* d_error;
-  // generation mode (wide generation requests on the tensor-core kernel): CTA = titem_map
+  // generation kernel (wide generation requests on the tensor cores): CTA = titem_map
   // entry (generation request, split x row group) x KV head
   int32_t G, kv_chunk, num_titems, mask_words;
-  int32_t kv_dtype;         // generation mode: pool element kind (pkv_dtype); 8-bit codes are
+  int32_t kv_dtype;         // generation kernel: pool element kind (pkv_dtype); 8-bit codes are
                             // converted to f16 in shared memory (head_dim 128 only)
   int64_t total_parts;
   const int2* titem_map;
@@ -217,11 +217,12 @@ cudaError_t launch_decode(const DecodeParams& p, int kv_dtype, bool wide, cudaSt
 cudaError_t launch_combine(const DecodeParams& p, int max_splits, cudaStream_t s);
 cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s);
 // q_map / kv_map are CUtensorMap objects (128-byte, opaque here) built by the front end.
-// dec = false: context units; true: wide generation requests (rows = (token, head) pairs of one
-// KV head, q_map boxes g heads x 128/g tokens, partial results for split requests).
-// out_map: the output rows as a tiled map (box 128 rows x 64 columns of one head) for the
-// context tiles' TMA stores; unused by the generation mode.
+// Context units (persistent kernel, at most num_ctas CTAs); out_map: the output rows as a tiled
+// map (box 128 rows x 64 columns of one head) for the full tiles' TMA stores.
 cudaError_t launch_context(const ContextParams& p, const void* q_map, const void* kv_map, const void* out_map,
-                           bool dec, cudaStream_t s);
+                           cudaStream_t s);
+// Wide generation requests on the tensor cores (rows = (token, head) pairs of one KV head, q_map
+// boxes g heads x 128/g tokens, partial results for split requests).
+cudaError_t launch_gen_tc(const ContextParams& p, const void* q_map, const void* kv_map, cudaStream_t s);
 
 }  // namespace pkv

@@ -3,7 +3,7 @@ lengths, position offsets, packed mask; the Medusa candidate tree on page "Tenso
 拆解(一)") through the C-ABI against the fp64 oracle: draft tokens rotated for past + offset and
 stored at past + i (bit-exact pool and q_out), attention under chain (causal) or tree masks.
 Narrow requests run on the split-KV decode kernel, whose score-tile columns are (token, query
-head) pairs of one KV head; wider ones on the tcgen05 kernel's generation mode (rows = those
+head) pairs of one KV head; wider ones on the tcgen05 generation kernel (rows = those
 pairs; 8-bit pools at head_dim 128 have their codes converted to f16 in shared memory) or, for
 groups that do not divide 128 and 8-bit pools at head_dim 64, on the wide mma.sync kernel."""
 import dataclasses
@@ -27,7 +27,7 @@ CASES = [
     ("chain_gqa16", [], [(2, 64), (3, 4100), 700], 32, 2, 128, 128, False),
     ("group32_single", [], [900, 33, 4097], 64, 2, 128, 64, False),
     ("mixed_ctx_tree", [(200, 64), (31, 0)], [(6, 500), 1200, (9, 2500)], 16, 4, 128, 32, True),
-    # tensor-core generation mode: one head per row (g = 1), several 128-row groups per request
+    # tensor-core generation kernel: one head per row (g = 1), several 128-row groups per request
     ("tree_mha_d64_64tok", [], [(64, 300), (20, 5000), 70], 4, 4, 64, 16, True),
     ("tree_gqa8_row_groups", [], [(20, 700), (64, 2000), (16, 4100)], 16, 2, 128, 32, True),
     # 16-token pages: eight pages per 128-key tile (one TMA box per producer lane)
