@@ -88,6 +88,30 @@ def test_context_matches_oracle(case, kv_dtype):
         assert max_err(got, unq, label="unquantised") <= max_err(o.out, unq, label="unquantised") + FP8_DEQ_TOL
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("D", [128, 64])
+def test_context_many_units_per_cta(D, kv_dtype):
+    """More (unit, query head) items than SMs: every persistent context CTA claims several items
+    of different shapes in turn (full and partial 256-row units, long and short cached prefixes,
+    one-row requests), carrying its rings, TMEM and the output staging tile from one item to the
+    next.  Every row of every head is checked against the oracle."""
+    rng = np.random.default_rng(77 + D)
+    ctx = []
+    for i in range(40):
+        n = int(rng.choice([1, 5, 128, 129, 256, 300, 511, 600]))
+        ctx.append((n, int(rng.integers(0, 700))))
+    b = _batch(f"many_units_d{D}", ctx, [], 8, 2, D, 32, kv_dtype)
+    units = sum((n + 255) // 256 for n, _ in ctx)
+    assert units * 8 > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    g = gpu_run(b)
+    assert g.error == 0
+    o = oracle_run(b)
+    assert o.status == 0
+    assert max_err(gpu_out_f64(g, b), o.out) <= (BF16_TOL if kv_dtype == "bf16" else FP8_DEQ_TOL)
+    g2 = gpu_run(b)  # the queue order differs from run to run; the results do not
+    assert torch.equal(g.out, g2.out)
+
+
 def test_deterministic_and_page_permutation_invariant():
     b = _batch("perm", [(200, 100)], [900, 45, 3000], 16, 4, 128, 32)
     g1, g2 = gpu_run(b), gpu_run(b)
