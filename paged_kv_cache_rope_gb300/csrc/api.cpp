@@ -475,6 +475,48 @@ int append_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& hp
   return cuda_status(e);
 }
 
+// Persistent context CTAs when the generation kernels run beside the context kernel.  A context
+// CTA holds its SM (all of its shared memory and registers) until the unit queue is empty, so
+// the generation kernels on the auxiliary stream get only the SMs it leaves free.  On a bf16 pool
+// the generation kernels stream at the HBM limit from about two thirds of the SMs, so the context
+// kernel gets the share that lets both finish together: the N minimising
+//   max(Tc * S / N, Tg * max(1, (2S/3) / (S - N)))
+// with Tc the context kernel's time alone (1.45 us per pair of 128-row Q tile and 128-key tile
+// and 1.9 us per (unit, query head) per SM, times 1.3 for running beside HBM-bound work) and Tg
+// the generation requests' K and V bytes at 6.3 TB/s (calibrated on GB300 over mixes of 2 to 16
+// chunked contexts with 64 to 128 decodes and over the 16K prefill beside 8 long decodes: steps
+// 5-12% shorter than with every SM).  8-bit pools (their decode is bound by instruction issue,
+// not by HBM) and bucket plans (the lengths are on the device only) keep every SM.
+int context_ctas(const pkv_pool* pool, const pkv_batch* b, const HostPlan& hp, int Hq, int S) {
+  if (hp.dyn || pool->dtype != PKV_BF16 || hp.G == 0 || S < 8) return S;
+  double tile_pairs = 0.0, items = 0.0;
+  for (int r = 0; r < hp.C; ++r) {
+    const int64_t n = b->h_context_lengths[r], c = b->h_past_kv_lengths[r];
+    for (int64_t j = 0; pkv::kCtxRowsPerCta * j < n; ++j) {
+      const int64_t first = pkv::kCtxRowsPerCta * j;
+      const int64_t rows = std::min<int64_t>(pkv::kCtxRowsPerCta, n - first);
+      tile_pairs += static_cast<double>((c + first + rows + pkv::kCtxTileN - 1) / pkv::kCtxTileN);
+      items += 1.0;
+    }
+  }
+  double gen_keys = 0.0;
+  for (int r = hp.C; r < hp.R; ++r)
+    gen_keys += static_cast<double>(b->h_past_kv_lengths[r]) + static_cast<double>(b->h_context_lengths[r]);
+  const double t_ctx = 1.3 * (tile_pairs * 1.45 + items * 1.9) * Hq / S;                       // us
+  const double t_gen = gen_keys * pool->num_kv_heads * pool->head_dim * 4.0 / 6.3e6;           // us
+  const double m_sat = 2.0 * S / 3.0;
+  int best = S;
+  double best_t = t_ctx + t_gen;  // every SM: the generation work mostly waits for the context
+  for (int n = std::max(1, S / 8); n < S; ++n) {
+    const double t = std::max(t_ctx * S / n, t_gen * std::max(1.0, m_sat / (S - n)));
+    if (t < best_t) {
+      best_t = t;
+      best = n;
+    }
+  }
+  return best;
+}
+
 // The attention's argument checks and launches, shared by the exact and the bucket entry
 // points: every grid comes from the plan's counts (exact) or capacities (bucket); the kernels
 // read the device plan's counts and skip what this batch does not use.
@@ -605,7 +647,7 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
     cp.NB = static_cast<int32_t>(ctx_blocks);
     cp.max_blocks = batch->max_blocks_per_seq;
     cp.num_tiles = hp.num_tiles;
-    cp.num_ctas = device_sm_count();
+    cp.num_ctas = aux ? context_ctas(pool, batch, hp, num_q_heads, device_sm_count()) : device_sm_count();
     cp.counts = counts;
     cp.cursor = ws + hp.lay.counts + pkv::kCntCursor;
     cp.cu_q = ws + hp.lay.cu_q;
