@@ -475,21 +475,12 @@ int append_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& hp
   return cuda_status(e);
 }
 
-// Persistent context CTAs when the generation kernels run beside the context kernel.  A context
-// CTA holds its SM (all of its shared memory and registers) until the unit queue is empty, so
-// the generation kernels on the auxiliary stream get only the SMs it leaves free.  On a bf16 pool
-// the generation kernels stream at the HBM limit from about two thirds of the SMs, so the context
-// kernel gets the share that lets both finish together: the N minimising
-//   max(Tc * S / N, Tg * max(1, (2S/3) / (S - N)))
-// with Tc the context kernel's time alone (1.45 us per pair of 128-row Q tile and 128-key tile
-// and 1.9 us per (unit, query head) per SM, times 1.3 for running beside HBM-bound work) and Tg
-// the generation requests' K and V bytes at 6.3 TB/s (calibrated on GB300 over mixes of 2 to 16
-// chunked contexts with 64 to 128 decodes and over the 16K prefill beside 8 long decodes: steps
-// 5-12% shorter than with every SM).  8-bit pools (their decode is bound by instruction issue,
-// not by HBM) and bucket plans (the lengths are on the device only) keep every SM.
+// Persistent context CTAs beside the generation kernels (pkv::context_cta_share) from the host
+// lengths of an exact plan; 8-bit pools (their decode is bound by instruction issue, not by HBM)
+// keep every SM, and bucket plans leave the choice to the plan kernel.
 int context_ctas(const pkv_pool* pool, const pkv_batch* b, const HostPlan& hp, int Hq, int S) {
   if (hp.dyn || pool->dtype != PKV_BF16 || hp.G == 0 || S < 8) return S;
-  double tile_pairs = 0.0, items = 0.0;
+  double tile_pairs = 0.0, items = 0.0;  // per query head
   for (int r = 0; r < hp.C; ++r) {
     const int64_t n = b->h_context_lengths[r], c = b->h_past_kv_lengths[r];
     for (int64_t j = 0; pkv::kCtxRowsPerCta * j < n; ++j) {
@@ -502,19 +493,8 @@ int context_ctas(const pkv_pool* pool, const pkv_batch* b, const HostPlan& hp, i
   double gen_keys = 0.0;
   for (int r = hp.C; r < hp.R; ++r)
     gen_keys += static_cast<double>(b->h_past_kv_lengths[r]) + static_cast<double>(b->h_context_lengths[r]);
-  const double t_ctx = 1.3 * (tile_pairs * 1.45 + items * 1.9) * Hq / S;                       // us
-  const double t_gen = gen_keys * pool->num_kv_heads * pool->head_dim * 4.0 / 6.3e6;           // us
-  const double m_sat = 2.0 * S / 3.0;
-  int best = S;
-  double best_t = t_ctx + t_gen;  // every SM: the generation work mostly waits for the context
-  for (int n = std::max(1, S / 8); n < S; ++n) {
-    const double t = std::max(t_ctx * S / n, t_gen * std::max(1.0, m_sat / (S - n)));
-    if (t < best_t) {
-      best_t = t;
-      best = n;
-    }
-  }
-  return best;
+  return pkv::context_cta_share(static_cast<float>(tile_pairs), static_cast<float>(items), static_cast<float>(gen_keys), Hq,
+                                pool->num_kv_heads, pool->head_dim, S);
 }
 
 // The attention's argument checks and launches, shared by the exact and the bucket entry
@@ -534,6 +514,13 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t* ws = static_cast<int32_t*>(workspace);
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  // generation work on the auxiliary stream when a context kernel runs beside it; while the
+  // caller has per-kernel timing events set, every kernel stays on `stream` so that each pair
+  // of events brackets one kernel's own work
+  const bool has_ctx = hp.num_tiles > 0;
+  const bool has_gen = hp.num_items + hp.num_witems + hp.num_titems > 0;
+  const bool concurrent = has_ctx && has_gen && !g_events;
 
   pkv::PlanParams pp{};
   pp.R = hp.R;
@@ -556,6 +543,9 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
   pp.max_ctx_tokens = hp.max_ctx_tokens;
   pp.max_kv_len = hp.max_kv_len;
   pp.max_gen_tokens = hp.max_gen_tokens;
+  pp.ctx_share = (concurrent && hp.dyn && pool->dtype == PKV_BF16) ? 1 : 0;
+  pp.num_sms = device_sm_count();
+  pp.D = D;
   pp.cap_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
   pp.cap_tiles = hp.num_tiles;
   pp.cap_splits = hp.num_splits;
@@ -575,13 +565,8 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   ++launches;
 
-  // generation work on the auxiliary stream when a context kernel runs beside it; while the
-  // caller has per-kernel timing events set, every kernel stays on `stream` so that each pair
-  // of events brackets one kernel's own work
-  const bool has_ctx = hp.num_tiles > 0;
-  const bool has_gen = hp.num_items + hp.num_witems + hp.num_titems > 0;
   const int32_t* counts = ws + hp.lay.counts;
-  AuxStream* aux = (has_ctx && has_gen && !g_events) ? aux_stream_for_current_device(s) : nullptr;
+  AuxStream* aux = concurrent ? aux_stream_for_current_device(s) : nullptr;
   std::unique_lock<std::mutex> aux_hold;
   const cudaStream_t cs = s;  // context kernels
   cudaStream_t gs = s;        // generation kernels

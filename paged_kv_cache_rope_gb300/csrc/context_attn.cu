@@ -914,6 +914,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   pdl_wait();
 
   const int n_items = __ldg(p.counts + kCntUnits) * p.Hq;
+  // CTAs that take work: the grid, or fewer when the plan leaves SMs to the generation kernels
+  // running beside this one (the others go straight to the teardown)
+  const int active = min(static_cast<int>(gridDim.x), __ldg(p.counts + kCntCtxCtas));
   // An item: query head hq of unit y (the plan's descriptor: request, first q row, key position
   // of that row, rows of the request from there on).  Every role derives the same geometry.
   struct Item {
@@ -970,7 +973,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     tc::regs_dec<kRegsControl>();
     if (warp == kProducerWarp) {
       // ======================= item queue + TMA producer =======================
-      int w = blockIdx.x;
+      int w = static_cast<int>(blockIdx.x) < active ? static_cast<int>(blockIdx.x) : n_items;
       int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items)
       int nq0 = 0, nq1 = 0;            // Q loads per slot
       bool pok = true;
@@ -1054,7 +1057,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         if (!pok) break;
         // claim the next item while this one's tiles are still being consumed
         int nxt = 0;
-        if (lane == 0) nxt = atomicAdd(p.cursor, 1) + static_cast<int>(gridDim.x);
+        if (lane == 0) nxt = atomicAdd(p.cursor, 1) + active;
         w = __shfl_sync(0xffffffffu, nxt, 0);
       }
       if (!pok && lane == 0) fail();

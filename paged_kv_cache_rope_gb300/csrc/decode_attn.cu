@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ Int8v s_carry;
   __shared__ int32_t s_ctx_rows;
   __shared__ int32_t s_units;
+  __shared__ unsigned long long s_gen_keys, s_tile_pairs;  // for the context CTA share
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int32_t* counts = p.ws + p.lay.counts;
   int32_t* cu = p.ws + p.lay.cu_q;
@@ -119,6 +120,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   if (tid == 0) {
     s_carry = Int8v{z4, z4};
     s_ctx_rows = 0;
+    s_gen_keys = 0ull;
+    s_tile_pairs = 0ull;
   }
   __syncthreads();
   // rows of the context requests: generation row k is packed row (context rows) + k
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   }
   __syncthreads();
   const int gen_row0 = s_ctx_rows;
+  unsigned long long gen_keys = 0ull;  // this thread's generation requests' keys
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + tid;
     // a: (new tokens, context units, generation splits, staged 8-bit context pages)
@@ -155,6 +159,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         x.a.y = (n + kCtxRowsPerCta - 1) / kCtxRowsPerCta;
         if (staging && n > 0) x.a.w = (past + n + p.B - 1) / p.B;
       } else if (n > 0) {
+        gen_keys += static_cast<unsigned long long>(past + n);
         const int sr = (past + n + chunk - 1) / chunk, ncols = n * p.group;
         x.a.z = sr;
         if (ncols <= kDecodeNarrowMaxCols) x.b.x = sr * ((ncols + cols - 1) / cols);
@@ -215,12 +220,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   if (tid == 0) {
     // the counts every later kernel of the call reads; a rejected batch runs nothing
     const Int8v t = s_carry;
-    const int32_t v[kCntWords] = {t.a.x, gen_row0, t.a.x - gen_row0, t.a.y, t.b.x, t.b.z, t.b.w, t.b.y, t.a.w};
+    // (the cursor starts at zero; every launched context CTA takes work unless the share below
+    // says otherwise)
+    const int32_t v[kCntWords] = {t.a.x, gen_row0, t.a.x - gen_row0, t.a.y, t.b.x, t.b.z, t.b.w, t.b.y, t.a.w, 0,
+                                  1 << 30};
 #pragma unroll
     for (int i = 0; i < kCntWords; ++i) counts[i] = any_bad ? 0 : v[i];
     if (any_bad) flag_error(p.d_error, dyn ? PKV_DEVERR_BUCKET : PKV_DEVERR_PLAN_MISMATCH);
   }
   if (any_bad) return;
+  if (p.ctx_share) {  // the generation requests' keys, for the context CTA share below
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gen_keys += __shfl_xor_sync(0xffffffffu, gen_keys, o);
+    if (lane == 0 && gen_keys) atomicAdd(&s_gen_keys, gen_keys);
+  }
 
   // ---- context units, most KV tiles first: a counting sort by tile count (descending) ----
   // Each slot gets the unit's descriptor (request, first q row, past + first row, rows left), so
@@ -249,8 +262,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int keys = d.z + min(kCtxRowsPerCta, d.w);
     return min(kBins - 1, (keys + kCtxTileN - 1) / kCtxTileN);
   };
-  for (int u = tid; u < U; u += kPlanThreads) atomicAdd(&s_hist[kBins - 1 - unit_cost(unit_desc(u))], 1);
+  unsigned long long tile_pairs = 0ull;
+  for (int u = tid; u < U; u += kPlanThreads) {
+    const int c = unit_cost(unit_desc(u));
+    tile_pairs += static_cast<unsigned long long>(c);
+    atomicAdd(&s_hist[kBins - 1 - c], 1);
+  }
+  if (p.ctx_share) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tile_pairs += __shfl_xor_sync(0xffffffffu, tile_pairs, o);
+    if (lane == 0 && tile_pairs) atomicAdd(&s_tile_pairs, tile_pairs);
+  }
   __syncthreads();
+  if (p.ctx_share && tid == 0)  // bucket plan, bf16 pool, generation kernels beside the context kernel
+    counts[kCntCtxCtas] = context_cta_share(static_cast<float>(s_tile_pairs), static_cast<float>(U),
+                                            static_cast<float>(s_gen_keys), p.Hq, p.Hkv, p.D, p.num_sms);
   // exclusive scan of the (reversed) histogram: each thread owns kBins / kPlanThreads bins
   constexpr int kPer = kBins / kPlanThreads;
   int own = 0;

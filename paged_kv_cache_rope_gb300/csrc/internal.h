@@ -37,6 +37,7 @@ enum PlanCount {
   kCntParts = 7,       // split-KV partial rows per query head
   kCntStagePages = 8,  // 8-bit pools: staged context pages
   kCntCursor = 9,      // work-queue cursor of the context kernel (written as zero by the plan)
+  kCntCtxCtas = 10,    // context CTAs that take work (the rest exit at once), see context_cta_share
   kCntWords = 16
 };
 
@@ -97,6 +98,54 @@ struct AppendParams {
 // Without a bucket (dyn = 0) the cap_* fields are the exact counts the host planned from its
 // copies of the lengths, and a device count that differs is a plan mismatch.  With a bucket
 // (dyn = 1) they are capacities: the grids' sizes for the bucket's largest batch.
+#if defined(__CUDACC__)
+#define PKV_HD __host__ __device__
+#else
+#define PKV_HD
+#endif
+
+// Persistent context CTAs when the generation kernels run beside the context kernel.  A context
+// CTA holds its SM (all of its shared memory and registers) until the unit queue is empty, so
+// the generation kernels get only the SMs it leaves free.  On a bf16 pool the generation kernels
+// stream at the HBM limit from about two thirds of the SMs, so the context kernel gets the share
+// that lets both finish together: the N minimising
+//   max(Tc * S / N, Tg * max(1, (2S/3) / (S - N)))
+// with Tc the context kernel's time alone (1.45 us per pair of 128-row Q tile and 128-key tile
+// and 1.9 us per (unit, query head), per SM, times 1.3 for running beside HBM-bound work) and Tg
+// the generation requests' K and V bytes at 6.3 TB/s (calibrated on GB300 over mixes of 2 to 16
+// chunked contexts with 64 to 128 decodes and over the 16K prefill beside 8 long decodes: steps
+// 5-12% shorter than with every SM).  tile_pairs and units are per query head.
+PKV_HD inline int context_cta_share(float tile_pairs, float units, float gen_keys, int Hq, int Hkv, int D, int S) {
+  if (S < 8) return S;
+  const float t_ctx = 1.3f * (tile_pairs * 1.45f + units * 1.9f) * Hq / S;  // us
+  const float t_gen = gen_keys * Hkv * D * 4.0f / 6.3e6f;                   // us
+  if (!(t_gen > 0.f)) return S;
+  // cost(N) = max(t_ctx S / N, t_gen max(1, m_sat / (S - N))): the first term falls and the
+  // second rises with N, so the best N is where they cross (or an end of [S/8, S - 1]); with
+  // every SM the generation work mostly waits for the context.  Closed form, no loop: the plan
+  // kernel evaluates this on one thread.
+  const float a = t_ctx * S, m_sat = 2.0f * S / 3.0f;
+  float n = a / t_gen;                                    // crossing with S - N >= m_sat
+  if (n > S - m_sat) n = a * S / (a + t_gen * m_sat);    // crossing with S - N < m_sat
+  auto cost = [&](int k) {
+    const float tc = a / k, tg = t_gen * (m_sat > S - k ? m_sat / (S - k) : 1.0f);
+    return tc > tg ? tc : tg;
+  };
+  int best = S;
+  float best_t = t_ctx + t_gen;
+  const int lo = S / 8, hi = S - 1;
+  const int k0 = static_cast<int>(n);
+  for (int k = k0; k <= k0 + 1; ++k) {
+    const int kc = k < lo ? lo : (k > hi ? hi : k);
+    const float t = cost(kc);
+    if (t < best_t) {
+      best_t = t;
+      best = kc;
+    }
+  }
+  return best;
+}
+
 struct PlanParams {
   int32_t R, C, G, T, Hkv, B, cap_tiles, cap_splits, kv_chunk, cap_stage_pages;
   int32_t Hq, group;
@@ -108,6 +157,9 @@ struct PlanParams {
   int32_t dyn;
   // bucket limits (dyn = 1): a batch over any of them is rejected (PKV_DEVERR_BUCKET)
   int32_t max_ctx_tokens, max_kv_len, max_gen_tokens;
+  // 1: the plan picks the context CTAs beside the generation kernels (context_cta_share) from
+  // the device lengths (bucket plans on a bf16 pool); 0: every launched context CTA takes work
+  int32_t ctx_share, num_sms, D;
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words
