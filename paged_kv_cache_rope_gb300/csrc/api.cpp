@@ -238,7 +238,8 @@ void plan_layout(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan*
   L.item_map = (L.part_prefix + hp->G + 1 + 1) & ~1LL;  // int2 entries: 8-byte aligned
   L.witem_map = L.item_map + 2LL * hp->num_items;
   L.titem_map = L.witem_map + 2LL * hp->num_witems;
-  L.row_map = (L.titem_map + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
+  L.titem_order = L.titem_map + 2LL * hp->num_titems;
+  L.row_map = (L.titem_order + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
   L.unit_info = L.row_map + 4LL * hp->gen_rows;                 // int4 entries: 16-byte aligned
   L.stage_prefix = L.unit_info + 4LL * hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (hp->staging ? hp->C + 1 : 0);
@@ -744,10 +745,12 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
       tp.d_error = d_error;
       tp.G = hp.G;
       tp.counts = counts;
+      tp.num_ctas = device_sm_count();
+      tp.gen_cursor = ws + hp.lay.counts + pkv::kCntGenCursor;
       tp.kv_chunk = hp.kv_chunk;
       tp.num_titems = hp.num_titems;
       tp.total_parts = hp.num_parts;
-      tp.titem_map = reinterpret_cast<const int2*>(ws + hp.lay.titem_map);
+      tp.titem_map = reinterpret_cast<const int2*>(ws + hp.lay.titem_order);  // most KV tiles first
       tp.split_prefix = ws + hp.lay.split_prefix;
       tp.part_prefix = ws + hp.lay.part_prefix;
       tp.mask = batch->d_packed_mask;

@@ -85,7 +85,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could
 // consumer and the two halves alternate.
 // With an 8-bit pool (KV != 0): Q, K[2], V[2] (f16; for E4M3 the K[0] area holds the
 // hi and lo E4M3 Q tiles instead), a ring of the raw codes (K[2], V[2]) that TMA fills and the
-// softmax warpgroups convert, and the per-row Q scales.
+// softmax warpgroups convert, and the per-row Q scales.  Then B's (m, l) per row for A's
+// merge (its own area: the K ring already holds the next item's tiles when an item ends).
 template <int D, int KV = 0>
 struct GenSmem {
   static constexpr bool kQ8 = KV != 0;
@@ -99,9 +100,10 @@ struct GenSmem {
   static constexpr int kRawKOff = kVOff + kStages * kTile;
   static constexpr int kRawVOff = kRawKOff + (kQ8 ? 2 : 0) * kRawTile;
   static constexpr int kBarOff = kRawVOff + (kQ8 ? 2 : 0) * kRawTile;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 320;
   static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 1 / (Q row's power-of-two scale)
-  static constexpr int kBytes = kQScaleOff + (kQ8 ? 128 * 4 : 0) + 1024;  // + alignment slack
+  static constexpr int kXchOff = kQScaleOff + (kQ8 ? 128 * 4 : 0);  // [2][128] floats: B's m, l
+  static constexpr int kBytes = kXchOff + 2 * 128 * 4 + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
   static_assert(!kQ8 || D == 128, "8-bit codes only at head_dim 128");
 };
@@ -122,7 +124,12 @@ enum {
   BAR_RAWKEMPTY = 25, // +2: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
   BAR_RAWVEMPTY = 27, // +2: a raw V stage has been converted
   BAR_QRAW = 29,   // the bf16 Q tile landed (warpgroup A rescales and re-encodes it)
-  NUM_BARS = 30
+  BAR_QFREE = 30,  // an item's last S MMA is done: its Q tile (and re-encoding) may be replaced
+  BAR_ITEM = 31,   // +2: item ring entry written
+  BAR_ITEMFREE = 33,  // +2: item ring entry read by the MMA warp and the eight softmax warps
+  BAR_IDONE = 35,  // an item is finished by the MMA warp (issued) and the eight softmax warps
+  BAR_QSREAD = 36, // 8-bit pool: warpgroup A has read the item's Q row scales
+  NUM_BARS = 37
 };
 
 
@@ -149,6 +156,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L::kBarOff + 8 * NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * NUM_BARS + 4);
+  volatile int* s_item = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * NUM_BARS + 8);  // [2]
+  static_assert(8 * NUM_BARS + 16 <= L::kBarBytes, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -181,6 +190,13 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     }
     tc::mbar_init(bar(BAR_MMADONE), 1);
     tc::mbar_init(bar(BAR_MERGE), 128);
+    tc::mbar_init(bar(BAR_QFREE), 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(BAR_ITEM + s), 1);
+      tc::mbar_init(bar(BAR_ITEMFREE + s), 9);  // the MMA warp and the eight softmax warps
+    }
+    tc::mbar_init(bar(BAR_IDONE), 9);
+    tc::mbar_init(bar(BAR_QSREAD), 4);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -199,55 +215,55 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 
   pdl_wait();
 
-  // ---- the work item ----
-  // CTA = (generation request, KV head hk, split of the keys, group of 128 rows); rows are the
+  // ---- work items: (tensor-core generation CTA of the plan, KV head hk) ----
+  // Item = (generation request, KV head hk, split of the keys, group of 128 rows); rows are the
   // (token i, query head hk*g + hl) pairs r = i*g + hl of the request's new tokens, keys
   // kt0 .. kend-1 of the split, visibility per draft-token mask; partial results go to the split
-  // workspace when the request has several splits.
-  int hk = 0, r = 0, past = 0, L_r = 0, nv0 = 0, nv1 = 0, nkt0 = 0, nkt1 = 0, kt0 = 0, kend = 0, q_row = 0;
-  int gr = 0, n_new = 0, s_idx = 0, num_splits = 1, pr0 = 0, tok0 = 0;
-  bool item_ok = false;
-  // the plan's counts: a CTA past this batch's share of the grid (a bucket's spare one) has no
-  // work and goes straight to the teardown
-  const bool idle = static_cast<int>(blockIdx.x) >= __ldg(p.counts + kCntTitems);
+  // workspace when the request has several splits.  A CTA claims items from a queue (a cursor
+  // the plan zeroes), keeps its TMEM, barriers and rings across them, and every role derives the
+  // same geometry from the item index.  The softmax warps start an item, and the MMA warp its
+  // first PV, only once all nine have finished the previous one (the item's first S MMAs go out
+  // before); the producer runs ahead (the next item's Q once the previous item's last S MMA is
+  // done, its K / V tiles as stages free up).
+  const int n_items = __ldg(p.counts + kCntTitems) * p.Hkv;
   const int gen_row0 = __ldg(p.counts + kCntGenRow0);
-  if (!idle) {
-    hk = blockIdx.y;
-    const int2 im = p.titem_map[blockIdx.x];
-    gr = min(max(im.x, 0), p.G - 1);
-    r = p.C + gr;
-    n_new = __ldg(p.ctx_len + r);
-    past = __ldg(p.past + r);
-    L_r = past + n_new;
-    const int rows = n_new * p.group;
+  struct Item {
+    int hk, r, past, L_r, nv0, nv1, nkt0, nkt1, kt0, kend, q_row, gr, n_new, s_idx, num_splits, pr0, tok0;
+    bool ok;
+  };
+  auto item_of = [&](int w) {
+    Item it;
+    const int ti = w / p.Hkv;
+    it.hk = w - ti * p.Hkv;
+    const int2 im = p.titem_map[ti];
+    it.gr = min(max(im.x, 0), p.G - 1);
+    it.r = p.C + it.gr;
+    it.n_new = __ldg(p.ctx_len + it.r);
+    it.past = __ldg(p.past + it.r);
+    it.L_r = it.past + it.n_new;
+    const int rows = it.n_new * p.group;
     const int n_rg = (rows + kCtxTileM - 1) / kCtxTileM;
-    s_idx = im.y / max(n_rg, 1);
-    const int rg = im.y - s_idx * n_rg;
-    num_splits = __ldg(p.split_prefix + gr + 1) - __ldg(p.split_prefix + gr);
-    kt0 = s_idx * p.kv_chunk;
-    kend = min(L_r, kt0 + p.kv_chunk);
-    pr0 = rg * kCtxTileM;  // first (token, head) pair of the CTA: one Q tile of 128 pairs
-    tok0 = __ldg(p.cu_q + r);
-    q_row = tok0 + pr0 / p.group;
-    nv0 = max(0, min(128, rows - pr0));
+    it.s_idx = im.y / max(n_rg, 1);
+    const int rg = im.y - it.s_idx * n_rg;
+    it.num_splits = __ldg(p.split_prefix + it.gr + 1) - __ldg(p.split_prefix + it.gr);
+    it.kt0 = it.s_idx * p.kv_chunk;
+    it.kend = min(it.L_r, it.kt0 + p.kv_chunk);
+    it.pr0 = rg * kCtxTileM;  // first (token, head) pair of the item: one Q tile of 128 pairs
+    it.tok0 = __ldg(p.cu_q + it.r);
+    it.q_row = it.tok0 + it.pr0 / p.group;
+    it.nv0 = max(0, min(128, rows - it.pr0));
     // both halves of the pipeline serve the same rows: A takes the split's even KV tiles, B the
     // odd ones, each with its own S, P, O and softmax state, merged at the end
-    const int nk = (kend - kt0 + kCtxTileN - 1) / kCtxTileN;
-    nkt0 = (nk + 1) / 2;
-    nkt1 = nk / 2;
-    nv1 = nkt1 > 0 ? nv0 : 0;
-    item_ok = im.y >= 0 && s_idx < num_splits && kt0 < kend && nv0 > 0 && n_new >= 1 &&
-              n_new <= PKV_MAX_GEN_TOKENS && tok0 >= gen_row0 && tok0 + n_new <= p.T &&
-              static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(num_splits) * n_new <= p.total_parts;
-  }
-  if (!idle && !item_ok && threadIdx.x == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
-  const bool hasB = nv1 > 0;
-  // KV tiles this CTA streams (A the even ones, B the odd ones); the user of the last V tile
-  // zeroes its tail
-  const int nT = nkt0 + nkt1;
-  const int zero_x = (nT - 1) & 1;
-  // tile j of half x: which K / V tile of the stream (ring stage, phase)
-  auto gtile = [&](int j, int x) { return 2 * j + x; };
+    const int nk = (it.kend - it.kt0 + kCtxTileN - 1) / kCtxTileN;
+    it.nkt0 = (nk + 1) / 2;
+    it.nkt1 = nk / 2;
+    it.nv1 = it.nkt1 > 0 ? it.nv0 : 0;
+    it.ok = im.y >= 0 && it.s_idx < it.num_splits && it.kt0 < it.kend && it.nv0 > 0 && it.n_new >= 1 &&
+            it.n_new <= PKV_MAX_GEN_TOKENS && it.tok0 >= gen_row0 && it.tok0 + it.n_new <= p.T &&
+            static_cast<int64_t>(__ldg(p.part_prefix + it.gr)) + static_cast<int64_t>(it.num_splits) * it.n_new <=
+                p.total_parts;
+    return it;
+  };
 
   const uint32_t sQ = base_s + L::kQOff;
   auto sK = [&](int st) { return base_s + L::kKOff + st * L::kTile; };
@@ -263,10 +279,25 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     return __all_sync(0xffffffffu, tc::mbar_wait(b, parity)) != 0;
   };
   auto warp_abort = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0) != 0; };
+  // consumers: item k of this CTA from the ring (-1: no more work), entry handed back
+  auto take_item = [&](int k, int& w) {
+    const int slot = k & 1;
+    if (!warp_wait(bar(BAR_ITEM + slot), (k >> 1) & 1)) return false;
+    w = *(s_item + slot);
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar(BAR_ITEMFREE + slot));
+    return true;
+  };
+  // the end of an item for the MMA warp and the softmax warps; the next one starts when all nine
+  // warps have got here (n: items this CTA has finished so far)
+  auto item_done = [&]() {
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar(BAR_IDONE));
+  };
+  auto wait_prev = [&](int n) { return n == 0 || warp_wait(bar(BAR_IDONE), (n - 1) & 1); };
 
-  if (!item_ok) {
-    // nothing to do: fall through to the teardown (TMEM is already allocated)
-  } else if (warp >= 8) {
+  if (warp >= 8) {
     // one setmaxnreg instruction for all four warps of the control warpgroup
     tc::regs_dec<kRegsControl>();
     // The producer and MMA warps run their loops with all 32 lanes (waits and control flow
@@ -274,105 +305,138 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     // diverged on one lane gets issue slots far less often next to a busy softmax warp on the
     // same sub-partition, and the tensor pipe then runs dry between MMA batches.
     if (warp == kProducerWarp) {
-      // ======================= TMA producer =======================
-      const int32_t* tbl = p.tbl + static_cast<int64_t>(r) * p.max_blocks;
-      const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
-      const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
-      const int n_pages_seq = (L_r + p.B - 1) / p.B;
+      // ======================= item queue + TMA producer =======================
+      int w = static_cast<int>(blockIdx.x);
+      int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items)
+      int nq = 0;                      // Q tiles loaded
       const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: warpgroup A re-encodes Q first
-      if (tc::elect_one()) {  // one Q tile (128 / g tokens x the group's g heads), shared by A and B
-        tc::mbar_arrive_expect_tx(bar(q_bar), 128 * D * 2);
-        for (int dh = 0; dh < D / 64; ++dh)
-          tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, hk * p.group, q_row);
-      }
-      __syncwarp();
-      int issued_k = 0, issued_v = 0;
       bool pok = true;
-      for (int j = 0; j < nT && !warp_abort(); ++j) {
-        const int st = stg(j);
-        // lane pp < pages_per_tile looks up page pp of the tile (B <= 128: whole pages per tile)
-        const int lb = (kt0 + j * kCtxTileN) / p.B + lane;
-        int pg = -1;
-        if (lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
-          pg = __ldg(tbl + lb);
-          if (pg < 0 || pg >= p.NB) {
-            flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
-            pg = -1;
+      for (int k = 0; pok; ++k) {
+        const int slot = k & 1;
+        if (k >= 2 && !warp_wait(bar(BAR_ITEMFREE + slot), ((k - 2) >> 1) & 1)) { pok = false; break; }
+        const bool more = w < n_items;
+        if (lane == 0) {
+          *(s_item + slot) = more ? w : -1;
+          tc::mbar_arrive(bar(BAR_ITEM + slot));
+        }
+        __syncwarp();
+        if (!more) break;
+        const Item it = item_of(w);
+        if (!it.ok) {
+          if (lane == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
+        } else {
+          const int nT = it.nkt0 + it.nkt1;
+          const int32_t* tbl = p.tbl + static_cast<int64_t>(it.r) * p.max_blocks;
+          const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
+          const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
+          const int n_pages_seq = (it.L_r + p.B - 1) / p.B;
+          // tile j of the item into the next stage of the CTA's stream
+          auto issue_tile = [&](int j) {
+            if (warp_abort()) return false;
+            const int g = issued_k;  // == issued_v: the tile's place in the CTA's stream
+            // lane pp < pages_per_tile looks up page pp of the tile (B <= 128: whole pages per tile)
+            const int lb = (it.kt0 + j * kCtxTileN) / p.B + lane;
+            int pg = -1;
+            if (lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
+              pg = __ldg(tbl + lb);
+              if (pg < 0 || pg >= p.NB) {
+                flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+                pg = -1;
+              }
+            }
+            const uint32_t bytes =
+                static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
+            if constexpr (Q8) {
+              // raw codes of page `lane` into the raw rings; K and V stages are freed separately
+              // (a V stage waits for the PV two tiles back, a K stage only for its S or conversion)
+              const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
+              const int rs = g & 1, rph = ((g - 2) >> 1) & 1;
+              if (g >= 2 && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) return false;
+              if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWK + rs), bytes);
+              __syncwarp();
+              if (pg >= 0)
+                tc::tma_load_3d(base_s + L::kRawKOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + rs), 0, it.hk,
+                                (pg * 2 + 0) * p.B);
+              __syncwarp();
+              ++issued_k;
+              if (g >= 2 && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) return false;
+              if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWV + rs), bytes);
+              __syncwarp();
+              if (pg >= 0)
+                tc::tma_load_3d(base_s + L::kRawVOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + rs), 0, it.hk,
+                                (pg * 2 + 1) * p.B);
+              __syncwarp();
+              ++issued_v;
+              return true;
+            }
+            // one lane registers the tile's bytes, then every lane with a page issues its own
+            // copies (no shuffles, no serial issue loop on one lane)
+            const int st = stg(g);
+            const uint32_t koff = static_cast<uint32_t>(lane * box_rows * 128);
+            if (g >= S && !warp_wait(bar(BAR_KEMPTY + st), phs(g - S))) return false;
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
+            __syncwarp();
+            if (pg >= 0)
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_load_4d(sK(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_KFULL + st), 0, dh, it.hk,
+                                (pg * 2 + 0) * p.B);
+            __syncwarp();
+            ++issued_k;
+            if (g >= S && !warp_wait(bar(BAR_VEMPTY + st), phs(g - S))) return false;
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
+            __syncwarp();
+            if (pg >= 0)
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_load_4d(sV(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_VFULL + st), 0, dh, it.hk,
+                                (pg * 2 + 1) * p.B);
+            __syncwarp();
+            ++issued_v;
+            return true;
+          };
+          // the item's first tiles go out as soon as stages free up (while the previous item
+          // ends), its Q tile once the previous item's last S MMA is done, then the rest
+          const int pre = min(nT, 1);
+          for (int j = 0; pok && j < pre; ++j) pok = issue_tile(j);
+          if (pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
+          if (!pok) break;
+          // one Q tile (128 / g tokens x the group's g heads), shared by A and B
+          if (tc::elect_one()) {
+            tc::mbar_arrive_expect_tx(bar(q_bar), 128 * D * 2);
+            for (int dh = 0; dh < D / 64; ++dh)
+              tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, it.hk * p.group, it.q_row);
           }
+          __syncwarp();
+          ++nq;
+          for (int j = pre; pok && j < nT; ++j) pok = issue_tile(j);
         }
-        const uint32_t bytes =
-            static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
-        if constexpr (Q8) {
-          // raw codes of page `lane` into the raw rings; K and V stages are freed separately (a
-          // V stage waits for the PV two tiles back, a K stage only for its S or conversion)
-          const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
-          const int rs = j & 1, rph = ((j - 2) >> 1) & 1;
-          if (j >= 2 && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) { pok = false; break; }
-          if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWK + rs), bytes);
-          __syncwarp();
-          if (pg >= 0)
-            tc::tma_load_3d(base_s + L::kRawKOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + rs), 0, hk,
-                            (pg * 2 + 0) * p.B);
-          __syncwarp();
-          ++issued_k;
-          if (j >= 2 && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) { pok = false; break; }
-          if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWV + rs), bytes);
-          __syncwarp();
-          if (pg >= 0)
-            tc::tma_load_3d(base_s + L::kRawVOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + rs), 0, hk,
-                            (pg * 2 + 1) * p.B);
-          __syncwarp();
-          ++issued_v;
-          continue;
-        }
-        // one lane registers the tile's bytes, then every lane with a page issues its own copies
-        // (no shuffles, no serial issue loop on one lane)
-        const uint32_t koff = static_cast<uint32_t>(lane * box_rows * 128);
-        if (j >= S && !warp_wait(bar(BAR_KEMPTY + st), phs(j - S))) { pok = false; break; }
-        if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
-        __syncwarp();
-        if (pg >= 0)
-          for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sK(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_KFULL + st), 0, dh, hk, (pg * 2 + 0) * p.B);
-        __syncwarp();
-        ++issued_k;
-        if (j >= S && !warp_wait(bar(BAR_VEMPTY + st), phs(j - S))) { pok = false; break; }
-        if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
-        __syncwarp();
-        if (pg >= 0)
-          for (int dh = 0; dh < D / 64; ++dh)
-            tc::tma_load_4d(sV(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_VFULL + st), 0, dh, hk, (pg * 2 + 1) * p.B);
-        __syncwarp();
-        ++issued_v;
+        if (!pok) break;
+        // claim the next item while this one's tiles are still being consumed
+        int nxt = 0;
+        if (lane == 0) nxt = atomicAdd(p.gen_cursor, 1) + static_cast<int>(gridDim.x);
+        w = __shfl_sync(0xffffffffu, nxt, 0);
       }
       if (!pok && lane == 0) fail();
       __syncwarp();
-      if (warp_abort()) {  // let copies already in flight land before the CTA winds down
-        if constexpr (Q8) {
-          for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
-            tc::mbar_wait(bar(BAR_RAWK + (j & 1)), (j >> 1) & 1, 200000000LL);
-          for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
-            tc::mbar_wait(bar(BAR_RAWV + (j & 1)), (j >> 1) & 1, 200000000LL);
-        } else {
-          for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
-            tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
-          for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
-            tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
-        }
-        tc::mbar_wait(bar(q_bar), 0, 200000000LL);
+      // the last copy into each stage and the last Q tile have landed before the CTA can wind
+      // down, however the consumers fare (on the normal path these phases completed long ago)
+      if constexpr (Q8) {
+        for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
+          tc::mbar_wait(bar(BAR_RAWK + (j & 1)), (j >> 1) & 1, 200000000LL);
+        for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
+          tc::mbar_wait(bar(BAR_RAWV + (j & 1)), (j >> 1) & 1, 200000000LL);
+      } else {
+        for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
+          tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
+        for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
+          tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
       }
+      if (nq > 0) tc::mbar_wait(bar(q_bar), (nq - 1) & 1, 200000000LL);
     } else if (warp == kMmaWarp) {
       // ======================= MMA issuer =======================
       // tcgen05.commit tracks the MMAs of the thread that issues it: elect.sync on a converged
       // warp picks the same (lowest) lane every time, so MMAs and commits share one thread.
       constexpr uint32_t idesc_s = Q8 ? tc::idesc_f16(128, kCtxTileN, 0) : tc::idesc_bf16(128, kCtxTileN, 0);
       constexpr uint32_t idesc_o = Q8 ? tc::idesc_f16(128, D, 1) : tc::idesc_bf16(128, D, 1);
-      auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
-      auto kfull = [&](int j, int x) {
-        const int g = gtile(j, x);
-        if constexpr (F8S) return warp_wait(bar(BAR_RAWK + (g & 1)), (g >> 1) & 1);  // raw codes landed
-        return warp_wait(bar(BAR_KFULL + stg(g)), phs(g));
-      };
       // Descriptors are built once per operand tile and advanced by adding the byte offset / 16
       // (the start address occupies the low bits and never carries out inside a tile): this
       // warp competes for issue slots with a busy softmax warp, so every instruction counts.
@@ -381,81 +445,116 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
       const uint64_t dv0 = tc::sdesc_sw128(sV(0), L::kHalf, 1024);
       auto stage_off = [](int st) { return static_cast<uint64_t>(st) * (L::kTile / 16); };
-      auto issue_s = [&](int j, int x) {
-        const int st = stg(gtile(j, x));
-        const uint64_t a0 = dq0;  // A and B share the Q tile
-        const uint64_t b0 = dk0 + stage_off(st);
-        if constexpr (F8S) {
-          // Q hi and lo tiles (one 128-byte row of codes per Q row) sit in the f16 K stage 0
-          // area; K is the raw tile: four K=32 steps of 32 bytes, hi then lo
+      int G = 0;             // K / V stream tiles of earlier items
+      int sc0 = 0, sc1 = 0;  // S / P tiles of earlier items, per half
+      int nq = 0, ndone = 0; // Q tiles consumed, items finished
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        int w = -1;
+        if (!take_item(k, w)) { ok = false; break; }
+        if (w < 0) break;
+        const Item it = item_of(w);
+        if (!it.ok) continue;
+        const int nkt0 = it.nkt0, nkt1 = it.nkt1;
+        const bool hasB = it.nv1 > 0;
+        auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
+        // tile j of half x: the (G + 2j + x)-th K / V tile of the CTA's stream
+        auto gtile = [&](int j, int x) { return G + 2 * j + x; };
+        auto kfull = [&](int j, int x) {
           const int g = gtile(j, x);
-          const uint64_t aq = tc::sdesc_sw128(sK(0), 16, 1024);
-          const uint64_t bk = tc::sdesc_sw128(base_s + L::kRawKOff + (g & 1) * L::kRawTile, 16, 1024);
-          constexpr uint64_t kLo = 128 * 128 / 16;  // lo tile: 16 KB after hi
+          if constexpr (F8S) return warp_wait(bar(BAR_RAWK + (g & 1)), (g >> 1) & 1);  // raw codes landed
+          return warp_wait(bar(BAR_KFULL + stg(g)), phs(g));
+        };
+        auto issue_s = [&](int j, int x) {
+          const int g = gtile(j, x);
+          const int st = stg(g);
+          const uint64_t a0 = dq0;  // A and B share the Q tile
+          const uint64_t b0 = dk0 + stage_off(st);
+          if constexpr (F8S) {
+            // Q hi and lo tiles (one 128-byte row of codes per Q row) sit in the f16 K stage 0
+            // area; K is the raw tile: four K=32 steps of 32 bytes, hi then lo
+            const uint64_t aq = tc::sdesc_sw128(sK(0), 16, 1024);
+            const uint64_t bk = tc::sdesc_sw128(base_s + L::kRawKOff + (g & 1) * L::kRawTile, 16, 1024);
+            constexpr uint64_t kLo = 128 * 128 / 16;  // lo tile: 16 KB after hi
+            if (tc::elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc::mma_e4m3_ss(tmem + 128 * x, aq + 2 * kk, bk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3_ss(tmem + 128 * x, aq + kLo + 2 * kk, bk + 2 * kk, idesc_s, 1u);
+              tc::mma_commit(bar(BAR_SFULL + x));
+              tc::mma_commit(bar(BAR_RAWKEMPTY + (g & 1)));  // the raw K stage may be refilled
+              if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(BAR_QFREE));  // the item's last S
+            }
+            __syncwarp();
+            return;
+          }
           if (tc::elect_one()) {
+            if constexpr (D == 128) {
+              // steps kk: ((kk / 4) * 16 KB + (kk % 4) * 32 B) / 16
+              tc::mma_bf16_ss_x8<0, 2, 4, 6, L::kHalf / 16, L::kHalf / 16 + 2, L::kHalf / 16 + 4, L::kHalf / 16 + 6>(
+                  tmem + 128 * x, a0, b0, idesc_s, 0u);
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::mma_e4m3_ss(tmem + 128 * x, aq + 2 * kk, bk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3_ss(tmem + 128 * x, aq + kLo + 2 * kk, bk + 2 * kk, idesc_s, 1u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4);
+                tc::mma_bf16_ss(tmem + 128 * x, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+              }
+            }
             tc::mma_commit(bar(BAR_SFULL + x));
-            tc::mma_commit(bar(BAR_RAWKEMPTY + (g & 1)));  // the raw K stage may be refilled
+            tc::mma_commit(bar(BAR_KEMPTY + st));  // each K / V tile has one user
+            // the item's last S: the Q tile (and its re-encoding) may be replaced once it is done
+            if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(BAR_QFREE));
           }
           __syncwarp();
-          return;
-        }
-        if (tc::elect_one()) {
-          if constexpr (D == 128) {
-            // steps kk: ((kk / 4) * 16 KB + (kk % 4) * 32 B) / 16
-            tc::mma_bf16_ss_x8<0, 2, 4, 6, L::kHalf / 16, L::kHalf / 16 + 2, L::kHalf / 16 + 4, L::kHalf / 16 + 6>(
-                tmem + 128 * x, a0, b0, idesc_s, 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4);
-              tc::mma_bf16_ss(tmem + 128 * x, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
+        };
+        ok = warp_wait(bar(BAR_Q), nq & 1) && kfull(0, 0);
+        ++nq;
+        if (ok) {
+          tc::fence_after_sync();
+          issue_s(0, 0);
+          if (hasB) {
+            ok = kfull(0, 1);  // B's first tile is the stream's second
+            if (ok) {
+              tc::fence_after_sync();
+              issue_s(0, 1);
             }
           }
-          tc::mma_commit(bar(BAR_SFULL + x));
-          tc::mma_commit(bar(BAR_KEMPTY + st));  // each K / V tile has one user
         }
-        __syncwarp();
-      };
-      bool ok = warp_wait(bar(BAR_Q), 0) && kfull(0, 0);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_s(0, 0);
-        if (hasB) {
-          ok = kfull(0, 1);  // B's first tile is the stream's second
-          if (ok) {
+        // The item's first S MMAs go out while the previous item's epilogue runs (they touch
+        // only S); its first PV waits until every warp has finished that item (A's merge reads
+        // both O halves).
+        if (ok && !wait_prev(ndone)) ok = false;
+        // no abort-flag poll per tile: a shared-memory load here sits on the critical path
+        // (P ready -> next MMA); if another warp gave up, the waits below run out instead
+        for (int j = 0; ok && j < nkt0; ++j) {
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!uses(j, x)) continue;
+            const int g = gtile(j, x);
+            if (!warp_wait(bar(BAR_PFULL + x), ((x ? sc1 : sc0) + j) & 1)) { ok = false; break; }
+            if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
             tc::fence_after_sync();
-            issue_s(0, 1);
+            const uint64_t v0 = dv0 + stage_off(stg(g));
+            if (tc::elect_one()) {
+              static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
+              tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
+              tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
+              if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
+            }
+            __syncwarp();
+            if (uses(j + 1, x)) {
+              if (!kfull(j + 1, x)) { ok = false; break; }
+              tc::fence_after_sync();
+              issue_s(j + 1, x);
+            }
           }
         }
-      }
-      // no abort-flag poll per tile: a shared-memory load here sits on the critical path
-      // (P ready -> next MMA); if another warp gave up, the waits below run out instead
-      for (int j = 0; ok && j < nkt0; ++j) {
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (!uses(j, x)) continue;
-          const int g = gtile(j, x);
-          if (!warp_wait(bar(BAR_PFULL + x), j & 1)) { ok = false; break; }
-          if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint64_t v0 = dv0 + stage_off(stg(g));
-          if (tc::elect_one()) {
-            static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
-            tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
-            tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
-            if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
-          }
-          __syncwarp();
-          if (uses(j + 1, x)) {
-            if (!kfull(j + 1, x)) { ok = false; break; }
-            tc::fence_after_sync();
-            issue_s(j + 1, x);
-          }
-        }
+        if (!ok) break;
+        G += nkt0 + nkt1;
+        sc0 += nkt0;
+        sc1 += nkt1;
+        item_done();
+        ++ndone;
       }
       if (!ok && lane == 0) fail();
       if (tc::elect_one()) {
@@ -472,27 +571,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128 * x + lane_off;
     const uint32_t tO = tmem + 256 + 128 * x + lane_off;
-    const int nvx = x ? nv1 : nv0, nk = x ? nkt1 : nkt0;
-    // the row's token and the new keys it sees (bit j: key past + j)
-    uint64_t vis = ~0ull;
-    int tok_i = 0, hl = 0;
-    {
-      const int pr = pr0 + row;  // A and B hold the same rows
-      if (row < nvx) {
-        tok_i = pr / p.group;
-        hl = pr - tok_i * p.group;
-        if (p.mask != nullptr) {
-          const uint32_t* mrow = p.mask + static_cast<int64_t>(tok0 + tok_i - gen_row0) * p.mask_words;
-          vis = __ldg(mrow);
-          if (n_new > 32 && p.mask_words > 1) vis |= static_cast<uint64_t>(__ldg(mrow + 1)) << 32;
-          vis |= 1ull << tok_i;
-        } else {
-          vis = (2ull << tok_i) - 1;  // j <= i (i = 63 wraps to all ones)
-        }
-      }
-    }
-    float sl2 = p.scale_log2;
-    bool ok = true;
+    float* xch = reinterpret_cast<float*>(base + L::kXchOff);  // [2][128]: B's m, l per row
     // ---- 8-bit pool: this warpgroup turns the raw codes of its own tiles into f16 ----
     // Thread `row` converts tile row `row`: 128 codes in the 128-byte swizzle TMA wrote (16-byte
     // chunk j at j ^ (row % 8)) become 16 f16 chunks of the K-major 128-byte-swizzled layout the
@@ -544,258 +623,300 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       }
       return true;
     };
-    if constexpr (Q8) {
-      float* qscale = reinterpret_cast<float*>(base + L::kQScaleOff);
-      if (x == 0) {
-        // Q row `row`: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
-        // below f16's 65504), in place; the scores take 2^(e - 14) back
-        ok = warp_wait(bar(BAR_QRAW), 0);
-        if (ok) {
-          float amax = 0.f;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (c >> 3) * L::kHalf + row * 128 +
-                                                            (((c & 7) ^ (row & 7)) << 4));
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
-          }
-          int ex = 0;
-          if (amax > 0.f) frexpf(amax, &ex);
-          // f16: |q| * up in [2^13, 2^14); E4M3 hi + lo: |q| * up in [128, 256), under 448
-          const float up = ldexpf(1.f, (F8S ? 8 : 14) - ex);
-          if constexpr (F8S) {
-            // code chunk jc (16 codes = q elements 16 jc ..) from bf16 chunks 2 (jc % 4) and
-            // 2 (jc % 4) + 1 of head-dim half jc / 4; hi tile at sK(0), lo tile 16 KB after it
-#pragma unroll
-            for (int jc = 0; jc < 8; ++jc) {
-              uint32_t hw[4], lw[4];
-#pragma unroll
-              for (int hc = 0; hc < 2; ++hc) {
-                const int c = 2 * (jc & 3) + hc;
-                const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (jc >> 2) * L::kHalf + row * 128 +
-                                                                ((c ^ (row & 7)) << 4));
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int k = 0; k < 4; k += 2) {
-                  uint32_t h0, l0, h1, l1;
-                  split_e4m3x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up, h0, l0);
-                  split_e4m3x2(__uint_as_float(u[k + 1] << 16) * up, __uint_as_float(u[k + 1] & 0xFFFF0000u) * up, h1,
-                               l1);
-                  hw[2 * hc + (k >> 1)] = (h0 & 0xFFFFu) | (h1 << 16);
-                  lw[2 * hc + (k >> 1)] = (l0 & 0xFFFFu) | (l1 << 16);
-                }
-              }
-              const uint32_t off = static_cast<uint32_t>(row * 128 + ((jc ^ (row & 7)) << 4));
-              st_shared_v4(sK(0) + off, hw[0], hw[1], hw[2], hw[3]);
-              st_shared_v4(sK(0) + 128 * 128 + off, lw[0], lw[1], lw[2], lw[3]);
-            }
+    int G = 0, sc = 0, nq = 0;        // stream tiles, this half's S / P tiles, Q tiles of earlier items
+    int n_epi = 0, n_merge = 0, ndone = 0;  // this half's epilogues, merges, items finished
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      int w = -1;
+      if (!take_item(k, w)) { ok = false; break; }
+      if (w < 0) break;
+      const Item it = item_of(w);
+      if (!it.ok) continue;
+      const int nvx = x ? it.nv1 : it.nv0, nk = x ? it.nkt1 : it.nkt0;
+      const int nT = it.nkt0 + it.nkt1;  // KV tiles of the item (A the even ones, B the odd ones)
+      const int zero_x = (nT - 1) & 1;   // the user of the last V tile zeroes its tail
+      auto gtile = [&](int j) { return G + 2 * j + x; };  // this half's j-th tile in the CTA's stream
+      // the row's token and the new keys it sees (bit j: key past + j)
+      uint64_t vis = ~0ull;
+      int tok_i = 0, hl = 0;
+      {
+        const int pr = it.pr0 + row;  // A and B hold the same rows
+        if (row < nvx) {
+          tok_i = pr / p.group;
+          hl = pr - tok_i * p.group;
+          if (p.mask != nullptr) {
+            const uint32_t* mrow = p.mask + static_cast<int64_t>(it.tok0 + tok_i - gen_row0) * p.mask_words;
+            vis = __ldg(mrow);
+            if (it.n_new > 32 && p.mask_words > 1) vis |= static_cast<uint64_t>(__ldg(mrow + 1)) << 32;
+            vis |= 1ull << tok_i;
           } else {
+            vis = (2ull << tok_i) - 1;  // j <= i (i = 63 wraps to all ones)
+          }
+        }
+      }
+      // 8-bit pool: warpgroup B (whose epilogue is the short one) re-encodes the item's Q and
+      // each warpgroup converts its first tile, before waiting for the previous item to end:
+      // they touch shared memory only, and their barriers order them against its MMAs.
+      float sl2 = p.scale_log2;
+      float* qscale = reinterpret_cast<float*>(base + L::kQScaleOff);
+      if constexpr (Q8) {
+        if (x == 1) {
+          // Q row `row`: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
+          // below f16's 65504), in place; the scores take 2^(e - 14) back
+          ok = warp_wait(bar(BAR_QRAW), nq & 1);
+          if (ok) {
+            float amax = 0.f;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-              const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
+              const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (c >> 3) * L::kHalf + row * 128 +
+                                                              (((c & 7) ^ (row & 7)) << 4));
               const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-              uint32_t h[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
-              st_shared_v4(a, h[0], h[1], h[2], h[3]);
+                amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
             }
+            int ex = 0;
+            if (amax > 0.f) frexpf(amax, &ex);
+            // f16: |q| * up in [2^13, 2^14); E4M3 hi + lo: |q| * up in [128, 256), under 448
+            const float up = ldexpf(1.f, (F8S ? 8 : 14) - ex);
+            // the previous item's scales are read by both warpgroups before they are replaced
+            if (nq > 0 && !warp_wait(bar(BAR_QSREAD), (nq - 1) & 1)) { ok = false; break; }
+            if constexpr (F8S) {
+              // code chunk jc (16 codes = q elements 16 jc ..) from bf16 chunks 2 (jc % 4) and
+              // 2 (jc % 4) + 1 of head-dim half jc / 4; hi tile at sK(0), lo tile 16 KB after it
+#pragma unroll
+              for (int jc = 0; jc < 8; ++jc) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                  const int c = 2 * (jc & 3) + hc;
+                  const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (jc >> 2) * L::kHalf + row * 128 +
+                                                                  ((c ^ (row & 7)) << 4));
+                  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int k = 0; k < 4; k += 2) {
+                    uint32_t h0, l0, h1, l1;
+                    split_e4m3x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up, h0, l0);
+                    split_e4m3x2(__uint_as_float(u[k + 1] << 16) * up, __uint_as_float(u[k + 1] & 0xFFFF0000u) * up, h1,
+                                 l1);
+                    hw[2 * hc + (k >> 1)] = (h0 & 0xFFFFu) | (h1 << 16);
+                    lw[2 * hc + (k >> 1)] = (l0 & 0xFFFFu) | (l1 << 16);
+                  }
+                }
+                const uint32_t off = static_cast<uint32_t>(row * 128 + ((jc ^ (row & 7)) << 4));
+                st_shared_v4(sK(0) + off, hw[0], hw[1], hw[2], hw[3]);
+                st_shared_v4(sK(0) + 128 * 128 + off, lw[0], lw[1], lw[2], lw[3]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const uint32_t a = base_s + L::kQOff + (c >> 3) * L::kHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                const uint4 w = *reinterpret_cast<const uint4*>(base + (a - base_s));
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                uint32_t h[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  h[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
+                st_shared_v4(a, h[0], h[1], h[2], h[3]);
+              }
+            }
+            qscale[row] = 1.f / up;
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
           }
-          qscale[row] = 1.f / up;
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
         }
+        if (ok && nk > 0) ok = convert_tile(gtile(0));  // this warpgroup's first tile
+        if (!ok) break;
       }
-      if (ok && nk > 0) ok = convert_tile(x);  // this warpgroup's first tile
-      if (ok) ok = warp_wait(bar(BAR_Q), 0);
-      if (ok) sl2 *= qscale[row];
-    }
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int j = 0; ok && j < nk; ++j) {
-      if (!warp_wait(bar(BAR_SFULL + x), j & 1)) { ok = false; break; }
-      tc::fence_after_sync();
-      uint32_t v0[32], v1[32], v2[32], v3[32];
-      tc::tmem_ld32_async(tS + 0, v0);
-      tc::tmem_ld32_async(tS + 32, v1);
-      tc::tmem_ld32_async(tS + 64, v2);
-      tc::tmem_ld32_async(tS + 96, v3);
-      tc::tmem_wait_ld_dep(v0);
-      tc::reg_dep(v1);
-      tc::reg_dep(v2);
-      tc::reg_dep(v3);
-      const int tb = kt0 + gtile(j, x) * kCtxTileN;  // key of column 0
-      if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
-        // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
-        // keys this row's token sees (bits of vis), nothing at or past the split's end
-        auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
-        auto word = [&](int w) {
-          const int t0 = tb + 32 * w, sh = t0 - past;
-          uint32_t nv = 0u;
-          if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
-          else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
-          return (low(past - t0) | nv) & low(kend - t0);
-        };
-        const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
+      if (!wait_prev(ndone)) { ok = false; break; }
+      if constexpr (Q8) {
+        ok = warp_wait(bar(BAR_Q), nq & 1);
+        if (ok) sl2 *= qscale[row];
+        ++nq;
+        if (!ok) break;
+        __syncwarp();
+        if (x == 0 && lane == 0) tc::mbar_arrive(bar(BAR_QSREAD));
+      }
+      const int kt0 = it.kt0, kend = it.kend, past = it.past;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; ok && j < nk; ++j) {
+        if (!warp_wait(bar(BAR_SFULL + x), (sc + j) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        tc::tmem_ld32_async(tS + 0, v0);
+        tc::tmem_ld32_async(tS + 32, v1);
+        tc::tmem_ld32_async(tS + 64, v2);
+        tc::tmem_ld32_async(tS + 96, v3);
+        tc::tmem_wait_ld_dep(v0);
+        tc::reg_dep(v1);
+        tc::reg_dep(v2);
+        tc::reg_dep(v3);
+        const int tb = kt0 + (2 * j + x) * kCtxTileN;  // key of column 0
+        if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
+          // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
+          // keys this row's token sees (bits of vis), nothing at or past the split's end
+          auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
+          auto word = [&](int wd) {
+            const int t0 = tb + 32 * wd, sh = t0 - past;
+            uint32_t nv = 0u;
+            if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
+            else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
+            return (low(past - t0) | nv) & low(kend - t0);
+          };
+          const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
-          v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
-          v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
-          v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
+          for (int e = 0; e < 32; ++e) {
+            v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+            v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
+            v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
+            v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
+          }
         }
-      }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        mx[0] = max3f(mx[0], __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
-        mx[1] = max3f(mx[1], __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
-        mx[2] = max3f(mx[2], __uint_as_float(v2[e]), __uint_as_float(v2[e + 1]));
-        mx[3] = max3f(mx[3], __uint_as_float(v3[e]), __uint_as_float(v3[e + 1]));
-      }
-      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
-      float m_use = m_run;
-      if (j == 0) {
-        m_use = m_new;  // O is still empty
-      } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
-        // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
-        const float f = ex2_approx(m_run - m_new);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tc::tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-          tc::tmem_st32(tO + cc * 32, o);
-        }
-        l_run *= f;
-        m_use = m_new;
-      }
-      m_run = m_use;
-      // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
-      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      const float m_base = m_use == -INFINITY ? 0.f : m_use;  // no visible key yet (generation splits)
-      const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
-      auto emit = [&](uint32_t(&v)[32], int c) {
-        uint32_t pk[16];
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
-          const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
-          ls[c] = fadd2(ls[c], pv);
-          pk[e >> 1] = Q8 ? pack_f16x2(pv.x, pv.y) : pack_bf16x2(pv.x, pv.y);
+          mx[0] = max3f(mx[0], __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
+          mx[1] = max3f(mx[1], __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
+          mx[2] = max3f(mx[2], __uint_as_float(v2[e]), __uint_as_float(v2[e + 1]));
+          mx[3] = max3f(mx[3], __uint_as_float(v3[e]), __uint_as_float(v3[e + 1]));
         }
-        tc::tmem_st16(tS + 16 * c, pk);
-      };
-      emit(v0, 0);
-      emit(v1, 1);
-      emit(v2, 2);
-      emit(v3, 3);
-      const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
-      l_run += lsum.x + lsum.y;
-      tc::tmem_wait_st();
-      if (gtile(j, x) == nT - 1 && x == zero_x) {
-        // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
-        const int g = nT - 1;
-        if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
-        if (kt0 + g * kCtxTileN + row >= kend) {
-          uint8_t* vrow = base + (sV(stg(g)) - base_s) + row * 128;
+        const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
+        float m_use = m_run;
+        if (j == 0) {
+          m_use = m_new;  // O is still empty
+        } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
+          // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
+          const float f = ex2_approx(m_run - m_new);
 #pragma unroll
-          for (int dh = 0; dh < D / 64; ++dh)
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + cc * 32, o);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              reinterpret_cast<uint4*>(vrow + dh * L::kHalf)[k] = make_uint4(0u, 0u, 0u, 0u);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tc::tmem_st32(tO + cc * 32, o);
+          }
+          l_run *= f;
+          m_use = m_new;
         }
-        tc::fence_proxy_async_smem();
+        m_run = m_use;
+        // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
+        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float m_base = m_use == -INFINITY ? 0.f : m_use;  // no visible key yet (generation splits)
+        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
+        auto emit = [&](uint32_t(&v)[32], int c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
+            const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+            ls[c] = fadd2(ls[c], pv);
+            pk[e >> 1] = Q8 ? pack_f16x2(pv.x, pv.y) : pack_bf16x2(pv.x, pv.y);
+          }
+          tc::tmem_st16(tS + 16 * c, pk);
+        };
+        emit(v0, 0);
+        emit(v1, 1);
+        emit(v2, 2);
+        emit(v3, 3);
+        const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+        l_run += lsum.x + lsum.y;
+        tc::tmem_wait_st();
+        if (2 * j + x == nT - 1 && x == zero_x) {
+          // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
+          const int g = G + nT - 1;
+          if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
+          if (kt0 + (nT - 1) * kCtxTileN + row >= kend) {
+            uint8_t* vrow = base + (sV(stg(g)) - base_s) + row * 128;
+#pragma unroll
+            for (int dh = 0; dh < D / 64; ++dh)
+#pragma unroll
+              for (int kq = 0; kq < 8; ++kq)
+                reinterpret_cast<uint4*>(vrow + dh * L::kHalf)[kq] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc::fence_proxy_async_smem();
+        }
+        // one arrive per warp after the warp has synchronised (fewer atomics on one word)
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(BAR_PFULL + x));
+        if constexpr (Q8) {  // the warpgroup's next tile, while its PV and the other tile's MMAs run
+          if (j + 1 < nk && !convert_tile(gtile(j + 1))) { ok = false; break; }
+        }
       }
-      // one arrive per warp after the warp has synchronised (fewer atomics on one word)
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(bar(BAR_PFULL + x));
-      if constexpr (Q8) {  // the warpgroup's next tile, while its PV and the other tile's MMAs run
-        if (j + 1 < nk && !convert_tile(gtile(j + 1, x))) { ok = false; break; }
-      }
-    }
-    if (!ok) fail();
-    // ---- epilogue: O / l -> bf16 rows ----
-    if (nk > 0) {
-      if (ok && !warp_abort() && warp_wait(bar(BAR_ODONE + x), 0)) {
+      if (!ok) break;
+      // ---- epilogue: the two halves of the split's keys: B hands its (m, l) over through
+      // shared memory and A merges O_A and O_B from TMEM into the output row or a partial row ----
+      if (nk > 0) {
+        if (warp_abort() || !warp_wait(bar(BAR_ODONE + x), n_epi & 1)) { ok = false; break; }
+        ++n_epi;
         tc::fence_after_sync();
-        // the two halves of the split's keys: B hands its (m, l) over through shared memory
-        // (the K ring is idle once both halves are done) and A merges O_A and O_B from TMEM
-        float* xch = reinterpret_cast<float*>(base + (sK(0) - base_s));  // [2][128]
         if (x == 1) {
           xch[row] = m_run;
           xch[128 + row] = l_run;
           tc::mbar_arrive(bar(BAR_MERGE));
         } else {
           float mB = -INFINITY, lB = 0.f;
-          bool merged = true;
-          if (nkt1 > 0) {
-            merged = warp_wait(bar(BAR_MERGE), 0);
-            if (merged) {
-              tc::fence_after_sync();
-              mB = xch[row];
-              lB = xch[128 + row];
+          if (it.nkt1 > 0) {
+            if (!warp_wait(bar(BAR_MERGE), n_merge & 1)) { ok = false; break; }
+            tc::fence_after_sync();
+            mB = xch[row];
+            lB = xch[128 + row];
+          }
+          const float M = fmaxf(m_run, mB), Mb = M == -INFINITY ? 0.f : M;
+          const float fA = ex2_approx(m_run - Mb), fB = ex2_approx(mB - Mb);
+          const float l = fA * l_run + fB * lB;
+          const bool store = row < nvx;
+          const int64_t head = static_cast<int64_t>(it.hk) * p.group + hl;
+          const bool whole = it.num_splits == 1;  // else a partial result for the combine
+          const float osc = p.out_scale;
+          const float sA = whole ? fA * osc / l : fA * osc;
+          const float sB = whole ? fB * osc / l : fB * osc;
+          uint16_t* orow = p.out + static_cast<int64_t>(it.tok0 + tok_i) * p.out_stride + head * D;
+          const int64_t pi = (static_cast<int64_t>(__ldg(p.part_prefix + it.gr)) +
+                              static_cast<int64_t>(it.s_idx) * it.n_new + tok_i) * p.Hq + head;
+          float* prow = p.part_o + pi * D;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t va[32], vb[32];
+            tc::tmem_ld32(tO + cc * 32, va);
+            if (it.nkt1 > 0) {
+              tc::tmem_ld32(tO + 128 + cc * 32, vb);  // O_B, same lanes
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) vb[e] = 0u;
+            }
+            float o[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(va[e]) * sA + __uint_as_float(vb[e]) * sB;
+            if (store && whole) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o[e], o[e + 1]);
+#pragma unroll
+              for (int kq = 0; kq < 4; ++kq)
+                reinterpret_cast<uint4*>(orow + cc * 32)[kq] =
+                    make_uint4(pk[4 * kq], pk[4 * kq + 1], pk[4 * kq + 2], pk[4 * kq + 3]);
+            } else if (store) {
+#pragma unroll
+              for (int kq = 0; kq < 8; ++kq)
+                reinterpret_cast<float4*>(prow + cc * 32)[kq] =
+                    make_float4(o[4 * kq], o[4 * kq + 1], o[4 * kq + 2], o[4 * kq + 3]);
             }
           }
-          if (!merged) {
-            ok = false;
-          } else {
-            const float M = fmaxf(m_run, mB), Mb = M == -INFINITY ? 0.f : M;
-            const float fA = ex2_approx(m_run - Mb), fB = ex2_approx(mB - Mb);
-            const float l = fA * l_run + fB * lB;
-            const bool store = row < nvx;
-            const int64_t head = static_cast<int64_t>(hk) * p.group + hl;
-            const bool whole = num_splits == 1;  // else a partial result for the combine
-            const float osc = p.out_scale;
-            const float sA = whole ? fA * osc / l : fA * osc;
-            const float sB = whole ? fB * osc / l : fB * osc;
-            uint16_t* orow = p.out + static_cast<int64_t>(tok0 + tok_i) * p.out_stride + head * D;
-            const int64_t pi =
-                (static_cast<int64_t>(__ldg(p.part_prefix + gr)) + static_cast<int64_t>(s_idx) * n_new + tok_i) * p.Hq +
-                head;
-            float* prow = p.part_o + pi * D;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-              uint32_t va[32], vb[32];
-              tc::tmem_ld32(tO + cc * 32, va);
-              if (nkt1 > 0) {
-                tc::tmem_ld32(tO + 128 + cc * 32, vb);  // O_B, same lanes
-              } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) vb[e] = 0u;
-              }
-              float o[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(va[e]) * sA + __uint_as_float(vb[e]) * sB;
-              if (store && whole) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o[e], o[e + 1]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  reinterpret_cast<uint4*>(orow + cc * 32)[k] =
-                      make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-              } else if (store) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  reinterpret_cast<float4*>(prow + cc * 32)[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-              }
-            }
-            if (store && !whole) {
-              p.part_ml[pi * 2] = M;
-              p.part_ml[pi * 2 + 1] = l;
-            }
+          if (store && !whole) {
+            p.part_ml[pi * 2] = M;
+            p.part_ml[pi * 2 + 1] = l;
           }
         }
-      } else if (ok) {
-        fail();
       }
+      if (it.nkt1 > 0) ++n_merge;
+      G += nT;
+      sc += nk;
+      item_done();
+      ++ndone;
     }
+    if (!ok) fail();
   }
 
   tc::fence_before_sync();
@@ -1425,7 +1546,10 @@ cudaError_t launch_gen_t(const ContextParams& p, const CUtensorMap& qm, const CU
   constexpr int bytes = GenSmem<D, KV>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(p.num_titems, p.Hkv), dim3(kThreads), bytes, s, p, qm, km);
+  // persistent: at most one CTA per SM, items = (generation CTA of the plan, KV head)
+  const int64_t items = static_cast<int64_t>(p.num_titems) * p.Hkv;
+  const int grid = static_cast<int>(std::min<int64_t>(items, std::max(p.num_ctas, 1)));
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), bytes, s, p, qm, km);
 }
 
 template <int D>

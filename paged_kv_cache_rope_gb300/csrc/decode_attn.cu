@@ -94,11 +94,51 @@ __device__ __forceinline__ Int8v scan_chunk(const Int8v x, Int8v* s_warp, const 
   return Int8v{add4(add4(carry.a, sw.a), sub4(incl.a, x.a)), add4(add4(carry.b, sw.b), sub4(incl.b, x.b))};
 }
 
+// Exclusive scan, in place, of the plan kernel's kPlanBins-bin shared histogram: each thread owns
+// kPlanBins / kPlanThreads bins; shuffles inside each warp, then one warp scans the warps' totals.
+// Every thread of the block calls it.
+constexpr int kPlanBins = 2048;  // cost bins of the plan's counting sorts (larger costs share the top bin)
+__device__ __forceinline__ void plan_hist_scan(int32_t* s_hist, int32_t* s_part, int tid, int lane, int wid) {
+  constexpr int kPer = kPlanBins / kPlanThreads;
+  int own = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) own += s_hist[tid * kPer + i];
+  int incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_part[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = lane < kPlanThreads / 32 ? s_part[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kPlanThreads / 32) s_part[kPlanThreads / 32 + lane] = wi - w;  // exclusive warp offsets
+  }
+  __syncthreads();
+  int run = s_part[kPlanThreads / 32 + wid] + incl - own;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int v = s_hist[tid * kPer + i];
+    s_hist[tid * kPer + i] = run;
+    run += v;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ Int8v s_warp[kPlanThreads / 32];
   __shared__ Int8v s_carry;
   __shared__ int32_t s_ctx_rows;
-  __shared__ int32_t s_units;
+  __shared__ int32_t s_units, s_titems;
+  __shared__ int32_t s_hist[kPlanBins];
+  __shared__ int32_t s_part[kPlanThreads];
   __shared__ unsigned long long s_gen_keys, s_tile_pairs;  // for the context CTA share
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int32_t* counts = p.ws + p.lay.counts;
@@ -215,6 +255,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                 (staging && t.a.w != p.cap_stage_pages);
     }
     s_units = t.a.y;
+    s_titems = t.b.w;
   }
   const bool any_bad = __syncthreads_or(bad || bad_tot) != 0;
   if (tid == 0) {
@@ -235,15 +276,38 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (lane == 0 && gen_keys) atomicAdd(&s_gen_keys, gen_keys);
   }
 
+  constexpr int kBins = kPlanBins;
+
+  // ---- tensor-core generation CTAs, most KV tiles first: a counting sort by the tile count of
+  // the CTA's split (the generation kernel claims them in this order, so that its last claims
+  // are short ones) ----
+  const int NT = s_titems;
+  if (NT > 0) {
+    int2* torder = reinterpret_cast<int2*>(p.ws + p.lay.titem_order);
+    auto titem_cost = [&](const int2 im) {
+      const int r = C + im.x, n = __ldg(p.ctx_len + r);
+      const int L = __ldg(p.past + r) + n, n_rg = max((n * p.group + kCtxTileM - 1) / kCtxTileM, 1);
+      const int kt0 = (im.y / n_rg) * chunk, keys = max(min(L, kt0 + chunk) - kt0, 0);
+      return min(kBins - 1, (keys + kCtxTileN - 1) / kCtxTileN);
+    };
+    for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
+    __syncthreads();  // titem_map (this block's global writes) and the zeroed histogram are visible
+    for (int t = tid; t < NT; t += kPlanThreads) atomicAdd(&s_hist[kBins - 1 - titem_cost(titem_map[t])], 1);
+    __syncthreads();
+    plan_hist_scan(s_hist, s_part, tid, lane, wid);
+    for (int t = tid; t < NT; t += kPlanThreads) {
+      const int2 im = titem_map[t];
+      torder[atomicAdd(&s_hist[kBins - 1 - titem_cost(im)], 1)] = im;
+    }
+    __syncthreads();  // the histogram is free again
+  }
+
   // ---- context units, most KV tiles first: a counting sort by tile count (descending) ----
   // Each slot gets the unit's descriptor (request, first q row, past + first row, rows left), so
   // a context CTA reads one int4 instead of searching the tile prefix itself.
   const int U = s_units;
   int4* order = reinterpret_cast<int4*>(p.ws + p.lay.unit_info);
   if (U <= 0) return;
-  constexpr int kBins = 2048;  // units with more tiles share the top bin
-  __shared__ int32_t s_hist[kBins];
-  __shared__ int32_t s_part[kPlanThreads];
   for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
   __syncthreads();  // tiles[] (this block's global writes) and the zeroed histogram are visible
   // the unit's request: the last slot whose unit prefix is <= u (an empty slot shares its
@@ -277,40 +341,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   if (p.ctx_share && tid == 0)  // bucket plan, bf16 pool, generation kernels beside the context kernel
     counts[kCntCtxCtas] = context_cta_share(static_cast<float>(s_tile_pairs), static_cast<float>(U),
                                             static_cast<float>(s_gen_keys), p.Hq, p.Hkv, p.D, p.num_sms);
-  // exclusive scan of the (reversed) histogram: each thread owns kBins / kPlanThreads bins
-  constexpr int kPer = kBins / kPlanThreads;
-  int own = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) own += s_hist[tid * kPer + i];
-  // block-wide exclusive scan of the per-thread totals: shuffles inside each warp, then the
-  // warps' totals (one warp scans them)
-  int incl = own;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_part[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int w = lane < kPlanThreads / 32 ? s_part[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    if (lane < kPlanThreads / 32) s_part[kPlanThreads / 32 + lane] = wi - w;  // exclusive warp offsets
-  }
-  __syncthreads();
-  int run = s_part[kPlanThreads / 32 + wid] + incl - own;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int v = s_hist[tid * kPer + i];
-    s_hist[tid * kPer + i] = run;
-    run += v;
-  }
-  __syncthreads();
+  plan_hist_scan(s_hist, s_part, tid, lane, wid);
   for (int u = tid; u < U; u += kPlanThreads) {
     const int4 d = unit_desc(u);
     order[atomicAdd(&s_hist[kBins - 1 - unit_cost(d)], 1)] = d;

@@ -38,6 +38,7 @@ enum PlanCount {
   kCntStagePages = 8,  // 8-bit pools: staged context pages
   kCntCursor = 9,      // work-queue cursor of the context kernel (written as zero by the plan)
   kCntCtxCtas = 10,    // context CTAs that take work (the rest exit at once), see context_cta_share
+  kCntGenCursor = 11,  // work-queue cursor of the tensor-core generation kernel (zeroed by the plan)
   kCntWords = 16
 };
 
@@ -52,6 +53,7 @@ struct PlanLayout {
   int64_t item_map;      // [num_items] int2 (generation request, item index within it)
   int64_t witem_map;     // [num_witems] the same for the wide decode kernel's CTAs
   int64_t titem_map;     // [num_titems] the same for the tensor-core kernel's generation CTAs
+  int64_t titem_order;   // [num_titems] int2: titem_map's entries, most KV tiles first
   int64_t row_map;       // [generation rows] int4 (splits, partial row of split 0, rows between
                          // splits = the request's new tokens, token index), 16-byte aligned
   int64_t unit_info;     // [num context units] int4 (request, first q row, past + first row,
@@ -199,7 +201,8 @@ struct ContextParams {
   int32_t C, T, Hq, Hkv, group, D, B, NB, max_blocks, num_tiles;
   int32_t num_ctas;         // context mode: persistent CTAs (one per SM at most)
   const int32_t* counts;    // the plan's PlanCount words
-  int32_t* cursor;          // context mode: the counts block's work-queue word
+  int32_t* cursor;          // context kernel: the counts block's work-queue word
+  int32_t* gen_cursor;      // generation kernel: its work-queue word
   const int32_t* cu_q;
   const int32_t* tile_prefix;
   const int4* unit_info;      // [num_tiles] context units in launch order: (request r, first
@@ -213,7 +216,7 @@ struct ContextParams {
   float scale_log2;
   float out_scale;          // multiplies O at the end (the FP8 dequantisation scale, else 1)
   int32_t* d_error;
-  // generation kernel (wide generation requests on the tensor cores): CTA = titem_map
+  // generation kernel (wide generation requests on the tensor cores): work items = titem_map
   // entry (generation request, split x row group) x KV head
   int32_t G, kv_chunk, num_titems, mask_words;
   int32_t kv_dtype;         // generation kernel: pool element kind (pkv_dtype); 8-bit codes are
