@@ -27,7 +27,7 @@ def _sample_rows(b: W.Batch, stride: int, tail: int) -> np.ndarray:
 
 @pytest.mark.parametrize("idx,kv_dtype,stride", [
     (1, "bf16", 1), (2, "bf16", 1), (3, "bf16", 1), (3, "fp8", 1), (4, "bf16", 29), (5, "bf16", 257),
-    (6, "bf16", 1), (6, "fp8", 1), (3, "int8", 1), (4, "int8", 29),
+    (6, "bf16", 1), (6, "fp8", 1), (6, "int8", 1), (3, "int8", 1), (4, "int8", 29), (4, "fp8", 29),
 ])
 def test_workload_full_size(idx, kv_dtype, stride):
     b = W.workload(idx, kv_dtype=kv_dtype, device="cuda")
