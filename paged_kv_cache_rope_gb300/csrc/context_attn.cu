@@ -48,9 +48,10 @@
 // 128 whose codes TMA lands raw: E4M3 scores run on kind::f8f6f4 from the raw K codes against Q
 // split into hi + lo E4M3 tiles, INT8 K is converted to f16 with Q made f16, and V is converted
 // to f16 for a kind::f16 PV -- each conversion by the softmax warpgroup that will read the tile;
-// Q takes a power-of-two scale per row that the scores give back.  CTA = (request, KV head,
-// split, 128 rows): a 128-row tile is 128/g draft tokens x the g query heads of one KV head (the
-// Q box spans g heads), so each K / V tile serves the whole group; the two softmax warpgroups
+// Q takes a power-of-two scale per row that the scores give back.  Persistent like the context
+// kernel: work item = (request, KV head, split, 128 rows), claimed longest first; a 128-row tile
+// is 128/g draft tokens x the g query heads of one KV head (the Q box spans g heads), so each
+// K / V tile serves the whole group; the two softmax warpgroups
 // take the even and the odd KV tiles of one split of kv_chunk keys against the same Q tile; at
 // the end B hands its (max, sum) over through shared memory, A merges O_A and O_B from TMEM and
 // writes the output row (one split) or a partial row for the combine kernel.  Visibility of the
