@@ -115,6 +115,7 @@ struct HostPlan {
   int gen_rows = 0;                                  // rows of the generation requests
   int num_tiles = 0, num_splits = 0, kv_chunk = 0, max_splits = 0;
   int decode_nt = 1, num_items = 0, num_parts = 0;  // narrow decode n-tiles per CTA, CTAs per KV head, partial rows
+  bool decode_merge = false;                         // every narrow request has at most 4 columns
   int num_witems = 0;                                // wide decode CTAs per KV head
   int num_titems = 0;                                // tensor-core generation CTAs per KV head
   bool tc_wide = false;                              // wide requests take the tensor-core kernel
@@ -224,6 +225,7 @@ void plan_decode_shape(const pkv_pool* pool, int32_t Hq, int64_t total, int max_
                               pkv::kTcChunkAlign));
   }
   hp->decode_nt = max_narrow > 8 ? 2 : 1;
+  hp->decode_merge = max_narrow <= 4;
 }
 
 // Workspace layout for the plan's counts and capacities (hp->lay.stage_pages set by the caller).
@@ -674,6 +676,7 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
     dp.total_witems = hp.num_witems;
     dp.total_parts = hp.num_parts;
     dp.nt = hp.decode_nt;
+    dp.merge_hilo = hp.decode_merge ? 1 : 0;
     dp.pool = static_cast<const uint8_t*>(pool->pool);
     dp.kv_scale = q8 ? pool->kv_scale_quant_orig : 1.0f;
     dp.scale_log2 = scale_log2;

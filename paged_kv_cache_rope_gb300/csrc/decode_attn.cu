@@ -408,7 +408,11 @@ __device__ __forceinline__ void transpose4x4_bytes(const uint32_t (&w)[4], uint3
   d[3] = __byte_perm(x1, y1, 0x7632);
 }
 
-template <int D, int KVK, int NT, bool WIDE>
+// MRG (E4M3 narrow kernel, one n-tile, at most 4 (token, head) columns per request): the hi and
+// lo halves of Q go into the n-tile's columns 0-3 and 4-7 of one MMA instead of two MMAs over
+// half-empty tiles, and likewise the hi and lo halves of P; the two halves of the scores are
+// added with one shuffle, those of O at the end.
+template <int D, int KVK, int NT, bool WIDE, bool MRG = false>
 __global__ void __launch_bounds__(DecodeCfg<D, KVK, WIDE>::kThreads)
 decode_splitkv_kernel(DecodeParams p) {
   using Cfg = DecodeCfg<D, KVK, WIDE>;
@@ -420,6 +424,7 @@ decode_splitkv_kernel(DecodeParams p) {
   // overflow the register file, converting was 17% faster.
   constexpr bool F16 = I8 || (KVK == kKvE4m3 && WIDE);
   constexpr bool FP8 = KVK == kKvE4m3 && !F16;
+  static_assert(!MRG || (FP8 && NT == 1 && !WIDE), "merged hi / lo columns: E4M3 narrow kernel, one n-tile");
   constexpr int KS = D / 16;  // k-steps over the head dim / m-tiles of O^T
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -471,7 +476,7 @@ decode_splitkv_kernel(DecodeParams p) {
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int c = wcol0 + nt * 8 + 2 * q4 + j;
+      const int c = wcol0 + nt * 8 + (MRG ? (2 * q4 + j) & 3 : 2 * q4 + j);
       uint64_t v = ~0ull;
       if (c < ncols) {
         const int i = c / p.group;
@@ -498,7 +503,7 @@ decode_splitkv_kernel(DecodeParams p) {
   float colscale[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int c = wcol0 + nt * 8 + g8;
+    const int c = wcol0 + nt * 8 + (MRG ? g8 & 3 : g8);  // MRG: columns 4-7 repeat 0-3 (lo half)
     const bool valid = c < ncols;
     const int ci = valid ? c / p.group : 0, hl = valid ? c - ci * p.group : 0;
     const uint16_t* qh = p.q + static_cast<int64_t>(row0 + ci) * p.q_stride + static_cast<int64_t>(h * p.group + hl) * D;
@@ -540,15 +545,15 @@ decode_splitkv_kernel(DecodeParams p) {
             uint32_t h01, l01, h23, l23;
             split_e4m3x2(xs[0] * up, xs[1] * up, h01, l01);
             split_e4m3x2(xs[2] * up, xs[3] * up, h23, l23);
-            qb[nt][kk][b] = h01 | (h23 << 16);
+            qb[nt][kk][b] = (MRG && g8 >= 4) ? (l01 | (l23 << 16)) : (h01 | (h23 << 16));
             ql[nt][kk][b] = l01 | (l23 << 16);
           }
         }
       }
       // score columns 2*q4, 2*q4+1 belong to heads held by lanes (2*q4)*4 and (2*q4+1)*4
       const float down = 1.f / up;
-      const float d0 = __shfl_sync(0xffffffffu, down, (2 * q4) * 4);
-      const float d1 = __shfl_sync(0xffffffffu, down, (2 * q4 + 1) * 4);
+      const float d0 = __shfl_sync(0xffffffffu, down, (MRG ? (2 * q4) & 3 : 2 * q4) * 4);
+      const float d1 = __shfl_sync(0xffffffffu, down, (MRG ? (2 * q4 + 1) & 3 : 2 * q4 + 1) * 4);
       colscale[nt][0] = d0 * p.kv_scale * p.scale_log2;
       colscale[nt][1] = d1 * p.kv_scale * p.scale_log2;
     }
@@ -680,8 +685,12 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               mma_e4m3_16832(sacc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-              mma_e4m3_16832(sacc[u][nt], a, ql[nt][kk][0], ql[nt][kk][1]);
+              if constexpr (!MRG) mma_e4m3_16832(sacc[u][nt], a, ql[nt][kk][0], ql[nt][kk][1]);
             }
+          }
+          if constexpr (MRG) {  // columns j and j + 4 hold the hi and lo halves of column j
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sacc[u][0][i] += __shfl_xor_sync(0xffffffffu, sacc[u][0][i], 2);
           }
         } else {
 #pragma unroll
@@ -824,8 +833,13 @@ decode_splitkv_kernel(DecodeParams p) {
             const uint32_t a[4] = {dj[0][2 * half], dj[0][2 * half + 1], dj[1][2 * half], dj[1][2 * half + 1]};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][0][0], p8[nt][0][1]);
-              mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][1][0], p8[nt][1][1]);
+              if constexpr (MRG) {  // hi codes in columns 0-3, lo codes in columns 4-7
+                const int hl = g8 >= 4 ? 1 : 0;
+                mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][hl][0], p8[nt][hl][1]);
+              } else {
+                mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][0][0], p8[nt][0][1]);
+                mma_e4m3_16832(o[nt][2 * pp + half], a, p8[nt][1][0], p8[nt][1][1]);
+              }
             }
           }
         } else {  // per 16-token sub-tile: dims 32pp + 4g + 2half + {0, 1} as rows
@@ -903,7 +917,8 @@ decode_splitkv_kernel(DecodeParams p) {
 #pragma unroll
       for (int w = 0; w < Cfg::kWarps; ++w) {
         const float f = ex2_approx(sm_m[w * HN + cl] - Mb);
-        acc += f * sm_o[(w * HN + cl) * D + d];
+        const float ow = sm_o[(w * HN + cl) * D + d] + (MRG ? sm_o[(w * HN + cl + 4) * D + d] : 0.f);
+        acc += f * ow;
         lsum += f * sm_l[w * HN + cl];
       }
     }
@@ -1036,10 +1051,10 @@ __global__ void __launch_bounds__(W * 32) combine_kernel(DecodeParams p) {
   *reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(row) * p.Hq * D + static_cast<int64_t>(hq) * D + 4 * lane) = packed;
 }
 
-template <int D, int KVK, int NT, bool WIDE>
+template <int D, int KVK, int NT, bool WIDE, bool MRG = false>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   using Cfg = DecodeCfg<D, KVK, WIDE>;
-  auto kern = decode_splitkv_kernel<D, KVK, NT, WIDE>;
+  auto kern = decode_splitkv_kernel<D, KVK, NT, WIDE, MRG>;
   constexpr int kMerge = Cfg::kWarps * NT * 8 * (D + 2) * 4;  // the epilogue's staging
   constexpr int kSmem = Cfg::kRingsBytes > kMerge ? Cfg::kRingsBytes : kMerge;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -1071,6 +1086,10 @@ template <int KVK>
 cudaError_t launch_decode_kind(const DecodeParams& p, bool wide, cudaStream_t s) {
   if (wide) {  // 16 columns per warp, 64 per CTA
     return p.D == 128 ? launch_decode_t<128, KVK, 2, true>(p, s) : launch_decode_t<64, KVK, 2, true>(p, s);
+  }
+  if constexpr (KVK == kKvE4m3) {  // at most 4 columns per request: hi and lo in one n-tile
+    if (p.merge_hilo && p.nt == 1)
+      return p.D == 128 ? launch_decode_t<128, KVK, 1, false, true>(p, s) : launch_decode_t<64, KVK, 1, false, true>(p, s);
   }
   if (p.D == 128) return p.nt == 1 ? launch_decode_t<128, KVK, 1, false>(p, s) : launch_decode_t<128, KVK, 2, false>(p, s);
   return p.nt == 1 ? launch_decode_t<64, KVK, 1, false>(p, s) : launch_decode_t<64, KVK, 2, false>(p, s);

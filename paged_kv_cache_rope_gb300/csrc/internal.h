@@ -175,6 +175,7 @@ struct DecodeParams {
   int32_t total_parts;      // partial-result rows the workspace holds (per query head)
   const int32_t* counts;    // the plan's PlanCount words
   int32_t nt;               // n-tiles of 8 columns per decode CTA (1 or 2)
+  int32_t merge_hilo;       // E4M3 narrow kernel: every request has at most 4 columns
   const uint8_t* pool;
   float kv_scale;           // dequantisation multiplier (1 for bf16)
   float scale_log2;         // softmax_scale * log2(e)
