@@ -84,24 +84,31 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could
 
 // Generation kernel: one Q tile (A and B share it), K[3], V[3] -- each K / V tile has one
 // consumer and the two halves alternate.
-// With an 8-bit pool (KV != 0): Q, K[2], V[2] (f16; for E4M3 the K[0] area holds the
-// hi and lo E4M3 Q tiles instead), a ring of the raw codes (K[2], V[2]) that TMA fills and the
-// softmax warpgroups convert, and the per-row Q scales.  Then B's (m, l) per row for A's
-// merge (its own area: the K ring already holds the next item's tiles when an item ends).
+// With an INT8 pool: Q, K[2], V[2] (f16), a ring of the raw codes (K[2], V[2]) that TMA fills
+// and the softmax warpgroups convert, and the per-row Q scales.  With an E4M3 pool the scores
+// read the raw K codes and Q's hi and lo E4M3 tiles, which replace the bf16 Q tile in place (a
+// row's two 128-code halves take the 256 bytes of its bf16 codes), so there is no f16 K ring:
+// Q, V[3] (f16), raw K[3], raw V[3] -- a V tile is converted into a stage whose previous PV was
+// the other warpgroup's, issued half a cycle earlier, not the converting warpgroup's own PV that
+// has just been issued.  Then B's (m, l) per row for A's merge (its own area: the K ring
+// already holds the next item's tiles when an item ends).
 template <int D, int KV = 0>
 struct GenSmem {
   static constexpr bool kQ8 = KV != 0;
+  static constexpr bool kF8S = KV == PKV_FP8_E4M3;
   static constexpr int kHalf = 128 * 128;         // one 64-wide half of a 128-row tile (bytes)
   static constexpr int kTile = (D / 64) * kHalf;  // one Q tile or one K / V stage
-  static constexpr int kStages = kQ8 ? 2 : 3;
+  static constexpr int kStages = (kQ8 && !kF8S) ? 2 : 3;  // V stages (and K stages, but E4M3 has none)
+  static constexpr int kKStages = kF8S ? 0 : kStages;
+  static constexpr int kRawStages = kF8S ? 3 : 2;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kTile;
-  static constexpr int kVOff = kKOff + kStages * kTile;
+  static constexpr int kVOff = kKOff + kKStages * kTile;
   static constexpr int kRawTile = 128 * D;        // 128 rows of D one-byte codes
   static constexpr int kRawKOff = kVOff + kStages * kTile;
-  static constexpr int kRawVOff = kRawKOff + (kQ8 ? 2 : 0) * kRawTile;
-  static constexpr int kBarOff = kRawVOff + (kQ8 ? 2 : 0) * kRawTile;
-  static constexpr int kBarBytes = 320;
+  static constexpr int kRawVOff = kRawKOff + (kQ8 ? kRawStages : 0) * kRawTile;
+  static constexpr int kBarOff = kRawVOff + (kQ8 ? kRawStages : 0) * kRawTile;
+  static constexpr int kBarBytes = 384;
   static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 1 / (Q row's power-of-two scale)
   static constexpr int kXchOff = kQScaleOff + (kQ8 ? 128 * 4 : 0);  // [2][128] floats: B's m, l
   static constexpr int kBytes = kXchOff + 2 * 128 * 4 + 1024;  // + alignment slack
@@ -120,17 +127,17 @@ enum {
   BAR_ODONE = 17,  // +2
   BAR_MMADONE = 19,
   BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
-  BAR_RAWK = 21,   // +2: 8-bit pool, raw K codes landed (TMA)
-  BAR_RAWV = 23,   // +2: raw V codes landed
-  BAR_RAWKEMPTY = 25, // +2: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
-  BAR_RAWVEMPTY = 27, // +2: a raw V stage has been converted
-  BAR_QRAW = 29,   // the bf16 Q tile landed (warpgroup A rescales and re-encodes it)
-  BAR_QFREE = 30,  // an item's last S MMA is done: its Q tile (and re-encoding) may be replaced
-  BAR_ITEM = 31,   // +2: item ring entry written
-  BAR_ITEMFREE = 33,  // +2: item ring entry read by the MMA warp and the eight softmax warps
-  BAR_IDONE = 35,  // an item is finished by the MMA warp (issued) and the eight softmax warps
-  BAR_QSREAD = 36, // 8-bit pool: warpgroup A has read the item's Q row scales
-  NUM_BARS = 37
+  BAR_RAWK = 21,   // +3: 8-bit pool, raw K codes landed (TMA)
+  BAR_RAWV = 24,   // +3: raw V codes landed
+  BAR_RAWKEMPTY = 27, // +3: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
+  BAR_RAWVEMPTY = 30, // +3: a raw V stage has been converted
+  BAR_QRAW = 33,   // the bf16 Q tile landed (warpgroup B rescales and re-encodes it)
+  BAR_QFREE = 34,  // an item's last S MMA is done: its Q tile (and re-encoding) may be replaced
+  BAR_ITEM = 35,   // +2: item ring entry written
+  BAR_ITEMFREE = 37,  // +2: item ring entry read by the MMA warp and the eight softmax warps
+  BAR_IDONE = 39,  // an item is finished by the MMA warp (issued) and the eight softmax warps
+  BAR_QSREAD = 40, // 8-bit pool: warpgroup A has read the item's Q row scales
+  NUM_BARS = 41
 };
 
 
@@ -146,9 +153,12 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
   // E4M3 codes (about 8 significant bits together); only V is converted to f16
   constexpr bool F8S = KV == PKV_FP8_E4M3;
   constexpr int S = L::kStages;
-  // ring stage and phase of the g-th K / V tile of the stream
+  constexpr int R = L::kRawStages;
+  // ring stage and phase of the g-th K / V tile of the stream (f16 / bf16 rings, raw rings)
   auto stg = [](int g) { return g % S; };
   auto phs = [](int g) { return (g / S) & 1; };
+  auto rstg = [](int g) { return g % R; };
+  auto rphs = [](int g) { return (g / R) & 1; };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -176,7 +186,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       tc::mbar_init(bar(BAR_VEMPTY + s), 1);
     }
     if (Q8) {
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < R; ++s) {
         tc::mbar_init(bar(BAR_RAWK + s), 1);
         tc::mbar_init(bar(BAR_RAWV + s), 1);
         tc::mbar_init(bar(BAR_RAWKEMPTY + s), F8S ? 1 : 4);
@@ -331,28 +341,30 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
           const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
           const int n_pages_seq = (it.L_r + p.B - 1) / p.B;
-          // tile j of the item into the next stage of the CTA's stream
-          auto issue_tile = [&](int j) {
+          // lane pp < pages_per_tile holds page pp of tile j (B <= 128: whole pages per tile); the
+          // table entry is read a step ahead of its copies, so its load overlaps the waits before them
+          auto has_page = [&](int j) {
+            const int lb = (it.kt0 + j * kCtxTileN) / p.B + lane;
+            return lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks;
+          };
+          auto lookup = [&](int j) { return has_page(j) ? __ldg(tbl + (it.kt0 + j * kCtxTileN) / p.B + lane) : -1; };
+          // tile j of the item (table entries pg) into the next stage of the CTA's stream
+          auto issue_tile = [&](int j, int pg) {
             if (warp_abort()) return false;
             const int g = issued_k;  // == issued_v: the tile's place in the CTA's stream
-            // lane pp < pages_per_tile looks up page pp of the tile (B <= 128: whole pages per tile)
-            const int lb = (it.kt0 + j * kCtxTileN) / p.B + lane;
-            int pg = -1;
-            if (lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks) {
-              pg = __ldg(tbl + lb);
-              if (pg < 0 || pg >= p.NB) {
-                flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
-                pg = -1;
-              }
+            if (has_page(j) && (pg < 0 || pg >= p.NB)) {
+              flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+              pg = -1;
             }
             const uint32_t bytes =
                 static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
             if constexpr (Q8) {
               // raw codes of page `lane` into the raw rings; K and V stages are freed separately
-              // (a V stage waits for the PV two tiles back, a K stage only for its S or conversion)
+              // (a raw V stage once its codes are converted, a raw K stage once its S is done
+              // (E4M3) or its codes are converted (INT8))
               const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
-              const int rs = g & 1, rph = ((g - 2) >> 1) & 1;
-              if (g >= 2 && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) return false;
+              const int rs = rstg(g), rph = rphs(g - R);
+              if (g >= R && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) return false;
               if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWK + rs), bytes);
               __syncwarp();
               if (pg >= 0)
@@ -360,7 +372,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
                                 (pg * 2 + 0) * p.B);
               __syncwarp();
               ++issued_k;
-              if (g >= 2 && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) return false;
+              if (g >= R && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) return false;
               if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWV + rs), bytes);
               __syncwarp();
               if (pg >= 0)
@@ -394,8 +406,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             ++issued_v;
             return true;
           };
-          // the item's first tiles go out as soon as stages free up (while the previous item
-          // ends), its Q tile once the previous item's last S MMA is done, then the rest
+          // the item's Q tile goes out as soon as the previous item's last S MMA is done, then its
+          // tiles as stages free up; the first tile's table entries load meanwhile
 #ifdef PKV_SELFTEST
           // Self-test build only (compiled by the tests, never into libpaged_kv.so): no K / V
           // copy is issued, so the MMA warp's wait for the first K tile and the softmax warps'
@@ -405,8 +417,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 #else
           const int n_issue = nT;
 #endif
-          const int pre = min(n_issue, 1);
-          for (int j = 0; pok && j < pre; ++j) pok = issue_tile(j);
+          int pg_next = n_issue > 0 ? lookup(0) : -1;
           if (pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
           if (!pok) break;
           // one Q tile (128 / g tokens x the group's g heads), shared by A and B
@@ -417,7 +428,11 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           }
           __syncwarp();
           ++nq;
-          for (int j = pre; pok && j < n_issue; ++j) pok = issue_tile(j);
+          for (int j = 0; pok && j < n_issue; ++j) {
+            const int pg = pg_next;
+            if (j + 1 < n_issue) pg_next = lookup(j + 1);
+            pok = issue_tile(j, pg);
+          }
         }
         if (!pok) break;
         // claim the next item while this one's tiles are still being consumed
@@ -430,10 +445,10 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       // the last copy into each stage and the last Q tile have landed before the CTA can wind
       // down, however the consumers fare (on the normal path these phases completed long ago)
       if constexpr (Q8) {
-        for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
-          tc::mbar_wait(bar(BAR_RAWK + (j & 1)), (j >> 1) & 1, 200000000LL);
-        for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
-          tc::mbar_wait(bar(BAR_RAWV + (j & 1)), (j >> 1) & 1, 200000000LL);
+        for (int j = (issued_k > R ? issued_k - R : 0); j < issued_k; ++j)
+          tc::mbar_wait(bar(BAR_RAWK + rstg(j)), rphs(j), 200000000LL);
+        for (int j = (issued_v > R ? issued_v - R : 0); j < issued_v; ++j)
+          tc::mbar_wait(bar(BAR_RAWV + rstg(j)), rphs(j), 200000000LL);
       } else {
         for (int j = (issued_k > S ? issued_k - S : 0); j < issued_k; ++j)
           tc::mbar_wait(bar(BAR_KFULL + stg(j)), phs(j), 200000000LL);
@@ -472,7 +487,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         auto gtile = [&](int j, int x) { return G + 2 * j + x; };
         auto kfull = [&](int j, int x) {
           const int g = gtile(j, x);
-          if constexpr (F8S) return warp_wait(bar(BAR_RAWK + (g & 1)), (g >> 1) & 1);  // raw codes landed
+          if constexpr (F8S) return warp_wait(bar(BAR_RAWK + rstg(g)), rphs(g));  // raw codes landed
           return warp_wait(bar(BAR_KFULL + stg(g)), phs(g));
         };
         auto issue_s = [&](int j, int x) {
@@ -481,11 +496,11 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           const uint64_t a0 = dq0;  // A and B share the Q tile
           const uint64_t b0 = dk0 + stage_off(st);
           if constexpr (F8S) {
-            // Q hi and lo tiles (one 128-byte row of codes per Q row) sit in the f16 K stage 0
-            // area; K is the raw tile: four K=32 steps of 32 bytes, hi then lo
-            const uint64_t aq = tc::sdesc_sw128(sK(0), 16, 1024);
-            const uint64_t bk = tc::sdesc_sw128(base_s + L::kRawKOff + (g & 1) * L::kRawTile, 16, 1024);
-            constexpr uint64_t kLo = 128 * 128 / 16;  // lo tile: 16 KB after hi
+            // Q hi and lo tiles (one 128-byte row of codes per Q row) replace the bf16 Q tile's
+            // two halves; K is the raw tile: four K=32 steps of 32 bytes, hi then lo
+            const uint64_t aq = dq0;
+            const uint64_t bk = tc::sdesc_sw128(base_s + L::kRawKOff + rstg(g) * L::kRawTile, 16, 1024);
+            constexpr uint64_t kLo = L::kHalf / 16;  // lo tile: the Q tile's second half
             if (tc::elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
@@ -493,7 +508,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3_ss(tmem + 128 * x, aq + kLo + 2 * kk, bk + 2 * kk, idesc_s, 1u);
               tc::mma_commit(bar(BAR_SFULL + x));
-              tc::mma_commit(bar(BAR_RAWKEMPTY + (g & 1)));  // the raw K stage may be refilled
+              tc::mma_commit(bar(BAR_RAWKEMPTY + rstg(g)));  // the raw K stage may be refilled
               if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(BAR_QFREE));  // the item's last S
             }
             __syncwarp();
@@ -588,11 +603,13 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     // MMAs read, in 64-wide head-dim halves.  Both code kinds are exact in f16: E4M3 through the
     // hardware conversion (measured 4% faster here than placing the bits with integer ops),
     // INT8 as integers.  A warpgroup converts its next tile right after handing over its P,
-    // while its own PV and the other warpgroup's MMAs run.
-    auto cvt_row = [&](uint32_t raw_off, uint32_t dst_s) {
+    // while its own PV and the other warpgroup's MMAs run.  A V row past the end of the sequence
+    // (stale or unloaded slot) is written as zeros instead.
+    auto cvt_row = [&](uint32_t raw_off, uint32_t dst_s, bool zero) {
 #pragma unroll
       for (int jc = 0; jc < 8; ++jc) {
-        const uint4 w = *reinterpret_cast<const uint4*>(base + raw_off + row * 128 + ((jc ^ (row & 7)) << 4));
+        const uint4 w = zero ? make_uint4(0u, 0u, 0u, 0u)
+                             : *reinterpret_cast<const uint4*>(base + raw_off + row * 128 + ((jc ^ (row & 7)) << 4));
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
         uint32_t f[8];
 #pragma unroll
@@ -609,27 +626,28 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         st_shared_v4(drow + (((c0 + 1) ^ static_cast<uint32_t>(row & 7)) << 4), f[4], f[5], f[6], f[7]);
       }
     };
-    // tile g of the stream (this warpgroup's parity): K into f16 stage g % 2 once the stage's
-    // previous S is done, then V once its previous PV is done; each step frees a raw stage
-    auto convert_tile = [&](int g) {
-      const int st = g & 1, ph = (g >> 1) & 1, ph_prev = ((g - 2) >> 1) & 1;
+    // tile g of the stream (this warpgroup's), whose first vrows rows hold keys of the split: raw
+    // stage g % R into f16 stage g % S -- K once the stage's previous S is done, then V once its
+    // previous PV is done; each step frees a raw stage
+    auto convert_tile = [&](int g, int vrows) {
+      const int rs = rstg(g), rph = rphs(g), st = stg(g), ph_prev = phs(g - S);
       if constexpr (!F8S) {  // E4M3 scores read the raw K codes themselves
-        if (!warp_wait(bar(BAR_RAWK + st), ph) || (g >= 2 && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) return false;
-        cvt_row(L::kRawKOff + st * L::kRawTile, sK(st));
+        if (!warp_wait(bar(BAR_RAWK + rs), rph) || (g >= S && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) return false;
+        cvt_row(L::kRawKOff + rs * L::kRawTile, sK(st), false);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tc::mbar_arrive(bar(BAR_KFULL + st));
-          tc::mbar_arrive(bar(BAR_RAWKEMPTY + st));
+          tc::mbar_arrive(bar(BAR_RAWKEMPTY + rs));
         }
       }
-      if (!warp_wait(bar(BAR_RAWV + st), ph) || (g >= 2 && !warp_wait(bar(BAR_VEMPTY + st), ph_prev))) return false;
-      cvt_row(L::kRawVOff + st * L::kRawTile, sV(st));
+      if (!warp_wait(bar(BAR_RAWV + rs), rph) || (g >= S && !warp_wait(bar(BAR_VEMPTY + st), ph_prev))) return false;
+      cvt_row(L::kRawVOff + rs * L::kRawTile, sV(st), row >= vrows);
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(bar(BAR_VFULL + st));
-        tc::mbar_arrive(bar(BAR_RAWVEMPTY + st));
+        tc::mbar_arrive(bar(BAR_RAWVEMPTY + rs));
       }
       return true;
     };
@@ -693,15 +711,19 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             if (nq > 0 && !warp_wait(bar(BAR_QSREAD), (nq - 1) & 1)) { ok = false; break; }
             if constexpr (F8S) {
               // code chunk jc (16 codes = q elements 16 jc ..) from bf16 chunks 2 (jc % 4) and
-              // 2 (jc % 4) + 1 of head-dim half jc / 4; hi tile at sK(0), lo tile 16 KB after it
+              // 2 (jc % 4) + 1 of head-dim half jc / 4; the hi tile replaces the row's first half
+              // and the lo tile its second, so the whole row is read before any of it is written
+              uint4 qr[16];
+#pragma unroll
+              for (int c = 0; c < 16; ++c)
+                qr[c] = *reinterpret_cast<const uint4*>(base + L::kQOff + (c >> 3) * L::kHalf + row * 128 +
+                                                        (((c & 7) ^ (row & 7)) << 4));
 #pragma unroll
               for (int jc = 0; jc < 8; ++jc) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int hc = 0; hc < 2; ++hc) {
-                  const int c = 2 * (jc & 3) + hc;
-                  const uint4 w = *reinterpret_cast<const uint4*>(base + L::kQOff + (jc >> 2) * L::kHalf + row * 128 +
-                                                                  ((c ^ (row & 7)) << 4));
+                  const uint4 w = qr[(jc >> 2) * 8 + 2 * (jc & 3) + hc];
                   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                   for (int k = 0; k < 4; k += 2) {
@@ -714,8 +736,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
                   }
                 }
                 const uint32_t off = static_cast<uint32_t>(row * 128 + ((jc ^ (row & 7)) << 4));
-                st_shared_v4(sK(0) + off, hw[0], hw[1], hw[2], hw[3]);
-                st_shared_v4(sK(0) + 128 * 128 + off, lw[0], lw[1], lw[2], lw[3]);
+                st_shared_v4(sQ + off, hw[0], hw[1], hw[2], hw[3]);
+                st_shared_v4(sQ + L::kHalf + off, lw[0], lw[1], lw[2], lw[3]);
               }
             } else {
 #pragma unroll
@@ -736,7 +758,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
           }
         }
-        if (ok && nk > 0) ok = convert_tile(gtile(0));  // this warpgroup's first tile
+        if (ok && nk > 0) ok = convert_tile(gtile(0), it.kend - (it.kt0 + x * kCtxTileN));  // its first tile
         if (!ok) break;
       }
       if (!wait_prev(ndone)) { ok = false; break; }
@@ -774,13 +796,24 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
             return (low(past - t0) | nv) & low(kend - t0);
           };
+          // a select per key only in the words where some row misses some key
           const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
+          const uint32_t all = 0xffffffffu;
+          if (__any_sync(all, m0 != all)) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
-            v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
-            v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
-            v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
+            for (int e = 0; e < 32; ++e) v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+          }
+          if (__any_sync(all, m1 != all)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
+          }
+          if (__any_sync(all, m2 != all)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
+          }
+          if (__any_sync(all, m3 != all)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
           }
         }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -832,8 +865,9 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
         l_run += lsum.x + lsum.y;
         tc::tmem_wait_st();
-        if (2 * j + x == nT - 1 && x == zero_x) {
-          // zero V rows past the end of the sequence (stale or unloaded slots) before any PV
+        if (!Q8 && 2 * j + x == nT - 1 && x == zero_x) {
+          // zero V rows past the end of the sequence (stale or unloaded slots) before any PV (an
+          // 8-bit pool's conversion writes them as zeros)
           const int g = G + nT - 1;
           if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
           if (kt0 + (nT - 1) * kCtxTileN + row >= kend) {
@@ -851,7 +885,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(BAR_PFULL + x));
         if constexpr (Q8) {  // the warpgroup's next tile, while its PV and the other tile's MMAs run
-          if (j + 1 < nk && !convert_tile(gtile(j + 1))) { ok = false; break; }
+          if (j + 1 < nk && !convert_tile(gtile(j + 1), kend - (kt0 + (2 * j + 2 + x) * kCtxTileN))) { ok = false; break; }
         }
       }
       if (!ok) break;
