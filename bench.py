@@ -577,6 +577,9 @@ SUB_WORKLOADS = (
     ("mixed_fp8", 4, "fp8"),
     ("decode_gqa", 3, "bf16"),
     ("decode_gqa_fp8", 3, "fp8"),
+    ("draft", 6, "bf16"),
+    ("draft_fp8", 6, "fp8"),
+    ("draft_int8", 6, "int8"),
     ("tiny", 1, "bf16"),
 )
 
@@ -638,7 +641,8 @@ def run_ours(args):
     ctx_cpu = []
     if not args.no_sub and args.workload == 2 and args.max_gen is None:
         # the rest of the metric, measured in the same run: the prefill TFLOP/s half on the 16K
-        # prefill, the mixed inflight batch, the GQA decode, the tiny batch's launch overhead
+        # prefill, the mixed inflight batch, the GQA decode, draft-token verification on the
+        # three pool kinds, the tiny batch's launch overhead
         sub_steps = max(3, min(args.steps, 20))
         subs = {}
         for key, wl, kd in SUB_WORKLOADS:
