@@ -118,6 +118,7 @@ struct HostPlan {
   bool decode_merge = false;                         // every narrow request has at most 4 columns
   int num_witems = 0;                                // wide decode CTAs per KV head
   int num_titems = 0;                                // tensor-core generation CTAs per KV head
+  int max_tc_cols = 0;                               // most (token, head) columns of such a request
   bool tc_wide = false;                              // wide requests take the tensor-core kernel
   bool staging = false;                              // 8-bit pool with context rows: stage their pages
   bool dyn = false;                                  // bucket mode
@@ -275,13 +276,18 @@ void plan_attention(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPl
   plan_decode_shape(pool, Hq, total, max_narrow, any_wide, hp);
   const int cols = 8 * hp->decode_nt;
   hp->num_splits = hp->max_splits = hp->num_items = hp->num_witems = hp->num_titems = hp->num_parts = 0;
+  hp->max_tc_cols = 0;
   for (int r = hp->C; r < hp->R; ++r) {
     const int n = b->h_context_lengths[r], cols_r = n * group;
     const int s = (b->h_past_kv_lengths[r] + n + hp->kv_chunk - 1) / hp->kv_chunk;
     hp->num_splits += s;
     if (cols_r <= pkv::kDecodeNarrowMaxCols) hp->num_items += s * ((cols_r + cols - 1) / cols);
-    else if (hp->tc_wide) hp->num_titems += s * ((cols_r + pkv::kCtxTileM - 1) / pkv::kCtxTileM);
-    else hp->num_witems += s * ((cols_r + pkv::kDecodeWideCols - 1) / pkv::kDecodeWideCols);
+    else if (hp->tc_wide) {
+      hp->num_titems += s * ((cols_r + pkv::kCtxTileM - 1) / pkv::kCtxTileM);
+      hp->max_tc_cols = std::max(hp->max_tc_cols, cols_r);
+    } else {
+      hp->num_witems += s * ((cols_r + pkv::kDecodeWideCols - 1) / pkv::kDecodeWideCols);
+    }
     hp->num_parts += s * n;
     hp->max_splits = std::max(hp->max_splits, s);
   }
@@ -344,6 +350,7 @@ void plan_attention_bucket(const pkv_pool* pool, const pkv_batch* b, int32_t Hq,
                        ? hp->G * s_max * ((wide_cols + pkv::kDecodeWideCols - 1) / pkv::kDecodeWideCols)
                        : 0;
   hp->num_titems = hp->tc_wide ? hp->G * s_max * ((wide_cols + pkv::kCtxTileM - 1) / pkv::kCtxTileM) : 0;
+  hp->max_tc_cols = hp->tc_wide ? wide_cols : 0;
   hp->num_parts = s_max * hp->gen_rows;
   hp->lay.stage_pages =
       hp->staging ? static_cast<int64_t>(hp->C) * ((hp->max_kv_len + pool->tokens_per_block - 1) / pool->tokens_per_block)
@@ -717,8 +724,12 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
       // wide generation requests on the tensor-core kernel: a Q box is g heads x 128/g tokens,
       // i.e. 128 (token, head) rows of one KV head
       const int group = num_q_heads / Hkv;
+      // at most 64 rows per request (and g dividing 16): two threads per Q row, the Q tile
+      // loaded as four boxes of 16 rows (g heads x 16 / g tokens)
+      const bool half_rows = hp.max_tc_cols <= pkv::kCtxTileM / 2 && 16 % group == 0;
       CUtensorMap qmap_g, kvmap_g;
-      if (!encode_rows_map(&qmap_g, q_rot, D, num_q_heads, hp.T, q_row_stride * 2, pkv::kCtxTileM / group, group))
+      if (!encode_rows_map(&qmap_g, q_rot, D, num_q_heads, hp.T, q_row_stride * 2,
+                           (half_rows ? 16 : pkv::kCtxTileM) / group, group))
         return PKV_ERR_CUDA;
       const int64_t pool_rows_g = static_cast<int64_t>(pool->num_blocks) * 2 * pool->tokens_per_block;
       const int box_rows_g = std::min(pool->tokens_per_block, pkv::kCtxTileN);
@@ -745,6 +756,7 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
       tp.scale_log2 = q8 ? scale_log2 * pool->kv_scale_quant_orig : scale_log2;
       tp.out_scale = q8 ? pool->kv_scale_quant_orig : 1.0f;
       tp.kv_dtype = pool->dtype;
+      tp.half_rows = half_rows ? 1 : 0;
       tp.d_error = d_error;
       tp.G = hp.G;
       tp.counts = counts;

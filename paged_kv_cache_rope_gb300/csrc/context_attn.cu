@@ -56,7 +56,11 @@
 // the end B hands its (max, sum) over through shared memory, A merges O_A and O_B from TMEM and
 // writes the output row (one split) or a partial row for the combine kernel.  Visibility of the
 // new keys comes from the draft-token mask words (bitmaps per row), applied only to the tiles
-// that hold new keys.
+// that hold new keys.  When no request has more than 64 rows (e.g. 8 draft tokens x 8 heads) and
+// g divides 16, the Q rows sit in the first 16 TMEM lanes of each warp's quarter and two threads
+// share a row through the 16x32bx2 TMEM shape, each taking half of a tile's keys (max and sum
+// combined with one shuffle) and half of the output columns: the softmax of a tile is spread over
+// all four sub-partitions instead of running on the two whose lanes hold the rows.
 //
 // Rows past the request's end and keys past the causal limit are masked by select (never by
 // arithmetic on the loaded values); V rows past the sequence end are zeroed before PV, so
@@ -141,7 +145,7 @@ enum {
 };
 
 
-template <int D, int KV>
+template <int D, int KV, bool HALF>
 __global__ void __launch_bounds__(kThreads, 1)
 gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
                 const __grid_constant__ CUtensorMap kv_map) {
@@ -342,7 +346,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
           const int n_pages_seq = (it.L_r + p.B - 1) / p.B;
           // lane pp < pages_per_tile holds page pp of tile j (B <= 128: whole pages per tile); the
-          // table entry is read a step ahead of its copies, so its load overlaps the waits before them
+          // table entry is read a tile ahead of its copies, so its load overlaps the waits before them
           auto has_page = [&](int j) {
             const int lb = (it.kt0 + j * kCtxTileN) / p.B + lane;
             return lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks;
@@ -420,11 +424,20 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           int pg_next = n_issue > 0 ? lookup(0) : -1;
           if (pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
           if (!pok) break;
-          // one Q tile (128 / g tokens x the group's g heads), shared by A and B
+          // one Q tile (128 / g tokens x the group's g heads), shared by A and B; HALF: 64 rows,
+          // rows 16k .. 16k+15 into tile rows 32k .. 32k+15 (a box of g heads x 16 / g tokens)
           if (tc::elect_one()) {
-            tc::mbar_arrive_expect_tx(bar(q_bar), 128 * D * 2);
-            for (int dh = 0; dh < D / 64; ++dh)
-              tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, it.hk * p.group, it.q_row);
+            if constexpr (HALF) {
+              tc::mbar_arrive_expect_tx(bar(q_bar), 64 * D * 2);
+              for (int kq = 0; kq < 4; ++kq)
+                for (int dh = 0; dh < D / 64; ++dh)
+                  tc::tma_load_4d(sQ + dh * L::kHalf + kq * 32 * 128, &q_map, bar(q_bar), 0, dh, it.hk * p.group,
+                                  it.q_row + kq * 16 / p.group);
+            } else {
+              tc::mbar_arrive_expect_tx(bar(q_bar), 128 * D * 2);
+              for (int dh = 0; dh < D / 64; ++dh)
+                tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, it.hk * p.group, it.q_row);
+            }
           }
           __syncwarp();
           ++nq;
@@ -592,7 +605,13 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     // ======================= softmax warpgroups =======================
     tc::regs_inc<kRegsSoftmax>();
     const int x = warp >> 2;                 // Q tile A (0) or B (1)
-    const int row = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const int row = (warp & 3) * 32 + lane;  // tile row == TMEM lane (K / V rows, Q re-encoding)
+    // HALF (at most 64 Q rows): Q row qrow sits in tile row srow, the first 16 lanes of each
+    // warp's quarter; threads t and t + 16 of a warp share it, each on one half (kh) of the keys
+    // of a tile and of the output columns.  Otherwise a thread owns tile row `row` whole.
+    const int qrow = HALF ? (warp & 3) * 16 + (lane & 15) : row;
+    const int srow = HALF ? (warp & 3) * 32 + (lane & 15) : row;
+    const int kh = HALF ? (lane >> 4) : 0;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128 * x + lane_off;
     const uint32_t tO = tmem + 256 + 128 * x + lane_off;
@@ -668,8 +687,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       uint64_t vis = ~0ull;
       int tok_i = 0, hl = 0;
       {
-        const int pr = it.pr0 + row;  // A and B hold the same rows
-        if (row < nvx) {
+        const int pr = it.pr0 + qrow;  // A and B hold the same rows
+        if (qrow < nvx) {
           tok_i = pr / p.group;
           hl = pr - tok_i * p.group;
           if (p.mask != nullptr) {
@@ -764,7 +783,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       if (!wait_prev(ndone)) { ok = false; break; }
       if constexpr (Q8) {
         ok = warp_wait(bar(BAR_Q), nq & 1);
-        if (ok) sl2 *= qscale[row];
+        if (ok) sl2 *= qscale[srow];
         ++nq;
         if (!ok) break;
         __syncwarp();
@@ -775,96 +794,174 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       for (int j = 0; ok && j < nk; ++j) {
         if (!warp_wait(bar(BAR_SFULL + x), (sc + j) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        uint32_t v0[32], v1[32], v2[32], v3[32];
-        tc::tmem_ld32_async(tS + 0, v0);
-        tc::tmem_ld32_async(tS + 32, v1);
-        tc::tmem_ld32_async(tS + 64, v2);
-        tc::tmem_ld32_async(tS + 96, v3);
-        tc::tmem_wait_ld_dep(v0);
-        tc::reg_dep(v1);
-        tc::reg_dep(v2);
-        tc::reg_dep(v3);
-        const int tb = kt0 + (2 * j + x) * kCtxTileN;  // key of column 0
-        if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
-          // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
-          // keys this row's token sees (bits of vis), nothing at or past the split's end
-          auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
-          auto word = [&](int wd) {
-            const int t0 = tb + 32 * wd, sh = t0 - past;
-            uint32_t nv = 0u;
-            if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
-            else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
-            return (low(past - t0) | nv) & low(kend - t0);
-          };
-          // a select per key only in the words where some row misses some key
-          const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
-          const uint32_t all = 0xffffffffu;
-          if (__any_sync(all, m0 != all)) {
+        if constexpr (HALF) {
+          // the thread's half of the tile row: keys 64 kh + [0, 32) in v0, 64 kh + [32, 64) in v1
+          uint32_t v0[32], v1[32];
+          tc::tmem_ld16x2_x32_async<64>(tS + 0, v0);
+          tc::tmem_ld16x2_x32_async<64>(tS + 32, v1);
+          tc::tmem_wait_ld_dep(v0);
+          tc::reg_dep(v1);
+          const int tb = kt0 + (2 * j + x) * kCtxTileN;  // key of column 0
+          if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
+            auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
+            auto word = [&](int wd) {
+              const int t0 = tb + 32 * wd, sh = t0 - past;
+              uint32_t nv = 0u;
+              if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
+              else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
+              return (low(past - t0) | nv) & low(kend - t0);
+            };
+            const uint32_t m0 = word(2 * kh), m1 = word(2 * kh + 1);
+            const uint32_t all = 0xffffffffu;
+            if (__any_sync(all, m0 != all)) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+              for (int e = 0; e < 32; ++e) v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+            }
+            if (__any_sync(all, m1 != all)) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
+            }
           }
-          if (__any_sync(all, m1 != all)) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
-          }
-          if (__any_sync(all, m2 != all)) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
-          }
-          if (__any_sync(all, m3 != all)) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
-          }
-        }
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          mx[0] = max3f(mx[0], __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
-          mx[1] = max3f(mx[1], __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
-          mx[2] = max3f(mx[2], __uint_as_float(v2[e]), __uint_as_float(v2[e + 1]));
-          mx[3] = max3f(mx[3], __uint_as_float(v3[e]), __uint_as_float(v3[e + 1]));
-        }
-        const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
-        float m_use = m_run;
-        if (j == 0) {
-          m_use = m_new;  // O is still empty
-        } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
-          // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
-          const float f = ex2_approx(m_run - m_new);
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tc::tmem_st32(tO + cc * 32, o);
-          }
-          l_run *= f;
-          m_use = m_new;
-        }
-        m_run = m_use;
-        // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
-        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float m_base = m_use == -INFINITY ? 0.f : m_use;  // no visible key yet (generation splits)
-        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
-        auto emit = [&](uint32_t(&v)[32], int c) {
-          uint32_t pk[16];
+          float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
-            const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
-            ls[c] = fadd2(ls[c], pv);
-            pk[e >> 1] = Q8 ? pack_f16x2(pv.x, pv.y) : pack_bf16x2(pv.x, pv.y);
+            mx0 = max3f(mx0, __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
+            mx1 = max3f(mx1, __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
           }
-          tc::tmem_st16(tS + 16 * c, pk);
-        };
-        emit(v0, 0);
-        emit(v1, 1);
-        emit(v2, 2);
-        emit(v3, 3);
-        const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
-        l_run += lsum.x + lsum.y;
-        tc::tmem_wait_st();
+          float mt = fmaxf(mx0, mx1);
+          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));  // the row's other half
+          const float m_new = fmaxf(m_run, mt * sl2);
+          float m_use = m_run;
+          if (j == 0) {
+            m_use = m_new;  // O is still empty
+          } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
+            // each thread rescales its half of the row's O columns
+            const float f = ex2_approx(m_run - m_new);
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+              uint32_t o[32];
+              tc::tmem_ld16x2_x32_async<D / 2>(tO + cc * 32, o);
+              tc::tmem_wait_ld_dep(o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+              tc::tmem_st16x2_x32<D / 2>(tO + cc * 32, o);
+            }
+            l_run *= f;
+            m_use = m_new;
+          }
+          m_run = m_use;
+          // P pairs of keys 64 kh + [0, 64) into S columns 32 kh + [0, 32) of the shared lane
+          float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float m_base = m_use == -INFINITY ? 0.f : m_use;
+          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
+          auto emit = [&](uint32_t(&v)[32], int c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
+              const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+              ls[c] = fadd2(ls[c], pv);
+              pk[e >> 1] = Q8 ? pack_f16x2(pv.x, pv.y) : pack_bf16x2(pv.x, pv.y);
+            }
+            tc::tmem_st16x2_x16<32>(tS + 16 * c, pk);
+          };
+          emit(v0, 0);
+          emit(v1, 1);
+          const float2 lsum = fadd2(ls[0], ls[1]);
+          l_run += lsum.x + lsum.y;  // this thread's half; the pair's halves are added at the end
+          tc::tmem_wait_st();
+        } else {
+          uint32_t v0[32], v1[32], v2[32], v3[32];
+          tc::tmem_ld32_async(tS + 0, v0);
+          tc::tmem_ld32_async(tS + 32, v1);
+          tc::tmem_ld32_async(tS + 64, v2);
+          tc::tmem_ld32_async(tS + 96, v3);
+          tc::tmem_wait_ld_dep(v0);
+          tc::reg_dep(v1);
+          tc::reg_dep(v2);
+          tc::reg_dep(v3);
+          const int tb = kt0 + (2 * j + x) * kCtxTileN;  // key of column 0
+          if (__any_sync(0xffffffffu, tb + kCtxTileN > kend || tb + kCtxTileN > past)) {
+            // visibility of columns 32w .. 32w+31 as one word: cached keys (t < past), the new
+            // keys this row's token sees (bits of vis), nothing at or past the split's end
+            auto low = [](int c) { return c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : (1u << c) - 1u); };
+            auto word = [&](int wd) {
+              const int t0 = tb + 32 * wd, sh = t0 - past;
+              uint32_t nv = 0u;
+              if (sh >= 0) nv = sh < 64 ? static_cast<uint32_t>(vis >> sh) : 0u;
+              else if (sh > -32) nv = static_cast<uint32_t>(vis << (-sh));
+              return (low(past - t0) | nv) & low(kend - t0);
+            };
+            // a select per key only in the words where some row misses some key
+            const uint32_t m0 = word(0), m1 = word(1), m2 = word(2), m3 = word(3);
+            const uint32_t all = 0xffffffffu;
+            if (__any_sync(all, m0 != all)) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v0[e] = (m0 >> e) & 1u ? v0[e] : __float_as_uint(-INFINITY);
+            }
+            if (__any_sync(all, m1 != all)) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v1[e] = (m1 >> e) & 1u ? v1[e] : __float_as_uint(-INFINITY);
+            }
+            if (__any_sync(all, m2 != all)) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v2[e] = (m2 >> e) & 1u ? v2[e] : __float_as_uint(-INFINITY);
+            }
+            if (__any_sync(all, m3 != all)) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v3[e] = (m3 >> e) & 1u ? v3[e] : __float_as_uint(-INFINITY);
+            }
+          }
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            mx[0] = max3f(mx[0], __uint_as_float(v0[e]), __uint_as_float(v0[e + 1]));
+            mx[1] = max3f(mx[1], __uint_as_float(v1[e]), __uint_as_float(v1[e + 1]));
+            mx[2] = max3f(mx[2], __uint_as_float(v2[e]), __uint_as_float(v2[e + 1]));
+            mx[3] = max3f(mx[3], __uint_as_float(v3[e]), __uint_as_float(v3[e + 1]));
+          }
+          const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
+          float m_use = m_run;
+          if (j == 0) {
+            m_use = m_new;  // O is still empty
+          } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
+            // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
+            const float f = ex2_approx(m_run - m_new);
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tc::tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+              tc::tmem_st32(tO + cc * 32, o);
+            }
+            l_run *= f;
+            m_use = m_new;
+          }
+          m_run = m_use;
+          // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
+          float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float m_base = m_use == -INFINITY ? 0.f : m_use;  // no visible key yet (generation splits)
+          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
+          auto emit = [&](uint32_t(&v)[32], int c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
+              const float2 pv = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+              ls[c] = fadd2(ls[c], pv);
+              pk[e >> 1] = Q8 ? pack_f16x2(pv.x, pv.y) : pack_bf16x2(pv.x, pv.y);
+            }
+            tc::tmem_st16(tS + 16 * c, pk);
+          };
+          emit(v0, 0);
+          emit(v1, 1);
+          emit(v2, 2);
+          emit(v3, 3);
+          const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+          l_run += lsum.x + lsum.y;
+          tc::tmem_wait_st();
+        }
         if (!Q8 && 2 * j + x == nT - 1 && x == zero_x) {
           // zero V rows past the end of the sequence (stale or unloaded slots) before any PV (an
           // 8-bit pool's conversion writes them as zeros)
@@ -895,22 +992,26 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         if (warp_abort() || !warp_wait(bar(BAR_ODONE + x), n_epi & 1)) { ok = false; break; }
         ++n_epi;
         tc::fence_after_sync();
+        // HALF: the row's sum is its two threads' halves added (both hold the same running max)
+        const float l_row = HALF ? l_run + __shfl_xor_sync(0xffffffffu, l_run, 16) : l_run;
         if (x == 1) {
-          xch[row] = m_run;
-          xch[128 + row] = l_run;
+          if (kh == 0) {
+            xch[qrow] = m_run;
+            xch[128 + qrow] = l_row;
+          }
           tc::mbar_arrive(bar(BAR_MERGE));
         } else {
           float mB = -INFINITY, lB = 0.f;
           if (it.nkt1 > 0) {
             if (!warp_wait(bar(BAR_MERGE), n_merge & 1)) { ok = false; break; }
             tc::fence_after_sync();
-            mB = xch[row];
-            lB = xch[128 + row];
+            mB = xch[qrow];
+            lB = xch[128 + qrow];
           }
           const float M = fmaxf(m_run, mB), Mb = M == -INFINITY ? 0.f : M;
           const float fA = ex2_approx(m_run - Mb), fB = ex2_approx(mB - Mb);
-          const float l = fA * l_run + fB * lB;
-          const bool store = row < nvx;
+          const float l = fA * l_row + fB * lB;
+          const bool store = qrow < nvx;
           const int64_t head = static_cast<int64_t>(it.hk) * p.group + hl;
           const bool whole = it.num_splits == 1;  // else a partial result for the combine
           const float osc = p.out_scale;
@@ -920,16 +1021,29 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           const int64_t pi = (static_cast<int64_t>(__ldg(p.part_prefix + it.gr)) +
                               static_cast<int64_t>(it.s_idx) * it.n_new + tok_i) * p.Hq + head;
           float* prow = p.part_o + pi * D;
+          // HALF: each of the row's two threads takes D / 2 of its output columns
+          constexpr int kChunks = HALF ? D / 64 : D / 32;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < kChunks; ++cc) {
             uint32_t va[32], vb[32];
-            tc::tmem_ld32(tO + cc * 32, va);
-            if (it.nkt1 > 0) {
-              tc::tmem_ld32(tO + 128 + cc * 32, vb);  // O_B, same lanes
+            if constexpr (HALF) {
+              tc::tmem_ld16x2_x32_async<D / 2>(tO + cc * 32, va);
+              tc::tmem_wait_ld_dep(va);
+            } else {
+              tc::tmem_ld32(tO + cc * 32, va);
+            }
+            if (it.nkt1 > 0) {  // O_B, same lanes
+              if constexpr (HALF) {
+                tc::tmem_ld16x2_x32_async<D / 2>(tO + 128 + cc * 32, vb);
+                tc::tmem_wait_ld_dep(vb);
+              } else {
+                tc::tmem_ld32(tO + 128 + cc * 32, vb);
+              }
             } else {
 #pragma unroll
               for (int e = 0; e < 32; ++e) vb[e] = 0u;
             }
+            const int c0 = kh * (D / 2) + cc * 32;  // output column of o[0]
             float o[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(va[e]) * sA + __uint_as_float(vb[e]) * sB;
@@ -939,16 +1053,16 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
               for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o[e], o[e + 1]);
 #pragma unroll
               for (int kq = 0; kq < 4; ++kq)
-                reinterpret_cast<uint4*>(orow + cc * 32)[kq] =
+                reinterpret_cast<uint4*>(orow + c0)[kq] =
                     make_uint4(pk[4 * kq], pk[4 * kq + 1], pk[4 * kq + 2], pk[4 * kq + 3]);
             } else if (store) {
 #pragma unroll
               for (int kq = 0; kq < 8; ++kq)
-                reinterpret_cast<float4*>(prow + cc * 32)[kq] =
+                reinterpret_cast<float4*>(prow + c0)[kq] =
                     make_float4(o[4 * kq], o[4 * kq + 1], o[4 * kq + 2], o[4 * kq + 3]);
             }
           }
-          if (store && !whole) {
+          if (store && !whole && kh == 0) {
             p.part_ml[pi * 2] = M;
             p.part_ml[pi * 2 + 1] = l;
           }
@@ -1586,7 +1700,7 @@ cudaError_t launch_stage_q8(const StageParams& p, cudaStream_t s) {
 
 template <int D, int KV>
 cudaError_t launch_gen_t(const ContextParams& p, const CUtensorMap& qm, const CUtensorMap& km, cudaStream_t s) {
-  auto kern = gen_attn_kernel<D, KV>;
+  auto kern = p.half_rows ? gen_attn_kernel<D, KV, true> : gen_attn_kernel<D, KV, false>;
   constexpr int bytes = GenSmem<D, KV>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;

@@ -222,6 +222,8 @@ struct ContextParams {
   int32_t G, kv_chunk, num_titems, mask_words;
   int32_t kv_dtype;         // generation kernel: pool element kind (pkv_dtype); 8-bit codes are
                             // converted to f16 in shared memory (head_dim 128 only)
+  int32_t half_rows;        // generation kernel: every item has at most 64 rows and 16 % group == 0
+                            // (two threads per Q row, the Q map's box 16 / group tokens)
   int64_t total_parts;
   const int2* titem_map;
   const int32_t* split_prefix;
