@@ -22,7 +22,11 @@
  *     PKV_NOALLOC_SCRATCH_BYTES that exists on every GPU loading the library, with its address
  *     cached per device.  No call synchronises a stream: each call only enqueues kernels and
  *     returns, and its effects are ordered on `stream` like one kernel's (same-stream FIFO
- *     ordering as in [NOTES] 五 "完整的推理流程", 5.2 CPU/GPU Overlap).
+ *     ordering as in [NOTES] 五 "完整的推理流程", 5.2 CPU/GPU Overlap).  The kernels are
+ *     launched with programmatic stream serialisation; the append kernel signals its dependents
+ *     early, so a caller's kernel launched right after it with that attribute may start before
+ *     the append ends and must run griddepcontrol.wait before it reads q_out or the pool (an
+ *     ordinary launch, an event or a stream wait still sees the call complete).
  *   - Return value: PKV_OK (0) or a negative PKV_ERR_* detected on the host before anything
  *     was enqueued.  Errors only the device can see (a page id outside [0, num_blocks), a
  *     bounded wait that ran out) are OR-ed as PKV_DEVERR_* bits into the caller's device int

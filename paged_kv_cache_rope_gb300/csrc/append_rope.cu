@@ -199,6 +199,10 @@ __global__ void __launch_bounds__(kMaxAppendThreads, 2) append_rope_kernel(Appen
   }
   __syncthreads();  // the barriers are initialised before anyone uses them
   pdl_wait();
+  // The attention call's plan kernel, launched next, reads only request lengths -- visible now
+  // (the wait above) and never written here -- so it may run beside this kernel; it waits for
+  // this kernel before it ends, so everything after it still sees the appended rows.
+  pdl_launch_dependents();
   // The first stages' q / k / v rows depend on nothing but the token index: the producer issues
   // them before the scan below, so their latency overlaps the scan and the first lookups (their
   // RoPE rows follow once the positions are known).  Rows past the batch's rows are still inside

@@ -21,6 +21,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // while the previous kernel on the stream drains; it must wait here before touching memory that
 // earlier work produces.  A no-op when launched without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next kernel on the stream (launched with programmatic serialisation) start before this
+// one ends; every such kernel here still runs griddepcontrol.wait before it reads what the
+// kernels before it wrote.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 __device__ __forceinline__ void flag_error(int32_t* d_error, uint32_t bits) {
   if (d_error) atomicOr(reinterpret_cast<unsigned int*>(d_error), bits);

@@ -155,7 +155,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   const bool staging = p.staging != 0, dyn = p.dyn != 0;
   const int C = p.C, chunk = p.kv_chunk, cols = p.cols_per_cta;
   bool bad = false;
-  pdl_wait();
+  // The plan reads only the request lengths (written before the append kernel that precedes it,
+  // which waited for them) and writes only its own words, so it runs beside that kernel's tail
+  // and waits for it just before it ends (griddepcontrol.wait on every exit below): the kernels
+  // after the plan start once it has ended, hence after the append too.
   const int4 z4 = make_int4(0, 0, 0, 0);
   if (tid == 0) {
     s_carry = Int8v{z4, z4};
@@ -269,7 +272,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     for (int i = 0; i < kCntWords; ++i) counts[i] = any_bad ? 0 : v[i];
     if (any_bad) flag_error(p.d_error, dyn ? PKV_DEVERR_BUCKET : PKV_DEVERR_PLAN_MISMATCH);
   }
-  if (any_bad) return;
+  if (any_bad) {
+    pdl_wait();
+    return;
+  }
   if (p.ctx_share) {  // the generation requests' keys, for the context CTA share below
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) gen_keys += __shfl_xor_sync(0xffffffffu, gen_keys, o);
@@ -307,7 +313,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   // a context CTA reads one int4 instead of searching the tile prefix itself.
   const int U = s_units;
   int4* order = reinterpret_cast<int4*>(p.ws + p.lay.unit_info);
-  if (U <= 0) return;
+  if (U <= 0) {
+    pdl_wait();
+    return;
+  }
   for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
   __syncthreads();  // tiles[] (this block's global writes) and the zeroed histogram are visible
   // the unit's request: the last slot whose unit prefix is <= u (an empty slot shares its
@@ -346,6 +355,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int4 d = unit_desc(u);
     order[atomicAdd(&s_hist[kBins - 1 - unit_cost(d)], 1)] = d;
   }
+  pdl_wait();
 }
 
 // --------------------------------------------------------------------------------------------
