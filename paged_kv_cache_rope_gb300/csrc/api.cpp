@@ -242,7 +242,8 @@ void plan_layout(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPlan*
   L.witem_map = L.item_map + 2LL * hp->num_items;
   L.titem_map = L.witem_map + 2LL * hp->num_witems;
   L.titem_order = L.titem_map + 2LL * hp->num_titems;
-  L.row_map = (L.titem_order + 2LL * hp->num_titems + 3) & ~3LL;  // int4 entries: 16-byte aligned
+  L.item_order = L.titem_order + 2LL * hp->num_titems;
+  L.row_map = (L.item_order + 2LL * hp->num_items + 3) & ~3LL;  // int4 entries: 16-byte aligned
   L.unit_info = L.row_map + 4LL * hp->gen_rows;                 // int4 entries: 16-byte aligned
   L.stage_prefix = L.unit_info + 4LL * hp->num_tiles;
   L.stage_tbl = L.stage_prefix + (hp->staging ? hp->C + 1 : 0);
@@ -556,6 +557,7 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
   pp.ctx_share = (concurrent && hp.dyn && pool->dtype == PKV_BF16) ? 1 : 0;
   pp.num_sms = device_sm_count();
   pp.D = D;
+  pp.sort_items = pool->dtype != PKV_BF16 ? 1 : 0;
   pp.cap_stage_pages = static_cast<int32_t>(hp.lay.stage_pages);
   pp.cap_tiles = hp.num_tiles;
   pp.cap_splits = hp.num_splits;
@@ -695,7 +697,8 @@ int forward_impl(const pkv_pool* pool, const pkv_batch* batch, const HostPlan& h
     dp.tbl = batch->d_block_offsets;
     dp.cu_q = ws + hp.lay.cu_q;
     dp.split_prefix = ws + hp.lay.split_prefix;
-    dp.item_map = reinterpret_cast<const int2*>(ws + hp.lay.item_map);
+    // 8-bit pools: most KV tiles first (sorted by the plan); bf16: request order
+    dp.item_map = reinterpret_cast<const int2*>(ws + (q8 ? hp.lay.item_order : hp.lay.item_map));
     dp.witem_map = reinterpret_cast<const int2*>(ws + hp.lay.witem_map);
     dp.row_map = reinterpret_cast<const int4*>(ws + hp.lay.row_map);
     dp.part_prefix = ws + hp.lay.part_prefix;

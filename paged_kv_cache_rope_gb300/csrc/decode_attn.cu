@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ Int8v s_warp[kPlanThreads / 32];
   __shared__ Int8v s_carry;
   __shared__ int32_t s_ctx_rows;
-  __shared__ int32_t s_units, s_titems;
+  __shared__ int32_t s_units, s_titems, s_items;
   __shared__ int32_t s_hist[kPlanBins];
   __shared__ int32_t s_part[kPlanThreads];
   __shared__ unsigned long long s_gen_keys, s_tile_pairs;  // for the context CTA share
@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
     s_units = t.a.y;
     s_titems = t.b.w;
+    s_items = t.b.x;
   }
   const bool any_bad = __syncthreads_or(bad || bad_tot) != 0;
   if (tid == 0) {
@@ -304,6 +305,32 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     for (int t = tid; t < NT; t += kPlanThreads) {
       const int2 im = titem_map[t];
       torder[atomicAdd(&s_hist[kBins - 1 - titem_cost(im)], 1)] = im;
+    }
+    __syncthreads();  // the histogram is free again
+  }
+
+  // ---- 8-bit pools: narrow decode CTAs, most KV tiles first -- the same counting sort by the
+  // tile count of the CTA's split; the decode grid launches them in this order (KV head fastest),
+  // so that its last wave is made of short ones.  (Measured: 4 % faster on 8-bit pools, whose
+  // splits hold twice the keys of a bf16 split and make fewer waves; on bf16 pools request order
+  // was faster, as the long splits first left a last phase of short, overhead-bound CTAs.) ----
+  const int NI = p.sort_items ? s_items : 0;
+  if (NI > 0) {
+    int2* iorder = reinterpret_cast<int2*>(p.ws + p.lay.item_order);
+    auto item_cost = [&](const int2 im) {
+      const int r = C + im.x, n = __ldg(p.ctx_len + r);
+      const int L = __ldg(p.past + r) + n, n_cg = max((n * p.group + cols - 1) / cols, 1);
+      const int kt0 = (im.y / n_cg) * chunk, keys = max(min(L, kt0 + chunk) - kt0, 0);
+      return min(kBins - 1, (keys + kDecodeTile - 1) / kDecodeTile);
+    };
+    for (int b = tid; b < kBins; b += kPlanThreads) s_hist[b] = 0;
+    __syncthreads();  // item_map (this block's global writes) and the zeroed histogram are visible
+    for (int t = tid; t < NI; t += kPlanThreads) atomicAdd(&s_hist[kBins - 1 - item_cost(item_map[t])], 1);
+    __syncthreads();
+    plan_hist_scan(s_hist, s_part, tid, lane, wid);
+    for (int t = tid; t < NI; t += kPlanThreads) {
+      const int2 im = item_map[t];
+      iorder[atomicAdd(&s_hist[kBins - 1 - item_cost(im)], 1)] = im;
     }
     __syncthreads();  // the histogram is free again
   }
@@ -439,7 +466,10 @@ decode_splitkv_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g8 = lane >> 2, q4 = lane & 3;  // fragment row group / column pair
-  const int item = blockIdx.x, h = blockIdx.y;
+  // narrow: one flat grid over (item in the plan's longest-first order, KV head), head fastest;
+  // wide: (item, KV head)
+  const int item = WIDE ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) / p.Hkv;
+  const int h = WIDE ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x) % p.Hkv;
 
   // ---- which generation request, split and column group this CTA owns ----
   // Columns of the score tile are (token i, query head h*group + hl) pairs of this KV head,
@@ -1070,7 +1100,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int items = WIDE ? p.total_witems : p.total_items;
-  return launch_pdl(kern, dim3(items, p.Hkv), dim3(Cfg::kThreads), kSmem, s, p);
+  const dim3 grid = WIDE ? dim3(items, p.Hkv) : dim3(static_cast<unsigned>(items) * p.Hkv, 1);
+  return launch_pdl(kern, grid, dim3(Cfg::kThreads), kSmem, s, p);
 }
 
 }  // namespace

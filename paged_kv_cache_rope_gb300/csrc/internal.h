@@ -54,6 +54,7 @@ struct PlanLayout {
   int64_t witem_map;     // [num_witems] the same for the wide decode kernel's CTAs
   int64_t titem_map;     // [num_titems] the same for the tensor-core kernel's generation CTAs
   int64_t titem_order;   // [num_titems] int2: titem_map's entries, most KV tiles first
+  int64_t item_order;    // [num_items] int2: item_map's entries, most KV tiles first (8-bit pools)
   int64_t row_map;       // [generation rows] int4 (splits, partial row of split 0, rows between
                          // splits = the request's new tokens, token index), 16-byte aligned
   int64_t unit_info;     // [num context units] int4 (request, first q row, past + first row,
@@ -162,6 +163,9 @@ struct PlanParams {
   // 1: the plan picks the context CTAs beside the generation kernels (context_cta_share) from
   // the device lengths (bucket plans on a bf16 pool); 0: every launched context CTA takes work
   int32_t ctx_share, num_sms, D;
+  // 1 (8-bit pools): the narrow decode CTAs are launched in the order item_order lists them
+  // (most KV tiles first); 0: in request order (item_map)
+  int32_t sort_items;
   const int32_t* ctx_len;
   const int32_t* past;
   int32_t* ws;  // plan words
