@@ -181,19 +181,27 @@ int validate_batch(const pkv_pool* pool, const pkv_batch* b, int32_t Hq, HostPla
   return PKV_OK;
 }
 
+// Largest K+V byte count one decode CTA streams.  Measured on the 7B-like, 70B-like GQA and
+// mixed batches with the flat (item, KV head) grid: bf16 pools are fastest at 1 MB (2048 keys
+// of a 128-dim head; 512 KB and 2 MB were 1-5 % slower), 8-bit pools at 2 MB (8192 keys), whose
+// per-CTA set-up (Q split into hi / lo codes, the warps' merge) is dearer per key.
 #ifndef PKV_DECODE_SPLIT_KB
-#define PKV_DECODE_SPLIT_KB 512  // largest K+V byte count one decode CTA streams (measured best)
+#define PKV_DECODE_SPLIT_KB 1024
+#endif
+#ifndef PKV_DECODE_SPLIT_KB_8BIT
+#define PKV_DECODE_SPLIT_KB_8BIT 2048
 #endif
 
 // Decode split length (tokens, multiple of 16): about 4 CTAs per SM over the whole batch, each
-// CTA streaming at most PKV_DECODE_SPLIT_KB of K+V (1024 tokens of a bf16 head of 128 dims,
-// 2048 of an FP8 one), so per-CTA set-up is amortised over the same bytes for either dtype.
+// CTA streaming at most the pool kind's byte cap above.
 int choose_kv_chunk(const pkv_pool* pool, int64_t total) {
   const int64_t target = static_cast<int64_t>(device_sm_count()) * 4;
   int64_t chunk = (total * pool->num_kv_heads + target - 1) / std::max<int64_t>(target, 1);
   chunk = (chunk + 15) / 16 * 16;
-  const int64_t token_bytes = 2LL * pool->head_dim * (pool->dtype != PKV_BF16 ? 1 : 2);
-  const int64_t cap = std::max<int64_t>(64, (PKV_DECODE_SPLIT_KB * 1024LL / token_bytes) / 16 * 16);
+  const bool q8 = pool->dtype != PKV_BF16;
+  const int64_t token_bytes = 2LL * pool->head_dim * (q8 ? 1 : 2);
+  const int64_t cap_kb = q8 ? PKV_DECODE_SPLIT_KB_8BIT : PKV_DECODE_SPLIT_KB;
+  const int64_t cap = std::max<int64_t>(64, (cap_kb * 1024LL / token_bytes) / 16 * 16);
   return static_cast<int>(std::min<int64_t>(cap, std::max<int64_t>(64, chunk)));
 }
 

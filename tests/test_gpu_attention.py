@@ -31,6 +31,9 @@ DECODE = [
     ("gqa16_d128_b128", [5, 129, 1000], 32, 2, 128, 128),
     ("gqa2_d64_b64", [70, 2000], 4, 2, 64, 64),
     ("gqa3_d128_b16", [40, 600], 6, 2, 128, 16),
+    # one long request of a small batch: 64-key splits, 130 of them (the widest combine, 16
+    # warps over the splits)
+    ("gqa2_d128_130_splits", [8300, 40], 4, 2, 128, 64),
 ]
 
 
