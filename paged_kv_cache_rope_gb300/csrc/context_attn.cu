@@ -1093,6 +1093,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 //     issued the current item's last K / V tile, publishes it through a two-entry ring in
 //     shared memory, and loads the next Q tile into a slot as soon as the slot's last S MMA is
 //     done and the next K / V tiles as soon as stages free up;
+//   - the producer publishes each item with its unit descriptor (read while the previous
+//     item's tiles were still in flight), so no consumer waits on a global load between items;
 //   - the MMA warp goes from the last PV of one item straight to the first S of the next;
 //   - output tiles leave through their own staging tile (one, handed from epilogue to epilogue
 //     in order), so a Q slot never waits for an output store.
@@ -1109,7 +1111,7 @@ struct CtxSmem {
   static constexpr int kVOff = kKOff + kStages * kTile;    // V ring
   static constexpr int kOOff = kVOff + kStages * kTile;    // output staging tile
   static constexpr int kBarOff = kOOff + kTile;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
 };
@@ -1150,8 +1152,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L::kBarOff + 8 * PB_NUM);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * PB_NUM + 4);
-  volatile int* s_item = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * PB_NUM + 8);  // [2]
-  static_assert(8 * PB_NUM + 16 <= L::kBarBytes, "barrier area");
+  // item ring: [2][8] ints, entry = item index (-1: no more work) and the unit's descriptor
+  volatile int* s_item = reinterpret_cast<volatile int*>(base + L::kBarOff + 8 * PB_NUM + 16);
+  static_assert(8 * PB_NUM + 16 + 2 * 8 * 4 <= L::kBarBytes, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -1202,12 +1205,11 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     int hq, hk, r, q_row, past, L_r, nv0, nv1, nkt0, nkt1, nT;
     bool ok, hasB, fullA, fullB;
   };
-  auto item_of = [&](int w) {
+  auto item_of = [&](int w, const int4 u) {
     Item it;
     const int y = w / p.Hq;
     it.hq = w - y * p.Hq;
     it.hk = it.hq / p.group;
-    const int4 u = __ldg(p.unit_info + y);
     it.r = u.x;
     it.q_row = u.y;
     it.past = u.z;
@@ -1239,10 +1241,12 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
   };
   auto warp_abort = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0) != 0; };
   // consumers: item k of this CTA from the ring (-1: no more work), entry handed back
-  auto take_item = [&](int k, int& w) {
+  auto take_item = [&](int k, int& w, int4& u) {
     const int slot = k & 1;
     if (!warp_wait(bar(PB_ITEM + slot), (k >> 1) & 1)) return false;
-    w = *(s_item + slot);
+    const volatile int* e = s_item + 8 * slot;
+    w = e[0];
+    u = make_int4(e[1], e[2], e[3], e[4]);
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(bar(PB_ITEMFREE + slot));
     return true;
@@ -1253,6 +1257,9 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     if (warp == kProducerWarp) {
       // ======================= item queue + TMA producer =======================
       int w = static_cast<int>(blockIdx.x) < active ? static_cast<int>(blockIdx.x) : n_items;
+      // the first unit's descriptor, loaded beside the item count (in bounds: the grid has at
+      // most num_tiles x Hq CTAs and unit_info num_tiles entries; unused past the item count)
+      int4 u = __ldg(p.unit_info + static_cast<int>(blockIdx.x) / p.Hq);
       int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items)
       int nq0 = 0, nq1 = 0;            // Q loads per slot
       bool pok = true;
@@ -1261,12 +1268,17 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         if (k >= 2 && !warp_wait(bar(PB_ITEMFREE + slot), ((k - 2) >> 1) & 1)) { pok = false; break; }
         const bool more = w < n_items;
         if (lane == 0) {
-          *(s_item + slot) = more ? w : -1;
+          volatile int* e = s_item + 8 * slot;
+          e[0] = more ? w : -1;
+          e[1] = u.x;
+          e[2] = u.y;
+          e[3] = u.z;
+          e[4] = u.w;
           tc::mbar_arrive(bar(PB_ITEM + slot));
         }
         __syncwarp();
         if (!more) break;
-        const Item it = item_of(w);
+        const Item it = item_of(w, u);
         if (!it.ok) {
           if (lane == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
         } else {
@@ -1338,6 +1350,7 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
         int nxt = 0;
         if (lane == 0) nxt = atomicAdd(p.cursor, 1) + active;
         w = __shfl_sync(0xffffffffu, nxt, 0);
+        if (w < n_items) u = __ldg(p.unit_info + w / p.Hq);  // before the ring slot frees up
       }
       if (!pok && lane == 0) fail();
       __syncwarp();
@@ -1364,9 +1377,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
       bool ok = true;
       for (int k = 0; ok; ++k) {
         int w = -1;
-        if (!take_item(k, w)) { ok = false; break; }
+        int4 u;
+        if (!take_item(k, w, u)) { ok = false; break; }
         if (w < 0) break;
-        const Item it = item_of(w);
+        const Item it = item_of(w, u);
         if (!it.ok) continue;
         auto uses = [&](int j, int x) { return j < (x ? it.nkt1 : it.nkt0); };
         auto frees = [&](int j, int x) { return x == ((it.hasB && j < it.nkt1) ? 1 : 0); };
@@ -1458,9 +1472,10 @@ context_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q
     bool ok = true;
     for (int k = 0; ok; ++k) {
       int w = -1;
-      if (!take_item(k, w)) { ok = false; break; }
+      int4 u;
+      if (!take_item(k, w, u)) { ok = false; break; }
       if (w < 0) break;
-      const Item it = item_of(w);
+      const Item it = item_of(w, u);
       if (!it.ok) continue;
       const int nvx = x ? it.nv1 : it.nv0, nk = x ? it.nkt1 : it.nkt0;
       const int stg_idx = n_stg + (x ? (it.fullA ? 1 : 0) : 0);  // A's store goes first
