@@ -102,6 +102,17 @@ __device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi2, 
   lo2 = f32x2_to_e4m3x2(x0 - hv.x, x1 - hv.y);
 }
 
+// The same split for 0 <= x <= 448 without a round trip through E4M3: hi is x cut to three
+// mantissa bits (an E4M3 value from 2^-6 up, converted exactly) and lo = e4m3(x - hi); together
+// about seven significant bits (below 2^-6 hi rounds to E4M3's 2^-9 steps, an absolute error
+// under 2^-10).
+__device__ __forceinline__ void split_cut_e4m3x2(float x0, float x1, uint32_t& hi2, uint32_t& lo2) {
+  const float h0 = __uint_as_float(__float_as_uint(x0) & 0xFFF00000u);
+  const float h1 = __uint_as_float(__float_as_uint(x1) & 0xFFF00000u);
+  hi2 = f32x2_to_e4m3x2(h0, h1);
+  lo2 = f32x2_to_e4m3x2(x0 - h0, x1 - h1);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

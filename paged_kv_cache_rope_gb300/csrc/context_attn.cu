@@ -85,26 +85,30 @@ constexpr uint32_t kRegsSoftmax = 216;
 constexpr uint32_t kRegsControl = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O once P could exceed 2^8
+// E4M3 P (generation kernel, E4M3 pool): P is emitted as 2^4 * exp2(s - m) with m at most 4 below
+// the row's true running maximum, so a code never exceeds 2^8 (E4M3 tops out at 448) and values
+// down to 2^-10 of the maximum keep E4M3's normal range; O and l carry the same 2^4.
+constexpr float kRescaleThresholdE4M3 = 4.0f;
+constexpr float kPScaleLog2E4M3 = 4.0f;
 
 // Generation kernel: one Q tile (A and B share it), K[3], V[3] -- each K / V tile has one
 // consumer and the two halves alternate.
 // With an INT8 pool: Q, K[2], V[2] (f16), a ring of the raw codes (K[2], V[2]) that TMA fills
-// and the softmax warpgroups convert, and the per-row Q scales.  With an E4M3 pool the scores
-// read the raw K codes and Q's hi and lo E4M3 tiles, which replace the bf16 Q tile in place (a
-// row's two 128-code halves take the 256 bytes of its bf16 codes), so there is no f16 K ring:
-// Q, V[3] (f16), raw K[3], raw V[3] -- a V tile is converted into a stage whose previous PV was
-// the other warpgroup's, issued half a cycle earlier, not the converting warpgroup's own PV that
-// has just been issued.  Then B's (m, l) per row for A's merge (its own area: the K ring
-// already holds the next item's tiles when an item ends).
+// and the softmax warpgroups convert, and the per-row Q scales.  With an E4M3 pool nothing is
+// converted: the scores read the raw K codes and Q's hi and lo E4M3 tiles, which replace the
+// bf16 Q tile in place (a row's two 128-code halves take the 256 bytes of its bf16 codes), and
+// PV reads the raw V codes against P's hi and lo E4M3 codes in TMEM: Q, raw K[5], raw V[5].
+// Then B's (m, l) per row for A's merge (its own area: the K ring already holds the next item's
+// tiles when an item ends).
 template <int D, int KV = 0>
 struct GenSmem {
   static constexpr bool kQ8 = KV != 0;
   static constexpr bool kF8S = KV == PKV_FP8_E4M3;
   static constexpr int kHalf = 128 * 128;         // one 64-wide half of a 128-row tile (bytes)
   static constexpr int kTile = (D / 64) * kHalf;  // one Q tile or one K / V stage
-  static constexpr int kStages = (kQ8 && !kF8S) ? 2 : 3;  // V stages (and K stages, but E4M3 has none)
-  static constexpr int kKStages = kF8S ? 0 : kStages;
-  static constexpr int kRawStages = kF8S ? 3 : 2;
+  static constexpr int kStages = kF8S ? 0 : (kQ8 ? 2 : 3);  // f16 / bf16 V stages (and K stages)
+  static constexpr int kKStages = kStages;
+  static constexpr int kRawStages = kF8S ? 5 : 2;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kTile;
   static constexpr int kVOff = kKOff + kKStages * kTile;
@@ -112,7 +116,7 @@ struct GenSmem {
   static constexpr int kRawKOff = kVOff + kStages * kTile;
   static constexpr int kRawVOff = kRawKOff + (kQ8 ? kRawStages : 0) * kRawTile;
   static constexpr int kBarOff = kRawVOff + (kQ8 ? kRawStages : 0) * kRawTile;
-  static constexpr int kBarBytes = 384;
+  static constexpr int kBarBytes = 512;
   static constexpr int kQScaleOff = kBarOff + kBarBytes;  // [128] floats: 1 / (Q row's power-of-two scale)
   static constexpr int kXchOff = kQScaleOff + (kQ8 ? 128 * 4 : 0);  // [2][128] floats: B's m, l
   static constexpr int kBytes = kXchOff + 2 * 128 * 4 + 1024;  // + alignment slack
@@ -131,18 +135,19 @@ enum {
   BAR_ODONE = 17,  // +2
   BAR_MMADONE = 19,
   BAR_MERGE = 20,  // generation: tile B's softmax state is in shared memory
-  BAR_RAWK = 21,   // +3: 8-bit pool, raw K codes landed (TMA)
-  BAR_RAWV = 24,   // +3: raw V codes landed
-  BAR_RAWKEMPTY = 27, // +3: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
-  BAR_RAWVEMPTY = 30, // +3: a raw V stage has been converted
-  BAR_QRAW = 33,   // the bf16 Q tile landed (warpgroup B rescales and re-encodes it)
-  BAR_QFREE = 34,  // an item's last S MMA is done: its Q tile (and re-encoding) may be replaced
-  BAR_ITEM = 35,   // +2: item ring entry written
-  BAR_ITEMFREE = 37,  // +2: item ring entry read by the MMA warp and the eight softmax warps
-  BAR_IDONE = 39,  // an item is finished by the MMA warp (issued) and the eight softmax warps
-  BAR_QSREAD = 40, // 8-bit pool: warpgroup A has read the item's Q row scales
-  NUM_BARS = 41
+  BAR_RAWK = 21,   // +6: 8-bit pool, raw K codes landed (TMA)
+  BAR_RAWV = 27,   // +6: raw V codes landed
+  BAR_RAWKEMPTY = 33, // +6: a raw K stage may be refilled (E4M3: its S is done; INT8: converted)
+  BAR_RAWVEMPTY = 39, // +6: a raw V stage may be refilled (E4M3: its PV is done; INT8: converted)
+  BAR_QRAW = 45,   // the bf16 Q tile landed (warpgroup B rescales and re-encodes it)
+  BAR_QFREE = 46,  // an item's last S MMA is done: its Q tile (and re-encoding) may be replaced
+  BAR_ITEM = 47,   // +2: item ring entry written
+  BAR_ITEMFREE = 49,  // +2: item ring entry read by the MMA warp and the eight softmax warps
+  BAR_IDONE = 51,  // an item is finished by the MMA warp (issued) and the eight softmax warps
+  BAR_QSREAD = 52, // 8-bit pool: warpgroup A has read the item's Q row scales
+  NUM_BARS = 53
 };
+constexpr int kMaxRawStages = 6;
 
 
 template <int D, int KV, bool HALF>
@@ -153,11 +158,12 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
   // 8-bit pool: the producer lands raw codes and the softmax warpgroups
   // convert what the MMAs cannot read as stored (Q, V, and INT8 K)
   constexpr bool Q8 = L::kQ8;
-  // E4M3 pools: scores on kind::f8f6f4 straight from the raw K codes, with Q split into hi + lo
-  // E4M3 codes (about 8 significant bits together); only V is converted to f16
+  // E4M3 pools: scores and PV on kind::f8f6f4 straight from the raw K and V codes, with Q and P
+  // split into hi + lo E4M3 codes (7-8 significant bits together); nothing is converted
   constexpr bool F8S = KV == PKV_FP8_E4M3;
-  constexpr int S = L::kStages;
+  constexpr int S = L::kStages > 0 ? L::kStages : 1;  // (E4M3: no f16 ring; one nominal stage)
   constexpr int R = L::kRawStages;
+  static_assert(R <= kMaxRawStages, "raw ring barriers");
   // ring stage and phase of the g-th K / V tile of the stream (f16 / bf16 rings, raw rings)
   auto stg = [](int g) { return g % S; };
   auto phs = [](int g) { return (g / S) & 1; };
@@ -194,7 +200,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         tc::mbar_init(bar(BAR_RAWK + s), 1);
         tc::mbar_init(bar(BAR_RAWV + s), 1);
         tc::mbar_init(bar(BAR_RAWKEMPTY + s), F8S ? 1 : 4);
-        tc::mbar_init(bar(BAR_RAWVEMPTY + s), 4);
+        tc::mbar_init(bar(BAR_RAWVEMPTY + s), F8S ? 1 : 4);  // E4M3: its PV is done
       }
       tc::mbar_init(bar(BAR_QRAW), 1);
     }
@@ -345,13 +351,33 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           const int box_rows = p.B < kCtxTileN ? p.B : kCtxTileN;
           const int pages_per_tile = kCtxTileN / box_rows;  // <= 8 (B >= 16)
           const int n_pages_seq = (it.L_r + p.B - 1) / p.B;
-          // lane pp < pages_per_tile holds page pp of tile j (B <= 128: whole pages per tile); the
-          // table entry is read a tile ahead of its copies, so its load overlaps the waits before them
+          // lane pp < pages_per_tile holds page pp of tile j (B <= 128: whole pages per tile)
           auto has_page = [&](int j) {
             const int lb = (it.kt0 + j * kCtxTileN) / p.B + lane;
             return lane < pages_per_tile && lb < n_pages_seq && lb < p.max_blocks;
           };
-          auto lookup = [&](int j) { return has_page(j) ? __ldg(tbl + (it.kt0 + j * kCtxTileN) / p.B + lane) : -1; };
+          // The split's table entries, 32 at a time: lane l holds entry 32 w + l of window w (the
+          // split starts on a page boundary: kt0 is a multiple of 128), and the next window's load
+          // is in flight while the current one serves its tiles, so a tile's copies never wait for
+          // a table read (one read per tile, a tile ahead, paced the copies at the read latency
+          // under the batch's own traffic)
+          const int page0 = it.kt0 / p.B;
+          auto load_win = [&](int wn) {
+            const int lb = page0 + 32 * wn + lane;
+            return (lb < n_pages_seq && lb < p.max_blocks) ? __ldg(tbl + lb) : -1;
+          };
+          int win = 0;
+          int pg_win = load_win(0), pg_win_next = load_win(1);
+          auto lookup = [&](int j) {
+            const int pi = (j * kCtxTileN) / p.B;  // the tile's first page within the split
+            if ((pi >> 5) != win) {                 // tiles go in order: the next window
+              win = pi >> 5;
+              pg_win = pg_win_next;
+              pg_win_next = load_win(win + 1);
+            }
+            const int pg = __shfl_sync(0xffffffffu, pg_win, (pi & 31) + (lane < pages_per_tile ? lane : 0));
+            return has_page(j) ? pg : -1;
+          };
           // tile j of the item (table entries pg) into the next stage of the CTA's stream
           auto issue_tile = [&](int j, int pg) {
             if (warp_abort()) return false;
@@ -411,7 +437,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             return true;
           };
           // the item's Q tile goes out as soon as the previous item's last S MMA is done, then its
-          // tiles as stages free up; the first tile's table entries load meanwhile
+          // tiles as stages free up; the first table window loads meanwhile
 #ifdef PKV_SELFTEST
           // Self-test build only (compiled by the tests, never into libpaged_kv.so): no K / V
           // copy is issued, so the MMA warp's wait for the first K tile and the softmax warps'
@@ -421,7 +447,6 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 #else
           const int n_issue = nT;
 #endif
-          int pg_next = n_issue > 0 ? lookup(0) : -1;
           if (pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
           if (!pok) break;
           // one Q tile (128 / g tokens x the group's g heads), shared by A and B; HALF: 64 rows,
@@ -441,11 +466,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           }
           __syncwarp();
           ++nq;
-          for (int j = 0; pok && j < n_issue; ++j) {
-            const int pg = pg_next;
-            if (j + 1 < n_issue) pg_next = lookup(j + 1);
-            pok = issue_tile(j, pg);
-          }
+          for (int j = 0; pok && j < n_issue; ++j) pok = issue_tile(j, lookup(j));
         }
         if (!pok) break;
         // claim the next item while this one's tiles are still being consumed
@@ -482,6 +503,9 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       // per-stage K / V descriptors: stages are L::kTile apart, i.e. kTile / 16 descriptor units
       const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
       const uint64_t dv0 = tc::sdesc_sw128(sV(0), L::kHalf, 1024);
+      // E4M3: raw V stages, MN-major (a 128-code row per key, one 128-byte swizzle atom wide;
+      // 8-row groups 1 KB apart)
+      const uint64_t dv8 = tc::sdesc_sw128(base_s + L::kRawVOff, L::kRawTile, 1024);
       auto stage_off = [](int st) { return static_cast<uint64_t>(st) * (L::kTile / 16); };
       int G = 0;             // K / V stream tiles of earlier items
       int sc0 = 0, sc1 = 0;  // S / P tiles of earlier items, per half
@@ -570,16 +594,32 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             if (!uses(j, x)) continue;
             const int g = gtile(j, x);
             if (!warp_wait(bar(BAR_PFULL + x), ((x ? sc1 : sc0) + j) & 1)) { ok = false; break; }
-            if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
-            tc::fence_after_sync();
-            const uint64_t v0 = dv0 + stage_off(stg(g));
-            if (tc::elect_one()) {
-              static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
-              tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
-              tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
-              if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
+            if constexpr (F8S) {
+              if (!warp_wait(bar(BAR_RAWV + rstg(g)), rphs(g))) { ok = false; break; }
+              tc::fence_after_sync();
+              const uint64_t bv = dv8 + static_cast<uint64_t>(rstg(g)) * (L::kRawTile / 16);
+              if (tc::elect_one()) {
+                // P's hi codes (the tile's TMEM columns 0-31), then its lo codes (32-63), against
+                // the raw V codes read MN-major: four K=32 steps of 32 rows (4 KB) each
+                static_assert(kCtxTileN == 128, "four K=32 steps per KV tile");
+                tc::mma_e4m3_ts_x4<32 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, bv, idesc_o, j > 0 ? 1u : 0u);
+                tc::mma_e4m3_ts_x4<32 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x + 32, bv, idesc_o, 1u);
+                tc::mma_commit(bar(BAR_RAWVEMPTY + rstg(g)));  // the raw V stage may be refilled
+                if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
+              }
+              __syncwarp();
+            } else {
+              if (!warp_wait(bar(BAR_VFULL + stg(g)), phs(g))) { ok = false; break; }
+              tc::fence_after_sync();
+              const uint64_t v0 = dv0 + stage_off(stg(g));
+              if (tc::elect_one()) {
+                static_assert(kCtxTileN == 128, "eight K=16 steps per KV tile");
+                tc::mma_bf16_ts_x8<16 * 128 / 16>(tmem + 256 + 128 * x, tmem + 128 * x, v0, idesc_o, j > 0 ? 1u : 0u);
+                tc::mma_commit(bar(BAR_VEMPTY + stg(g)));
+                if (j == (x ? nkt1 : nkt0) - 1) tc::mma_commit(bar(BAR_ODONE + x));
+              }
+              __syncwarp();
             }
-            __syncwarp();
             if (uses(j + 1, x)) {
               if (!kfull(j + 1, x)) { ok = false; break; }
               tc::fence_after_sync();
@@ -616,6 +656,25 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     const uint32_t tS = tmem + 128 * x + lane_off;
     const uint32_t tO = tmem + 256 + 128 * x + lane_off;
     float* xch = reinterpret_cast<float*>(base + L::kXchOff);  // [2][128]: B's m, l per row
+    // E4M3 P: 32 scores (v) -> P' = exp2(s * sl2 - m + kPOff), summed into ls, as 8 words of hi
+    // codes and 8 of lo codes (four keys per word, key 4i + b in byte b) at hw / lw[w0 ..]
+    auto emit_e4m3 = [&](uint32_t(&v)[32], float2& ls, uint32_t(&hw)[16], uint32_t(&lw)[16], int w0, float2 sl2x2,
+                         float2 negm) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float2 xa = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm);
+        const float2 xb = ffma2(make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl2x2, negm);
+        const float2 pa = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+        const float2 pb = make_float2(ex2_approx(xb.x), ex2_approx(xb.y));
+        ls = fadd2(ls, pa);
+        ls = fadd2(ls, pb);
+        uint32_t h01, l01, h23, l23;
+        split_cut_e4m3x2(pa.x, pa.y, h01, l01);
+        split_cut_e4m3x2(pb.x, pb.y, h23, l23);
+        hw[w0 + (e >> 2)] = __byte_perm(h01, h23, 0x5410);
+        lw[w0 + (e >> 2)] = __byte_perm(l01, l23, 0x5410);
+      }
+    };
     // ---- 8-bit pool: this warpgroup turns the raw codes of its own tiles into f16 ----
     // Thread `row` converts tile row `row`: 128 codes in the 128-byte swizzle TMA wrote (16-byte
     // chunk j at j ^ (row % 8)) become 16 f16 chunks of the K-major 128-byte-swizzled layout the
@@ -777,7 +836,9 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
           }
         }
-        if (ok && nk > 0) ok = convert_tile(gtile(0), it.kend - (it.kt0 + x * kCtxTileN));  // its first tile
+        if constexpr (!F8S) {
+          if (ok && nk > 0) ok = convert_tile(gtile(0), it.kend - (it.kt0 + x * kCtxTileN));  // its first tile
+        }
         if (!ok) break;
       }
       if (!wait_prev(ndone)) { ok = false; break; }
@@ -790,6 +851,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         if (x == 0 && lane == 0) tc::mbar_arrive(bar(BAR_QSREAD));
       }
       const int kt0 = it.kt0, kend = it.kend, past = it.past;
+      constexpr float kThr = F8S ? kRescaleThresholdE4M3 : kRescaleThreshold;
+      constexpr float kPOff = F8S ? kPScaleLog2E4M3 : 0.f;  // P is emitted as 2^kPOff * exp2(s - m)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; ok && j < nk; ++j) {
         if (!warp_wait(bar(BAR_SFULL + x), (sc + j) & 1)) { ok = false; break; }
@@ -834,7 +897,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           float m_use = m_run;
           if (j == 0) {
             m_use = m_new;  // O is still empty
-          } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
+          } else if (__any_sync(0xffffffffu, m_new > m_run + kThr)) {
             // each thread rescales its half of the row's O columns
             const float f = ex2_approx(m_run - m_new);
 #pragma unroll
@@ -851,9 +914,17 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           }
           m_run = m_use;
           // P pairs of keys 64 kh + [0, 64) into S columns 32 kh + [0, 32) of the shared lane
+          // (E4M3: hi codes of the keys into columns 16 kh + [0, 16), lo codes 32 further on)
           float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
           const float m_base = m_use == -INFINITY ? 0.f : m_use;
-          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
+          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(kPOff - m_base, kPOff - m_base);
+          if constexpr (F8S) {
+            uint32_t hw[16], lw[16];
+            emit_e4m3(v0, ls[0], hw, lw, 0, sl2x2, negm);
+            emit_e4m3(v1, ls[1], hw, lw, 8, sl2x2, negm);
+            tc::tmem_st16x2_x16<16>(tS + 0, hw);
+            tc::tmem_st16x2_x16<16>(tS + 32, lw);
+          }
           auto emit = [&](uint32_t(&v)[32], int c) {
             uint32_t pk[16];
 #pragma unroll
@@ -865,8 +936,10 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             }
             tc::tmem_st16x2_x16<32>(tS + 16 * c, pk);
           };
-          emit(v0, 0);
-          emit(v1, 1);
+          if constexpr (!F8S) {
+            emit(v0, 0);
+            emit(v1, 1);
+          }
           const float2 lsum = fadd2(ls[0], ls[1]);
           l_run += lsum.x + lsum.y;  // this thread's half; the pair's halves are added at the end
           tc::tmem_wait_st();
@@ -924,7 +997,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           float m_use = m_run;
           if (j == 0) {
             m_use = m_new;  // O is still empty
-          } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
+          } else if (__any_sync(0xffffffffu, m_new > m_run + kThr)) {
             // PV_x(j-1) completed before S_x(j) was signalled; rescale O (whole warp, per-row factor)
             const float f = ex2_approx(m_run - m_new);
 #pragma unroll
@@ -942,7 +1015,18 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           // P = exp2(s * scale_log2 - m) as bf16 pairs into S columns 0..63 (keys 2c, 2c+1 in column c)
           float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
           const float m_base = m_use == -INFINITY ? 0.f : m_use;  // no visible key yet (generation splits)
-          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_base, -m_base);
+          const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(kPOff - m_base, kPOff - m_base);
+          if constexpr (F8S) {  // E4M3: hi codes of keys 4c .. 4c+3 in column c, lo codes in 32 + c
+            uint32_t hw[16], lw[16];
+            emit_e4m3(v0, ls[0], hw, lw, 0, sl2x2, negm);
+            emit_e4m3(v1, ls[1], hw, lw, 8, sl2x2, negm);
+            tc::tmem_st16(tS + 0, hw);
+            tc::tmem_st16(tS + 32, lw);
+            emit_e4m3(v2, ls[2], hw, lw, 0, sl2x2, negm);
+            emit_e4m3(v3, ls[3], hw, lw, 8, sl2x2, negm);
+            tc::tmem_st16(tS + 16, hw);
+            tc::tmem_st16(tS + 48, lw);
+          }
           auto emit = [&](uint32_t(&v)[32], int c) {
             uint32_t pk[16];
 #pragma unroll
@@ -954,13 +1038,27 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             }
             tc::tmem_st16(tS + 16 * c, pk);
           };
-          emit(v0, 0);
-          emit(v1, 1);
-          emit(v2, 2);
-          emit(v3, 3);
+          if constexpr (!F8S) {
+            emit(v0, 0);
+            emit(v1, 1);
+            emit(v2, 2);
+            emit(v3, 3);
+          }
           const float2 lsum = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
           l_run += lsum.x + lsum.y;
           tc::tmem_wait_st();
+        }
+        if (F8S && 2 * j + x == nT - 1 && x == zero_x) {
+          // E4M3: zero the raw V rows past the end of the split (stale or unloaded slots; a zero
+          // P against a NaN code would still poison the row) before its PV
+          const int g = G + nT - 1;
+          if (!warp_wait(bar(BAR_RAWV + rstg(g)), rphs(g))) { ok = false; break; }
+          if (kt0 + (nT - 1) * kCtxTileN + row >= kend) {
+            uint4* vrow = reinterpret_cast<uint4*>(base + L::kRawVOff + rstg(g) * L::kRawTile + row * 128);
+#pragma unroll
+            for (int kq = 0; kq < 8; ++kq) vrow[kq] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc::fence_proxy_async_smem();
         }
         if (!Q8 && 2 * j + x == nT - 1 && x == zero_x) {
           // zero V rows past the end of the sequence (stale or unloaded slots) before any PV (an
@@ -981,7 +1079,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(BAR_PFULL + x));
-        if constexpr (Q8) {  // the warpgroup's next tile, while its PV and the other tile's MMAs run
+        if constexpr (Q8 && !F8S) {  // the warpgroup's next tile, while its PV and the other tile's MMAs run
           if (j + 1 < nk && !convert_tile(gtile(j + 1), kend - (kt0 + (2 * j + 2 + x) * kCtxTileN))) { ok = false; break; }
         }
       }

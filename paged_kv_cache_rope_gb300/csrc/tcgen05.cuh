@@ -230,6 +230,22 @@ __device__ __forceinline__ void mma_bf16_ts_x8(uint32_t d_tmem, uint32_t a_tmem,
       "n"(4 * BSTEP), "n"(5 * BSTEP), "n"(6 * BSTEP), "n"(7 * BSTEP)
       : "memory");
 }
+// kind::f8f6f4: four K=32 steps of P(TMEM) x V with E4M3 A in TMEM (four codes per 32-bit
+// column, code k of a row in byte k % 4 of column k / 4) and E4M3 B from shared memory; A
+// advances 8 columns per step, B by `BSTEP` descriptor units.
+template <uint32_t BSTEP>
+__device__ __forceinline__ void mma_e4m3_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 b;\n .reg .b32 a;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n"
+      " add.u32 a, %1, 8;\n add.s64 b, %2, %5;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 16;\n add.s64 b, %2, %6;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a], b, %3, q;\n"
+      " add.u32 a, %1, 24;\n add.s64 b, %2, %7;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a], b, %3, q;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
                : "memory");
