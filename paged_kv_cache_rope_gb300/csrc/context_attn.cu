@@ -78,6 +78,7 @@ namespace {
 
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;  // generation kernel: the V copies (warp 8: item ring, Q and K)
 constexpr int kThreads = 12 * 32;  // three warpgroups: softmax A, softmax B, producer + MMA (+2 idle)
 // Registers: 168 per thread at launch (64512 per CTA).  The softmax warpgroups take 216 each and
 // the producer / MMA warpgroup keeps 64: 2 * 128 * 216 + 128 * 64 = 63488 <= 64512.
@@ -142,7 +143,7 @@ enum {
   BAR_QRAW = 45,   // the bf16 Q tile landed (warpgroup B rescales and re-encodes it)
   BAR_QFREE = 46,  // an item's last S MMA is done: its Q tile (and re-encoding) may be replaced
   BAR_ITEM = 47,   // +2: item ring entry written
-  BAR_ITEMFREE = 49,  // +2: item ring entry read by the MMA warp and the eight softmax warps
+  BAR_ITEMFREE = 49,  // +2: item ring entry read by the V producer, the MMA warp and the eight softmax warps
   BAR_IDONE = 51,  // an item is finished by the MMA warp (issued) and the eight softmax warps
   BAR_QSREAD = 52, // 8-bit pool: warpgroup A has read the item's Q row scales
   NUM_BARS = 53
@@ -214,7 +215,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     tc::mbar_init(bar(BAR_QFREE), 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(BAR_ITEM + s), 1);
-      tc::mbar_init(bar(BAR_ITEMFREE + s), 9);  // the MMA warp and the eight softmax warps
+      tc::mbar_init(bar(BAR_ITEMFREE + s), 10);  // the V producer, the MMA warp and the eight softmax warps
     }
     tc::mbar_init(bar(BAR_IDONE), 9);
     tc::mbar_init(bar(BAR_QSREAD), 4);
@@ -325,26 +326,35 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     // warp-uniform) and let one elected lane issue the TMA copies / MMAs: a warp that sits
     // diverged on one lane gets issue slots far less often next to a busy softmax warp on the
     // same sub-partition, and the tensor pipe then runs dry between MMA batches.
-    if (warp == kProducerWarp) {
-      // ======================= item queue + TMA producer =======================
+    if (warp == kProducerWarp || warp == kVProducerWarp) {
+      // ======================= item queue + TMA producers =======================
+      // Warp 8 publishes the items and copies Q and K, warp 10 (its own sub-partition) takes
+      // the items from the ring like a consumer and copies V: each tile's copies are issued by
+      // two warps that share their sub-partitions with busy softmax warps, instead of one.
+      const bool vwarp = warp == kVProducerWarp;
       int w = static_cast<int>(blockIdx.x);
-      int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items)
+      int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items; each warp its kind)
       int nq = 0;                      // Q tiles loaded
       const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: warpgroup A re-encodes Q first
       bool pok = true;
       for (int k = 0; pok; ++k) {
-        const int slot = k & 1;
-        if (k >= 2 && !warp_wait(bar(BAR_ITEMFREE + slot), ((k - 2) >> 1) & 1)) { pok = false; break; }
-        const bool more = w < n_items;
-        if (lane == 0) {
-          *(s_item + slot) = more ? w : -1;
-          tc::mbar_arrive(bar(BAR_ITEM + slot));
+        if (vwarp) {
+          if (!take_item(k, w)) { pok = false; break; }
+          if (w < 0) break;
+        } else {
+          const int slot = k & 1;
+          if (k >= 2 && !warp_wait(bar(BAR_ITEMFREE + slot), ((k - 2) >> 1) & 1)) { pok = false; break; }
+          const bool more = w < n_items;
+          if (lane == 0) {
+            *(s_item + slot) = more ? w : -1;
+            tc::mbar_arrive(bar(BAR_ITEM + slot));
+          }
+          __syncwarp();
+          if (!more) break;
         }
-        __syncwarp();
-        if (!more) break;
         const Item it = item_of(w);
         if (!it.ok) {
-          if (lane == 0) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
+          if (lane == 0 && !vwarp) flag_error(p.d_error, PKV_DEVERR_PLAN_MISMATCH);  // plan disagrees
         } else {
           const int nT = it.nkt0 + it.nkt1;
           const int32_t* tbl = p.tbl + static_cast<int64_t>(it.r) * p.max_blocks;
@@ -381,9 +391,9 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           // tile j of the item (table entries pg) into the next stage of the CTA's stream
           auto issue_tile = [&](int j, int pg) {
             if (warp_abort()) return false;
-            const int g = issued_k;  // == issued_v: the tile's place in the CTA's stream
+            const int g = vwarp ? issued_v : issued_k;  // the tile's place in the CTA's stream
             if (has_page(j) && (pg < 0 || pg >= p.NB)) {
-              flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
+              if (!vwarp) flag_error(p.d_error, PKV_DEVERR_BAD_PAGE);
               pg = -1;
             }
             const uint32_t bytes =
@@ -394,46 +404,52 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
               // (E4M3) or its codes are converted (INT8))
               const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
               const int rs = rstg(g), rph = rphs(g - R);
-              if (g >= R && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) return false;
-              if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWK + rs), bytes);
-              __syncwarp();
-              if (pg >= 0)
-                tc::tma_load_3d(base_s + L::kRawKOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + rs), 0, it.hk,
-                                (pg * 2 + 0) * p.B);
-              __syncwarp();
-              ++issued_k;
-              if (g >= R && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) return false;
-              if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWV + rs), bytes);
-              __syncwarp();
-              if (pg >= 0)
-                tc::tma_load_3d(base_s + L::kRawVOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + rs), 0, it.hk,
-                                (pg * 2 + 1) * p.B);
-              __syncwarp();
-              ++issued_v;
+              if (!vwarp) {
+                if (g >= R && !warp_wait(bar(BAR_RAWKEMPTY + rs), rph)) return false;
+                if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWK + rs), bytes);
+                __syncwarp();
+                if (pg >= 0)
+                  tc::tma_load_3d(base_s + L::kRawKOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWK + rs), 0, it.hk,
+                                  (pg * 2 + 0) * p.B);
+                __syncwarp();
+                ++issued_k;
+              } else {
+                if (g >= R && !warp_wait(bar(BAR_RAWVEMPTY + rs), rph)) return false;
+                if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_RAWV + rs), bytes);
+                __syncwarp();
+                if (pg >= 0)
+                  tc::tma_load_3d(base_s + L::kRawVOff + rs * L::kRawTile + roff, &kv_map, bar(BAR_RAWV + rs), 0, it.hk,
+                                  (pg * 2 + 1) * p.B);
+                __syncwarp();
+                ++issued_v;
+              }
               return true;
             }
             // one lane registers the tile's bytes, then every lane with a page issues its own
             // copies (no shuffles, no serial issue loop on one lane)
             const int st = stg(g);
             const uint32_t koff = static_cast<uint32_t>(lane * box_rows * 128);
-            if (g >= S && !warp_wait(bar(BAR_KEMPTY + st), phs(g - S))) return false;
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
-            __syncwarp();
-            if (pg >= 0)
-              for (int dh = 0; dh < D / 64; ++dh)
-                tc::tma_load_4d(sK(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_KFULL + st), 0, dh, it.hk,
-                                (pg * 2 + 0) * p.B);
-            __syncwarp();
-            ++issued_k;
-            if (g >= S && !warp_wait(bar(BAR_VEMPTY + st), phs(g - S))) return false;
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
-            __syncwarp();
-            if (pg >= 0)
-              for (int dh = 0; dh < D / 64; ++dh)
-                tc::tma_load_4d(sV(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_VFULL + st), 0, dh, it.hk,
-                                (pg * 2 + 1) * p.B);
-            __syncwarp();
-            ++issued_v;
+            if (!vwarp) {
+              if (g >= S && !warp_wait(bar(BAR_KEMPTY + st), phs(g - S))) return false;
+              if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_KFULL + st), bytes);
+              __syncwarp();
+              if (pg >= 0)
+                for (int dh = 0; dh < D / 64; ++dh)
+                  tc::tma_load_4d(sK(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_KFULL + st), 0, dh, it.hk,
+                                  (pg * 2 + 0) * p.B);
+              __syncwarp();
+              ++issued_k;
+            } else {
+              if (g >= S && !warp_wait(bar(BAR_VEMPTY + st), phs(g - S))) return false;
+              if (lane == 0) tc::mbar_arrive_expect_tx(bar(BAR_VFULL + st), bytes);
+              __syncwarp();
+              if (pg >= 0)
+                for (int dh = 0; dh < D / 64; ++dh)
+                  tc::tma_load_4d(sV(st) + dh * L::kHalf + koff, &kv_map, bar(BAR_VFULL + st), 0, dh, it.hk,
+                                  (pg * 2 + 1) * p.B);
+              __syncwarp();
+              ++issued_v;
+            }
             return true;
           };
           // the item's Q tile goes out as soon as the previous item's last S MMA is done, then its
@@ -447,11 +463,11 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 #else
           const int n_issue = nT;
 #endif
-          if (pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
+          if (!vwarp && pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
           if (!pok) break;
           // one Q tile (128 / g tokens x the group's g heads), shared by A and B; HALF: 64 rows,
           // rows 16k .. 16k+15 into tile rows 32k .. 32k+15 (a box of g heads x 16 / g tokens)
-          if (tc::elect_one()) {
+          if (!vwarp && tc::elect_one()) {
             if constexpr (HALF) {
               tc::mbar_arrive_expect_tx(bar(q_bar), 64 * D * 2);
               for (int kq = 0; kq < 4; ++kq)
@@ -465,14 +481,16 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             }
           }
           __syncwarp();
-          ++nq;
+          if (!vwarp) ++nq;
           for (int j = 0; pok && j < n_issue; ++j) pok = issue_tile(j, lookup(j));
         }
         if (!pok) break;
-        // claim the next item while this one's tiles are still being consumed
-        int nxt = 0;
-        if (lane == 0) nxt = atomicAdd(p.gen_cursor, 1) + static_cast<int>(gridDim.x);
-        w = __shfl_sync(0xffffffffu, nxt, 0);
+        if (!vwarp) {
+          // claim the next item while this one's tiles are still being consumed
+          int nxt = 0;
+          if (lane == 0) nxt = atomicAdd(p.gen_cursor, 1) + static_cast<int>(gridDim.x);
+          w = __shfl_sync(0xffffffffu, nxt, 0);
+        }
       }
       if (!pok && lane == 0) fail();
       __syncwarp();
