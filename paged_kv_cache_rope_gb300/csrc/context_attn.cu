@@ -788,7 +788,55 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           // Q row `row`: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
           // below f16's 65504), in place; the scores take 2^(e - 14) back
           ok = warp_wait(bar(BAR_QRAW), nq & 1);
-          if (ok) {
+          if constexpr (F8S && HALF) {
+            // 64 rows, two threads per row: thread kh splits head-dim half kh of row srow (both
+            // halves of every row are read before any code is written: the lo codes of half 0
+            // land where half 1's bf16 codes sat)
+            if (ok) {
+              const uint32_t rbase = static_cast<uint32_t>(L::kQOff + kh * L::kHalf + srow * 128);
+              uint4 qr[8];
+              float amax = 0.f;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                qr[c] = *reinterpret_cast<const uint4*>(base + rbase + ((c ^ (srow & 7)) << 4));
+                const uint32_t u[4] = {qr[c].x, qr[c].y, qr[c].z, qr[c].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
+              }
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));  // the row's other half
+              int ex = 0;
+              if (amax > 0.f) frexpf(amax, &ex);
+              const float up = ldexpf(1.f, 8 - ex);  // |q| * up in [128, 256), under 448
+              if (nq > 0 && !warp_wait(bar(BAR_QSREAD), (nq - 1) & 1)) { ok = false; break; }
+              __syncwarp();
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {  // code chunk jc = 4 kh + jj from bf16 chunks 2 jj, 2 jj + 1
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                  const uint4 w = qr[2 * jj + hc];
+                  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int k = 0; k < 4; k += 2) {
+                    uint32_t h0, l0, h1, l1;
+                    split_e4m3x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up, h0, l0);
+                    split_e4m3x2(__uint_as_float(u[k + 1] << 16) * up, __uint_as_float(u[k + 1] & 0xFFFF0000u) * up, h1,
+                                 l1);
+                    hw[2 * hc + (k >> 1)] = (h0 & 0xFFFFu) | (h1 << 16);
+                    lw[2 * hc + (k >> 1)] = (l0 & 0xFFFFu) | (l1 << 16);
+                  }
+                }
+                const uint32_t off = static_cast<uint32_t>(srow * 128 + (((4 * kh + jj) ^ (srow & 7)) << 4));
+                st_shared_v4(sQ + off, hw[0], hw[1], hw[2], hw[3]);
+                st_shared_v4(sQ + L::kHalf + off, lw[0], lw[1], lw[2], lw[3]);
+              }
+              if (kh == 0) qscale[srow] = 1.f / up;
+              tc::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
+            }
+          } else if (ok) {
             float amax = 0.f;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
