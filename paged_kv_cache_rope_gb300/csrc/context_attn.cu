@@ -45,10 +45,11 @@
 //
 // gen_attn_kernel: generation requests with more (token, query head) pairs than the mma.sync
 // decode kernel's columns, on the same tcgen05 pipeline; bf16 pools, or 8-bit pools at head_dim
-// 128 whose codes TMA lands raw: E4M3 scores run on kind::f8f6f4 from the raw K codes against Q
-// split into hi + lo E4M3 tiles, INT8 K is converted to f16 with Q made f16, and V is converted
-// to f16 for a kind::f16 PV -- each conversion by the softmax warpgroup that will read the tile;
-// Q takes a power-of-two scale per row that the scores give back.  Persistent like the context
+// 128 whose codes TMA lands raw: on E4M3 pools S and PV both run on kind::f8f6f4 straight from
+// the raw K and V codes, against Q and P split into hi + lo E4M3 codes (P in TMEM); on INT8
+// pools K and V are converted to f16 by the softmax warpgroup that will read the tile, Q is made
+// f16, and S and PV run on kind::f16.  Q takes a power-of-two scale per row that the scores give
+// back.  Persistent like the context
 // kernel: work item = (request, KV head, split, 128 rows), claimed longest first; a 128-row tile
 // is 128/g draft tokens x the g query heads of one KV head (the Q box spans g heads), so each
 // K / V tile serves the whole group; the two softmax warpgroups
@@ -156,8 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map,
                 const __grid_constant__ CUtensorMap kv_map) {
   using L = GenSmem<D, KV>;
-  // 8-bit pool: the producer lands raw codes and the softmax warpgroups
-  // convert what the MMAs cannot read as stored (Q, V, and INT8 K)
+  // 8-bit pool: the producer lands raw codes and the softmax warpgroups re-encode what the MMAs
+  // cannot read as stored (Q, and on INT8 pools K and V)
   constexpr bool Q8 = L::kQ8;
   // E4M3 pools: scores and PV on kind::f8f6f4 straight from the raw K and V codes, with Q and P
   // split into hi + lo E4M3 codes (7-8 significant bits together); nothing is converted
@@ -400,8 +401,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
                 static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, pg >= 0))) * box_rows * D * (Q8 ? 1 : 2);
             if constexpr (Q8) {
               // raw codes of page `lane` into the raw rings; K and V stages are freed separately
-              // (a raw V stage once its codes are converted, a raw K stage once its S is done
-              // (E4M3) or its codes are converted (INT8))
+              // (a raw K stage once its S is done (E4M3) or its codes are converted (INT8), a raw
+              // V stage once its PV is done (E4M3) or its codes are converted (INT8))
               const uint32_t roff = static_cast<uint32_t>(lane * box_rows * D);
               const int rs = rstg(g), rph = rphs(g - R);
               if (!vwarp) {
@@ -693,14 +694,13 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         lw[w0 + (e >> 2)] = __byte_perm(l01, l23, 0x5410);
       }
     };
-    // ---- 8-bit pool: this warpgroup turns the raw codes of its own tiles into f16 ----
-    // Thread `row` converts tile row `row`: 128 codes in the 128-byte swizzle TMA wrote (16-byte
-    // chunk j at j ^ (row % 8)) become 16 f16 chunks of the K-major 128-byte-swizzled layout the
-    // MMAs read, in 64-wide head-dim halves.  Both code kinds are exact in f16: E4M3 through the
-    // hardware conversion (measured 4% faster here than placing the bits with integer ops),
-    // INT8 as integers.  A warpgroup converts its next tile right after handing over its P,
-    // while its own PV and the other warpgroup's MMAs run.  A V row past the end of the sequence
-    // (stale or unloaded slot) is written as zeros instead.
+    // ---- INT8 pool: this warpgroup turns the raw codes of its own tiles into f16 ----
+    // (E4M3 pools read their codes as stored.)  Thread `row` converts tile row `row`: 128 codes
+    // in the 128-byte swizzle TMA wrote (16-byte chunk j at j ^ (row % 8)) become 16 f16 chunks of
+    // the K-major 128-byte-swizzled layout the MMAs read, in 64-wide head-dim halves; every int8
+    // is exact in f16.  A warpgroup converts its next tile right after handing over its P, while
+    // its own PV and the other warpgroup's MMAs run.  A V row past the end of the sequence (stale
+    // or unloaded slot) is written as zeros instead.
     auto cvt_row = [&](uint32_t raw_off, uint32_t dst_s, bool zero) {
 #pragma unroll
       for (int jc = 0; jc < 8; ++jc) {
@@ -724,10 +724,10 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     };
     // tile g of the stream (this warpgroup's), whose first vrows rows hold keys of the split: raw
     // stage g % R into f16 stage g % S -- K once the stage's previous S is done, then V once its
-    // previous PV is done; each step frees a raw stage
+    // previous PV is done; each step frees a raw stage (INT8 pools only)
     auto convert_tile = [&](int g, int vrows) {
       const int rs = rstg(g), rph = rphs(g), st = stg(g), ph_prev = phs(g - S);
-      if constexpr (!F8S) {  // E4M3 scores read the raw K codes themselves
+      if constexpr (!F8S) {
         if (!warp_wait(bar(BAR_RAWK + rs), rph) || (g >= S && !warp_wait(bar(BAR_KEMPTY + st), ph_prev))) return false;
         cvt_row(L::kRawKOff + rs * L::kRawTile, sK(st), false);
         tc::fence_proxy_async_smem();
@@ -778,7 +778,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
           }
         }
       }
-      // 8-bit pool: warpgroup B (whose epilogue is the short one) re-encodes the item's Q and
+      // 8-bit pool: warpgroup B (whose epilogue is the short one) re-encodes the item's Q and (INT8)
       // each warpgroup converts its first tile, before waiting for the previous item to end:
       // they touch shared memory only, and their barriers order them against its MMAs.
       float sl2 = p.scale_log2;
