@@ -147,7 +147,11 @@ enum {
   BAR_ITEMFREE = 49,  // +2: item ring entry read by the V producer, the MMA warp and the eight softmax warps
   BAR_IDONE = 51,  // an item is finished by the MMA warp (issued) and the eight softmax warps
   BAR_QSREAD = 52, // 8-bit pool: warpgroup A has read the item's Q row scales
-  NUM_BARS = 53
+  BAR_Q2 = 53,     // the same four for the second set of Q rows (two threads per row)
+  BAR_QRAW2 = 54,
+  BAR_QFREE2 = 55,
+  BAR_QSREAD2 = 56,
+  NUM_BARS = 57
 };
 constexpr int kMaxRawStages = 6;
 
@@ -166,6 +170,17 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
   constexpr int S = L::kStages > 0 ? L::kStages : 1;  // (E4M3: no f16 ring; one nominal stage)
   constexpr int R = L::kRawStages;
   static_assert(R <= kMaxRawStages, "raw ring barriers");
+  // Q row sets: with two threads per row (HALF) an item's 64 Q rows take 16 of the 32 lanes of
+  // each warp's quarter, so consecutive items alternate between lanes 0-15 and 16-31 and the
+  // next item's Q is copied (and, on E4M3 pools, split) while the current item still runs.
+  // (INT8 pools re-encode Q row by row over the whole tile: one set.)
+  constexpr int QS = (HALF && KV != PKV_INT8) ? 2 : 1;
+  // set s's barriers: Q landed / re-encoded (the MMAs may read it), raw bf16 landed (8-bit), the
+  // set's last S MMA done (it may be refilled), its row scales read by warpgroup A (8-bit)
+  auto b_qready = [](int s) { return s ? BAR_Q2 : BAR_Q; };
+  auto b_qraw = [](int s) { return s ? BAR_QRAW2 : BAR_QRAW; };
+  auto b_qfree = [](int s) { return s ? BAR_QFREE2 : BAR_QFREE; };
+  auto b_qsread = [](int s) { return s ? BAR_QSREAD2 : BAR_QSREAD; };
   // ring stage and phase of the g-th K / V tile of the stream (f16 / bf16 rings, raw rings)
   auto stg = [](int g) { return g % S; };
   auto phs = [](int g) { return (g / S) & 1; };
@@ -191,6 +206,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     // softmax warpgroup that converted them
     const uint32_t ready_count = Q8 ? 4 : 1;
     tc::mbar_init(bar(BAR_Q), ready_count);
+    tc::mbar_init(bar(BAR_Q2), ready_count);
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar(BAR_KFULL + s), ready_count);
       tc::mbar_init(bar(BAR_KEMPTY + s), 1);
@@ -205,6 +221,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         tc::mbar_init(bar(BAR_RAWVEMPTY + s), F8S ? 1 : 4);  // E4M3: its PV is done
       }
       tc::mbar_init(bar(BAR_QRAW), 1);
+      tc::mbar_init(bar(BAR_QRAW2), 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(BAR_SFULL + s), 1);
@@ -214,12 +231,14 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     tc::mbar_init(bar(BAR_MMADONE), 1);
     tc::mbar_init(bar(BAR_MERGE), 128);
     tc::mbar_init(bar(BAR_QFREE), 1);
+    tc::mbar_init(bar(BAR_QFREE2), 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(BAR_ITEM + s), 1);
       tc::mbar_init(bar(BAR_ITEMFREE + s), 10);  // the V producer, the MMA warp and the eight softmax warps
     }
     tc::mbar_init(bar(BAR_IDONE), 9);
     tc::mbar_init(bar(BAR_QSREAD), 4);
+    tc::mbar_init(bar(BAR_QSREAD2), 4);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -336,7 +355,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       int w = static_cast<int>(blockIdx.x);
       int issued_k = 0, issued_v = 0;  // K / V stream tiles issued (all items; each warp its kind)
       int nq = 0;                      // Q tiles loaded
-      const int q_bar = Q8 ? BAR_QRAW : BAR_Q;  // 8-bit: warpgroup A re-encodes Q first
+      auto q_bar = [&](int qs) { return Q8 ? b_qraw(qs) : b_qready(qs); };  // 8-bit: warpgroup B re-encodes Q first
       bool pok = true;
       for (int k = 0; pok; ++k) {
         if (vwarp) {
@@ -464,21 +483,22 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
 #else
           const int n_issue = nT;
 #endif
-          if (!vwarp && pok && nq > 0 && !warp_wait(bar(BAR_QFREE), (nq - 1) & 1)) pok = false;
+          const int qset = nq % QS;  // the item's Q rows, refilled once their previous item's last S is done
+          if (!vwarp && pok && nq >= QS && !warp_wait(bar(b_qfree(qset)), ((nq / QS) - 1) & 1)) pok = false;
           if (!pok) break;
           // one Q tile (128 / g tokens x the group's g heads), shared by A and B; HALF: 64 rows,
           // rows 16k .. 16k+15 into tile rows 32k .. 32k+15 (a box of g heads x 16 / g tokens)
           if (!vwarp && tc::elect_one()) {
             if constexpr (HALF) {
-              tc::mbar_arrive_expect_tx(bar(q_bar), 64 * D * 2);
+              tc::mbar_arrive_expect_tx(bar(q_bar(qset)), 64 * D * 2);
               for (int kq = 0; kq < 4; ++kq)
                 for (int dh = 0; dh < D / 64; ++dh)
-                  tc::tma_load_4d(sQ + dh * L::kHalf + kq * 32 * 128, &q_map, bar(q_bar), 0, dh, it.hk * p.group,
-                                  it.q_row + kq * 16 / p.group);
+                  tc::tma_load_4d(sQ + dh * L::kHalf + (kq * 32 + qset * 16) * 128, &q_map, bar(q_bar(qset)), 0, dh,
+                                  it.hk * p.group, it.q_row + kq * 16 / p.group);
             } else {
-              tc::mbar_arrive_expect_tx(bar(q_bar), 128 * D * 2);
+              tc::mbar_arrive_expect_tx(bar(q_bar(0)), 128 * D * 2);
               for (int dh = 0; dh < D / 64; ++dh)
-                tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar), 0, dh, it.hk * p.group, it.q_row);
+                tc::tma_load_4d(sQ + dh * L::kHalf, &q_map, bar(q_bar(0)), 0, dh, it.hk * p.group, it.q_row);
             }
           }
           __syncwarp();
@@ -508,7 +528,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         for (int j = (issued_v > S ? issued_v - S : 0); j < issued_v; ++j)
           tc::mbar_wait(bar(BAR_VFULL + stg(j)), phs(j), 200000000LL);
       }
-      if (nq > 0) tc::mbar_wait(bar(q_bar), (nq - 1) & 1, 200000000LL);
+      for (int i = (nq > QS ? nq - QS : 0); i < nq; ++i) tc::mbar_wait(bar(q_bar(i % QS)), (i / QS) & 1, 200000000LL);
     } else if (warp == kMmaWarp) {
       // ======================= MMA issuer =======================
       // tcgen05.commit tracks the MMAs of the thread that issues it: elect.sync on a converged
@@ -538,6 +558,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         if (!it.ok) continue;
         const int nkt0 = it.nkt0, nkt1 = it.nkt1;
         const bool hasB = it.nv1 > 0;
+        const int qset = nq % QS;  // the item's Q rows
         auto uses = [&](int j, int x) { return j < (x ? nkt1 : nkt0); };
         // tile j of half x: the (G + 2j + x)-th K / V tile of the CTA's stream
         auto gtile = [&](int j, int x) { return G + 2 * j + x; };
@@ -565,7 +586,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
               for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3_ss(tmem + 128 * x, aq + kLo + 2 * kk, bk + 2 * kk, idesc_s, 1u);
               tc::mma_commit(bar(BAR_SFULL + x));
               tc::mma_commit(bar(BAR_RAWKEMPTY + rstg(g)));  // the raw K stage may be refilled
-              if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(BAR_QFREE));  // the item's last S
+              if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(b_qfree(qset)));  // the item's last S
             }
             __syncwarp();
             return;
@@ -585,11 +606,11 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             tc::mma_commit(bar(BAR_SFULL + x));
             tc::mma_commit(bar(BAR_KEMPTY + st));  // each K / V tile has one user
             // the item's last S: the Q tile (and its re-encoding) may be replaced once it is done
-            if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(BAR_QFREE));
+            if (2 * j + x == nkt0 + nkt1 - 1) tc::mma_commit(bar(b_qfree(qset)));
           }
           __syncwarp();
         };
-        ok = warp_wait(bar(BAR_Q), nq & 1) && kfull(0, 0);
+        ok = warp_wait(bar(b_qready(qset)), (nq / QS) & 1) && kfull(0, 0);
         ++nq;
         if (ok) {
           tc::fence_after_sync();
@@ -669,11 +690,11 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
     // warp's quarter; threads t and t + 16 of a warp share it, each on one half (kh) of the keys
     // of a tile and of the output columns.  Otherwise a thread owns tile row `row` whole.
     const int qrow = HALF ? (warp & 3) * 16 + (lane & 15) : row;
-    const int srow = HALF ? (warp & 3) * 32 + (lane & 15) : row;
+    const int srow0 = HALF ? (warp & 3) * 32 + (lane & 15) : row;
     const int kh = HALF ? (lane >> 4) : 0;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + 128 * x + lane_off;
-    const uint32_t tO = tmem + 256 + 128 * x + lane_off;
+    const uint32_t tS0 = tmem + 128 * x + lane_off;
+    const uint32_t tO0 = tmem + 256 + 128 * x + lane_off;
     float* xch = reinterpret_cast<float*>(base + L::kXchOff);  // [2][128]: B's m, l per row
     // E4M3 P: 32 scores (v) -> P' = exp2(s * sl2 - m + kPOff), summed into ls, as 8 words of hi
     // codes and 8 of lo codes (four keys per word, key 4i + b in byte b) at hw / lw[w0 ..]
@@ -756,6 +777,11 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       if (w < 0) break;
       const Item it = item_of(w);
       if (!it.ok) continue;
+      // the item's Q rows: lanes 16 qset .. 16 qset + 15 of each quarter (HALF), else all
+      const int qset = nq % QS;
+      const int srow = srow0 + 16 * qset;
+      const uint32_t tS = tS0 + (static_cast<uint32_t>(16 * qset) << 16);
+      const uint32_t tO = tO0 + (static_cast<uint32_t>(16 * qset) << 16);
       const int nvx = x ? it.nv1 : it.nv0, nk = x ? it.nkt1 : it.nkt0;
       const int nT = it.nkt0 + it.nkt1;  // KV tiles of the item (A the even ones, B the odd ones)
       const int zero_x = (nT - 1) & 1;   // the user of the last V tile zeroes its tail
@@ -787,7 +813,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
         if (x == 1) {
           // Q row `row`: bf16 -> f16 times 2^(14 - e), e the exponent of the row's largest |q| (far
           // below f16's 65504), in place; the scores take 2^(e - 14) back
-          ok = warp_wait(bar(BAR_QRAW), nq & 1);
+          ok = warp_wait(bar(b_qraw(qset)), (nq / QS) & 1);
           if constexpr (F8S && HALF) {
             // 64 rows, two threads per row: thread kh splits head-dim half kh of row srow (both
             // halves of every row are read before any code is written: the lo codes of half 0
@@ -808,7 +834,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
               int ex = 0;
               if (amax > 0.f) frexpf(amax, &ex);
               const float up = ldexpf(1.f, 8 - ex);  // |q| * up in [128, 256), under 448
-              if (nq > 0 && !warp_wait(bar(BAR_QSREAD), (nq - 1) & 1)) { ok = false; break; }
+              if (nq >= QS && !warp_wait(bar(b_qsread(qset)), ((nq / QS) - 1) & 1)) { ok = false; break; }
               __syncwarp();
 #pragma unroll
               for (int jj = 0; jj < 4; ++jj) {  // code chunk jc = 4 kh + jj from bf16 chunks 2 jj, 2 jj + 1
@@ -834,7 +860,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
               if (kh == 0) qscale[srow] = 1.f / up;
               tc::fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
+              if (lane == 0) tc::mbar_arrive(bar(b_qready(qset)));
             }
           } else if (ok) {
             float amax = 0.f;
@@ -852,7 +878,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             // f16: |q| * up in [2^13, 2^14); E4M3 hi + lo: |q| * up in [128, 256), under 448
             const float up = ldexpf(1.f, (F8S ? 8 : 14) - ex);
             // the previous item's scales are read by both warpgroups before they are replaced
-            if (nq > 0 && !warp_wait(bar(BAR_QSREAD), (nq - 1) & 1)) { ok = false; break; }
+            if (nq >= QS && !warp_wait(bar(b_qsread(qset)), ((nq / QS) - 1) & 1)) { ok = false; break; }
             if constexpr (F8S) {
               // code chunk jc (16 codes = q elements 16 jc ..) from bf16 chunks 2 (jc % 4) and
               // 2 (jc % 4) + 1 of head-dim half jc / 4; the hi tile replaces the row's first half
@@ -899,7 +925,7 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
             qscale[row] = 1.f / up;
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(BAR_Q));
+            if (lane == 0) tc::mbar_arrive(bar(b_qready(qset)));
           }
         }
         if constexpr (!F8S) {
@@ -909,13 +935,13 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
       }
       if (!wait_prev(ndone)) { ok = false; break; }
       if constexpr (Q8) {
-        ok = warp_wait(bar(BAR_Q), nq & 1);
+        ok = warp_wait(bar(b_qready(qset)), (nq / QS) & 1);
         if (ok) sl2 *= qscale[srow];
-        ++nq;
         if (!ok) break;
         __syncwarp();
-        if (x == 0 && lane == 0) tc::mbar_arrive(bar(BAR_QSREAD));
+        if (x == 0 && lane == 0) tc::mbar_arrive(bar(b_qsread(qset)));
       }
+      ++nq;  // every pool: the next item's Q rows are the other set
       const int kt0 = it.kt0, kend = it.kend, past = it.past;
       constexpr float kThr = F8S ? kRescaleThresholdE4M3 : kRescaleThreshold;
       constexpr float kPOff = F8S ? kPScaleLog2E4M3 : 0.f;  // P is emitted as 2^kPOff * exp2(s - m)
