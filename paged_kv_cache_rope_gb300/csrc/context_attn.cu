@@ -172,9 +172,8 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
   static_assert(R <= kMaxRawStages, "raw ring barriers");
   // Q row sets: with two threads per row (HALF) an item's 64 Q rows take 16 of the 32 lanes of
   // each warp's quarter, so consecutive items alternate between lanes 0-15 and 16-31 and the
-  // next item's Q is copied (and, on E4M3 pools, split) while the current item still runs.
-  // (INT8 pools re-encode Q row by row over the whole tile: one set.)
-  constexpr int QS = (HALF && KV != PKV_INT8) ? 2 : 1;
+  // next item's Q is copied (and, on 8-bit pools, re-encoded) while the current item still runs.
+  constexpr int QS = HALF ? 2 : 1;
   // set s's barriers: Q landed / re-encoded (the MMAs may read it), raw bf16 landed (8-bit), the
   // set's last S MMA done (it may be refilled), its row scales read by warpgroup A (8-bit)
   auto b_qready = [](int s) { return s ? BAR_Q2 : BAR_Q; };
@@ -856,6 +855,40 @@ gen_attn_kernel(const ContextParams p, const __grid_constant__ CUtensorMap q_map
                 const uint32_t off = static_cast<uint32_t>(srow * 128 + (((4 * kh + jj) ^ (srow & 7)) << 4));
                 st_shared_v4(sQ + off, hw[0], hw[1], hw[2], hw[3]);
                 st_shared_v4(sQ + L::kHalf + off, lw[0], lw[1], lw[2], lw[3]);
+              }
+              if (kh == 0) qscale[srow] = 1.f / up;
+              tc::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(bar(b_qready(qset)));
+            }
+          } else if constexpr (HALF) {
+            // INT8 pool, 64 rows, two threads per row: thread kh makes head-dim half kh of row
+            // srow f16 in place (the row's scale from both halves)
+            if (ok) {
+              const uint32_t rbase = static_cast<uint32_t>(L::kQOff + kh * L::kHalf + srow * 128);
+              uint4 qr[8];
+              float amax = 0.f;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                qr[c] = *reinterpret_cast<const uint4*>(base + rbase + ((c ^ (srow & 7)) << 4));
+                const uint32_t u[4] = {qr[c].x, qr[c].y, qr[c].z, qr[c].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  amax = max3f(amax, fabsf(__uint_as_float(u[k] << 16)), fabsf(__uint_as_float(u[k] & 0xFFFF0000u)));
+              }
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+              int ex = 0;
+              if (amax > 0.f) frexpf(amax, &ex);
+              const float up = ldexpf(1.f, 14 - ex);  // |q| * up in [2^13, 2^14)
+              if (nq >= QS && !warp_wait(bar(b_qsread(qset)), ((nq / QS) - 1) & 1)) { ok = false; break; }
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t u[4] = {qr[c].x, qr[c].y, qr[c].z, qr[c].w};
+                uint32_t hh[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  hh[k] = pack_f16x2(__uint_as_float(u[k] << 16) * up, __uint_as_float(u[k] & 0xFFFF0000u) * up);
+                st_shared_v4(base_s + rbase + ((c ^ (srow & 7)) << 4), hh[0], hh[1], hh[2], hh[3]);
               }
               if (kh == 0) qscale[srow] = 1.f / up;
               tc::fence_proxy_async_smem();
